@@ -1,0 +1,140 @@
+"""CPU oracle for dense GEMM -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library
+(``dense_gemm_transformer_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``oracle_gemm.c`` (plain C, fp64, a triple loop with k
+ascending); this module only marshals numpy arrays into it.  It computes the
+textbook matmul of "bare-metal-bard", first paragraph (the one-thread-per-output
+kernel), with BLAS scaling:
+
+    Cref = alpha * op(A) @ op(B) + beta * Cin,   D = |op(A)| @ |op(B)|
+
+with the operands first reduced to the mode's precision (FP32: unchanged,
+TF32: reduced to 10 mantissa bits, BF16: bfloat16 inputs widened exactly).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+MODES = {"fp32": 0, "tf32": 1, "bf16": 2}
+TF32_RULES = {"truncate": 0, "nearest_away": 1}
+# The reading taken for how the tensor cores treat raw fp32 operands in
+# kind::tf32: the 13 low mantissa bits are dropped.  A GPU test checks this
+# reading against the hardware on a one-column probe.
+DEFAULT_TF32_RULE = "truncate"
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle_gemm.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP, no fast-math, no FMA contraction)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        i64, p, d = ctypes.c_int64, ctypes.c_void_p, ctypes.c_double
+        lib.oracle_gemm.restype = ctypes.c_int
+        lib.oracle_gemm.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    i64, i64, i64, d, p, i64, p, i64, d, p, i64,
+                                    i64, i64, p, p, i64]
+        lib.oracle_tf32_array.restype = None
+        lib.oracle_tf32_array.argtypes = [ctypes.c_int, p, p, i64]
+        lib.oracle_bf16_array.restype = None
+        lib.oracle_bf16_array.argtypes = [p, p, i64]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def _operand(x, mode):
+    want = np.uint16 if mode == "bf16" else np.float32
+    x = np.asarray(x)
+    if x.dtype != want:
+        raise TypeError(f"mode {mode} takes {want.__name__} operands, got {x.dtype}")
+    if x.ndim != 2:
+        raise ValueError("operands must be 2-D")
+    if x.size == 0:
+        return np.ascontiguousarray(x)
+    if x.strides[1] != x.itemsize:
+        raise ValueError("operands need unit stride in the last dimension")
+    return x
+
+
+def gemm(mode, A, B, *, transA=False, transB=False, alpha=1.0, beta=0.0, C=None,
+         rows=None, tf32_rule=DEFAULT_TF32_RULE):
+    """Return (Cref, D) as float64 arrays of shape (rows, N).
+
+    A, B: 2-D numpy arrays, float32 for fp32/tf32, uint16 bfloat16 bit patterns
+    for bf16, stored as described for gemm_run (row-major, op() by trans flag).
+    C: float32 M x N input, read only when beta != 0.
+    rows: (row0, row1) to compute only part of the output.
+    """
+    lib = _load()
+    A = _operand(A, mode)
+    B = _operand(B, mode)
+    M, K = (A.shape[1], A.shape[0]) if transA else A.shape
+    Kb, N = (B.shape[1], B.shape[0]) if transB else B.shape
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    row0, row1 = rows if rows is not None else (0, M)
+    if beta != 0.0:
+        if C is None:
+            raise ValueError("beta != 0 needs C")
+        C = np.asarray(C)
+        if C.dtype != np.float32 or C.shape != (M, N) or C.strides[1] != 4:
+            raise ValueError("C must be float32 M x N with unit column stride")
+        ldc = C.strides[0] // 4
+    else:
+        C, ldc = None, max(N, 1)
+    out = np.zeros((row1 - row0, N), dtype=np.float64)
+    D = np.zeros((row1 - row0, N), dtype=np.float64)
+    rc = lib.oracle_gemm(MODES[mode], TF32_RULES[tf32_rule], int(bool(transA)), int(bool(transB)),
+                         M, N, K, float(alpha), _ptr(A), A.strides[0] // A.itemsize,
+                         _ptr(B), B.strides[0] // B.itemsize, float(beta), _ptr(C), ldc,
+                         row0, row1, _ptr(out), _ptr(D), max(N, 1))
+    if rc != 0:
+        raise ValueError(f"oracle_gemm rejected its arguments ({rc})")
+    return out, D
+
+
+def tf32(x, rule=DEFAULT_TF32_RULE):
+    """Reduce float32 values to TF32 by the given rule (elementwise)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    lib.oracle_tf32_array(TF32_RULES[rule], _ptr(x), _ptr(out), x.size)
+    return out
+
+
+def bf16_to_f64(bits):
+    """Widen bfloat16 bit patterns (uint16) to float64 exactly."""
+    lib = _load()
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    lib.oracle_bf16_array(_ptr(bits), _ptr(out), bits.size)
+    return out

@@ -1,0 +1,142 @@
+/*
+ * oracle_gemm.c -- the CPU oracle for dense GEMM.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg use this
+ * file.  The library never links, loads or calls it, and it shares no code,
+ * header or constant with the library.
+ *
+ * What it computes is the plain definition of the operation described on
+ * "bare-metal-bard" (ethanyanxu.com), first paragraph: the textbook matmul in
+ * which one thread computes one output element, extended by the usual BLAS
+ * scaling C = alpha * op(A) * op(B) + beta * C.  For every output element the
+ * oracle walks k = 0 .. K-1 in ascending order and accumulates in IEEE double:
+ *
+ *     Cref[i][j] = alpha * sum_k r(opA[i][k]) * r(opB[k][j]) + beta * Cin[i][j]
+ *     D[i][j]    =         sum_k |r(opA[i][k])| * |r(opB[k][j])|
+ *
+ * D is the scale used by the error metric err = |C - Cref| / D.
+ *
+ * r() is the precision of the mode's operands:
+ *   FP32 : the fp32 value itself.
+ *   TF32 : the fp32 value reduced to TF32 (sign, 8-bit exponent, 10 explicit
+ *          mantissa bits).  The first paragraph of "bare-metal-bard" says TF32
+ *          trades accuracy for speed but not how fp32 inputs are reduced; two
+ *          readings are offered: dropping the 13 low mantissa bits
+ *          (truncation toward zero) or rounding to nearest with ties away from
+ *          zero.  The caller chooses.
+ *   BF16 : the inputs arrive as bfloat16 bit patterns and are widened exactly.
+ *
+ * Conventions the pages leave open (BLAS readings): when K == 0 or alpha == 0
+ * A and B are not read; when beta == 0 Cin is not read, so a NaN there does
+ * not reach the result.
+ *
+ * Matrices are row-major.  op(A) is M x K: stored M x K (lda >= K) when
+ * transA == 0, or K x M (lda >= M) when transA == 1.  op(B) is K x N: stored
+ * K x N (ldb >= N) when transB == 0, or N x K (ldb >= K) when transB == 1.
+ *
+ * Rows row0 .. row1-1 of the result are produced (a sample of rows for large
+ * shapes); output row i is stored at Cref[(i - row0) * ldr + j].  Rows are
+ * spread over OpenMP threads; each element is still a plain ascending-k loop.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_MODE_FP32 0
+#define ORACLE_MODE_TF32 1
+#define ORACLE_MODE_BF16 2
+
+#define ORACLE_TF32_TRUNCATE 0
+#define ORACLE_TF32_NEAREST_AWAY 1
+
+static uint32_t float_bits(float x) {
+  uint32_t u;
+  memcpy(&u, &x, sizeof u);
+  return u;
+}
+
+static float bits_float(uint32_t u) {
+  float x;
+  memcpy(&x, &u, sizeof x);
+  return x;
+}
+
+/* TF32 keeps the top 19 bits of an fp32 pattern (1 sign, 8 exponent, 10
+ * mantissa).  NaN and Inf pass through unchanged (a NaN keeps its payload so
+ * that it stays a NaN). */
+float oracle_tf32_truncate(float x) {
+  uint32_t u = float_bits(x);
+  if ((u & 0x7f800000u) == 0x7f800000u) return x;
+  return bits_float(u & 0xffffe000u);
+}
+
+/* Round to the nearest TF32 value, ties away from zero: add half of the
+ * dropped range (bit 12) to the magnitude, then drop the 13 low bits.  A carry
+ * out of the mantissa steps the exponent, which is the correct rounding; a
+ * carry into the all-ones exponent gives Inf, which is the correct overflow. */
+float oracle_tf32_nearest_away(float x) {
+  uint32_t u = float_bits(x);
+  if ((u & 0x7f800000u) == 0x7f800000u) return x;
+  uint32_t sign = u & 0x80000000u;
+  uint32_t mag = (u & 0x7fffffffu) + 0x00001000u;
+  return bits_float(sign | (mag & 0x7fffe000u));
+}
+
+/* A bfloat16 value is the upper half of an fp32 pattern; widening is exact. */
+double oracle_bf16_to_double(uint16_t b) {
+  return (double)bits_float((uint32_t)b << 16);
+}
+
+static double operand(int mode, int tf32_rule, const void* base, int64_t idx) {
+  if (mode == ORACLE_MODE_BF16) return oracle_bf16_to_double(((const uint16_t*)base)[idx]);
+  float v = ((const float*)base)[idx];
+  if (mode == ORACLE_MODE_TF32)
+    v = (tf32_rule == ORACLE_TF32_NEAREST_AWAY) ? oracle_tf32_nearest_away(v) : oracle_tf32_truncate(v);
+  return (double)v;
+}
+
+/* Elementwise TF32 reduction of an array (used by the tests to pin r()). */
+void oracle_tf32_array(int tf32_rule, const float* in, float* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i)
+    out[i] = (tf32_rule == ORACLE_TF32_NEAREST_AWAY) ? oracle_tf32_nearest_away(in[i]) : oracle_tf32_truncate(in[i]);
+}
+
+/* Elementwise exact widening of bfloat16 bit patterns (used by the tests). */
+void oracle_bf16_array(const uint16_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_double(in[i]);
+}
+
+/* Returns 0 on success, a negative number for an argument it cannot take. */
+int oracle_gemm(int mode, int tf32_rule, int transA, int transB,
+                int64_t M, int64_t N, int64_t K, double alpha,
+                const void* A, int64_t lda, const void* B, int64_t ldb,
+                double beta, const float* Cin, int64_t ldc,
+                int64_t row0, int64_t row1, double* Cref, double* D, int64_t ldr) {
+  if (mode < ORACLE_MODE_FP32 || mode > ORACLE_MODE_BF16) return -1;
+  if (M < 0 || N < 0 || K < 0) return -2;
+  if (row0 < 0 || row1 < row0 || row1 > M) return -3;
+  if (ldr < N) return -4;
+  const int read_ab = (K > 0 && alpha != 0.0);
+  const int read_c = (beta != 0.0);
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = row0; i < row1; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      double acc = 0.0, mag = 0.0;
+      if (read_ab) {
+        for (int64_t k = 0; k < K; ++k) {
+          int64_t ia = transA ? k * lda + i : i * lda + k;
+          int64_t ib = transB ? j * ldb + k : k * ldb + j;
+          double p = operand(mode, tf32_rule, A, ia) * operand(mode, tf32_rule, B, ib);
+          acc += p;
+          mag += fabs(p);
+        }
+      }
+      double c = alpha * acc;
+      if (read_c) c += beta * (double)Cin[i * ldc + j];
+      Cref[(i - row0) * ldr + j] = c;
+      if (D) D[(i - row0) * ldr + j] = mag;
+    }
+  }
+  return 0;
+}

@@ -1,0 +1,139 @@
+"""Seeded synthetic inputs and the workload shapes, shared by both sides.
+
+This module only draws random numbers and names shapes.  It holds none of the
+GEMM arithmetic: the library (``dense_gemm_transformer_gb300``) and the oracle
+(``oracle``) both take their inputs from here and share nothing else.
+
+Inputs are drawn on the CPU with ``torch.Generator`` so that every machine
+produces the same tensors for the same seed.  The seed scheme is
+``1234 + 1000 * config + 10 * shape + tensor_id`` (seed 1234 is the one the
+"gpu kernels" write-up on devpost uses for its synthetic tensors, section
+"Tools").
+
+Workloads (every one stands in for data that is not available here):
+
+* ``square256``: C = A B with M = N = K = 256, A and B uniform on [-1, 1];
+  the same shape with integers in [-4, 4] for the exact check.
+* GPT projections: the matmuls of a 6-layer, d_model = 384, 6-head character
+  GPT at batch 64 x context 256 (16384 token rows), which "bare-metal-bard"
+  (second paragraph) trains with its own kernels.  Weights W are stored
+  K_in x N_out (so forward is NN, dX = dY W^T is NT and dW = X^T dY is TN),
+  activations X and upstream gradients dY are N(0, 1), weights N(0, 0.02^2).
+* the square sweep 1024 / 2048 / 4096, the large bf16 shapes, and the skinny
+  decode shapes (1, 4 or 16 token rows against 1536 x 8960, 8960 x 1536 and
+  1536 x 151936 weights: the hidden, MLP and vocabulary widths of the decode
+  step on vidyal.ai's "One Token, Kernel by Kernel").
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+BASE_SEED = 1234
+GPT_TOKENS = 64 * 256
+# (name, K_in, N_out) of each projection of the d_model = 384 GPT; the
+# vocabulary of the character model has 65 symbols.
+GPT_PROJECTIONS = (
+    ("qkv", 384, 1152),
+    ("attn_out", 384, 384),
+    ("mlp_up", 384, 1536),
+    ("mlp_down", 1536, 384),
+    ("lm_head", 384, 65),
+)
+SQUARE_SWEEP = (1024, 2048, 4096)
+LARGE_BF16 = ((8192, 8192, 8192), (8192, 28672, 8192))
+SKINNY_M = (1, 4, 16)
+SKINNY_WEIGHTS = ((1536, 8960), (8960, 1536), (1536, 151936))  # K x N
+
+
+def seed_for(config: int, shape: int, tensor_id: int) -> int:
+    return BASE_SEED + 1000 * config + 10 * shape + tensor_id
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def uniform(shape, seed, lo=-1.0, hi=1.0) -> torch.Tensor:
+    """fp32 i.i.d. uniform on [lo, hi)."""
+    u = torch.rand(tuple(shape), generator=_gen(seed), dtype=torch.float32)
+    return u * (hi - lo) + lo
+
+
+def normal(shape, seed, std=1.0) -> torch.Tensor:
+    """fp32 i.i.d. N(0, std^2)."""
+    return torch.randn(tuple(shape), generator=_gen(seed), dtype=torch.float32) * std
+
+
+def integers(shape, seed, lo=-4, hi=4) -> torch.Tensor:
+    """fp32 holding i.i.d. integers drawn uniformly from [lo, hi]."""
+    return torch.randint(lo, hi + 1, tuple(shape), generator=_gen(seed)).to(torch.float32)
+
+
+def to_bf16(t: torch.Tensor) -> torch.Tensor:
+    """Round fp32 to bfloat16 (torch's round-to-nearest-even) on the CPU."""
+    return t.to(torch.bfloat16)
+
+
+def bf16_bits(t: torch.Tensor):
+    """The uint16 bit patterns of a bfloat16 tensor, as a numpy array."""
+    assert t.dtype == torch.bfloat16
+    return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+@dataclass(frozen=True)
+class GemmCase:
+    """One GEMM of a workload: C (M x N) = alpha op(A) op(B) + beta C."""
+    name: str
+    transA: bool
+    transB: bool
+    M: int
+    N: int
+    K: int
+
+    @property
+    def a_shape(self):
+        return (self.K, self.M) if self.transA else (self.M, self.K)
+
+    @property
+    def b_shape(self):
+        return (self.N, self.K) if self.transB else (self.K, self.N)
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+def gpt_cases():
+    """The 15 GEMMs of one GPT training step's projections (forward, dX, dW)."""
+    out = []
+    T = GPT_TOKENS
+    for name, kin, nout in GPT_PROJECTIONS:
+        out.append(GemmCase(f"{name}.fwd", False, False, T, nout, kin))   # Y  = X W
+        out.append(GemmCase(f"{name}.dX", False, True, T, kin, nout))     # dX = dY W^T
+        out.append(GemmCase(f"{name}.dW", True, False, kin, nout, T))     # dW = X^T dY
+    return out
+
+
+def gpt_tensors(shape_index: int, kin: int, nout: int, config: int = 1):
+    """X (T x K_in), W (K_in x N_out), dY (T x N_out) for one projection."""
+    T = GPT_TOKENS
+    X = normal((T, kin), seed_for(config, shape_index, 0))
+    W = normal((kin, nout), seed_for(config, shape_index, 1), std=0.02)
+    dY = normal((T, nout), seed_for(config, shape_index, 2))
+    return X, W, dY
+
+
+def square_case(n: int) -> GemmCase:
+    return GemmCase(f"square{n}", False, False, n, n, n)
+
+
+def skinny_cases():
+    out = []
+    for m in SKINNY_M:
+        for k, n in SKINNY_WEIGHTS:
+            out.append(GemmCase(f"skinny_m{m}_{k}x{n}", False, False, m, n, k))
+    return out

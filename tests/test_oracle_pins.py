@@ -1,0 +1,299 @@
+"""Pins of the CPU oracle to things other than itself (no GPU needed).
+
+Each test ties the oracle to a fact fixed by mathematics or by an independent
+routine: exact rational arithmetic on tiny shapes, identity and permutation
+matrices, integer products, a rank-one closed form, torch's float64 matmul,
+the TF32 and bfloat16 formats from their definitions, and a hand-computed
+example.  A wrong sign, a dropped term, a transposed operand or a missing
+rounding step in the oracle fails at least one of them.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from tests import _gate
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+TRANS = [(False, False), (False, True), (True, False), (True, True)]
+
+
+# ---------------------------------------------------------------- formats
+def _tf32_by_definition(x: float, rule: str) -> float:
+    """TF32 from its definition: fp32's exponent range, 10 fraction bits.
+
+    The spacing of TF32 values near |x| is 2^(e - 10) with e the binade of |x|
+    (never below fp32's smallest normal binade, -126).  Truncation keeps the
+    multiple of the spacing below |x|; nearest-away rounds half up in magnitude.
+    """
+    if x == 0.0 or math.isinf(x) or math.isnan(x):
+        return x
+    f = Fraction(x)
+    mag = abs(f)
+    e = max(math.frexp(x)[1] - 1, -126)
+    q = Fraction(2) ** (e - 10)
+    if rule == "truncate":
+        n = mag // q
+    else:
+        n = (mag / q + Fraction(1, 2)).__floor__()
+    r = n * q
+    if r >= Fraction(2) ** 128:
+        return math.copysign(math.inf, x)
+    return math.copysign(float(r), x)
+
+
+def _special_patterns():
+    pats = [0x00000000, 0x80000000, 0x00000001, 0x00001000, 0x00001fff, 0x00002000,
+            0x007fffff, 0x00800000, 0x3f800000, 0x3f801000, 0x3f802000, 0x3f803000,
+            0x3f800fff, 0x3f801001, 0xbf801000, 0xbf803000, 0x7f7fffff, 0x7f7ff000,
+            0x7f7fefff, 0xff7fffff, 0x3fffffff, 0x3ffff000, 0x4b7ff000]
+    return np.array(pats, dtype=np.uint32)
+
+
+@pytest.mark.parametrize("rule", ["truncate", "nearest_away"])
+def test_tf32_reduction_matches_definition(rule):
+    rng = np.random.default_rng(7)
+    pats = rng.integers(0, 2**32, size=4000, dtype=np.uint64).astype(np.uint32)
+    pats = np.concatenate([pats, _special_patterns()])
+    x = pats.view(np.float32)
+    x = x[np.isfinite(x)]
+    got = oracle.tf32(x, rule)
+    for xi, gi in zip(x.tolist(), got.tolist()):
+        want = _tf32_by_definition(xi, rule)
+        assert (gi == want and math.copysign(1, gi) == math.copysign(1, want)), (rule, xi, gi, want)
+
+
+def test_tf32_passes_inf_and_nan():
+    x = np.array([np.inf, -np.inf, np.nan], dtype=np.float32)
+    for rule in ("truncate", "nearest_away"):
+        got = oracle.tf32(x, rule)
+        assert got[0] == np.inf and got[1] == -np.inf and np.isnan(got[2])
+
+
+def test_tf32_rules_differ_only_at_half_spacing():
+    # 1 + 2^-11 is exactly half a TF32 spacing above 1: truncation keeps 1,
+    # nearest-away goes up to 1 + 2^-10.
+    x = np.array([1 + 2.0 ** -11, 1 + 2.0 ** -11 - 2.0 ** -23], dtype=np.float32)
+    assert oracle.tf32(x, "truncate").tolist() == [1.0, 1.0]
+    assert oracle.tf32(x, "nearest_away").tolist() == [1 + 2.0 ** -10, 1.0]
+
+
+def test_bf16_widening_exhaustive():
+    bits = np.arange(65536, dtype=np.uint16)
+    got = oracle.bf16_to_f64(bits)
+    want = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+# ---------------------------------------------------------------- helpers
+def _operands(mode, a, b):
+    """numpy operands for the oracle plus their exact values as Fractions."""
+    if mode == "bf16":
+        ab, bb = si.to_bf16(torch.from_numpy(a)), si.to_bf16(torch.from_numpy(b))
+        qa, qb = ab.to(torch.float64).numpy(), bb.to(torch.float64).numpy()
+        return si.bf16_bits(ab), si.bf16_bits(bb), qa, qb
+    if mode == "tf32":
+        qa = np.vectorize(lambda v: _tf32_by_definition(float(v), oracle.DEFAULT_TF32_RULE))(a)
+        qb = np.vectorize(lambda v: _tf32_by_definition(float(v), oracle.DEFAULT_TF32_RULE))(b)
+        return a, b, qa, qb
+    return a, b, a.astype(np.float64), b.astype(np.float64)
+
+
+def _op(x, t):
+    return x.T if t else x
+
+
+# ---------------------------------------------------------------- brute force
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+@pytest.mark.parametrize("tA,tB", TRANS)
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (0.5, 1.0), (-2.0, 0.25)])
+def test_bruteforce_exact_rational(mode, tA, tB, alpha, beta):
+    rng = np.random.default_rng(hash((mode, tA, tB, alpha)) % 2**32)
+    M, N, K = 5, 6, 7
+    a = rng.uniform(-1, 1, size=(K, M) if tA else (M, K)).astype(np.float32)
+    b = rng.uniform(-1, 1, size=(N, K) if tB else (K, N)).astype(np.float32)
+    c = rng.standard_normal((M, N)).astype(np.float32)
+    A, B, qa, qb = _operands(mode, a, b)
+    got, D = oracle.gemm(mode, A, B, transA=tA, transB=tB, alpha=alpha, beta=beta, C=c)
+    oa, ob = _op(qa, tA), _op(qb, tB)
+    for i in range(M):
+        for j in range(N):
+            s = sum(Fraction(float(oa[i, k])) * Fraction(float(ob[k, j])) for k in range(K))
+            d = sum(abs(Fraction(float(oa[i, k])) * Fraction(float(ob[k, j]))) for k in range(K))
+            exact = Fraction(alpha) * s + Fraction(beta) * Fraction(float(c[i, j]))
+            bound = 2 * (K + 2) * 2.0 ** -53 * (abs(alpha) * float(d) + abs(beta * float(c[i, j])))
+            assert abs(Fraction(float(got[i, j])) - exact) <= Fraction(bound), (i, j)
+            assert abs(Fraction(float(D[i, j])) - d) <= Fraction(2 * K * 2.0 ** -53 * float(d))
+
+
+def test_golden_hand_computed_example():
+    """A 2x3 by 3x2 product written out by hand (tests/golden)."""
+    path = os.path.join(GOLDEN, "hand_2x3x2.txt")
+    blocks = {}
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, vals = line.split(":", 1)
+            blocks[key.strip()] = [float(v) for v in vals.split()]
+    A = np.array(blocks["A"], dtype=np.float32).reshape(2, 3)
+    B = np.array(blocks["B"], dtype=np.float32).reshape(3, 2)
+    C = np.array(blocks["C"], dtype=np.float32).reshape(2, 2)
+    alpha, beta = blocks["alpha"][0], blocks["beta"][0]
+    want = np.array(blocks["expected"]).reshape(2, 2)
+    for mode in ("fp32", "tf32"):
+        got, _ = oracle.gemm(mode, A, B, alpha=alpha, beta=beta, C=C)
+        assert np.array_equal(got, want), mode
+    got, _ = oracle.gemm("bf16", si.bf16_bits(si.to_bf16(torch.from_numpy(A))),
+                         si.bf16_bits(si.to_bf16(torch.from_numpy(B))), alpha=alpha, beta=beta, C=C)
+    assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------- structure
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+def test_identity_and_permutation(mode):
+    rng = np.random.default_rng(3)
+    M, N = 9, 11
+    b = rng.standard_normal((M, N)).astype(np.float32)
+    c = rng.standard_normal((M, N)).astype(np.float32)
+    eye = np.eye(M, dtype=np.float32)
+    A, B, _, qb = _operands(mode, eye, b)
+    got, _ = oracle.gemm(mode, A, B)
+    assert np.array_equal(got, qb)
+    got, _ = oracle.gemm(mode, A, B, alpha=0.5, beta=1.0, C=c)
+    assert np.array_equal(got, 0.5 * qb + c.astype(np.float64))
+    perm = rng.permutation(M)
+    P = np.zeros((M, M), dtype=np.float32)
+    P[np.arange(M), perm] = 1.0
+    A, B, _, qb = _operands(mode, P, b)
+    got, _ = oracle.gemm(mode, A, B)
+    assert np.array_equal(got, qb[perm])
+    # B = P^T on the right permutes columns of A
+    A2, B2, qa2, _ = _operands(mode, b.T.copy(), P.T.copy())
+    got, _ = oracle.gemm(mode, A2, B2)
+    assert np.array_equal(got, qa2[:, perm])
+
+
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+@pytest.mark.parametrize("tA,tB", TRANS)
+def test_small_integers_are_exact(mode, tA, tB):
+    M, N, K = 40, 33, 1024
+    a = si.integers((K, M) if tA else (M, K), 11).numpy()
+    b = si.integers((N, K) if tB else (K, N), 12).numpy()
+    A, B, _, _ = _operands(mode, a, b)
+    got, D = oracle.gemm(mode, A, B, transA=tA, transB=tB)
+    want = _op(a.astype(np.int64), tA) @ _op(b.astype(np.int64), tB)
+    assert np.array_equal(got, want.astype(np.float64))
+    assert np.array_equal(D, np.abs(_op(a.astype(np.int64), tA)) @ np.abs(_op(b.astype(np.int64), tB)))
+
+
+def test_rank_one_closed_form():
+    M, N, K = 13, 17, 300
+    u = (np.arange(M, dtype=np.float32) - 6) / 4
+    v = (np.arange(N, dtype=np.float32) - 8) / 8
+    A = np.repeat(u[:, None], K, axis=1)
+    B = np.repeat(v[None, :], K, axis=0)
+    c = np.full((M, N), 3.0, dtype=np.float32)
+    got, D = oracle.gemm("fp32", A, B, alpha=2.0, beta=-1.0, C=c)
+    want = 2.0 * K * np.outer(u.astype(np.float64), v.astype(np.float64)) - 3.0
+    assert np.array_equal(got, want)
+    assert np.array_equal(D, K * np.abs(np.outer(u, v)).astype(np.float64))
+
+
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+def test_transpose_flags_match_explicit_transpose(mode):
+    rng = np.random.default_rng(5)
+    M, N, K = 19, 23, 29
+    a = rng.standard_normal((M, K)).astype(np.float32)
+    b = rng.standard_normal((K, N)).astype(np.float32)
+    A, B, _, _ = _operands(mode, a, b)
+    ref, _ = oracle.gemm(mode, A, B)
+    for tA, tB in TRANS:
+        At = np.ascontiguousarray(A.T) if tA else A
+        Bt = np.ascontiguousarray(B.T) if tB else B
+        got, _ = oracle.gemm(mode, At, Bt, transA=tA, transB=tB)
+        assert np.array_equal(got, ref), (tA, tB)
+
+
+def test_leading_dimensions_and_row_sampling():
+    rng = np.random.default_rng(6)
+    M, N, K = 12, 10, 8
+    big = rng.standard_normal((M, K + 5)).astype(np.float32)
+    a = big[:, :K]                       # lda = K + 5
+    b = rng.standard_normal((K, N)).astype(np.float32)
+    full, _ = oracle.gemm("fp32", a, b)
+    part, _ = oracle.gemm("fp32", a, b, rows=(3, 9))
+    assert np.array_equal(part, full[3:9])
+    assert np.array_equal(full, oracle.gemm("fp32", np.ascontiguousarray(a), b)[0])
+
+
+def test_matches_torch_float64_matmul():
+    M, N, K = 64, 48, 512
+    a = si.normal((M, K), 21).numpy()
+    b = si.normal((K, N), 22).numpy()
+    got, D = oracle.gemm("fp32", a, b)
+    want = (torch.from_numpy(a).double() @ torch.from_numpy(b).double()).numpy()
+    assert np.max(np.abs(got - want) / D) < 1e-12
+
+
+# ---------------------------------------------------------------- conventions
+def test_k_zero_and_alpha_zero_give_beta_c():
+    c = np.arange(6, dtype=np.float32).reshape(2, 3)
+    got, D = oracle.gemm("fp32", np.zeros((2, 0), np.float32), np.zeros((0, 3), np.float32),
+                         alpha=1.0, beta=2.0, C=c)
+    assert np.array_equal(got, 2.0 * c) and not D.any()
+    nanA = np.full((2, 4), np.nan, dtype=np.float32)
+    got, _ = oracle.gemm("fp32", nanA, np.ones((4, 3), np.float32), alpha=0.0, beta=-1.0, C=c)
+    assert np.array_equal(got, -c.astype(np.float64))
+
+
+def test_beta_zero_does_not_read_c():
+    a = np.ones((2, 2), np.float32)
+    got, _ = oracle.gemm("fp32", a, a, beta=0.0, C=np.full((2, 2), np.nan, np.float32))
+    assert np.array_equal(got, np.full((2, 2), 2.0))
+
+
+# ---------------------------------------------------------------- error model
+def test_tf32_error_is_of_the_expected_size():
+    """TF32 operands cost about 2^-11 relative error per product; FP32 about 2^-24.
+
+    "bare-metal-bard" (first paragraph) puts TF32's error at thousands of
+    times FP32's; the ratio of the unit roundoffs is 2^13 = 8192.
+    """
+    M, N, K = 64, 64, 1024
+    a = si.normal((M, K), 31).numpy()
+    b = si.normal((K, N), 32).numpy()
+    ref, D = oracle.gemm("fp32", a, b)
+    tf, _ = oracle.gemm("tf32", a, b)
+    e_tf32 = np.abs(tf - ref) / D
+    assert 1e-6 < np.max(e_tf32) < _gate.TOL["tf32"]
+    sgemm = (torch.from_numpy(a) @ torch.from_numpy(b)).numpy().astype(np.float64)
+    e_fp32 = np.abs(sgemm - ref) / D
+    assert np.max(e_fp32) < _gate.TOL["fp32"]
+    ratio = np.median(e_tf32) / max(np.median(e_fp32), 1e-30)
+    assert 1e2 < ratio < 1e5, ratio
+
+
+def test_gate_rejects_one_dropped_term():
+    """The gate is not vacuous: an oracle with one k-term dropped fails it."""
+    M, N, K = 32, 32, 256
+    a = si.uniform((M, K), 41).numpy()
+    b = si.uniform((K, N), 42).numpy()
+    ref, D = oracle.gemm("fp32", a, b)
+    broken, _ = oracle.gemm("fp32", a[:, 1:].copy(), b[1:, :].copy())  # planted: k = 0 dropped
+    assert _gate.max_err(broken, ref, D) > _gate.TOL["bf16"]
+    with pytest.raises(AssertionError):
+        _gate.assert_within("fp32", broken, ref, D)
+    flipped, _ = oracle.gemm("fp32", a, b, alpha=-1.0)  # planted: wrong sign
+    with pytest.raises(AssertionError):
+        _gate.assert_within("bf16", flipped, ref, D)
+    _gate.assert_within("fp32", ref.astype(np.float32), ref, D)
