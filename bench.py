@@ -1,0 +1,410 @@
+"""Benchmark of the GB300 dense GEMM library.
+
+Default workload: the projection GEMMs of one training step of the 6-layer,
+d_model = 384 character GPT of "bare-metal-bard" (second paragraph) at batch
+64 x context 256 (16384 token rows): for each of the five projections (QKV,
+attention out, MLP up, MLP down, LM head) the forward Y = X W, the input
+gradient dX = dY W^T and the weight gradient dW = X^T dY, each in FP32 (CUDA
+cores) and in TF32 (tensor cores): 30 GEMMs per step.  Activations and
+gradients are N(0, 1), weights N(0, 0.02^2), drawn from seeded generators
+(seeded_inputs.py); there is no dataset.
+
+One JSON line on rank 0: whole-job TFLOP/s over the timed steps (CUDA events
+on the launching stream), the end-to-end figure through the C ABI with the
+inputs copied from pinned host memory and the outputs copied back inside the
+timed region, the roofline of the dominant kernel, the per-shape breakdown,
+and the oracle timed on a bounded sample on the host cores.
+
+`--impl reference` times the CPU oracle (the only reference arm there is:
+the pages publish no code) on a bounded sample of the same workload.
+`--gpus N` under torchrun runs N independent replicas (GEMM shards with no
+exchange), one per rank; value = all ranks' FLOPs / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "GEMM TFLOP/s per shape & % of GB300 roofline (tensor peak or HBM BW), 1 GPU"
+SMS = 152
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2070.0
+# Nominal dense rates (recipe): tf32 1.1 PF vs bf16 2.25 PF.
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    src = "measured"
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        hbm, bf16, bf16_s = p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"]
+    except Exception:
+        hbm, bf16, bf16_s, src = 6800.0, 1900.0, 1700.0, "fallback"
+    fp32_alu = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
+    return {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": bf16_s,
+            "tf32_tflops": bf16 * TF32_OVER_BF16, "tf32_tflops_sustained": bf16_s * TF32_OVER_BF16,
+            "fp32_alu_tflops": fp32_alu, "source": src}
+
+
+class Call:
+    """One GEMM of the step with its buffers."""
+
+    def __init__(self, case: si.GemmCase, mode: str, A, B, C):
+        self.case, self.mode, self.A, self.B, self.C = case, mode, A, B, C
+
+    @property
+    def name(self):
+        return f"{self.mode}.{self.case.name}"
+
+    def bytes(self):
+        es = 2 if self.mode == "bf16" else 4
+        c = self.case
+        return es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N
+
+
+def gpt_workload(device):
+    """Inputs X, W, dY of every projection and one output per (mode, GEMM)."""
+    calls, inputs = [], []
+    cases = si.gpt_cases()
+    for p, (name, kin, nout) in enumerate(si.GPT_PROJECTIONS):
+        X, W, dY = si.gpt_tensors(p, kin, nout)
+        inputs += [X, W, dY]
+    dev_inputs = [t.to(device) for t in inputs]
+    for mode in ("fp32", "tf32"):
+        for p in range(len(si.GPT_PROJECTIONS)):
+            X, W, dY = dev_inputs[3 * p: 3 * p + 3]
+            fwd, dx, dw = cases[3 * p: 3 * p + 3]
+            calls.append(Call(fwd, mode, X, W, torch.empty((fwd.M, fwd.N), device=device)))
+            calls.append(Call(dx, mode, dY, W, torch.empty((dx.M, dx.N), device=device)))
+            calls.append(Call(dw, mode, X, dY, torch.empty((dw.M, dw.N), device=device)))
+    return calls, inputs, dev_inputs
+
+
+def run_call(h, c: Call, stream):
+    h.run(c.A, c.B, c.C, mode=c.mode, transA=c.case.transA, transB=c.case.transB, stream=stream)
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv") if os.path.isdir(
+            os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        try:
+            self.fh.close()
+        except Exception:
+            pass
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+def oracle_sample(calls_meta, budget_macs):
+    """Time the oracle on the first rows of every GEMM; returns (flops, seconds, rows)."""
+    import numpy as np
+
+    import oracle
+    cores = os.cpu_count() or 1
+    flops, secs, desc = 0, 0.0, []
+    per_call = budget_macs / max(len(calls_meta), 1)
+    cache = {}
+    for mode, case, (a_t, b_t) in calls_meta:
+        key = (id(a_t), id(b_t))
+        if key not in cache:
+            cache[key] = (a_t.numpy(), b_t.numpy())
+        a, b = cache[key]
+        rows = int(max(cores, min(case.M, per_call // max(case.N * case.K, 1))))
+        rows = min(rows, case.M)
+        t0 = time.perf_counter()
+        oracle.gemm(mode, a, b, transA=case.transA, transB=case.transB, rows=(0, rows))
+        secs += time.perf_counter() - t0
+        flops += 2 * rows * case.N * case.K
+        desc.append(rows)
+    return flops, secs, desc
+
+
+def cpu_meta():
+    """The (mode, case, host tensors) list of the GPT workload, host side only."""
+    cases = si.gpt_cases()
+    meta = []
+    host = []
+    for p, (name, kin, nout) in enumerate(si.GPT_PROJECTIONS):
+        host.append(si.gpt_tensors(p, kin, nout))
+    for mode in ("fp32", "tf32"):
+        for p in range(len(si.GPT_PROJECTIONS)):
+            X, W, dY = host[p]
+            fwd, dx, dw = cases[3 * p: 3 * p + 3]
+            meta += [(mode, fwd, (X, W)), (mode, dx, (dY, W)), (mode, dw, (X, dY))]
+    return meta
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl != "reference" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def bench_reference(args, world, rank):
+    """The CPU oracle as the reference arm, on a bounded sample per step."""
+    if rank != 0:
+        return
+    meta = cpu_meta()
+    total_flops = sum(2 * c.M * c.N * c.K for _, c, _ in meta)
+    for _ in range(args.warmup):
+        oracle_sample(meta[:2], 1e7)
+    flops = secs = 0.0
+    rows = None
+    for _ in range(args.steps):
+        f, s, rows = oracle_sample(meta, args.ref_macs)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    sample = (f"first rows of each of the 30 GEMMs ({min(rows)}..{max(rows)} rows, "
+              f"{flops / args.steps / total_flops * 100:.3f}% of a step's FLOPs per step)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
+            "config": {"workload": "gpt_projections_fp32_tf32", "tokens": si.GPT_TOKENS, "d_model": 384,
+                       "gemms_per_step": 30},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def bench_ours(args, world, rank, local):
+    import dense_gemm_transformer_gb300 as dg
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    dg.load(build_if_missing=True)
+    h = dg.Gemm()
+    stream = torch.cuda.Stream(dev)
+    calls, host_inputs, dev_inputs = gpt_workload(dev)
+    step_flops = sum(c.case.flops for c in calls)
+    pk = peaks()
+
+    def step():
+        for c in calls:
+            run_call(h, c, stream)
+
+    # Launch counts per call (deterministic plans).
+    launches = 0
+    with torch.cuda.stream(stream):
+        for c in calls:
+            run_call(h, c, stream)
+            launches += h.plan()["kernels"]
+    stream.synchronize()
+    assert h.check_device(stream) == 0
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+
+    # Timed region: K whole steps, CUDA events around every call on the stream.
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.4)
+        t_start.record(stream)
+        for s in range(args.steps):
+            for i, c in enumerate(calls):
+                ev[s][i][0].record(stream)
+                run_call(h, c, stream)
+                ev[s][i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    assert h.check_device(stream) == 0
+    per_call_ms = [statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
+                   for i in range(len(calls))]
+    ms_per_step = total_ms / args.steps
+    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+
+    # Per-shape breakdown against each mode's roof.
+    shapes = []
+    for c, ms in zip(calls, per_call_ms):
+        peak = pk["fp32_alu_tflops"] if c.mode == "fp32" else pk["tf32_tflops_sustained"]
+        t_roof = max(c.case.flops / (peak * 1e12), c.bytes() / (pk["hbm_gbs"] * 1e9))
+        bound = ("alu" if c.mode == "fp32" else "tensor") if c.case.flops / (peak * 1e12) >= c.bytes() / (
+            pk["hbm_gbs"] * 1e9) else "hbm"
+        shapes.append({"gemm": c.name, "M": c.case.M, "N": c.case.N, "K": c.case.K, "ms": round(ms, 4),
+                       "tflops": round(c.case.flops / (ms * 1e-3) / 1e12, 2), "bound": bound,
+                       "roofline_frac": round(t_roof / (ms * 1e-3), 3)})
+
+    # Dominant kernel family = the mode with the larger share of the step.
+    fam_ms = {m: sum(ms for c, ms in zip(calls, per_call_ms) if c.mode == m) for m in ("fp32", "tf32")}
+    dom = max(fam_ms, key=fam_ms.get)
+    dom_flops = sum(c.case.flops for c in calls if c.mode == dom)
+    n_launch = sum(1 for c in calls if c.mode == dom)
+    achieved = dom_flops / (fam_ms[dom] * 1e-3) / 1e12
+    if dom == "fp32":
+        roof = {"bound": "alu", "kernel": "simt_gemm_kernel (FP32 FFMA)", "achieved": achieved,
+                "peak": pk["fp32_alu_tflops"], "unit": "TFLOP/s",
+                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz"}
+    else:
+        roof = {"bound": "tensor", "kernel": "tc_gemm_kernel (tcgen05 kind::tf32)", "achieved": achieved,
+                "peak": pk["tf32_tflops_sustained"], "unit": "TFLOP/s",
+                "peak_source": f"{pk['source']} bf16 sustained x 1.1/2.25 (nominal tf32/bf16)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["launches_per_step"] = n_launch
+    roof["share_of_step"] = fam_ms[dom] / sum(per_call_ms)
+
+    # End to end through the C ABI: pinned host inputs -> device, the 30 GEMMs,
+    # every output -> pinned host, all inside the timed region.
+    e2e = None
+    if not args.no_e2e:
+        pinned_in = [t.pin_memory() for t in host_inputs]
+        pinned_out = [torch.empty(c.C.shape, dtype=c.C.dtype, pin_memory=True) for c in calls]
+        h2d = sum(t.numel() * t.element_size() for t in pinned_in)
+        d2h = sum(t.numel() * t.element_size() for t in pinned_out)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for src, dst in zip(pinned_in, dev_inputs):
+                    dst.copy_(src, non_blocking=True)
+                step()
+                for c, dst in zip(calls, pinned_out):
+                    dst.copy_(c.C, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        stream.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
+        e2e = {"value": world * step_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, s, rows = oracle_sample(cpu_meta(), args.cpu_macs)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"first {min(rows)}..{max(rows)} rows of each of the 30 GEMMs "
+                         f"({f / step_flops * 100:.3f}% of a step's FLOPs, {s:.1f} s)"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32+tf32",
+                "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
+                "config": {"workload": "gpt_projections_fp32_tf32", "tokens": si.GPT_TOKENS, "d_model": 384,
+                           "gemms_per_step": len(calls), "parallelism": f"replicas{world}",
+                           "l2": "inputs larger than L2: a step touches %.2f GB; no tensor is re-read "
+                                 "before >4x L2 of other traffic" % (sum(c.bytes() for c in calls) / 1e9)},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * args.steps,
+                "clocks": clk.summary(), "shapes": shapes, "peaks": pk}
+        print(json.dumps(line), flush=True)
+    h.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-macs", type=float, default=3e9, help="oracle multiply-adds in the CPU baseline")
+    ap.add_argument("--ref-macs", type=float, default=3e8, help="oracle multiply-adds per reference step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        bench_reference(args, world, rank)
+    else:
+        bench_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+"""Python binding of libgemm.so, the GB300 dense GEMM library.
+
+Argument marshalling only: torch tensors are turned into device pointers,
+sizes, leading dimensions and the current CUDA stream, and every call goes
+through the C ABI declared in include/gemm.h.  All arithmetic happens in the
+library's kernels; there is no CPU or PyTorch fallback, and using the library
+without the built extension raises.
+
+    import torch, dense_gemm_transformer_gb300 as dg
+    C = torch.empty(M, N, device="cuda")
+    dg.gemm(A, B, C, mode="tf32")                # C = A @ B
+    dg.gemm(A, W, C, mode="bf16", transB=True)   # C = A @ W^T, W stored N x K
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import _build
+
+MODES = {"fp32": 0, "tf32": 1, "bf16": 2}
+FAMILIES = {"auto": 0, "simt": 1, "tc": 2, "skinny": 3}
+OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3}
+STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED", 3: "GEMM_ERR_MISALIGNED",
+          4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_ALLOC", 6: "GEMM_ERR_DEVICE_TIMEOUT"}
+HEADER = os.path.join(_build.ROOT, "include", "gemm.h")
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("family", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("tile_k", ctypes.c_int32), ("split_k", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("kernels", ctypes.c_int32), ("packed", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 7)]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Load libgemm.so (building it first only if asked) and declare its ABI."""
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if build_if_missing:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                               "(the library has no fallback path)")
+        lib = ctypes.CDLL(path)
+        i64, vp, f32, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+        lib.gemm_create.argtypes = [ctypes.POINTER(vp)]
+        lib.gemm_destroy.argtypes = [vp]
+        lib.gemm_run.argtypes = [vp, i32, i32, i32, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        lib.gemm_validate.argtypes = [i32, i32, i32, i64, i64, i64, f32, vp, i64, vp, i64, vp, i64]
+        lib.gemm_set_option.argtypes = [vp, i32, i64]
+        lib.gemm_get_plan.argtypes = [vp, ctypes.POINTER(Plan)]
+        lib.gemm_check_device.argtypes = [vp, vp]
+        lib.gemm_status_string.argtypes = [i32]
+        lib.gemm_status_string.restype = ctypes.c_char_p
+        for name in ("gemm_create", "gemm_destroy", "gemm_run", "gemm_validate", "gemm_set_option",
+                     "gemm_get_plan", "gemm_check_device"):
+            getattr(lib, name).restype = i32
+        _lib = lib
+        return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/gemm.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:gemm_status_t|const char\*)\s+(gemm_\w+)\s*\(", text, re.M)))
+
+
+def status_string(status: int) -> str:
+    return load().gemm_status_string(int(status)).decode()
+
+
+def validate(mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc) -> int:
+    """Run the library's argument checks on raw pointers (no device needed)."""
+    return load().gemm_validate(MODES[mode] if isinstance(mode, str) else int(mode), int(transA), int(transB),
+                                M, N, K, float(alpha), A, lda, B, ldb, C, ldc)
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise GemmError(status, what)
+
+
+def _matrix(t, name):
+    """(device pointer, leading dimension) of a row-major 2-D tensor."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    rows, cols = t.shape
+    if rows > 0 and cols > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} needs unit stride along its last dimension (row-major storage)")
+    ld = t.stride(0) if rows > 1 else max(cols, 1)
+    if rows > 1 and ld < cols:
+        raise ValueError(f"{name} has overlapping rows")
+    return t.data_ptr(), ld
+
+
+class Gemm:
+    """A library handle bound to the current CUDA device."""
+
+    def __init__(self):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _check(self._lib.gemm_create(ctypes.byref(h)), "gemm_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            st = self._lib.gemm_destroy(self._h)
+            self._h = None
+            _check(st, "gemm_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_option(self, name: str, value):
+        if name == "family" and isinstance(value, str):
+            value = FAMILIES[value]
+        _check(self._lib.gemm_set_option(self._h, OPTIONS[name], int(value)), f"gemm_set_option({name})")
+
+    def plan(self) -> dict:
+        p = Plan()
+        _check(self._lib.gemm_get_plan(self._h, ctypes.byref(p)), "gemm_get_plan")
+        fam = {v: k for k, v in FAMILIES.items()}.get(p.family, "none")
+        return {"family": fam if p.kernels else "none", "tile_m": p.tile_m, "tile_n": p.tile_n,
+                "tile_k": p.tile_k, "split_k": p.split_k, "stages": p.stages, "grid": p.grid,
+                "kernels": p.kernels, "packed": p.packed}
+
+    def check_device(self, stream=None) -> int:
+        """Synchronize the stream and return the device status (0 = ok)."""
+        return self._lib.gemm_check_device(self._h, _stream_ptr(stream))
+
+    def run_ptr(self, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+        """gemm_run on raw device pointers; `stream` is a torch stream, a raw handle or None."""
+        st = self._lib.gemm_run(self._h, MODES[mode] if isinstance(mode, str) else int(mode), int(transA),
+                                int(transB), int(M), int(N), int(K), float(alpha), A, int(lda), B, int(ldb),
+                                float(beta), C, int(ldc), _stream_ptr(stream))
+        _check(st, "gemm_run")
+
+    def run(self, A, B, C, mode="fp32", transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
+        """C = alpha * op(A) op(B) + beta * C on torch CUDA tensors (row-major)."""
+        import torch
+        want = torch.bfloat16 if mode == "bf16" else torch.float32
+        if A.dtype != want or B.dtype != want:
+            raise TypeError(f"mode {mode} takes {want} operands")
+        if C.dtype != torch.float32:
+            raise TypeError("C must be float32")
+        M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])
+        Kb, N = (B.shape[1], B.shape[0]) if transB else (B.shape[0], B.shape[1])
+        if K != Kb or tuple(C.shape) != (M, N):
+            raise ValueError(f"shapes do not agree: op(A) {M}x{K}, op(B) {Kb}x{N}, C {tuple(C.shape)}")
+        pa, lda = _matrix(A, "A")
+        pb, ldb = _matrix(B, "B")
+        pc, ldc = _matrix(C, "C")
+        if stream is None:
+            stream = torch.cuda.current_stream(C.device)
+        self.run_ptr(mode, transA, transB, M, N, K, alpha, pa, lda, pb, ldb, beta, pc, ldc, stream)
+        return C
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+_default = {}
+
+
+def default_handle() -> Gemm:
+    import torch
+    dev = torch.cuda.current_device()
+    if dev not in _default:
+        _default[dev] = Gemm()
+    return _default[dev]
+
+
+def gemm(A, B, C, mode="fp32", transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
+    """C = alpha * op(A) op(B) + beta * C with the current device's default handle."""
+    return default_handle().run(A, B, C, mode, transA, transB, alpha, beta, stream)

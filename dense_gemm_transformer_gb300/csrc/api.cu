@@ -1,0 +1,388 @@
+// api.cu -- the C ABI (gemm.h): handles, argument checks, the planner and the
+// workspace.
+//
+// The planner maps a call to one kernel family with a fixed rule (no runtime
+// autotuning):
+//   FP32             -> the register-tiled SIMT kernel; K is split when the
+//                       output has fewer 128 x 128 tiles than the two CTAs per
+//                       SM the kernel can keep resident.
+//   TF32, BF16       -> the persistent tcgen05 kernel; the tile width (128 or
+//                       256 columns) is the one that wastes the least work
+//                       over whole waves of one tile per SM, and K is split
+//                       when there are fewer tiles than half the SMs.
+// An operand whose base or leading dimension breaks the TMA unit's 16-byte
+// rule is first copied into the workspace with an aligned leading dimension.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "../../include/gemm.h"
+#include "kernels.h"
+
+struct gemm_handle_s {
+  int device = 0;
+  int sms = 0;
+  int* d_status = nullptr;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  int opt_family = GEMM_FAMILY_AUTO;
+  int opt_split_k = 0;
+  int opt_tile_n = 0;
+  gemm_plan_t plan{};
+};
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+gemm_status_t check_args(int mode, int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                         const void* A, int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc) {
+  if (mode < GEMM_MODE_FP32 || mode > GEMM_MODE_BF16) return GEMM_ERR_INVALID_VALUE;
+  if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return GEMM_ERR_INVALID_VALUE;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr || ldc < std::max<int64_t>(N, 1)) return GEMM_ERR_INVALID_VALUE;
+  if (!aligned(C, 4)) return GEMM_ERR_MISALIGNED;
+  if (K == 0 || alpha == 0.f) return GEMM_OK;  // A and B are not read
+  if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_VALUE;
+  if (lda < std::max<int64_t>(transA ? M : K, 1)) return GEMM_ERR_INVALID_VALUE;
+  if (ldb < std::max<int64_t>(transB ? K : N, 1)) return GEMM_ERR_INVALID_VALUE;
+  const size_t es = (mode == GEMM_MODE_BF16) ? 2 : 4;
+  if (!aligned(A, es) || !aligned(B, es)) return GEMM_ERR_MISALIGNED;
+  return GEMM_OK;
+}
+
+gemm_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA; }
+
+// Grow the workspace to at least `bytes`.  Freeing the old block waits for
+// the device, so earlier launches that still use it are finished.
+gemm_status_t ensure_ws(gemm_handle_s* h, size_t bytes) {
+  if (bytes <= h->ws_bytes) return GEMM_OK;
+  if (h->ws) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+    cudaFree(h->ws);
+    h->ws = nullptr;
+    h->ws_bytes = 0;
+  }
+  size_t want = std::max<size_t>(bytes, size_t(1) << 20);
+  if (cudaMalloc(&h->ws, want) != cudaSuccess) {
+    cudaGetLastError();
+    h->ws = nullptr;
+    return GEMM_ERR_ALLOC;
+  }
+  h->ws_bytes = want;
+  return GEMM_OK;
+}
+
+struct WsLayout {
+  size_t a_off = 0, b_off = 0, p_off = 0, total = 0;
+};
+
+void set_plan(gemm_handle_s* h, int family, int tm, int tn, int tk, int splits, int stages, int grid, int kernels,
+              int packed) {
+  gemm_plan_t p{};
+  p.family = family;
+  p.tile_m = tm;
+  p.tile_n = tn;
+  p.tile_k = tk;
+  p.split_k = splits;
+  p.stages = stages;
+  p.grid = grid;
+  p.kernels = kernels;
+  p.packed = packed;
+  h->plan = p;
+}
+
+gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                       const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+                       cudaStream_t s) {
+  using namespace dgt;
+  const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, kSimtTileN);
+  int64_t splits = 1;
+  if (h->opt_split_k > 0) {
+    splits = h->opt_split_k;
+  } else if (tiles < h->sms && K >= 1024) {
+    splits = std::min<int64_t>(ceil_div(2 * h->sms, tiles), K / 256);
+    splits = std::max<int64_t>(splits, 1);
+  }
+  int64_t kps = round_up(ceil_div(K, splits), kSimtTileK);
+  splits = ceil_div(K, kps);
+  SimtArgs a{};
+  a.transA = transA;
+  a.transB = transB;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = A;
+  a.lda = lda;
+  a.B = B;
+  a.ldb = ldb;
+  a.C = C;
+  a.ldc = ldc;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.splits = static_cast<int>(splits);
+  a.k_per_split = kps;
+  a.ws_ld = round_up(N, 4);
+  if (splits > 1) {
+    gemm_status_t st = ensure_ws(h, static_cast<size_t>(splits * M * a.ws_ld) * sizeof(float));
+    if (st != GEMM_OK) return st;
+    a.ws = static_cast<float*>(h->ws);
+  }
+  if (ceil_div(M, kSimtTileM) > 65535) return GEMM_ERR_NOT_SUPPORTED;
+  cudaError_t e = launch_simt(a, s);
+  if (e != cudaSuccess) return GEMM_ERR_CUDA;
+  int kernels = 1;
+  if (splits > 1) {
+    e = launch_splitk_reduce(M, N, a.splits, a.ws, a.ws_ld, C, ldc, alpha, beta, s);
+    if (e != cudaSuccess) return GEMM_ERR_CUDA;
+    ++kernels;
+  }
+  set_plan(h, GEMM_FAMILY_SIMT, kSimtTileM, kSimtTileN, kSimtTileK, a.splits, 2, static_cast<int>(tiles * splits),
+           kernels, 0);
+  return GEMM_OK;
+}
+
+gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
+                     float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
+                     int64_t ldc, cudaStream_t s) {
+  using namespace dgt;
+  const int es = (mode == GEMM_MODE_BF16) ? 2 : 4;
+  const int bk = tc_tile_k(mode);
+  const int sms = h->sms;
+
+  // Tile width: the fewest padded columns over whole waves of one tile per SM.
+  int tile_n = h->opt_tile_n;
+  if (tile_n != 128 && tile_n != 256) {
+    const int64_t tm = ceil_div(M, 128);
+    int64_t best = -1;
+    for (int bn : {256, 128}) {
+      const int64_t waves = ceil_div(tm * ceil_div(N, bn), sms);
+      const int64_t cost = waves * bn;
+      if (best < 0 || cost < best) {
+        best = cost;
+        tile_n = bn;
+      }
+    }
+  }
+  const int64_t tiles = ceil_div(M, 128) * ceil_div(N, tile_n);
+  const int64_t kb = ceil_div(K, bk);
+  int64_t splits = 1;
+  if (h->opt_split_k > 0) {
+    splits = std::min<int64_t>(h->opt_split_k, kb);
+  } else if (2 * tiles <= sms && kb >= 8) {
+    splits = std::min<int64_t>(sms / tiles, kb / 4);
+    splits = std::max<int64_t>(splits, 1);
+  }
+  const int64_t kb_per = ceil_div(kb, splits);
+  splits = ceil_div(kb, kb_per);
+
+  // Workspace: re-packed operands (when the TMA rule needs them) and partials.
+  const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
+  const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
+  const bool pack_a = !aligned(A, 16) || (lda * es) % 16 != 0;
+  const bool pack_b = !aligned(B, 16) || (ldb * es) % 16 != 0;
+  const int64_t lda_p = round_up(a_cols, 16 / es), ldb_p = round_up(b_cols, 16 / es);
+  WsLayout L;
+  L.a_off = 0;
+  L.b_off = round_up(pack_a ? a_rows * lda_p * es : 0, 256);
+  L.p_off = L.b_off + round_up(pack_b ? b_rows * ldb_p * es : 0, 256);
+  const int64_t ws_ld = round_up(N, 4);
+  L.total = L.p_off + (splits > 1 ? static_cast<size_t>(splits * M * ws_ld) * sizeof(float) : 0);
+  if (L.total > 0) {
+    gemm_status_t st = ensure_ws(h, L.total);
+    if (st != GEMM_OK) return st;
+  }
+  char* ws = static_cast<char*>(h->ws);
+  int kernels = 0;
+  const void* Ause = A;
+  const void* Buse = B;
+  int64_t lda_use = lda, ldb_use = ldb;
+  if (pack_a) {
+    if (launch_pack(A, lda, ws + L.a_off, lda_p, a_rows, a_cols, es, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    Ause = ws + L.a_off;
+    lda_use = lda_p;
+    ++kernels;
+  }
+  if (pack_b) {
+    if (launch_pack(B, ldb, ws + L.b_off, ldb_p, b_rows, b_cols, es, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    Buse = ws + L.b_off;
+    ldb_use = ldb_p;
+    ++kernels;
+  }
+
+  TcArgs a{};
+  a.mode = mode;
+  a.a_mn_major = transA ? 1 : 0;
+  a.b_mn_major = transB ? 0 : 1;
+  a.tile_n = tile_n;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.A = Ause;
+  a.lda = lda_use;
+  a.B = Buse;
+  a.ldb = ldb_use;
+  a.C = C;
+  a.ldc = ldc;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.splits = static_cast<int>(splits);
+  a.kb_per_split = static_cast<int>(kb_per);
+  a.ws = splits > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
+  a.ws_ld = ws_ld;
+  a.status = h->d_status;
+  a.grid = static_cast<int>(std::min<int64_t>(tiles * splits, sms));
+  a.group_m = 16;
+  if (launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  ++kernels;
+  if (splits > 1) {
+    if (launch_splitk_reduce(M, N, a.splits, a.ws, ws_ld, C, ldc, alpha, beta, s) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    ++kernels;
+  }
+  set_plan(h, GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n), a.grid, kernels,
+           (pack_a ? 1 : 0) | (pack_b ? 2 : 0));
+  return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_create(gemm_handle_t* out) {
+  if (out == nullptr) return GEMM_ERR_INVALID_VALUE;
+  *out = nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  // The kernels are built for sm_103a only.
+  if (major != 10 || minor != 3) return GEMM_ERR_NOT_SUPPORTED;
+  gemm_handle_s* h = new (std::nothrow) gemm_handle_s();
+  if (h == nullptr) return GEMM_ERR_ALLOC;
+  h->device = dev;
+  h->sms = sms;
+  if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return GEMM_ERR_ALLOC;
+  }
+  if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
+    cudaFree(h->d_status);
+    delete h;
+    return GEMM_ERR_CUDA;
+  }
+  *out = h;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_destroy(gemm_handle_t h) {
+  if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(h->device);
+  gemm_status_t st = cuda_status(cudaDeviceSynchronize());
+  if (h->ws) cudaFree(h->ws);
+  if (h->d_status) cudaFree(h->d_status);
+  cudaSetDevice(prev);
+  delete h;
+  return st;
+}
+
+gemm_status_t gemm_validate(int mode, int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                            const void* A, int64_t lda, const void* B, int64_t ldb, const float* C, int64_t ldc) {
+  return check_args(mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc);
+}
+
+gemm_status_t gemm_run(gemm_handle_t h, int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
+                       float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
+                       int64_t ldc, void* stream) {
+  if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
+  gemm_status_t st = check_args(mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc);
+  if (st != GEMM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 0 || N == 0) {
+    set_plan(h, 0, 0, 0, 0, 0, 0, 0, 0, 0);
+    return GEMM_OK;
+  }
+  if (K == 0 || alpha == 0.f) {
+    if (dgt::launch_scale(M, N, C, ldc, beta, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    set_plan(h, 0, 0, 0, 0, 1, 0, 0, 1, 0);
+    return GEMM_OK;
+  }
+  const int fam = h->opt_family;
+  if (mode == GEMM_MODE_FP32) {
+    if (fam != GEMM_FAMILY_AUTO && fam != GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
+    return run_simt(h, transA, transB, M, N, K, alpha, static_cast<const float*>(A), lda,
+                    static_cast<const float*>(B), ldb, beta, C, ldc, s);
+  }
+  if (fam != GEMM_FAMILY_AUTO && fam != GEMM_FAMILY_TC) return GEMM_ERR_NOT_SUPPORTED;
+  return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s);
+}
+
+gemm_status_t gemm_set_option(gemm_handle_t h, int option, int64_t value) {
+  if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
+  switch (option) {
+    case GEMM_OPT_FAMILY:
+      if (value < GEMM_FAMILY_AUTO || value > GEMM_FAMILY_SKINNY) return GEMM_ERR_INVALID_VALUE;
+      h->opt_family = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_SPLIT_K:
+      if (value < 0 || value > 4096) return GEMM_ERR_INVALID_VALUE;
+      h->opt_split_k = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_TILE_N:
+      if (value != 0 && value != 128 && value != 256) return GEMM_ERR_INVALID_VALUE;
+      h->opt_tile_n = static_cast<int>(value);
+      return GEMM_OK;
+    default:
+      return GEMM_ERR_INVALID_VALUE;
+  }
+}
+
+gemm_status_t gemm_get_plan(gemm_handle_t h, gemm_plan_t* out) {
+  if (h == nullptr || out == nullptr) return GEMM_ERR_INVALID_VALUE;
+  *out = h->plan;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_check_device(gemm_handle_t h, void* stream) {
+  if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GEMM_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (v != 0) {
+    if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+    return GEMM_ERR_DEVICE_TIMEOUT;
+  }
+  return GEMM_OK;
+}
+
+const char* gemm_status_string(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_VALUE: return "GEMM_ERR_INVALID_VALUE";
+    case GEMM_ERR_NOT_SUPPORTED: return "GEMM_ERR_NOT_SUPPORTED";
+    case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_ALLOC: return "GEMM_ERR_ALLOC";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT";
+    default: return "GEMM_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,122 @@
+// aux.cu -- the small HBM-bound kernels around the GEMM kernels: the split-K
+// reduction with the fused alpha/beta epilogue, the beta-only update used when
+// K == 0 or alpha == 0, and the operand re-pack that gives an operand with an
+// unaligned leading dimension a 16-byte-aligned copy the TMA unit can read.
+// All three are grid-stride loops over rows x 4-wide column groups, sized to a
+// few CTAs per SM.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace dgt {
+namespace {
+
+int grid_for(int64_t work, int threads) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (work + threads - 1) / threads;
+  int64_t cap = static_cast<int64_t>(sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<int>(blocks);
+}
+
+// One thread per 4-column group of a row; the workspace rows are 16-byte
+// aligned (ws_ld % 4 == 0), C is read/written by float4 only when CVEC.
+template <bool CVEC>
+__global__ void splitk_reduce_kernel(int64_t M, int64_t N, int splits, const float* __restrict__ ws, int64_t ws_ld,
+                                     float* __restrict__ C, int64_t ldc, float alpha, float beta) {
+  const int64_t groups = (N + 3) / 4;
+  const int64_t total = M * groups;
+  const int64_t slice = M * ws_ld;
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = g / groups, c = (g % groups) * 4;
+    const float* src = ws + r * ws_ld + c;
+    float4 s = *reinterpret_cast<const float4*>(src);
+    for (int k = 1; k < splits; ++k) {
+      const float4 t = *reinterpret_cast<const float4*>(src + k * slice);
+      s.x += t.x;
+      s.y += t.y;
+      s.z += t.z;
+      s.w += t.w;
+    }
+    float v[4] = {alpha * s.x, alpha * s.y, alpha * s.z, alpha * s.w};
+    float* dst = C + r * ldc + c;
+    if (CVEC && c + 3 < N) {
+      float4* d4 = reinterpret_cast<float4*>(dst);
+      if (beta != 0.f) {
+        const float4 old = *d4;
+        v[0] = fmaf(beta, old.x, v[0]);
+        v[1] = fmaf(beta, old.y, v[1]);
+        v[2] = fmaf(beta, old.z, v[2]);
+        v[3] = fmaf(beta, old.w, v[3]);
+      }
+      *d4 = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+      for (int j = 0; j < 4 && c + j < N; ++j) dst[j] = (beta != 0.f) ? fmaf(beta, dst[j], v[j]) : v[j];
+    }
+  }
+}
+
+__global__ void scale_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_t ldc, float beta) {
+  const int64_t total = M * N;
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = g / N, c = g % N;
+    float* p = C + r * ldc + c;
+    *p = (beta != 0.f) ? beta * *p : 0.f;
+  }
+}
+
+template <typename T>
+__global__ void pack_kernel(const T* __restrict__ src, int64_t ld_src, T* __restrict__ dst, int64_t ld_dst,
+                            int64_t rows, int64_t cols) {
+  const int64_t total = rows * cols;
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = g / cols, c = g % cols;
+    dst[r * ld_dst + c] = src[r * ld_src + c];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_splitk_reduce(int64_t M, int64_t N, int splits, const float* ws, int64_t ws_ld, float* C,
+                                 int64_t ldc, float alpha, float beta, cudaStream_t stream) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = grid_for(M * ((N + 3) / 4), threads);
+  const bool cvec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && (ldc % 4 == 0);
+  if (cvec)
+    splitk_reduce_kernel<true><<<blocks, threads, 0, stream>>>(M, N, splits, ws, ws_ld, C, ldc, alpha, beta);
+  else
+    splitk_reduce_kernel<false><<<blocks, threads, 0, stream>>>(M, N, splits, ws, ws_ld, C, ldc, alpha, beta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta, cudaStream_t stream) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  const int threads = 256;
+  scale_kernel<<<grid_for(M * N, threads), threads, 0, stream>>>(M, N, C, ldc, beta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
+                        int elem_bytes, cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = grid_for(rows * cols, threads);
+  if (elem_bytes == 2)
+    pack_kernel<uint16_t><<<blocks, threads, 0, stream>>>(static_cast<const uint16_t*>(src), ld_src,
+                                                           static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+  else
+    pack_kernel<float><<<blocks, threads, 0, stream>>>(static_cast<const float*>(src), ld_src,
+                                                        static_cast<float*>(dst), ld_dst, rows, cols);
+  return cudaGetLastError();
+}
+
+}  // namespace dgt

@@ -1,0 +1,73 @@
+// kernels.h -- host-side launch entry points of the library's kernels (internal).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dgt {
+
+// ---------------------------------------------------------------- FP32 SIMT
+// C = alpha * op(A) op(B) + beta * C with FFMA, 128 x 128 block tiles.  With
+// splits > 1, slice s of K (k_per_split elements, a multiple of 16) writes its
+// raw partial sums to ws + s * M * ws_ld and a reduce kernel finishes.
+struct SimtArgs {
+  int transA, transB;
+  int64_t M, N, K;
+  const float* A;
+  int64_t lda;
+  const float* B;
+  int64_t ldb;
+  float* C;
+  int64_t ldc;
+  float alpha, beta;
+  int splits;
+  int64_t k_per_split;
+  float* ws;
+  int64_t ws_ld;
+};
+constexpr int kSimtTileM = 128, kSimtTileN = 128, kSimtTileK = 16, kSimtThreads = 256;
+cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- tcgen05
+// Persistent TMA + tcgen05 kernel: one 128 x tile_n output tile per work unit,
+// an smem ring fed by a TMA producer warp, a single-thread MMA issuer with a
+// double-buffered TMEM accumulator, and four epilogue warps.
+struct TcArgs {
+  int mode;              // 1 = tf32, 2 = bf16 (gemm_mode_t)
+  int a_mn_major;        // A stored with M contiguous (transA == 1)
+  int b_mn_major;        // B stored with N contiguous (transB == 0)
+  int tile_n;            // 128 or 256
+  int64_t M, N, K;
+  const void* A;         // base of the (possibly re-packed) operand
+  int64_t lda;           // elements
+  const void* B;
+  int64_t ldb;
+  float* C;
+  int64_t ldc;
+  float alpha, beta;
+  int splits;            // slices of K; > 1 writes partials to ws
+  int kb_per_split;      // k blocks per slice
+  float* ws;
+  int64_t ws_ld;
+  int* status;           // device status word
+  int grid;              // persistent CTAs
+  int group_m;           // raster group height in M tiles
+};
+int tc_tile_k(int mode);              // k elements per stage (128 bytes)
+int tc_stages(int mode, int tile_n);  // pipeline depth
+cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream);
+cudaError_t tc_init_driver();         // resolves cuTensorMapEncodeTiled once
+
+// ---------------------------------------------------------------- helpers
+// C = alpha * sum_s ws[s] + beta * C over an M x N matrix (s ascending).
+cudaError_t launch_splitk_reduce(int64_t M, int64_t N, int splits, const float* ws, int64_t ws_ld,
+                                 float* C, int64_t ldc, float alpha, float beta, cudaStream_t stream);
+// C = beta * C (beta == 0 writes zeros without reading C).
+cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta, cudaStream_t stream);
+// Copy a rows x cols matrix of elem_bytes-sized elements to dst with a new
+// leading dimension (elements).
+cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
+                        int elem_bytes, cudaStream_t stream);
+
+}  // namespace dgt

@@ -1,0 +1,97 @@
+// tc.cu -- tensor-map encoding and launch of the tcgen05 kernel.
+//
+// The TMA descriptors are encoded on the host with cuTensorMapEncodeTiled,
+// obtained through the runtime's driver entry-point query so that the library
+// needs no link-time dependency on the driver library.  Operand boxes are 128
+// bytes wide along the contiguous dimension with the 128-byte swizzle, the
+// layout the shared-memory descriptors of the kernel expect:
+//   K-major operand (K contiguous):   box {BK, rows}    one box per stage
+//   MN-major operand (M/N contiguous): box {CH, BK}     rows/CH boxes per stage
+// Out-of-range rows and columns of a box are filled with zeros by the TMA unit.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tc_launch.cuh"
+
+namespace dgt {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_status = cudaSuccess;
+
+cudaError_t encode_2d(CUtensorMap* m, int mode, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
+                      uint32_t box_inner, uint32_t box_outer) {
+  const int es = (mode == 2) ? 2 : 4;
+  const CUtensorMapDataType dt = (mode == 2) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t tc_init_driver() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      g_encode_status = (e != cudaSuccess) ? e : cudaErrorNotSupported;
+      return;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode_status;
+}
+
+int tc_tile_k(int mode) { return mode == 2 ? 64 : 32; }
+
+int tc_stages(int mode, int tile_n) {
+  (void)mode;
+  return tile_n == 256 ? TcCfg<2, 256>::STAGES : TcCfg<2, 128>::STAGES;
+}
+
+cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
+  cudaError_t e = tc_init_driver();
+  if (e != cudaSuccess) return e;
+  const int bk = tc_tile_k(a.mode);
+  const int ch = (a.mode == 2) ? 64 : 32;  // elements in a 128-byte MN-major row
+  CUtensorMap ta, tb;
+  e = a.a_mn_major ? encode_2d(&ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
+                   : encode_2d(&ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
+  if (e != cudaSuccess) return e;
+  e = a.b_mn_major ? encode_2d(&tb, a.mode, a.B, a.N, a.K, a.ldb, ch, bk)
+                   : encode_2d(&tb, a.mode, a.B, a.K, a.N, a.ldb, bk, a.tile_n);
+  if (e != cudaSuccess) return e;
+
+  TcParams p;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.num_tm = static_cast<int>((a.M + 127) / 128);
+  p.num_tn = static_cast<int>((a.N + a.tile_n - 1) / a.tile_n);
+  p.num_kb = static_cast<int>((a.K + bk - 1) / bk);
+  p.splits = a.splits;
+  p.kb_per_split = a.kb_per_split;
+  p.num_units = p.num_tm * p.num_tn * a.splits;
+  p.group_m = a.group_m;
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.ws = a.ws;
+  p.ws_ld = a.ws_ld;
+  p.status = a.status;
+  p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
+  if (a.mode == 2) return tc_launch_bf16(a.tile_n, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, p, a.grid, stream);
+  return tc_launch_tf32(a.tile_n, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, p, a.grid, stream);
+}
+
+}  // namespace dgt

@@ -1,0 +1,345 @@
+// tc_kernel.cuh -- the persistent TMA + tcgen05 GEMM kernel (TF32 and BF16).
+//
+// "bare-metal-bard" (first paragraph) ends its ladder with a tensor-core
+// kernel in TF32.  On this part the tensor cores are driven by tcgen05: one
+// thread issues asynchronous 128 x N x K MMAs whose operands are read from
+// shared memory through descriptors and whose fp32 accumulator lives in TMEM.
+// The kernel is organised around that:
+//
+//   warp 0      TMA producer: fills a ring of shared-memory stages (one A box
+//               of 128 rows and one B box of tile_n rows, 128-byte swizzled,
+//               128 bytes of K per row) and arms each stage's "full" mbarrier
+//               with the bytes it expects;
+//   warp 1      allocates TMEM (two accumulators of tile_n fp32 columns), then
+//               one lane issues the MMAs of a stage and commits them to the
+//               stage's "empty" mbarrier, and commits a finished tile to its
+//               accumulator's "full" mbarrier;
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4)..+31, i.e. those rows of the tile), the fused
+//               alpha/beta update, and the stores; then they release the
+//               accumulator so the next tile's MMAs can start.  Two
+//               accumulators let the epilogue of tile i overlap the mainloop
+//               of tile i+1.
+//
+// Work units are (tile, K slice) pairs handed out round-robin to a persistent
+// grid of one CTA per SM, in a grouped raster order (group_m tiles of M walk
+// all tiles of N) so that CTAs running at the same time share A and B tiles
+// in L2.  With more than one K slice, each unit writes raw partial sums to the
+// workspace and a separate kernel reduces the slices in a fixed order.
+//
+// Every mbarrier wait is bounded (ptx.cuh); on a timeout the CTA records the
+// cause in the device status word, waits (bounded) for its own copies and
+// MMAs in flight, frees its TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dgt {
+
+struct TcParams {
+  int M, N, K;
+  int num_tm, num_tn, num_kb;
+  int splits, kb_per_split, num_units, group_m;
+  float alpha, beta;
+  float* C;
+  int64_t ldc;
+  float* ws;
+  int64_t ws_ld;
+  int* status;
+  int c_vec;  // C rows are 16-byte aligned (ldc % 4 == 0 and C aligned)
+};
+
+// MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands).
+template <int MODE, int BN>
+struct TcCfg {
+  static constexpr int ES = (MODE == 2) ? 2 : 4;      // operand bytes
+  static constexpr int BM = 128;                      // rows of the tile (UMMA M)
+  static constexpr int BK = 128 / ES;                 // K elements per stage: one 128-byte swizzle row
+  static constexpr int UK = (MODE == 2) ? 16 : 8;     // K of one MMA instruction (32 bytes)
+  static constexpr int CH = 128 / ES;                 // M/N elements of one 128-byte MN-major row
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;  // 192 KB of operand stages
+  static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
+  static constexpr int NUM_BARS = 2 * STAGES + 5;     // full/empty per stage, acc full/empty x2, drain
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr uint32_t FORMAT = (MODE == 2) ? 1u : 2u;  // bf16 / tf32 in the instruction descriptor
+  static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
+};
+
+template <int MODE>
+__device__ __forceinline__ void issue_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if (MODE == 2)
+    mma_bf16(d, a, b, idesc, acc);
+  else
+    mma_tf32(d, a, b, idesc, acc);
+}
+
+struct Unit {
+  int tm, tn, split, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
+  Unit w;
+  const int tiles = p.num_tm * p.num_tn;
+  const int t = u % tiles;
+  w.split = u / tiles;
+  const int span = p.group_m * p.num_tn;
+  const int g = t / span;
+  const int first_m = g * p.group_m;
+  const int rem = p.num_tm - first_m;
+  const int gm = rem < p.group_m ? rem : p.group_m;
+  const int r = t % span;
+  w.tm = first_m + r % gm;
+  w.tn = r / gm;
+  w.kb0 = w.split * p.kb_per_split;
+  const int e = w.kb0 + p.kb_per_split;
+  w.kb1 = e < p.num_kb ? e : p.num_kb;
+  return w;
+}
+
+// Bounded wait used only on the abort path: it ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicExch(status, kDevTimeoutDrain);
+      return;
+    }
+  }
+}
+
+template <int MODE, bool A_MN, bool B_MN, int BN>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const TcParams p) {
+  using Cfg = TcCfg<MODE, BN>;
+  constexpr int S = Cfg::STAGES;
+  constexpr uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN, B_MN, Cfg::BM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t smem0 = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto accf_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(u, p);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, kDevTimeoutEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+          const uint32_t a_dst = smem0 + stage * Cfg::STAGE_BYTES;
+          const uint32_t b_dst = a_dst + Cfg::A_BYTES;
+          const int k0 = kb * Cfg::BK;
+          if (A_MN) {
+#pragma unroll
+            for (int c = 0; c < Cfg::BM / Cfg::CH; ++c)
+              tma_load_2d(a_dst + c * Cfg::BK * 128, &tmA, fb, w.tm * Cfg::BM + c * Cfg::CH, k0);
+          } else {
+            tma_load_2d(a_dst, &tmA, fb, k0, w.tm * Cfg::BM);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int c = 0; c < BN / Cfg::CH; ++c)
+              tma_load_2d(b_dst + c * Cfg::BK * 128, &tmB, fb, w.tn * BN + c * Cfg::CH, k0);
+          } else {
+            tma_load_2d(b_dst, &tmB, fb, k0, w.tn * BN);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Wait for every copy still in flight before the CTA can exit.
+        const uint32_t n = issued < static_cast<uint32_t>(S) ? issued : static_cast<uint32_t>(S);
+        for (uint32_t i = issued - n; i < issued; ++i) drain_wait(full_bar(i % S), (i / S) & 1u, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit(u, p);
+        if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem0 + stage * Cfg::STAGE_BYTES;
+          const uint32_t b_base = a_base + Cfg::A_BYTES;
+#pragma unroll
+          for (int j = 0; j < Cfg::BK / Cfg::UK; ++j) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(a_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
+                                     : smem_desc_sw128(a_base + j * Cfg::UK * Cfg::ES, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(b_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
+                                     : smem_desc_sw128(b_base + j * Cfg::UK * Cfg::ES, 16, 1024);
+            issue_mma<MODE>(d_tmem, ad, bd, IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit(empty_bar(stage));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(accf_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // Every MMA this thread issued has finished once drain_bar flips.
+      mma_commit(drain_bar);
+      drain_wait(drain_bar, 0, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int sub = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const bool partial = p.splits > 1;
+    const bool read_c = !partial && p.beta != 0.f;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+      const Unit w = decode_unit(u, p);
+      if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull)) break;
+      tc_fence_after();
+      const int64_t row = static_cast<int64_t>(w.tm) * Cfg::BM + sub * 32 + lane;
+      const bool row_ok = row < p.M;
+      float* out = partial ? p.ws + (static_cast<int64_t>(w.split) * p.M + (row_ok ? row : 0)) * p.ws_ld
+                           : p.C + (row_ok ? row : 0) * p.ldc;
+      const bool vec_ok = partial || p.c_vec;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(t_row + cc * 32, r);
+        tmem_wait_ld();
+        const int64_t col0 = static_cast<int64_t>(w.tn) * BN + cc * 32;
+        if (!row_ok || col0 >= p.N) {
+          // nothing of this 32-column chunk is inside C for this thread
+        } else if (vec_ok && col0 + 32 <= p.N) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 v;
+            v.x = __uint_as_float(r[4 * q + 0]);
+            v.y = __uint_as_float(r[4 * q + 1]);
+            v.z = __uint_as_float(r[4 * q + 2]);
+            v.w = __uint_as_float(r[4 * q + 3]);
+            float4* dst = reinterpret_cast<float4*>(out + col0 + 4 * q);
+            if (!partial) {
+              v.x *= p.alpha;
+              v.y *= p.alpha;
+              v.z *= p.alpha;
+              v.w *= p.alpha;
+              if (read_c) {
+                const float4 c = *dst;
+                v.x = fmaf(p.beta, c.x, v.x);
+                v.y = fmaf(p.beta, c.y, v.y);
+                v.z = fmaf(p.beta, c.z, v.z);
+                v.w = fmaf(p.beta, c.w, v.w);
+              }
+            }
+            *dst = v;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t col = col0 + j;
+            if (col < p.N) {
+              float v = __uint_as_float(r[j]);
+              if (!partial) {
+                v *= p.alpha;
+                if (read_c) v = fmaf(p.beta, out[col], v);
+              }
+              out[col] = v;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace dgt

@@ -1,0 +1,43 @@
+// tc_launch.cuh -- host-side launch of the tcgen05 kernel for one operand mode
+// (included once by each of tc_tf32.cu and tc_bf16.cu so the two modes
+// compile in parallel).
+#pragma once
+
+#include "tc_kernel.cuh"
+
+namespace dgt {
+
+template <int MODE, bool A_MN, bool B_MN, int BN>
+cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p, int grid,
+                          cudaStream_t s) {
+  using Cfg = TcCfg<MODE, BN>;
+  auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 192, Cfg::SMEM_BYTES, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+template <int MODE, int BN>
+cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
+                         int grid, cudaStream_t s) {
+  if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN>(ta, tb, p, grid, s);
+  if (!a_mn && b_mn) return tc_launch_one<MODE, false, true, BN>(ta, tb, p, grid, s);
+  if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN>(ta, tb, p, grid, s);
+  return tc_launch_one<MODE, true, true, BN>(ta, tb, p, grid, s);
+}
+
+template <int MODE>
+cudaError_t tc_launch_mode(int tile_n, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const TcParams& p, int grid, cudaStream_t s) {
+  if (tile_n == 256) return tc_launch_bn<MODE, 256>(a_mn, b_mn, ta, tb, p, grid, s);
+  return tc_launch_bn<MODE, 128>(a_mn, b_mn, ta, tb, p, grid, s);
+}
+
+// Defined in tc_tf32.cu (MODE 1) and tc_bf16.cu (MODE 2).
+cudaError_t tc_launch_tf32(int tile_n, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const TcParams& p, int grid, cudaStream_t s);
+cudaError_t tc_launch_bf16(int tile_n, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const TcParams& p, int grid, cudaStream_t s);
+
+}  // namespace dgt

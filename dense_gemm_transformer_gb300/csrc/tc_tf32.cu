@@ -1,0 +1,9 @@
+// tc_tf32.cu -- instantiations of the tcgen05 kernel for TF32 operands (kind::tf32).
+#include "tc_launch.cuh"
+
+namespace dgt {
+cudaError_t tc_launch_tf32(int tile_n, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+                           const TcParams& p, int grid, cudaStream_t s) {
+  return tc_launch_mode<1>(tile_n, a_mn, b_mn, ta, tb, p, grid, s);
+}
+}  // namespace dgt

@@ -1,0 +1,138 @@
+/*
+ * gemm.h -- C ABI of the GB300 dense GEMM library (libgemm.so).
+ *
+ * The operation is the dense matrix multiply that "bare-metal-bard"
+ * (ethanyanxu.com) builds as a ladder of kernels and uses for every projection
+ * of a small GPT (first and second paragraphs), in its BLAS form
+ *
+ *     C = alpha * op(A) * op(B) + beta * C
+ *
+ * computed in one of three modes: exact FP32 on the CUDA cores, TF32 on the
+ * tensor cores (the mode the page's tensor-core kernel uses, first paragraph),
+ * or BF16 inputs on the tensor cores.  Every mode accumulates in FP32 and
+ * writes FP32.
+ *
+ * Layout (all matrices row-major, element (r, c) at base[r * ld + c]):
+ *   op(A) is M x K.  transA == 0: A is stored M x K, lda >= max(K, 1).
+ *                    transA == 1: A is stored K x M, lda >= max(M, 1).
+ *   op(B) is K x N.  transB == 0: B is stored K x N, ldb >= max(N, 1).
+ *                    transB == 1: B is stored N x K, ldb >= max(K, 1).
+ *   C is M x N float, ldc >= max(N, 1).
+ *   A and B are float in GEMM_MODE_FP32 and GEMM_MODE_TF32 and bfloat16
+ *   (raw 16-bit patterns) in GEMM_MODE_BF16.  In TF32 mode the fp32 operands
+ *   are passed to the tensor cores unchanged; the hardware drops their 13 low
+ *   mantissa bits.
+ *
+ * Ownership: the caller owns A, B and C, which are device memory.  A handle
+ * owns its device properties, a device status word and a scratch workspace
+ * (split-K partial sums and re-packed operands) that grows on demand and is
+ * freed by gemm_destroy.  A handle is bound to the device that was current at
+ * gemm_create and must not be used from two streams at the same time.
+ *
+ * Errors: every call returns a status and never throws.  Arguments are checked
+ * before anything is launched; a failed check launches nothing and leaves C
+ * untouched.  Launch failures are reported as GEMM_ERR_CUDA.  There is no
+ * fallback to the CPU or to another library.
+ */
+#ifndef DENSE_GEMM_GB300_GEMM_H
+#define DENSE_GEMM_GB300_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_handle_s* gemm_handle_t;
+
+typedef enum {
+  GEMM_MODE_FP32 = 0, /* fp32 operands, FFMA on CUDA cores, exact fp32 products */
+  GEMM_MODE_TF32 = 1, /* fp32 operands, tcgen05 kind::tf32, fp32 accumulate   */
+  GEMM_MODE_BF16 = 2  /* bf16 operands, tcgen05 kind::f16, fp32 accumulate    */
+} gemm_mode_t;
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_VALUE = 1, /* null handle/pointer, bad mode or flag, negative size, ld too small */
+  GEMM_ERR_NOT_SUPPORTED = 2, /* device is not sm_103 / sm_100 class, or option not available     */
+  GEMM_ERR_MISALIGNED = 3,    /* a pointer is not aligned to its element size                        */
+  GEMM_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed                                */
+  GEMM_ERR_ALLOC = 5,         /* device memory for the handle's workspace could not be allocated    */
+  GEMM_ERR_DEVICE_TIMEOUT = 6 /* a kernel gave up a bounded wait and set the device status word      */
+} gemm_status_t;
+
+/* Kernel families the planner chooses among (gemm_set_option/GEMM_OPT_FAMILY). */
+typedef enum {
+  GEMM_FAMILY_AUTO = 0,
+  GEMM_FAMILY_SIMT = 1,   /* register-tiled FFMA kernel (GEMM_MODE_FP32 only)           */
+  GEMM_FAMILY_TC = 2,     /* persistent TMA + tcgen05 kernel, 1 CTA per tile (TF32/BF16) */
+  GEMM_FAMILY_SKINNY = 3  /* HBM-bound small-M kernel (BF16)                             */
+} gemm_family_t;
+
+typedef enum {
+  GEMM_OPT_FAMILY = 1,   /* value: gemm_family_t; AUTO lets the planner choose            */
+  GEMM_OPT_SPLIT_K = 2,  /* value: 0 = planner's choice, n >= 1 = force n slices of K      */
+  GEMM_OPT_TILE_N = 3    /* value: 0 = planner's choice, 128 or 256 for the TC family       */
+} gemm_option_t;
+
+/* What the last successful gemm_run on a handle launched. */
+typedef struct {
+  int32_t family;        /* gemm_family_t actually used (0 when nothing was launched) */
+  int32_t tile_m, tile_n, tile_k;
+  int32_t split_k;       /* slices of K (1 = no split) */
+  int32_t stages;        /* shared-memory pipeline depth */
+  int32_t grid;          /* CTAs of the main kernel */
+  int32_t kernels;       /* kernels launched by the call */
+  int32_t packed;        /* bit 0: A re-packed, bit 1: B re-packed into the workspace */
+  int32_t reserved[7];
+} gemm_plan_t;
+
+/* Create a handle on the current device.  Reads the device properties and
+ * allocates the 4-byte device status word.  *out is set to NULL on failure. */
+gemm_status_t gemm_create(gemm_handle_t* out);
+
+/* Free the handle, its status word and its workspace.  Synchronizes the
+ * device first so that no launched kernel still uses the workspace.
+ * A NULL handle is GEMM_ERR_INVALID_VALUE. */
+gemm_status_t gemm_destroy(gemm_handle_t h);
+
+/* C = alpha * op(A) * op(B) + beta * C on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream).  Asynchronous: returns once the kernels are
+ * enqueued.  M == 0 or N == 0 is a no-op.  K == 0 or alpha == 0 gives
+ * C = beta * C without reading A or B.  beta == 0 writes C without reading it
+ * (a NaN in C does not propagate).  C must not overlap A or B.  The workspace
+ * may grow (cudaMalloc) on the first call that needs a larger one. */
+gemm_status_t gemm_run(gemm_handle_t h, int mode, int transA, int transB,
+                       int64_t M, int64_t N, int64_t K, float alpha,
+                       const void* A, int64_t lda, const void* B, int64_t ldb,
+                       float beta, float* C, int64_t ldc, void* stream);
+
+/* The argument checks gemm_run performs, without a handle or a device.
+ * Returns GEMM_OK or the status gemm_run would return for these arguments
+ * (A and B are checked only when K > 0 and alpha != 0, since only then are
+ * they read). */
+gemm_status_t gemm_validate(int mode, int transA, int transB,
+                            int64_t M, int64_t N, int64_t K, float alpha,
+                            const void* A, int64_t lda, const void* B, int64_t ldb,
+                            const float* C, int64_t ldc);
+
+/* Set a planner option (gemm_option_t) for later calls on this handle. */
+gemm_status_t gemm_set_option(gemm_handle_t h, int option, int64_t value);
+
+/* Copy the plan of the last successful gemm_run into *out. */
+gemm_status_t gemm_get_plan(gemm_handle_t h, gemm_plan_t* out);
+
+/* Synchronize `stream`, then read and clear the handle's device status word.
+ * Returns GEMM_ERR_DEVICE_TIMEOUT if a kernel abandoned a bounded wait since
+ * the last check (its output is then undefined), GEMM_ERR_CUDA if the stream
+ * reports an error, GEMM_OK otherwise. */
+gemm_status_t gemm_check_device(gemm_handle_t h, void* stream);
+
+/* A static string naming a status code. */
+const char* gemm_status_string(gemm_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_GEMM_GB300_GEMM_H */

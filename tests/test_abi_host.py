@@ -1,0 +1,105 @@
+"""The C ABI on the host: symbols, argument checks, status strings, and the
+register/spill guard of the built kernels.  No GPU and no kernel launch."""
+import ctypes
+import re
+
+import pytest
+
+import dense_gemm_transformer_gb300 as dg
+from dense_gemm_transformer_gb300 import _build
+
+OK, INVALID, NOT_SUPPORTED, MISALIGNED = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return dg.load(build_if_missing=True)
+
+
+def test_library_exports_every_declared_function(lib):
+    names = dg.header_functions()
+    assert {"gemm_create", "gemm_run", "gemm_destroy", "gemm_status_string"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in dg.STATUS.items():
+        assert dg.status_string(code) == name
+    assert dg.status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+P = 0x10000  # a 64 KiB-aligned fake device address: never dereferenced by the checks
+
+
+def v(mode="fp32", tA=0, tB=0, M=8, N=8, K=8, alpha=1.0, A=P, lda=None, B=P, ldb=None, C=P, ldc=None):
+    lda = lda if lda is not None else (M if tA else K)
+    ldb = ldb if ldb is not None else (K if tB else N)
+    ldc = ldc if ldc is not None else N
+    return dg.validate(mode, tA, tB, M, N, K, alpha, A, lda, B, ldb, C, ldc)
+
+
+def test_validate_accepts_good_arguments(lib):
+    for mode in ("fp32", "tf32", "bf16"):
+        for tA in (0, 1):
+            for tB in (0, 1):
+                assert v(mode, tA, tB, M=33, N=17, K=5) == OK
+    assert v(M=4, N=3, K=2, lda=100, ldb=100, ldc=100) == OK
+
+
+def test_validate_rejects_bad_flags_and_sizes(lib):
+    assert dg.validate(3, 0, 0, 8, 8, 8, 1.0, P, 8, P, 8, P, 8) == INVALID
+    assert dg.validate(-1, 0, 0, 8, 8, 8, 1.0, P, 8, P, 8, P, 8) == INVALID
+    assert v(tA=2) == INVALID and v(tB=-1) == INVALID
+    assert v(M=-1) == INVALID and v(N=-5) == INVALID and v(K=-1) == INVALID
+    assert v(M=2**31) == INVALID
+
+
+def test_validate_leading_dimensions(lib):
+    assert v(M=8, K=16, lda=15) == INVALID            # A stored M x K needs lda >= K
+    assert v(tA=1, M=8, K=16, lda=7) == INVALID       # A stored K x M needs lda >= M
+    assert v(tA=1, M=8, K=16, lda=8) == OK
+    assert v(N=9, K=4, ldb=8) == INVALID              # B stored K x N needs ldb >= N
+    assert v(tB=1, N=9, K=4, ldb=3) == INVALID        # B stored N x K needs ldb >= K
+    assert v(N=9, ldc=8) == INVALID
+
+
+def test_validate_null_and_misaligned_pointers(lib):
+    assert v(A=None) == INVALID and v(B=None) == INVALID and v(C=None) == INVALID
+    assert v(mode="fp32", A=P + 2) == MISALIGNED
+    assert v(mode="bf16", A=P + 2) == OK              # bf16 needs 2-byte alignment only
+    assert v(mode="bf16", B=P + 1) == MISALIGNED
+    assert v(C=P + 2) == MISALIGNED
+
+
+def test_validate_degenerate_sizes(lib):
+    # M == 0 or N == 0: nothing is touched, nothing else is checked.
+    assert v(M=0, A=None, B=None, C=None) == OK
+    assert v(N=0, A=None, B=None, C=None) == OK
+    # K == 0 or alpha == 0: C = beta * C, A and B are never read.
+    assert v(K=0, A=None, B=None) == OK
+    assert v(alpha=0.0, A=None, B=None, lda=0, ldb=0) == OK
+    assert v(K=0, C=None) == INVALID
+
+
+def test_null_handle_is_rejected_everywhere(lib):
+    assert lib.gemm_run(None, 0, 0, 0, 8, 8, 8, 1.0, P, 8, P, 8, 0.0, P, 8, None) == INVALID
+    assert lib.gemm_destroy(None) == INVALID
+    assert lib.gemm_set_option(None, 1, 0) == INVALID
+    assert lib.gemm_get_plan(None, ctypes.byref(dg.Plan())) == INVALID
+    assert lib.gemm_check_device(None, None) == INVALID
+    assert lib.gemm_create(None) == INVALID
+
+
+def test_every_kernel_is_free_of_spills(lib):
+    """Spilling to local memory (or trading it for registers past an occupancy
+    step) is the silent regression "bare-metal-bard" describes in its fourth
+    paragraph; the build's ptxas report must show zero spill bytes."""
+    with open(_build.PTXAS_REPORT) as f:
+        text = f.read()
+    spills = re.findall(r"(\d+) bytes spill stores, (\d+) bytes spill loads", text)
+    assert spills, "ptxas report has no kernels"
+    assert all(s == "0" and l == "0" for s, l in spills), spills
+    regs = [int(r) for r in re.findall(r"Used (\d+) registers", text)]
+    # SIMT kernel: two 256-thread CTAs per SM need <= 128 registers per thread.
+    assert max(regs) <= 128, max(regs)

@@ -1,0 +1,235 @@
+"""Parity of the library's kernels with the CPU oracle, through the C ABI.
+
+Every mode and transpose combination, ragged shapes that span several tiles
+with a partial last tile, forced split-K and tile widths, unaligned leading
+dimensions, alpha/beta, the degenerate sizes, bit-exact small-integer inputs,
+and guard bands around C.  Tolerances (tests/_gate.py): 1e-6 FP32, 2e-3 TF32,
+8e-3 BF16 of |alpha| * sum|a||b| (+ |beta c|).
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_transformer_gb300 as dg
+import oracle
+import seeded_inputs as si
+from tests import _cases, _gate
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["fp32", "tf32", "bf16"]
+TRANS = [(False, False), (False, True), (True, False), (True, True)]
+
+
+@pytest.fixture(scope="module")
+def h():
+    dg.load(build_if_missing=True)
+    handle = dg.Gemm()
+    yield handle
+    handle.close()
+
+
+@pytest.fixture(autouse=True)
+def _reset(h):
+    h.set_option("family", "auto")
+    h.set_option("split_k", 0)
+    h.set_option("tile_n", 0)
+    yield
+
+
+# ------------------------------------------------------------ the 256^3 case
+@pytest.mark.parametrize("mode", MODES)
+def test_square256_uniform(h, mode):
+    _cases.run_and_check(h, mode, 256, 256, 256, seed=si.seed_for(0, 0, 0))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("tA,tB", TRANS)
+def test_square256_integers_bit_exact(h, mode, tA, tB):
+    _cases.run_and_check(h, mode, 256, 256, 256, tA, tB, seed=si.seed_for(0, 1, 0), dist="int", exact=True)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_integers_bit_exact_deep_k(h, mode):
+    # K = 1024 integers in [-4, 4]: every partial sum is an integer below 2^24.
+    _cases.run_and_check(h, mode, 300, 200, 1024, seed=7, dist="int", exact=True)
+    h.set_option("split_k", 3)
+    _cases.run_and_check(h, mode, 300, 200, 1024, seed=8, dist="int", exact=True)
+
+
+# ------------------------------------------------------------ shapes and layouts
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("tA,tB", TRANS)
+def test_ragged_all_layouts(h, mode, tA, tB):
+    _cases.run_and_check(h, mode, 300, 264, 200, tA, tB, seed=11, dist="normal")
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (7, 9, 5), (65, 65, 65), (127, 129, 33), (129, 127, 130),
+                                   (1, 300, 64), (300, 1, 64), (33, 520, 16), (520, 33, 17)])
+def test_edge_shapes(h, mode, M, N, K):
+    _cases.run_and_check(h, mode, M, N, K, False, False, seed=13, dist="normal")
+    _cases.run_and_check(h, mode, M, N, K, True, True, seed=14, dist="normal")
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("alpha,beta", [(0.5, 1.0), (-1.5, 0.25), (1.0, -1.0)])
+def test_alpha_beta(h, mode, alpha, beta):
+    _cases.run_and_check(h, mode, 260, 300, 96, alpha=alpha, beta=beta, seed=17, dist="normal")
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tA,tB", TRANS)
+def test_tc_tile_widths(h, mode, tile_n, tA, tB):
+    h.set_option("tile_n", tile_n)
+    _cases.run_and_check(h, mode, 384, 520, 160, tA, tB, seed=19, dist="normal")
+    assert h.plan()["family"] == "tc" and h.plan()["tile_n"] == tile_n
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("splits", [2, 5])
+def test_forced_split_k(h, mode, splits):
+    h.set_option("split_k", splits)
+    _cases.run_and_check(h, mode, 200, 272, 1000, False, True, alpha=0.75, beta=0.5, seed=23, dist="normal")
+    assert h.plan()["split_k"] == splits
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_many_tiles_persistent_loop(h, mode):
+    # More tiles than SMs: every CTA of the persistent grid loops over several
+    # tiles and both TMEM accumulators are reused.
+    _cases.run_and_check(h, mode, 2048 + 64, 2048 + 40, 256, seed=29, dist="normal", rows=_cases.sample_rows(2112))
+
+
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+@pytest.mark.parametrize("tA,tB", TRANS)
+def test_unaligned_leading_dimension(h, mode, tA, tB):
+    # N = K = 65: a row of 65 elements breaks the 16-byte rule of the TMA unit,
+    # so TF32/BF16 operands go through the re-pack into the workspace.
+    _cases.run_and_check(h, mode, 190, 65, 65, tA, tB, seed=31, dist="normal")
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_padded_leading_dimensions_and_offsets(h, mode):
+    M, N, K = 150, 90, 70
+    ops, _ = _cases.make(mode, M, N, K, seed=37, dist="normal")
+    dt = ops.A.dtype
+    # operands inside larger buffers, starting one element in
+    Abig = torch.zeros((M, K + 9), dtype=dt, device="cuda")
+    Bbig = torch.zeros((K, N + 5), dtype=dt, device="cuda")
+    Abig[:, 1:K + 1] = ops.A
+    Bbig[:, 3:N + 3] = ops.B
+    Cbig = torch.full((M + 2, N + 11), 7.0, device="cuda")
+    A, B, C = Abig[:, 1:K + 1], Bbig[:, 3:N + 3], Cbig[1:M + 1, 2:N + 2]
+    h.run(A, B, C, mode=mode)
+    assert h.check_device() == 0
+    ref, D = oracle.gemm(mode, ops.a_host, ops.b_host)
+    _gate.assert_within(mode, C.cpu().numpy(), ref, D)
+    host = Cbig.cpu().numpy()
+    mask = np.ones_like(host, dtype=bool)
+    mask[1:M + 1, 2:N + 2] = False
+    assert np.all(host[mask] == 7.0), "wrote outside C"
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_guard_bands_untouched(h, mode):
+    """C sits inside a buffer whose every other element is a NaN canary."""
+    M, N, K = 257, 130, 48
+    ops, _ = _cases.make(mode, M, N, K, seed=41, dist="normal")
+    canary = float("nan")
+    buf = torch.full((M + 4) * (N + 8) + 64, canary, device="cuda")
+    C = buf[32:32 + (M + 4) * (N + 8)].view(M + 4, N + 8)[2:M + 2, 4:N + 4]
+    h.run(ops.A, ops.B, C, mode=mode)
+    assert h.check_device() == 0
+    ref, D = oracle.gemm(mode, ops.a_host, ops.b_host)
+    _gate.assert_within(mode, C.cpu().numpy(), ref, D)
+    host = buf.cpu().numpy()
+    inside = np.zeros(host.shape, dtype=bool)
+    idx = 32 + (np.arange(2, M + 2)[:, None] * (N + 8) + np.arange(4, N + 4)[None, :])
+    inside[idx.ravel()] = True
+    assert np.all(np.isnan(host[~inside])), "a canary was overwritten"
+
+
+# ------------------------------------------------------------ degenerate calls
+@pytest.mark.parametrize("mode", MODES)
+def test_k_zero_and_alpha_zero(h, mode):
+    M, N = 70, 50
+    c0 = si.normal((M, N), 43)
+    dt = torch.bfloat16 if mode == "bf16" else torch.float32
+    C = c0.clone().cuda()
+    h.run(torch.empty((M, 0), dtype=dt, device="cuda"), torch.empty((0, N), dtype=dt, device="cuda"), C,
+          mode=mode, beta=-2.0)
+    assert torch.equal(C.cpu(), -2.0 * c0)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    A = torch.full((M, 8), float("nan"), device="cuda").to(dt)
+    B = torch.ones((8, N), device="cuda").to(dt)
+    h.run(A, B, C, mode=mode, alpha=0.0, beta=0.0)
+    assert torch.equal(C.cpu(), torch.zeros(M, N))
+
+
+def test_empty_output_is_a_no_op(h):
+    C = torch.empty((0, 5), device="cuda")
+    h.run(torch.empty((0, 3), device="cuda"), torch.empty((3, 5), device="cuda"), C)
+    assert h.plan()["kernels"] == 0
+
+
+def test_beta_zero_ignores_nan_in_c(h):
+    for mode in MODES:
+        _cases.run_and_check(h, mode, 140, 150, 40, beta=0.0, seed=47)  # C starts as NaN
+
+
+def test_bad_arguments_launch_nothing(h):
+    C = torch.full((4, 4), 3.0, device="cuda")
+    A = torch.ones((4, 4), device="cuda")
+    with pytest.raises(dg.GemmError) as e:
+        h.run_ptr("fp32", 0, 0, 4, 4, 4, 1.0, A.data_ptr(), 3, A.data_ptr(), 4, 0.0, C.data_ptr(), 4)
+    assert e.value.status == 1
+    assert torch.equal(C.cpu(), torch.full((4, 4), 3.0))
+    with pytest.raises(dg.GemmError):
+        h.set_option("family", "tc")
+        h.run(A, A, C, mode="fp32")  # the FP32 mode has no tensor-core family
+    assert torch.equal(C.cpu(), torch.full((4, 4), 3.0))
+
+
+# ------------------------------------------------------------ TF32 operand rule
+def test_tf32_operand_reduction_matches_oracle_reading():
+    """A one-column probe: C[i] = a_i * 1 for a_i = 1 + i * 2^-12 .. shows
+    whether the tensor cores drop or round the 13 low mantissa bits."""
+    dg.load(build_if_missing=True)
+    h = dg.Gemm()
+    M = 64
+    a = torch.tensor([1.0 + i * 2.0 ** -12 for i in range(M)], dtype=torch.float32).reshape(M, 1)
+    a = torch.cat([a, -a[: M // 2]], 0)
+    b = torch.ones((1, 16), dtype=torch.float32)
+    C = torch.zeros((a.shape[0], 16), device="cuda")
+    h.run(a.cuda(), b.cuda(), C, mode="tf32")
+    got = C.cpu().numpy()[:, 0]
+    want = oracle.tf32(a.numpy()[:, 0])          # the oracle's reading (truncation)
+    other = oracle.tf32(a.numpy()[:, 0], "nearest_away")
+    h.close()
+    assert np.array_equal(got, want), (got[:8], want[:8], other[:8])
+
+
+# ------------------------------------------------------------ the GPT shapes, full size
+@pytest.mark.parametrize("mode", ["fp32", "tf32"])
+@pytest.mark.parametrize("proj", range(len(si.GPT_PROJECTIONS)))
+def test_gpt_projection_shapes_sampled(h, mode, proj):
+    """Full-size forward, dX and dW of one projection in the launch
+    configuration the benchmark uses; sampled rows against the oracle."""
+    name, kin, nout = si.GPT_PROJECTIONS[proj]
+    X, W, dY = si.gpt_tensors(proj, kin, nout)
+    Xd, Wd, dYd = X.cuda(), W.cuda(), dY.cuda()
+    T = si.GPT_TOKENS
+    cases = [("fwd", Xd, Wd, X, W, False, False, T, nout, kin),
+             ("dX", dYd, Wd, dY, W, False, True, T, kin, nout),
+             ("dW", Xd, dYd, X, dY, True, False, kin, nout, T)]
+    for tag, Ad, Bd, Ah, Bh, tA, tB, M, N, K in cases:
+        C = torch.full((M, N), float("nan"), device="cuda")
+        h.run(Ad, Bd, C, mode=mode, transA=tA, transB=tB)
+        assert h.check_device() == 0
+        got = C.cpu().numpy()
+        width = 1 if K > 4096 else 2
+        for r0, r1 in _cases.sample_rows(M, width=width):
+            ref, D = oracle.gemm(mode, Ah.numpy(), Bh.numpy(), transA=tA, transB=tB, rows=(r0, r1))
+            _gate.assert_within(mode, got[r0:r1], ref, D, what=f"{name}.{tag} rows {r0}:{r1}")
