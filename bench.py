@@ -255,6 +255,11 @@ def bench_ours(args, world, rank, local):
     h = dg.Gemm()
     stream = torch.cuda.Stream(dev)
     calls, host_inputs, dev_inputs = gpt_workload(dev)
+    if args.only:
+        import re
+        calls = [c for c in calls if re.fullmatch(args.only, c.name)]
+        if not calls:
+            raise SystemExit(f"--only {args.only!r} matches no GEMM of the step")
     step_flops = sum(c.case.flops for c in calls)
     pk = peaks()
 
@@ -312,7 +317,8 @@ def bench_ours(args, world, rank, local):
                        "roofline_frac": round(t_roof / (ms * 1e-3), 3)})
 
     # Dominant kernel family = the mode with the larger share of the step.
-    fam_ms = {m: sum(ms for c, ms in zip(calls, per_call_ms) if c.mode == m) for m in ("fp32", "tf32")}
+    fam_ms = {m: sum(ms for c, ms in zip(calls, per_call_ms) if c.mode == m) for m in ("fp32", "tf32")
+              if any(c.mode == m for c in calls)}
     dom = max(fam_ms, key=fam_ms.get)
     dom_flops = sum(c.case.flops for c in calls if c.mode == dom)
     n_launch = sum(1 for c in calls if c.mode == dom)
@@ -383,6 +389,112 @@ def bench_ours(args, world, rank, local):
     h.close()
 
 
+def sweep_cases(workload):
+    """(label, mode, case, alpha, beta, weight_std) of a per-shape sweep."""
+    out = []
+    if workload == "square":
+        for n in si.SQUARE_SWEEP:
+            for mode in ("fp32", "tf32", "bf16"):
+                for alpha, beta in ((1.0, 0.0), (0.5, 1.0)):
+                    out.append((f"{mode}.square{n}.a{alpha}b{beta}", mode, si.square_case(n), alpha, beta, 1.0))
+    elif workload == "large":
+        for M, N, K in si.LARGE_BF16:
+            out.append((f"bf16.{M}x{N}x{K}", "bf16", si.GemmCase(f"{M}x{N}x{K}", False, False, M, N, K),
+                        1.0, 0.0, 1.0))
+    elif workload == "skinny":
+        for tB in (False, True):
+            for c in si.skinny_cases():
+                case = si.GemmCase(c.name + (".T" if tB else ""), False, tB, c.M, c.N, c.K)
+                out.append((f"bf16.{case.name}", "bf16", case, 1.0, 0.0, 0.02))
+    return out
+
+
+def bench_sweep(args):
+    """Per-shape TFLOP/s and roofline fractions for the other configurations.
+
+    Each shape: warm-up, then R back-to-back launches between two CUDA events
+    on the launching stream, with the operands rotated over enough copies that
+    the working set of one rotation exceeds 3x the L2 (so every launch reads
+    its weights from HBM).  Skinny shapes are also timed as a CUDA graph of
+    the R launches, which removes the host launch gaps.
+    """
+    import dense_gemm_transformer_gb300 as dg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dg.load(build_if_missing=True)
+    h = dg.Gemm()
+    stream = torch.cuda.Stream(dev)
+    pk = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    shapes = []
+    for label, mode, c, alpha, beta, wstd in sweep_cases(args.workload):
+        dt = torch.bfloat16 if mode == "bf16" else torch.float32
+        es = 2 if mode == "bf16" else 4
+        per_set = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N
+        copies = max(1, min(32, -(-3 * l2 // per_set)))
+        g = torch.Generator(device="cpu")
+        g.manual_seed(si.BASE_SEED)
+        A0 = torch.randn(c.a_shape, generator=g).to(dt).to(dev)
+        B0 = (torch.randn(c.b_shape, generator=g) * wstd).to(dt).to(dev)
+        sets = []
+        for i in range(copies):
+            A = A0 if i == 0 else A0.clone()
+            B = B0 if i == 0 else B0.clone()
+            C = torch.randn((c.M, c.N), generator=g).to(dev)
+            sets.append((A, B, C))
+        reps = max(3 * copies, 10)
+        with torch.cuda.stream(stream):
+            for A, B, C in sets:
+                h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta, stream=stream)
+        stream.synchronize()
+        plan = h.plan()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for r in range(reps):
+                A, B, C = sets[r % copies]
+                h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta, stream=stream)
+            e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        graph_ms = None
+        if args.workload == "skinny":
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for r in range(reps):
+                    A, B, C = sets[r % copies]
+                    h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta,
+                          stream=stream)
+            graph.replay()
+            stream.synchronize()
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+            stream.synchronize()
+            graph_ms = e0.elapsed_time(e1) / reps
+        assert h.check_device(stream) == 0
+        t = graph_ms if graph_ms is not None else ms
+        byts = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N * (2 if beta != 0 else 1)
+        peak = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops"], "bf16": pk["bf16_tflops"]}[mode]
+        t_c, t_m = c.flops / (peak * 1e12), byts / (pk["hbm_gbs"] * 1e9)
+        shapes.append({"gemm": label, "M": c.M, "N": c.N, "K": c.K, "ms": round(t, 5),
+                       "ms_stream": round(ms, 5), "tflops": round(c.flops / (t * 1e-3) / 1e12, 2),
+                       "gbs": round(byts / (t * 1e-3) / 1e9, 1), "bound": "hbm" if t_m > t_c else
+                       ("alu" if mode == "fp32" else "tensor"), "roofline_frac": round(max(t_c, t_m) / (t * 1e-3), 3),
+                       "plan": plan, "copies": copies})
+        del sets, A0, B0
+        torch.cuda.empty_cache()
+    total_flops = sum(2 * x["M"] * x["N"] * x["K"] for x in shapes)
+    total_s = sum(x["ms"] for x in shapes) * 1e-3
+    line = {"metric": METRIC, "value": total_flops / total_s / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+            "higher_is_better": True, "dtype": "see shapes", "data": "synthetic",
+            "config": {"workload": args.workload, "l2": "operands rotated over copies > 3x L2"},
+            "shapes": shapes, "peaks": pk}
+    print(json.dumps(line), flush=True)
+    h.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -393,12 +505,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-macs", type=float, default=3e9, help="oracle multiply-adds in the CPU baseline")
     ap.add_argument("--ref-macs", type=float, default=3e8, help="oracle multiply-adds per reference step")
+    ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
+    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny"],
+                    help="gpt: the timed step; the others print a per-shape sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         bench_reference(args, world, rank)
+    elif args.workload != "gpt":
+        bench_sweep(args)
     else:
         bench_ours(args, world, rank, local)
     if world > 1:

@@ -10,6 +10,10 @@
 //                       256 columns) is the one that wastes the least work
 //                       over whole waves of one tile per SM, and K is split
 //                       when there are fewer tiles than half the SMs.
+//   M <= 16, A M x K -> the same kernel in its swapped form (C^T = B^T A^T):
+//                       the weights stream once through the 128-row MMA side,
+//                       the activations are a 16-column operand, and K is
+//                       split so that the units fill whole waves of the SMs.
 // An operand whose base or leading dimension breaks the TMA unit's 16-byte
 // rule is first copied into the workspace with an aligned leading dimension.
 #include <cuda_runtime.h>
@@ -150,21 +154,49 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   return GEMM_OK;
 }
 
+// K slices for the small-M form: the count whose units fill whole waves of one
+// CTA per SM best, with at least two K blocks per slice (ties go to fewer).
+int64_t skinny_splits(int64_t tiles, int64_t kb, int sms) {
+  int64_t best = 1;
+  double best_eff = 0.0;
+  const int64_t max_s = std::max<int64_t>(1, std::min<int64_t>(32, kb / 2));
+  for (int64_t s = 1; s <= max_s; ++s) {
+    const int64_t per = ceil_div(kb, s);
+    const int64_t eff_s = ceil_div(kb, per);  // slices actually used
+    if (eff_s != s) continue;
+    const int64_t units = tiles * s;
+    const double eff = static_cast<double>(units) / (ceil_div(units, sms) * sms);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = s;
+    }
+  }
+  return best;
+}
+
 gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
                      float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
-                     int64_t ldc, cudaStream_t s) {
+                     int64_t ldc, cudaStream_t s, bool swap) {
   using namespace dgt;
   const int es = (mode == GEMM_MODE_BF16) ? 2 : 4;
   const int bk = tc_tile_k(mode);
   const int sms = h->sms;
+  // The swapped form computes C^T = op(B)^T op(A)^T: the kernel sees M' = N,
+  // N' = M, A' = B and B' = A, and stores its tiles transposed.
+  const int64_t Mk = swap ? N : M, Nk = swap ? M : N;
+  const int ta_k = swap ? !transB : transA;  // is the kernel's A stored K x M'?
+  const int tb_k = swap ? !transA : transB;  // is the kernel's B stored N' x K?
+  const void* Ak = swap ? B : A;
+  const void* Bk = swap ? A : B;
+  const int64_t ldak = swap ? ldb : lda, ldbk = swap ? lda : ldb;
 
   // Tile width: the fewest padded columns over whole waves of one tile per SM.
-  int tile_n = h->opt_tile_n;
-  if (tile_n != 128 && tile_n != 256) {
-    const int64_t tm = ceil_div(M, 128);
+  int tile_n = swap ? 16 : h->opt_tile_n;
+  if (tile_n != 128 && tile_n != 256 && tile_n != 16) {
+    const int64_t tm = ceil_div(Mk, 128);
     int64_t best = -1;
     for (int bn : {256, 128}) {
-      const int64_t waves = ceil_div(tm * ceil_div(N, bn), sms);
+      const int64_t waves = ceil_div(tm * ceil_div(Nk, bn), sms);
       const int64_t cost = waves * bn;
       if (best < 0 || cost < best) {
         best = cost;
@@ -172,11 +204,13 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
       }
     }
   }
-  const int64_t tiles = ceil_div(M, 128) * ceil_div(N, tile_n);
+  const int64_t tiles = ceil_div(Mk, 128) * ceil_div(Nk, tile_n);
   const int64_t kb = ceil_div(K, bk);
   int64_t splits = 1;
   if (h->opt_split_k > 0) {
     splits = std::min<int64_t>(h->opt_split_k, kb);
+  } else if (swap) {
+    splits = skinny_splits(tiles, kb, sms);
   } else if (2 * tiles <= sms && kb >= 8) {
     splits = std::min<int64_t>(sms / tiles, kb / 4);
     splits = std::max<int64_t>(splits, 1);
@@ -185,10 +219,10 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   splits = ceil_div(kb, kb_per);
 
   // Workspace: re-packed operands (when the TMA rule needs them) and partials.
-  const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
-  const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
-  const bool pack_a = !aligned(A, 16) || (lda * es) % 16 != 0;
-  const bool pack_b = !aligned(B, 16) || (ldb * es) % 16 != 0;
+  const int64_t a_rows = ta_k ? K : Mk, a_cols = ta_k ? Mk : K;
+  const int64_t b_rows = tb_k ? Nk : K, b_cols = tb_k ? K : Nk;
+  const bool pack_a = !aligned(Ak, 16) || (ldak * es) % 16 != 0;
+  const bool pack_b = !aligned(Bk, 16) || (ldbk * es) % 16 != 0;
   const int64_t lda_p = round_up(a_cols, 16 / es), ldb_p = round_up(b_cols, 16 / es);
   WsLayout L;
   L.a_off = 0;
@@ -202,17 +236,17 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   }
   char* ws = static_cast<char*>(h->ws);
   int kernels = 0;
-  const void* Ause = A;
-  const void* Buse = B;
-  int64_t lda_use = lda, ldb_use = ldb;
+  const void* Ause = Ak;
+  const void* Buse = Bk;
+  int64_t lda_use = ldak, ldb_use = ldbk;
   if (pack_a) {
-    if (launch_pack(A, lda, ws + L.a_off, lda_p, a_rows, a_cols, es, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (launch_pack(Ak, ldak, ws + L.a_off, lda_p, a_rows, a_cols, es, s) != cudaSuccess) return GEMM_ERR_CUDA;
     Ause = ws + L.a_off;
     lda_use = lda_p;
     ++kernels;
   }
   if (pack_b) {
-    if (launch_pack(B, ldb, ws + L.b_off, ldb_p, b_rows, b_cols, es, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (launch_pack(Bk, ldbk, ws + L.b_off, ldb_p, b_rows, b_cols, es, s) != cudaSuccess) return GEMM_ERR_CUDA;
     Buse = ws + L.b_off;
     ldb_use = ldb_p;
     ++kernels;
@@ -220,11 +254,11 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
 
   TcArgs a{};
   a.mode = mode;
-  a.a_mn_major = transA ? 1 : 0;
-  a.b_mn_major = transB ? 0 : 1;
+  a.a_mn_major = ta_k ? 1 : 0;
+  a.b_mn_major = tb_k ? 0 : 1;
   a.tile_n = tile_n;
-  a.M = M;
-  a.N = N;
+  a.M = Mk;
+  a.N = Nk;
   a.K = K;
   a.A = Ause;
   a.lda = lda_use;
@@ -238,6 +272,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.kb_per_split = static_cast<int>(kb_per);
   a.ws = splits > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
   a.ws_ld = ws_ld;
+  a.ws_slice = M * ws_ld;  // partial sums are kept in the caller's M x N orientation
   a.status = h->d_status;
   a.grid = static_cast<int>(std::min<int64_t>(tiles * splits, sms));
   a.group_m = 16;
@@ -248,8 +283,8 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
       return GEMM_ERR_CUDA;
     ++kernels;
   }
-  set_plan(h, GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n), a.grid, kernels,
-           (pack_a ? 1 : 0) | (pack_b ? 2 : 0));
+  set_plan(h, swap ? GEMM_FAMILY_SKINNY : GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n),
+           a.grid, kernels, (swap ? ((pack_b ? 1 : 0) | (pack_a ? 2 : 0)) : ((pack_a ? 1 : 0) | (pack_b ? 2 : 0))));
   return GEMM_OK;
 }
 
@@ -330,8 +365,13 @@ gemm_status_t gemm_run(gemm_handle_t h, int mode, int transA, int transB, int64_
     return run_simt(h, transA, transB, M, N, K, alpha, static_cast<const float*>(A), lda,
                     static_cast<const float*>(B), ldb, beta, C, ldc, s);
   }
-  if (fam != GEMM_FAMILY_AUTO && fam != GEMM_FAMILY_TC) return GEMM_ERR_NOT_SUPPORTED;
-  return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s);
+  // Small M: the swapped form, which streams the weights through the 128-row
+  // MMA side once (activations must be stored M x K).
+  const bool skinny_ok = (transA == 0) && M <= 16;
+  if (fam == GEMM_FAMILY_SKINNY && !skinny_ok) return GEMM_ERR_NOT_SUPPORTED;
+  if (fam == GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
+  const bool swap = (fam == GEMM_FAMILY_SKINNY) || (fam == GEMM_FAMILY_AUTO && skinny_ok);
+  return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, swap);
 }
 
 gemm_status_t gemm_set_option(gemm_handle_t h, int option, int64_t value) {

@@ -50,10 +50,14 @@ struct TcArgs {
   int kb_per_split;      // k blocks per slice
   float* ws;
   int64_t ws_ld;
+  int64_t ws_slice;      // elements between successive K slices' partial sums
   int* status;           // device status word
   int grid;              // persistent CTAs
   int group_m;           // raster group height in M tiles
 };
+// tile_n == 16 selects the swapped small-M form: the caller passes the
+// operands exchanged (C^T = op(B)^T op(A)^T, M and N exchanged) and the
+// kernel stores its tile transposed into the caller's C.
 int tc_tile_k(int mode);              // k elements per stage (128 bytes)
 int tc_stages(int mode, int tile_n);  // pipeline depth
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream);

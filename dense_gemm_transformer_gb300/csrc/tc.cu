@@ -10,6 +10,7 @@
 // Out-of-range rows and columns of a box are filled with zeros by the TMA unit.
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "tc_launch.cuh"
@@ -35,6 +36,19 @@ cudaError_t encode_2d(CUtensorMap* m, int mode, const void* ptr, int64_t inner, 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The fp32 output (C, or the split-K partial sums as S slices of M x N) as a
+// 3-D map for the epilogue's TMA stores: box of 32 columns x 32 rows x 1 slice.
+cudaError_t encode_out(CUtensorMap* m, float* ptr, int64_t N, int64_t M, int64_t S, int64_t ld, int64_t slice) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(S)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4, static_cast<cuuint64_t>(slice) * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t tc_init_driver() {
@@ -54,8 +68,10 @@ cudaError_t tc_init_driver() {
 int tc_tile_k(int mode) { return mode == 2 ? 64 : 32; }
 
 int tc_stages(int mode, int tile_n) {
-  (void)mode;
-  return tile_n == 256 ? TcCfg<2, 256>::STAGES : TcCfg<2, 128>::STAGES;
+  (void)mode;  // a stage holds 128 bytes of K per row in both modes
+  if (tile_n == 256) return TcCfg<2, 256>::STAGES;
+  if (tile_n == 128) return TcCfg<2, 128>::STAGES;
+  return TcCfg<2, 16>::STAGES;
 }
 
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
@@ -88,10 +104,25 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.ldc = a.ldc;
   p.ws = a.ws;
   p.ws_ld = a.ws_ld;
+  p.ws_slice = a.ws_slice;
   p.status = a.status;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
-  if (a.mode == 2) return tc_launch_bf16(a.tile_n, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, p, a.grid, stream);
-  return tc_launch_tf32(a.tile_n, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, p, a.grid, stream);
+  // Tiles leave through TMA stores when the destination allows it: not the
+  // transposed small-M form, no read of C (beta == 0, or partial sums), and
+  // 16-byte aligned rows.
+  CUtensorMap tcm;
+  std::memset(&tcm, 0, sizeof tcm);
+  p.c_tma = 0;
+  if (a.tile_n >= 128) {
+    if (a.splits > 1) {
+      p.c_tma = (encode_out(&tcm, a.ws, a.N, a.M, a.splits, a.ws_ld, a.ws_slice) == cudaSuccess) ? 1 : 0;
+    } else if (a.beta == 0.f && p.c_vec) {
+      p.c_tma = (encode_out(&tcm, a.C, a.N, a.M, 1, a.ldc, a.M * a.ldc) == cudaSuccess) ? 1 : 0;
+    }
+  }
+  if (a.mode == 2)
+    return tc_launch_bf16(a.tile_n, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
+  return tc_launch_tf32(a.tile_n, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
 }
 
 }  // namespace dgt

@@ -3,7 +3,7 @@
 
 namespace dgt {
 cudaError_t tc_launch_bf16(int tile_n, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const TcParams& p, int grid, cudaStream_t s) {
-  return tc_launch_mode<2>(tile_n, a_mn, b_mn, ta, tb, p, grid, s);
+                           const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s) {
+  return tc_launch_mode<2>(tile_n, a_mn, b_mn, ta, tb, tc, p, grid, s);
 }
 }  // namespace dgt

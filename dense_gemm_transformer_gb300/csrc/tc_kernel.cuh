@@ -51,8 +51,10 @@ struct TcParams {
   int64_t ldc;
   float* ws;
   int64_t ws_ld;
+  int64_t ws_slice;  // elements between the partial sums of successive K slices
   int* status;
   int c_vec;  // C rows are 16-byte aligned (ldc % 4 == 0 and C aligned)
+  int c_tma;  // tiles leave through shared memory and TMA stores (tmC is valid)
 };
 
 // MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands).
@@ -66,12 +68,20 @@ struct TcCfg {
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;  // 192 KB of operand stages
-  static constexpr int TMEM_COLS = 2 * BN;            // two accumulators
+  // ~192-200 KB of operand stages
+  static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128) ? 6 : 200 * 1024 / STAGE_BYTES;
+  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;  // two accumulators (allocation >= 32 columns)
+  static constexpr int CW = BN < 32 ? BN : 32;                    // accumulator columns per TMEM load
   static constexpr int NUM_BARS = 2 * STAGES + 5;     // full/empty per stage, acc full/empty x2, drain
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // Epilogue staging for TMA stores: 2 buffers of 32 rows x 128 bytes per
+  // epilogue warp (the swapped small-M form stores directly and has none).
+  static constexpr int STAGING_BYTES = (BN >= 128) ? 4 * 2 * 32 * 128 : 0;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
   static constexpr uint32_t FORMAT = (MODE == 2) ? 1u : 2u;  // bf16 / tf32 in the instruction descriptor
   static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
+  static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
 };
 
 template <int MODE>
@@ -116,17 +126,21 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
   }
 }
 
-template <int MODE, bool A_MN, bool B_MN, int BN>
+// TRANS_C: the kernel computes C^T = op(B)^T op(A)^T with the operands
+// swapped by the host (a small-M product whose weights fill the 128-row MMA
+// side), so element (r, c) of its tile is stored at C[c * ldc + r].
+template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C>
 __global__ void __launch_bounds__(192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using Cfg = TcCfg<MODE, BN>;
   constexpr int S = Cfg::STAGES;
   constexpr uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN, B_MN, Cfg::BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+  uint8_t* staging = smem + S * Cfg::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -157,6 +171,7 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.c_tma) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -266,28 +281,62 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     const bool partial = p.splits > 1;
     const bool read_c = !partial && p.beta != 0.f;
+    constexpr int CW = Cfg::CW;
+    uint32_t tma_buf = 0;  // staging buffers used by this warp so far
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
       const Unit w = decode_unit(u, p);
       if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull)) break;
       tc_fence_after();
       const int64_t row = static_cast<int64_t>(w.tm) * Cfg::BM + sub * 32 + lane;
       const bool row_ok = row < p.M;
-      float* out = partial ? p.ws + (static_cast<int64_t>(w.split) * p.M + (row_ok ? row : 0)) * p.ws_ld
-                           : p.C + (row_ok ? row : 0) * p.ldc;
-      const bool vec_ok = partial || p.c_vec;
+      float* base = partial ? p.ws + static_cast<int64_t>(w.split) * p.ws_slice : p.C;
+      const int64_t ld = partial ? p.ws_ld : p.ldc;
+      float* out = TRANS_C ? base : base + (row_ok ? row : 0) * ld;
+      const bool vec_ok = !TRANS_C && (partial || p.c_vec);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 32; ++cc) {
-        uint32_t r[32];
+      for (int cc = 0; cc < BN / CW; ++cc) {
+        uint32_t r[CW];
         __syncwarp();
-        tmem_ld_32x32b_x32(t_row + cc * 32, r);
+        tmem_ld_32x32b<CW>(t_row + cc * CW, r);
         tmem_wait_ld();
-        const int64_t col0 = static_cast<int64_t>(w.tn) * BN + cc * 32;
-        if (!row_ok || col0 >= p.N) {
-          // nothing of this 32-column chunk is inside C for this thread
-        } else if (vec_ok && col0 + 32 <= p.N) {
+        const int64_t col0 = static_cast<int64_t>(w.tn) * BN + cc * CW;
+        if constexpr (Cfg::STAGING_BYTES > 0 && CW == 32) {
+          if (p.c_tma) {
+            // Through shared memory: this warp's 32 rows x 32 columns go to
+            // one of its two 4 KB buffers in the 128-byte-swizzled layout the
+            // TMA unit reads (16-byte chunk j of row t sits at chunk j ^ (t % 8)),
+            // then one lane stores the box; the unit clips rows past M and
+            // columns past N.
+            uint8_t* buf = staging + (sub * 2 + (tma_buf & 1)) * 4096;
+            if (lane == 0) bulk_wait_group_read<1>();  // the buffer's previous store has read it
+            __syncwarp();
+            const float a = partial ? 1.f : p.alpha;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < 8; ++q) {
+              float4 v;
+              v.x = a * __uint_as_float(r[4 * q + 0]);
+              v.y = a * __uint_as_float(r[4 * q + 1]);
+              v.z = a * __uint_as_float(r[4 * q + 2]);
+              v.w = a * __uint_as_float(r[4 * q + 3]);
+              *reinterpret_cast<float4*>(buf + lane * 128 + ((q ^ (lane & 7)) * 16)) = v;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmC, smem_u32(buf), static_cast<int32_t>(col0), w.tm * Cfg::BM + sub * 32,
+                           partial ? w.split : 0);
+              bulk_commit_group();
+            }
+            ++tma_buf;
+            continue;
+          }
+        }
+        if (!row_ok || col0 >= p.N) {
+          // nothing of this chunk is inside C for this thread
+        } else if (vec_ok && col0 + CW <= p.N) {
+#pragma unroll
+          for (int q = 0; q < CW / 4; ++q) {
             float4 v;
             v.x = __uint_as_float(r[4 * q + 0]);
             v.y = __uint_as_float(r[4 * q + 1]);
@@ -311,15 +360,17 @@ __global__ void __launch_bounds__(192, 1)
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < CW; ++j) {
             const int64_t col = col0 + j;
             if (col < p.N) {
+              // TRANS_C: lanes hold consecutive rows, so each store of the warp is contiguous.
+              float* dst = TRANS_C ? out + col * ld + row : out + col;
               float v = __uint_as_float(r[j]);
               if (!partial) {
                 v *= p.alpha;
-                if (read_c) v = fmaf(p.beta, out[col], v);
+                if (read_c) v = fmaf(p.beta, *dst, v);
               }
-              out[col] = v;
+              *dst = v;
             }
           }
         }
@@ -332,11 +383,15 @@ __global__ void __launch_bounds__(192, 1)
         acc_phase ^= 1u;
       }
     }
+    // Every TMA store of this warp has completed before the CTA exits.
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }

@@ -7,37 +7,45 @@
 
 namespace dgt {
 
-template <int MODE, bool A_MN, bool B_MN, int BN>
-cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p, int grid,
+template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C = false>
+cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p, int grid,
                           cudaStream_t s) {
   using Cfg = TcCfg<MODE, BN>;
-  auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN>;
+  auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN, TRANS_C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 192, Cfg::SMEM_BYTES, s>>>(ta, tb, p);
+  kern<<<grid, 192, Cfg::SMEM_BYTES, s>>>(ta, tb, tc, p);
   return cudaGetLastError();
 }
 
 template <int MODE, int BN>
-cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const TcParams& p,
+cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p,
                          int grid, cudaStream_t s) {
-  if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN>(ta, tb, p, grid, s);
-  if (!a_mn && b_mn) return tc_launch_one<MODE, false, true, BN>(ta, tb, p, grid, s);
-  if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN>(ta, tb, p, grid, s);
-  return tc_launch_one<MODE, true, true, BN>(ta, tb, p, grid, s);
+  if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN>(ta, tb, tc, p, grid, s);
+  if (!a_mn && b_mn) return tc_launch_one<MODE, false, true, BN>(ta, tb, tc, p, grid, s);
+  if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN>(ta, tb, tc, p, grid, s);
+  return tc_launch_one<MODE, true, true, BN>(ta, tb, tc, p, grid, s);
 }
 
+// tile_n == 16 is the swapped small-M form: the weights are the 128-row
+// operand (K-major or MN-major), the activations a K-major 16-row operand,
+// and C is written transposed.
 template <int MODE>
 cudaError_t tc_launch_mode(int tile_n, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const TcParams& p, int grid, cudaStream_t s) {
-  if (tile_n == 256) return tc_launch_bn<MODE, 256>(a_mn, b_mn, ta, tb, p, grid, s);
-  return tc_launch_bn<MODE, 128>(a_mn, b_mn, ta, tb, p, grid, s);
+                           const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s) {
+  if (tile_n == 256) return tc_launch_bn<MODE, 256>(a_mn, b_mn, ta, tb, tc, p, grid, s);
+  if (tile_n == 128) return tc_launch_bn<MODE, 128>(a_mn, b_mn, ta, tb, tc, p, grid, s);
+  if (tile_n == 16 && !b_mn) {
+    return a_mn ? tc_launch_one<MODE, true, false, 16, true>(ta, tb, tc, p, grid, s)
+                : tc_launch_one<MODE, false, false, 16, true>(ta, tb, tc, p, grid, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 // Defined in tc_tf32.cu (MODE 1) and tc_bf16.cu (MODE 2).
 cudaError_t tc_launch_tf32(int tile_n, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const TcParams& p, int grid, cudaStream_t s);
+                           const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s);
 cudaError_t tc_launch_bf16(int tile_n, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const TcParams& p, int grid, cudaStream_t s);
+                           const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s);
 
 }  // namespace dgt

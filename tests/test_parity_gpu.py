@@ -233,3 +233,40 @@ def test_gpt_projection_shapes_sampled(h, mode, proj):
         for r0, r1 in _cases.sample_rows(M, width=width):
             ref, D = oracle.gemm(mode, Ah.numpy(), Bh.numpy(), transA=tA, transB=tB, rows=(r0, r1))
             _gate.assert_within(mode, got[r0:r1], ref, D, what=f"{name}.{tag} rows {r0}:{r1}")
+
+
+# ------------------------------------------------------------ small M (swapped form)
+@pytest.mark.parametrize("mode", ["bf16", "tf32"])
+@pytest.mark.parametrize("tB", [False, True])
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 700), (7, 300, 64), (16, 129, 2000), (3, 65, 40)])
+def test_skinny_ragged(h, mode, tB, M, N, K):
+    _cases.run_and_check(h, mode, M, N, K, False, tB, seed=53, dist="normal")
+    assert h.plan()["family"] == "skinny"
+    _cases.run_and_check(h, mode, M, N, K, False, tB, alpha=0.5, beta=1.0, seed=54, dist="normal")
+
+
+def _column_ranges(N, tile=128, width=3):
+    picks = sorted({0, tile - 1, N // 2, N - width})
+    return [(c, min(c + width, N)) for c in picks if 0 <= c < N]
+
+
+@pytest.mark.parametrize("M", si.SKINNY_M)
+@pytest.mark.parametrize("w", range(len(si.SKINNY_WEIGHTS)))
+@pytest.mark.parametrize("tB", [False, True])
+def test_skinny_decode_shapes_sampled(h, M, w, tB):
+    """The decode shapes at full size in bf16 (the benchmark's launch
+    configuration), checked on sampled columns against the oracle."""
+    K, N = si.SKINNY_WEIGHTS[w]
+    a32 = si.normal((M, K), si.seed_for(4, w, 0))
+    b32 = si.normal((N, K) if tB else (K, N), si.seed_for(4, w, 1), std=0.02)
+    a16, b16 = si.to_bf16(a32), si.to_bf16(b32)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    h.run(a16.cuda(), b16.cuda(), C, mode="bf16", transB=tB)
+    assert h.check_device() == 0
+    assert h.plan()["family"] == "skinny"
+    got = C.cpu().numpy()
+    abits, bbits = si.bf16_bits(a16), si.bf16_bits(b16)
+    for c0, c1 in _column_ranges(N):
+        bcols = bbits[c0:c1, :] if tB else bbits[:, c0:c1]
+        ref, D = oracle.gemm("bf16", abits, bcols, transB=tB)
+        _gate.assert_within("bf16", got[:, c0:c1], ref, D, what=f"skinny M={M} {K}x{N} cols {c0}:{c1}")
