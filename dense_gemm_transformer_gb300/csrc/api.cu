@@ -23,7 +23,7 @@
 #include <cstring>
 #include <new>
 
-#include "../../include/gemm.h"
+#include "gemm.h"
 #include "kernels.h"
 
 struct gemm_handle_s {
@@ -154,6 +154,42 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   return GEMM_OK;
 }
 
+// How one tensor-core operand reaches the kernel.  `rows x cols` is the
+// operand as stored (row-major, pitch `ld`); `mn_major` says its contiguous
+// dimension is M (or N) rather than K.
+struct OperandPack {
+  enum Kind { kNone, kCopy, kTranspose } kind = kNone;
+  const void* src = nullptr;
+  int64_t ld = 0, rows = 0, cols = 0, dst_ld = 0;
+  bool mn_major_after = false;
+  size_t bytes = 0;
+};
+
+OperandPack plan_pack(const void* src, int64_t ld, int64_t rows, int64_t cols, bool mn_major, int mode, int es) {
+  OperandPack p;
+  p.src = src;
+  p.ld = ld;
+  p.rows = rows;
+  p.cols = cols;
+  p.mn_major_after = mn_major;
+  if (mode == GEMM_MODE_TF32 && mn_major) {
+    p.kind = OperandPack::kTranspose;  // stored K x MN -> MN x K
+    p.dst_ld = round_up(rows, 16 / es);
+    p.bytes = static_cast<size_t>(cols * p.dst_ld * es);
+    p.mn_major_after = false;
+  } else if (!aligned(src, 16) || (ld * es) % 16 != 0) {
+    p.kind = OperandPack::kCopy;
+    p.dst_ld = round_up(cols, 16 / es);
+    p.bytes = static_cast<size_t>(rows * p.dst_ld * es);
+  }
+  return p;
+}
+
+cudaError_t run_pack(const OperandPack& p, void* dst, int es, cudaStream_t s) {
+  if (p.kind == OperandPack::kTranspose) return dgt::launch_transpose(p.src, p.ld, dst, p.dst_ld, p.rows, p.cols, es, s);
+  return dgt::launch_pack(p.src, p.ld, dst, p.dst_ld, p.rows, p.cols, es, s);
+}
+
 // K slices for the small-M form: the count whose units fill whole waves of one
 // CTA per SM best, with at least two K blocks per slice (ties go to fewer).
 int64_t skinny_splits(int64_t tiles, int64_t kb, int sms) {
@@ -218,16 +254,18 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   const int64_t kb_per = ceil_div(kb, splits);
   splits = ceil_div(kb, kb_per);
 
-  // Workspace: re-packed operands (when the TMA rule needs them) and partials.
-  const int64_t a_rows = ta_k ? K : Mk, a_cols = ta_k ? Mk : K;
-  const int64_t b_rows = tb_k ? Nk : K, b_cols = tb_k ? K : Nk;
-  const bool pack_a = !aligned(Ak, 16) || (ldak * es) % 16 != 0;
-  const bool pack_b = !aligned(Bk, 16) || (ldbk * es) % 16 != 0;
-  const int64_t lda_p = round_up(a_cols, 16 / es), ldb_p = round_up(b_cols, 16 / es);
+  // Workspace: re-packed operands and split-K partials.  An operand is copied
+  // when the TMA unit cannot read it in place (base not 16-byte aligned, or a
+  // row pitch that is not a multiple of 16 bytes), and transposed into K-major
+  // order when it is MN-major in TF32 mode: kind::tf32 takes K-major operands
+  // only (an MN-major TF32 operand produced zeros on this part, while BF16
+  // reads both orders).
+  OperandPack pa = plan_pack(Ak, ldak, ta_k ? K : Mk, ta_k ? Mk : K, ta_k != 0, mode, es);
+  OperandPack pb = plan_pack(Bk, ldbk, tb_k ? Nk : K, tb_k ? K : Nk, tb_k == 0, mode, es);
   WsLayout L;
   L.a_off = 0;
-  L.b_off = round_up(pack_a ? a_rows * lda_p * es : 0, 256);
-  L.p_off = L.b_off + round_up(pack_b ? b_rows * ldb_p * es : 0, 256);
+  L.b_off = round_up(static_cast<int64_t>(pa.bytes), 256);
+  L.p_off = L.b_off + round_up(static_cast<int64_t>(pb.bytes), 256);
   const int64_t ws_ld = round_up(N, 4);
   L.total = L.p_off + (splits > 1 ? static_cast<size_t>(splits * M * ws_ld) * sizeof(float) : 0);
   if (L.total > 0) {
@@ -239,23 +277,27 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   const void* Ause = Ak;
   const void* Buse = Bk;
   int64_t lda_use = ldak, ldb_use = ldbk;
-  if (pack_a) {
-    if (launch_pack(Ak, ldak, ws + L.a_off, lda_p, a_rows, a_cols, es, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  bool a_mn = ta_k != 0, b_mn = tb_k == 0;
+  if (pa.kind != OperandPack::kNone) {
+    if (run_pack(pa, ws + L.a_off, es, s) != cudaSuccess) return GEMM_ERR_CUDA;
     Ause = ws + L.a_off;
-    lda_use = lda_p;
+    lda_use = pa.dst_ld;
+    a_mn = pa.mn_major_after;
     ++kernels;
   }
-  if (pack_b) {
-    if (launch_pack(Bk, ldbk, ws + L.b_off, ldb_p, b_rows, b_cols, es, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (pb.kind != OperandPack::kNone) {
+    if (run_pack(pb, ws + L.b_off, es, s) != cudaSuccess) return GEMM_ERR_CUDA;
     Buse = ws + L.b_off;
-    ldb_use = ldb_p;
+    ldb_use = pb.dst_ld;
+    b_mn = pb.mn_major_after;
     ++kernels;
   }
+  const bool pack_a = pa.kind != OperandPack::kNone, pack_b = pb.kind != OperandPack::kNone;
 
   TcArgs a{};
   a.mode = mode;
-  a.a_mn_major = ta_k ? 1 : 0;
-  a.b_mn_major = tb_k ? 0 : 1;
+  a.a_mn_major = a_mn ? 1 : 0;
+  a.b_mn_major = b_mn ? 1 : 0;
   a.tile_n = tile_n;
   a.M = Mk;
   a.N = Nk;

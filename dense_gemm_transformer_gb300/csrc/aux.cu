@@ -1,9 +1,9 @@
 // aux.cu -- the small HBM-bound kernels around the GEMM kernels: the split-K
 // reduction with the fused alpha/beta epilogue, the beta-only update used when
-// K == 0 or alpha == 0, and the operand re-pack that gives an operand with an
-// unaligned leading dimension a 16-byte-aligned copy the TMA unit can read.
-// All three are grid-stride loops over rows x 4-wide column groups, sized to a
-// few CTAs per SM.
+// K == 0 or alpha == 0, the operand re-pack that gives an operand with an
+// unaligned leading dimension a 16-byte-aligned copy the TMA unit can read,
+// and the transpose that turns an MN-major TF32 operand K-major.
+// All are grid-stride loops sized to at most eight CTAs per SM.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -83,7 +83,46 @@ __global__ void pack_kernel(const T* __restrict__ src, int64_t ld_src, T* __rest
   }
 }
 
+// 32 x 32 tiles through shared memory (one padding column keeps the
+// transposed reads free of bank conflicts); reads and writes are both
+// coalesced along rows.  Blocks of 32 x 8 threads loop over the tiles.
+template <typename T>
+__global__ void transpose_kernel(const T* __restrict__ src, int64_t ld_src, T* __restrict__ dst, int64_t ld_dst,
+                                 int64_t rows, int64_t cols) {
+  __shared__ T tile[32][33];
+  const int64_t tiles_c = (cols + 31) / 32;
+  const int64_t tiles = ((rows + 31) / 32) * tiles_c;
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const int64_t r0 = (t / tiles_c) * 32, c0 = (t % tiles_c) * 32;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+      const int64_t r = r0 + i, c = c0 + threadIdx.x;
+      if (r < rows && c < cols) tile[i][threadIdx.x] = src[r * ld_src + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+      const int64_t c = c0 + i, r = r0 + threadIdx.x;
+      if (c < cols && r < rows) dst[c * ld_dst + r] = tile[threadIdx.x][i];
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
+                             int elem_bytes, cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
+  const int blocks = grid_for(tiles * 256, 256);
+  const dim3 block(32, 8);
+  if (elem_bytes == 2)
+    transpose_kernel<uint16_t><<<blocks, block, 0, stream>>>(static_cast<const uint16_t*>(src), ld_src,
+                                                              static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+  else
+    transpose_kernel<float><<<blocks, block, 0, stream>>>(static_cast<const float*>(src), ld_src,
+                                                           static_cast<float*>(dst), ld_dst, rows, cols);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_splitk_reduce(int64_t M, int64_t N, int splits, const float* ws, int64_t ws_ld, float* C,
                                  int64_t ldc, float alpha, float beta, cudaStream_t stream) {

@@ -74,4 +74,8 @@ cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta
 cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
                         int elem_bytes, cudaStream_t stream);
 
+// dst (cols x rows, leading dimension ld_dst) = transpose of src (rows x cols).
+cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
+                             int elem_bytes, cudaStream_t stream);
+
 }  // namespace dgt

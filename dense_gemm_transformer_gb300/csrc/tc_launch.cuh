@@ -18,10 +18,13 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
   return cudaGetLastError();
 }
 
+// kind::tf32 takes K-major operands only (the planner transposes MN-major
+// TF32 operands first), so only BF16 instantiates the MN-major forms.
 template <int MODE, int BN>
-cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p,
-                         int grid, cudaStream_t s) {
+cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                         const TcParams& p, int grid, cudaStream_t s) {
   if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN>(ta, tb, tc, p, grid, s);
+  if constexpr (MODE == 1) return cudaErrorInvalidValue;
   if (!a_mn && b_mn) return tc_launch_one<MODE, false, true, BN>(ta, tb, tc, p, grid, s);
   if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN>(ta, tb, tc, p, grid, s);
   return tc_launch_one<MODE, true, true, BN>(ta, tb, tc, p, grid, s);
@@ -36,8 +39,8 @@ cudaError_t tc_launch_mode(int tile_n, bool a_mn, bool b_mn, const CUtensorMap& 
   if (tile_n == 256) return tc_launch_bn<MODE, 256>(a_mn, b_mn, ta, tb, tc, p, grid, s);
   if (tile_n == 128) return tc_launch_bn<MODE, 128>(a_mn, b_mn, ta, tb, tc, p, grid, s);
   if (tile_n == 16 && !b_mn) {
-    return a_mn ? tc_launch_one<MODE, true, false, 16, true>(ta, tb, tc, p, grid, s)
-                : tc_launch_one<MODE, false, false, 16, true>(ta, tb, tc, p, grid, s);
+    if (!a_mn) return tc_launch_one<MODE, false, false, 16, true>(ta, tb, tc, p, grid, s);
+    if constexpr (MODE == 2) return tc_launch_one<MODE, true, false, 16, true>(ta, tb, tc, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
