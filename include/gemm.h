@@ -21,12 +21,14 @@
  *   A and B are float in GEMM_MODE_FP32 and GEMM_MODE_TF32 and bfloat16
  *   (raw 16-bit patterns) in GEMM_MODE_BF16.  In TF32 mode the fp32 operands
  *   are passed to the tensor cores unchanged; the hardware drops their 13 low
- *   mantissa bits.
+ *   mantissa bits.  The TF32 tensor-core instruction reads K-major operands
+ *   only, so in TF32 mode an operand stored with M (or N) contiguous (A with
+ *   transA == 1, B with transB == 0) is first transposed into the workspace.
  *
  * Ownership: the caller owns A, B and C, which are device memory.  A handle
  * owns its device properties, a device status word and a scratch workspace
- * (split-K partial sums and re-packed operands) that grows on demand and is
- * freed by gemm_destroy.  A handle is bound to the device that was current at
+ * (split-K partial sums, re-packed and transposed operands) that grows on
+ * demand and is freed by gemm_destroy.  A handle is bound to the device that was current at
  * gemm_create and must not be used from two streams at the same time.
  *
  * Errors: every call returns a status and never throws.  Arguments are checked
