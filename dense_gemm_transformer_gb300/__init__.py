@@ -24,7 +24,7 @@ MODES = {"fp32": 0, "tf32": 1, "bf16": 2}
 FAMILIES = {"auto": 0, "simt": 1, "tc": 2, "skinny": 3}
 OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3}
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED", 3: "GEMM_ERR_MISALIGNED",
-          4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_ALLOC", 6: "GEMM_ERR_DEVICE_TIMEOUT"}
+          4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_ALLOC", 6: "GEMM_ERR_DEVICE_TIMEOUT", 7: "GEMM_ERR_TOO_LARGE"}
 HEADER = os.path.join(_build.ROOT, "include", "gemm.h")
 
 
@@ -202,3 +202,30 @@ def default_handle() -> Gemm:
 def gemm(A, B, C, mode="fp32", transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
     """C = alpha * op(A) op(B) + beta * C with the current device's default handle."""
     return default_handle().run(A, B, C, mode, transA, transB, alpha, beta, stream)
+
+
+def run_small_m_noalloc(A, B, C, mode="bf16", transB=False, alpha=1.0, beta=0.0, stream=None):
+    """C = alpha * A op(B) + beta * C for M <= 16 through gemm_run_small_m_noalloc.
+
+    For callers that may not allocate device memory (a runtime that owns all
+    allocations, a plug-in in another program's CUDA context): the library
+    uses only its fixed internal scratch array and no handle.  A is M x K,
+    B is K x N (or N x K with transB), C is M x N float32, all on the device.
+    """
+    import torch
+    lib = load()
+    fn = lib.gemm_run_small_m_noalloc
+    if fn.argtypes is None:
+        i64, vp, f32, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+        fn.argtypes = [i32, i32, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, vp]
+        fn.restype = i32
+    M, K = A.shape
+    N = B.shape[0] if transB else B.shape[1]
+    pa, lda = _matrix(A, "A")
+    pb, ldb = _matrix(B, "B")
+    pc, ldc = _matrix(C, "C")
+    if stream is None:
+        stream = torch.cuda.current_stream(C.device)
+    _check(fn(MODES[mode], int(bool(transB)), M, N, K, float(alpha), pa, lda, pb, ldb, float(beta), pc, ldc,
+              _stream_ptr(stream)), "gemm_run_small_m_noalloc")
+    return C

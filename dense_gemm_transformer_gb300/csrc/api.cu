@@ -463,6 +463,7 @@ const char* gemm_status_string(gemm_status_t s) {
     case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
     case GEMM_ERR_ALLOC: return "GEMM_ERR_ALLOC";
     case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT";
+    case GEMM_ERR_TOO_LARGE: return "GEMM_ERR_TOO_LARGE";
     default: return "GEMM_ERR_UNKNOWN";
   }
 }

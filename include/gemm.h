@@ -60,7 +60,8 @@ typedef enum {
   GEMM_ERR_MISALIGNED = 3,    /* a pointer is not aligned to its element size                        */
   GEMM_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed                                */
   GEMM_ERR_ALLOC = 5,         /* device memory for the handle's workspace could not be allocated    */
-  GEMM_ERR_DEVICE_TIMEOUT = 6 /* a kernel gave up a bounded wait and set the device status word      */
+  GEMM_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up a bounded wait and set the device status word     */
+  GEMM_ERR_TOO_LARGE = 7       /* the problem exceeds gemm_run_small_m_noalloc's limits (M, scratch)  */
 } gemm_status_t;
 
 /* Kernel families the planner chooses among (gemm_set_option/GEMM_OPT_FAMILY). */
@@ -129,6 +130,45 @@ gemm_status_t gemm_get_plan(gemm_handle_t h, gemm_plan_t* out);
  * the last check (its output is then undefined), GEMM_ERR_CUDA if the stream
  * reports an error, GEMM_OK otherwise. */
 gemm_status_t gemm_check_device(gemm_handle_t h, void* stream);
+
+/* Bytes of the fixed device array that gemm_run_small_m_noalloc uses as its
+ * only scratch memory (one array per device, held until the process exits). */
+#define GEMM_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* The small-M product of gemm_run (M <= 16: a few token rows against a weight
+ * matrix, as in one decode step) for callers that cannot allocate device
+ * memory.  The source pages have no counterpart to this call; it exists for
+ * code that runs where cudaMalloc is unavailable or forbidden -- an inference
+ * runtime that owns every allocation through its own pool, a plug-in inside
+ * another program's CUDA context, a loop that must never enter the allocator.
+ * gemm_run cannot serve such callers because its handle allocates a status
+ * word when created and a workspace when first used.
+ *
+ * Same arithmetic and kernels as gemm_run picks for these shapes: A is stored
+ * M x K (transA is always 0), B is K x N (transB == 0) or N x K (transB == 1),
+ * mode is GEMM_MODE_BF16 or GEMM_MODE_TF32 (TF32 needs transB == 1), C is
+ * M x N fp32.  The caller passes inputs and outputs; the only scratch is a
+ * fixed device array of GEMM_NOALLOC_SCRATCH_BYTES inside the library (the
+ * device status word and the split-K partial sums).  The call makes no
+ * cudaMalloc, no cudaFree and no allocating library call.
+ *
+ * Limits and errors: M > 16, or split-K partial sums that would not fit the
+ * array even with a single K slice, give GEMM_ERR_TOO_LARGE; an operand the
+ * TMA unit cannot read in place (base not 16-byte aligned, row pitch not a
+ * multiple of 16 bytes) gives GEMM_ERR_MISALIGNED; FP32 mode or TF32 with
+ * transB == 0 gives GEMM_ERR_NOT_SUPPORTED; the other checks are gemm_run's.
+ * The planner's K-slice count is lowered when its partial sums would not fit.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call on a device shares the one array and leaves its contents behind: the
+ * call clears the status word itself, and calls whose kernels overlap on the
+ * GPU (different streams, no ordering between them) race on the array and
+ * give undefined results.  A device-side wait that times out is recorded in
+ * the array's status word but not reported by this call. */
+gemm_status_t gemm_run_small_m_noalloc(int mode, int transB, int64_t M, int64_t N, int64_t K, float alpha,
+                                       const void* A, int64_t lda, const void* B, int64_t ldb,
+                                       float beta, float* C, int64_t ldc, void* stream);
 
 /* A static string naming a status code. */
 const char* gemm_status_string(gemm_status_t s);
