@@ -38,7 +38,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("family", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("tile_k", ctypes.c_int32), ("split_k", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("kernels", ctypes.c_int32), ("packed", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 7)]
+                ("schedule", ctypes.c_int32), ("reserved", ctypes.c_int32 * 6)]
 
 
 _lib = None
@@ -146,7 +146,8 @@ class Gemm:
         fam = {v: k for k, v in FAMILIES.items()}.get(p.family, "none")
         return {"family": fam if p.kernels else "none", "tile_m": p.tile_m, "tile_n": p.tile_n,
                 "tile_k": p.tile_k, "split_k": p.split_k, "stages": p.stages, "grid": p.grid,
-                "kernels": p.kernels, "packed": p.packed}
+                "kernels": p.kernels, "packed": p.packed,
+                "schedule": {0: "tiles", 1: "split_k", 2: "stream_k"}.get(p.schedule, "tiles")}
 
     def check_device(self, stream=None) -> int:
         """Synchronize the stream and return the device status (0 = ok)."""

@@ -3,9 +3,10 @@
 //
 // The planner maps a call to one kernel family with a fixed rule (no runtime
 // autotuning):
-//   FP32             -> the register-tiled SIMT kernel; K is split when the
-//                       output has fewer 128 x 128 tiles than the two CTAs per
-//                       SM the kernel can keep resident.
+//   FP32             -> the register-tiled SIMT kernel, one CTA per 128 x 128
+//                       tile when the tiles fill whole waves of the two CTAs
+//                       per SM it keeps resident (>= 92%), stream-K over the
+//                       resident CTAs otherwise.
 //   TF32, BF16       -> the persistent tcgen05 kernel; the tile width (128 or
 //                       256 columns) is the one that wastes the least work
 //                       over whole waves of one tile per SM, and K is split
@@ -109,15 +110,8 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
                        cudaStream_t s) {
   using namespace dgt;
   const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, kSimtTileN);
-  int64_t splits = 1;
-  if (h->opt_split_k > 0) {
-    splits = h->opt_split_k;
-  } else if (tiles < h->sms && K >= 1024) {
-    splits = std::min<int64_t>(ceil_div(2 * h->sms, tiles), K / 256);
-    splits = std::max<int64_t>(splits, 1);
-  }
-  int64_t kps = round_up(ceil_div(K, splits), kSimtTileK);
-  splits = ceil_div(K, kps);
+  const int64_t kt = ceil_div(K, kSimtTileK);
+  const int64_t slots = 2 * static_cast<int64_t>(h->sms);  // resident CTAs (two per SM)
   SimtArgs a{};
   a.transA = transA;
   a.transB = transB;
@@ -132,25 +126,50 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   a.ldc = ldc;
   a.alpha = alpha;
   a.beta = beta;
-  a.splits = static_cast<int>(splits);
-  a.k_per_split = kps;
   a.ws_ld = round_up(N, 4);
-  if (splits > 1) {
-    gemm_status_t st = ensure_ws(h, static_cast<size_t>(splits * M * a.ws_ld) * sizeof(float));
+  a.splits = 1;
+  a.k_per_split = K;
+  int grid = static_cast<int>(std::min<int64_t>(tiles, INT32_MAX));
+  int kernels = 1;
+  // Whole tiles when they fill whole waves of the resident CTAs (or the
+  // problem is too small to share out); stream-K otherwise.
+  const double wave_eff = static_cast<double>(tiles) / (ceil_div(tiles, slots) * slots);
+  if (h->opt_split_k > 0) {
+    int64_t splits = h->opt_split_k;
+    const int64_t kps = round_up(ceil_div(K, splits), kSimtTileK);
+    splits = ceil_div(K, kps);
+    a.schedule = splits > 1 ? kSimtSplitK : kSimtTiles;
+    a.splits = static_cast<int>(splits);
+    a.k_per_split = kps;
+    grid = static_cast<int>(tiles * splits);
+  } else if (wave_eff >= 0.92 || tiles * kt < 4 * slots) {
+    a.schedule = kSimtTiles;
+  } else {
+    a.schedule = kSimtStreamK;
+    a.iters = tiles * kt;
+    // at least 8 k-tiles per CTA; at most 510 CTAs (the fixup's part list)
+    a.grid = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(slots, 510), a.iters / 8));
+    grid = static_cast<int>(a.grid);
+  }
+  if (a.schedule == kSimtSplitK) {
+    gemm_status_t st = ensure_ws(h, static_cast<size_t>(a.splits * M * a.ws_ld) * sizeof(float));
     if (st != GEMM_OK) return st;
     a.ws = static_cast<float*>(h->ws);
+  } else if (a.schedule == kSimtStreamK) {
+    gemm_status_t st = ensure_ws(h, static_cast<size_t>(2 * a.grid * simt_streamk_slot_floats()) * sizeof(float));
+    if (st != GEMM_OK) return st;
+    a.ws = static_cast<float*>(h->ws);
+    ++kernels;  // the fixup
   }
-  if (ceil_div(M, kSimtTileM) > 65535) return GEMM_ERR_NOT_SUPPORTED;
-  cudaError_t e = launch_simt(a, s);
-  if (e != cudaSuccess) return GEMM_ERR_CUDA;
-  int kernels = 1;
-  if (splits > 1) {
-    e = launch_splitk_reduce(M, N, a.splits, a.ws, a.ws_ld, C, ldc, alpha, beta, s);
-    if (e != cudaSuccess) return GEMM_ERR_CUDA;
+  if (a.schedule != kSimtStreamK && ceil_div(M, kSimtTileM) > 65535) return GEMM_ERR_NOT_SUPPORTED;
+  if (launch_simt(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (a.schedule == kSimtSplitK) {
+    if (launch_splitk_reduce(M, N, a.splits, a.ws, a.ws_ld, C, ldc, alpha, beta, s) != cudaSuccess)
+      return GEMM_ERR_CUDA;
     ++kernels;
   }
-  set_plan(h, GEMM_FAMILY_SIMT, kSimtTileM, kSimtTileN, kSimtTileK, a.splits, 2, static_cast<int>(tiles * splits),
-           kernels, 0);
+  set_plan(h, GEMM_FAMILY_SIMT, kSimtTileM, kSimtTileN, kSimtTileK, a.splits, 3, grid, kernels, 0);
+  h->plan.schedule = a.schedule;
   return GEMM_OK;
 }
 

@@ -11,8 +11,14 @@
 //     that the lanes sharing a row or column receive by broadcast;
 //   * A is stored k-major in shared memory (transposed on the way in when the
 //     operand is stored M x K) so both operands are read as float4 along M / N;
-//   * the next K tile is copied global -> shared with cp.async (no register
-//     staging) into the second buffer while the current one is multiplied;
+//   * K tiles are copied global -> shared with cp.async (no register
+//     staging) into a three-stage ring, two tiles ahead of the multiply, with
+//     one barrier per tile;
+//   * work is scheduled as whole tiles when they fill whole waves of the
+//     2 x 152 resident CTAs, and otherwise as stream-K: the (tile, k-tile)
+//     iterations are cut into one equal contiguous run per resident CTA, runs
+//     that cover part of a tile store a raw partial tile, and a fixup kernel
+//     sums each tile's partials in ascending k order (deterministic);
 //   * products are single-rounded FFMA in fp32, the accumulation order along
 //     K is ascending, and the alpha/beta epilogue is fused into the stores.
 #include <cuda_runtime.h>
@@ -113,107 +119,182 @@ struct TileCopier {
   }
 };
 
+constexpr int STAGES = 3;
+constexpr int STAGE_FLOATS = BK * LDS;                         // one operand, one stage
+constexpr int SMEM_BYTES = 2 * STAGES * STAGE_FLOATS * 4;      // A and B rings: 50,688 bytes
+
+// The k-tile range [ks, ke) of one tile that a CTA accumulates in one go, and
+// where the result goes.
+struct Segment {
+  int64_t tile;
+  int ks, ke;
+  int dest;       // kToC: finished tile; kToSlice: split-K slice; kToSlot: stream-K partial
+  int64_t index;  // slice (kToSlice) or slot (kToSlot)
+};
+enum { kToC = 0, kToSlice = 1, kToSlot = 2 };
+
+// First k-tile iteration of stream-K CTA c: iterations are the (tile, k-tile)
+// pairs in tile-major order, split evenly over the grid.
+__host__ __device__ __forceinline__ int64_t sk_begin(int64_t c, int64_t iters, int64_t grid) {
+  return c * iters / grid;
+}
+
 template <bool TA, bool TB, bool VEC, bool CVEC>
 __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(SimtArgs p) {
-  __shared__ __align__(16) float As[2][BK][LDS];
-  __shared__ __align__(16) float Bs[2][BK][LDS];
+  extern __shared__ __align__(16) float smem[];
+  float (*As)[BK][LDS] = reinterpret_cast<float (*)[BK][LDS]>(smem);
+  float (*Bs)[BK][LDS] = reinterpret_cast<float (*)[BK][LDS]>(smem + STAGES * STAGE_FLOATS);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int wm = warp >> 1, wn = warp & 1;  // 4 x 2 warps
   const int lm = lane >> 3, ln = lane & 7;  // 4 x 8 lanes
-  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BM;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * BN;
+  const int am = wm * 32 + lm * 4;          // A rows of quadrant 0 (quadrant 1: +16)
+  const int bn = wn * 64 + ln * 4;          // B cols of quadrant 0 (quadrant 1: +32)
+  const int64_t tiles_n = (p.N + BN - 1) / BN;
+  const int kt = static_cast<int>((p.K + BK - 1) / BK);  // k-tiles of a whole tile
 
-  const int64_t kbeg = static_cast<int64_t>(blockIdx.z) * p.k_per_split;
-  const int64_t kend = (kbeg + p.k_per_split < p.K) ? kbeg + p.k_per_split : p.K;
-  const int kspan = static_cast<int>(kend - kbeg);  // K elements of this slice (< 2^31)
-  const int ntiles = (kspan + BK - 1) / BK;
-
-  float acc[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-
-  // op(A) is K-contiguous when A is stored M x K (TA == 0); op(B) is
-  // K-contiguous when B is stored N x K (TB == 1).
-  TileCopier<!TA, VEC> ca;
-  TileCopier<TB, VEC> cb;
-  ca.init(p.A, p.lda, m0, p.M, kbeg, tid);
-  cb.init(p.B, p.ldb, n0, p.N, kbeg, tid);
-  if (ntiles > 0) {
-    ca.issue(As[0], kspan, tid, p.A, p.lda);
-    cb.issue(Bs[0], kspan, tid, p.B, p.ldb);
-  }
-  cp_async_commit();
-
-  const int am = wm * 32 + lm * 4;  // A rows of quadrant 0 (quadrant 1: +16)
-  const int bn = wn * 64 + ln * 4;  // B cols of quadrant 0 (quadrant 1: +32)
-
-  for (int t = 0; t < ntiles; ++t) {
-    const int cur = t & 1;
-    if (t + 1 < ntiles) {
-      const int k_rem = kspan - (t + 1) * BK;
-      ca.issue(As[cur ^ 1], k_rem, tid, p.A, p.lda);
-      cb.issue(Bs[cur ^ 1], k_rem, tid, p.B, p.ldb);
-      cp_async_commit();
-      cp_async_wait<1>();  // tile t has landed, tile t+1 may still be in flight
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < BK; ++k) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][am]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][k][am + 16]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][k][bn]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][k][bn + 32]);
-      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();  // every warp is done with buffer `cur` before it is refilled
+  // The CTA's work: one segment (whole tile / split-K slice), or a contiguous
+  // run of stream-K iterations that may span several tiles.
+  int64_t it = 0, it_end = 1, it_first = 0;
+  if (p.schedule == kSimtStreamK) {
+    it_first = it = sk_begin(blockIdx.x, p.iters, p.grid);
+    it_end = sk_begin(blockIdx.x + 1, p.iters, p.grid);
   }
 
-  // Epilogue.  Rows: am + {0..3} and am + 16 + {0..3}; cols: bn + {0..3} and bn + 32 + {0..3}.
-  const bool partial = p.splits > 1;
-  float* __restrict__ out = partial ? p.ws + static_cast<int64_t>(blockIdx.z) * p.M * p.ws_ld : p.C;
-  const int64_t ldo = partial ? p.ws_ld : p.ldc;
-  const bool read_c = !partial && p.beta != 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t row = m0 + am + (i & 3) + (i >> 2) * 16;
-    if (row >= p.M) continue;
-    float* __restrict__ crow = out + row * ldo;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t col = n0 + bn + h * 32;
-      float v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = partial ? acc[i][h * 4 + j] : p.alpha * acc[i][h * 4 + j];
-      // the workspace is always 16-byte aligned with ws_ld % 4 == 0
-      const bool vec = (partial || CVEC) && col + 3 < p.N;
-      if (vec) {
-        float4* dst = reinterpret_cast<float4*>(crow + col);
-        if (read_c) {
-          const float4 c = *dst;
-          v[0] = fmaf(p.beta, c.x, v[0]);
-          v[1] = fmaf(p.beta, c.y, v[1]);
-          v[2] = fmaf(p.beta, c.z, v[2]);
-          v[3] = fmaf(p.beta, c.w, v[3]);
-        }
-        *dst = make_float4(v[0], v[1], v[2], v[3]);
+  while (it < it_end) {
+    Segment sg;
+    if (p.schedule == kSimtStreamK) {
+      sg.tile = it / kt;
+      sg.ks = static_cast<int>(it % kt);
+      const int64_t left = it_end - it;
+      sg.ke = (kt - sg.ks <= left) ? kt : sg.ks + static_cast<int>(left);
+      if (sg.ks == 0 && sg.ke == kt) {
+        sg.dest = kToC;
       } else {
+        sg.dest = kToSlot;
+        sg.index = 2 * static_cast<int64_t>(blockIdx.x) + (it == it_first ? 0 : 1);
+      }
+      it += sg.ke - sg.ks;
+    } else {
+      sg.tile = static_cast<int64_t>(blockIdx.y) * tiles_n + blockIdx.x;
+      if (p.schedule == kSimtSplitK) {
+        const int per = static_cast<int>(p.k_per_split / BK);
+        sg.ks = blockIdx.z * per;
+        sg.ke = (sg.ks + per < kt) ? sg.ks + per : kt;
+        sg.dest = kToSlice;
+        sg.index = blockIdx.z;
+      } else {
+        sg.ks = 0;
+        sg.ke = kt;
+        sg.dest = kToC;
+      }
+      it = it_end;
+    }
+    const int64_t m0 = (sg.tile / tiles_n) * BM;
+    const int64_t n0 = (sg.tile % tiles_n) * BN;
+    const int n = sg.ke - sg.ks;
+
+    float acc[8][8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (col + j < p.N) {
-            float r = v[j];
-            if (read_c) r = fmaf(p.beta, crow[col + j], r);
-            crow[col + j] = r;
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    // op(A) is K-contiguous when A is stored M x K (TA == 0); op(B) is
+    // K-contiguous when B is stored N x K (TB == 1).
+    TileCopier<!TA, VEC> ca;
+    TileCopier<TB, VEC> cb;
+    const int64_t kbeg = static_cast<int64_t>(sg.ks) * BK;
+    ca.init(p.A, p.lda, m0, p.M, kbeg, tid);
+    cb.init(p.B, p.ldb, n0, p.N, kbeg, tid);
+    // Three-stage ring: tiles t+1 and t+2 are in flight while tile t is
+    // multiplied; one barrier per tile both publishes tile t and frees the
+    // stage that tile t+2 overwrites (it held tile t-1).
+#pragma unroll
+    for (int st = 0; st < STAGES - 1; ++st) {
+      if (st < n) {
+        const int k_rem = static_cast<int>(p.K - (kbeg + st * BK));
+        ca.issue(As[st], k_rem, tid, p.A, p.lda);
+        cb.issue(Bs[st], k_rem, tid, p.B, p.ldb);
+      }
+      cp_async_commit();
+    }
+    for (int t = 0; t < n; ++t) {
+      cp_async_wait<STAGES - 2>();
+      __syncthreads();
+      if (t + STAGES - 1 < n) {
+        const int nx = (t + STAGES - 1) % STAGES;
+        const int k_rem = static_cast<int>(p.K - (kbeg + static_cast<int64_t>(t + STAGES - 1) * BK));
+        ca.issue(As[nx], k_rem, tid, p.A, p.lda);
+        cb.issue(Bs[nx], k_rem, tid, p.B, p.ldb);
+      }
+      cp_async_commit();
+      const int cur = t % STAGES;
+#pragma unroll
+      for (int k = 0; k < BK; ++k) {
+        const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][am]);
+        const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][k][am + 16]);
+        const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][k][bn]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][k][bn + 32]);
+        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // the ring is idle before the next segment refills it
+
+    // Epilogue.  Rows am + {0..3}, am + 16 + {0..3}; cols bn + {0..3}, bn + 32 + {0..3}.
+    if (sg.dest == kToSlot) {
+      // A stream-K partial: the raw 128 x 128 tile, rows of 128 floats.
+      float* __restrict__ slot = p.ws + sg.index * (BM * BN);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float* rowp = slot + (am + (i & 3) + (i >> 2) * 16) * BN + bn;
+        *reinterpret_cast<float4*>(rowp) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        *reinterpret_cast<float4*>(rowp + 32) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+      }
+      continue;
+    }
+    const bool partial = sg.dest == kToSlice;
+    float* __restrict__ out = partial ? p.ws + sg.index * p.M * p.ws_ld : p.C;
+    const int64_t ldo = partial ? p.ws_ld : p.ldc;
+    const bool read_c = !partial && p.beta != 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t row = m0 + am + (i & 3) + (i >> 2) * 16;
+      if (row >= p.M) continue;
+      float* __restrict__ crow = out + row * ldo;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t col = n0 + bn + h * 32;
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = partial ? acc[i][h * 4 + j] : p.alpha * acc[i][h * 4 + j];
+        // the workspace is always 16-byte aligned with ws_ld % 4 == 0
+        const bool vec = (partial || CVEC) && col + 3 < p.N;
+        if (vec) {
+          float4* dst = reinterpret_cast<float4*>(crow + col);
+          if (read_c) {
+            const float4 c = *dst;
+            v[0] = fmaf(p.beta, c.x, v[0]);
+            v[1] = fmaf(p.beta, c.y, v[1]);
+            v[2] = fmaf(p.beta, c.z, v[2]);
+            v[3] = fmaf(p.beta, c.w, v[3]);
+          }
+          *dst = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (col + j < p.N) {
+              float r = v[j];
+              if (read_c) r = fmaf(p.beta, crow[col + j], r);
+              crow[col + j] = r;
+            }
           }
         }
       }
@@ -221,12 +302,64 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(SimtArgs p) {
   }
 }
 
+// Stream-K fixup: one CTA per output tile.  A tile that one CTA finished in
+// one segment was stored already; otherwise its partial tiles (one per CTA
+// that touched it, in ascending k order) are summed in that fixed order and
+// the alpha/beta epilogue is applied.
+__global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
+  constexpr int kMaxParts = 512;  // > the 2 x 152 resident CTAs that can share one tile
+  __shared__ int64_t slots[kMaxParts];
+  __shared__ int nparts;
+  const int64_t tile = blockIdx.x;
+  if (threadIdx.x == 0) {
+    const int64_t kt = (p.K + BK - 1) / BK;
+    const int64_t f = tile * kt, l = f + kt - 1;
+    auto owner = [&](int64_t x) {
+      int64_t c = x * p.grid / p.iters;
+      while (c + 1 < p.grid && sk_begin(c + 1, p.iters, p.grid) <= x) ++c;
+      while (c > 0 && sk_begin(c, p.iters, p.grid) > x) --c;
+      return c;
+    };
+    const int64_t cf = owner(f), cl = owner(l);
+    int n = 0;
+    if (cf != cl) {
+      for (int64_t c = cf; c <= cl && n < kMaxParts; ++c)
+        slots[n++] = 2 * c + (sk_begin(c, p.iters, p.grid) >= f ? 0 : 1);
+    }
+    nparts = n;
+  }
+  __syncthreads();
+  const int n = nparts;
+  if (n == 0) return;  // one CTA finished this tile in one segment and stored it
+  const int64_t tiles_n = (p.N + BN - 1) / BN;
+  const int64_t m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
+  for (int e = threadIdx.x; e < BM * BN / 4; e += NT) {
+    const int r = e / (BN / 4), c4 = (e % (BN / 4)) * 4;
+    const int64_t row = m0 + r;
+    if (row >= p.M || n0 + c4 >= p.N) continue;
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < n; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(p.ws + slots[q] * (BM * BN) + r * BN + c4);
+      sum.x += v.x;
+      sum.y += v.y;
+      sum.z += v.z;
+      sum.w += v.w;
+    }
+    float* crow = p.C + row * p.ldc + n0 + c4;
+    const int64_t left = p.N - (n0 + c4);
+    if (left > 0) crow[0] = (p.beta != 0.f) ? fmaf(p.beta, crow[0], p.alpha * sum.x) : p.alpha * sum.x;
+    if (left > 1) crow[1] = (p.beta != 0.f) ? fmaf(p.beta, crow[1], p.alpha * sum.y) : p.alpha * sum.y;
+    if (left > 2) crow[2] = (p.beta != 0.f) ? fmaf(p.beta, crow[2], p.alpha * sum.z) : p.alpha * sum.z;
+    if (left > 3) crow[3] = (p.beta != 0.f) ? fmaf(p.beta, crow[3], p.alpha * sum.w) : p.alpha * sum.w;
+  }
+}
+
 template <bool TA, bool TB, bool VEC>
 cudaError_t launch_cvec(const SimtArgs& a, dim3 grid, cudaStream_t s, bool cvec) {
-  if (cvec)
-    simt_gemm_kernel<TA, TB, VEC, true><<<grid, NT, 0, s>>>(a);
-  else
-    simt_gemm_kernel<TA, TB, VEC, false><<<grid, NT, 0, s>>>(a);
+  auto kern = cvec ? simt_gemm_kernel<TA, TB, VEC, true> : simt_gemm_kernel<TA, TB, VEC, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, NT, SMEM_BYTES, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -239,16 +372,33 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+int64_t simt_streamk_slot_floats() { return static_cast<int64_t>(BM) * BN; }
+
 cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream) {
-  const int64_t gx = (a.N + BN - 1) / BN, gy = (a.M + BM - 1) / BM;
-  if (gy > 65535 || a.splits > 65535) return cudaErrorInvalidConfiguration;
-  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(a.splits));
+  dim3 grid;
+  if (a.schedule == kSimtStreamK) {
+    grid = dim3(static_cast<unsigned>(a.grid));
+  } else {
+    const int64_t gx = (a.N + BN - 1) / BN, gy = (a.M + BM - 1) / BM;
+    if (gy > 65535 || a.splits > 65535) return cudaErrorInvalidConfiguration;
+    grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
+                static_cast<unsigned>(a.schedule == kSimtSplitK ? a.splits : 1));
+  }
   const bool vec = aligned16(a.A) && aligned16(a.B) && (a.lda % 4 == 0) && (a.ldb % 4 == 0);
   const bool cvec = aligned16(a.C) && (a.ldc % 4 == 0);
-  if (!a.transA && !a.transB) return launch_vec<false, false>(a, grid, stream, vec, cvec);
-  if (!a.transA && a.transB) return launch_vec<false, true>(a, grid, stream, vec, cvec);
-  if (a.transA && !a.transB) return launch_vec<true, false>(a, grid, stream, vec, cvec);
-  return launch_vec<true, true>(a, grid, stream, vec, cvec);
+  cudaError_t e;
+  if (!a.transA && !a.transB)
+    e = launch_vec<false, false>(a, grid, stream, vec, cvec);
+  else if (!a.transA && a.transB)
+    e = launch_vec<false, true>(a, grid, stream, vec, cvec);
+  else if (a.transA && !a.transB)
+    e = launch_vec<true, false>(a, grid, stream, vec, cvec);
+  else
+    e = launch_vec<true, true>(a, grid, stream, vec, cvec);
+  if (e != cudaSuccess || a.schedule != kSimtStreamK) return e;
+  const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+  simt_streamk_fixup_kernel<<<static_cast<unsigned>(tiles), NT, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace dgt

@@ -87,7 +87,8 @@ typedef struct {
   int32_t grid;          /* CTAs of the main kernel */
   int32_t kernels;       /* kernels launched by the call */
   int32_t packed;        /* bit 0: A re-packed, bit 1: B re-packed into the workspace */
-  int32_t reserved[7];
+  int32_t schedule;      /* SIMT: 0 one CTA per tile, 1 split-K slices, 2 stream-K */
+  int32_t reserved[6];
 } gemm_plan_t;
 
 /* Create a handle on the current device.  Reads the device properties and

@@ -96,6 +96,17 @@ def test_forced_split_k(h, mode, splits):
     assert 1 < h.plan()["split_k"] <= splits
 
 
+@pytest.mark.parametrize("tA,tB", TRANS)
+@pytest.mark.parametrize("M,N,K", [(1000, 700, 3000), (130, 390, 20000), (4000, 384, 384)])
+def test_fp32_stream_k(h, tA, tB, M, N, K):
+    """FP32 shapes whose tiles do not fill whole waves run as stream-K: runs
+    of k-tiles that end mid-tile, partial tiles summed by the fixup kernel."""
+    rows = _cases.sample_rows(M) if M * N * K > 2e9 else None
+    _cases.run_and_check(h, "fp32", M, N, K, tA, tB, alpha=0.5, beta=0.75, seed=61, dist="normal", rows=rows)
+    assert h.plan()["schedule"] == "stream_k"
+    _cases.run_and_check(h, "fp32", M, N, min(K, 1024), tA, tB, seed=62, dist="int", exact=True)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_many_tiles_persistent_loop(h, mode):
     # More tiles than SMs: every CTA of the persistent grid loops over several
