@@ -423,6 +423,8 @@ def bench_sweep(args):
     torch.cuda.set_device(dev)
     dg.load(build_if_missing=True)
     h = dg.Gemm()
+    if args.tile_n:
+        h.set_option("tile_n", args.tile_n)
     stream = torch.cuda.Stream(dev)
     pk = peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -505,6 +507,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-macs", type=float, default=3e9, help="oracle multiply-adds in the CPU baseline")
     ap.add_argument("--ref-macs", type=float, default=3e8, help="oracle multiply-adds per reference step")
+    ap.add_argument("--tile-n", type=int, default=0, help="sweeps: force the tensor-core tile width (128/256)")
     ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
     ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny"],
                     help="gpt: the timed step; the others print a per-shape sweep")

@@ -306,11 +306,16 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(SimtArgs p) {
 // one segment was stored already; otherwise its partial tiles (one per CTA
 // that touched it, in ascending k order) are summed in that fixed order and
 // the alpha/beta epilogue is applied.
+// Each tile's 128 rows are shared by kFixupChunks CTAs so that tiles summed
+// from many partials (deep K, few tiles) still spread over the SMs.
+constexpr int kFixupChunks = 16;
+
 __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
   constexpr int kMaxParts = 512;  // > the 2 x 152 resident CTAs that can share one tile
   __shared__ int64_t slots[kMaxParts];
   __shared__ int nparts;
-  const int64_t tile = blockIdx.x;
+  const int64_t tile = blockIdx.x / kFixupChunks;
+  const int chunk = blockIdx.x % kFixupChunks;
   if (threadIdx.x == 0) {
     const int64_t kt = (p.K + BK - 1) / BK;
     const int64_t f = tile * kt, l = f + kt - 1;
@@ -333,7 +338,8 @@ __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
   if (n == 0) return;  // one CTA finished this tile in one segment and stored it
   const int64_t tiles_n = (p.N + BN - 1) / BN;
   const int64_t m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
-  for (int e = threadIdx.x; e < BM * BN / 4; e += NT) {
+  constexpr int kChunkVec = BM * BN / 4 / kFixupChunks;  // float4 groups per chunk
+  for (int e = chunk * kChunkVec + threadIdx.x; e < (chunk + 1) * kChunkVec; e += NT) {
     const int r = e / (BN / 4), c4 = (e % (BN / 4)) * 4;
     const int64_t row = m0 + r;
     if (row >= p.M || n0 + c4 >= p.N) continue;
@@ -397,7 +403,7 @@ cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream) {
     e = launch_vec<true, true>(a, grid, stream, vec, cvec);
   if (e != cudaSuccess || a.schedule != kSimtStreamK) return e;
   const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
-  simt_streamk_fixup_kernel<<<static_cast<unsigned>(tiles), NT, 0, stream>>>(a);
+  simt_streamk_fixup_kernel<<<static_cast<unsigned>(tiles * kFixupChunks), NT, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
