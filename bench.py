@@ -253,6 +253,8 @@ def bench_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     dg.load(build_if_missing=True)
     h = dg.Gemm()
+    if args.tile_n:
+        h.set_option("tile_n", args.tile_n)
     stream = torch.cuda.Stream(dev)
     calls, host_inputs, dev_inputs = gpt_workload(dev)
     if args.only:
@@ -430,6 +432,10 @@ def bench_sweep(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     shapes = []
     for label, mode, c, alpha, beta, wstd in sweep_cases(args.workload):
+        if args.only:
+            import re
+            if not re.fullmatch(args.only, label):
+                continue
         dt = torch.bfloat16 if mode == "bf16" else torch.float32
         es = 2 if mode == "bf16" else 4
         per_set = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N

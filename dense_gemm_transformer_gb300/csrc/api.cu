@@ -3,13 +3,13 @@
 //
 // The planner maps a call to one kernel family with a fixed rule (no runtime
 // autotuning):
-//   FP32             -> the register-tiled SIMT kernel, one CTA per 128 x 128
-//                       tile when the tiles fill whole waves of the two CTAs
-//                       per SM it keeps resident (>= 92%), stream-K over the
-//                       resident CTAs otherwise.
+//   FP32             -> the register-tiled SIMT kernel with 128 x 128 or
+//                       128 x 256 tiles, one CTA per tile when the tiles fill
+//                       whole waves of the resident CTAs (>= 92%), stream-K
+//                       over the resident CTAs otherwise.
 //   TF32, BF16       -> the persistent tcgen05 kernel; the tile width (128 or
-//                       256 columns) is the one that wastes the least work
-//                       over whole waves of one tile per SM, and K is split
+//                       256 columns) is the one with the least time over
+//                       whole waves of one tile per SM, and K is split
 //                       when there are fewer tiles than half the SMs.
 //   M <= 16, A M x K -> the same kernel in its swapped form (C^T = B^T A^T):
 //                       the weights stream once through the 128-row MMA side,
@@ -105,13 +105,38 @@ void set_plan(gemm_handle_s* h, int family, int tm, int tn, int tk, int splits, 
   h->plan = p;
 }
 
+// Whole-tile schedule efficiency: the fraction of the resident CTA slots the
+// tiles keep busy over their waves.
+double wave_eff(int64_t tiles, int64_t slots) {
+  return static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, slots) * slots);
+}
+
 gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                        const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
                        cudaStream_t s) {
   using namespace dgt;
-  const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, kSimtTileN);
   const int64_t kt = ceil_div(K, kSimtTileK);
-  const int64_t slots = 2 * static_cast<int64_t>(h->sms);  // resident CTAs (two per SM)
+  // Tile width: 256 columns halve the shared-memory reads per FFMA but leave
+  // one CTA per SM and pad N to a multiple of 256.  Estimated time = padded
+  // work / (schedule efficiency x relative speed), with stream-K counted at
+  // 0.93 (its fixup) and the 128-column kernel at 0.85 of the 256 one.
+  int tile_n = (h->opt_tile_n == 128 || h->opt_tile_n == 256) ? h->opt_tile_n : 0;
+  if (tile_n == 0) {
+    double best = 0.0;
+    for (int tn : {256, 128}) {
+      const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, tn);
+      const int64_t slots = (tn == 256 ? 1 : 2) * static_cast<int64_t>(h->sms);
+      const double e = wave_eff(tiles, slots);
+      const double sched = (e >= 0.92) ? e : 0.93;
+      const double t = static_cast<double>(tiles * tn) / (sched * (tn == 256 ? 1.0 : 0.85));
+      if (tile_n == 0 || t < best) {
+        best = t;
+        tile_n = tn;
+      }
+    }
+  }
+  const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, tile_n);
+  const int64_t slots = (tile_n == 256 ? 1 : 2) * static_cast<int64_t>(h->sms);  // resident CTAs
   SimtArgs a{};
   a.transA = transA;
   a.transB = transB;
@@ -126,6 +151,7 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   a.ldc = ldc;
   a.alpha = alpha;
   a.beta = beta;
+  a.tile_n = tile_n;
   a.ws_ld = round_up(N, 4);
   a.splits = 1;
   a.k_per_split = K;
@@ -133,7 +159,6 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   int kernels = 1;
   // Whole tiles when they fill whole waves of the resident CTAs (or the
   // problem is too small to share out); stream-K otherwise.
-  const double wave_eff = static_cast<double>(tiles) / (ceil_div(tiles, slots) * slots);
   if (h->opt_split_k > 0) {
     int64_t splits = h->opt_split_k;
     const int64_t kps = round_up(ceil_div(K, splits), kSimtTileK);
@@ -142,7 +167,7 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
     a.splits = static_cast<int>(splits);
     a.k_per_split = kps;
     grid = static_cast<int>(tiles * splits);
-  } else if (wave_eff >= 0.92 || tiles * kt < 4 * slots) {
+  } else if (wave_eff(tiles, slots) >= 0.92 || tiles * kt < 4 * slots) {
     a.schedule = kSimtTiles;
   } else {
     a.schedule = kSimtStreamK;
@@ -156,7 +181,8 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
     if (st != GEMM_OK) return st;
     a.ws = static_cast<float*>(h->ws);
   } else if (a.schedule == kSimtStreamK) {
-    gemm_status_t st = ensure_ws(h, static_cast<size_t>(2 * a.grid * simt_streamk_slot_floats()) * sizeof(float));
+    gemm_status_t st =
+        ensure_ws(h, static_cast<size_t>(2 * a.grid * simt_streamk_slot_floats(tile_n)) * sizeof(float));
     if (st != GEMM_OK) return st;
     a.ws = static_cast<float*>(h->ws);
     ++kernels;  // the fixup
@@ -168,7 +194,7 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
       return GEMM_ERR_CUDA;
     ++kernels;
   }
-  set_plan(h, GEMM_FAMILY_SIMT, kSimtTileM, kSimtTileN, kSimtTileK, a.splits, 3, grid, kernels, 0);
+  set_plan(h, GEMM_FAMILY_SIMT, kSimtTileM, tile_n, kSimtTileK, a.splits, tile_n == 256 ? 4 : 3, grid, kernels, 0);
   h->plan.schedule = a.schedule;
   return GEMM_OK;
 }
@@ -245,19 +271,16 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   const void* Bk = swap ? A : B;
   const int64_t ldak = swap ? ldb : lda, ldbk = swap ? lda : ldb;
 
-  // Tile width: the fewest padded columns over whole waves of one tile per SM.
+  // Tile width: the least time over whole waves of one tile per SM, where a
+  // 128-column tile runs at 3/4 the speed per column of a 256-column one (it
+  // stages twice the shared-memory operand bytes per MMA flop; measured on
+  // square and large shapes).  Ties go to 256.
   int tile_n = swap ? 16 : h->opt_tile_n;
   if (tile_n != 128 && tile_n != 256 && tile_n != 16) {
     const int64_t tm = ceil_div(Mk, 128);
-    int64_t best = -1;
-    for (int bn : {256, 128}) {
-      const int64_t waves = ceil_div(tm * ceil_div(Nk, bn), sms);
-      const int64_t cost = waves * bn;
-      if (best < 0 || cost < best) {
-        best = cost;
-        tile_n = bn;
-      }
-    }
+    const double cost256 = static_cast<double>(ceil_div(tm * ceil_div(Nk, 256), sms)) * 256.0;
+    const double cost128 = static_cast<double>(ceil_div(tm * ceil_div(Nk, 128), sms)) * 128.0 / 0.75;
+    tile_n = (cost128 < cost256) ? 128 : 256;
   }
   const int64_t tiles = ceil_div(Mk, 128) * ceil_div(Nk, tile_n);
   const int64_t kb = ceil_div(K, bk);

@@ -8,15 +8,15 @@
 namespace dgt {
 
 // ---------------------------------------------------------------- FP32 SIMT
-// C = alpha * op(A) op(B) + beta * C with FFMA, 128 x 128 block tiles, in one
-// of three schedules:
+// C = alpha * op(A) op(B) + beta * C with FFMA, 128 x tile_n block tiles
+// (tile_n 128: two CTAs per SM; 256: one), in one of three schedules:
 //   kSimtTiles   one CTA per output tile (2-D grid);
 //   kSimtSplitK  one CTA per (tile, K slice); slice s (k_per_split elements, a
 //                multiple of 16) writes raw partial sums to ws + s * M * ws_ld
 //                and launch_splitk_reduce finishes;
 //   kSimtStreamK `grid` persistent CTAs share the `iters` (tile, k-tile)
 //                iterations evenly; partial tiles go to 2 * grid slots of
-//                128 x 128 floats at ws, and launch_simt also launches the
+//                128 x tile_n floats at ws, and launch_simt also launches the
 //                fixup kernel that sums them in a fixed order.
 enum { kSimtTiles = 0, kSimtSplitK = 1, kSimtStreamK = 2 };
 struct SimtArgs {
@@ -29,6 +29,7 @@ struct SimtArgs {
   float* C;
   int64_t ldc;
   float alpha, beta;
+  int tile_n;
   int schedule;
   int splits;
   int64_t k_per_split;
@@ -38,7 +39,7 @@ struct SimtArgs {
   int64_t ws_ld;
 };
 constexpr int kSimtTileM = 128, kSimtTileN = 128, kSimtTileK = 16, kSimtThreads = 256;
-int64_t simt_streamk_slot_floats();  // floats per stream-K partial slot
+int64_t simt_streamk_slot_floats(int tile_n);  // floats per stream-K partial slot
 cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tcgen05

@@ -4,21 +4,24 @@
 // thread per output to coalesced loads, shared-memory tiling, register
 // tiling, float4 loads, warp-level blocking and double buffering.  This is
 // that end point, re-sized for a 152-SM part with 64K registers per SM:
-//   * a 128 x 128 block tile, BK = 16, 256 threads, two CTAs per SM;
-//   * warps tile the block 4 (M) x 2 (N) with 32 x 64 warp tiles, lanes tile a
-//     warp 4 x 8, and every thread owns an 8 x 8 register tile split into
-//     four 4 x 4 quadrants so each of its shared-memory reads is one float4
-//     that the lanes sharing a row or column receive by broadcast;
-//   * A is stored k-major in shared memory (transposed on the way in when the
-//     operand is stored M x K) so both operands are read as float4 along M / N;
+//   * a 128 x TBN block tile (TBN = 128: two CTAs per SM, 8 x 8 outputs per
+//     thread; TBN = 256: one CTA per SM, 8 x 16 outputs per thread, which
+//     halves the shared-memory reads per FFMA), BK = 16, 256 threads;
+//   * warps tile the block 4 (M) x 2 (N), lanes tile a warp 4 x 8, and every
+//     thread's register tile is split into 4 x 4 quadrants so each of its
+//     shared-memory reads is one float4 that the lanes sharing a row or column
+//     receive by broadcast;
+//   * both operands sit k-major in shared memory (a K-contiguous operand is
+//     transposed on the way in) so they are read as float4 along M / N;
 //   * K tiles are copied global -> shared with cp.async (no register
-//     staging) into a three-stage ring, two tiles ahead of the multiply, with
-//     one barrier per tile;
+//     staging) into a ring of 3 (TBN = 128) or 4 (TBN = 256) stages, with one
+//     barrier per tile; with TBN = 256 the register fragments of step k+1 are
+//     loaded while step k is multiplied;
 //   * work is scheduled as whole tiles when they fill whole waves of the
-//     2 x 152 resident CTAs, and otherwise as stream-K: the (tile, k-tile)
-//     iterations are cut into one equal contiguous run per resident CTA, runs
-//     that cover part of a tile store a raw partial tile, and a fixup kernel
-//     sums each tile's partials in ascending k order (deterministic);
+//     resident CTAs, and otherwise as stream-K: the (tile, k-tile) iterations
+//     are cut into one equal contiguous run per resident CTA, runs that cover
+//     part of a tile store a raw partial tile, and a fixup kernel sums each
+//     tile's partials in ascending k order (deterministic);
 //   * products are single-rounded FFMA in fp32, the accumulation order along
 //     K is ascending, and the alpha/beta epilogue is fused into the stores.
 #include <cuda_runtime.h>
@@ -28,9 +31,22 @@
 namespace dgt {
 namespace {
 
-constexpr int BM = kSimtTileM, BN = kSimtTileN, BK = kSimtTileK, NT = kSimtThreads;
+constexpr int BM = kSimtTileM, BK = kSimtTileK, NT = kSimtThreads;
 constexpr int PAD = 4;  // keeps rows 16-byte aligned and staggers the transposed copies across banks
-constexpr int LDS = BM + PAD;
+
+template <int TBN>
+struct SimtCfg {
+  static constexpr int LDA = BM + PAD;
+  static constexpr int LDB = TBN + PAD;
+  static constexpr int STAGES = (TBN == 256) ? 4 : 3;
+  static constexpr int MIN_BLOCKS = (TBN == 256) ? 1 : 2;
+  static constexpr int TN = TBN / 16;  // outputs per thread along N
+  static constexpr int QN = TN / 4;    // float4 quadrants along N
+  static constexpr int A_STAGE = BK * LDA;
+  static constexpr int B_STAGE = BK * LDB;
+  static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+  static constexpr bool PREFETCH_FRAGMENTS = (TBN == 256);  // registers allow it at one CTA per SM
+};
 
 // cp.async copies global -> shared without staging in registers.  A source
 // size of 0 copies nothing and fills the destination with zeros, which is how
@@ -52,25 +68,27 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Copies successive K tiles of a 128-wide operand into s[k][mn], keeping only
-// two running source pointers per thread.
+// Copies successive K tiles of a ROWS-wide operand into s[k * LD + mn],
+// keeping only a few running source pointers per thread.
 // K_CONTIG: the operand is stored with K contiguous (A as M x K, or B as N x K);
 // each element lands transposed, so it is copied 4 bytes at a time (thread ->
-// rows tid/4 and tid/4 + 64, k quad (tid%4)*4).  Otherwise the rows of the
-// tile are contiguous in memory and are copied 16 bytes at a time when aligned
-// (thread -> k rows tid/32 and tid/32 + 8, quad (tid%32)*4).
-template <bool K_CONTIG, bool VEC>
+// rows tid/4 + 64h, k quad (tid%4)*4).  Otherwise the rows of the tile are
+// contiguous in memory and are copied 16 bytes at a time when aligned
+// (thread -> k rows tid/32 and tid/32 + 8, quads (tid%32)*4 + 128g).
+template <bool K_CONTIG, bool VEC, int ROWS, int LD>
 struct TileCopier {
-  const float* ptr[2];
-  int avail;  // columns of this thread's quad inside the matrix (non-K_CONTIG)
-  bool row_ok[2];
+  static constexpr int H = K_CONTIG ? ROWS / 64 : 2;
+  static constexpr int G = K_CONTIG ? 1 : ROWS / 128;
+  const float* ptr[H];
+  int avail[G];  // columns of each quad inside the matrix (non-K_CONTIG)
+  bool row_ok[H];
 
   __device__ __forceinline__ void init(const float* __restrict__ base, int64_t ld, int64_t mn0, int64_t lim,
                                        int64_t kbeg, int tid) {
     if (K_CONTIG) {
       const int row = tid >> 2, kq = (tid & 3) * 4;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < H; ++h) {
         const int64_t r = mn0 + row + 64 * h;
         row_ok[h] = r < lim;
         ptr[h] = base + (row_ok[h] ? r : 0) * ld + kbeg + kq;
@@ -78,39 +96,47 @@ struct TileCopier {
     } else {
       const int kr = tid >> 5, q = (tid & 31) * 4;
       const int64_t mn = mn0 + q;
-      const int64_t left = lim - mn;
-      avail = left <= 0 ? 0 : (left >= 4 ? 4 : static_cast<int>(left));
 #pragma unroll
-      for (int h = 0; h < 2; ++h) ptr[h] = base + (kbeg + kr + 8 * h) * ld + mn;
+      for (int g = 0; g < G; ++g) {
+        const int64_t left = lim - (mn + 128 * g);
+        avail[g] = left <= 0 ? 0 : (left >= 4 ? 4 : static_cast<int>(left));
+      }
+#pragma unroll
+      for (int h = 0; h < H; ++h) ptr[h] = base + (kbeg + kr + 8 * h) * ld + mn;
     }
   }
 
   // k_rem: how many K indices of this tile exist (>= BK except at the tail).
   // safe: any valid address, handed to copies of size 0; ld: leading dimension.
-  __device__ __forceinline__ void issue(float (*s)[LDS], int k_rem, int tid, const float* safe, int64_t ld) {
+  __device__ __forceinline__ void issue(float* s, int k_rem, int tid, const float* safe, int64_t ld) {
     if (K_CONTIG) {
       const int row = tid >> 2, kq = (tid & 3) * 4;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < H; ++h) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const bool ok = row_ok[h] && kq + j < k_rem;
-          cp_async4(&s[kq + j][row + 64 * h], ok ? ptr[h] + j : safe, ok);
+          cp_async4(s + (kq + j) * LD + row + 64 * h, ok ? ptr[h] + j : safe, ok);
         }
         ptr[h] += BK;
       }
     } else {
       const int kr = tid >> 5, q = (tid & 31) * 4;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < H; ++h) {
         const bool k_ok = kr + 8 * h < k_rem;
-        if (VEC && avail == 4) {
-          cp_async16(&s[kr + 8 * h][q], k_ok ? ptr[h] : safe, k_ok);
-        } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const bool ok = k_ok && j < avail;
-            cp_async4(&s[kr + 8 * h][q + j], ok ? ptr[h] + j : safe, ok);
+        for (int g = 0; g < G; ++g) {
+          float* d = s + (kr + 8 * h) * LD + q + 128 * g;
+          const float* src = ptr[h] + 128 * g;
+          if (VEC && avail[g] == 4) {
+            cp_async16(d, k_ok ? src : safe, k_ok);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const bool ok = k_ok && j < avail[g];
+              cp_async4(d + j, ok ? src + j : safe, ok);
+            }
           }
         }
         ptr[h] += BK * ld;
@@ -118,10 +144,6 @@ struct TileCopier {
     }
   }
 };
-
-constexpr int STAGES = 3;
-constexpr int STAGE_FLOATS = BK * LDS;                         // one operand, one stage
-constexpr int SMEM_BYTES = 2 * STAGES * STAGE_FLOATS * 4;      // A and B rings: 50,688 bytes
 
 // The k-tile range [ks, ke) of one tile that a CTA accumulates in one go, and
 // where the result goes.
@@ -139,19 +161,21 @@ __host__ __device__ __forceinline__ int64_t sk_begin(int64_t c, int64_t iters, i
   return c * iters / grid;
 }
 
-template <bool TA, bool TB, bool VEC, bool CVEC>
-__global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(SimtArgs p) {
+template <int TBN, bool TA, bool TB, bool VEC, bool CVEC>
+__global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel(SimtArgs p) {
+  using Cfg = SimtCfg<TBN>;
+  constexpr int S = Cfg::STAGES, TN = Cfg::TN, QN = Cfg::QN, LDA = Cfg::LDA, LDB = Cfg::LDB;
   extern __shared__ __align__(16) float smem[];
-  float (*As)[BK][LDS] = reinterpret_cast<float (*)[BK][LDS]>(smem);
-  float (*Bs)[BK][LDS] = reinterpret_cast<float (*)[BK][LDS]>(smem + STAGES * STAGE_FLOATS);
+  float* As = smem;                      // [S][BK][LDA]
+  float* Bs = smem + S * Cfg::A_STAGE;   // [S][BK][LDB]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int wm = warp >> 1, wn = warp & 1;  // 4 x 2 warps
   const int lm = lane >> 3, ln = lane & 7;  // 4 x 8 lanes
   const int am = wm * 32 + lm * 4;          // A rows of quadrant 0 (quadrant 1: +16)
-  const int bn = wn * 64 + ln * 4;          // B cols of quadrant 0 (quadrant 1: +32)
-  const int64_t tiles_n = (p.N + BN - 1) / BN;
+  const int bn = wn * (TBN / 2) + ln * 4;   // B cols of quadrant 0 (quadrant q: +32q)
+  const int64_t tiles_n = (p.N + TBN - 1) / TBN;
   const int kt = static_cast<int>((p.K + BK - 1) / BK);  // k-tiles of a whole tile
 
   // The CTA's work: one segment (whole tile / split-K slice), or a contiguous
@@ -192,71 +216,116 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(SimtArgs p) {
       it = it_end;
     }
     const int64_t m0 = (sg.tile / tiles_n) * BM;
-    const int64_t n0 = (sg.tile % tiles_n) * BN;
+    const int64_t n0 = (sg.tile % tiles_n) * TBN;
     const int n = sg.ke - sg.ks;
 
-    float acc[8][8];
+    float acc[8][TN];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+      for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
     // op(A) is K-contiguous when A is stored M x K (TA == 0); op(B) is
     // K-contiguous when B is stored N x K (TB == 1).
-    TileCopier<!TA, VEC> ca;
-    TileCopier<TB, VEC> cb;
+    TileCopier<!TA, VEC, BM, LDA> ca;
+    TileCopier<TB, VEC, TBN, LDB> cb;
     const int64_t kbeg = static_cast<int64_t>(sg.ks) * BK;
     ca.init(p.A, p.lda, m0, p.M, kbeg, tid);
     cb.init(p.B, p.ldb, n0, p.N, kbeg, tid);
-    // Three-stage ring: tiles t+1 and t+2 are in flight while tile t is
-    // multiplied; one barrier per tile both publishes tile t and frees the
-    // stage that tile t+2 overwrites (it held tile t-1).
+    // The ring: tiles t+1 .. t+S-1 are in flight while tile t is multiplied;
+    // one barrier per tile both publishes tile t and frees the stage that
+    // tile t+S-1 overwrites (it held tile t-1).
 #pragma unroll
-    for (int st = 0; st < STAGES - 1; ++st) {
+    for (int st = 0; st < S - 1; ++st) {
       if (st < n) {
         const int k_rem = static_cast<int>(p.K - (kbeg + st * BK));
-        ca.issue(As[st], k_rem, tid, p.A, p.lda);
-        cb.issue(Bs[st], k_rem, tid, p.B, p.ldb);
+        ca.issue(As + st * Cfg::A_STAGE, k_rem, tid, p.A, p.lda);
+        cb.issue(Bs + st * Cfg::B_STAGE, k_rem, tid, p.B, p.ldb);
       }
       cp_async_commit();
     }
     for (int t = 0; t < n; ++t) {
-      cp_async_wait<STAGES - 2>();
+      cp_async_wait<S - 2>();
       __syncthreads();
-      if (t + STAGES - 1 < n) {
-        const int nx = (t + STAGES - 1) % STAGES;
-        const int k_rem = static_cast<int>(p.K - (kbeg + static_cast<int64_t>(t + STAGES - 1) * BK));
-        ca.issue(As[nx], k_rem, tid, p.A, p.lda);
-        cb.issue(Bs[nx], k_rem, tid, p.B, p.ldb);
+      if (t + S - 1 < n) {
+        const int nx = (t + S - 1) % S;
+        const int k_rem = static_cast<int>(p.K - (kbeg + static_cast<int64_t>(t + S - 1) * BK));
+        ca.issue(As + nx * Cfg::A_STAGE, k_rem, tid, p.A, p.lda);
+        cb.issue(Bs + nx * Cfg::B_STAGE, k_rem, tid, p.B, p.ldb);
       }
       cp_async_commit();
-      const int cur = t % STAGES;
+      const float* a_s = As + (t % S) * Cfg::A_STAGE;
+      const float* b_s = Bs + (t % S) * Cfg::B_STAGE;
+      if constexpr (Cfg::PREFETCH_FRAGMENTS) {
+        float af[2][8], bf[2][TN];
+        auto load = [&](int k, int buf) {
 #pragma unroll
-      for (int k = 0; k < BK; ++k) {
-        const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][am]);
-        const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][k][am + 16]);
-        const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][k][bn]);
-        const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][k][bn + 32]);
-        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+          for (int r = 0; r < 2; ++r) {
+            const float4 v = *reinterpret_cast<const float4*>(a_s + k * LDA + am + 16 * r);
+            af[buf][4 * r + 0] = v.x;
+            af[buf][4 * r + 1] = v.y;
+            af[buf][4 * r + 2] = v.z;
+            af[buf][4 * r + 3] = v.w;
+          }
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+          for (int q = 0; q < QN; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(b_s + k * LDB + bn + 32 * q);
+            bf[buf][4 * q + 0] = v.x;
+            bf[buf][4 * q + 1] = v.y;
+            bf[buf][4 * q + 2] = v.z;
+            bf[buf][4 * q + 3] = v.w;
+          }
+        };
+        load(0, 0);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int k = 0; k < BK; ++k) {
+          if (k + 1 < BK) load(k + 1, (k + 1) & 1);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(af[k & 1][i], bf[k & 1][j], acc[i][j]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < BK; ++k) {
+          float a[8], b[TN];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float4 v = *reinterpret_cast<const float4*>(a_s + k * LDA + am + 16 * r);
+            a[4 * r + 0] = v.x;
+            a[4 * r + 1] = v.y;
+            a[4 * r + 2] = v.z;
+            a[4 * r + 3] = v.w;
+          }
+#pragma unroll
+          for (int q = 0; q < QN; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(b_s + k * LDB + bn + 32 * q);
+            b[4 * q + 0] = v.x;
+            b[4 * q + 1] = v.y;
+            b[4 * q + 2] = v.z;
+            b[4 * q + 3] = v.w;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
       }
     }
     cp_async_wait<0>();
     __syncthreads();  // the ring is idle before the next segment refills it
 
-    // Epilogue.  Rows am + {0..3}, am + 16 + {0..3}; cols bn + {0..3}, bn + 32 + {0..3}.
+    // Epilogue.  Rows am + {0..3}, am + 16 + {0..3}; cols bn + 32q + {0..3}.
     if (sg.dest == kToSlot) {
-      // A stream-K partial: the raw 128 x 128 tile, rows of 128 floats.
-      float* __restrict__ slot = p.ws + sg.index * (BM * BN);
+      // A stream-K partial: the raw 128 x TBN tile, rows of TBN floats.
+      float* __restrict__ slot = p.ws + sg.index * (BM * TBN);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        float* rowp = slot + (am + (i & 3) + (i >> 2) * 16) * BN + bn;
-        *reinterpret_cast<float4*>(rowp) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        *reinterpret_cast<float4*>(rowp + 32) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+        float* rowp = slot + (am + (i & 3) + (i >> 2) * 16) * TBN + bn;
+#pragma unroll
+        for (int q = 0; q < QN; ++q)
+          *reinterpret_cast<float4*>(rowp + 32 * q) =
+              make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
       }
       continue;
     }
@@ -270,11 +339,11 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(SimtArgs p) {
       if (row >= p.M) continue;
       float* __restrict__ crow = out + row * ldo;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t col = n0 + bn + h * 32;
+      for (int q = 0; q < QN; ++q) {
+        const int64_t col = n0 + bn + 32 * q;
         float v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = partial ? acc[i][h * 4 + j] : p.alpha * acc[i][h * 4 + j];
+        for (int j = 0; j < 4; ++j) v[j] = partial ? acc[i][4 * q + j] : p.alpha * acc[i][4 * q + j];
         // the workspace is always 16-byte aligned with ws_ld % 4 == 0
         const bool vec = (partial || CVEC) && col + 3 < p.N;
         if (vec) {
@@ -302,16 +371,16 @@ __global__ void __launch_bounds__(NT, 2) simt_gemm_kernel(SimtArgs p) {
   }
 }
 
-// Stream-K fixup: one CTA per output tile.  A tile that one CTA finished in
-// one segment was stored already; otherwise its partial tiles (one per CTA
-// that touched it, in ascending k order) are summed in that fixed order and
-// the alpha/beta epilogue is applied.
-// Each tile's 128 rows are shared by kFixupChunks CTAs so that tiles summed
-// from many partials (deep K, few tiles) still spread over the SMs.
+// Stream-K fixup: each output tile is handled by kFixupChunks CTAs (so that
+// tiles summed from many partials -- deep K, few tiles -- still spread over
+// the SMs).  A tile that one CTA finished in one segment was stored already;
+// otherwise its partial tiles (one per CTA that touched it, in ascending k
+// order) are summed in that fixed order and the alpha/beta epilogue applied.
 constexpr int kFixupChunks = 16;
 
+template <int TBN>
 __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
-  constexpr int kMaxParts = 512;  // > the 2 x 152 resident CTAs that can share one tile
+  constexpr int kMaxParts = 512;  // > the most resident CTAs that can share one tile
   __shared__ int64_t slots[kMaxParts];
   __shared__ int nparts;
   const int64_t tile = blockIdx.x / kFixupChunks;
@@ -336,16 +405,16 @@ __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
   __syncthreads();
   const int n = nparts;
   if (n == 0) return;  // one CTA finished this tile in one segment and stored it
-  const int64_t tiles_n = (p.N + BN - 1) / BN;
-  const int64_t m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * BN;
-  constexpr int kChunkVec = BM * BN / 4 / kFixupChunks;  // float4 groups per chunk
+  const int64_t tiles_n = (p.N + TBN - 1) / TBN;
+  const int64_t m0 = (tile / tiles_n) * BM, n0 = (tile % tiles_n) * TBN;
+  constexpr int kChunkVec = BM * TBN / 4 / kFixupChunks;  // float4 groups per chunk
   for (int e = chunk * kChunkVec + threadIdx.x; e < (chunk + 1) * kChunkVec; e += NT) {
-    const int r = e / (BN / 4), c4 = (e % (BN / 4)) * 4;
+    const int r = e / (TBN / 4), c4 = (e % (TBN / 4)) * 4;
     const int64_t row = m0 + r;
     if (row >= p.M || n0 + c4 >= p.N) continue;
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int q = 0; q < n; ++q) {
-      const float4 v = *reinterpret_cast<const float4*>(p.ws + slots[q] * (BM * BN) + r * BN + c4);
+      const float4 v = *reinterpret_cast<const float4*>(p.ws + slots[q] * (BM * TBN) + r * TBN + c4);
       sum.x += v.x;
       sum.y += v.y;
       sum.z += v.z;
@@ -360,51 +429,58 @@ __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
   }
 }
 
-template <bool TA, bool TB, bool VEC>
+template <int TBN, bool TA, bool TB, bool VEC>
 cudaError_t launch_cvec(const SimtArgs& a, dim3 grid, cudaStream_t s, bool cvec) {
-  auto kern = cvec ? simt_gemm_kernel<TA, TB, VEC, true> : simt_gemm_kernel<TA, TB, VEC, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  constexpr int smem = SimtCfg<TBN>::SMEM_BYTES;
+  auto kern = cvec ? simt_gemm_kernel<TBN, TA, TB, VEC, true> : simt_gemm_kernel<TBN, TA, TB, VEC, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, NT, SMEM_BYTES, s>>>(a);
+  kern<<<grid, NT, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-template <bool TA, bool TB>
+template <int TBN, bool TA, bool TB>
 cudaError_t launch_vec(const SimtArgs& a, dim3 grid, cudaStream_t s, bool vec, bool cvec) {
-  return vec ? launch_cvec<TA, TB, true>(a, grid, s, cvec) : launch_cvec<TA, TB, false>(a, grid, s, cvec);
+  return vec ? launch_cvec<TBN, TA, TB, true>(a, grid, s, cvec) : launch_cvec<TBN, TA, TB, false>(a, grid, s, cvec);
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-}  // namespace
-
-int64_t simt_streamk_slot_floats() { return static_cast<int64_t>(BM) * BN; }
-
-cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream) {
+template <int TBN>
+cudaError_t launch_tbn(const SimtArgs& a, cudaStream_t stream) {
   dim3 grid;
   if (a.schedule == kSimtStreamK) {
     grid = dim3(static_cast<unsigned>(a.grid));
   } else {
-    const int64_t gx = (a.N + BN - 1) / BN, gy = (a.M + BM - 1) / BM;
+    const int64_t gx = (a.N + TBN - 1) / TBN, gy = (a.M + BM - 1) / BM;
     if (gy > 65535 || a.splits > 65535) return cudaErrorInvalidConfiguration;
     grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
                 static_cast<unsigned>(a.schedule == kSimtSplitK ? a.splits : 1));
   }
+  const auto aligned16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
   const bool vec = aligned16(a.A) && aligned16(a.B) && (a.lda % 4 == 0) && (a.ldb % 4 == 0);
   const bool cvec = aligned16(a.C) && (a.ldc % 4 == 0);
   cudaError_t e;
   if (!a.transA && !a.transB)
-    e = launch_vec<false, false>(a, grid, stream, vec, cvec);
+    e = launch_vec<TBN, false, false>(a, grid, stream, vec, cvec);
   else if (!a.transA && a.transB)
-    e = launch_vec<false, true>(a, grid, stream, vec, cvec);
+    e = launch_vec<TBN, false, true>(a, grid, stream, vec, cvec);
   else if (a.transA && !a.transB)
-    e = launch_vec<true, false>(a, grid, stream, vec, cvec);
+    e = launch_vec<TBN, true, false>(a, grid, stream, vec, cvec);
   else
-    e = launch_vec<true, true>(a, grid, stream, vec, cvec);
+    e = launch_vec<TBN, true, true>(a, grid, stream, vec, cvec);
   if (e != cudaSuccess || a.schedule != kSimtStreamK) return e;
-  const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
-  simt_streamk_fixup_kernel<<<static_cast<unsigned>(tiles * kFixupChunks), NT, 0, stream>>>(a);
+  const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + TBN - 1) / TBN);
+  simt_streamk_fixup_kernel<TBN><<<static_cast<unsigned>(tiles * kFixupChunks), NT, 0, stream>>>(a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t simt_streamk_slot_floats(int tile_n) { return static_cast<int64_t>(BM) * tile_n; }
+
+cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream) {
+  if (a.tile_n == 256) return launch_tbn<256>(a, stream);
+  if (a.tile_n == 128) return launch_tbn<128>(a, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace dgt

@@ -75,7 +75,7 @@ typedef enum {
 typedef enum {
   GEMM_OPT_FAMILY = 1,   /* value: gemm_family_t; AUTO lets the planner choose            */
   GEMM_OPT_SPLIT_K = 2,  /* value: 0 = planner's choice, n >= 1 = force n slices of K      */
-  GEMM_OPT_TILE_N = 3    /* value: 0 = planner's choice, 128 or 256 for the TC family       */
+  GEMM_OPT_TILE_N = 3    /* value: 0 = planner's choice, 128 or 256 (TC and SIMT families)  */
 } gemm_option_t;
 
 /* What the last successful gemm_run on a handle launched. */

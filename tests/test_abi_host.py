@@ -100,6 +100,11 @@ def test_every_kernel_is_free_of_spills(lib):
     spills = re.findall(r"(\d+) bytes spill stores, (\d+) bytes spill loads", text)
     assert spills, "ptxas report has no kernels"
     assert all(s == "0" and l == "0" for s, l in spills), spills
-    regs = [int(r) for r in re.findall(r"Used (\d+) registers", text)]
-    # SIMT kernel: two 256-thread CTAs per SM need <= 128 registers per thread.
-    assert max(regs) <= 128, max(regs)
+    # Registers per kernel: the 128-column SIMT kernel keeps two 256-thread
+    # CTAs per SM only at <= 128 registers; one 256-thread CTA of the
+    # 256-column kernel fits the 64K register file at <= 255.
+    per_kernel = re.findall(r"Compiling entry function '(\w+)'.*?Used (\d+) registers", text, re.S)
+    assert per_kernel
+    for name, regs in per_kernel:
+        limit = 128 if "simt_gemm_kernelILi128" in name else 255
+        assert int(regs) <= limit, (name, regs)

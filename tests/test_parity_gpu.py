@@ -107,6 +107,18 @@ def test_fp32_stream_k(h, tA, tB, M, N, K):
     _cases.run_and_check(h, "fp32", M, N, min(K, 1024), tA, tB, seed=62, dist="int", exact=True)
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tA,tB", TRANS)
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (1000, 700, 3000), (129, 257, 1025)])
+def test_fp32_tile_widths(h, tile_n, tA, tB, M, N, K):
+    """Both SIMT tile widths, whatever schedule the planner gives them."""
+    h.set_option("tile_n", tile_n)
+    rows = _cases.sample_rows(M) if M * N * K > 2e9 else None
+    _cases.run_and_check(h, "fp32", M, N, K, tA, tB, alpha=-0.5, beta=0.5, seed=67, dist="normal", rows=rows)
+    assert h.plan()["tile_n"] == tile_n
+    _cases.run_and_check(h, "fp32", M, N, min(K, 1024), tA, tB, seed=68, dist="int", exact=True)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_many_tiles_persistent_loop(h, mode):
     # More tiles than SMs: every CTA of the persistent grid loops over several
