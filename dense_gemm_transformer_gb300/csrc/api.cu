@@ -116,24 +116,14 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
                        cudaStream_t s) {
   using namespace dgt;
   const int64_t kt = ceil_div(K, kSimtTileK);
-  // Tile width: 256 columns halve the shared-memory reads per FFMA but leave
-  // one CTA per SM and pad N to a multiple of 256.  Estimated time = padded
-  // work / (schedule efficiency x relative speed), with stream-K counted at
-  // 0.93 (its fixup) and the 128-column kernel at 0.85 of the 256 one.
+  // Tile width: the 128-column kernel (two CTAs per SM) measured as fast per
+  // FLOP as the 256-column one (one CTA per SM, half the shared-memory reads
+  // per FFMA) and pads N less, so it is the default; 256 columns only when N
+  // is a multiple of 256 and there are at least two waves of such tiles.
   int tile_n = (h->opt_tile_n == 128 || h->opt_tile_n == 256) ? h->opt_tile_n : 0;
   if (tile_n == 0) {
-    double best = 0.0;
-    for (int tn : {256, 128}) {
-      const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, tn);
-      const int64_t slots = (tn == 256 ? 1 : 2) * static_cast<int64_t>(h->sms);
-      const double e = wave_eff(tiles, slots);
-      const double sched = (e >= 0.92) ? e : 0.93;
-      const double t = static_cast<double>(tiles * tn) / (sched * (tn == 256 ? 1.0 : 0.85));
-      if (tile_n == 0 || t < best) {
-        best = t;
-        tile_n = tn;
-      }
-    }
+    const int64_t tiles256 = ceil_div(M, kSimtTileM) * ceil_div(N, 256);
+    tile_n = (N % 256 == 0 && tiles256 >= 2 * static_cast<int64_t>(h->sms)) ? 256 : 128;
   }
   const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, tile_n);
   const int64_t slots = (tile_n == 256 ? 1 : 2) * static_cast<int64_t>(h->sms);  // resident CTAs
@@ -288,7 +278,9 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   if (h->opt_split_k > 0) {
     splits = std::min<int64_t>(h->opt_split_k, kb);
   } else if (swap) {
-    splits = skinny_splits(tiles, kb, sms);
+    // Split K only when the tiles alone leave SMs idle: with two or more
+    // waves, partial sums would only add HBM traffic.
+    splits = (tiles >= 2 * sms) ? 1 : skinny_splits(tiles, kb, sms);
   } else if (2 * tiles <= sms && kb >= 8) {
     splits = std::min<int64_t>(sms / tiles, kb / 4);
     splits = std::max<int64_t>(splits, 1);

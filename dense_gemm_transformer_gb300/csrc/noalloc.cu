@@ -132,7 +132,7 @@ extern "C" gemm_status_t gemm_run_small_m_noalloc(int mode, int transB, int64_t 
   const int64_t kb = ceil_div(K, bk);
   const int64_t ws_ld = round_up(N, 4);
   const int64_t slice_bytes = M * ws_ld * static_cast<int64_t>(sizeof(float));
-  int64_t splits = planned_splits(tiles, kb, d.sms);
+  int64_t splits = (tiles >= 2 * d.sms) ? 1 : planned_splits(tiles, kb, d.sms);
   const int64_t room = static_cast<int64_t>(kScratchBytes - kStatusBytes);
   while (splits > 1 && splits * slice_bytes > room) --splits;
   const int64_t kb_per = ceil_div(kb, splits);
