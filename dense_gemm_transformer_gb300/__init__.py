@@ -22,7 +22,7 @@ from . import _build
 
 MODES = {"fp32": 0, "tf32": 1, "bf16": 2}
 FAMILIES = {"auto": 0, "simt": 1, "tc": 2, "skinny": 3}
-OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3}
+OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3, "pretranspose": 4}
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED", 3: "GEMM_ERR_MISALIGNED",
           4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_ALLOC", 6: "GEMM_ERR_DEVICE_TIMEOUT", 7: "GEMM_ERR_TOO_LARGE"}
 HEADER = os.path.join(_build.ROOT, "include", "gemm.h")

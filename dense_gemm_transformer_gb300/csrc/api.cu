@@ -6,7 +6,8 @@
 //   FP32             -> the register-tiled SIMT kernel with 128 x 128 or
 //                       128 x 256 tiles, one CTA per tile when the tiles fill
 //                       whole waves of the resident CTAs (>= 92%), stream-K
-//                       over the resident CTAs otherwise.
+//                       over the resident CTAs otherwise; K-contiguous
+//                       operands of long GEMMs are transposed first.
 //   TF32, BF16       -> the persistent tcgen05 kernel; the tile width (128 or
 //                       256 columns) is the one with the least time over
 //                       whole waves of one tile per SM, and K is split
@@ -36,6 +37,7 @@ struct gemm_handle_s {
   int opt_family = GEMM_FAMILY_AUTO;
   int opt_split_k = 0;
   int opt_tile_n = 0;
+  int opt_pretranspose = 0;
   gemm_plan_t plan{};
 };
 
@@ -127,6 +129,16 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   }
   const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, tile_n);
   const int64_t slots = (tile_n == 256 ? 1 : 2) * static_cast<int64_t>(h->sms);  // resident CTAs
+  // An operand stored with K contiguous reaches shared memory through 4-byte
+  // transposing copies, which load the L1/shared-memory pipe far more than
+  // the 16-byte copies of an M- or N-contiguous operand.  Transposing it once
+  // into the workspace costs 8 bytes of HBM traffic per element against
+  // 2 x (N or M) FLOPs per element of the GEMM: under 10% of the GEMM's time
+  // when the other dimension is >= 512 (A) or >= 256 (B), so it is done then.
+  const int pre = h->opt_pretranspose;  // 0 planner, 1 never, 2 always
+  const bool tr_a = !transA && K > 0 && (pre == 2 || (pre == 0 && N >= 512 && M >= 128 && K >= 64));
+  const bool tr_b = transB && K > 0 && (pre == 2 || (pre == 0 && M >= 256 && N >= 128 && K >= 64));
+  const int64_t lda_t = round_up(M, 4), ldb_t = round_up(N, 4);
   SimtArgs a{};
   a.transA = transA;
   a.transB = transB;
@@ -166,25 +178,48 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
     a.grid = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(slots, 510), a.iters / 8));
     grid = static_cast<int>(a.grid);
   }
-  if (a.schedule == kSimtSplitK) {
-    gemm_status_t st = ensure_ws(h, static_cast<size_t>(a.splits * M * a.ws_ld) * sizeof(float));
+  // Workspace: [split-K slices or stream-K slots][A transposed][B transposed].
+  size_t part_bytes = 0;
+  if (a.schedule == kSimtSplitK) part_bytes = static_cast<size_t>(a.splits * M * a.ws_ld) * sizeof(float);
+  if (a.schedule == kSimtStreamK)
+    part_bytes = static_cast<size_t>(2 * a.grid * simt_streamk_slot_floats(tile_n)) * sizeof(float);
+  const size_t a_off = round_up(static_cast<int64_t>(part_bytes), 256);
+  const size_t a_bytes = tr_a ? static_cast<size_t>(K * lda_t) * sizeof(float) : 0;
+  const size_t b_off = a_off + round_up(static_cast<int64_t>(a_bytes), 256);
+  const size_t b_bytes = tr_b ? static_cast<size_t>(K * ldb_t) * sizeof(float) : 0;
+  const size_t total = b_off + b_bytes;
+  if (total > 0) {
+    gemm_status_t st = ensure_ws(h, total);
     if (st != GEMM_OK) return st;
-    a.ws = static_cast<float*>(h->ws);
-  } else if (a.schedule == kSimtStreamK) {
-    gemm_status_t st =
-        ensure_ws(h, static_cast<size_t>(2 * a.grid * simt_streamk_slot_floats(tile_n)) * sizeof(float));
-    if (st != GEMM_OK) return st;
-    a.ws = static_cast<float*>(h->ws);
-    ++kernels;  // the fixup
   }
+  char* ws = static_cast<char*>(h->ws);
+  if (part_bytes > 0) a.ws = reinterpret_cast<float*>(ws);
+  if (a.schedule == kSimtStreamK) ++kernels;  // the fixup
   if (a.schedule != kSimtStreamK && ceil_div(M, kSimtTileM) > 65535) return GEMM_ERR_NOT_SUPPORTED;
+  if (tr_a) {
+    float* at = reinterpret_cast<float*>(ws + a_off);
+    if (launch_transpose(A, lda, at, lda_t, M, K, 4, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    a.A = at;
+    a.lda = lda_t;
+    a.transA = 1;
+    ++kernels;
+  }
+  if (tr_b) {
+    float* bt = reinterpret_cast<float*>(ws + b_off);
+    if (launch_transpose(B, ldb, bt, ldb_t, N, K, 4, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    a.B = bt;
+    a.ldb = ldb_t;
+    a.transB = 0;
+    ++kernels;
+  }
   if (launch_simt(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
   if (a.schedule == kSimtSplitK) {
     if (launch_splitk_reduce(M, N, a.splits, a.ws, a.ws_ld, C, ldc, alpha, beta, s) != cudaSuccess)
       return GEMM_ERR_CUDA;
     ++kernels;
   }
-  set_plan(h, GEMM_FAMILY_SIMT, kSimtTileM, tile_n, kSimtTileK, a.splits, tile_n == 256 ? 4 : 3, grid, kernels, 0);
+  set_plan(h, GEMM_FAMILY_SIMT, kSimtTileM, tile_n, kSimtTileK, a.splits, tile_n == 256 ? 4 : 3, grid, kernels,
+           (tr_a ? 1 : 0) | (tr_b ? 2 : 0));
   h->plan.schedule = a.schedule;
   return GEMM_OK;
 }
@@ -464,6 +499,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, int option, int64_t value) {
     case GEMM_OPT_TILE_N:
       if (value != 0 && value != 128 && value != 256) return GEMM_ERR_INVALID_VALUE;
       h->opt_tile_n = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_PRETRANSPOSE:
+      if (value < 0 || value > 2) return GEMM_ERR_INVALID_VALUE;
+      h->opt_pretranspose = static_cast<int>(value);
       return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_VALUE;

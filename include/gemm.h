@@ -75,7 +75,9 @@ typedef enum {
 typedef enum {
   GEMM_OPT_FAMILY = 1,   /* value: gemm_family_t; AUTO lets the planner choose            */
   GEMM_OPT_SPLIT_K = 2,  /* value: 0 = planner's choice, n >= 1 = force n slices of K      */
-  GEMM_OPT_TILE_N = 3    /* value: 0 = planner's choice, 128 or 256 (TC and SIMT families)  */
+  GEMM_OPT_TILE_N = 3,   /* value: 0 = planner's choice, 128 or 256 (TC and SIMT families)  */
+  GEMM_OPT_PRETRANSPOSE = 4 /* SIMT: 0 = planner's choice, 1 = never, 2 = always transpose
+                               K-contiguous operands into the workspace first             */
 } gemm_option_t;
 
 /* What the last successful gemm_run on a handle launched. */
@@ -86,7 +88,7 @@ typedef struct {
   int32_t stages;        /* shared-memory pipeline depth */
   int32_t grid;          /* CTAs of the main kernel */
   int32_t kernels;       /* kernels launched by the call */
-  int32_t packed;        /* bit 0: A re-packed, bit 1: B re-packed into the workspace */
+  int32_t packed;        /* bit 0: A re-packed (or transposed), bit 1: B, into the workspace */
   int32_t schedule;      /* SIMT: 0 one CTA per tile, 1 split-K slices, 2 stream-K */
   int32_t reserved[6];
 } gemm_plan_t;

@@ -34,6 +34,7 @@ def _reset(h):
     h.set_option("family", "auto")
     h.set_option("split_k", 0)
     h.set_option("tile_n", 0)
+    h.set_option("pretranspose", 0)
     yield
 
 
@@ -117,6 +118,20 @@ def test_fp32_tile_widths(h, tile_n, tA, tB, M, N, K):
     _cases.run_and_check(h, "fp32", M, N, K, tA, tB, alpha=-0.5, beta=0.5, seed=67, dist="normal", rows=rows)
     assert h.plan()["tile_n"] == tile_n
     _cases.run_and_check(h, "fp32", M, N, min(K, 1024), tA, tB, seed=68, dist="int", exact=True)
+
+
+@pytest.mark.parametrize("pre", [1, 2])
+@pytest.mark.parametrize("tA,tB", TRANS)
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (129, 257, 1025), (1000, 700, 3000)])
+def test_fp32_pretranspose(h, pre, tA, tB, M, N, K):
+    """FP32 with K-contiguous operands read in place (1) or transposed into
+    the workspace first (2), on ragged shapes and both schedules."""
+    h.set_option("pretranspose", pre)
+    rows = _cases.sample_rows(M) if M * N * K > 2e9 else None
+    _cases.run_and_check(h, "fp32", M, N, K, tA, tB, alpha=1.25, beta=-0.5, seed=71, dist="normal", rows=rows)
+    want = 0 if pre == 1 else ((0 if tA else 1) | (2 if tB else 0))
+    assert h.plan()["packed"] == want
+    _cases.run_and_check(h, "fp32", M, N, min(K, 1024), tA, tB, seed=72, dist="int", exact=True)
 
 
 @pytest.mark.parametrize("mode", MODES)
