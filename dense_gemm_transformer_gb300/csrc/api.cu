@@ -118,15 +118,13 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
                        cudaStream_t s) {
   using namespace dgt;
   const int64_t kt = ceil_div(K, kSimtTileK);
-  // Tile width: the 128-column kernel (two CTAs per SM) measured as fast per
-  // FLOP as the 256-column one (one CTA per SM, half the shared-memory reads
-  // per FFMA) and pads N less, so it is the default; 256 columns only when N
-  // is a multiple of 256 and there are at least two waves of such tiles.
+  // Tile width: the 256-column kernel (one CTA per SM, half the shared-memory
+  // reads per FFMA) measured 5-10% faster when N needs no padding and M is
+  // large, and slower on deep-K products with few output rows (more stream-K
+  // partial traffic) or when N pads up; so 256 columns only for N % 256 == 0
+  // and M >= 1024, 128 otherwise.
   int tile_n = (h->opt_tile_n == 128 || h->opt_tile_n == 256) ? h->opt_tile_n : 0;
-  if (tile_n == 0) {
-    const int64_t tiles256 = ceil_div(M, kSimtTileM) * ceil_div(N, 256);
-    tile_n = (N % 256 == 0 && tiles256 >= 2 * static_cast<int64_t>(h->sms)) ? 256 : 128;
-  }
+  if (tile_n == 0) tile_n = (N % 256 == 0 && M >= 1024) ? 256 : 128;
   const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, tile_n);
   const int64_t slots = (tile_n == 256 ? 1 : 2) * static_cast<int64_t>(h->sms);  // resident CTAs
   // An operand stored with K contiguous reaches shared memory through 4-byte
