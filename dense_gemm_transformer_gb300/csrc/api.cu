@@ -32,6 +32,7 @@ struct gemm_handle_s {
   int device = 0;
   int sms = 0;
   int* d_status = nullptr;
+  int* d_counters = nullptr;  // per-tile arrival counters of the fused K-slice reduction (zero between calls)
   void* ws = nullptr;
   size_t ws_bytes = 0;
   int opt_family = GEMM_FAMILY_AUTO;
@@ -44,6 +45,7 @@ struct gemm_handle_s {
 namespace {
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+constexpr int64_t kCounterTiles = 16384;  // tiles the fused K-slice reduction can count
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -383,11 +385,15 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.ws_ld = ws_ld;
   a.ws_slice = M * ws_ld;  // partial sums are kept in the caller's M x N orientation
   a.status = h->d_status;
+  // The swapped form reduces its K slices inside the kernel (the last CTA to
+  // finish a tile sums the slices); the other forms use the reduce kernel.
+  const bool fused = swap && splits > 1 && tiles <= kCounterTiles;
+  a.counters = fused ? h->d_counters : nullptr;
   a.grid = static_cast<int>(std::min<int64_t>(tiles * splits, sms));
   a.group_m = 16;
   if (launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
   ++kernels;
-  if (splits > 1) {
+  if (splits > 1 && !fused) {
     if (launch_splitk_reduce(M, N, a.splits, a.ws, ws_ld, C, ldc, alpha, beta, s) != cudaSuccess)
       return GEMM_ERR_CUDA;
     ++kernels;
@@ -430,6 +436,18 @@ gemm_status_t gemm_create(gemm_handle_t* out) {
     delete h;
     return GEMM_ERR_CUDA;
   }
+  if (cudaMalloc(&h->d_counters, kCounterTiles * sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->d_status);
+    delete h;
+    return GEMM_ERR_ALLOC;
+  }
+  if (cudaMemset(h->d_counters, 0, kCounterTiles * sizeof(int)) != cudaSuccess) {
+    cudaFree(h->d_counters);
+    cudaFree(h->d_status);
+    delete h;
+    return GEMM_ERR_CUDA;
+  }
   *out = h;
   return GEMM_OK;
 }
@@ -442,6 +460,7 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
   gemm_status_t st = cuda_status(cudaDeviceSynchronize());
   if (h->ws) cudaFree(h->ws);
   if (h->d_status) cudaFree(h->d_status);
+  if (h->d_counters) cudaFree(h->d_counters);
   cudaSetDevice(prev);
   delete h;
   return st;
@@ -519,7 +538,9 @@ gemm_status_t gemm_check_device(gemm_handle_t h, void* stream) {
   int v = 0;
   if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
   if (v != 0) {
+    // An abandoned kernel may have left tile counters mid-count.
     if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cudaMemset(h->d_counters, 0, kCounterTiles * sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
     return GEMM_ERR_DEVICE_TIMEOUT;
   }
   return GEMM_OK;

@@ -65,6 +65,8 @@ struct TcArgs {
   int64_t ws_ld;
   int64_t ws_slice;      // elements between successive K slices' partial sums
   int* status;           // device status word
+  int* counters;         // tile_n == 16 with splits > 1: zeroed per-tile counters for the fused
+                         // reduction (null: the caller launches launch_splitk_reduce)
   int grid;              // persistent CTAs
   int group_m;           // raster group height in M tiles
 };

@@ -106,6 +106,7 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.ws_ld = a.ws_ld;
   p.ws_slice = a.ws_slice;
   p.status = a.status;
+  p.counters = (a.tile_n == 16 && a.splits > 1) ? a.counters : nullptr;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
   // Tiles leave through TMA stores when the destination allows it: not the
   // transposed small-M form, no read of C (beta == 0, or partial sums), and

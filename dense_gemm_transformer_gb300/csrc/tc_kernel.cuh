@@ -53,6 +53,8 @@ struct TcParams {
   int64_t ws_ld;
   int64_t ws_slice;  // elements between the partial sums of successive K slices
   int* status;
+  int* counters;  // swapped form with K slices: per-tile arrival counts (all zero between calls),
+                  // or null to leave the reduction of the slices to a separate kernel
   int c_vec;  // C rows are 16-byte aligned (ldc % 4 == 0 and C aligned)
   int c_tma;  // tiles leave through shared memory and TMA stores (tmC is valid)
 };
@@ -143,6 +145,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;  // epilogue: this CTA reduces the tile's K slices
 
   const uint32_t smem0 = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
@@ -381,6 +384,39 @@ __global__ void __launch_bounds__(192, 1)
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
+      }
+      if constexpr (TRANS_C) {
+        // Fused K-slice reduction: the CTA whose slice of a tile arrives last
+        // sums all the tile's slices in slice order and writes C (the same
+        // order and arithmetic as the separate reduce kernel).  The partial
+        // stores above are made visible before the arrival is counted, and
+        // the last arriver reads the slices from L2 (no stale L1 lines).
+        if (partial && p.counters != nullptr) {
+          __threadfence();
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          const int tile_id = w.tm * p.num_tn + w.tn;
+          if (warp == 2 && lane == 0) *last_flag = (atomicAdd(p.counters + tile_id, 1) == p.splits - 1) ? 1 : 0;
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (*last_flag) {
+            __threadfence();
+            if (row_ok) {
+              const int64_t col0 = static_cast<int64_t>(w.tn) * BN;
+#pragma unroll 1
+              for (int j = 0; j < BN; ++j) {
+                const int64_t col = col0 + j;
+                if (col < p.N) {
+                  float sum = __ldcg(p.ws + col * p.ws_ld + row);
+                  for (int sp = 1; sp < p.splits; ++sp) sum += __ldcg(p.ws + sp * p.ws_slice + col * p.ws_ld + row);
+                  float v = p.alpha * sum;
+                  float* dst = p.C + col * p.ldc + row;
+                  if (p.beta != 0.f) v = fmaf(p.beta, *dst, v);
+                  *dst = v;
+                }
+              }
+            }
+            if (warp == 2 && lane == 0) p.counters[tile_id] = 0;  // ready for the next call
+          }
+        }
       }
     }
     // Every TMA store of this warp has completed before the CTA exits.

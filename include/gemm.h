@@ -94,7 +94,9 @@ typedef struct {
 } gemm_plan_t;
 
 /* Create a handle on the current device.  Reads the device properties and
- * allocates the 4-byte device status word.  *out is set to NULL on failure. */
+ * allocates the 4-byte device status word and 64 KB of zeroed per-tile
+ * counters (used by the small-M path's in-kernel K-slice reduction).  *out is
+ * set to NULL on failure. */
 gemm_status_t gemm_create(gemm_handle_t* out);
 
 /* Free the handle, its status word and its workspace.  Synchronizes the
