@@ -1,0 +1,63 @@
+"""Host-side checks of bench.py without a GPU: the reference arm's JSON line,
+and the multi-rank path (replicas: barrier and max-over-ranks timing) as two
+gloo ranks on the CPU."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(cmd, env_extra=None, timeout=240):
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    env.setdefault("OMP_NUM_THREADS", "2")
+    return subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=timeout)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = _run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3",
+              "--ref-macs", "2e7"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "gpt_projections_fp32_tf32"
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    r = _run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+              "--master-addr", "127.0.0.1", "--master-port", "29561", "bench.py", "--impl", "reference",
+              "--gpus", "2", "--steps", "1", "--warmup", "3", "--ref-macs", "2e7"])
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout  # rank 0 alone prints
+    assert json.loads(lines[0])["n_gpus"] == 2
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    t = bench.max_over_ranks(1.0 + rank, world, "cpu")
+    out[rank] = t
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_gloo():
+    world = 2
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker, args=(world, 29562, out), nprocs=world, join=True)
+        assert dict(out) == {0: 2.0, 1: 2.0}
