@@ -400,17 +400,35 @@ __global__ void __launch_bounds__(192, 1)
           if (*last_flag) {
             __threadfence();
             if (row_ok) {
+              // Up to 4 slices x BN columns of loads in flight per round; each
+              // column still sums its slices in ascending order.
               const int64_t col0 = static_cast<int64_t>(w.tn) * BN;
-#pragma unroll 1
+              const float* src = p.ws + col0 * p.ws_ld + row;
+              float sum[BN];
+#pragma unroll
+              for (int j = 0; j < BN; ++j) sum[j] = 0.f;
+              for (int sp0 = 0; sp0 < p.splits; sp0 += 4) {
+                float v[4][BN];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                  for (int j = 0; j < BN; ++j)
+                    v[q][j] = (sp0 + q < p.splits && col0 + j < p.N)
+                                  ? __ldcg(src + (sp0 + q) * p.ws_slice + j * p.ws_ld)
+                                  : 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                  for (int j = 0; j < BN; ++j)
+                    if (sp0 + q < p.splits) sum[j] = (sp0 + q == 0) ? v[q][j] : sum[j] + v[q][j];
+              }
+#pragma unroll
               for (int j = 0; j < BN; ++j) {
-                const int64_t col = col0 + j;
-                if (col < p.N) {
-                  float sum = __ldcg(p.ws + col * p.ws_ld + row);
-                  for (int sp = 1; sp < p.splits; ++sp) sum += __ldcg(p.ws + sp * p.ws_slice + col * p.ws_ld + row);
-                  float v = p.alpha * sum;
-                  float* dst = p.C + col * p.ldc + row;
-                  if (p.beta != 0.f) v = fmaf(p.beta, *dst, v);
-                  *dst = v;
+                if (col0 + j < p.N) {
+                  float* dst = p.C + (col0 + j) * p.ldc + row;
+                  float out = p.alpha * sum[j];
+                  if (p.beta != 0.f) out = fmaf(p.beta, *dst, out);
+                  *dst = out;
                 }
               }
             }
