@@ -133,10 +133,11 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   // transposing copies, which load the L1/shared-memory pipe far more than
   // the 16-byte copies of an M- or N-contiguous operand.  Transposing it once
   // into the workspace costs 8 bytes of HBM traffic per element against
-  // 2 x (N or M) FLOPs per element of the GEMM: under 10% of the GEMM's time
-  // when the other dimension is >= 512 (A) or >= 256 (B), so it is done then.
+  // 2 x (N or M) FLOPs per element of the GEMM: under ~10% of the GEMM's
+  // time when the other dimension is >= 256, and the copies it avoids cost
+  // more than that, so it is done then.
   const int pre = h->opt_pretranspose;  // 0 planner, 1 never, 2 always
-  const bool tr_a = !transA && K > 0 && (pre == 2 || (pre == 0 && N >= 512 && M >= 128 && K >= 64));
+  const bool tr_a = !transA && K > 0 && (pre == 2 || (pre == 0 && N >= 256 && M >= 128 && K >= 64));
   const bool tr_b = transB && K > 0 && (pre == 2 || (pre == 0 && M >= 256 && N >= 128 && K >= 64));
   const int64_t lda_t = round_up(M, 4), ldb_t = round_up(N, 4);
   SimtArgs a{};
