@@ -339,21 +339,33 @@ def bench_ours(args, world, rank, local):
     roof["share_of_step"] = fam_ms[dom] / sum(per_call_ms)
 
     # End to end through the C ABI: pinned host inputs -> device, the 30 GEMMs,
-    # every output -> pinned host, all inside the timed region.
+    # every output -> pinned host, all inside the timed region.  The inputs go
+    # up on one copy stream; each output goes down on another as soon as its
+    # GEMM has finished, overlapping the GEMMs that follow (the next step's
+    # uploads wait for this step's GEMMs, its GEMMs for this step's downloads).
     e2e = None
     if not args.no_e2e:
         pinned_in = [t.pin_memory() for t in host_inputs]
         pinned_out = [torch.empty(c.C.shape, dtype=c.C.dtype, pin_memory=True) for c in calls]
         h2d = sum(t.numel() * t.element_size() for t in pinned_in)
         d2h = sum(t.numel() * t.element_size() for t in pinned_out)
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        done = [torch.cuda.Event() for _ in calls]
 
         def e2e_step():
-            with torch.cuda.stream(stream):
+            up.wait_stream(stream)
+            with torch.cuda.stream(up):
                 for src, dst in zip(pinned_in, dev_inputs):
                     dst.copy_(src, non_blocking=True)
-                step()
-                for c, dst in zip(calls, pinned_out):
+            stream.wait_stream(up)
+            stream.wait_stream(down)
+            for c, dst, ev in zip(calls, pinned_out, done):
+                run_call(h, c, stream)
+                ev.record(stream)
+                down.wait_event(ev)
+                with torch.cuda.stream(down):
                     dst.copy_(c.C, non_blocking=True)
+            stream.wait_stream(down)
 
         for _ in range(2):
             e2e_step()
