@@ -173,10 +173,17 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   } else if (wave_eff(tiles, slots) >= 0.92 || tiles * kt < 4 * slots) {
     a.schedule = kSimtTiles;
   } else {
+    // Whole-tile waves first, stream-K over the rest: the last partial wave
+    // (or, when it would give each CTA fewer than 4 k-tiles, the last wave
+    // and a half) is shared out, so only those tiles go through the fixup.
     a.schedule = kSimtStreamK;
-    a.iters = tiles * kt;
-    // at least 8 k-tiles per CTA; at most 510 CTAs (the fixup's part list)
-    a.grid = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(slots, 510), a.iters / 8));
+    const int64_t g = std::min<int64_t>(slots, 510);  // at most 510 CTAs (the fixup's part list)
+    int64_t dp_waves = tiles / g;
+    if (dp_waves > 0 && (tiles - dp_waves * g) * kt < 4 * g) --dp_waves;
+    a.dp_tiles = dp_waves * g;
+    a.iters = (tiles - a.dp_tiles) * kt;
+    // at least 8 k-tiles per CTA when stream-K is all there is
+    a.grid = a.dp_tiles > 0 ? g : std::max<int64_t>(1, std::min<int64_t>(g, a.iters / 8));
     grid = static_cast<int>(a.grid);
   }
   // Workspace: [split-K slices or stream-K slots][A transposed][B transposed].

@@ -33,7 +33,8 @@ struct SimtArgs {
   int schedule;
   int splits;
   int64_t k_per_split;
-  int64_t iters;
+  int64_t dp_tiles;  // stream-K: leading tiles processed whole, round-robin over the grid
+  int64_t iters;     // stream-K: (tile, k-tile) iterations of the tiles from dp_tiles on
   int64_t grid;
   float* ws;
   int64_t ws_ld;
@@ -73,6 +74,8 @@ struct TcArgs {
 // tile_n == 16 selects the swapped small-M form: the caller passes the
 // operands exchanged (C^T = op(B)^T op(A)^T, M and N exchanged) and the
 // kernel stores its tile transposed into the caller's C.
+constexpr int kTcEpiWarps = 8;                        // epilogue warps (two per TMEM lane quarter)
+constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);  // producer + MMA warps + epilogue warps
 int tc_tile_k(int mode);              // k elements per stage (128 bytes)
 int tc_stages(int mode, int tile_n);  // pipeline depth
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream);

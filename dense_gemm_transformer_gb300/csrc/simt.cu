@@ -18,10 +18,11 @@
 //     barrier per tile; with TBN = 256 the register fragments of step k+1 are
 //     loaded while step k is multiplied;
 //   * work is scheduled as whole tiles when they fill whole waves of the
-//     resident CTAs, and otherwise as stream-K: the (tile, k-tile) iterations
-//     are cut into one equal contiguous run per resident CTA, runs that cover
-//     part of a tile store a raw partial tile, and a fixup kernel sums each
-//     tile's partials in ascending k order (deterministic);
+//     resident CTAs, and otherwise as whole-tile waves followed by stream-K
+//     for the rest: the remaining (tile, k-tile) iterations are cut into one
+//     equal contiguous run per resident CTA, runs that cover part of a tile
+//     store a raw partial tile, and a fixup kernel sums each such tile's
+//     partials in ascending k order (deterministic);
 //   * products are single-rounded FFMA in fp32, the accumulation order along
 //     K is ascending, and the alpha/beta epilogue is fused into the stores.
 #include <cuda_runtime.h>
@@ -178,46 +179,77 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
   const int64_t tiles_n = (p.N + TBN - 1) / TBN;
   const int kt = static_cast<int>((p.K + BK - 1) / BK);  // k-tiles of a whole tile
 
-  // The CTA's work: one segment (whole tile / split-K slice), or a contiguous
-  // run of stream-K iterations that may span several tiles.
-  int64_t it = 0, it_end = 1, it_first = 0;
-  if (p.schedule == kSimtStreamK) {
-    it_first = it = sk_begin(blockIdx.x, p.iters, p.grid);
-    it_end = sk_begin(blockIdx.x + 1, p.iters, p.grid);
+  // The CTA's work: one segment (whole tile / split-K slice); or, for
+  // stream-K, first whole tiles dp, dp + grid, ... below dp_tiles, then a
+  // contiguous run of the (tile, k-tile) iterations of the remaining tiles,
+  // which may span several tiles.  Thread 0 decodes each segment into shared
+  // memory, so the scheduling state occupies no registers in the mainloop.
+  struct SegState {
+    Segment sg;
+    int64_t it, it_end, dp;
+    int valid;
+  };
+  __shared__ SegState sh;
+  if (tid == 0) {
+    if (p.schedule == kSimtStreamK) {
+      sh.it = sk_begin(blockIdx.x, p.iters, p.grid);
+      sh.it_end = sk_begin(blockIdx.x + 1, p.iters, p.grid);
+    } else {
+      sh.it = 0;
+      sh.it_end = 1;
+    }
+    sh.dp = blockIdx.x;
   }
 
-  while (it < it_end) {
-    Segment sg;
-    if (p.schedule == kSimtStreamK) {
-      sg.tile = it / kt;
-      sg.ks = static_cast<int>(it % kt);
-      const int64_t left = it_end - it;
-      sg.ke = (kt - sg.ks <= left) ? kt : sg.ks + static_cast<int>(left);
-      if (sg.ks == 0 && sg.ke == kt) {
-        sg.dest = kToC;
-      } else {
-        sg.dest = kToSlot;
-        sg.index = 2 * static_cast<int64_t>(blockIdx.x) + (it == it_first ? 0 : 1);
-      }
-      it += sg.ke - sg.ks;
-    } else {
-      sg.tile = static_cast<int64_t>(blockIdx.y) * tiles_n + blockIdx.x;
-      if (p.schedule == kSimtSplitK) {
-        const int per = static_cast<int>(p.k_per_split / BK);
-        sg.ks = blockIdx.z * per;
-        sg.ke = (sg.ks + per < kt) ? sg.ks + per : kt;
-        sg.dest = kToSlice;
-        sg.index = blockIdx.z;
-      } else {
+  for (;;) {
+    __syncthreads();  // every thread is done with the previous segment's descriptor
+    if (tid == 0) {
+      Segment sg;
+      sh.valid = 1;
+      if (p.schedule == kSimtStreamK && sh.dp < p.dp_tiles) {
+        sg.tile = sh.dp;
         sg.ks = 0;
         sg.ke = kt;
         sg.dest = kToC;
+        sh.dp += gridDim.x;
+      } else if (p.schedule == kSimtStreamK && sh.it < sh.it_end) {
+        const int64_t it = sh.it;
+        sg.tile = p.dp_tiles + it / kt;
+        sg.ks = static_cast<int>(it % kt);
+        const int64_t left = sh.it_end - it;
+        sg.ke = (kt - sg.ks <= left) ? kt : sg.ks + static_cast<int>(left);
+        if (sg.ks == 0 && sg.ke == kt) {
+          sg.dest = kToC;
+        } else {
+          sg.dest = kToSlot;
+          sg.index = 2 * static_cast<int64_t>(blockIdx.x) +
+                     (it == sk_begin(blockIdx.x, p.iters, p.grid) ? 0 : 1);
+        }
+        sh.it += sg.ke - sg.ks;
+      } else if (p.schedule != kSimtStreamK && sh.it < sh.it_end) {
+        sg.tile = static_cast<int64_t>(blockIdx.y) * tiles_n + blockIdx.x;
+        if (p.schedule == kSimtSplitK) {
+          const int per = static_cast<int>(p.k_per_split / BK);
+          sg.ks = blockIdx.z * per;
+          sg.ke = (sg.ks + per < kt) ? sg.ks + per : kt;
+          sg.dest = kToSlice;
+          sg.index = blockIdx.z;
+        } else {
+          sg.ks = 0;
+          sg.ke = kt;
+          sg.dest = kToC;
+        }
+        sh.it = sh.it_end;
+      } else {
+        sh.valid = 0;
       }
-      it = it_end;
+      sh.sg = sg;
     }
-    const int64_t m0 = (sg.tile / tiles_n) * BM;
-    const int64_t n0 = (sg.tile % tiles_n) * TBN;
-    const int n = sg.ke - sg.ks;
+    __syncthreads();
+    if (!sh.valid) break;
+    const int64_t m0 = (sh.sg.tile / tiles_n) * BM;
+    const int64_t n0 = (sh.sg.tile % tiles_n) * TBN;
+    const int n = sh.sg.ke - sh.sg.ks;
 
     float acc[8][TN];
 #pragma unroll
@@ -229,7 +261,7 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
     // K-contiguous when B is stored N x K (TB == 1).
     TileCopier<!TA, VEC, BM, LDA> ca;
     TileCopier<TB, VEC, TBN, LDB> cb;
-    const int64_t kbeg = static_cast<int64_t>(sg.ks) * BK;
+    const int64_t kbeg = static_cast<int64_t>(sh.sg.ks) * BK;
     ca.init(p.A, p.lda, m0, p.M, kbeg, tid);
     cb.init(p.B, p.ldb, n0, p.N, kbeg, tid);
     // The ring: tiles t+1 .. t+S-1 are in flight while tile t is multiplied;
@@ -316,9 +348,13 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
     __syncthreads();  // the ring is idle before the next segment refills it
 
     // Epilogue.  Rows am + {0..3}, am + 16 + {0..3}; cols bn + 32q + {0..3}.
-    if (sg.dest == kToSlot) {
+    const int dest = sh.sg.dest;
+    const int64_t index = sh.sg.index;
+    const int64_t em0 = (sh.sg.tile / tiles_n) * BM;  // re-read: the mainloop kept no copy
+    const int64_t en0 = (sh.sg.tile % tiles_n) * TBN;
+    if (dest == kToSlot) {
       // A stream-K partial: the raw 128 x TBN tile, rows of TBN floats.
-      float* __restrict__ slot = p.ws + sg.index * (BM * TBN);
+      float* __restrict__ slot = p.ws + index * (BM * TBN);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float* rowp = slot + (am + (i & 3) + (i >> 2) * 16) * TBN + bn;
@@ -329,18 +365,18 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
       }
       continue;
     }
-    const bool partial = sg.dest == kToSlice;
-    float* __restrict__ out = partial ? p.ws + sg.index * p.M * p.ws_ld : p.C;
+    const bool partial = dest == kToSlice;
+    float* __restrict__ out = partial ? p.ws + index * p.M * p.ws_ld : p.C;
     const int64_t ldo = partial ? p.ws_ld : p.ldc;
     const bool read_c = !partial && p.beta != 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int64_t row = m0 + am + (i & 3) + (i >> 2) * 16;
+      const int64_t row = em0 + am + (i & 3) + (i >> 2) * 16;
       if (row >= p.M) continue;
       float* __restrict__ crow = out + row * ldo;
 #pragma unroll
       for (int q = 0; q < QN; ++q) {
-        const int64_t col = n0 + bn + 32 * q;
+        const int64_t col = en0 + bn + 32 * q;
         float v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) v[j] = partial ? acc[i][4 * q + j] : p.alpha * acc[i][4 * q + j];
@@ -383,11 +419,11 @@ __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
   constexpr int kMaxParts = 512;  // > the most resident CTAs that can share one tile
   __shared__ int64_t slots[kMaxParts];
   __shared__ int nparts;
-  const int64_t tile = blockIdx.x / kFixupChunks;
+  const int64_t tile = p.dp_tiles + blockIdx.x / kFixupChunks;  // tiles below dp_tiles were stored whole
   const int chunk = blockIdx.x % kFixupChunks;
   if (threadIdx.x == 0) {
     const int64_t kt = (p.K + BK - 1) / BK;
-    const int64_t f = tile * kt, l = f + kt - 1;
+    const int64_t f = (tile - p.dp_tiles) * kt, l = f + kt - 1;
     auto owner = [&](int64_t x) {
       int64_t c = x * p.grid / p.iters;
       while (c + 1 < p.grid && sk_begin(c + 1, p.iters, p.grid) <= x) ++c;
@@ -469,7 +505,7 @@ cudaError_t launch_tbn(const SimtArgs& a, cudaStream_t stream) {
     e = launch_vec<TBN, true, true>(a, grid, stream, vec, cvec);
   if (e != cudaSuccess || a.schedule != kSimtStreamK) return e;
   const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + TBN - 1) / TBN);
-  simt_streamk_fixup_kernel<TBN><<<static_cast<unsigned>(tiles * kFixupChunks), NT, 0, stream>>>(a);
+  simt_streamk_fixup_kernel<TBN><<<static_cast<unsigned>((tiles - a.dp_tiles) * kFixupChunks), NT, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

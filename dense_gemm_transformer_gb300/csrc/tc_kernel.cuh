@@ -14,12 +14,12 @@
 //               one lane issues the MMAs of a stage and commits them to the
 //               stage's "empty" mbarrier, and commits a finished tile to its
 //               accumulator's "full" mbarrier;
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lanes 32*(w%4)..+31, i.e. those rows of the tile), the fused
-//               alpha/beta update, and the stores; then they release the
-//               accumulator so the next tile's MMAs can start.  Two
-//               accumulators let the epilogue of tile i overlap the mainloop
-//               of tile i+1.
+//   warps 2-9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4)..+31, i.e. those rows of the tile; warps w
+//               and w+4 split the tile's columns), the fused alpha/beta
+//               update, and the stores; then they release the accumulator
+//               so the next tile's MMAs can start.  Two accumulators let the
+//               epilogue of tile i overlap the mainloop of tile i+1.
 //
 // Work units are (tile, K slice) pairs handed out round-robin to a persistent
 // grid of one CTA per SM, in a grouped raster order (group_m tiles of M walk
@@ -75,9 +75,9 @@ struct TcCfg {
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;  // two accumulators (allocation >= 32 columns)
   static constexpr int CW = BN < 32 ? BN : 32;                    // accumulator columns per TMEM load
   static constexpr int NUM_BARS = 2 * STAGES + 5;     // full/empty per stage, acc full/empty x2, drain
-  // Epilogue staging for TMA stores: 2 buffers of 32 rows x 128 bytes per
+  // Epilogue staging for TMA stores: one buffer of 32 rows x 128 bytes per
   // epilogue warp (the swapped small-M form stores directly and has none).
-  static constexpr int STAGING_BYTES = (BN >= 128) ? 4 * 2 * 32 * 128 : 0;
+  static constexpr int STAGING_BYTES = (BN >= 128) ? kTcEpiWarps * 32 * 128 : 0;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
   static constexpr uint32_t FORMAT = (MODE == 2) ? 1u : 2u;  // bf16 / tf32 in the instruction descriptor
@@ -132,7 +132,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
 // swapped by the host (a small-M product whose weights fill the 128-row MMA
 // side), so element (r, c) of its tile is stored at C[c * ldc + r].
 template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   using Cfg = TcCfg<MODE, BN>;
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
-      mbar_init(acce_bar(a), 4);  // one arrival per epilogue warp
+      mbar_init(acce_bar(a), kTcEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -279,7 +279,8 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int sub = warp & 3;  // TMEM lane quarter this warp may access
+    const int sub = warp & 3;          // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the tile's column chunks it stores
     int acc = 0;
     uint32_t acc_phase = 0;
     const bool partial = p.splits > 1;
@@ -297,8 +298,11 @@ __global__ void __launch_bounds__(192, 1)
       float* out = TRANS_C ? base : base + (row_ok ? row : 0) * ld;
       const bool vec_ok = !TRANS_C && (partial || p.c_vec);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      constexpr int NCH = BN / CW;  // column chunks of a tile
+      const int cc_begin = (NCH >= 2) ? half * (NCH / 2) : (half == 0 ? 0 : NCH);
+      const int cc_end = (NCH >= 2) ? (half + 1) * (NCH / 2) : NCH;
 #pragma unroll 1
-      for (int cc = 0; cc < BN / CW; ++cc) {
+      for (int cc = cc_begin; cc < cc_end; ++cc) {
         uint32_t r[CW];
         __syncwarp();
         tmem_ld_32x32b<CW>(t_row + cc * CW, r);
@@ -311,8 +315,8 @@ __global__ void __launch_bounds__(192, 1)
             // TMA unit reads (16-byte chunk j of row t sits at chunk j ^ (t % 8)),
             // then one lane stores the box; the unit clips rows past M and
             // columns past N.
-            uint8_t* buf = staging + (sub * 2 + (tma_buf & 1)) * 4096;
-            if (lane == 0) bulk_wait_group_read<1>();  // the buffer's previous store has read it
+            uint8_t* buf = staging + (warp - 2) * 4096;
+            if (lane == 0) bulk_wait_group_read<0>();  // the buffer's previous store has read it
             __syncwarp();
             const float a = partial ? 1.f : p.alpha;
 #pragma unroll
@@ -391,7 +395,7 @@ __global__ void __launch_bounds__(192, 1)
         // order and arithmetic as the separate reduce kernel).  The partial
         // stores above are made visible before the arrival is counted, and
         // the last arriver reads the slices from L2 (no stale L1 lines).
-        if (partial && p.counters != nullptr) {
+        if (partial && p.counters != nullptr && half == 0) {
           __threadfence();
           asm volatile("bar.sync 1, 128;" ::: "memory");
           const int tile_id = w.tm * p.num_tn + w.tn;

@@ -14,7 +14,7 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
   auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN, TRANS_C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 192, Cfg::SMEM_BYTES, s>>>(ta, tb, tc, p);
+  kern<<<grid, kTcThreads, Cfg::SMEM_BYTES, s>>>(ta, tb, tc, p);
   return cudaGetLastError();
 }
 
