@@ -286,7 +286,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool partial = p.splits > 1;
     const bool read_c = !partial && p.beta != 0.f;
     constexpr int CW = Cfg::CW;
-    uint32_t tma_buf = 0;  // staging buffers used by this warp so far
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
       const Unit w = decode_unit(u, p);
       if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull)) break;
@@ -335,7 +334,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                            partial ? w.split : 0);
               bulk_commit_group();
             }
-            ++tma_buf;
             continue;
           }
         }
