@@ -46,6 +46,27 @@ SM_MAX_MHZ = 2070.0
 TF32_OVER_BF16 = 1.1 / 2.25
 
 
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
+# capture of the step's 15 FP32 GEMM launches (cold L2).  The figure belongs
+# to the kernel source it was measured on: if the source's SHA-256 differs,
+# "traffic" is reported as null.
+PROFILED_TRAFFIC = {
+    "fp32": {"source": "dense_gemm_transformer_gb300/csrc/simt.cu", "sha256": None, "bytes_per_launch": None,
+             "capture": "profiles/simt_gemm_kernel_dram_per_launch.md"},
+}
+
+
+def profiled_traffic(family):
+    import hashlib
+    rec = PROFILED_TRAFFIC.get(family)
+    if not rec or rec["sha256"] is None:
+        return None
+    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != rec["sha256"]:
+            return None
+    return rec["bytes_per_launch"]
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     src = "measured"
@@ -334,7 +355,8 @@ def bench_ours(args, world, rank, local):
                 "peak": pk["tf32_tflops_sustained"], "unit": "TFLOP/s",
                 "peak_source": f"{pk['source']} bf16 sustained x 1.1/2.25 (nominal tf32/bf16)"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = profiled_traffic(dom)
+    roof["algorithmic_bytes_per_launch"] = sum(c.bytes() for c in calls if c.mode == dom) / max(n_launch, 1)
     roof["launches_per_step"] = n_launch
     roof["share_of_step"] = fam_ms[dom] / sum(per_call_ms)
 
