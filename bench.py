@@ -100,12 +100,18 @@ class Call:
 
 def gpt_workload(device):
     """Inputs X, W, dY of every projection and one output per (mode, GEMM)."""
-    calls, inputs = [], []
-    cases = si.gpt_cases()
+    inputs = []
     for p, (name, kin, nout) in enumerate(si.GPT_PROJECTIONS):
         X, W, dY = si.gpt_tensors(p, kin, nout)
         inputs += [X, W, dY]
     dev_inputs = [t.to(device) for t in inputs]
+    return gpt_calls(dev_inputs, device), inputs, dev_inputs
+
+
+def gpt_calls(dev_inputs, device):
+    """The 30 GEMMs of a step on the given device inputs, each with its own C."""
+    calls = []
+    cases = si.gpt_cases()
     for mode in ("fp32", "tf32"):
         for p in range(len(si.GPT_PROJECTIONS)):
             X, W, dY = dev_inputs[3 * p: 3 * p + 3]
@@ -113,7 +119,7 @@ def gpt_workload(device):
             calls.append(Call(fwd, mode, X, W, torch.empty((fwd.M, fwd.N), device=device)))
             calls.append(Call(dx, mode, dY, W, torch.empty((dx.M, dx.N), device=device)))
             calls.append(Call(dw, mode, X, dY, torch.empty((dw.M, dw.N), device=device)))
-    return calls, inputs, dev_inputs
+    return calls
 
 
 def run_call(h, c: Call, stream):
@@ -361,42 +367,60 @@ def bench_ours(args, world, rank, local):
     roof["share_of_step"] = fam_ms[dom] / sum(per_call_ms)
 
     # End to end through the C ABI: pinned host inputs -> device, the 30 GEMMs,
-    # every output -> pinned host, all inside the timed region.  The inputs go
-    # up on one copy stream; each output goes down on another as soon as its
-    # GEMM has finished, overlapping the GEMMs that follow (the next step's
-    # uploads wait for this step's GEMMs, its GEMMs for this step's downloads).
+    # every output -> pinned host, all inside the timed region.  Inputs and
+    # outputs are double-buffered on the device so that step s+1's uploads
+    # (one copy stream) run while step s computes, and each output goes down
+    # on another copy stream as soon as its GEMM has finished.
     e2e = None
     if not args.no_e2e:
         pinned_in = [t.pin_memory() for t in host_inputs]
-        pinned_out = [torch.empty(c.C.shape, dtype=c.C.dtype, pin_memory=True) for c in calls]
         h2d = sum(t.numel() * t.element_size() for t in pinned_in)
+        dev_inputs2 = [torch.empty_like(t) for t in dev_inputs]
+        bufs = [(dev_inputs, calls), (dev_inputs2, gpt_calls(dev_inputs2, dev))]
+        if args.only:
+            import re
+            bufs[1] = (dev_inputs2, [c for c in bufs[1][1] if re.fullmatch(args.only, c.name)])
+        pinned_out = [torch.empty(c.C.shape, dtype=c.C.dtype, pin_memory=True) for c in calls]
         d2h = sum(t.numel() * t.element_size() for t in pinned_out)
         up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         done = [torch.cuda.Event() for _ in calls]
+        up_done = [torch.cuda.Event(), torch.cuda.Event()]
+        comp_done = [torch.cuda.Event(), torch.cuda.Event()]
+        down_done = [torch.cuda.Event(), torch.cuda.Event()]
 
-        def e2e_step():
-            up.wait_stream(stream)
+        def e2e_step(s):
+            b = s % 2
+            ins, cls = bufs[b]
+            up.wait_event(comp_done[b])  # the GEMMs that last read these inputs are done
             with torch.cuda.stream(up):
-                for src, dst in zip(pinned_in, dev_inputs):
+                for src, dst in zip(pinned_in, ins):
                     dst.copy_(src, non_blocking=True)
-            stream.wait_stream(up)
-            stream.wait_stream(down)
-            for c, dst, ev in zip(calls, pinned_out, done):
+            up_done[b].record(up)
+            stream.wait_event(up_done[b])
+            stream.wait_event(down_done[b])  # these outputs have been downloaded
+            for c, dst, ev in zip(cls, pinned_out, done):
                 run_call(h, c, stream)
                 ev.record(stream)
                 down.wait_event(ev)
                 with torch.cuda.stream(down):
                     dst.copy_(c.C, non_blocking=True)
+            comp_done[b].record(stream)
+            down_done[b].record(down)
+
+        def run_steps(n):
+            up.wait_stream(stream)
+            down.wait_stream(stream)
+            for s in range(n):
+                e2e_step(s)
+            stream.wait_stream(up)
             stream.wait_stream(down)
 
-        for _ in range(2):
-            e2e_step()
+        run_steps(2)
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        run_steps(args.steps)
         e1.record(stream)
         stream.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / args.steps
@@ -451,8 +475,9 @@ def bench_sweep(args):
     Each shape: warm-up, then R back-to-back launches between two CUDA events
     on the launching stream, with the operands rotated over enough copies that
     the working set of one rotation exceeds 3x the L2 (so every launch reads
-    its weights from HBM).  Skinny shapes are also timed as back-to-back
-    replays of one-call CUDA graphs, which removes the host's per-call cost.
+    its weights from HBM).  The reported time is for calls that run back to
+    back on the device (a spin kernel holds the stream while the host enqueues
+    them); "ms_stream" is the same calls as the host issues them.
     """
     import dense_gemm_transformer_gb300 as dg
     dev = torch.device("cuda", 0)
@@ -491,6 +516,8 @@ def bench_sweep(args):
         stream.synchronize()
         plan = h.plan()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # Launches as the host issues them (includes the host's per-call cost
+        # whenever it exceeds the kernel time) ...
         with torch.cuda.stream(stream):
             e0.record(stream)
             for r in range(reps):
@@ -499,30 +526,20 @@ def bench_sweep(args):
             e1.record(stream)
         stream.synchronize()
         ms = e0.elapsed_time(e1) / reps
-        graph_ms = None
-        if args.workload == "skinny":
-            # One CUDA graph per operand copy, each holding one call; the
-            # replays run back to back without the host's per-call cost.
-            graphs = []
-            for A, B, C in sets:
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta,
-                          stream=stream)
-                graphs.append(g)
-            with torch.cuda.stream(stream):
-                for g in graphs:
-                    g.replay()
-            stream.synchronize()
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                for r in range(reps):
-                    graphs[r % copies].replay()
-                e1.record(stream)
-            stream.synchronize()
-            graph_ms = e0.elapsed_time(e1) / reps
+        # ... and back to back on the device: a spin kernel holds the stream
+        # while the host enqueues all the calls, so the timed calls run with
+        # no host gaps between them.
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(max(4e6, reps * 1e5)))  # ~50 us of spin per queued call
+            e0.record(stream)
+            for r in range(reps):
+                A, B, C = sets[r % copies]
+                h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta, stream=stream)
+            e1.record(stream)
+        stream.synchronize()
+        dev_ms = e0.elapsed_time(e1) / reps
         assert h.check_device(stream) == 0
-        t = graph_ms if graph_ms is not None else ms
+        t = dev_ms
         byts = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N * (2 if beta != 0 else 1)
         peak = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops"], "bf16": pk["bf16_tflops"]}[mode]
         t_c, t_m = c.flops / (peak * 1e12), byts / (pk["hbm_gbs"] * 1e9)
