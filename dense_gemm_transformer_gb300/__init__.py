@@ -22,7 +22,7 @@ from . import _build
 
 MODES = {"fp32": 0, "tf32": 1, "bf16": 2}
 FAMILIES = {"auto": 0, "simt": 1, "tc": 2, "skinny": 3}
-OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3, "pretranspose": 4}
+OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3, "pretranspose": 4, "pair": 5}
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED", 3: "GEMM_ERR_MISALIGNED",
           4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_ALLOC", 6: "GEMM_ERR_DEVICE_TIMEOUT", 7: "GEMM_ERR_TOO_LARGE"}
 HEADER = os.path.join(_build.ROOT, "include", "gemm.h")
@@ -38,7 +38,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("family", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("tile_k", ctypes.c_int32), ("split_k", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("kernels", ctypes.c_int32), ("packed", ctypes.c_int32),
-                ("schedule", ctypes.c_int32), ("reserved", ctypes.c_int32 * 6)]
+                ("schedule", ctypes.c_int32), ("cluster", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
 
 
 _lib = None
@@ -147,7 +147,8 @@ class Gemm:
         return {"family": fam if p.kernels else "none", "tile_m": p.tile_m, "tile_n": p.tile_n,
                 "tile_k": p.tile_k, "split_k": p.split_k, "stages": p.stages, "grid": p.grid,
                 "kernels": p.kernels, "packed": p.packed,
-                "schedule": {0: "tiles", 1: "split_k", 2: "stream_k"}.get(p.schedule, "tiles")}
+                "schedule": {0: "tiles", 1: "split_k", 2: "stream_k"}.get(p.schedule, "tiles"),
+                "cluster": p.cluster}
 
     def check_device(self, stream=None) -> int:
         """Synchronize the stream and return the device status (0 = ok)."""

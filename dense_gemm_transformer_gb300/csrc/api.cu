@@ -39,6 +39,7 @@ struct gemm_handle_s {
   int opt_split_k = 0;
   int opt_tile_n = 0;
   int opt_pretranspose = 0;
+  int opt_pair = 0;
   gemm_plan_t plan{};
 };
 
@@ -397,8 +398,18 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   // finish a tile sums the slices); the other forms use the reduce kernel.
   const bool fused = swap && splits > 1 && tiles <= kCounterTiles;
   a.counters = fused ? h->d_counters : nullptr;
-  a.grid = static_cast<int>(std::min<int64_t>(tiles * splits, sms));
-  a.group_m = 16;
+  // Two-CTA clusters sharing each B tile (TMA multicast) for 256-column
+  // tiles with at least two rows of tiles: each CTA then pulls 32 KB per
+  // stage from L2 instead of 48 KB.
+  const int64_t tm_tiles = ceil_div(Mk, 128);
+  a.pair = (!swap && tile_n == 256 && tm_tiles >= 2 && h->opt_pair != 1) ? 1 : 0;
+  if (a.pair) {
+    const int64_t units = ceil_div(tm_tiles, 2) * ceil_div(Nk, tile_n) * splits;
+    a.grid = static_cast<int>(2 * std::min<int64_t>(units, sms / 2));
+  } else {
+    a.grid = static_cast<int>(std::min<int64_t>(tiles * splits, sms));
+  }
+  a.group_m = a.pair ? 8 : 16;
   if (launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
   ++kernels;
   if (splits > 1 && !fused) {
@@ -408,6 +419,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   }
   set_plan(h, swap ? GEMM_FAMILY_SKINNY : GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n),
            a.grid, kernels, (swap ? ((pack_b ? 1 : 0) | (pack_a ? 2 : 0)) : ((pack_a ? 1 : 0) | (pack_b ? 2 : 0))));
+  h->plan.cluster = a.pair ? 2 : 1;
   return GEMM_OK;
 }
 
@@ -528,6 +540,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, int option, int64_t value) {
     case GEMM_OPT_PRETRANSPOSE:
       if (value < 0 || value > 2) return GEMM_ERR_INVALID_VALUE;
       h->opt_pretranspose = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_PAIR:
+      if (value < 0 || value > 1) return GEMM_ERR_INVALID_VALUE;
+      h->opt_pair = static_cast<int>(value);
       return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_VALUE;

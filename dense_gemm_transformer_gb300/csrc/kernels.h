@@ -51,7 +51,8 @@ struct TcArgs {
   int mode;              // 1 = tf32, 2 = bf16 (gemm_mode_t)
   int a_mn_major;        // A stored with M contiguous (transA == 1)
   int b_mn_major;        // B stored with N contiguous (transB == 0)
-  int tile_n;            // 128 or 256
+  int tile_n;            // 128 or 256 (16: the swapped small-M form)
+  int pair;              // tile_n 256: two-CTA clusters sharing each B tile by TMA multicast
   int64_t M, N, K;
   const void* A;         // base of the (possibly re-packed) operand
   int64_t lda;           // elements

@@ -83,8 +83,10 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   e = a.a_mn_major ? encode_2d(&ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
                    : encode_2d(&ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
   if (e != cudaSuccess) return e;
+  // A pair of CTAs loads one half of each B tile apiece (K-major: half the rows).
+  const bool pair = a.pair != 0 && a.tile_n == 256;
   e = a.b_mn_major ? encode_2d(&tb, a.mode, a.B, a.N, a.K, a.ldb, ch, bk)
-                   : encode_2d(&tb, a.mode, a.B, a.K, a.N, a.ldb, bk, a.tile_n);
+                   : encode_2d(&tb, a.mode, a.B, a.K, a.N, a.ldb, bk, pair ? a.tile_n / 2 : a.tile_n);
   if (e != cudaSuccess) return e;
 
   TcParams p;
@@ -92,6 +94,7 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.N = static_cast<int>(a.N);
   p.K = static_cast<int>(a.K);
   p.num_tm = static_cast<int>((a.M + 127) / 128);
+  if (pair) p.num_tm = (p.num_tm + 1) / 2;  // units are pairs of vertically adjacent tiles
   p.num_tn = static_cast<int>((a.N + a.tile_n - 1) / a.tile_n);
   p.num_kb = static_cast<int>((a.K + bk - 1) / bk);
   p.splits = a.splits;
@@ -122,8 +125,8 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
     }
   }
   if (a.mode == 2)
-    return tc_launch_bf16(a.tile_n, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
-  return tc_launch_tf32(a.tile_n, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
+    return tc_launch_bf16(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
+  return tc_launch_tf32(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
 }
 
 }  // namespace dgt

@@ -2,8 +2,8 @@
 #include "tc_launch.cuh"
 
 namespace dgt {
-cudaError_t tc_launch_bf16(int tile_n, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t tc_launch_bf16(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s) {
-  return tc_launch_mode<2>(tile_n, a_mn, b_mn, ta, tb, tc, p, grid, s);
+  return tc_launch_mode<2>(tile_n, pair, a_mn, b_mn, ta, tb, tc, p, grid, s);
 }
 }  // namespace dgt

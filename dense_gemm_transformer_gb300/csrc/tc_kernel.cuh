@@ -131,7 +131,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
 // TRANS_C: the kernel computes C^T = op(B)^T op(A)^T with the operands
 // swapped by the host (a small-M product whose weights fill the 128-row MMA
 // side), so element (r, c) of its tile is stored at C[c * ldc + r].
-template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C>
+// PAIR: the grid is made of two-CTA clusters that work on vertically
+// adjacent tiles (same columns) in lockstep; each CTA loads its own A tile
+// and one half of the shared B tile, which TMA multicast writes into both
+// CTAs' shared memory, so each stage costs each CTA 16 KB of L2 traffic for
+// B instead of 32 KB.  A stage may be refilled only when both CTAs' MMAs have
+// read it: each MMA warp commits to the "empty" barrier of both CTAs.
+template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -156,11 +162,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  static_assert(!PAIR || (!TRANS_C && BN >= 128), "paired CTAs share a B tile of 128 or 256 columns");
+  // Work units: one per CTA, or one per two-CTA cluster (the pair's rank
+  // picks its row of tiles).  The cluster of a pair is blockIdx.x / 2.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  auto tile_row = [&](const Unit& w) { return PAIR ? 2 * w.tm + static_cast<int>(rank) : w.tm; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), PAIR ? 2 : 1);  // PAIR: both CTAs' MMAs must have read the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
@@ -182,6 +195,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // PAIR: the peer's barriers must be initialised before any multicast copy
+  // or commit can signal them.
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -192,8 +208,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Unit w = decode_unit(u, p);
+        const int tm = tile_row(w);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, kDevTimeoutEmpty)) {
             ok = false;
@@ -207,11 +224,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (A_MN) {
 #pragma unroll
             for (int c = 0; c < Cfg::BM / Cfg::CH; ++c)
-              tma_load_2d(a_dst + c * Cfg::BK * 128, &tmA, fb, w.tm * Cfg::BM + c * Cfg::CH, k0);
+              tma_load_2d(a_dst + c * Cfg::BK * 128, &tmA, fb, tm * Cfg::BM + c * Cfg::CH, k0);
           } else {
-            tma_load_2d(a_dst, &tmA, fb, k0, w.tm * Cfg::BM);
+            tma_load_2d(a_dst, &tmA, fb, k0, tm * Cfg::BM);
           }
-          if (B_MN) {
+          if constexpr (PAIR) {
+            // This CTA's half of B, written into both CTAs of the pair.
+            constexpr uint16_t kBoth = 0x3;
+            if (B_MN) {
+              constexpr int NC = BN / Cfg::CH;
+#pragma unroll
+              for (int c = static_cast<int>(rank) * NC / 2; c < (static_cast<int>(rank) + 1) * NC / 2; ++c)
+                tma_load_2d_multicast(b_dst + c * Cfg::BK * 128, &tmB, fb, w.tn * BN + c * Cfg::CH, k0, kBoth);
+            } else {
+              tma_load_2d_multicast(b_dst + rank * (BN / 2) * 128, &tmB, fb, k0, w.tn * BN + rank * (BN / 2), kBoth);
+            }
+          } else if (B_MN) {
 #pragma unroll
             for (int c = 0; c < BN / Cfg::CH; ++c)
               tma_load_2d(b_dst + c * Cfg::BK * 128, &tmB, fb, w.tn * BN + c * Cfg::CH, k0);
@@ -239,7 +267,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Unit w = decode_unit(u, p);
         if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty)) break;
         tc_fence_after();
@@ -260,7 +288,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                      : smem_desc_sw128(b_base + j * Cfg::UK * Cfg::ES, 16, 1024);
             issue_mma<MODE>(d_tmem, ad, bd, IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
           }
-          mma_commit(empty_bar(stage));
+          if constexpr (PAIR)
+            mma_commit_multicast(empty_bar(stage), 0x3);  // both CTAs' copies of the stage are free
+          else
+            mma_commit(empty_bar(stage));
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -286,11 +317,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool partial = p.splits > 1;
     const bool read_c = !partial && p.beta != 0.f;
     constexpr int CW = Cfg::CW;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    for (int u = unit0; u < p.num_units; u += unit_step) {
       const Unit w = decode_unit(u, p);
       if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull)) break;
       tc_fence_after();
-      const int64_t row = static_cast<int64_t>(w.tm) * Cfg::BM + sub * 32 + lane;
+      const int tm = tile_row(w);
+      const int64_t row = static_cast<int64_t>(tm) * Cfg::BM + sub * 32 + lane;
       const bool row_ok = row < p.M;
       float* base = partial ? p.ws + static_cast<int64_t>(w.split) * p.ws_slice : p.C;
       const int64_t ld = partial ? p.ws_ld : p.ldc;
@@ -330,7 +362,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(&tmC, smem_u32(buf), static_cast<int32_t>(col0), w.tm * Cfg::BM + sub * 32,
+              tma_store_3d(&tmC, smem_u32(buf), static_cast<int32_t>(col0), tm * Cfg::BM + sub * 32,
                            partial ? w.split : 0);
               bulk_commit_group();
             }
@@ -446,6 +478,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // PAIR: the peer may still commit to this CTA's barriers until it is done.
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

@@ -76,8 +76,10 @@ typedef enum {
   GEMM_OPT_FAMILY = 1,   /* value: gemm_family_t; AUTO lets the planner choose            */
   GEMM_OPT_SPLIT_K = 2,  /* value: 0 = planner's choice, n >= 1 = force n slices of K      */
   GEMM_OPT_TILE_N = 3,   /* value: 0 = planner's choice, 128 or 256 (TC and SIMT families)  */
-  GEMM_OPT_PRETRANSPOSE = 4 /* SIMT: 0 = planner's choice, 1 = never, 2 = always transpose
-                               K-contiguous operands into the workspace first             */
+  GEMM_OPT_PRETRANSPOSE = 4, /* SIMT: 0 = planner's choice, 1 = never, 2 = always transpose
+                                K-contiguous operands into the workspace first             */
+  GEMM_OPT_PAIR = 5          /* TC: 0 = two-CTA clusters sharing B tiles where the planner
+                                chooses them, 1 = never                                     */
 } gemm_option_t;
 
 /* What the last successful gemm_run on a handle launched. */
@@ -90,7 +92,8 @@ typedef struct {
   int32_t kernels;       /* kernels launched by the call */
   int32_t packed;        /* bit 0: A re-packed (or transposed), bit 1: B, into the workspace */
   int32_t schedule;      /* SIMT: 0 one CTA per tile, 1 split-K slices, 2 stream-K */
-  int32_t reserved[6];
+  int32_t cluster;       /* TC: CTAs per cluster (2 = pairs sharing each B tile) */
+  int32_t reserved[5];
 } gemm_plan_t;
 
 /* Create a handle on the current device.  Reads the device properties and

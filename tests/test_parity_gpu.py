@@ -35,6 +35,7 @@ def _reset(h):
     h.set_option("split_k", 0)
     h.set_option("tile_n", 0)
     h.set_option("pretranspose", 0)
+    h.set_option("pair", 0)
     yield
 
 
@@ -86,6 +87,23 @@ def test_tc_tile_widths(h, mode, tile_n, tA, tB):
     h.set_option("tile_n", tile_n)
     _cases.run_and_check(h, mode, 384, 520, 160, tA, tB, seed=19, dist="normal")
     assert h.plan()["family"] == "tc" and h.plan()["tile_n"] == tile_n
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("tA,tB", TRANS)
+@pytest.mark.parametrize("M,N,K", [(640, 600, 200), (300, 260, 1000), (1100, 300, 64)])
+def test_tc_paired_ctas(h, mode, pair, tA, tB, M, N, K):
+    """256-column tiles with and without two-CTA clusters sharing B tiles by
+    TMA multicast; odd tile-row counts leave the second CTA of the last pair
+    with no rows of C."""
+    h.set_option("tile_n", 256)
+    h.set_option("pair", pair)
+    _cases.run_and_check(h, mode, M, N, K, tA, tB, alpha=0.5, beta=-1.0, seed=77, dist="normal")
+    assert h.plan()["cluster"] == (1 if pair else 2)
+    _cases.run_and_check(h, mode, M, N, min(K, 1024), tA, tB, seed=78, dist="int", exact=True)
+    h.set_option("split_k", 3)
+    _cases.run_and_check(h, mode, M, N, K, tA, tB, seed=79, dist="normal")
 
 
 @pytest.mark.parametrize("mode", MODES)
