@@ -27,12 +27,12 @@
 
 #include "gemm.h"
 #include "kernels.h"
+#include "skinny.cuh"
 
 struct gemm_handle_s {
   int device = 0;
   int sms = 0;
   int* d_status = nullptr;
-  int* d_counters = nullptr;  // per-tile arrival counters of the fused K-slice reduction (zero between calls)
   void* ws = nullptr;
   size_t ws_bytes = 0;
   int opt_family = GEMM_FAMILY_AUTO;
@@ -40,13 +40,13 @@ struct gemm_handle_s {
   int opt_tile_n = 0;
   int opt_pretranspose = 0;
   int opt_pair = 0;
+  int sk_active[2][dgt::kSkinnyMaxCluster + 1];  // small-M kernel: resident clusters (-1: not queried)
   gemm_plan_t plan{};
 };
 
 namespace {
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
-constexpr int64_t kCounterTiles = 16384;  // tiles the fused K-slice reduction can count
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -289,6 +289,23 @@ int64_t skinny_splits(int64_t tiles, int64_t kb, int sms) {
   return best;
 }
 
+// K slices (= CTAs per cluster) for the small-M kernel: as many as one wave
+// of two resident CTAs per SM holds, at least two K blocks per slice, at
+// most 16, and above the portable cluster size of 8 only a size the device
+// can launch.  (Measured on the decode shapes: 280 CTAs for 70 tiles and
+// 192 for 12 tiles ran fastest; 140 and 96 ran 25-30% slower.)
+int64_t skinny_cluster_size(gemm_handle_s* h, int mode, bool a_mn, int64_t tiles, int64_t kb) {
+  int64_t cs = std::min<int64_t>(2 * h->sms / tiles, dgt::kSkinnyMaxCluster);
+  cs = std::max<int64_t>(1, std::min<int64_t>(cs, kb / 2));
+  while (cs > 8) {
+    int& act = h->sk_active[mode == GEMM_MODE_BF16 ? 1 : 0][cs];
+    if (act < 0) act = dgt::skinny_max_active_clusters(mode, a_mn, static_cast<int>(cs));
+    if (act > 0) break;
+    --cs;
+  }
+  return cs;
+}
+
 gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
                      float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
                      int64_t ldc, cudaStream_t s, bool swap) {
@@ -318,8 +335,16 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   }
   const int64_t tiles = ceil_div(Mk, 128) * ceil_div(Nk, tile_n);
   const int64_t kb = ceil_div(K, bk);
+  // Small M with fewer than two waves of weight tiles: the cluster kernel
+  // (one tile and K slice per CTA, slices reduced within the cluster).
+  // With more tiles, the persistent kernel streams them without a split.
+  const bool cluster_form = swap && tiles < 2 * sms;
   int64_t splits = 1;
-  if (h->opt_split_k > 0) {
+  if (cluster_form) {
+    splits = (h->opt_split_k > 0)
+                 ? std::min<int64_t>({static_cast<int64_t>(h->opt_split_k), dgt::kSkinnyMaxCluster, kb})
+                 : skinny_cluster_size(h, mode, mode == GEMM_MODE_BF16 && ta_k != 0, tiles, kb);
+  } else if (h->opt_split_k > 0) {
     splits = std::min<int64_t>(h->opt_split_k, kb);
   } else if (swap) {
     // Split K only when the tiles alone leave SMs idle: with two or more
@@ -345,7 +370,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   L.b_off = round_up(static_cast<int64_t>(pa.bytes), 256);
   L.p_off = L.b_off + round_up(static_cast<int64_t>(pb.bytes), 256);
   const int64_t ws_ld = round_up(N, 4);
-  L.total = L.p_off + (splits > 1 ? static_cast<size_t>(splits * M * ws_ld) * sizeof(float) : 0);
+  L.total = L.p_off + (splits > 1 && !cluster_form ? static_cast<size_t>(splits * M * ws_ld) * sizeof(float) : 0);
   if (L.total > 0) {
     gemm_status_t st = ensure_ws(h, L.total);
     if (st != GEMM_OK) return st;
@@ -390,14 +415,20 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.beta = beta;
   a.splits = static_cast<int>(splits);
   a.kb_per_split = static_cast<int>(kb_per);
+  if (cluster_form) {
+    a.status = h->d_status;
+    a.grid = static_cast<int>(tiles * splits);
+    if (launch_skinny(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    ++kernels;
+    set_plan(h, GEMM_FAMILY_SKINNY, 128, 16, bk, a.splits, dgt::kSkinnyStages, a.grid, kernels,
+             (pack_b ? 1 : 0) | (pack_a ? 2 : 0));
+    h->plan.cluster = a.splits;
+    return GEMM_OK;
+  }
   a.ws = splits > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
   a.ws_ld = ws_ld;
   a.ws_slice = M * ws_ld;  // partial sums are kept in the caller's M x N orientation
   a.status = h->d_status;
-  // The swapped form reduces its K slices inside the kernel (the last CTA to
-  // finish a tile sums the slices); the other forms use the reduce kernel.
-  const bool fused = swap && splits > 1 && tiles <= kCounterTiles;
-  a.counters = fused ? h->d_counters : nullptr;
   // Two-CTA clusters sharing each B tile (TMA multicast) for 256-column
   // tiles with at least two rows of tiles: each CTA then pulls 32 KB per
   // stage from L2 instead of 48 KB.
@@ -412,7 +443,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.group_m = a.pair ? 8 : 16;
   if (launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
   ++kernels;
-  if (splits > 1 && !fused) {
+  if (splits > 1) {
     if (launch_splitk_reduce(M, N, a.splits, a.ws, ws_ld, C, ldc, alpha, beta, s) != cudaSuccess)
       return GEMM_ERR_CUDA;
     ++kernels;
@@ -446,24 +477,14 @@ gemm_status_t gemm_create(gemm_handle_t* out) {
   if (h == nullptr) return GEMM_ERR_ALLOC;
   h->device = dev;
   h->sms = sms;
+  for (auto& per_mode : h->sk_active)
+    for (int& n : per_mode) n = -1;
   if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess) {
     cudaGetLastError();
     delete h;
     return GEMM_ERR_ALLOC;
   }
   if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
-    cudaFree(h->d_status);
-    delete h;
-    return GEMM_ERR_CUDA;
-  }
-  if (cudaMalloc(&h->d_counters, kCounterTiles * sizeof(int)) != cudaSuccess) {
-    cudaGetLastError();
-    cudaFree(h->d_status);
-    delete h;
-    return GEMM_ERR_ALLOC;
-  }
-  if (cudaMemset(h->d_counters, 0, kCounterTiles * sizeof(int)) != cudaSuccess) {
-    cudaFree(h->d_counters);
     cudaFree(h->d_status);
     delete h;
     return GEMM_ERR_CUDA;
@@ -480,7 +501,6 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
   gemm_status_t st = cuda_status(cudaDeviceSynchronize());
   if (h->ws) cudaFree(h->ws);
   if (h->d_status) cudaFree(h->d_status);
-  if (h->d_counters) cudaFree(h->d_counters);
   cudaSetDevice(prev);
   delete h;
   return st;
@@ -562,9 +582,7 @@ gemm_status_t gemm_check_device(gemm_handle_t h, void* stream) {
   int v = 0;
   if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
   if (v != 0) {
-    // An abandoned kernel may have left tile counters mid-count.
     if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
-    if (cudaMemset(h->d_counters, 0, kCounterTiles * sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
     return GEMM_ERR_DEVICE_TIMEOUT;
   }
   return GEMM_OK;

@@ -67,8 +67,6 @@ struct TcArgs {
   int64_t ws_ld;
   int64_t ws_slice;      // elements between successive K slices' partial sums
   int* status;           // device status word
-  int* counters;         // tile_n == 16 with splits > 1: zeroed per-tile counters for the fused
-                         // reduction (null: the caller launches launch_splitk_reduce)
   int grid;              // persistent CTAs
   int group_m;           // raster group height in M tiles
 };
@@ -80,6 +78,11 @@ constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);  // producer + MMA warps + ep
 int tc_tile_k(int mode);              // k elements per stage (128 bytes)
 int tc_stages(int mode, int tile_n);  // pipeline depth
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream);
+// The small-M kernel (tile_n 16, operands swapped as for launch_tc): one
+// (tile, K slice) per CTA, `splits` K slices per cluster reduced in
+// distributed shared memory (ws and group_m unused), grid = tiles
+// * splits.
+cudaError_t launch_skinny(const TcArgs& a, cudaStream_t stream);
 cudaError_t tc_init_driver();         // resolves cuTensorMapEncodeTiled once
 
 // ---------------------------------------------------------------- helpers

@@ -1,0 +1,41 @@
+// skinny.cuh -- parameters and launcher of the small-M (decode-shaped) kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace dgt {
+
+// The kernel computes C^T = W^T X^T for C = X W with X of M <= 16 rows: the
+// weights W are its 128-row MMA operand ("A", tiles of 128 weight columns
+// of C), the activations X its 16-column operand ("B", K-major, rows past M
+// zero-filled by the TMA unit).  Tile t covers C[:, 128 t .. 128 t + 127].
+struct SkParams {
+  int M;        // rows of the kernel's A: the caller's N (columns of C)
+  int N;        // rows of the kernel's B: the caller's M (<= 16)
+  int num_kb;   // K blocks of 128 bytes
+  int kb_per;   // K blocks per slice
+  int cluster;  // K slices = CTAs per cluster (1: no split)
+  float alpha, beta;
+  float* C;     // caller's C, element (m, n) at C[m * ldc + n]
+  int64_t ldc;
+  int* status;  // device status word (bounded waits)
+};
+
+constexpr int kSkinnyThreads = 192;  // TMA producer warp, MMA warp, four epilogue warps
+constexpr int kSkinnyMaxCluster = 16;
+
+constexpr int kSkinnyStages = 6;  // ~109 KB of shared memory: two CTAs per SM
+
+// Launch on `grid` = tiles * p.cluster CTAs, clusters of p.cluster CTAs
+// along x, with programmatic dependent launch.  a_mn: the weights are stored
+// with the caller's N contiguous (transB == 0); BF16 only.
+cudaError_t skinny_launch(int mode, bool a_mn, const CUtensorMap& ta, const CUtensorMap& tb, const SkParams& p,
+                          int grid, cudaStream_t s);
+// Clusters of `cluster` CTAs of the kernel that can be resident at once
+// (0 when that cluster size cannot be launched).
+int skinny_max_active_clusters(int mode, bool a_mn, int cluster);
+
+}  // namespace dgt

@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "skinny.cuh"
 #include "tc_launch.cuh"
 
 namespace dgt {
@@ -109,7 +110,6 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.ws_ld = a.ws_ld;
   p.ws_slice = a.ws_slice;
   p.status = a.status;
-  p.counters = (a.tile_n == 16 && a.splits > 1) ? a.counters : nullptr;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
   // Tiles leave through TMA stores when the destination allows it: not the
   // transposed small-M form, no read of C (beta == 0, or partial sums), and
@@ -127,6 +127,32 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   if (a.mode == 2)
     return tc_launch_bf16(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
   return tc_launch_tf32(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
+}
+
+cudaError_t launch_skinny(const TcArgs& a, cudaStream_t stream) {
+  cudaError_t e = tc_init_driver();
+  if (e != cudaSuccess) return e;
+  const int bk = tc_tile_k(a.mode);
+  const int ch = (a.mode == 2) ? 64 : 32;
+  CUtensorMap ta, tb;
+  e = a.a_mn_major ? encode_2d(&ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
+                   : encode_2d(&ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
+  if (e != cudaSuccess) return e;
+  if (a.b_mn_major) return cudaErrorInvalidValue;
+  e = encode_2d(&tb, a.mode, a.B, a.K, a.N, a.ldb, bk, 16);
+  if (e != cudaSuccess) return e;
+  SkParams p;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.num_kb = static_cast<int>((a.K + bk - 1) / bk);
+  p.kb_per = a.kb_per_split;
+  p.cluster = a.splits;
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.status = a.status;
+  return skinny_launch(a.mode, a.a_mn_major != 0, ta, tb, p, a.grid, stream);
 }
 
 }  // namespace dgt

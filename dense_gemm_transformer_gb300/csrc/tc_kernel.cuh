@@ -53,8 +53,6 @@ struct TcParams {
   int64_t ws_ld;
   int64_t ws_slice;  // elements between the partial sums of successive K slices
   int* status;
-  int* counters;  // swapped form with K slices: per-tile arrival counts (all zero between calls),
-                  // or null to leave the reduction of the slices to a separate kernel
   int c_vec;  // C rows are 16-byte aligned (ldc % 4 == 0 and C aligned)
   int c_tma;  // tiles leave through shared memory and TMA stores (tmC is valid)
 };
@@ -117,17 +115,6 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
   return w;
 }
 
-// Bounded wait used only on the abort path: it ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      atomicExch(status, kDevTimeoutDrain);
-      return;
-    }
-  }
-}
-
 // TRANS_C: the kernel computes C^T = op(B)^T op(A)^T with the operands
 // swapped by the host (a small-M product whose weights fill the 128-row MMA
 // side), so element (r, c) of its tile is stored at C[c * ldc + r].
@@ -151,7 +138,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = abort_flag + 1;  // epilogue: this CTA reduces the tile's K slices
 
   const uint32_t smem0 = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
@@ -418,57 +404,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
-      }
-      if constexpr (TRANS_C) {
-        // Fused K-slice reduction: the CTA whose slice of a tile arrives last
-        // sums all the tile's slices in slice order and writes C (the same
-        // order and arithmetic as the separate reduce kernel).  The partial
-        // stores above are made visible before the arrival is counted, and
-        // the last arriver reads the slices from L2 (no stale L1 lines).
-        if (partial && p.counters != nullptr && half == 0) {
-          __threadfence();
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-          const int tile_id = w.tm * p.num_tn + w.tn;
-          if (warp == 2 && lane == 0) *last_flag = (atomicAdd(p.counters + tile_id, 1) == p.splits - 1) ? 1 : 0;
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-          if (*last_flag) {
-            __threadfence();
-            if (row_ok) {
-              // Up to 4 slices x BN columns of loads in flight per round; each
-              // column still sums its slices in ascending order.
-              const int64_t col0 = static_cast<int64_t>(w.tn) * BN;
-              const float* src = p.ws + col0 * p.ws_ld + row;
-              float sum[BN];
-#pragma unroll
-              for (int j = 0; j < BN; ++j) sum[j] = 0.f;
-              for (int sp0 = 0; sp0 < p.splits; sp0 += 4) {
-                float v[4][BN];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                  for (int j = 0; j < BN; ++j)
-                    v[q][j] = (sp0 + q < p.splits && col0 + j < p.N)
-                                  ? __ldcg(src + (sp0 + q) * p.ws_slice + j * p.ws_ld)
-                                  : 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                  for (int j = 0; j < BN; ++j)
-                    if (sp0 + q < p.splits) sum[j] = (sp0 + q == 0) ? v[q][j] : sum[j] + v[q][j];
-              }
-#pragma unroll
-              for (int j = 0; j < BN; ++j) {
-                if (col0 + j < p.N) {
-                  float* dst = p.C + (col0 + j) * p.ldc + row;
-                  float out = p.alpha * sum[j];
-                  if (p.beta != 0.f) out = fmaf(p.beta, *dst, out);
-                  *dst = out;
-                }
-              }
-            }
-            if (warp == 2 && lane == 0) p.counters[tile_id] = 0;  // ready for the next call
-          }
-        }
       }
     }
     // Every TMA store of this warp has completed before the CTA exits.

@@ -69,7 +69,7 @@ typedef enum {
   GEMM_FAMILY_AUTO = 0,
   GEMM_FAMILY_SIMT = 1,   /* register-tiled FFMA kernel (GEMM_MODE_FP32 only)           */
   GEMM_FAMILY_TC = 2,     /* persistent TMA + tcgen05 kernel, 1 CTA per tile (TF32/BF16) */
-  GEMM_FAMILY_SKINNY = 3  /* HBM-bound small-M kernel (BF16)                             */
+  GEMM_FAMILY_SKINNY = 3  /* HBM-bound small-M kernels, M <= 16 (TF32/BF16)             */
 } gemm_family_t;
 
 typedef enum {
@@ -97,9 +97,7 @@ typedef struct {
 } gemm_plan_t;
 
 /* Create a handle on the current device.  Reads the device properties and
- * allocates the 4-byte device status word and 64 KB of zeroed per-tile
- * counters (used by the small-M path's in-kernel K-slice reduction).  *out is
- * set to NULL on failure. */
+ * allocates the 4-byte device status word.  *out is set to NULL on failure. */
 gemm_status_t gemm_create(gemm_handle_t* out);
 
 /* Free the handle, its status word and its workspace.  Synchronizes the
@@ -112,7 +110,15 @@ gemm_status_t gemm_destroy(gemm_handle_t h);
  * enqueued.  M == 0 or N == 0 is a no-op.  K == 0 or alpha == 0 gives
  * C = beta * C without reading A or B.  beta == 0 writes C without reading it
  * (a NaN in C does not propagate).  C must not overlap A or B.  The workspace
- * may grow (cudaMalloc) on the first call that needs a larger one. */
+ * may grow (cudaMalloc) on the first call that needs a larger one.
+ *
+ * Small M (M <= 16, transA == 0, TF32/BF16) with fewer than two waves of
+ * 128-column weight tiles runs one kernel that splits K across the CTAs of a
+ * thread-block cluster and sums the slices in distributed shared memory (no
+ * workspace).  It is launched with programmatic dependent launch: its set-up
+ * and an L2 prefetch of the weights may overlap the end of the previous
+ * kernel in `stream`, but it reads and writes no memory before that kernel
+ * has completed, so stream order is kept. */
 gemm_status_t gemm_run(gemm_handle_t h, int mode, int transA, int transB,
                        int64_t M, int64_t N, int64_t K, float alpha,
                        const void* A, int64_t lda, const void* B, int64_t ldb,

@@ -302,6 +302,45 @@ def test_skinny_ragged(h, mode, tB, M, N, K):
     _cases.run_and_check(h, mode, M, N, K, False, tB, alpha=0.5, beta=1.0, seed=54, dist="normal")
 
 
+@pytest.mark.parametrize("mode", ["bf16", "tf32"])
+@pytest.mark.parametrize("tB", [False, True])
+@pytest.mark.parametrize("cs", [1, 2, 3, 8, 12, 16])
+def test_skinny_cluster_k_slices(h, mode, tB, cs):
+    """The small-M kernel with K cut into `cs` slices across one cluster
+    (above 8: non-portable cluster sizes), slices summed in distributed
+    shared memory; ragged N (3 tiles, the last partial) and ragged K."""
+    h.set_option("family", "skinny")
+    h.set_option("split_k", cs)
+    M, N, K = 5, 300, 3000 if mode == "bf16" else 1500
+    _cases.run_and_check(h, mode, M, N, K, False, tB, seed=61, dist="normal")
+    plan = h.plan()
+    assert plan["family"] == "skinny" and plan["split_k"] == cs and plan["cluster"] == cs
+    assert plan["grid"] == 3 * cs
+    _cases.run_and_check(h, mode, M, N, K, False, tB, alpha=0.5, beta=1.0, seed=62, dist="normal")
+
+
+@pytest.mark.parametrize("mode", ["bf16", "tf32"])
+@pytest.mark.parametrize("cs", [1, 8, 13])
+def test_skinny_cluster_integers_bit_exact(h, mode, cs):
+    h.set_option("split_k", cs)
+    K = 1024
+    _cases.run_and_check(h, mode, 16, 260, K, False, True, seed=63, dist="int", exact=True)
+    kb = -(-K // (64 if mode == "bf16" else 32))
+    per = -(-kb // cs)
+    assert h.plan()["cluster"] == -(-kb // per)  # slices actually used: none of them empty
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_skinny_one_slice_many_tiles(h, M):
+    """Between one and two waves of weight tiles: one CTA per tile, no
+    split, C written straight from TMEM."""
+    N, K = 128 * 160 - 37, 200
+    rows = [(0, M)]
+    _cases.run_and_check(h, "bf16", M, N, K, False, False, seed=64, dist="normal", rows=rows)
+    plan = h.plan()
+    assert plan["family"] == "skinny" and plan["split_k"] == 1 and plan["grid"] == 160
+
+
 def _column_ranges(N, tile=128, width=3):
     picks = sorted({0, tile - 1, N // 2, N - width})
     return [(c, min(c + width, N)) for c in picks if 0 <= c < N]
