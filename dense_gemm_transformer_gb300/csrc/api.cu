@@ -126,7 +126,8 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   // large, and slower on deep-K products with few output rows (more stream-K
   // partial traffic) or when N pads up; so 256 columns only for N % 256 == 0
   // and M >= 1024, 128 otherwise.
-  int tile_n = (h->opt_tile_n == 128 || h->opt_tile_n == 256) ? h->opt_tile_n : 0;
+  if (h->opt_tile_n != 0 && h->opt_tile_n != 128 && h->opt_tile_n != 256) return GEMM_ERR_NOT_SUPPORTED;
+  int tile_n = h->opt_tile_n;
   if (tile_n == 0) tile_n = (N % 256 == 0 && M >= 1024) ? 256 : 128;
   const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, tile_n);
   const int64_t slots = (tile_n == 256 ? 1 : 2) * static_cast<int64_t>(h->sms);  // resident CTAs
@@ -289,19 +290,19 @@ int64_t skinny_splits(int64_t tiles, int64_t kb, int sms) {
   return best;
 }
 
-// K slices (= CTAs per cluster) for the small-M kernel: as many as one wave
-// of two resident CTAs per SM holds, at least two K blocks per slice, at
-// most 16, and above the portable cluster size of 8 only a size the device
-// can launch.  (Measured on the decode shapes: 280 CTAs for 70 tiles and
-// 192 for 12 tiles ran fastest; 140 and 96 ran 25-30% slower.)
+// K slices (= CTAs per cluster) for the small-M kernel: at most as many as
+// one wave of two resident CTAs per SM holds, at least two K blocks per
+// slice, at most 16, and the largest such count of which every tile's
+// cluster can be resident at once (else the largest count).  Measured on the
+// decode shapes: 280 CTAs for 70 tiles and 192 for 12 tiles ran fastest,
+// 140 and 96 ran 25-30% slower.
 int64_t skinny_cluster_size(gemm_handle_s* h, int mode, bool a_mn, int64_t tiles, int64_t kb) {
   int64_t cs = std::min<int64_t>(2 * h->sms / tiles, dgt::kSkinnyMaxCluster);
   cs = std::max<int64_t>(1, std::min<int64_t>(cs, kb / 2));
-  while (cs > 8) {
-    int& act = h->sk_active[mode == GEMM_MODE_BF16 ? 1 : 0][cs];
-    if (act < 0) act = dgt::skinny_max_active_clusters(mode, a_mn, static_cast<int>(cs));
-    if (act > 0) break;
-    --cs;
+  for (int64_t c = cs; c >= 2; --c) {
+    int& act = h->sk_active[mode == GEMM_MODE_BF16 ? 1 : 0][c];
+    if (act < 0) act = dgt::skinny_max_active_clusters(mode, a_mn, static_cast<int>(c));
+    if (act >= tiles) return c;
   }
   return cs;
 }
@@ -322,16 +323,36 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   const void* Bk = swap ? A : B;
   const int64_t ldak = swap ? ldb : lda, ldbk = swap ? lda : ldb;
 
-  // Tile width: the least time over whole waves of one tile per SM, where a
-  // 128-column tile runs at 3/4 the speed per column of a 256-column one (it
-  // stages twice the shared-memory operand bytes per MMA flop; measured on
-  // square and large shapes).  Ties go to 256.
-  int tile_n = swap ? 16 : h->opt_tile_n;
-  if (tile_n != 128 && tile_n != 256 && tile_n != 16) {
-    const int64_t tm = ceil_div(Mk, 128);
-    const double cost256 = static_cast<double>(ceil_div(tm * ceil_div(Nk, 256), sms)) * 256.0;
-    const double cost128 = static_cast<double>(ceil_div(tm * ceil_div(Nk, 128), sms)) * 128.0 / 0.75;
-    tile_n = (cost128 < cost256) ? 128 : 256;
+  // Tile width (128, 192, 224 or 256 columns): the least time over whole
+  // waves of work units, a unit being one tile per CTA or, where two CTAs
+  // share each B tile, two vertically adjacent tiles per CTA pair.  A
+  // tile's time is taken as proportional to the shared-memory bytes of one
+  // stage, A (128 rows) + B (tile_n rows) of 128 bytes each: that makes a
+  // 128-column tile 3/4 as fast per column as a 256-column one, as measured
+  // on square and large shapes.  Ties go to the wider tile.  The B layout the
+  // kernel reads is MN-major only for BF16 (TF32 operands are made K-major).
+  const bool b_mn_kernel = (mode == GEMM_MODE_BF16) && tb_k == 0;
+  const int64_t tm_tiles = ceil_div(Mk, 128);
+  auto pair_ok = [&](int tn) {
+    return !swap && tm_tiles >= 2 && h->opt_pair != 1 && dgt::tc_tile_ok(mode, tn, true, b_mn_kernel);
+  };
+  int tile_n = 16;
+  if (!swap && h->opt_tile_n != 0) {
+    if (!dgt::tc_tile_ok(mode, h->opt_tile_n, false, b_mn_kernel)) return GEMM_ERR_NOT_SUPPORTED;
+    tile_n = h->opt_tile_n;
+  } else if (!swap) {
+    double best = 0.0;
+    for (int tn : {256, 224, 192, 128}) {
+      if (!dgt::tc_tile_ok(mode, tn, false, b_mn_kernel)) continue;
+      const bool pr = pair_ok(tn);
+      const int64_t units = (pr ? ceil_div(tm_tiles, 2) : tm_tiles) * ceil_div(Nk, tn);
+      const int64_t waves = ceil_div(units, pr ? sms / 2 : sms);
+      const double cost = static_cast<double>(waves) * (128.0 * 128.0 + 128.0 * tn);
+      if (tile_n == 16 || cost < best) {
+        best = cost;
+        tile_n = tn;
+      }
+    }
   }
   const int64_t tiles = ceil_div(Mk, 128) * ceil_div(Nk, tile_n);
   const int64_t kb = ceil_div(K, bk);
@@ -429,11 +450,10 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.ws_ld = ws_ld;
   a.ws_slice = M * ws_ld;  // partial sums are kept in the caller's M x N orientation
   a.status = h->d_status;
-  // Two-CTA clusters sharing each B tile (TMA multicast) for 256-column
-  // tiles with at least two rows of tiles: each CTA then pulls 32 KB per
-  // stage from L2 instead of 48 KB.
-  const int64_t tm_tiles = ceil_div(Mk, 128);
-  a.pair = (!swap && tile_n == 256 && tm_tiles >= 2 && h->opt_pair != 1) ? 1 : 0;
+  // Two-CTA clusters sharing each B tile (TMA multicast) for tiles of 192
+  // columns or more with at least two rows of tiles: each CTA then pulls
+  // half of B per stage from L2 (256 columns: 32 KB instead of 48 KB).
+  a.pair = pair_ok(tile_n) ? 1 : 0;
   if (a.pair) {
     const int64_t units = ceil_div(tm_tiles, 2) * ceil_div(Nk, tile_n) * splits;
     a.grid = static_cast<int>(2 * std::min<int64_t>(units, sms / 2));
@@ -554,7 +574,7 @@ gemm_status_t gemm_set_option(gemm_handle_t h, int option, int64_t value) {
       h->opt_split_k = static_cast<int>(value);
       return GEMM_OK;
     case GEMM_OPT_TILE_N:
-      if (value != 0 && value != 128 && value != 256) return GEMM_ERR_INVALID_VALUE;
+      if (value != 0 && value != 128 && value != 192 && value != 224 && value != 256) return GEMM_ERR_INVALID_VALUE;
       h->opt_tile_n = static_cast<int>(value);
       return GEMM_OK;
     case GEMM_OPT_PRETRANSPOSE:

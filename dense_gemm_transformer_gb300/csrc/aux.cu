@@ -9,6 +9,7 @@
 #include <cstdint>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace dgt {
 namespace {
@@ -29,6 +30,8 @@ int grid_for(int64_t work, int threads) {
 template <bool CVEC>
 __global__ void splitk_reduce_kernel(int64_t M, int64_t N, int splits, const float* __restrict__ ws, int64_t ws_ld,
                                      float* __restrict__ C, int64_t ldc, float alpha, float beta) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t groups = (N + 3) / 4;
   const int64_t total = M * groups;
   const int64_t slice = M * ws_ld;
@@ -63,6 +66,8 @@ __global__ void splitk_reduce_kernel(int64_t M, int64_t N, int splits, const flo
 }
 
 __global__ void scale_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_t ldc, float beta) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t total = M * N;
   for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
        g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -75,6 +80,8 @@ __global__ void scale_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_
 template <typename T>
 __global__ void pack_kernel(const T* __restrict__ src, int64_t ld_src, T* __restrict__ dst, int64_t ld_dst,
                             int64_t rows, int64_t cols) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t total = rows * cols;
   for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
        g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -89,6 +96,8 @@ __global__ void pack_kernel(const T* __restrict__ src, int64_t ld_src, T* __rest
 template <typename T>
 __global__ void transpose_kernel(const T* __restrict__ src, int64_t ld_src, T* __restrict__ dst, int64_t ld_dst,
                                  int64_t rows, int64_t cols) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ T tile[32][33];
   const int64_t tiles_c = (cols + 31) / 32;
   const int64_t tiles = ((rows + 31) / 32) * tiles_c;
@@ -113,6 +122,8 @@ __global__ void transpose_kernel(const T* __restrict__ src, int64_t ld_src, T* _
 __global__ void __launch_bounds__(256) transpose_f32x4_kernel(const float* __restrict__ src, int64_t ld_src,
                                                               float* __restrict__ dst, int64_t ld_dst, int64_t rows,
                                                               int64_t cols) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ float tile[64][65];
   const int64_t tiles_c = (cols + 63) / 64;
   const int64_t tiles = ((rows + 63) / 64) * tiles_c;
@@ -169,54 +180,48 @@ cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t
   const bool a16 = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0;
   if (elem_bytes == 4 && a16 && ld_src % 4 == 0 && ld_dst % 4 == 0) {
     const int64_t tiles64 = ((rows + 63) / 64) * ((cols + 63) / 64);
-    transpose_f32x4_kernel<<<grid_for(tiles64 * 256, 256), 256, 0, stream>>>(
-        static_cast<const float*>(src), ld_src, static_cast<float*>(dst), ld_dst, rows, cols);
-    return cudaGetLastError();
+    return launch_pdl(transpose_f32x4_kernel, dim3(grid_for(tiles64 * 256, 256)), dim3(256), 0, stream,
+                      static_cast<const float*>(src), ld_src, static_cast<float*>(dst), ld_dst, rows, cols);
   }
   const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
-  const int blocks = grid_for(tiles * 256, 256);
+  const dim3 blocks(grid_for(tiles * 256, 256));
   const dim3 block(32, 8);
   if (elem_bytes == 2)
-    transpose_kernel<uint16_t><<<blocks, block, 0, stream>>>(static_cast<const uint16_t*>(src), ld_src,
-                                                              static_cast<uint16_t*>(dst), ld_dst, rows, cols);
-  else
-    transpose_kernel<float><<<blocks, block, 0, stream>>>(static_cast<const float*>(src), ld_src,
-                                                           static_cast<float*>(dst), ld_dst, rows, cols);
-  return cudaGetLastError();
+    return launch_pdl(transpose_kernel<uint16_t>, blocks, block, 0, stream, static_cast<const uint16_t*>(src),
+                      ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+  return launch_pdl(transpose_kernel<float>, blocks, block, 0, stream, static_cast<const float*>(src), ld_src,
+                    static_cast<float*>(dst), ld_dst, rows, cols);
 }
 
 cudaError_t launch_splitk_reduce(int64_t M, int64_t N, int splits, const float* ws, int64_t ws_ld, float* C,
                                  int64_t ldc, float alpha, float beta, cudaStream_t stream) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   const int threads = 256;
-  const int blocks = grid_for(M * ((N + 3) / 4), threads);
+  const dim3 blocks(grid_for(M * ((N + 3) / 4), threads));
   const bool cvec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && (ldc % 4 == 0);
   if (cvec)
-    splitk_reduce_kernel<true><<<blocks, threads, 0, stream>>>(M, N, splits, ws, ws_ld, C, ldc, alpha, beta);
-  else
-    splitk_reduce_kernel<false><<<blocks, threads, 0, stream>>>(M, N, splits, ws, ws_ld, C, ldc, alpha, beta);
-  return cudaGetLastError();
+    return launch_pdl(splitk_reduce_kernel<true>, blocks, dim3(threads), 0, stream, M, N, splits, ws, ws_ld, C, ldc,
+                      alpha, beta);
+  return launch_pdl(splitk_reduce_kernel<false>, blocks, dim3(threads), 0, stream, M, N, splits, ws, ws_ld, C, ldc,
+                    alpha, beta);
 }
 
 cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta, cudaStream_t stream) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   const int threads = 256;
-  scale_kernel<<<grid_for(M * N, threads), threads, 0, stream>>>(M, N, C, ldc, beta);
-  return cudaGetLastError();
+  return launch_pdl(scale_kernel, dim3(grid_for(M * N, threads)), dim3(threads), 0, stream, M, N, C, ldc, beta);
 }
 
 cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
                         int elem_bytes, cudaStream_t stream) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   const int threads = 256;
-  const int blocks = grid_for(rows * cols, threads);
+  const dim3 blocks(grid_for(rows * cols, threads));
   if (elem_bytes == 2)
-    pack_kernel<uint16_t><<<blocks, threads, 0, stream>>>(static_cast<const uint16_t*>(src), ld_src,
-                                                           static_cast<uint16_t*>(dst), ld_dst, rows, cols);
-  else
-    pack_kernel<float><<<blocks, threads, 0, stream>>>(static_cast<const float*>(src), ld_src,
-                                                        static_cast<float*>(dst), ld_dst, rows, cols);
-  return cudaGetLastError();
+    return launch_pdl(pack_kernel<uint16_t>, blocks, dim3(threads), 0, stream, static_cast<const uint16_t*>(src),
+                      ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+  return launch_pdl(pack_kernel<float>, blocks, dim3(threads), 0, stream, static_cast<const float*>(src), ld_src,
+                    static_cast<float*>(dst), ld_dst, rows, cols);
 }
 
 }  // namespace dgt

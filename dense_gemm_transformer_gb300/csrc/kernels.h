@@ -7,6 +7,28 @@
 
 namespace dgt {
 
+// Every kernel of the library is launched with programmatic dependent
+// launch: it may start (and run its set-up, which touches no global memory)
+// while the previous kernel in the stream is finishing; each kernel executes
+// griddepcontrol.wait before its first access to global memory, which
+// returns once every earlier kernel in the stream has completed and its
+// writes are visible, so stream order is kept.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---------------------------------------------------------------- FP32 SIMT
 // C = alpha * op(A) op(B) + beta * C with FFMA, 128 x tile_n block tiles
 // (tile_n 128: two CTAs per SM; 256: one), in one of three schedules:
@@ -51,8 +73,8 @@ struct TcArgs {
   int mode;              // 1 = tf32, 2 = bf16 (gemm_mode_t)
   int a_mn_major;        // A stored with M contiguous (transA == 1)
   int b_mn_major;        // B stored with N contiguous (transB == 0)
-  int tile_n;            // 128 or 256 (16: the swapped small-M form)
-  int pair;              // tile_n 256: two-CTA clusters sharing each B tile by TMA multicast
+  int tile_n;            // 128, 192, 224 or 256 (16: the swapped small-M form)
+  int pair;              // tile_n >= 192: two-CTA clusters sharing each B tile by TMA multicast
   int64_t M, N, K;
   const void* A;         // base of the (possibly re-packed) operand
   int64_t lda;           // elements
@@ -77,6 +99,9 @@ constexpr int kTcEpiWarps = 8;                        // epilogue warps (two per
 constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);  // producer + MMA warps + epilogue warps
 int tc_tile_k(int mode);              // k elements per stage (128 bytes)
 int tc_stages(int mode, int tile_n);  // pipeline depth
+// Whether the kernel is built for this tile width, pairing and B layout
+// (tile_n 128, 192, 224 or 256; pairs from 192 columns).
+bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major);
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream);
 // The small-M kernel (tile_n 16, operands swapped as for launch_tc): one
 // (tile, K slice) per CTA, `splits` K slices per cluster reduced in

@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace dgt {
 namespace {
@@ -166,6 +167,8 @@ template <int TBN, bool TA, bool TB, bool VEC, bool CVEC>
 __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel(SimtArgs p) {
   using Cfg = SimtCfg<TBN>;
   constexpr int S = Cfg::STAGES, TN = Cfg::TN, QN = Cfg::QN, LDA = Cfg::LDA, LDB = Cfg::LDB;
+  grid_dep_wait();
+  grid_dep_launch();
   extern __shared__ __align__(16) float smem[];
   float* As = smem;                      // [S][BK][LDA]
   float* Bs = smem + S * Cfg::A_STAGE;   // [S][BK][LDB]
@@ -419,6 +422,8 @@ __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
   constexpr int kMaxParts = 512;  // > the most resident CTAs that can share one tile
   __shared__ int64_t slots[kMaxParts];
   __shared__ int nparts;
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t tile = p.dp_tiles + blockIdx.x / kFixupChunks;  // tiles below dp_tiles were stored whole
   const int chunk = blockIdx.x % kFixupChunks;
   if (threadIdx.x == 0) {
@@ -471,8 +476,7 @@ cudaError_t launch_cvec(const SimtArgs& a, dim3 grid, cudaStream_t s, bool cvec)
   auto kern = cvec ? simt_gemm_kernel<TBN, TA, TB, VEC, true> : simt_gemm_kernel<TBN, TA, TB, VEC, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, NT, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(NT), smem, s, a);
 }
 
 template <int TBN, bool TA, bool TB>
@@ -505,8 +509,8 @@ cudaError_t launch_tbn(const SimtArgs& a, cudaStream_t stream) {
     e = launch_vec<TBN, true, true>(a, grid, stream, vec, cvec);
   if (e != cudaSuccess || a.schedule != kSimtStreamK) return e;
   const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + TBN - 1) / TBN);
-  simt_streamk_fixup_kernel<TBN><<<static_cast<unsigned>((tiles - a.dp_tiles) * kFixupChunks), NT, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(simt_streamk_fixup_kernel<TBN>, dim3(static_cast<unsigned>((tiles - a.dp_tiles) * kFixupChunks)),
+                    dim3(NT), 0, stream, a);
 }
 
 }  // namespace

@@ -71,8 +71,19 @@ int tc_tile_k(int mode) { return mode == 2 ? 64 : 32; }
 int tc_stages(int mode, int tile_n) {
   (void)mode;  // a stage holds 128 bytes of K per row in both modes
   if (tile_n == 256) return TcCfg<2, 256>::STAGES;
+  if (tile_n == 224) return TcCfg<2, 224>::STAGES;
+  if (tile_n == 192) return TcCfg<2, 192>::STAGES;
   if (tile_n == 128) return TcCfg<2, 128>::STAGES;
   return TcCfg<2, 16>::STAGES;
+}
+
+bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major) {
+  if (tile_n != 128 && tile_n != 192 && tile_n != 224 && tile_n != 256) return false;
+  if (pair && tile_n == 128) return false;
+  if (!b_mn_major) return true;
+  if (mode != 2) return false;  // kind::tf32: K-major operands only
+  const int ch = 64;            // bf16 columns in one 128-byte chunk
+  return tile_n % ch == 0 && (!pair || (tile_n / ch) % 2 == 0);
 }
 
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
@@ -85,7 +96,7 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
                    : encode_2d(&ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
   if (e != cudaSuccess) return e;
   // A pair of CTAs loads one half of each B tile apiece (K-major: half the rows).
-  const bool pair = a.pair != 0 && a.tile_n == 256;
+  const bool pair = a.pair != 0 && a.tile_n >= 192;
   e = a.b_mn_major ? encode_2d(&tb, a.mode, a.B, a.N, a.K, a.ldb, ch, bk)
                    : encode_2d(&tb, a.mode, a.B, a.K, a.N, a.ldb, bk, pair ? a.tile_n / 2 : a.tile_n);
   if (e != cudaSuccess) return e;
@@ -124,6 +135,8 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
       p.c_tma = (encode_out(&tcm, a.C, a.N, a.M, 1, a.ldc, a.M * a.ldc) == cudaSuccess) ? 1 : 0;
     }
   }
+  if (a.mode == 2 && (a.tile_n == 192 || a.tile_n == 224))
+    return tc_launch_bf16_mid(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
   if (a.mode == 2)
     return tc_launch_bf16(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
   return tc_launch_tf32(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);

@@ -69,8 +69,10 @@ struct TcCfg {
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // ~192-200 KB of operand stages
-  static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128) ? 6 : 200 * 1024 / STAGE_BYTES;
-  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;  // two accumulators (allocation >= 32 columns)
+  static constexpr int STAGES = (BN >= 192) ? 4 : (BN == 128) ? 6 : 200 * 1024 / STAGE_BYTES;
+  // Two accumulators; an allocation is a power of two of at least 32 columns.
+  static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                   : (2 * BN <= 256) ? 256 : 512;
   static constexpr int CW = BN < 32 ? BN : 32;                    // accumulator columns per TMEM load
   static constexpr int NUM_BARS = 2 * STAGES + 5;     // full/empty per stage, acc full/empty x2, drain
   // Epilogue staging for TMA stores: one buffer of 32 rows x 128 bytes per
@@ -82,6 +84,7 @@ struct TcCfg {
   static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
   static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+  static_assert(BN < 32 || BN % 32 == 0, "the epilogue moves 32-column chunks");
 };
 
 template <int MODE>
@@ -148,7 +151,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  static_assert(!PAIR || (!TRANS_C && BN >= 128), "paired CTAs share a B tile of 128 or 256 columns");
+  static_assert(!PAIR || (!TRANS_C && BN >= 128 && (!B_MN || (BN / Cfg::CH) % 2 == 0)),
+                "paired CTAs each load one half of the B tile");
   // Work units: one per CTA, or one per two-CTA cluster (the pair's rank
   // picks its row of tiles).  The cluster of a pair is blockIdx.x / 2.
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
@@ -186,6 +190,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Set-up above touches no global memory; from here on the kernel reads
+  // what earlier kernels in the stream wrote.
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -316,8 +324,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool vec_ok = !TRANS_C && (partial || p.c_vec);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
       constexpr int NCH = BN / CW;  // column chunks of a tile
-      const int cc_begin = (NCH >= 2) ? half * (NCH / 2) : (half == 0 ? 0 : NCH);
-      const int cc_end = (NCH >= 2) ? (half + 1) * (NCH / 2) : NCH;
+      // Warps of half 0 take the first ceil(NCH / 2) chunks, half 1 the rest.
+      const int cc_begin = (half == 0) ? 0 : (NCH + 1) / 2;
+      const int cc_end = (half == 0) ? (NCH + 1) / 2 : NCH;
 #pragma unroll 1
       for (int cc = cc_begin; cc < cc_end; ++cc) {
         uint32_t r[CW];

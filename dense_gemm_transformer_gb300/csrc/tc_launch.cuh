@@ -21,55 +21,84 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
   } else {
-    kern<<<grid, kTcThreads, Cfg::SMEM_BYTES, s>>>(ta, tb, tc, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kTcThreads), Cfg::SMEM_BYTES, s, ta, tb, tc, p);
   }
 }
 
-// kind::tf32 takes K-major operands only (the planner transposes MN-major
-// TF32 operands first), so only BF16 instantiates the MN-major forms.
+// Which operand layouts a tile width can take.  kind::tf32 reads K-major
+// operands only (the planner transposes MN-major TF32 operands first); an
+// MN-major B is loaded in 128-byte column chunks, so its tile width must be
+// a whole number of chunks, and an even number when a pair of CTAs loads
+// one half each.
+template <int MODE, int BN, bool PAIR>
+constexpr bool tc_mn_b_ok() {
+  return MODE == 2 && BN % TcCfg<MODE, BN>::CH == 0 && (!PAIR || (BN / TcCfg<MODE, BN>::CH) % 2 == 0);
+}
+
 template <int MODE, int BN, bool PAIR>
 cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                          const TcParams& p, int grid, cudaStream_t s) {
   if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN, false, PAIR>(ta, tb, tc, p, grid, s);
-  if constexpr (MODE == 1) {
-    return cudaErrorInvalidValue;
-  } else {
-    if (!a_mn && b_mn) return tc_launch_one<MODE, false, true, BN, false, PAIR>(ta, tb, tc, p, grid, s);
+  if constexpr (MODE == 2) {
     if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN, false, PAIR>(ta, tb, tc, p, grid, s);
-    return tc_launch_one<MODE, true, true, BN, false, PAIR>(ta, tb, tc, p, grid, s);
+    if constexpr (tc_mn_b_ok<MODE, BN, PAIR>()) {
+      if (!a_mn) return tc_launch_one<MODE, false, true, BN, false, PAIR>(ta, tb, tc, p, grid, s);
+      return tc_launch_one<MODE, true, true, BN, false, PAIR>(ta, tb, tc, p, grid, s);
+    }
   }
+  return cudaErrorInvalidValue;
 }
 
-// tile_n == 16 is the swapped small-M form: the weights are the 128-row
-// operand (K-major or MN-major), the activations a K-major 16-row operand,
-// and C is written transposed.  `pair` selects the two-CTA form (tile_n 256).
+// The 128- and 256-column tiles and the swapped small-M form (tile_n 16:
+// the weights are the 128-row operand, K-major or MN-major, the activations
+// a K-major 16-row operand, and C is written transposed).  `pair` selects
+// the two-CTA form (256 columns).
 template <int MODE>
 cudaError_t tc_launch_mode(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s) {
   if (tile_n == 256 && pair) return tc_launch_bn<MODE, 256, true>(a_mn, b_mn, ta, tb, tc, p, grid, s);
   if (tile_n == 256) return tc_launch_bn<MODE, 256, false>(a_mn, b_mn, ta, tb, tc, p, grid, s);
-  if (tile_n == 128) return tc_launch_bn<MODE, 128, false>(a_mn, b_mn, ta, tb, tc, p, grid, s);
-  if (tile_n == 16 && !b_mn) {
+  if (tile_n == 128 && !pair) return tc_launch_bn<MODE, 128, false>(a_mn, b_mn, ta, tb, tc, p, grid, s);
+  if (tile_n == 16 && !b_mn && !pair) {
     if (!a_mn) return tc_launch_one<MODE, false, false, 16, true>(ta, tb, tc, p, grid, s);
     if constexpr (MODE == 2) return tc_launch_one<MODE, true, false, 16, true>(ta, tb, tc, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
 
-// Defined in tc_tf32.cu (MODE 1) and tc_bf16.cu (MODE 2).
+// The 192- and 224-column tiles, which let the planner fill whole waves
+// where 256 would leave the last one mostly idle (4096 columns: 19 tiles of
+// 224 instead of 16 of 256).
+template <int MODE>
+cudaError_t tc_launch_mode_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
+                               const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p, int grid,
+                               cudaStream_t s) {
+  if (tile_n == 192 && pair) return tc_launch_bn<MODE, 192, true>(a_mn, b_mn, ta, tb, tc, p, grid, s);
+  if (tile_n == 192) return tc_launch_bn<MODE, 192, false>(a_mn, b_mn, ta, tb, tc, p, grid, s);
+  if (tile_n == 224 && pair) return tc_launch_bn<MODE, 224, true>(a_mn, b_mn, ta, tb, tc, p, grid, s);
+  if (tile_n == 224) return tc_launch_bn<MODE, 224, false>(a_mn, b_mn, ta, tb, tc, p, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+// Defined in tc_tf32.cu (MODE 1), tc_bf16.cu (MODE 2: 16, 128 and 256
+// columns) and tc_bf16_mid.cu (MODE 2: 192 and 224 columns).
 cudaError_t tc_launch_tf32(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s);
 cudaError_t tc_launch_bf16(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s);
+cudaError_t tc_launch_bf16_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
+                               const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p, int grid,
+                               cudaStream_t s);
 
 }  // namespace dgt

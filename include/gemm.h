@@ -75,11 +75,12 @@ typedef enum {
 typedef enum {
   GEMM_OPT_FAMILY = 1,   /* value: gemm_family_t; AUTO lets the planner choose            */
   GEMM_OPT_SPLIT_K = 2,  /* value: 0 = planner's choice, n >= 1 = force n slices of K      */
-  GEMM_OPT_TILE_N = 3,   /* value: 0 = planner's choice, 128 or 256 (TC and SIMT families)  */
+  GEMM_OPT_TILE_N = 3,   /* value: 0 = planner's choice; TC: 128, 192, 224 or 256 (224 and,
+                            for pairs, 192 need a K-major B in BF16); SIMT: 128 or 256    */
   GEMM_OPT_PRETRANSPOSE = 4, /* SIMT: 0 = planner's choice, 1 = never, 2 = always transpose
                                 K-contiguous operands into the workspace first             */
-  GEMM_OPT_PAIR = 5          /* TC: 0 = two-CTA clusters sharing B tiles where the planner
-                                chooses them, 1 = never                                     */
+  GEMM_OPT_PAIR = 5          /* TC: 0 = two-CTA clusters sharing B tiles (tiles of 192 or more
+                                columns) where the planner chooses them, 1 = never          */
 } gemm_option_t;
 
 /* What the last successful gemm_run on a handle launched. */

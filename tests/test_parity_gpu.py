@@ -81,26 +81,44 @@ def test_alpha_beta(h, mode, alpha, beta):
 
 
 @pytest.mark.parametrize("mode", ["tf32", "bf16"])
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tile_n", [128, 192, 224, 256])
 @pytest.mark.parametrize("tA,tB", TRANS)
 def test_tc_tile_widths(h, mode, tile_n, tA, tB):
+    """Every tile width in every layout; 224 columns (3.5 chunks of 128
+    bytes) cannot take an N-contiguous BF16 B and is refused."""
     h.set_option("tile_n", tile_n)
+    if mode == "bf16" and tile_n == 224 and not tB:
+        ops, _ = _cases.make(mode, 384, 520, 160, tA, tB)
+        C = torch.zeros((384, 520), device="cuda")
+        with pytest.raises(dg.GemmError) as e:
+            h.run(ops.A, ops.B, C, mode=mode, transA=tA, transB=tB)
+        assert e.value.status == 2  # GEMM_ERR_NOT_SUPPORTED
+        assert torch.count_nonzero(C).item() == 0
+        return
     _cases.run_and_check(h, mode, 384, 520, 160, tA, tB, seed=19, dist="normal")
     assert h.plan()["family"] == "tc" and h.plan()["tile_n"] == tile_n
+    _cases.run_and_check(h, mode, 384, 520, 160, tA, tB, alpha=2.0, beta=0.5, seed=20, dist="normal")
 
 
 @pytest.mark.parametrize("mode", ["tf32", "bf16"])
 @pytest.mark.parametrize("pair", [0, 1])
 @pytest.mark.parametrize("tA,tB", TRANS)
 @pytest.mark.parametrize("M,N,K", [(640, 600, 200), (300, 260, 1000), (1100, 300, 64)])
-def test_tc_paired_ctas(h, mode, pair, tA, tB, M, N, K):
-    """256-column tiles with and without two-CTA clusters sharing B tiles by
-    TMA multicast; odd tile-row counts leave the second CTA of the last pair
-    with no rows of C."""
-    h.set_option("tile_n", 256)
+@pytest.mark.parametrize("tile_n", [192, 224, 256])
+def test_tc_paired_ctas(h, mode, pair, tA, tB, M, N, K, tile_n):
+    """Tiles of 192-256 columns with and without two-CTA clusters sharing
+    B tiles by TMA multicast (each CTA loads one half); odd tile-row counts
+    leave the second CTA of the last pair with no rows of C.  An
+    N-contiguous BF16 B pairs only when its tile is an even number of
+    128-byte chunks (256), and takes no 224-column tile."""
+    b_mn = mode == "bf16" and not tB
+    if b_mn and tile_n == 224:
+        pytest.skip("224-column tiles need a K-major B in BF16 (covered by test_tc_tile_widths)")
+    h.set_option("tile_n", tile_n)
     h.set_option("pair", pair)
     _cases.run_and_check(h, mode, M, N, K, tA, tB, alpha=0.5, beta=-1.0, seed=77, dist="normal")
-    assert h.plan()["cluster"] == (1 if pair else 2)
+    paired = pair == 0 and not (b_mn and tile_n == 192)
+    assert h.plan()["cluster"] == (2 if paired else 1) and h.plan()["tile_n"] == tile_n
     _cases.run_and_check(h, mode, M, N, min(K, 1024), tA, tB, seed=78, dist="int", exact=True)
     h.set_option("split_k", 3)
     _cases.run_and_check(h, mode, M, N, K, tA, tB, seed=79, dist="normal")
