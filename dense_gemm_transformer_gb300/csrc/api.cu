@@ -290,19 +290,21 @@ int64_t skinny_splits(int64_t tiles, int64_t kb, int sms) {
   return best;
 }
 
-// K slices (= CTAs per cluster) for the small-M kernel: at most as many as
-// one wave of two resident CTAs per SM holds, at least two K blocks per
-// slice, at most 16, and the largest such count of which every tile's
-// cluster can be resident at once (else the largest count).  Measured on the
-// decode shapes: 280 CTAs for 70 tiles and 192 for 12 tiles ran fastest,
-// 140 and 96 ran 25-30% slower.
+// K slices (= CTAs per cluster) for the small-M kernel: as many as one wave
+// of two resident CTAs per SM holds, at least two K blocks per slice, at
+// most 16, and above the portable cluster size of 8 only a size the device
+// can launch.  Measured on the decode shapes (calls back to back): 280 CTAs
+// for 70 tiles and 192 for 12 tiles ran fastest, 140 and 96-120 ran 25-30%
+// slower, although only 7 clusters of 16 are resident at once (the next
+// call's CTAs, started early, fill the SMs the second wave leaves idle).
 int64_t skinny_cluster_size(gemm_handle_s* h, int mode, bool a_mn, int64_t tiles, int64_t kb) {
   int64_t cs = std::min<int64_t>(2 * h->sms / tiles, dgt::kSkinnyMaxCluster);
   cs = std::max<int64_t>(1, std::min<int64_t>(cs, kb / 2));
-  for (int64_t c = cs; c >= 2; --c) {
-    int& act = h->sk_active[mode == GEMM_MODE_BF16 ? 1 : 0][c];
-    if (act < 0) act = dgt::skinny_max_active_clusters(mode, a_mn, static_cast<int>(c));
-    if (act >= tiles) return c;
+  while (cs > 8) {
+    int& act = h->sk_active[mode == GEMM_MODE_BF16 ? 1 : 0][cs];
+    if (act < 0) act = dgt::skinny_max_active_clusters(mode, a_mn, static_cast<int>(cs));
+    if (act > 0) break;
+    --cs;
   }
   return cs;
 }

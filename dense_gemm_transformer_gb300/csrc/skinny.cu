@@ -310,11 +310,6 @@ cudaLaunchConfig_t make_config(const SkParams& p, int grid, cudaStream_t s, cuda
     attr[n].val.clusterDim.y = 1;
     attr[n].val.clusterDim.z = 1;
     ++n;
-    // Let two CTAs of a cluster share an SM: spread one CTA per SM, a
-    // cluster of 16 needs 16 SMs of one GPC, and only 7 fit at once.
-    attr[n].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
-    attr[n].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicyLoadBalancing;
-    ++n;
   }
   attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[n].val.programmaticStreamSerializationAllowed = 1;
@@ -336,7 +331,7 @@ template <int MODE, bool A_MN>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const SkParams& p, int grid, cudaStream_t s) {
   cudaError_t e = set_attributes<MODE, A_MN>();
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[3];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_config<MODE>(p, grid, s, attr);
   return cudaLaunchKernelEx(&cfg, skinny_gemm_kernel<MODE, A_MN>, ta, tb, p);
 }
@@ -346,7 +341,7 @@ int active_clusters(int cluster) {
   if (set_attributes<MODE, A_MN>() != cudaSuccess) return 0;
   SkParams p{};
   p.cluster = cluster;
-  cudaLaunchAttribute attr[3];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_config<MODE>(p, cluster, nullptr, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, skinny_gemm_kernel<MODE, A_MN>, &cfg) != cudaSuccess) {
