@@ -147,7 +147,7 @@ class Gemm:
         return {"family": fam if p.kernels else "none", "tile_m": p.tile_m, "tile_n": p.tile_n,
                 "tile_k": p.tile_k, "split_k": p.split_k, "stages": p.stages, "grid": p.grid,
                 "kernels": p.kernels, "packed": p.packed,
-                "schedule": {0: "tiles", 1: "split_k", 2: "stream_k"}.get(p.schedule, "tiles"),
+                "schedule": {0: "tiles", 1: "split_k", 2: "stream_k", 3: "tail_split"}.get(p.schedule, "tiles"),
                 "cluster": p.cluster}
 
     def check_device(self, stream=None) -> int:

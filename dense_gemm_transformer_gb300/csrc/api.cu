@@ -270,24 +270,52 @@ cudaError_t run_pack(const OperandPack& p, void* dst, int es, cudaStream_t s) {
   return dgt::launch_pack(p.src, p.ld, dst, p.dst_ld, p.rows, p.cols, es, s);
 }
 
-// K slices for the small-M form: the count whose units fill whole waves of one
-// CTA per SM best, with at least two K blocks per slice (ties go to fewer).
-int64_t skinny_splits(int64_t tiles, int64_t kb, int sms) {
-  int64_t best = 1;
-  double best_eff = 0.0;
-  const int64_t max_s = std::max<int64_t>(1, std::min<int64_t>(32, kb / 2));
-  for (int64_t s = 1; s <= max_s; ++s) {
-    const int64_t per = ceil_div(kb, s);
-    const int64_t eff_s = ceil_div(kb, per);  // slices actually used
-    if (eff_s != s) continue;
-    const int64_t units = tiles * s;
-    const double eff = static_cast<double>(units) / (ceil_div(units, sms) * sms);
-    if (eff > best_eff + 0.02) {
-      best_eff = eff;
-      best = s;
+// Nominal dense tensor rates (flop/s) used only to weigh a wave of tiles
+// against the extra reduction traffic of a K split.
+constexpr double kBf16Flops = 2.25e15;
+constexpr double kTf32Flops = 1.1e15;
+constexpr double kHbmBytes = 7.0e12;
+constexpr double kLaunchS = 2e-6;
+
+// Which last rows of work units to cut into K slices, and into how many:
+// units are handed out round-robin to `slots` persistent CTAs (or CTA
+// pairs), whole units first; each option's time is that of the busiest CTA
+// (a cut unit counts its share of K) plus the reduction of the cut rows'
+// partial sums by a separate kernel.  rows == 0: no cut.  O(rows x 7).
+struct TailPlan {
+  int64_t rows = 0, slices = 1, kb_per = 0;
+  double seconds = 0.0;  // estimated time of the chosen schedule
+};
+
+TailPlan plan_tail(int64_t unit_rows, int64_t unit_cols, int64_t kb, int64_t slots, double unit_s,
+                   double c_bytes_per_row, bool read_c) {
+  TailPlan best_plan;
+  const int64_t U = unit_rows * unit_cols;
+  double best = static_cast<double>(ceil_div(U, std::max<int64_t>(slots, 1))) * unit_s;
+  best_plan.seconds = best;
+  if (U <= slots || U % slots == 0 || kb < 8 || slots <= 0) return best_plan;
+  for (int64_t R = 1; R < unit_rows && R * unit_cols <= 2 * slots; ++R) {
+    const int64_t cut = R * unit_cols, D = U - cut;
+    for (int64_t want = 2; want <= 8 && kb / want >= 4; ++want) {
+      const int64_t per = ceil_div(kb, want), sl = ceil_div(kb, per);
+      const double f = static_cast<double>(per) / static_cast<double>(kb);
+      const int64_t T = D + cut * sl;
+      // CTA c runs the units c, c + slots, ...: its counts of whole units and
+      // of all units both fall as c grows, so CTA 0 is the busiest.
+      const double dp0 = static_cast<double>(ceil_div(D, slots));
+      const double worst = dp0 + (static_cast<double>(ceil_div(T, slots)) - dp0) * f;
+      const double reduce = static_cast<double>(R) * c_bytes_per_row * (sl + 1 + (read_c ? 1 : 0)) / kHbmBytes;
+      const double cost = worst * unit_s + reduce + kLaunchS;
+      if (cost < 0.97 * best) {
+        best = cost;
+        best_plan.rows = R;
+        best_plan.slices = sl;
+        best_plan.kb_per = per;
+        best_plan.seconds = cost;
+      }
     }
   }
-  return best;
+  return best_plan;
 }
 
 // K slices (= CTAs per cluster) for the small-M kernel: as many as one wave
@@ -325,18 +353,36 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   const void* Bk = swap ? A : B;
   const int64_t ldak = swap ? ldb : lda, ldbk = swap ? lda : ldb;
 
-  // Tile width (128, 192, 224 or 256 columns): the least time over whole
-  // waves of work units, a unit being one tile per CTA or, where two CTAs
-  // share each B tile, two vertically adjacent tiles per CTA pair.  A
-  // tile's time is taken as proportional to the shared-memory bytes of one
-  // stage, A (128 rows) + B (tile_n rows) of 128 bytes each: that makes a
-  // 128-column tile 3/4 as fast per column as a 256-column one, as measured
-  // on square and large shapes.  Ties go to the wider tile.  The B layout the
-  // kernel reads is MN-major only for BF16 (TF32 operands are made K-major).
+  // Tile width (128, 192, 224 or 256 columns) and schedule: the least
+  // estimated time over waves of work units, a unit being one tile per CTA
+  // or, where two CTAs share each B tile, two vertically adjacent tiles per
+  // CTA pair; the last rows of units may be cut into K slices to fill the
+  // final wave (plan_tail).  A tile's time is taken as proportional to the
+  // shared-memory bytes of one stage, A (128 rows) + B (tile_n rows) of 128
+  // bytes each: that makes a 128-column tile 3/4 as fast per column as a
+  // 256-column one, as measured on square and large shapes.  Ties go to the
+  // wider tile.  The B layout the kernel reads is MN-major only for BF16
+  // (TF32 operands are made K-major).
   const bool b_mn_kernel = (mode == GEMM_MODE_BF16) && tb_k == 0;
   const int64_t tm_tiles = ceil_div(Mk, 128);
+  const int64_t kb = ceil_div(K, bk);
   auto pair_ok = [&](int tn) {
     return !swap && tm_tiles >= 2 && h->opt_pair != 1 && dgt::tc_tile_ok(mode, tn, true, b_mn_kernel);
+  };
+  const double peak = (mode == GEMM_MODE_BF16 ? kBf16Flops : kTf32Flops) / sms;
+  auto plan_for = [&](int tn) {
+    const bool pr = pair_ok(tn);
+    const int64_t rows = pr ? ceil_div(tm_tiles, 2) : tm_tiles;
+    const double unit_s =
+        2.0 * 128.0 * 256.0 * static_cast<double>(K) / peak * (128.0 * 128.0 + 128.0 * tn) / (128.0 * 384.0);
+    const double c_row_bytes = 4.0 * static_cast<double>(Nk) * (pr ? 256.0 : 128.0);
+    const bool may_cut = !swap && h->opt_split_k == 0 && !(2 * tm_tiles * ceil_div(Nk, tn) <= sms && kb >= 8);
+    if (!may_cut) {
+      TailPlan none;
+      none.seconds = static_cast<double>(ceil_div(rows * ceil_div(Nk, tn), pr ? sms / 2 : sms)) * unit_s;
+      return none;
+    }
+    return plan_tail(rows, ceil_div(Nk, tn), kb, pr ? sms / 2 : sms, unit_s, c_row_bytes, beta != 0.f);
   };
   int tile_n = 16;
   if (!swap && h->opt_tile_n != 0) {
@@ -346,18 +392,14 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
     double best = 0.0;
     for (int tn : {256, 224, 192, 128}) {
       if (!dgt::tc_tile_ok(mode, tn, false, b_mn_kernel)) continue;
-      const bool pr = pair_ok(tn);
-      const int64_t units = (pr ? ceil_div(tm_tiles, 2) : tm_tiles) * ceil_div(Nk, tn);
-      const int64_t waves = ceil_div(units, pr ? sms / 2 : sms);
-      const double cost = static_cast<double>(waves) * (128.0 * 128.0 + 128.0 * tn);
-      if (tile_n == 16 || cost < best) {
+      const double cost = plan_for(tn).seconds;
+      if (tile_n == 16 || cost < best * 0.999) {
         best = cost;
         tile_n = tn;
       }
     }
   }
   const int64_t tiles = ceil_div(Mk, 128) * ceil_div(Nk, tile_n);
-  const int64_t kb = ceil_div(K, bk);
   // Small M with fewer than two waves of weight tiles: the cluster kernel
   // (one tile and K slice per CTA, slices reduced within the cluster).
   // With more tiles, the persistent kernel streams them without a split.
@@ -370,15 +412,27 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   } else if (h->opt_split_k > 0) {
     splits = std::min<int64_t>(h->opt_split_k, kb);
   } else if (swap) {
-    // Split K only when the tiles alone leave SMs idle: with two or more
-    // waves, partial sums would only add HBM traffic.
-    splits = (tiles >= 2 * sms) ? 1 : skinny_splits(tiles, kb, sms);
+    splits = 1;  // two or more waves of weight tiles: a K split would only add traffic
   } else if (2 * tiles <= sms && kb >= 8) {
     splits = std::min<int64_t>(sms / tiles, kb / 4);
     splits = std::max<int64_t>(splits, 1);
   }
-  const int64_t kb_per = ceil_div(kb, splits);
+  int64_t kb_per = ceil_div(kb, splits);
   splits = ceil_div(kb, kb_per);
+  // More than a wave of units that does not end on a whole wave: the last
+  // rows of units may be cut into K slices so that the final wave is full.
+  const bool pair = pair_ok(tile_n);
+  const int64_t unit_rows = pair ? ceil_div(tm_tiles, 2) : tm_tiles;
+  const int64_t unit_cols = ceil_div(Nk, tile_n);
+  TailPlan tail;
+  if (!swap && splits == 1 && h->opt_split_k == 0) {
+    tail = plan_for(tile_n);
+    if (tail.rows > 0) {
+      splits = tail.slices;
+      kb_per = tail.kb_per;
+    }
+  }
+  const int64_t tail_row0 = tail.rows > 0 ? (unit_rows - tail.rows) * (pair ? 256 : 128) : 0;  // first C row cut
 
   // Workspace: re-packed operands and split-K partials.  An operand is copied
   // when the TMA unit cannot read it in place (base not 16-byte aligned, or a
@@ -393,7 +447,8 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   L.b_off = round_up(static_cast<int64_t>(pa.bytes), 256);
   L.p_off = L.b_off + round_up(static_cast<int64_t>(pb.bytes), 256);
   const int64_t ws_ld = round_up(N, 4);
-  L.total = L.p_off + (splits > 1 && !cluster_form ? static_cast<size_t>(splits * M * ws_ld) * sizeof(float) : 0);
+  L.total = L.p_off +
+            (splits > 1 && !cluster_form ? static_cast<size_t>(splits * (M - tail_row0) * ws_ld) * sizeof(float) : 0);
   if (L.total > 0) {
     gemm_status_t st = ensure_ws(h, L.total);
     if (st != GEMM_OK) return st;
@@ -448,31 +503,34 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
     h->plan.cluster = a.splits;
     return GEMM_OK;
   }
+  // Partial sums are kept in the caller's M x N orientation, from C row
+  // tail_row0 on (0 unless only the last rows of units are cut).
   a.ws = splits > 1 ? reinterpret_cast<float*>(ws + L.p_off) : nullptr;
   a.ws_ld = ws_ld;
-  a.ws_slice = M * ws_ld;  // partial sums are kept in the caller's M x N orientation
+  a.ws_row0 = tail_row0;
+  a.ws_slice = (M - tail_row0) * ws_ld;
+  a.dp_units = static_cast<int>(tail.rows > 0 ? (unit_rows - tail.rows) * unit_cols : 0);
+  a.tail_tm0 = static_cast<int>(tail.rows > 0 ? unit_rows - tail.rows : 0);
   a.status = h->d_status;
   // Two-CTA clusters sharing each B tile (TMA multicast) for tiles of 192
   // columns or more with at least two rows of tiles: each CTA then pulls
   // half of B per stage from L2 (256 columns: 32 KB instead of 48 KB).
-  a.pair = pair_ok(tile_n) ? 1 : 0;
-  if (a.pair) {
-    const int64_t units = ceil_div(tm_tiles, 2) * ceil_div(Nk, tile_n) * splits;
-    a.grid = static_cast<int>(2 * std::min<int64_t>(units, sms / 2));
-  } else {
-    a.grid = static_cast<int>(std::min<int64_t>(tiles * splits, sms));
-  }
+  a.pair = pair ? 1 : 0;
+  const int64_t units = a.dp_units + (unit_rows - a.tail_tm0) * unit_cols * splits;
+  a.grid = static_cast<int>(pair ? 2 * std::min<int64_t>(units, sms / 2) : std::min<int64_t>(units, sms));
   a.group_m = a.pair ? 8 : 16;
   if (launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
   ++kernels;
   if (splits > 1) {
-    if (launch_splitk_reduce(M, N, a.splits, a.ws, ws_ld, C, ldc, alpha, beta, s) != cudaSuccess)
+    if (launch_splitk_reduce(M - tail_row0, N, a.splits, a.ws, ws_ld, C + tail_row0 * ldc, ldc, alpha, beta, s) !=
+        cudaSuccess)
       return GEMM_ERR_CUDA;
     ++kernels;
   }
   set_plan(h, swap ? GEMM_FAMILY_SKINNY : GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n),
            a.grid, kernels, (swap ? ((pack_b ? 1 : 0) | (pack_a ? 2 : 0)) : ((pack_a ? 1 : 0) | (pack_b ? 2 : 0))));
   h->plan.cluster = a.pair ? 2 : 1;
+  h->plan.schedule = tail.rows > 0 ? 3 : (a.splits > 1 ? 1 : 0);
   return GEMM_OK;
 }
 

@@ -85,6 +85,9 @@ struct TcArgs {
   float alpha, beta;
   int splits;            // slices of K; > 1 writes partials to ws
   int kb_per_split;      // k blocks per slice
+  int dp_units;          // whole tiles (rows of units below tail_tm0) computed before the split units
+  int tail_tm0;          // first row of units (pairs of tile rows for pairs) that is cut into K slices
+  int64_t ws_row0;       // C row that workspace row 0 holds (tail_tm0's first row; 0 for plain split-K)
   float* ws;
   int64_t ws_ld;
   int64_t ws_slice;      // elements between successive K slices' partial sums

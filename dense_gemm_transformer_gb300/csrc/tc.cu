@@ -111,7 +111,9 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.num_kb = static_cast<int>((a.K + bk - 1) / bk);
   p.splits = a.splits;
   p.kb_per_split = a.kb_per_split;
-  p.num_units = p.num_tm * p.num_tn * a.splits;
+  p.dp_units = a.dp_units;
+  p.tail_tm0 = a.tail_tm0;
+  p.num_units = a.dp_units + (p.num_tm - a.tail_tm0) * p.num_tn * a.splits;
   p.group_m = a.group_m;
   p.alpha = a.alpha;
   p.beta = a.beta;
@@ -120,26 +122,31 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.ws = a.ws;
   p.ws_ld = a.ws_ld;
   p.ws_slice = a.ws_slice;
+  p.ws_row0 = a.ws_row0;
   p.status = a.status;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
   // Tiles leave through TMA stores when the destination allows it: not the
   // transposed small-M form, no read of C (beta == 0, or partial sums), and
-  // 16-byte aligned rows.
-  CUtensorMap tcm;
+  // 16-byte aligned rows.  Whole tiles go to C, partial tiles to the
+  // workspace (its rows start at C row ws_row0).
+  CUtensorMap tcm, twm;
   std::memset(&tcm, 0, sizeof tcm);
+  std::memset(&twm, 0, sizeof twm);
   p.c_tma = 0;
+  p.w_tma = 0;
   if (a.tile_n >= 128) {
-    if (a.splits > 1) {
-      p.c_tma = (encode_out(&tcm, a.ws, a.N, a.M, a.splits, a.ws_ld, a.ws_slice) == cudaSuccess) ? 1 : 0;
-    } else if (a.beta == 0.f && p.c_vec) {
+    if (a.splits > 1)
+      p.w_tma = (encode_out(&twm, a.ws, a.N, a.M - a.ws_row0, a.splits, a.ws_ld, a.ws_slice) == cudaSuccess) ? 1 : 0;
+    const bool whole = a.splits == 1 || a.dp_units > 0;
+    if (whole && a.beta == 0.f && p.c_vec)
       p.c_tma = (encode_out(&tcm, a.C, a.N, a.M, 1, a.ldc, a.M * a.ldc) == cudaSuccess) ? 1 : 0;
-    }
   }
   if (a.mode == 2 && (a.tile_n == 192 || a.tile_n == 224))
-    return tc_launch_bf16_mid(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
+    return tc_launch_bf16_mid(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid,
+                              stream);
   if (a.mode == 2)
-    return tc_launch_bf16(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
-  return tc_launch_tf32(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, p, a.grid, stream);
+    return tc_launch_bf16(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid, stream);
+  return tc_launch_tf32(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid, stream);
 }
 
 cudaError_t launch_skinny(const TcArgs& a, cudaStream_t stream) {

@@ -42,19 +42,28 @@
 
 namespace dgt {
 
+// Work units.  Rows of units below tail_tm0 are whole tiles (dp_units of
+// them, full K, written to C); the rows from tail_tm0 on are cut into
+// `splits` K slices of kb_per_split blocks each, and with more than one
+// slice each unit writes raw partial sums to the workspace (C rows from
+// ws_row0 on, one M x N slab per slice) for the slice-reduce kernel.
+// tail_tm0 = 0 cuts every tile (plain split-K, or no split with splits = 1).
 struct TcParams {
   int M, N, K;
-  int num_tm, num_tn, num_kb;
+  int num_tm, num_tn, num_kb;  // num_tm counts rows of units (pairs of tile rows for PAIR)
   int splits, kb_per_split, num_units, group_m;
+  int dp_units, tail_tm0;
   float alpha, beta;
   float* C;
   int64_t ldc;
   float* ws;
   int64_t ws_ld;
   int64_t ws_slice;  // elements between the partial sums of successive K slices
+  int64_t ws_row0;   // the C row of workspace row 0
   int* status;
   int c_vec;  // C rows are 16-byte aligned (ldc % 4 == 0 and C aligned)
-  int c_tma;  // tiles leave through shared memory and TMA stores (tmC is valid)
+  int c_tma;  // whole tiles leave through shared memory and TMA stores (tmC is valid)
+  int w_tma;  // partial tiles likewise (tmW is valid)
 };
 
 // MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands).
@@ -97,24 +106,42 @@ __device__ __forceinline__ void issue_mma(uint32_t d, uint64_t a, uint64_t b, ui
 
 struct Unit {
   int tm, tn, split, kb0, kb1;
+  bool partial;
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
-  Unit w;
-  const int tiles = p.num_tm * p.num_tn;
-  const int t = u % tiles;
-  w.split = u / tiles;
+// Tile t of a region of `rows` unit rows starting at row0, in the grouped
+// raster order: group_m rows walk all columns, so units that run at the
+// same time share A and B tiles in L2.
+__device__ __forceinline__ void raster(int t, int row0, int rows, const TcParams& p, Unit& w) {
   const int span = p.group_m * p.num_tn;
   const int g = t / span;
   const int first_m = g * p.group_m;
-  const int rem = p.num_tm - first_m;
+  const int rem = rows - first_m;
   const int gm = rem < p.group_m ? rem : p.group_m;
   const int r = t % span;
-  w.tm = first_m + r % gm;
+  w.tm = row0 + first_m + r % gm;
   w.tn = r / gm;
+}
+
+__device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
+  Unit w;
+  if (u < p.dp_units) {
+    raster(u, 0, p.tail_tm0, p, w);
+    w.split = 0;
+    w.kb0 = 0;
+    w.kb1 = p.num_kb;
+    w.partial = false;
+    return w;
+  }
+  const int v = u - p.dp_units;
+  const int rows = p.num_tm - p.tail_tm0;
+  const int tiles = rows * p.num_tn;
+  raster(v % tiles, p.tail_tm0, rows, p, w);
+  w.split = v / tiles;
   w.kb0 = w.split * p.kb_per_split;
   const int e = w.kb0 + p.kb_per_split;
   w.kb1 = e < p.num_kb ? e : p.num_kb;
+  w.partial = p.splits > 1;
   return w;
 }
 
@@ -130,7 +157,8 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
 template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
+                   const TcParams p) {
   using Cfg = TcCfg<MODE, BN>;
   constexpr int S = Cfg::STAGES;
   constexpr uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN, B_MN, Cfg::BM, BN);
@@ -178,6 +206,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (p.c_tma) tma_prefetch_desc(&tmC);
+    if (p.w_tma) tma_prefetch_desc(&tmW);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -308,19 +337,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int half = (warp - 2) >> 2;  // which half of the tile's column chunks it stores
     int acc = 0;
     uint32_t acc_phase = 0;
-    const bool partial = p.splits > 1;
-    const bool read_c = !partial && p.beta != 0.f;
     constexpr int CW = Cfg::CW;
     for (int u = unit0; u < p.num_units; u += unit_step) {
       const Unit w = decode_unit(u, p);
       if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull)) break;
       tc_fence_after();
+      const bool partial = w.partial;
+      const bool read_c = !partial && p.beta != 0.f;
       const int tm = tile_row(w);
       const int64_t row = static_cast<int64_t>(tm) * Cfg::BM + sub * 32 + lane;
       const bool row_ok = row < p.M;
+      const int64_t row_base = partial ? p.ws_row0 : 0;  // C row of row 0 of the destination
+      const int64_t wrow = row - row_base;
       float* base = partial ? p.ws + static_cast<int64_t>(w.split) * p.ws_slice : p.C;
       const int64_t ld = partial ? p.ws_ld : p.ldc;
-      float* out = TRANS_C ? base : base + (row_ok ? row : 0) * ld;
+      float* out = TRANS_C ? base : base + (row_ok ? wrow : 0) * ld;
       const bool vec_ok = !TRANS_C && (partial || p.c_vec);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
       constexpr int NCH = BN / CW;  // column chunks of a tile
@@ -335,7 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_wait_ld();
         const int64_t col0 = static_cast<int64_t>(w.tn) * BN + cc * CW;
         if constexpr (Cfg::STAGING_BYTES > 0 && CW == 32) {
-          if (p.c_tma) {
+          if (partial ? p.w_tma : p.c_tma) {
             // Through shared memory: this warp's 32 rows x 32 columns go to
             // one of its two 4 KB buffers in the 128-byte-swizzled layout the
             // TMA unit reads (16-byte chunk j of row t sits at chunk j ^ (t % 8)),
@@ -357,8 +388,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(&tmC, smem_u32(buf), static_cast<int32_t>(col0), tm * Cfg::BM + sub * 32,
-                           partial ? w.split : 0);
+              tma_store_3d(partial ? &tmW : &tmC, smem_u32(buf), static_cast<int32_t>(col0),
+                           static_cast<int32_t>(tm * Cfg::BM + sub * 32 - row_base), partial ? w.split : 0);
               bulk_commit_group();
             }
             continue;
@@ -367,42 +398,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!row_ok || col0 >= p.N) {
           // nothing of this chunk is inside C for this thread
         } else if (vec_ok && col0 + CW <= p.N) {
+          float4* dst = reinterpret_cast<float4*>(out + col0);
+          // All of the chunk's loads of C are issued before any store, so
+          // their latencies overlap.
+          float4 c[CW / 4];
+          if (read_c) {
+#pragma unroll
+            for (int q = 0; q < CW / 4; ++q) c[q] = dst[q];
+          }
+          const float a = partial ? 1.f : p.alpha;
 #pragma unroll
           for (int q = 0; q < CW / 4; ++q) {
             float4 v;
-            v.x = __uint_as_float(r[4 * q + 0]);
-            v.y = __uint_as_float(r[4 * q + 1]);
-            v.z = __uint_as_float(r[4 * q + 2]);
-            v.w = __uint_as_float(r[4 * q + 3]);
-            float4* dst = reinterpret_cast<float4*>(out + col0 + 4 * q);
-            if (!partial) {
-              v.x *= p.alpha;
-              v.y *= p.alpha;
-              v.z *= p.alpha;
-              v.w *= p.alpha;
-              if (read_c) {
-                const float4 c = *dst;
-                v.x = fmaf(p.beta, c.x, v.x);
-                v.y = fmaf(p.beta, c.y, v.y);
-                v.z = fmaf(p.beta, c.z, v.z);
-                v.w = fmaf(p.beta, c.w, v.w);
-              }
+            v.x = a * __uint_as_float(r[4 * q + 0]);
+            v.y = a * __uint_as_float(r[4 * q + 1]);
+            v.z = a * __uint_as_float(r[4 * q + 2]);
+            v.w = a * __uint_as_float(r[4 * q + 3]);
+            if (read_c) {
+              v.x = fmaf(p.beta, c[q].x, v.x);
+              v.y = fmaf(p.beta, c[q].y, v.y);
+              v.z = fmaf(p.beta, c[q].z, v.z);
+              v.w = fmaf(p.beta, c[q].w, v.w);
             }
-            *dst = v;
+            dst[q] = v;
           }
         } else {
+          // TRANS_C: lanes hold consecutive rows, so each access of the warp is contiguous.
+          auto at = [&](int j) { return TRANS_C ? out + (col0 + j) * ld + wrow : out + col0 + j; };
+          float c[CW];
+          if (read_c) {
+#pragma unroll
+            for (int j = 0; j < CW; ++j) c[j] = (col0 + j < p.N) ? *at(j) : 0.f;
+          }
+          const float a = partial ? 1.f : p.alpha;
 #pragma unroll
           for (int j = 0; j < CW; ++j) {
-            const int64_t col = col0 + j;
-            if (col < p.N) {
-              // TRANS_C: lanes hold consecutive rows, so each store of the warp is contiguous.
-              float* dst = TRANS_C ? out + col * ld + row : out + col;
-              float v = __uint_as_float(r[j]);
-              if (!partial) {
-                v *= p.alpha;
-                if (read_c) v = fmaf(p.beta, *dst, v);
-              }
-              *dst = v;
+            if (col0 + j < p.N) {
+              float v = a * __uint_as_float(r[j]);
+              if (read_c) v = fmaf(p.beta, c[j], v);
+              *at(j) = v;
             }
           }
         }

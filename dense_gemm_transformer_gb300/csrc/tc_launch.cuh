@@ -8,8 +8,8 @@
 namespace dgt {
 
 template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C = false, bool PAIR = false>
-cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p,
-                          int grid, cudaStream_t s) {
+cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
+                          const TcParams& p, int grid, cudaStream_t s) {
   using Cfg = TcCfg<MODE, BN>;
   auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN, TRANS_C, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
@@ -30,9 +30,10 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
+    return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tw, p);
   } else {
-    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kTcThreads), Cfg::SMEM_BYTES, s, ta, tb, tc, p);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kTcThreads), Cfg::SMEM_BYTES, s, ta, tb, tc, tw,
+                      p);
   }
 }
 
@@ -48,13 +49,13 @@ constexpr bool tc_mn_b_ok() {
 
 template <int MODE, int BN, bool PAIR>
 cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                         const TcParams& p, int grid, cudaStream_t s) {
-  if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN, false, PAIR>(ta, tb, tc, p, grid, s);
+                         const CUtensorMap& tw, const TcParams& p, int grid, cudaStream_t s) {
+  if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
   if constexpr (MODE == 2) {
-    if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN, false, PAIR>(ta, tb, tc, p, grid, s);
+    if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
     if constexpr (tc_mn_b_ok<MODE, BN, PAIR>()) {
-      if (!a_mn) return tc_launch_one<MODE, false, true, BN, false, PAIR>(ta, tb, tc, p, grid, s);
-      return tc_launch_one<MODE, true, true, BN, false, PAIR>(ta, tb, tc, p, grid, s);
+      if (!a_mn) return tc_launch_one<MODE, false, true, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
+      return tc_launch_one<MODE, true, true, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
     }
   }
   return cudaErrorInvalidValue;
@@ -66,13 +67,14 @@ cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUte
 // the two-CTA form (256 columns).
 template <int MODE>
 cudaError_t tc_launch_mode(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s) {
-  if (tile_n == 256 && pair) return tc_launch_bn<MODE, 256, true>(a_mn, b_mn, ta, tb, tc, p, grid, s);
-  if (tile_n == 256) return tc_launch_bn<MODE, 256, false>(a_mn, b_mn, ta, tb, tc, p, grid, s);
-  if (tile_n == 128 && !pair) return tc_launch_bn<MODE, 128, false>(a_mn, b_mn, ta, tb, tc, p, grid, s);
+                           const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid,
+                           cudaStream_t s) {
+  if (tile_n == 256 && pair) return tc_launch_bn<MODE, 256, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
+  if (tile_n == 256) return tc_launch_bn<MODE, 256, false>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
+  if (tile_n == 128 && !pair) return tc_launch_bn<MODE, 128, false>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
   if (tile_n == 16 && !b_mn && !pair) {
-    if (!a_mn) return tc_launch_one<MODE, false, false, 16, true>(ta, tb, tc, p, grid, s);
-    if constexpr (MODE == 2) return tc_launch_one<MODE, true, false, 16, true>(ta, tb, tc, p, grid, s);
+    if (!a_mn) return tc_launch_one<MODE, false, false, 16, true>(ta, tb, tc, tw, p, grid, s);
+    if constexpr (MODE == 2) return tc_launch_one<MODE, true, false, 16, true>(ta, tb, tc, tw, p, grid, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -82,23 +84,25 @@ cudaError_t tc_launch_mode(int tile_n, bool pair, bool a_mn, bool b_mn, const CU
 // 224 instead of 16 of 256).
 template <int MODE>
 cudaError_t tc_launch_mode_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
-                               const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p, int grid,
-                               cudaStream_t s) {
-  if (tile_n == 192 && pair) return tc_launch_bn<MODE, 192, true>(a_mn, b_mn, ta, tb, tc, p, grid, s);
-  if (tile_n == 192) return tc_launch_bn<MODE, 192, false>(a_mn, b_mn, ta, tb, tc, p, grid, s);
-  if (tile_n == 224 && pair) return tc_launch_bn<MODE, 224, true>(a_mn, b_mn, ta, tb, tc, p, grid, s);
-  if (tile_n == 224) return tc_launch_bn<MODE, 224, false>(a_mn, b_mn, ta, tb, tc, p, grid, s);
+                               const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
+                               const TcParams& p, int grid, cudaStream_t s) {
+  if (tile_n == 192 && pair) return tc_launch_bn<MODE, 192, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
+  if (tile_n == 192) return tc_launch_bn<MODE, 192, false>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
+  if (tile_n == 224 && pair) return tc_launch_bn<MODE, 224, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
+  if (tile_n == 224) return tc_launch_bn<MODE, 224, false>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
   return cudaErrorInvalidValue;
 }
 
 // Defined in tc_tf32.cu (MODE 1), tc_bf16.cu (MODE 2: 16, 128 and 256
 // columns) and tc_bf16_mid.cu (MODE 2: 192 and 224 columns).
 cudaError_t tc_launch_tf32(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s);
+                           const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid,
+                           cudaStream_t s);
 cudaError_t tc_launch_bf16(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
-                           const CUtensorMap& tc, const TcParams& p, int grid, cudaStream_t s);
+                           const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid,
+                           cudaStream_t s);
 cudaError_t tc_launch_bf16_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
-                               const CUtensorMap& tb, const CUtensorMap& tc, const TcParams& p, int grid,
-                               cudaStream_t s);
+                               const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
+                               const TcParams& p, int grid, cudaStream_t s);
 
 }  // namespace dgt

@@ -92,7 +92,8 @@ typedef struct {
   int32_t grid;          /* CTAs of the main kernel */
   int32_t kernels;       /* kernels launched by the call */
   int32_t packed;        /* bit 0: A re-packed (or transposed), bit 1: B, into the workspace */
-  int32_t schedule;      /* SIMT: 0 one CTA per tile, 1 split-K slices, 2 stream-K */
+  int32_t schedule;      /* 0 one unit per tile, 1 split-K slices, 2 stream-K (SIMT),
+                            3 whole tiles then K slices for the last rows of tiles (TC) */
   int32_t cluster;       /* TC: CTAs per cluster (2 = pairs sharing each B tile) */
   int32_t reserved[5];
 } gemm_plan_t;

@@ -124,6 +124,33 @@ def test_tc_paired_ctas(h, mode, pair, tA, tB, M, N, K, tile_n):
     _cases.run_and_check(h, mode, M, N, K, tA, tB, seed=79, dist="normal")
 
 
+@pytest.mark.parametrize("mode,M,N,K,tile_n", [("bf16", 4096, 4096, 4096, 256), ("tf32", 2304, 2304, 1024, 0),
+                                                 ("tf32", 2200, 2100, 1000, 0)])
+@pytest.mark.parametrize("tB", [False, True])
+def test_tc_tail_rows_cut_into_k_slices(h, mode, M, N, K, tile_n, tB):
+    """Whole tiles for the leading rows of tile pairs, the last rows cut into
+    K slices whose partial sums the reduce kernel adds into C: checked on rows
+    of both regions, across their boundary and at the ragged bottom edge."""
+    h.set_option("tile_n", tile_n)
+    probe = torch.zeros((M, N), device="cuda")
+    ops, _ = _cases.make(mode, M, N, K, False, tB)
+    h.run(ops.A, ops.B, probe, mode=mode, transB=tB)
+    plan = h.plan()
+    assert plan["schedule"] == "tail_split" and plan["split_k"] > 1 and plan["cluster"] == 2, plan
+    rows = [(0, 2), (M // 2, M // 2 + 1), (M - 3, M)]
+    # the boundary lies on a pair-row (256 C rows) edge somewhere in the last quarter
+    for b in range(256 * ((M // 256) // 2), M, 256):
+        rows.append((b - 1, b + 1))
+    rows = sorted(set((max(0, r0), min(M, r1)) for r0, r1 in rows))
+    _cases.run_and_check(h, mode, M, N, K, False, tB, seed=81, dist="normal", rows=rows)
+    if K <= 1024:
+        _cases.run_and_check(h, mode, M, N, K, False, tB, seed=83, dist="int", rows=rows, exact=True)
+        assert h.plan()["schedule"] == "tail_split"
+    # beta != 0 adds a read of C to the reduction, which may tip the planner
+    # back to whole tiles; either way the result must hold
+    _cases.run_and_check(h, mode, M, N, K, False, tB, alpha=0.5, beta=1.0, seed=82, dist="normal", rows=rows)
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("splits", [2, 5])
 def test_forced_split_k(h, mode, splits):
