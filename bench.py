@@ -383,38 +383,45 @@ def bench_ours(args, world, rank, local):
             bufs[1] = (dev_inputs2, [c for c in bufs[1][1] if re.fullmatch(args.only, c.name)])
         pinned_out = [torch.empty(c.C.shape, dtype=c.C.dtype, pin_memory=True) for c in calls]
         d2h = sum(t.numel() * t.element_size() for t in pinned_out)
-        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        # Two copy streams per direction, so that transfers can use more
+        # than one copy engine at a time.
+        ups = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        downs = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
         done = [torch.cuda.Event() for _ in calls]
-        up_done = [torch.cuda.Event(), torch.cuda.Event()]
+        up_done = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(2)]
         comp_done = [torch.cuda.Event(), torch.cuda.Event()]
-        down_done = [torch.cuda.Event(), torch.cuda.Event()]
+        down_done = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(2)]
 
         def e2e_step(s):
             b = s % 2
             ins, cls = bufs[b]
-            up.wait_event(comp_done[b])  # the GEMMs that last read these inputs are done
-            with torch.cuda.stream(up):
-                for src, dst in zip(pinned_in, ins):
-                    dst.copy_(src, non_blocking=True)
-            up_done[b].record(up)
-            stream.wait_event(up_done[b])
-            stream.wait_event(down_done[b])  # these outputs have been downloaded
-            for c, dst, ev in zip(cls, pinned_out, done):
+            for i, up in enumerate(ups):
+                up.wait_event(comp_done[b])  # the GEMMs that last read these inputs are done
+                with torch.cuda.stream(up):
+                    for src, dst in list(zip(pinned_in, ins))[i::2]:
+                        dst.copy_(src, non_blocking=True)
+                up_done[i][b].record(up)
+                stream.wait_event(up_done[i][b])
+            for i in range(2):
+                stream.wait_event(down_done[i][b])  # these outputs have been downloaded
+            for j, (c, dst, ev) in enumerate(zip(cls, pinned_out, done)):
                 run_call(h, c, stream)
                 ev.record(stream)
+                down = downs[j % 2]
                 down.wait_event(ev)
                 with torch.cuda.stream(down):
                     dst.copy_(c.C, non_blocking=True)
             comp_done[b].record(stream)
-            down_done[b].record(down)
+            for i, down in enumerate(downs):
+                down_done[i][b].record(down)
 
         def run_steps(n):
-            up.wait_stream(stream)
-            down.wait_stream(stream)
+            for q in ups + downs:
+                q.wait_stream(stream)
             for s in range(n):
                 e2e_step(s)
-            stream.wait_stream(up)
-            stream.wait_stream(down)
+            for q in ups + downs:
+                stream.wait_stream(q)
 
         run_steps(2)
         stream.synchronize()
