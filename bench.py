@@ -494,6 +494,8 @@ def bench_sweep(args):
     h = dg.Gemm()
     if args.tile_n:
         h.set_option("tile_n", args.tile_n)
+    if args.pair is not None:
+        h.set_option("pair", args.pair)
     stream = torch.cuda.Stream(dev)
     pk = peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -580,6 +582,8 @@ def main():
     ap.add_argument("--ref-macs", type=float, default=3e8, help="oracle multiply-adds per reference step")
     ap.add_argument("--tile-n", type=int, default=0, help="sweeps: force the tensor-core tile width (128/256)")
     ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
+    ap.add_argument("--pair", type=int, default=None,
+                    help="sweeps: force the CTA-pair form (0 planner, 1 none, 2 multicast B, 3 one 256-row MMA per pair)")
     ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny"],
                     help="gpt: the timed step; the others print a per-shape sweep")
     args = ap.parse_args()

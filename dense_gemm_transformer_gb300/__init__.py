@@ -38,7 +38,8 @@ class Plan(ctypes.Structure):
     _fields_ = [("family", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("tile_k", ctypes.c_int32), ("split_k", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("kernels", ctypes.c_int32), ("packed", ctypes.c_int32),
-                ("schedule", ctypes.c_int32), ("cluster", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+                ("schedule", ctypes.c_int32), ("cluster", ctypes.c_int32), ("pair_mma", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 4)]
 
 
 _lib = None
@@ -148,7 +149,7 @@ class Gemm:
                 "tile_k": p.tile_k, "split_k": p.split_k, "stages": p.stages, "grid": p.grid,
                 "kernels": p.kernels, "packed": p.packed,
                 "schedule": {0: "tiles", 1: "split_k", 2: "stream_k", 3: "tail_split"}.get(p.schedule, "tiles"),
-                "cluster": p.cluster}
+                "cluster": p.cluster, "pair_mma": p.pair_mma}
 
     def check_device(self, stream=None) -> int:
         """Synchronize the stream and return the device status (0 = ok)."""

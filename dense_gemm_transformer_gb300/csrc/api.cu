@@ -270,12 +270,14 @@ cudaError_t run_pack(const OperandPack& p, void* dst, int es, cudaStream_t s) {
   return dgt::launch_pack(p.src, p.ld, dst, p.dst_ld, p.rows, p.cols, es, s);
 }
 
-// Nominal dense tensor rates (flop/s) used only to weigh a wave of tiles
-// against the extra reduction traffic of a K split.
-constexpr double kBf16Flops = 2.25e15;
-constexpr double kTf32Flops = 1.1e15;
-constexpr double kHbmBytes = 7.0e12;
-constexpr double kLaunchS = 2e-6;
+// Rates used only to weigh a wave of tiles against the extra reduction
+// traffic of a K split: dense tensor rates as measured on this part, a
+// kernel efficiency of 0.8 of them, HBM bandwidth and the cost of one more
+// (programmatically launched) kernel.
+constexpr double kBf16Flops = 1.9e15 * 0.8;
+constexpr double kTf32Flops = 0.95e15 * 0.8;
+constexpr double kHbmBytes = 6.5e12;
+constexpr double kLaunchS = 1.5e-6;
 
 // Which last rows of work units to cut into K slices, and into how many:
 // units are handed out round-robin to `slots` persistent CTAs (or CTA
@@ -306,7 +308,7 @@ TailPlan plan_tail(int64_t unit_rows, int64_t unit_cols, int64_t kb, int64_t slo
       const double worst = dp0 + (static_cast<double>(ceil_div(T, slots)) - dp0) * f;
       const double reduce = static_cast<double>(R) * c_bytes_per_row * (sl + 1 + (read_c ? 1 : 0)) / kHbmBytes;
       const double cost = worst * unit_s + reduce + kLaunchS;
-      if (cost < 0.97 * best) {
+      if (cost < 0.98 * best) {
         best = cost;
         best_plan.rows = R;
         best_plan.slices = sl;
@@ -370,11 +372,16 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
     return !swap && tm_tiles >= 2 && h->opt_pair != 1 && dgt::tc_tile_ok(mode, tn, true, b_mn_kernel);
   };
   const double peak = (mode == GEMM_MODE_BF16 ? kBf16Flops : kTf32Flops) / sms;
+  // Pairs of 256-column tiles issue one MMA of 256 rows per pair (tcgen05
+  // cta_group::2) unless told to share B by multicast only: each CTA then
+  // stages and reads half of B, which measured 1.14x the speed on large
+  // shapes (BF16 8192^3: 1687 -> 1929 TFLOP/s).
+  auto mma2_for = [&](int tn) { return tn == 256 && pair_ok(tn) && (h->opt_pair == 0 || h->opt_pair == 3); };
   auto plan_for = [&](int tn) {
     const bool pr = pair_ok(tn);
     const int64_t rows = pr ? ceil_div(tm_tiles, 2) : tm_tiles;
-    const double unit_s =
-        2.0 * 128.0 * 256.0 * static_cast<double>(K) / peak * (128.0 * 128.0 + 128.0 * tn) / (128.0 * 384.0);
+    const double unit_s = 2.0 * 128.0 * 256.0 * static_cast<double>(K) / peak *
+                          (128.0 * 128.0 + 128.0 * tn) / (128.0 * 384.0) / (mma2_for(tn) ? 1.14 : 1.0);
     const double c_row_bytes = 4.0 * static_cast<double>(Nk) * (pr ? 256.0 : 128.0);
     const bool may_cut = !swap && h->opt_split_k == 0 && !(2 * tm_tiles * ceil_div(Nk, tn) <= sms && kb >= 8);
     if (!may_cut) {
@@ -515,7 +522,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   // Two-CTA clusters sharing each B tile (TMA multicast) for tiles of 192
   // columns or more with at least two rows of tiles: each CTA then pulls
   // half of B per stage from L2 (256 columns: 32 KB instead of 48 KB).
-  a.pair = pair ? 1 : 0;
+  a.pair = !pair ? 0 : mma2_for(tile_n) ? 2 : 1;
   const int64_t units = a.dp_units + (unit_rows - a.tail_tm0) * unit_cols * splits;
   a.grid = static_cast<int>(pair ? 2 * std::min<int64_t>(units, sms / 2) : std::min<int64_t>(units, sms));
   a.group_m = a.pair ? 8 : 16;
@@ -530,6 +537,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   set_plan(h, swap ? GEMM_FAMILY_SKINNY : GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n),
            a.grid, kernels, (swap ? ((pack_b ? 1 : 0) | (pack_a ? 2 : 0)) : ((pack_a ? 1 : 0) | (pack_b ? 2 : 0))));
   h->plan.cluster = a.pair ? 2 : 1;
+  h->plan.pair_mma = a.pair == 2 ? 1 : 0;
   h->plan.schedule = tail.rows > 0 ? 3 : (a.splits > 1 ? 1 : 0);
   return GEMM_OK;
 }
@@ -642,7 +650,7 @@ gemm_status_t gemm_set_option(gemm_handle_t h, int option, int64_t value) {
       h->opt_pretranspose = static_cast<int>(value);
       return GEMM_OK;
     case GEMM_OPT_PAIR:
-      if (value < 0 || value > 1) return GEMM_ERR_INVALID_VALUE;
+      if (value < 0 || value > 3) return GEMM_ERR_INVALID_VALUE;
       h->opt_pair = static_cast<int>(value);
       return GEMM_OK;
     default:

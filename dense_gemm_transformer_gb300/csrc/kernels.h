@@ -74,7 +74,8 @@ struct TcArgs {
   int a_mn_major;        // A stored with M contiguous (transA == 1)
   int b_mn_major;        // B stored with N contiguous (transB == 0)
   int tile_n;            // 128, 192, 224 or 256 (16: the swapped small-M form)
-  int pair;              // tile_n >= 192: two-CTA clusters sharing each B tile by TMA multicast
+  int pair;              // tile_n >= 192: two-CTA clusters; 1: sharing each B tile by TMA multicast,
+                         // 2 (tile_n 256): one MMA of 256 rows per pair (tcgen05 cta_group::2)
   int64_t M, N, K;
   const void* A;         // base of the (possibly re-packed) operand
   int64_t lda;           // elements

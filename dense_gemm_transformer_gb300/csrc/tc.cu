@@ -95,8 +95,10 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   e = a.a_mn_major ? encode_2d(&ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
                    : encode_2d(&ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
   if (e != cudaSuccess) return e;
-  // A pair of CTAs loads one half of each B tile apiece (K-major: half the rows).
-  const bool pair = a.pair != 0 && a.tile_n >= 192;
+  // A pair of CTAs loads one half of each B tile apiece (K-major: half the
+  // rows): pair 1 shares the halves by multicast, pair 2 (256 columns)
+  // issues one MMA of 256 rows over both CTAs.
+  const int pair = (a.tile_n >= 192) ? a.pair : 0;
   e = a.b_mn_major ? encode_2d(&tb, a.mode, a.B, a.N, a.K, a.ldb, ch, bk)
                    : encode_2d(&tb, a.mode, a.B, a.K, a.N, a.ldb, bk, pair ? a.tile_n / 2 : a.tile_n);
   if (e != cudaSuccess) return e;

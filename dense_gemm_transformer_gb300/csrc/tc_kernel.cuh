@@ -66,8 +66,10 @@ struct TcParams {
   int w_tma;  // partial tiles likewise (tmW is valid)
 };
 
-// MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands).
-template <int MODE, int BN>
+// MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands).  BHALF: a
+// stage holds one half of the B tile (the two-CTA MMA, where the other CTA
+// of the pair holds the other half).
+template <int MODE, int BN, bool BHALF = false>
 struct TcCfg {
   static constexpr int ES = (MODE == 2) ? 2 : 4;      // operand bytes
   static constexpr int BM = 128;                      // rows of the tile (UMMA M)
@@ -75,18 +77,20 @@ struct TcCfg {
   static constexpr int UK = (MODE == 2) ? 16 : 8;     // K of one MMA instruction (32 bytes)
   static constexpr int CH = 128 / ES;                 // M/N elements of one 128-byte MN-major row
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int B_BYTES = BHALF ? BN * 64 : BN * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // ~192-200 KB of operand stages
-  static constexpr int STAGES = (BN >= 192) ? 4 : (BN == 128) ? 6 : 200 * 1024 / STAGE_BYTES;
+  // Epilogue staging for TMA stores: one buffer of 32 rows x 128 bytes per
+  // epilogue warp (the swapped small-M form stores directly and has none).
+  static constexpr int STAGING_BYTES = (BN >= 128) ? kTcEpiWarps * 32 * 128 : 0;
+  // ~192-200 KB of operand stages (as many as fit beside the staging when
+  // a stage holds half of B)
+  static constexpr int STAGES = BHALF ? (232448 - STAGING_BYTES - 1280) / STAGE_BYTES
+                                      : (BN >= 192) ? 4 : (BN == 128) ? 6 : 200 * 1024 / STAGE_BYTES;
   // Two accumulators; an allocation is a power of two of at least 32 columns.
   static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
   static constexpr int CW = BN < 32 ? BN : 32;                    // accumulator columns per TMEM load
   static constexpr int NUM_BARS = 2 * STAGES + 5;     // full/empty per stage, acc full/empty x2, drain
-  // Epilogue staging for TMA stores: one buffer of 32 rows x 128 bytes per
-  // epilogue warp (the swapped small-M form stores directly and has none).
-  static constexpr int STAGING_BYTES = (BN >= 128) ? kTcEpiWarps * 32 * 128 : 0;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
   static constexpr uint32_t FORMAT = (MODE == 2) ? 1u : 2u;  // bf16 / tf32 in the instruction descriptor
@@ -96,12 +100,29 @@ struct TcCfg {
   static_assert(BN < 32 || BN % 32 == 0, "the epilogue moves 32-column chunks");
 };
 
-template <int MODE>
+template <int MODE, bool MMA2>
 __device__ __forceinline__ void issue_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  if (MODE == 2)
-    mma_bf16(d, a, b, idesc, acc);
+  if constexpr (MMA2) {
+    if (MODE == 2)
+      mma_bf16_pair(d, a, b, idesc, acc);
+    else
+      mma_tf32_pair(d, a, b, idesc, acc);
+  } else {
+    if (MODE == 2)
+      mma_bf16(d, a, b, idesc, acc);
+    else
+      mma_tf32(d, a, b, idesc, acc);
+  }
+}
+
+// Bounded wait on a barrier of this CTA; MMA2 kernels wait with cluster
+// scope (the other CTA of the pair or its MMAs arrive on it).
+template <bool CLUSTER>
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status, int code) {
+  if constexpr (CLUSTER)
+    return mbar_wait_cluster(bar, parity, abort, status, code);
   else
-    mma_tf32(d, a, b, idesc, acc);
+    return mbar_wait(bar, parity, abort, status, code);
 }
 
 struct Unit {
@@ -154,14 +175,23 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
 // CTAs' shared memory, so each stage costs each CTA 16 KB of L2 traffic for
 // B instead of 32 KB.  A stage may be refilled only when both CTAs' MMAs have
 // read it: each MMA warp commits to the "empty" barrier of both CTAs.
-template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C, bool PAIR>
+// MMA2 (with PAIR): instead, the pair issues one MMA of 256 rows
+// (tcgen05 cta_group::2): each CTA loads its own 128 rows of A and its own
+// half of B into its own shared memory, and counts the bytes on the even
+// CTA's "full" barrier; one thread of the even CTA issues the MMAs, which
+// read A and B from both CTAs and write each CTA's 128 rows of the
+// accumulator into that CTA's TMEM, and commits to both CTAs' barriers;
+// both CTAs' epilogue warps release an accumulator on the even CTA's
+// barrier.  Each CTA then stages 32 KB per 256-column stage instead of 48.
+template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C, bool PAIR, bool MMA2 = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                    const TcParams p) {
-  using Cfg = TcCfg<MODE, BN>;
+  static_assert(!MMA2 || PAIR, "the two-CTA MMA runs on pairs");
+  using Cfg = TcCfg<MODE, BN, MMA2>;
   constexpr int S = Cfg::STAGES;
-  constexpr uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN, B_MN, Cfg::BM, BN);
+  constexpr uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN, B_MN, MMA2 ? 2 * Cfg::BM : Cfg::BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -184,6 +214,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // Work units: one per CTA, or one per two-CTA cluster (the pair's rank
   // picks its row of tiles).  The cluster of a pair is blockIdx.x / 2.
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0u;  // MMA2: the CTA that issues the pair's MMAs
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int unit_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   auto tile_row = [&](const Unit& w) { return PAIR ? 2 * w.tm + static_cast<int>(rank) : w.tm; };
@@ -191,11 +222,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), PAIR ? 2 : 1);  // PAIR: both CTAs' MMAs must have read the stage
+      // PAIR: both CTAs' MMAs must have read the stage; MMA2: the one pair MMA
+      mbar_init(empty_bar(s), (PAIR && !MMA2) ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
-      mbar_init(acce_bar(a), kTcEpiWarps);  // one arrival per epilogue warp
+      mbar_init(acce_bar(a), MMA2 ? 2 * kTcEpiWarps : kTcEpiWarps);  // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -209,8 +241,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (p.w_tma) tma_prefetch_desc(&tmW);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (MMA2) {
+      tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -235,15 +272,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const Unit w = decode_unit(u, p);
         const int tm = tile_row(w);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, kDevTimeoutEmpty)) {
+          if (!bar_wait<MMA2>(empty_bar(stage), phase ^ 1u, abort_flag, p.status, kDevTimeoutEmpty)) {
             ok = false;
             break;
           }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
           const uint32_t a_dst = smem0 + stage * Cfg::STAGE_BYTES;
           const uint32_t b_dst = a_dst + Cfg::A_BYTES;
           const int k0 = kb * Cfg::BK;
+          if constexpr (MMA2) {
+            // Both CTAs' copies are counted on the even CTA's barrier, which
+            // expects the bytes of the two (a copy of the odd CTA may land
+            // before that expectation: the barrier's phase cannot complete
+            // until the even CTA has arrived).
+            const uint32_t fb = dsmem_map(full_bar(stage), 0);
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::STAGE_BYTES);
+            if (A_MN) {
+#pragma unroll
+              for (int c = 0; c < Cfg::BM / Cfg::CH; ++c)
+                tma_load_2d_pair(a_dst + c * Cfg::BK * 128, &tmA, fb, tm * Cfg::BM + c * Cfg::CH, k0);
+            } else {
+              tma_load_2d_pair(a_dst, &tmA, fb, k0, tm * Cfg::BM);
+            }
+            if (B_MN) {
+              constexpr int NH = BN / Cfg::CH / 2;  // this CTA's 128-byte column chunks of B
+#pragma unroll
+              for (int c = 0; c < NH; ++c)
+                tma_load_2d_pair(b_dst + c * Cfg::BK * 128, &tmB, fb,
+                                 w.tn * BN + (static_cast<int>(rank) * NH + c) * Cfg::CH, k0);
+            } else {
+              tma_load_2d_pair(b_dst, &tmB, fb, k0, w.tn * BN + static_cast<int>(rank) * (BN / 2));
+            }
+            ++issued;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
           if (A_MN) {
 #pragma unroll
             for (int c = 0; c < Cfg::BM / Cfg::CH; ++c)
@@ -276,15 +343,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      if (!ok) {
-        // Wait for every copy still in flight before the CTA can exit.
+      if (!ok && (!MMA2 || leader)) {
+        // Wait for every copy still in flight before the CTA can exit (an
+        // MMA2 odd CTA's copies complete on the even CTA's barriers, whose
+        // drain covers them; the pair leaves together).
         const uint32_t n = issued < static_cast<uint32_t>(S) ? issued : static_cast<uint32_t>(S);
         for (uint32_t i = issued - n; i < issued; ++i) drain_wait(full_bar(i % S), (i / S) & 1u, p.status);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // MMA2: only the even CTA of the pair issues (its MMAs cover both CTAs).
+    if (lane == 0 && (!MMA2 || leader)) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -292,11 +362,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Unit w = decode_unit(u, p);
-        if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty)) break;
+        if (!bar_wait<MMA2>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull)) {
+          if (!bar_wait<MMA2>(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull)) {
             ok = false;
             break;
           }
@@ -309,9 +379,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                      : smem_desc_sw128(a_base + j * Cfg::UK * Cfg::ES, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(b_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
                                      : smem_desc_sw128(b_base + j * Cfg::UK * Cfg::ES, 16, 1024);
-            issue_mma<MODE>(d_tmem, ad, bd, IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
+            issue_mma<MODE, MMA2>(d_tmem, ad, bd, IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
           }
-          if constexpr (PAIR)
+          if constexpr (MMA2)
+            mma_commit_pair_multicast(empty_bar(stage), 0x3);  // both CTAs' halves of the stage are free
+          else if constexpr (PAIR)
             mma_commit_multicast(empty_bar(stage), 0x3);  // both CTAs' copies of the stage are free
           else
             mma_commit(empty_bar(stage));
@@ -321,14 +393,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(accf_bar(acc));
+        if constexpr (MMA2)
+          mma_commit_pair_multicast(accf_bar(acc), 0x3);  // each CTA's 128 rows are ready in its TMEM
+        else
+          mma_commit(accf_bar(acc));
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // Every MMA this thread issued has finished once drain_bar flips.
-      mma_commit(drain_bar);
+      if constexpr (MMA2)
+        mma_commit_pair(drain_bar);
+      else
+        mma_commit(drain_bar);
       drain_wait(drain_bar, 0, p.status);
     }
   } else {
@@ -340,7 +418,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int CW = Cfg::CW;
     for (int u = unit0; u < p.num_units; u += unit_step) {
       const Unit w = decode_unit(u, p);
-      if (!mbar_wait(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull)) break;
+      if (!bar_wait<MMA2>(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull)) break;
       tc_fence_after();
       const bool partial = w.partial;
       const bool read_c = !partial && p.beta != 0.f;
@@ -443,7 +521,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(acc));
+      if (lane == 0) {
+        if constexpr (MMA2)
+          mbar_arrive_cluster(dsmem_map(acce_bar(acc), 0));  // the even CTA's MMAs reuse the accumulator
+        else
+          mbar_arrive(acce_bar(acc));
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -461,7 +544,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if constexpr (MMA2)
+      tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
 }
 

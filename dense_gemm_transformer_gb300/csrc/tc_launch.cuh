@@ -7,11 +7,11 @@
 
 namespace dgt {
 
-template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C = false, bool PAIR = false>
+template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C = false, bool PAIR = false, bool MMA2 = false>
 cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                           const TcParams& p, int grid, cudaStream_t s) {
-  using Cfg = TcCfg<MODE, BN>;
-  auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN, TRANS_C, PAIR>;
+  using Cfg = TcCfg<MODE, BN, MMA2>;
+  auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN, TRANS_C, PAIR, MMA2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if constexpr (PAIR) {
@@ -47,15 +47,15 @@ constexpr bool tc_mn_b_ok() {
   return MODE == 2 && BN % TcCfg<MODE, BN>::CH == 0 && (!PAIR || (BN / TcCfg<MODE, BN>::CH) % 2 == 0);
 }
 
-template <int MODE, int BN, bool PAIR>
+template <int MODE, int BN, bool PAIR, bool MMA2 = false>
 cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                          const CUtensorMap& tw, const TcParams& p, int grid, cudaStream_t s) {
-  if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
+  if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN, false, PAIR, MMA2>(ta, tb, tc, tw, p, grid, s);
   if constexpr (MODE == 2) {
-    if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
+    if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN, false, PAIR, MMA2>(ta, tb, tc, tw, p, grid, s);
     if constexpr (tc_mn_b_ok<MODE, BN, PAIR>()) {
-      if (!a_mn) return tc_launch_one<MODE, false, true, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
-      return tc_launch_one<MODE, true, true, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
+      if (!a_mn) return tc_launch_one<MODE, false, true, BN, false, PAIR, MMA2>(ta, tb, tc, tw, p, grid, s);
+      return tc_launch_one<MODE, true, true, BN, false, PAIR, MMA2>(ta, tb, tc, tw, p, grid, s);
     }
   }
   return cudaErrorInvalidValue;
@@ -63,12 +63,15 @@ cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUte
 
 // The 128- and 256-column tiles and the swapped small-M form (tile_n 16:
 // the weights are the 128-row operand, K-major or MN-major, the activations
-// a K-major 16-row operand, and C is written transposed).  `pair` selects
-// the two-CTA form (256 columns).
+// a K-major 16-row operand, and C is written transposed).  `pair`: 0 one
+// CTA per tile, 1 pairs sharing B by multicast, 2 pairs issuing one MMA of
+// 256 rows (256 columns only).
 template <int MODE>
-cudaError_t tc_launch_mode(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t tc_launch_mode(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid,
                            cudaStream_t s) {
+  if (tile_n == 256 && pair == 2) return tc_launch_bn<MODE, 256, true, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
+  if (pair == 2) return cudaErrorInvalidValue;
   if (tile_n == 256 && pair) return tc_launch_bn<MODE, 256, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
   if (tile_n == 256) return tc_launch_bn<MODE, 256, false>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
   if (tile_n == 128 && !pair) return tc_launch_bn<MODE, 128, false>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
@@ -83,9 +86,10 @@ cudaError_t tc_launch_mode(int tile_n, bool pair, bool a_mn, bool b_mn, const CU
 // where 256 would leave the last one mostly idle (4096 columns: 19 tiles of
 // 224 instead of 16 of 256).
 template <int MODE>
-cudaError_t tc_launch_mode_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
+cudaError_t tc_launch_mode_mid(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
                                const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                                const TcParams& p, int grid, cudaStream_t s) {
+  if (pair == 2) return cudaErrorInvalidValue;
   if (tile_n == 192 && pair) return tc_launch_bn<MODE, 192, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
   if (tile_n == 192) return tc_launch_bn<MODE, 192, false>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
   if (tile_n == 224 && pair) return tc_launch_bn<MODE, 224, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
@@ -95,13 +99,13 @@ cudaError_t tc_launch_mode_mid(int tile_n, bool pair, bool a_mn, bool b_mn, cons
 
 // Defined in tc_tf32.cu (MODE 1), tc_bf16.cu (MODE 2: 16, 128 and 256
 // columns) and tc_bf16_mid.cu (MODE 2: 192 and 224 columns).
-cudaError_t tc_launch_tf32(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t tc_launch_tf32(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid,
                            cudaStream_t s);
-cudaError_t tc_launch_bf16(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t tc_launch_bf16(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid,
                            cudaStream_t s);
-cudaError_t tc_launch_bf16_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
+cudaError_t tc_launch_bf16_mid(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
                                const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                                const TcParams& p, int grid, cudaStream_t s);
 

@@ -79,8 +79,10 @@ typedef enum {
                             for pairs, 192 need a K-major B in BF16); SIMT: 128 or 256    */
   GEMM_OPT_PRETRANSPOSE = 4, /* SIMT: 0 = planner's choice, 1 = never, 2 = always transpose
                                 K-contiguous operands into the workspace first             */
-  GEMM_OPT_PAIR = 5          /* TC: 0 = two-CTA clusters sharing B tiles (tiles of 192 or more
-                                columns) where the planner chooses them, 1 = never          */
+  GEMM_OPT_PAIR = 5          /* TC: two-CTA clusters (tiles of 192 or more columns, two or more
+                                rows of tiles).  0 = planner's choice (256 columns: one 256-row
+                                MMA per pair, tcgen05 cta_group::2; 192/224: pairs sharing B by
+                                multicast), 1 = never, 2 = multicast pairs only, 3 = as 0     */
 } gemm_option_t;
 
 /* What the last successful gemm_run on a handle launched. */
@@ -95,7 +97,8 @@ typedef struct {
   int32_t schedule;      /* 0 one unit per tile, 1 split-K slices, 2 stream-K (SIMT),
                             3 whole tiles then K slices for the last rows of tiles (TC) */
   int32_t cluster;       /* TC: CTAs per cluster (2 = pairs sharing each B tile) */
-  int32_t reserved[5];
+  int32_t pair_mma;      /* TC: 1 when each CTA pair issues one 256-row MMA (tcgen05 cta_group::2) */
+  int32_t reserved[4];
 } gemm_plan_t;
 
 /* Create a handle on the current device.  Reads the device properties and
