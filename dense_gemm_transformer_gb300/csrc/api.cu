@@ -41,6 +41,7 @@ struct gemm_handle_s {
   int opt_pretranspose = 0;
   int opt_pair = 0;
   int sk_active[2][dgt::kSkinnyMaxCluster + 1];  // small-M kernel: resident clusters (-1: not queried)
+  dgt::TmaCache* tma_cache = nullptr;             // TMA descriptors of earlier calls
   gemm_plan_t plan{};
 };
 
@@ -500,6 +501,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.beta = beta;
   a.splits = static_cast<int>(splits);
   a.kb_per_split = static_cast<int>(kb_per);
+  a.tma_cache = h->tma_cache;
   if (cluster_form) {
     a.status = h->d_status;
     a.grid = static_cast<int>(tiles * splits);
@@ -577,6 +579,12 @@ gemm_status_t gemm_create(gemm_handle_t* out) {
     delete h;
     return GEMM_ERR_CUDA;
   }
+  h->tma_cache = new (std::nothrow) dgt::TmaCache();
+  if (h->tma_cache == nullptr) {
+    cudaFree(h->d_status);
+    delete h;
+    return GEMM_ERR_ALLOC;
+  }
   *out = h;
   return GEMM_OK;
 }
@@ -589,6 +597,7 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
   gemm_status_t st = cuda_status(cudaDeviceSynchronize());
   if (h->ws) cudaFree(h->ws);
   if (h->d_status) cudaFree(h->d_status);
+  delete h->tma_cache;
   cudaSetDevice(prev);
   delete h;
   return st;

@@ -1,11 +1,40 @@
 // kernels.h -- host-side launch entry points of the library's kernels (internal).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace dgt {
+
+// Runs `set_up` (a kernel's attribute set-up) once per device: `done` holds
+// one bit per device that has been set up (devices 0-63; others always run
+// it).
+template <typename F>
+cudaError_t once_per_device(std::atomic<uint64_t>& done, F&& set_up) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return set_up();
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  const cudaError_t e = set_up();
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// TMA descriptors encoded for earlier calls of a handle, keyed by every
+// argument of the encoding (a descriptor holds only the base pointer, the
+// sizes, the strides and the box, so an entry stays valid for equal keys).
+// Direct-mapped; a handle is used from one thread at a time.
+struct TmaCache {
+  static constexpr int kEntries = 64;
+  struct alignas(64) Entry {
+    CUtensorMap map;
+    int64_t key[8];
+    bool valid;
+  };
+  Entry entry[kEntries];
+};
 
 // Every kernel of the library is launched with programmatic dependent
 // launch: it may start (and run its set-up, which touches no global memory)
@@ -95,6 +124,7 @@ struct TcArgs {
   int* status;           // device status word
   int grid;              // persistent CTAs
   int group_m;           // raster group height in M tiles
+  TmaCache* tma_cache;   // the handle's descriptor cache (null: encode every call)
 };
 // tile_n == 16 selects the swapped small-M form: the caller passes the
 // operands exchanged (C^T = op(B)^T op(A)^T, M and N exchanged) and the

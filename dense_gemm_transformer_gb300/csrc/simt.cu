@@ -474,7 +474,10 @@ template <int TBN, bool TA, bool TB, bool VEC>
 cudaError_t launch_cvec(const SimtArgs& a, dim3 grid, cudaStream_t s, bool cvec) {
   constexpr int smem = SimtCfg<TBN>::SMEM_BYTES;
   auto kern = cvec ? simt_gemm_kernel<TBN, TA, TB, VEC, true> : simt_gemm_kernel<TBN, TA, TB, VEC, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<uint64_t> done[2] = {};
+  cudaError_t e = once_per_device(done[cvec ? 1 : 0], [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, grid, dim3(NT), smem, s, a);
 }

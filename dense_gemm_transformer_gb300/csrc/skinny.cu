@@ -321,10 +321,13 @@ cudaLaunchConfig_t make_config(const SkParams& p, int grid, cudaStream_t s, cuda
 
 template <int MODE, bool A_MN>
 cudaError_t set_attributes() {
-  auto kern = skinny_gemm_kernel<MODE, A_MN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SkCfg<MODE>::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  static std::atomic<uint64_t> done{0};
+  return once_per_device(done, [] {
+    auto kern = skinny_gemm_kernel<MODE, A_MN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SkCfg<MODE>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  });
 }
 
 template <int MODE, bool A_MN>

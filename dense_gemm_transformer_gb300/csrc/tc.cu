@@ -50,6 +50,50 @@ cudaError_t encode_out(CUtensorMap* m, float* ptr, int64_t N, int64_t M, int64_t
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// encode_2d / encode_out through the handle's cache (kind 0 / 1 in the key).
+cudaError_t cached(TmaCache* cache, CUtensorMap* m, const int64_t (&key)[8], cudaError_t (*encode)(CUtensorMap*,
+                                                                                            const int64_t (&)[8])) {
+  if (cache == nullptr) return encode(m, key);
+  uint64_t h = 1469598103934665603ull;
+  for (int64_t k : key) h = (h ^ static_cast<uint64_t>(k)) * 1099511628211ull;
+  TmaCache::Entry& e = cache->entry[(h >> 32) % TmaCache::kEntries];
+  bool hit = e.valid;
+  for (int i = 0; hit && i < 8; ++i) hit = e.key[i] == key[i];
+  if (!hit) {
+    const cudaError_t r = encode(&e.map, key);
+    if (r != cudaSuccess) {
+      e.valid = false;
+      return r;
+    }
+    for (int i = 0; i < 8; ++i) e.key[i] = key[i];
+    e.valid = true;
+  }
+  *m = e.map;
+  return cudaSuccess;
+}
+
+cudaError_t encode_2d_key(CUtensorMap* m, const int64_t (&k)[8]) {
+  return encode_2d(m, static_cast<int>(k[1]), reinterpret_cast<const void*>(k[0]), k[2], k[3], k[4],
+                   static_cast<uint32_t>(k[5]), static_cast<uint32_t>(k[6]));
+}
+
+cudaError_t encode_out_key(CUtensorMap* m, const int64_t (&k)[8]) {
+  return encode_out(m, reinterpret_cast<float*>(k[0]), k[2], k[3], k[4], k[5], k[6]);
+}
+
+cudaError_t encode_2d_c(TmaCache* cache, CUtensorMap* m, int mode, const void* ptr, int64_t inner, int64_t outer,
+                        int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  const int64_t key[8] = {static_cast<int64_t>(reinterpret_cast<uintptr_t>(ptr)), mode, inner, outer, ld,
+                          box_inner, box_outer, 0};
+  return cached(cache, m, key, encode_2d_key);
+}
+
+cudaError_t encode_out_c(TmaCache* cache, CUtensorMap* m, float* ptr, int64_t N, int64_t M, int64_t S, int64_t ld,
+                         int64_t slice) {
+  const int64_t key[8] = {static_cast<int64_t>(reinterpret_cast<uintptr_t>(ptr)), 256 + 1, N, M, S, ld, slice, 1};
+  return cached(cache, m, key, encode_out_key);
+}
+
 }  // namespace
 
 cudaError_t tc_init_driver() {
@@ -92,15 +136,15 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   const int bk = tc_tile_k(a.mode);
   const int ch = (a.mode == 2) ? 64 : 32;  // elements in a 128-byte MN-major row
   CUtensorMap ta, tb;
-  e = a.a_mn_major ? encode_2d(&ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
-                   : encode_2d(&ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
+  e = a.a_mn_major ? encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
+                   : encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
   if (e != cudaSuccess) return e;
   // A pair of CTAs loads one half of each B tile apiece (K-major: half the
   // rows): pair 1 shares the halves by multicast, pair 2 (256 columns)
   // issues one MMA of 256 rows over both CTAs.
   const int pair = (a.tile_n >= 192) ? a.pair : 0;
-  e = a.b_mn_major ? encode_2d(&tb, a.mode, a.B, a.N, a.K, a.ldb, ch, bk)
-                   : encode_2d(&tb, a.mode, a.B, a.K, a.N, a.ldb, bk, pair ? a.tile_n / 2 : a.tile_n);
+  e = a.b_mn_major ? encode_2d_c(a.tma_cache, &tb, a.mode, a.B, a.N, a.K, a.ldb, ch, bk)
+                   : encode_2d_c(a.tma_cache, &tb, a.mode, a.B, a.K, a.N, a.ldb, bk, pair ? a.tile_n / 2 : a.tile_n);
   if (e != cudaSuccess) return e;
 
   TcParams p;
@@ -138,10 +182,13 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.w_tma = 0;
   if (a.tile_n >= 128) {
     if (a.splits > 1)
-      p.w_tma = (encode_out(&twm, a.ws, a.N, a.M - a.ws_row0, a.splits, a.ws_ld, a.ws_slice) == cudaSuccess) ? 1 : 0;
+      p.w_tma = (encode_out_c(a.tma_cache, &twm, a.ws, a.N, a.M - a.ws_row0, a.splits, a.ws_ld, a.ws_slice) ==
+                 cudaSuccess)
+                    ? 1
+                    : 0;
     const bool whole = a.splits == 1 || a.dp_units > 0;
     if (whole && a.beta == 0.f && p.c_vec)
-      p.c_tma = (encode_out(&tcm, a.C, a.N, a.M, 1, a.ldc, a.M * a.ldc) == cudaSuccess) ? 1 : 0;
+      p.c_tma = (encode_out_c(a.tma_cache, &tcm, a.C, a.N, a.M, 1, a.ldc, a.M * a.ldc) == cudaSuccess) ? 1 : 0;
   }
   if (a.mode == 2 && (a.tile_n == 192 || a.tile_n == 224))
     return tc_launch_bf16_mid(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid,
@@ -157,11 +204,11 @@ cudaError_t launch_skinny(const TcArgs& a, cudaStream_t stream) {
   const int bk = tc_tile_k(a.mode);
   const int ch = (a.mode == 2) ? 64 : 32;
   CUtensorMap ta, tb;
-  e = a.a_mn_major ? encode_2d(&ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
-                   : encode_2d(&ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
+  e = a.a_mn_major ? encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
+                   : encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
   if (e != cudaSuccess) return e;
   if (a.b_mn_major) return cudaErrorInvalidValue;
-  e = encode_2d(&tb, a.mode, a.B, a.K, a.N, a.ldb, bk, 16);
+  e = encode_2d_c(a.tma_cache, &tb, a.mode, a.B, a.K, a.N, a.ldb, bk, 16);
   if (e != cudaSuccess) return e;
   SkParams p;
   p.M = static_cast<int>(a.M);

@@ -12,7 +12,10 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
                           const TcParams& p, int grid, cudaStream_t s) {
   using Cfg = TcCfg<MODE, BN, MMA2>;
   auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN, TRANS_C, PAIR, MMA2>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = once_per_device(attr_done, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+  });
   if (e != cudaSuccess) return e;
   if constexpr (PAIR) {
     // Two-CTA clusters along x: CTAs 2c and 2c+1 form pair c.
