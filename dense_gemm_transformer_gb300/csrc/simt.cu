@@ -65,6 +65,23 @@ __device__ __forceinline__ void cp_async16(float* dst, const float* src, bool ok
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
+// Packed pairs of fp32: fma.rn.f32x2 performs two independent
+// round-to-nearest FMAs (the same results as two scalar fmaf) in one
+// instruction, halving the issue slots the outer product needs.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ void ffma2(uint64_t& d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
@@ -254,11 +271,22 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
     const int64_t n0 = (sh.sg.tile % tiles_n) * TBN;
     const int n = sh.sg.ke - sh.sg.ks;
 
+    // Accumulators in pairs of adjacent columns (acc2[i][j] holds columns
+    // 2j and 2j + 1 of row i), multiplied with packed FMAs; each element
+    // still sums its products in ascending k with one fp32 FMA per product.
+    // The 128-column kernels whose tile copies hold the most registers (4-byte
+    // copies of an unaligned operand, or a K-contiguous A beside an
+    // N-contiguous B) keep scalar accumulators: the packed form would spill.
+    constexpr bool PACKED = TBN == 256 || (VEC && (TA || TB));
+    uint64_t acc2[8][TN / 2];
     float acc[8][TN];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+      for (int j = 0; j < TN / 2; ++j) acc2[i][j] = 0ull;  // +0.0f, +0.0f
 #pragma unroll
       for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+    }
 
     // op(A) is K-contiguous when A is stored M x K (TA == 0); op(B) is
     // K-contiguous when B is stored N x K (TB == 1).
@@ -292,7 +320,8 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
       const float* a_s = As + (t % S) * Cfg::A_STAGE;
       const float* b_s = Bs + (t % S) * Cfg::B_STAGE;
       if constexpr (Cfg::PREFETCH_FRAGMENTS) {
-        float af[2][8], bf[2][TN];
+        float af[2][8];
+        uint64_t bf[2][TN / 2];  // B fragment as column pairs, loaded as such
         auto load = [&](int k, int buf) {
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
@@ -304,11 +333,9 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
           }
 #pragma unroll
           for (int q = 0; q < QN; ++q) {
-            const float4 v = *reinterpret_cast<const float4*>(b_s + k * LDB + bn + 32 * q);
-            bf[buf][4 * q + 0] = v.x;
-            bf[buf][4 * q + 1] = v.y;
-            bf[buf][4 * q + 2] = v.z;
-            bf[buf][4 * q + 3] = v.w;
+            const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(b_s + k * LDB + bn + 32 * q);
+            bf[buf][2 * q + 0] = v.x;
+            bf[buf][2 * q + 1] = v.y;
           }
         };
         load(0, 0);
@@ -316,14 +343,16 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
         for (int k = 0; k < BK; ++k) {
           if (k + 1 < BK) load(k + 1, (k + 1) & 1);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
+          for (int i = 0; i < 8; ++i) {
+            const uint64_t a2 = pack2(af[k & 1][i], af[k & 1][i]);
 #pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(af[k & 1][i], bf[k & 1][j], acc[i][j]);
+            for (int j = 0; j < TN / 2; ++j) ffma2(acc2[i][j], a2, bf[k & 1][j]);
+          }
         }
       } else {
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
-          float a[8], b[TN];
+          float a[8];
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const float4 v = *reinterpret_cast<const float4*>(a_s + k * LDA + am + 16 * r);
@@ -332,20 +361,43 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
             a[4 * r + 2] = v.z;
             a[4 * r + 3] = v.w;
           }
+          if constexpr (PACKED) {
+            uint64_t b2[TN / 2];  // B fragment as column pairs, loaded as such
 #pragma unroll
-          for (int q = 0; q < QN; ++q) {
-            const float4 v = *reinterpret_cast<const float4*>(b_s + k * LDB + bn + 32 * q);
-            b[4 * q + 0] = v.x;
-            b[4 * q + 1] = v.y;
-            b[4 * q + 2] = v.z;
-            b[4 * q + 3] = v.w;
+            for (int q = 0; q < QN; ++q) {
+              const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(b_s + k * LDB + bn + 32 * q);
+              b2[2 * q + 0] = v.x;
+              b2[2 * q + 1] = v.y;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint64_t a2 = pack2(a[i], a[i]);
+#pragma unroll
+              for (int j = 0; j < TN / 2; ++j) ffma2(acc2[i][j], a2, b2[j]);
+            }
+          } else {
+            float b[TN];
+#pragma unroll
+            for (int q = 0; q < QN; ++q) {
+              const float4 v = *reinterpret_cast<const float4*>(b_s + k * LDB + bn + 32 * q);
+              b[4 * q + 0] = v.x;
+              b[4 * q + 1] = v.y;
+              b[4 * q + 2] = v.z;
+              b[4 * q + 3] = v.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+              for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
           }
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
       }
+    }
+    if constexpr (PACKED) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j) unpack2(acc2[i][j], acc[i][2 * j], acc[i][2 * j + 1]);
     }
     cp_async_wait<0>();
     __syncthreads();  // the ring is idle before the next segment refills it
