@@ -578,7 +578,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-macs", type=float, default=3e9, help="oracle multiply-adds in the CPU baseline")
+    ap.add_argument("--cpu-macs", type=float, default=4.5e10,
+                    help="oracle multiply-adds in the CPU baseline (about 10 s on 16 host cores)")
     ap.add_argument("--ref-macs", type=float, default=3e8, help="oracle multiply-adds per reference step")
     ap.add_argument("--tile-n", type=int, default=0, help="sweeps: force the tensor-core tile width (128/256)")
     ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
