@@ -143,6 +143,16 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   const bool tr_a = !transA && K > 0 && (pre == 2 || (pre == 0 && N >= 256 && M >= 128 && K >= 64));
   const bool tr_b = transB && K > 0 && (pre == 2 || (pre == 0 && M >= 256 && N >= 128 && K >= 64));
   const int64_t lda_t = round_up(M, 4), ldb_t = round_up(N, 4);
+  // An operand whose base or rows are not 16-byte aligned would make the
+  // kernel copy both operands 4 bytes at a time (and keep scalar FMAs); a copy
+  // with an aligned leading dimension costs one read and write of it and is
+  // made instead (not with pretranspose = 1, which keeps operands in place).
+  auto misaligned = [](const float* q, int64_t ld) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0 || ld % 4 != 0; };
+  const bool pk_a = !tr_a && K > 0 && pre != 1 && misaligned(A, lda);
+  const bool pk_b = !tr_b && K > 0 && pre != 1 && misaligned(B, ldb);
+  const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;  // A as stored
+  const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;  // B as stored
+  const int64_t lda_p = round_up(a_cols, 4), ldb_p = round_up(b_cols, 4);
   SimtArgs a{};
   a.transA = transA;
   a.transB = transB;
@@ -195,9 +205,11 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   if (a.schedule == kSimtStreamK)
     part_bytes = static_cast<size_t>(2 * a.grid * simt_streamk_slot_floats(tile_n)) * sizeof(float);
   const size_t a_off = round_up(static_cast<int64_t>(part_bytes), 256);
-  const size_t a_bytes = tr_a ? static_cast<size_t>(K * lda_t) * sizeof(float) : 0;
+  const size_t a_bytes = tr_a ? static_cast<size_t>(K * lda_t) * sizeof(float)
+                              : pk_a ? static_cast<size_t>(a_rows * lda_p) * sizeof(float) : 0;
   const size_t b_off = a_off + round_up(static_cast<int64_t>(a_bytes), 256);
-  const size_t b_bytes = tr_b ? static_cast<size_t>(K * ldb_t) * sizeof(float) : 0;
+  const size_t b_bytes = tr_b ? static_cast<size_t>(K * ldb_t) * sizeof(float)
+                              : pk_b ? static_cast<size_t>(b_rows * ldb_p) * sizeof(float) : 0;
   const size_t total = b_off + b_bytes;
   if (total > 0) {
     gemm_status_t st = ensure_ws(h, total);
@@ -223,6 +235,20 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
     a.transB = 0;
     ++kernels;
   }
+  if (pk_a) {
+    float* ap = reinterpret_cast<float*>(ws + a_off);
+    if (launch_pack(A, lda, ap, lda_p, a_rows, a_cols, 4, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    a.A = ap;
+    a.lda = lda_p;
+    ++kernels;
+  }
+  if (pk_b) {
+    float* bp = reinterpret_cast<float*>(ws + b_off);
+    if (launch_pack(B, ldb, bp, ldb_p, b_rows, b_cols, 4, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    a.B = bp;
+    a.ldb = ldb_p;
+    ++kernels;
+  }
   if (launch_simt(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
   if (a.schedule == kSimtSplitK) {
     if (launch_splitk_reduce(M, N, a.splits, a.ws, a.ws_ld, C, ldc, alpha, beta, s) != cudaSuccess)
@@ -230,7 +256,7 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
     ++kernels;
   }
   set_plan(h, GEMM_FAMILY_SIMT, kSimtTileM, tile_n, kSimtTileK, a.splits, tile_n == 256 ? 4 : 3, grid, kernels,
-           (tr_a ? 1 : 0) | (tr_b ? 2 : 0));
+           ((tr_a || pk_a) ? 1 : 0) | ((tr_b || pk_b) ? 2 : 0));
   h->plan.schedule = a.schedule;
   return GEMM_OK;
 }

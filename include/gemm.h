@@ -77,8 +77,9 @@ typedef enum {
   GEMM_OPT_SPLIT_K = 2,  /* value: 0 = planner's choice, n >= 1 = force n slices of K      */
   GEMM_OPT_TILE_N = 3,   /* value: 0 = planner's choice; TC: 128, 192, 224 or 256 (224 and,
                             for pairs, 192 need a K-major B in BF16); SIMT: 128 or 256    */
-  GEMM_OPT_PRETRANSPOSE = 4, /* SIMT: 0 = planner's choice, 1 = never, 2 = always transpose
-                                K-contiguous operands into the workspace first             */
+  GEMM_OPT_PRETRANSPOSE = 4, /* SIMT: 0 = planner's choice (K-contiguous operands transposed,
+                                misaligned ones re-packed into the workspace first), 1 = never
+                                (operands read in place), 2 = always transpose              */
   GEMM_OPT_PAIR = 5          /* TC: two-CTA clusters (tiles of 192 or more columns, two or more
                                 rows of tiles).  0 = planner's choice (256 columns: one 256-row
                                 MMA per pair, tcgen05 cta_group::2; 192/224: pairs sharing B by

@@ -202,7 +202,11 @@ def test_fp32_pretranspose(h, pre, tA, tB, M, N, K):
     h.set_option("pretranspose", pre)
     rows = _cases.sample_rows(M) if M * N * K > 2e9 else None
     _cases.run_and_check(h, "fp32", M, N, K, tA, tB, alpha=1.25, beta=-0.5, seed=71, dist="normal", rows=rows)
-    want = 0 if pre == 1 else ((0 if tA else 1) | (2 if tB else 0))
+    # pre = 2 transposes the K-contiguous operands; an M/N-contiguous one
+    # whose rows are not 16-byte aligned is re-packed (neither with pre = 1)
+    a_copy = (not tA) or M % 4 != 0
+    b_copy = tB or N % 4 != 0
+    want = 0 if pre == 1 else ((1 if a_copy else 0) | (2 if b_copy else 0))
     assert h.plan()["packed"] == want
     _cases.run_and_check(h, "fp32", M, N, min(K, 1024), tA, tB, seed=72, dist="int", exact=True)
 
@@ -220,6 +224,26 @@ def test_unaligned_leading_dimension(h, mode, tA, tB):
     # N = K = 65: a row of 65 elements breaks the 16-byte rule of the TMA unit,
     # so TF32/BF16 operands go through the re-pack into the workspace.
     _cases.run_and_check(h, mode, 190, 65, 65, tA, tB, seed=31, dist="normal")
+
+
+@pytest.mark.parametrize("pre", [0, 1])
+@pytest.mark.parametrize("tA,tB", TRANS)
+@pytest.mark.parametrize("M,N,K", [(700, 65, 384), (700, 384, 65), (65, 300, 1000)])
+def test_fp32_misaligned_operands(h, pre, tA, tB, M, N, K):
+    """FP32 operands whose rows are not 16-byte aligned (a dimension of 65):
+    the planner re-packs them into an aligned workspace copy (or transposes
+    a K-contiguous one); with pretranspose = 1 the kernel reads them in place
+    with 4-byte copies and scalar FMAs."""
+    h.set_option("pretranspose", pre)
+    _cases.run_and_check(h, "fp32", M, N, K, tA, tB, seed=39, dist="normal")
+    lda = M if tA else K
+    ldb = K if tB else N
+    plan = h.plan()
+    if pre == 1:
+        assert plan["packed"] == 0
+    elif lda % 4 or ldb % 4:
+        assert plan["packed"] != 0
+    _cases.run_and_check(h, "fp32", M, N, K, tA, tB, seed=40, dist="int", exact=True)
 
 
 @pytest.mark.parametrize("mode", MODES)
