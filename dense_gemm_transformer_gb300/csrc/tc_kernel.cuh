@@ -21,11 +21,15 @@
 //               so the next tile's MMAs can start.  Two accumulators let the
 //               epilogue of tile i overlap the mainloop of tile i+1.
 //
-// Work units are (tile, K slice) pairs handed out round-robin to a persistent
-// grid of one CTA per SM, in a grouped raster order (group_m tiles of M walk
-// all tiles of N) so that CTAs running at the same time share A and B tiles
-// in L2.  With more than one K slice, each unit writes raw partial sums to the
-// workspace and a separate kernel reduces the slices in a fixed order.
+// Work units are tiles, or (tile, K slice) pairs, handed out round-robin to
+// a persistent grid of one CTA per SM (or one CTA pair per two SMs, see PAIR
+// and MMA2 below), in a grouped raster order (group_m tiles of M walk all
+// tiles of N) so that CTAs running at the same time share A and B tiles in
+// L2.  Whole tiles come first; the last rows of tiles may be cut into K
+// slices to fill the final wave (or every tile, for plain split-K), and each
+// such unit writes raw partial sums to the workspace, which a separate kernel
+// reduces in a fixed slice order.  The kernel waits for the previous kernel
+// in the stream (programmatic dependent launch) only after its set-up.
 //
 // Every mbarrier wait is bounded (ptx.cuh); on a timeout the CTA records the
 // cause in the device status word, waits (bounded) for its own copies and
