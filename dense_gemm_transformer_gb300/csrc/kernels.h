@@ -132,7 +132,7 @@ struct TcArgs {
 constexpr int kTcEpiWarps = 8;                        // epilogue warps (two per TMEM lane quarter)
 constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);  // producer + MMA warps + epilogue warps
 int tc_tile_k(int mode);              // k elements per stage (128 bytes)
-int tc_stages(int mode, int tile_n);  // pipeline depth
+int tc_stages(int mode, int tile_n, bool mma2);  // pipeline depth (mma2: one 256-row MMA per CTA pair)
 // Whether the kernel is built for this tile width, pairing and B layout
 // (tile_n 128, 192, 224 or 256; pairs from 192 columns).
 bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major);

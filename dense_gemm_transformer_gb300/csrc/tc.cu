@@ -112,8 +112,9 @@ cudaError_t tc_init_driver() {
 
 int tc_tile_k(int mode) { return mode == 2 ? 64 : 32; }
 
-int tc_stages(int mode, int tile_n) {
+int tc_stages(int mode, int tile_n, bool mma2) {
   (void)mode;  // a stage holds 128 bytes of K per row in both modes
+  if (tile_n == 256 && mma2) return TcCfg<2, 256, true>::STAGES;
   if (tile_n == 256) return TcCfg<2, 256>::STAGES;
   if (tile_n == 224) return TcCfg<2, 224>::STAGES;
   if (tile_n == 192) return TcCfg<2, 192>::STAGES;
