@@ -165,6 +165,15 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t cluster_addr) {
   return v;
 }
 
+// Asynchronous 16-byte store into the shared memory of a CTA of the cluster
+// (`dst` a shared::cluster address), counted as transaction bytes on the
+// barrier `mbar` of that same CTA.
+__device__ __forceinline__ void st_async_f32x4(uint32_t dst, float4 v, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(mbar)
+               : "memory");
+}
+
 // Pull one box of a tensor into L2 only (no shared memory, no completion).
 // L2 is where global memory is kept coherent, so warming it can never expose
 // a stale value to a later read.

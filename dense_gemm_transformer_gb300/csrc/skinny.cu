@@ -8,18 +8,22 @@
 //   * the weights are the 128-row side of a tcgen05 MMA (128 x 16 x K per
 //     tile) and stream through a TMA ring; the activations are the
 //     16-column operand (rows past M are zero fill);
-//   * one (tile, K slice) per CTA, small enough (6 stages, ~109 KB of
-//     shared memory, 192 threads, 32 TMEM columns) for two CTAs per SM:
+//   * one (tile, K slice) per CTA, small enough (5 stages and an 8 KB
+//     receive buffer, ~100 KB of shared memory, 192 threads, 32 TMEM
+//     columns) for two CTAs per SM:
 //     clusters of up to 16 CTAs then fit twice into a GPC, and the next
 //     call's CTAs can start while this one finishes (one CTA per SM with
 //     twice the stages measured slower: its 12-CTA clusters fit only once
 //     per GPC, so a third of them waited for a second wave);
 //   * K is split across the CTAs of a thread-block cluster, and the slices
-//     are summed through distributed shared memory: each CTA leaves its
-//     128 x 16 partial tile in its own shared memory, and after a cluster
-//     barrier CTA r reduces the r-th share of the tile's elements over all
-//     slices in ascending order and writes C.  No workspace, no atomics and
-//     no second kernel;
+//     are summed through distributed shared memory: CTA r owns the r-th
+//     share of the tile's elements; each CTA pushes the other owners' shares
+//     of its 128 x 16 partial tile into their receive buffers with st.async
+//     (counted on the owner's barrier), and each owner, once its barrier has
+//     all the bytes, adds its share over all slices in ascending order and
+//     writes C.  No workspace, no atomics, no second kernel, and no barrier
+//     across the cluster after the MMAs (pulling the shares instead needed
+//     two, and measured 6-8% slower);
 //   * programmatic dependent launch: set-up (barriers, TMEM, descriptor
 //     prefetch) and an L2 warm-up of this CTA's weight slice run before
 //     griddepcontrol.wait, i.e. while the previous kernel in the stream is
@@ -27,8 +31,8 @@
 //     global memory is kept coherent, so no stale value can be read.
 //
 // Every mbarrier wait is bounded; on a timeout the CTA records the cause in
-// the status word, drains its own copies and MMAs, and still reaches both
-// cluster barriers, so the other CTAs of its cluster finish too.
+// the status word, drains its own copies and MMAs, and an owner whose shares
+// never arrive gives up its receive wait the same way.
 #include "skinny.cuh"
 
 #include "kernels.h"
@@ -50,8 +54,9 @@ struct SkCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = kSkinnyStages;
   static constexpr int TMEM_COLS = 32;                // one 16-column accumulator (allocation >= 32)
-  static constexpr int NUM_BARS = 2 * STAGES + 2;     // full/empty per stage, accumulator full, drain
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int NUM_BARS = 2 * STAGES + 3;     // full/empty per stage, accumulator full, drain, receive
+  static constexpr int RECV_BYTES = (BN * BM / 4 + kSkinnyMaxCluster) * 16;  // shares pushed by the peers
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + RECV_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr int PREFETCH_KB = 16;              // K blocks of weights warmed in L2 before the wait
   static constexpr uint32_t FORMAT = (MODE == 2) ? 1u : 2u;
   static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM (228 KB, 1 KB reserved per CTA)");
@@ -78,7 +83,8 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
+  float* recv = reinterpret_cast<float*>(smem + S * Cfg::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES + Cfg::RECV_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -88,6 +94,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
   const uint32_t accf_bar = bar0 + 8u * (2 * S);
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 1);
+  const uint32_t recv_bar = bar0 + 8u * (2 * S + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cs = p.cluster;
@@ -104,6 +111,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
     }
     mbar_init(accf_bar, 1);
     mbar_init(drain_bar, 1);
+    mbar_init(recv_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -128,6 +136,8 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
   }
   tc_fence_before();
   __syncthreads();
+  // Every CTA's receive barrier exists before any peer can push to it.
+  if (cs > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // From here on global memory written by earlier kernels is read or written.
@@ -239,52 +249,58 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
       float* red = reinterpret_cast<float*>(smem);
 #pragma unroll
       for (int j = 0; j < Cfg::BN; ++j) red[j * Cfg::BM + rt] = v[j];
-    }
-  }
-
-  if (cs > 1) {
-    // All partial tiles of the cluster are in shared memory after this barrier.
-    cluster_sync();
-    // CTA `rank` owns the rank-th share of the tile's groups of four rows
-    // (one 16-byte load from each slice per group); each element's slices
-    // are added in ascending order.
-    constexpr int G = Cfg::BM / 4;  // groups per column
-    const int total = p.N * G;
-    const int per = (total + cs - 1) / cs;
-    const int g0 = rank * per;
-    const int g1 = (g0 + per < total) ? g0 + per : total;
-    uint32_t peer[kSkinnyMaxCluster];
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+      // Groups of four rows of one column; CTA q owns groups [q per, (q+1) per).
+      // Push every other owner's groups into its receive buffer (slot of this
+      // rank), counted on its receive barrier.
+      constexpr int G = Cfg::BM / 4;
+      const int total = p.N * G;
+      const int per = (total + cs - 1) / cs;
+      const int et = static_cast<int>(threadIdx.x) - 64;
+      const uint32_t recv0 = smem_u32(recv);
+      for (int g = et; g < total; g += 128) {
+        const int q = g / per;
+        if (q == rank) continue;
+        const float4 val = *reinterpret_cast<const float4*>(red + 4 * g);
+        const uint32_t dst = dsmem_map(recv0 + 16u * static_cast<uint32_t>(rank * per + (g - q * per)),
+                                       static_cast<uint32_t>(q));
+        st_async_f32x4(dst, val, dsmem_map(recv_bar, static_cast<uint32_t>(q)));
+      }
+      const int g0 = rank * per;
+      const int g1 = (g0 + per < total) ? g0 + per : total;
+      const int mine = (g1 > g0) ? g1 - g0 : 0;
+      if (et == 0) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((cs - 1) * mine * 16));
+      const bool all_in = mbar_wait_cluster(recv_bar, 0, abort_flag, p.status, kDevTimeoutFull);
+      if (all_in) {
+        for (int g = g0 + et; g < g1; g += 128) {
+          float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q = 0; q < cs; ++q) {
+            const float4 x = (q == rank) ? *reinterpret_cast<const float4*>(red + 4 * g)
+                                         : *reinterpret_cast<const float4*>(recv + 4 * (q * per + (g - g0)));
+            if (q == 0) {
+              s4 = x;
+            } else {
+              s4.x += x.x;
+              s4.y += x.y;
+              s4.z += x.z;
+              s4.w += x.w;
+            }
+          }
+          const float sum[4] = {s4.x, s4.y, s4.z, s4.w};
+          const int col = g / G;
+          const int64_t row = static_cast<int64_t>(row0) + 4 * (g % G);
+          float* dst = p.C + static_cast<int64_t>(col) * p.ldc + row;
 #pragma unroll
-    for (int q = 0; q < kSkinnyMaxCluster; ++q) peer[q] = (q < cs) ? dsmem_map(smem0, static_cast<uint32_t>(q)) : 0u;
-    for (int g = g0 + static_cast<int>(threadIdx.x); g < g1; g += kSkinnyThreads) {
-      float4 x[kSkinnyMaxCluster];
-#pragma unroll
-      for (int q = 0; q < kSkinnyMaxCluster; ++q)
-        if (q < cs) x[q] = ld_dsmem_f32x4(peer[q] + 16u * static_cast<uint32_t>(g));
-      float sum[4] = {x[0].x, x[0].y, x[0].z, x[0].w};
-#pragma unroll
-      for (int q = 1; q < kSkinnyMaxCluster; ++q) {
-        if (q < cs) {
-          sum[0] += x[q].x;
-          sum[1] += x[q].y;
-          sum[2] += x[q].z;
-          sum[3] += x[q].w;
+          for (int i = 0; i < 4; ++i) {
+            if (row + i < p.M) {
+              float out = p.alpha * sum[i];
+              if (p.beta != 0.f) out = fmaf(p.beta, dst[i], out);
+              dst[i] = out;
+            }
+          }
         }
       }
-      const int col = g / G;
-      const int64_t row = static_cast<int64_t>(row0) + 4 * (g % G);
-      float* dst = p.C + static_cast<int64_t>(col) * p.ldc + row;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (row + i < p.M) {
-          float out = p.alpha * sum[i];
-          if (p.beta != 0.f) out = fmaf(p.beta, dst[i], out);
-          dst[i] = out;
-        }
-      }
     }
-    // No CTA leaves (releasing its shared memory) while a peer still reads it.
-    cluster_sync();
   }
 
   tc_fence_before();

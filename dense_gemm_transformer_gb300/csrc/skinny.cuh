@@ -27,7 +27,7 @@ struct SkParams {
 constexpr int kSkinnyThreads = 192;  // TMA producer warp, MMA warp, four epilogue warps
 constexpr int kSkinnyMaxCluster = 16;
 
-constexpr int kSkinnyStages = 6;  // ~109 KB of shared memory: two CTAs per SM
+constexpr int kSkinnyStages = 5;  // with the 8 KB receive buffer ~100 KB of shared memory: two CTAs per SM
 
 // Launch on `grid` = tiles * p.cluster CTAs, clusters of p.cluster CTAs
 // along x, with programmatic dependent launch.  a_mn: the weights are stored
