@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -477,15 +478,52 @@ def sweep_cases(workload):
     return out
 
 
+SAMPLES = 5          # timed samples per shape (median and spread)
+SAMPLE_MS = 20.0     # each sample covers at least this much device time
+MAX_REPS = 4000      # launches per sample at most
+QUEUE_CALLS = 600    # launches held behind one spin kernel at a time
+
+
+def _timed_back_to_back(fn, reps, stream, chunk):
+    """Device time per call of fn(0..reps-1), enqueued in chunks that each sit
+    behind a spin kernel while the host enqueues them, so the timed calls run
+    back to back with no host gaps; the chunk's events bracket only the calls."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    total, done = 0.0, 0
+    while done < reps:
+        n = min(chunk, reps - done)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(max(4e6, n * 1e5)))  # ~50 us of spin per queued call
+            e0.record(stream)
+            for r in range(done, done + n):
+                fn(r)
+            e1.record(stream)
+        stream.synchronize()
+        total += e0.elapsed_time(e1)
+        done += n
+    return total / reps
+
+
+def _stats(xs):
+    xs = sorted(xs)
+    return {"median": xs[len(xs) // 2], "min": xs[0], "max": xs[-1]}
+
+
 def bench_sweep(args):
     """Per-shape TFLOP/s and roofline fractions for the other configurations.
 
-    Each shape: warm-up, then R back-to-back launches between two CUDA events
-    on the launching stream, with the operands rotated over enough copies that
-    the working set of one rotation exceeds 3x the L2 (so every launch reads
-    its weights from HBM).  The reported time is for calls that run back to
-    back on the device (a spin kernel holds the stream while the host enqueues
-    them); "ms_stream" is the same calls as the host issues them.
+    Each shape, after warm-up, with the operands rotated over enough copies
+    that one rotation's working set exceeds 3x the L2 (every launch reads its
+    weights from HBM), and R launches per sample, R chosen so that a sample
+    covers >= 20 ms:
+      * "ms": calls back to back on the device (held behind a spin kernel
+        while the host enqueues them), median of 5 samples, with the spread;
+      * "ms_graph": the same R calls captured once in a CUDA graph, median of
+        5 replays (small-M shapes are gated on this one);
+      * "ms_stream": the calls as the host issues them (includes the host's
+        per-call cost whenever it exceeds the kernel time);
+      * "null_ms": gemm_launch_null -- an empty kernel with the launch
+        configuration of the call's main kernel -- timed like "ms".
     """
     import dense_gemm_transformer_gb300 as dg
     dev = torch.device("cuda", 0)
@@ -519,55 +557,130 @@ def bench_sweep(args):
             B = B0 if i == 0 else B0.clone()
             C = torch.randn((c.M, c.N), generator=g).to(dev)
             sets.append((A, B, C))
-        reps = max(3 * copies, 10)
+
+        def call(r):
+            A, B, C = sets[r % copies]
+            h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta, stream=stream)
+
         with torch.cuda.stream(stream):
-            for A, B, C in sets:
-                h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta, stream=stream)
+            for r in range(copies):
+                call(r)
         stream.synchronize()
         plan = h.plan()
+        chunk = max(copies, QUEUE_CALLS // max(plan["kernels"], 1))
+        # R: enough launches that one sample covers SAMPLE_MS of device time.
+        t_est = _timed_back_to_back(call, max(2 * copies, 10), stream, chunk)
+        reps = int(min(MAX_REPS, max(10, math.ceil(SAMPLE_MS / max(t_est, 1e-4)))))
+        reps = max(reps, copies)
+        dev_ms = [_timed_back_to_back(call, reps, stream, chunk) for _ in range(SAMPLES)]
+        # As the host issues them.
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        # Launches as the host issues them (includes the host's per-call cost
-        # whenever it exceeds the kernel time) ...
         with torch.cuda.stream(stream):
             e0.record(stream)
             for r in range(reps):
-                A, B, C = sets[r % copies]
-                h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta, stream=stream)
+                call(r)
             e1.record(stream)
         stream.synchronize()
-        ms = e0.elapsed_time(e1) / reps
-        # ... and back to back on the device: a spin kernel holds the stream
-        # while the host enqueues all the calls, so the timed calls run with
-        # no host gaps between them.
-        with torch.cuda.stream(stream):
-            torch.cuda._sleep(int(max(4e6, reps * 1e5)))  # ~50 us of spin per queued call
-            e0.record(stream)
-            for r in range(reps):
-                A, B, C = sets[r % copies]
-                h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta, stream=stream)
-            e1.record(stream)
-        stream.synchronize()
-        dev_ms = e0.elapsed_time(e1) / reps
+        stream_ms = e0.elapsed_time(e1) / reps
+        # One CUDA graph of the R calls, replayed.
+        graph_ms, graph_err = None, None
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for r in range(reps):
+                    call(r)
+            graph.replay()
+            stream.synchronize()
+            gm = []
+            for _ in range(SAMPLES):
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    graph.replay()
+                    e1.record(stream)
+                stream.synchronize()
+                gm.append(e0.elapsed_time(e1) / reps)
+            graph_ms = _stats(gm)
+            del graph
+        except Exception as exc:  # reported, not fatal: the stream timings stand
+            graph_err = f"{type(exc).__name__}: {exc}"[:200]
+            stream.synchronize()
         assert h.check_device(stream) == 0
-        t = dev_ms
+        # The identity null of this configuration.
+        call(0)
+        null_ms = _stats([_timed_back_to_back(lambda r: h.launch_null(stream), reps, stream, QUEUE_CALLS)
+                          for _ in range(SAMPLES)])
+        stream.synchronize()
         byts = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N * (2 if beta != 0 else 1)
         peak = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops"], "bf16": pk["bf16_tflops"]}[mode]
         t_c, t_m = c.flops / (peak * 1e12), byts / (pk["hbm_gbs"] * 1e9)
+        st = _stats(dev_ms)
+        gate_graph = plan["family"] == "skinny" or (c.M <= 16 and graph_ms is not None)
+        t = graph_ms["median"] if (gate_graph and graph_ms is not None) else st["median"]
         shapes.append({"gemm": label, "M": c.M, "N": c.N, "K": c.K, "ms": round(t, 5),
-                       "ms_stream": round(ms, 5), "tflops": round(c.flops / (t * 1e-3) / 1e12, 2),
+                       "timing": "graph" if (gate_graph and graph_ms is not None) else "back_to_back",
+                       "ms_back_to_back": {k: round(v, 5) for k, v in st.items()},
+                       "ms_graph": None if graph_ms is None else {k: round(v, 5) for k, v in graph_ms.items()},
+                       "graph_error": graph_err,
+                       "ms_stream": round(stream_ms, 5),
+                       "null_ms": {k: round(v, 5) for k, v in null_ms.items()},
+                       "samples": SAMPLES, "reps": reps,
+                       "tflops": round(c.flops / (t * 1e-3) / 1e12, 2),
                        "gbs": round(byts / (t * 1e-3) / 1e9, 1), "bound": "hbm" if t_m > t_c else
                        ("alu" if mode == "fp32" else "tensor"), "roofline_frac": round(max(t_c, t_m) / (t * 1e-3), 3),
                        "plan": plan, "copies": copies})
         del sets, A0, B0
         torch.cuda.empty_cache()
+    h.close()
+    return shapes
+
+
+def sweep_line(args, shapes, processes):
+    pk = peaks()
     total_flops = sum(2 * x["M"] * x["N"] * x["K"] for x in shapes)
     total_s = sum(x["ms"] for x in shapes) * 1e-3
-    line = {"metric": METRIC, "value": total_flops / total_s / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+    return {"metric": METRIC, "value": total_flops / total_s / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
             "higher_is_better": True, "dtype": "see shapes", "data": "synthetic",
-            "config": {"workload": args.workload, "l2": "operands rotated over copies > 3x L2"},
-            "shapes": shapes, "peaks": pk}
-    print(json.dumps(line), flush=True)
-    h.close()
+            "config": {"workload": args.workload, "l2": "operands rotated over copies > 3x L2",
+                       "samples": f"median of {SAMPLES} samples of >= {SAMPLE_MS:g} ms per process, "
+                                  f"median over {processes} process(es)"},
+            "processes": processes, "shapes": shapes, "peaks": pk}
+
+
+def bench_sweep_processes(args):
+    """The sweep in `args.processes` separate processes; per shape, the median
+    over the processes of their medians, with the spread across processes."""
+    if args.processes <= 1:
+        print(json.dumps(sweep_line(args, bench_sweep(args), 1)), flush=True)
+        return
+    runs = []
+    for _ in range(args.processes):
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", args.workload, "--processes", "1"]
+        if args.only:
+            cmd += ["--only", args.only]
+        if args.tile_n:
+            cmd += ["--tile-n", str(args.tile_n)]
+        if args.pair is not None:
+            cmd += ["--pair", str(args.pair)]
+        out = subprocess.run(cmd, capture_output=True, text=True, check=True).stdout
+        runs.append(json.loads(out.strip().splitlines()[-1])["shapes"])
+    print(json.dumps(sweep_line(args, merge_process_runs(runs), args.processes)), flush=True)
+
+
+def merge_process_runs(runs):
+    """Per shape (the same order in every run): the record of the process
+    whose time is the median across processes, with every process's time in
+    "ms_processes" (the spread)."""
+    shapes = []
+    for per in zip(*runs):
+        labels = {x["gemm"] for x in per}
+        if len(labels) != 1:
+            raise ValueError(f"processes timed different shapes: {sorted(labels)}")
+        ms = sorted(x["ms"] for x in per)
+        med = ms[len(ms) // 2]
+        rec = dict(next(x for x in per if x["ms"] == med))
+        rec["ms_processes"] = ms
+        shapes.append(rec)
+    return shapes
 
 
 def main():
@@ -587,6 +700,8 @@ def main():
                     help="sweeps: force the CTA-pair form (0 planner, 1 none, 2 multicast B, 3 one 256-row MMA per pair)")
     ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny"],
                     help="gpt: the timed step; the others print a per-shape sweep")
+    ap.add_argument("--processes", type=int, default=3,
+                    help="sweeps: separate processes to run the sweep in (median and spread across them)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -594,7 +709,7 @@ def main():
     if args.impl == "reference":
         bench_reference(args, world, rank)
     elif args.workload != "gpt":
-        bench_sweep(args)
+        bench_sweep_processes(args)
     else:
         bench_ours(args, world, rank, local)
     if world > 1:

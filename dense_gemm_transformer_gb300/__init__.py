@@ -71,10 +71,11 @@ def load(build_if_missing: bool = False):
         lib.gemm_set_option.argtypes = [vp, i32, i64]
         lib.gemm_get_plan.argtypes = [vp, ctypes.POINTER(Plan)]
         lib.gemm_check_device.argtypes = [vp, vp]
+        lib.gemm_launch_null.argtypes = [vp, vp]
         lib.gemm_status_string.argtypes = [i32]
         lib.gemm_status_string.restype = ctypes.c_char_p
         for name in ("gemm_create", "gemm_destroy", "gemm_run", "gemm_validate", "gemm_set_option",
-                     "gemm_get_plan", "gemm_check_device"):
+                     "gemm_get_plan", "gemm_check_device", "gemm_launch_null"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -154,6 +155,11 @@ class Gemm:
     def check_device(self, stream=None) -> int:
         """Synchronize the stream and return the device status (0 = ok)."""
         return self._lib.gemm_check_device(self._h, _stream_ptr(stream))
+
+    def launch_null(self, stream=None):
+        """gemm_launch_null: an empty kernel with the launch configuration of
+        the last call's main kernel, on `stream`."""
+        _check(self._lib.gemm_launch_null(self._h, _stream_ptr(stream)), "gemm_launch_null")
 
     def run_ptr(self, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
         """gemm_run on raw device pointers; `stream` is a torch stream, a raw handle or None."""

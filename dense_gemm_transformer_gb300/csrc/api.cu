@@ -43,6 +43,7 @@ struct gemm_handle_s {
   int sk_active[2][dgt::kSkinnyMaxCluster + 1];  // small-M kernel: resident clusters (-1: not queried)
   dgt::TmaCache* tma_cache = nullptr;             // TMA descriptors of earlier calls
   gemm_plan_t plan{};
+  dgt::LaunchShape null_shape;  // main kernel of the last successful gemm_run (for gemm_launch_null)
 };
 
 namespace {
@@ -570,6 +571,34 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   return GEMM_OK;
 }
 
+// gemm_run after its argument checks.
+gemm_status_t run_checked(gemm_handle_t h, int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
+                          float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
+                          int64_t ldc, cudaStream_t s) {
+  if (M == 0 || N == 0) {
+    set_plan(h, 0, 0, 0, 0, 0, 0, 0, 0, 0);
+    return GEMM_OK;
+  }
+  if (K == 0 || alpha == 0.f) {
+    if (dgt::launch_scale(M, N, C, ldc, beta, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    set_plan(h, 0, 0, 0, 0, 1, 0, 0, 1, 0);
+    return GEMM_OK;
+  }
+  const int fam = h->opt_family;
+  if (mode == GEMM_MODE_FP32) {
+    if (fam != GEMM_FAMILY_AUTO && fam != GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
+    return run_simt(h, transA, transB, M, N, K, alpha, static_cast<const float*>(A), lda,
+                    static_cast<const float*>(B), ldb, beta, C, ldc, s);
+  }
+  // Small M: the swapped form, which streams the weights through the 128-row
+  // MMA side once (activations must be stored M x K).
+  const bool skinny_ok = (transA == 0) && M <= 16;
+  if (fam == GEMM_FAMILY_SKINNY && !skinny_ok) return GEMM_ERR_NOT_SUPPORTED;
+  if (fam == GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
+  const bool swap = (fam == GEMM_FAMILY_SKINNY) || (fam == GEMM_FAMILY_AUTO && skinny_ok);
+  return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, swap);
+}
+
 }  // namespace
 
 extern "C" {
@@ -640,30 +669,18 @@ gemm_status_t gemm_run(gemm_handle_t h, int mode, int transA, int transB, int64_
   if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
   gemm_status_t st = check_args(mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc);
   if (st != GEMM_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (M == 0 || N == 0) {
-    set_plan(h, 0, 0, 0, 0, 0, 0, 0, 0, 0);
-    return GEMM_OK;
-  }
-  if (K == 0 || alpha == 0.f) {
-    if (dgt::launch_scale(M, N, C, ldc, beta, s) != cudaSuccess) return GEMM_ERR_CUDA;
-    set_plan(h, 0, 0, 0, 0, 1, 0, 0, 1, 0);
-    return GEMM_OK;
-  }
-  const int fam = h->opt_family;
-  if (mode == GEMM_MODE_FP32) {
-    if (fam != GEMM_FAMILY_AUTO && fam != GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
-    return run_simt(h, transA, transB, M, N, K, alpha, static_cast<const float*>(A), lda,
-                    static_cast<const float*>(B), ldb, beta, C, ldc, s);
-  }
-  // Small M: the swapped form, which streams the weights through the 128-row
-  // MMA side once (activations must be stored M x K).
-  const bool skinny_ok = (transA == 0) && M <= 16;
-  if (fam == GEMM_FAMILY_SKINNY && !skinny_ok) return GEMM_ERR_NOT_SUPPORTED;
-  if (fam == GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
-  const bool swap = (fam == GEMM_FAMILY_SKINNY) || (fam == GEMM_FAMILY_AUTO && skinny_ok);
-  return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, swap);
+  dgt::last_main_launch().valid = false;
+  st = run_checked(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                   static_cast<cudaStream_t>(stream));
+  if (st == GEMM_OK) h->null_shape = dgt::last_main_launch();
+  return st;
 }
+
+gemm_status_t gemm_launch_null(gemm_handle_t h, void* stream) {
+  if (h == nullptr || !h->null_shape.valid) return GEMM_ERR_INVALID_VALUE;
+  return cuda_status(dgt::launch_null(h->null_shape, static_cast<cudaStream_t>(stream)));
+}
+
 
 gemm_status_t gemm_set_option(gemm_handle_t h, int option, int64_t value) {
   if (h == nullptr) return GEMM_ERR_INVALID_VALUE;

@@ -3,7 +3,9 @@
 // K == 0 or alpha == 0, the operand re-pack that gives an operand with an
 // unaligned leading dimension a 16-byte-aligned copy the TMA unit can read,
 // and the transpose that turns an MN-major TF32 operand K-major.
-// All are grid-stride loops sized to at most eight CTAs per SM.
+// All are grid-stride loops sized to at most eight CTAs per SM.  Also here:
+// the empty kernel that reproduces a GEMM kernel's launch configuration
+// (the launch-cost floor a benchmark reports beside each shape).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -39,13 +41,25 @@ __global__ void splitk_reduce_kernel(int64_t M, int64_t N, int splits, const flo
        g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = g / groups, c = (g % groups) * 4;
     const float* src = ws + r * ws_ld + c;
+    // Slices are loaded kBatch at a time (independent loads in flight: with
+    // deep K there are dozens of slices and few output elements) and added in
+    // ascending order.
+    constexpr int kBatch = 8;
     float4 s = *reinterpret_cast<const float4*>(src);
-    for (int k = 1; k < splits; ++k) {
-      const float4 t = *reinterpret_cast<const float4*>(src + k * slice);
-      s.x += t.x;
-      s.y += t.y;
-      s.z += t.z;
-      s.w += t.w;
+    for (int k0 = 1; k0 < splits; k0 += kBatch) {
+      float4 t[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (k0 + u < splits) t[u] = *reinterpret_cast<const float4*>(src + (k0 + u) * slice);
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (k0 + u < splits) {
+          s.x += t[u].x;
+          s.y += t[u].y;
+          s.z += t[u].z;
+          s.w += t[u].w;
+        }
+      }
     }
     float v[4] = {alpha * s.x, alpha * s.y, alpha * s.z, alpha * s.w};
     float* dst = C + r * ldc + c;
@@ -172,7 +186,50 @@ __global__ void __launch_bounds__(256) transpose_f32x4_kernel(const float* __res
   }
 }
 
+__global__ void null_kernel() {
+  grid_dep_wait();
+  grid_dep_launch();
+}
+
 }  // namespace
+
+LaunchShape& last_main_launch() {
+  thread_local LaunchShape shape;
+  return shape;
+}
+
+cudaError_t launch_null(const LaunchShape& l, cudaStream_t stream) {
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = once_per_device(attr_done, [] {
+    int dev = 0, optin = 0;
+    cudaError_t r = cudaGetDevice(&dev);
+    if (r == cudaSuccess) r = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (r == cudaSuccess) r = cudaFuncSetAttribute(null_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (r == cudaSuccess) r = cudaFuncSetAttribute(null_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return r;
+  });
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = l.grid;
+  cfg.blockDim = l.block;
+  cfg.dynamicSmemBytes = l.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (l.cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(l.cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, null_kernel);
+}
 
 cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
                              int elem_bytes, cudaStream_t stream) {

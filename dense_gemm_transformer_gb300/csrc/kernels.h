@@ -58,6 +58,20 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// The launch configuration of the main GEMM kernel most recently launched
+// from this host thread (the SIMT, tcgen05 or small-M kernel of a call, not
+// its transposes, re-packs or reductions).
+struct LaunchShape {
+  dim3 grid, block;
+  size_t smem = 0;
+  int cluster = 1;  // CTAs per cluster along x
+  bool valid = false;
+};
+LaunchShape& last_main_launch();
+// An empty kernel with that configuration and programmatic dependent launch:
+// the launch, placement and exit cost of the configuration without its work.
+cudaError_t launch_null(const LaunchShape& l, cudaStream_t stream);
+
 // ---------------------------------------------------------------- FP32 SIMT
 // C = alpha * op(A) op(B) + beta * C with FFMA, 128 x tile_n block tiles
 // (tile_n 128: two CTAs per SM; 256: one), in one of three schedules:

@@ -505,13 +505,26 @@ __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
     const int r = e / (TBN / 4), c4 = (e % (TBN / 4)) * 4;
     const int64_t row = m0 + r;
     if (row >= p.M || n0 + c4 >= p.N) continue;
+    // Partials are loaded kBatch at a time (independent loads in flight: a
+    // deep-K tile has dozens of partials, and one dependent L2 round trip per
+    // partial would dominate) and added in ascending order.
+    constexpr int kBatch = 8;
+    const float* __restrict__ src = p.ws + r * TBN + c4;
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < n; ++q) {
-      const float4 v = *reinterpret_cast<const float4*>(p.ws + slots[q] * (BM * TBN) + r * TBN + c4);
-      sum.x += v.x;
-      sum.y += v.y;
-      sum.z += v.z;
-      sum.w += v.w;
+    for (int q0 = 0; q0 < n; q0 += kBatch) {
+      float4 v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (q0 + u < n) v[u] = *reinterpret_cast<const float4*>(src + slots[q0 + u] * (BM * TBN));
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (q0 + u < n) {
+          sum.x += v[u].x;
+          sum.y += v[u].y;
+          sum.z += v[u].z;
+          sum.w += v[u].w;
+        }
+      }
     }
     float* crow = p.C + row * p.ldc + n0 + c4;
     const int64_t left = p.N - (n0 + c4);
@@ -550,6 +563,7 @@ cudaError_t launch_tbn(const SimtArgs& a, cudaStream_t stream) {
     grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
                 static_cast<unsigned>(a.schedule == kSimtSplitK ? a.splits : 1));
   }
+  last_main_launch() = LaunchShape{grid, dim3(NT), static_cast<size_t>(SimtCfg<TBN>::SMEM_BYTES), 1, true};
   const auto aligned16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
   const bool vec = aligned16(a.A) && aligned16(a.B) && (a.lda % 4 == 0) && (a.ldb % 4 == 0);
   const bool cvec = aligned16(a.C) && (a.ldc % 4 == 0);

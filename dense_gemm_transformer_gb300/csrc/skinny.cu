@@ -352,6 +352,7 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const SkPar
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = make_config<MODE>(p, grid, s, attr);
+  last_main_launch() = LaunchShape{cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes, p.cluster, true};
   return cudaLaunchKernelEx(&cfg, skinny_gemm_kernel<MODE, A_MN>, ta, tb, p);
 }
 

@@ -17,6 +17,8 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   });
   if (e != cudaSuccess) return e;
+  last_main_launch() = LaunchShape{dim3(static_cast<unsigned>(grid)), dim3(kTcThreads),
+                                   static_cast<size_t>(Cfg::SMEM_BYTES), PAIR ? 2 : 1, true};
   if constexpr (PAIR) {
     // Two-CTA clusters along x: CTAs 2c and 2c+1 form pair c.
     cudaLaunchConfig_t cfg = {};

@@ -151,6 +151,18 @@ gemm_status_t gemm_get_plan(gemm_handle_t h, gemm_plan_t* out);
  * reports an error, GEMM_OK otherwise. */
 gemm_status_t gemm_check_device(gemm_handle_t h, void* stream);
 
+/* Launch, on `stream`, an empty kernel with the launch configuration of the
+ * main kernel of this handle's last successful gemm_run (its grid, block,
+ * dynamic shared memory, cluster size and programmatic dependent launch;
+ * not the transposes, re-packs or reductions around it).  It reads and
+ * writes no memory.  Timed like the GEMM, it gives the cost of launching,
+ * placing and retiring that configuration: the floor under the call's time
+ * (the "identity null" that the "gpu kernels" write-up on devpost times
+ * beside every shape, section "How we know the numbers are real").  GEMM_ERR_INVALID_VALUE when the last
+ * call launched no GEMM kernel (M, N or K zero, alpha zero) or none was made;
+ * GEMM_ERR_CUDA when the launch fails. */
+gemm_status_t gemm_launch_null(gemm_handle_t h, void* stream);
+
 /* Bytes of the fixed device array that gemm_run_small_m_noalloc uses as its
  * only scratch memory (one array per device, held until the process exits). */
 #define GEMM_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -61,3 +61,17 @@ def test_max_over_ranks_with_gloo():
         out = m.dict()
         mp.spawn(_worker, args=(world, 29562, out), nprocs=world, join=True)
         assert dict(out) == {0: 2.0, 1: 2.0}
+
+
+def test_sweep_processes_merge_takes_the_median_process():
+    """The per-shape result across processes is the median process's record
+    (its time, TFLOP/s and fraction together), with every time kept."""
+    import bench
+    mk = lambda g, ms: {"gemm": g, "ms": ms, "tflops": 1.0 / ms, "roofline_frac": 0.5 / ms}
+    runs = [[mk("a", 3.0), mk("b", 1.0)], [mk("a", 1.0), mk("b", 2.0)], [mk("a", 2.0), mk("b", 3.0)]]
+    out = bench.merge_process_runs(runs)
+    assert [x["gemm"] for x in out] == ["a", "b"]
+    assert out[0]["ms"] == 2.0 and out[0]["tflops"] == 0.5 and out[0]["ms_processes"] == [1.0, 2.0, 3.0]
+    assert out[1]["ms"] == 2.0 and out[1]["roofline_frac"] == 0.25
+    with pytest.raises(ValueError):
+        bench.merge_process_runs([[mk("a", 1.0)], [mk("b", 1.0)]])
