@@ -15,8 +15,8 @@
 //     transposed on the way in) so they are read as float4 along M / N;
 //   * K tiles are copied global -> shared with cp.async (no register
 //     staging) into a ring of 3 (TBN = 128) or 4 (TBN = 256) stages, with one
-//     barrier per tile; with TBN = 256 the register fragments of step k+1 are
-//     loaded while step k is multiplied;
+//     barrier per tile; the register fragments of step k+1 are loaded while
+//     step k is multiplied;
 //   * work is scheduled as whole tiles when they fill whole waves of the
 //     resident CTAs, and otherwise as whole-tile waves followed by stream-K
 //     for the rest: the remaining (tile, k-tile) iterations are cut into one
@@ -47,7 +47,6 @@ struct SimtCfg {
   static constexpr int A_STAGE = BK * LDA;
   static constexpr int B_STAGE = BK * LDB;
   static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
-  static constexpr bool PREFETCH_FRAGMENTS = (TBN == 256);  // registers allow it at one CTA per SM
 };
 
 // cp.async copies global -> shared without staging in registers.  A source
@@ -274,19 +273,11 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
     // Accumulators in pairs of adjacent columns (acc2[i][j] holds columns
     // 2j and 2j + 1 of row i), multiplied with packed FMAs; each element
     // still sums its products in ascending k with one fp32 FMA per product.
-    // The 128-column kernels whose tile copies hold the most registers (4-byte
-    // copies of an unaligned operand, or a K-contiguous A beside an
-    // N-contiguous B) keep scalar accumulators: the packed form would spill.
-    constexpr bool PACKED = TBN == 256 || (VEC && (TA || TB));
     uint64_t acc2[8][TN / 2];
-    float acc[8][TN];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int j = 0; j < TN / 2; ++j) acc2[i][j] = 0ull;  // +0.0f, +0.0f
-#pragma unroll
-      for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
-    }
 
     // op(A) is K-contiguous when A is stored M x K (TA == 0); op(B) is
     // K-contiguous when B is stored N x K (TB == 1).
@@ -319,86 +310,42 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
       cp_async_commit();
       const float* a_s = As + (t % S) * Cfg::A_STAGE;
       const float* b_s = Bs + (t % S) * Cfg::B_STAGE;
-      if constexpr (Cfg::PREFETCH_FRAGMENTS) {
-        float af[2][8];
-        uint64_t bf[2][TN / 2];  // B fragment as column pairs, loaded as such
-        auto load = [&](int k, int buf) {
+      // Fragments of step k + 1 are loaded while step k is multiplied.
+      float af[2][8];
+      uint64_t bf[2][TN / 2];  // B fragment as column pairs, loaded as such
+      auto load = [&](int k, int buf) {
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const float4 v = *reinterpret_cast<const float4*>(a_s + k * LDA + am + 16 * r);
-            af[buf][4 * r + 0] = v.x;
-            af[buf][4 * r + 1] = v.y;
-            af[buf][4 * r + 2] = v.z;
-            af[buf][4 * r + 3] = v.w;
-          }
-#pragma unroll
-          for (int q = 0; q < QN; ++q) {
-            const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(b_s + k * LDB + bn + 32 * q);
-            bf[buf][2 * q + 0] = v.x;
-            bf[buf][2 * q + 1] = v.y;
-          }
-        };
-        load(0, 0);
-#pragma unroll
-        for (int k = 0; k < BK; ++k) {
-          if (k + 1 < BK) load(k + 1, (k + 1) & 1);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint64_t a2 = pack2(af[k & 1][i], af[k & 1][i]);
-#pragma unroll
-            for (int j = 0; j < TN / 2; ++j) ffma2(acc2[i][j], a2, bf[k & 1][j]);
-          }
+        for (int r = 0; r < 2; ++r) {
+          const float4 v = *reinterpret_cast<const float4*>(a_s + k * LDA + am + 16 * r);
+          af[buf][4 * r + 0] = v.x;
+          af[buf][4 * r + 1] = v.y;
+          af[buf][4 * r + 2] = v.z;
+          af[buf][4 * r + 3] = v.w;
         }
-      } else {
 #pragma unroll
-        for (int k = 0; k < BK; ++k) {
-          float a[8];
+        for (int q = 0; q < QN; ++q) {
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(b_s + k * LDB + bn + 32 * q);
+          bf[buf][2 * q + 0] = v.x;
+          bf[buf][2 * q + 1] = v.y;
+        }
+      };
+      load(0, 0);
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const float4 v = *reinterpret_cast<const float4*>(a_s + k * LDA + am + 16 * r);
-            a[4 * r + 0] = v.x;
-            a[4 * r + 1] = v.y;
-            a[4 * r + 2] = v.z;
-            a[4 * r + 3] = v.w;
-          }
-          if constexpr (PACKED) {
-            uint64_t b2[TN / 2];  // B fragment as column pairs, loaded as such
+      for (int k = 0; k < BK; ++k) {
+        if (k + 1 < BK) load(k + 1, (k + 1) & 1);
 #pragma unroll
-            for (int q = 0; q < QN; ++q) {
-              const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(b_s + k * LDB + bn + 32 * q);
-              b2[2 * q + 0] = v.x;
-              b2[2 * q + 1] = v.y;
-            }
+        for (int i = 0; i < 8; ++i) {
+          const uint64_t a2 = pack2(af[k & 1][i], af[k & 1][i]);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint64_t a2 = pack2(a[i], a[i]);
-#pragma unroll
-              for (int j = 0; j < TN / 2; ++j) ffma2(acc2[i][j], a2, b2[j]);
-            }
-          } else {
-            float b[TN];
-#pragma unroll
-            for (int q = 0; q < QN; ++q) {
-              const float4 v = *reinterpret_cast<const float4*>(b_s + k * LDB + bn + 32 * q);
-              b[4 * q + 0] = v.x;
-              b[4 * q + 1] = v.y;
-              b[4 * q + 2] = v.z;
-              b[4 * q + 3] = v.w;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-              for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-          }
+          for (int j = 0; j < TN / 2; ++j) ffma2(acc2[i][j], a2, bf[k & 1][j]);
         }
       }
     }
-    if constexpr (PACKED) {
+    float acc[8][TN];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < TN / 2; ++j) unpack2(acc2[i][j], acc[i][2 * j], acc[i][2 * j + 1]);
-    }
+      for (int j = 0; j < TN / 2; ++j) unpack2(acc2[i][j], acc[i][2 * j], acc[i][2 * j + 1]);
     cp_async_wait<0>();
     __syncthreads();  // the ring is idle before the next segment refills it
 
