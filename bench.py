@@ -538,6 +538,13 @@ def bench_sweep(args):
     pk = peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     shapes = []
+    with ClockSampler(dev.index) as clk:
+        _sweep_shapes(args, h, stream, pk, l2, dev, shapes)
+    h.close()
+    return shapes, clk.summary()
+
+
+def _sweep_shapes(args, h, stream, pk, l2, dev, shapes):
     for label, mode, c, alpha, beta, wstd in sweep_cases(args.workload):
         if args.only:
             import re
@@ -612,7 +619,10 @@ def bench_sweep(args):
         stream.synchronize()
         byts = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N * (2 if beta != 0 else 1)
         peak = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops"], "bf16": pk["bf16_tflops"]}[mode]
+        peak_s = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops_sustained"],
+                  "bf16": pk["bf16_tflops_sustained"]}[mode]
         t_c, t_m = c.flops / (peak * 1e12), byts / (pk["hbm_gbs"] * 1e9)
+        t_cs = c.flops / (peak_s * 1e12)
         st = _stats(dev_ms)
         gate_graph = plan["family"] == "skinny" or (c.M <= 16 and graph_ms is not None)
         t = graph_ms["median"] if (gate_graph and graph_ms is not None) else st["median"]
@@ -627,14 +637,13 @@ def bench_sweep(args):
                        "tflops": round(c.flops / (t * 1e-3) / 1e12, 2),
                        "gbs": round(byts / (t * 1e-3) / 1e9, 1), "bound": "hbm" if t_m > t_c else
                        ("alu" if mode == "fp32" else "tensor"), "roofline_frac": round(max(t_c, t_m) / (t * 1e-3), 3),
+                       "roofline_frac_sustained": round(max(t_cs, t_m) / (t * 1e-3), 3),
                        "plan": plan, "copies": copies})
         del sets, A0, B0
         torch.cuda.empty_cache()
-    h.close()
-    return shapes
 
 
-def sweep_line(args, shapes, processes):
+def sweep_line(args, shapes, processes, clocks):
     pk = peaks()
     total_flops = sum(2 * x["M"] * x["N"] * x["K"] for x in shapes)
     total_s = sum(x["ms"] for x in shapes) * 1e-3
@@ -643,16 +652,20 @@ def sweep_line(args, shapes, processes):
             "config": {"workload": args.workload, "l2": "operands rotated over copies > 3x L2",
                        "samples": f"median of {SAMPLES} samples of >= {SAMPLE_MS:g} ms per process, "
                                   f"median over {processes} process(es)"},
-            "processes": processes, "shapes": shapes, "peaks": pk}
+            "processes": processes, "clocks": clocks, "shapes": shapes, "peaks": pk,
+            "roofline_note": "roofline_frac against the burst tensor peak (a kernel timed alone); "
+                             "roofline_frac_sustained against the sustained one (samples of >= 20 ms "
+                             "back to back run under the power cap)"}
 
 
 def bench_sweep_processes(args):
     """The sweep in `args.processes` separate processes; per shape, the median
     over the processes of their medians, with the spread across processes."""
     if args.processes <= 1:
-        print(json.dumps(sweep_line(args, bench_sweep(args), 1)), flush=True)
+        shapes, clocks = bench_sweep(args)
+        print(json.dumps(sweep_line(args, shapes, 1, clocks)), flush=True)
         return
-    runs = []
+    runs, clocks = [], []
     for _ in range(args.processes):
         cmd = [sys.executable, os.path.abspath(__file__), "--workload", args.workload, "--processes", "1"]
         if args.only:
@@ -662,8 +675,10 @@ def bench_sweep_processes(args):
         if args.pair is not None:
             cmd += ["--pair", str(args.pair)]
         out = subprocess.run(cmd, capture_output=True, text=True, check=True).stdout
-        runs.append(json.loads(out.strip().splitlines()[-1])["shapes"])
-    print(json.dumps(sweep_line(args, merge_process_runs(runs), args.processes)), flush=True)
+        line = json.loads(out.strip().splitlines()[-1])
+        runs.append(line["shapes"])
+        clocks.append(line.get("clocks"))
+    print(json.dumps(sweep_line(args, merge_process_runs(runs), args.processes, clocks)), flush=True)
 
 
 def merge_process_runs(runs):

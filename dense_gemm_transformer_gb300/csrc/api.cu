@@ -403,13 +403,19 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   // Pairs of 256-column tiles issue one MMA of 256 rows per pair (tcgen05
   // cta_group::2) unless told to share B by multicast only: each CTA then
   // stages and reads half of B, which measured 1.14x the speed on large
-  // shapes (BF16 8192^3: 1687 -> 1929 TFLOP/s).
+  // shapes (BF16 8192^3: 1687 -> 1929 TFLOP/s).  TF32 stages twice the bytes
+  // per FLOP, and with 24 or more K blocks the halved B measured worth more:
+  // on the N = 384 GPT products (K = 1152-1536) the 256-column pairs, padding
+  // N to 512, ran 8-10% faster than 192-column pairs (MLP-down forward 46.9
+  // -> 42.4 us), which a factor of 1.3 reproduces; with short K the tile's
+  // fixed cost dominates and 1.14 still ranks the widths as measured.
   auto mma2_for = [&](int tn) { return tn == 256 && pair_ok(tn) && (h->opt_pair == 0 || h->opt_pair == 3); };
+  const double mma2_gain = (mode == GEMM_MODE_TF32 && kb >= 24) ? 1.3 : 1.14;
   auto plan_for = [&](int tn) {
     const bool pr = pair_ok(tn);
     const int64_t rows = pr ? ceil_div(tm_tiles, 2) : tm_tiles;
     const double unit_s = 2.0 * 128.0 * 256.0 * static_cast<double>(K) / peak *
-                          (128.0 * 128.0 + 128.0 * tn) / (128.0 * 384.0) / (mma2_for(tn) ? 1.14 : 1.0);
+                          (128.0 * 128.0 + 128.0 * tn) / (128.0 * 384.0) / (mma2_for(tn) ? mma2_gain : 1.0);
     const double c_row_bytes = 4.0 * static_cast<double>(Nk) * (pr ? 256.0 : 128.0);
     const bool may_cut = !swap && h->opt_split_k == 0 && !(2 * tm_tiles * ceil_div(Nk, tn) <= sms && kb >= 8);
     if (!may_cut) {
