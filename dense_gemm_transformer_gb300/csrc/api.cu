@@ -133,21 +133,25 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   if (tile_n == 0) tile_n = (N % 256 == 0 && M >= 1024) ? 256 : 128;
   const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, tile_n);
   const int64_t slots = (tile_n == 256 ? 1 : 2) * static_cast<int64_t>(h->sms);  // resident CTAs
-  // An operand stored with K contiguous reaches shared memory through 4-byte
+  // An operand stored with K contiguous must be transposed on its way to
+  // shared memory.  Transposing it once into the workspace costs 8 bytes of
+  // HBM traffic per element against 2 x (N or M) FLOPs per element of the
+  // GEMM: ~33 / (the other dimension) of the GEMM's time.  A K-contiguous,
+  // aligned A is transposed inside the kernel instead (16-byte row copies and
+  // a shared-memory transpose), which costs a few percent of the kernel at
+  // any N: measured on the GPT products, the in-kernel form is 2-8% faster
+  // for N = 65-384 and 4-6% slower for N = 1152-1536, so A is transposed into
+  // the workspace from N >= 768.  A K-contiguous B is read with 4-byte
   // transposing copies, which load the L1/shared-memory pipe far more than
-  // the 16-byte copies of an M- or N-contiguous operand.  Transposing it once
-  // into the workspace costs 8 bytes of HBM traffic per element against
-  // 2 x (N or M) FLOPs per element of the GEMM: under ~10% of the GEMM's
-  // time when the other dimension is >= 256, and the copies it avoids cost
-  // more than that, so it is done then.
+  // 16-byte copies, so it is transposed into the workspace from M >= 256.
   const int pre = h->opt_pretranspose;  // 0 planner, 1 never, 2 always
-  const bool tr_a = !transA && K > 0 && (pre == 2 || (pre == 0 && N >= 256 && M >= 128 && K >= 64));
+  const bool tr_a = !transA && K > 0 && (pre == 2 || (pre == 0 && N >= 768 && M >= 128 && K >= 64));
   const bool tr_b = transB && K > 0 && (pre == 2 || (pre == 0 && M >= 256 && N >= 128 && K >= 64));
   const int64_t lda_t = round_up(M, 4), ldb_t = round_up(N, 4);
   // An operand whose base or rows are not 16-byte aligned would make the
-  // kernel copy both operands 4 bytes at a time (and keep scalar FMAs); a copy
-  // with an aligned leading dimension costs one read and write of it and is
-  // made instead (not with pretranspose = 1, which keeps operands in place).
+  // kernel copy both operands 4 bytes at a time; a copy with an aligned
+  // leading dimension costs one read and write of it and is made instead
+  // (not with pretranspose = 1, which keeps operands in place).
   auto misaligned = [](const float* q, int64_t ld) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0 || ld % 4 != 0; };
   const bool pk_a = !tr_a && K > 0 && pre != 1 && misaligned(A, lda);
   const bool pk_b = !tr_b && K > 0 && pre != 1 && misaligned(B, ldb);

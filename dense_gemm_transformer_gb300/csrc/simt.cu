@@ -11,8 +11,13 @@
 //     thread's register tile is split into 4 x 4 quadrants so each of its
 //     shared-memory reads is one float4 that the lanes sharing a row or column
 //     receive by broadcast;
-//   * both operands sit k-major in shared memory (a K-contiguous operand is
-//     transposed on the way in) so they are read as float4 along M / N;
+//   * both operands sit k-major in shared memory so they are read as float4
+//     along M / N.  A K-contiguous A (stored M x K, 16-byte aligned) is
+//     copied row by row with 16-byte copies into its stage and transposed in
+//     shared memory (two 16-byte reads and eight 4-byte writes per thread per
+//     K tile, then one more barrier); a K-contiguous operand that is not
+//     aligned, or a K-contiguous B, is transposed on the way in with 4-byte
+//     copies;
 //   * K tiles are copied global -> shared with cp.async (no register
 //     staging) into a ring of 3 (TBN = 128) or 4 (TBN = 256) stages, with one
 //     barrier per tile; the register fragments of step k+1 are loaded while
@@ -26,6 +31,8 @@
 //   * products are single-rounded FFMA in fp32, the accumulation order along
 //     K is ascending, and the alpha/beta epilogue is fused into the stores.
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -47,6 +54,12 @@ struct SimtCfg {
   static constexpr int A_STAGE = BK * LDA;
   static constexpr int B_STAGE = BK * LDB;
   static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+  // A stored M x K with K contiguous: each K tile lands row by row (rows of
+  // BK floats, padded to LDK) and is transposed in shared memory into one
+  // k-major buffer of A_STAGE floats.
+  static constexpr int LDK = BK + 4;
+  static constexpr int A_RAW_STAGE = BM * LDK;
+  static constexpr int SMEM_BYTES_RAW = (STAGES * (A_RAW_STAGE + B_STAGE) + A_STAGE) * 4;
 };
 
 // cp.async copies global -> shared without staging in registers.  A source
@@ -60,6 +73,13 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src, bool ok)
 __device__ __forceinline__ void cp_async16(float* dst, const float* src, bool ok) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(ok ? 16 : 0) : "memory");
+}
+
+// 16-byte copy of which the first `bytes` (0, 4, 8, 12 or 16) come from src
+// and the rest are zero-filled.
+__device__ __forceinline__ void cp_async16n(float* dst, const float* src, int bytes) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -163,6 +183,39 @@ struct TileCopier {
   }
 };
 
+// Copies successive K tiles of a K-contiguous, 16-byte-aligned operand of
+// ROWS rows into s[row * LDK + k] (rows as stored): thread -> rows tid/4 and
+// tid/4 + 64h, K quad tid%4; a quad that runs past K is zero-filled.
+template <int ROWS, int LDK>
+struct RowTileCopier {
+  static constexpr int H = ROWS / 64;
+  const float* ptr[H];
+  bool row_ok[H];
+
+  __device__ __forceinline__ void init(const float* __restrict__ base, int64_t ld, int64_t mn0, int64_t lim,
+                                       int64_t kbeg, int tid) {
+    const int row = tid >> 2, kq = (tid & 3) * 4;
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      const int64_t r = mn0 + row + 64 * h;
+      row_ok[h] = r < lim;
+      ptr[h] = base + (row_ok[h] ? r : 0) * ld + kbeg + kq;
+    }
+  }
+
+  __device__ __forceinline__ void issue(float* s, int k_rem, int tid, const float* safe) {
+    const int row = tid >> 2, kq = (tid & 3) * 4;
+    const int left = k_rem - kq;
+    const int bytes = left >= 4 ? 16 : left > 0 ? 4 * left : 0;
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      const int b = row_ok[h] ? bytes : 0;
+      cp_async16n(s + (row + 64 * h) * LDK + kq, b > 0 ? ptr[h] : safe, b);
+      ptr[h] += BK;
+    }
+  }
+};
+
 // The k-tile range [ks, ke) of one tile that a CTA accumulates in one go, and
 // where the result goes.
 struct Segment {
@@ -186,8 +239,12 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
   grid_dep_wait();
   grid_dep_launch();
   extern __shared__ __align__(16) float smem[];
-  float* As = smem;                      // [S][BK][LDA]
-  float* Bs = smem + S * Cfg::A_STAGE;   // [S][BK][LDB]
+  // A K-contiguous A lands row by row and is transposed in shared memory.
+  constexpr bool A_RAW = !TA && VEC;
+  constexpr int A_RING = A_RAW ? Cfg::A_RAW_STAGE : Cfg::A_STAGE;
+  float* As = smem;                      // [S][BK][LDA], or [S][BM][LDK] rows as stored
+  float* Bs = smem + S * A_RING;         // [S][BK][LDB]
+  float* Ax = Bs + S * Cfg::B_STAGE;     // [BK][LDA]: the transposed tile (A_RAW)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -281,11 +338,17 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
 
     // op(A) is K-contiguous when A is stored M x K (TA == 0); op(B) is
     // K-contiguous when B is stored N x K (TB == 1).
-    TileCopier<!TA, VEC, BM, LDA> ca;
+    std::conditional_t<A_RAW, RowTileCopier<BM, Cfg::LDK>, TileCopier<!TA, VEC, BM, LDA>> ca;
     TileCopier<TB, VEC, TBN, LDB> cb;
     const int64_t kbeg = static_cast<int64_t>(sh.sg.ks) * BK;
     ca.init(p.A, p.lda, m0, p.M, kbeg, tid);
     cb.init(p.B, p.ldb, n0, p.N, kbeg, tid);
+    auto issue_a = [&](float* dst, int k_rem) {
+      if constexpr (A_RAW)
+        ca.issue(dst, k_rem, tid, p.A);
+      else
+        ca.issue(dst, k_rem, tid, p.A, p.lda);
+    };
     // The ring: tiles t+1 .. t+S-1 are in flight while tile t is multiplied;
     // one barrier per tile both publishes tile t and frees the stage that
     // tile t+S-1 overwrites (it held tile t-1).
@@ -293,7 +356,7 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
     for (int st = 0; st < S - 1; ++st) {
       if (st < n) {
         const int k_rem = static_cast<int>(p.K - (kbeg + st * BK));
-        ca.issue(As + st * Cfg::A_STAGE, k_rem, tid, p.A, p.lda);
+        issue_a(As + st * A_RING, k_rem);
         cb.issue(Bs + st * Cfg::B_STAGE, k_rem, tid, p.B, p.ldb);
       }
       cp_async_commit();
@@ -304,12 +367,30 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
       if (t + S - 1 < n) {
         const int nx = (t + S - 1) % S;
         const int k_rem = static_cast<int>(p.K - (kbeg + static_cast<int64_t>(t + S - 1) * BK));
-        ca.issue(As + nx * Cfg::A_STAGE, k_rem, tid, p.A, p.lda);
+        issue_a(As + nx * A_RING, k_rem);
         cb.issue(Bs + nx * Cfg::B_STAGE, k_rem, tid, p.B, p.ldb);
       }
       cp_async_commit();
-      const float* a_s = As + (t % S) * Cfg::A_STAGE;
+      const float* a_s = As + (t % S) * A_RING;
       const float* b_s = Bs + (t % S) * Cfg::B_STAGE;
+      if constexpr (A_RAW) {
+        // Transpose tile t into Ax (each thread: rows m = tid % 128, K quads
+        // tid / 128 and tid / 128 + 2), then publish it.  Ax was last read by
+        // the previous tile's FMAs, which every thread finished before the
+        // barrier above.
+        const int m = tid & (BM - 1), kh = tid >> 7;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int kq = kh + 2 * j;
+          const float4 v = *reinterpret_cast<const float4*>(a_s + m * Cfg::LDK + 4 * kq);
+          Ax[(4 * kq + 0) * LDA + m] = v.x;
+          Ax[(4 * kq + 1) * LDA + m] = v.y;
+          Ax[(4 * kq + 2) * LDA + m] = v.z;
+          Ax[(4 * kq + 3) * LDA + m] = v.w;
+        }
+        __syncthreads();
+        a_s = Ax;
+      }
       // Fragments of step k + 1 are loaded while step k is multiplied.
       float af[2][8];
       uint64_t bf[2][TN / 2];  // B fragment as column pairs, loaded as such
@@ -484,7 +565,7 @@ __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
 
 template <int TBN, bool TA, bool TB, bool VEC>
 cudaError_t launch_cvec(const SimtArgs& a, dim3 grid, cudaStream_t s, bool cvec) {
-  constexpr int smem = SimtCfg<TBN>::SMEM_BYTES;
+  constexpr int smem = (!TA && VEC) ? SimtCfg<TBN>::SMEM_BYTES_RAW : SimtCfg<TBN>::SMEM_BYTES;
   auto kern = cvec ? simt_gemm_kernel<TBN, TA, TB, VEC, true> : simt_gemm_kernel<TBN, TA, TB, VEC, false>;
   static std::atomic<uint64_t> done[2] = {};
   cudaError_t e = once_per_device(done[cvec ? 1 : 0], [&] {
@@ -510,10 +591,12 @@ cudaError_t launch_tbn(const SimtArgs& a, cudaStream_t stream) {
     grid = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
                 static_cast<unsigned>(a.schedule == kSimtSplitK ? a.splits : 1));
   }
-  last_main_launch() = LaunchShape{grid, dim3(NT), static_cast<size_t>(SimtCfg<TBN>::SMEM_BYTES), 1, true};
   const auto aligned16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
   const bool vec = aligned16(a.A) && aligned16(a.B) && (a.lda % 4 == 0) && (a.ldb % 4 == 0);
   const bool cvec = aligned16(a.C) && (a.ldc % 4 == 0);
+  last_main_launch() = LaunchShape{
+      grid, dim3(NT),
+      static_cast<size_t>((!a.transA && vec) ? SimtCfg<TBN>::SMEM_BYTES_RAW : SimtCfg<TBN>::SMEM_BYTES), 1, true};
   cudaError_t e;
   if (!a.transA && !a.transB)
     e = launch_vec<TBN, false, false>(a, grid, stream, vec, cvec);

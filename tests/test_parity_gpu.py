@@ -211,6 +211,39 @@ def test_fp32_pretranspose(h, pre, tA, tB, M, N, K):
     _cases.run_and_check(h, "fp32", M, N, min(K, 1024), tA, tB, seed=72, dist="int", exact=True)
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("pre", [0, 1])
+@pytest.mark.parametrize("M,N,K", [(200, 300, 1), (129, 130, 3), (300, 260, 17), (1000, 384, 383),
+                                   (257, 520, 1537)])
+def test_fp32_k_contiguous_a_transposed_in_kernel(h, tile_n, pre, M, N, K):
+    """A stored M x K (K contiguous, rows 16-byte aligned) goes to shared
+    memory row by row and is transposed there.  Its rows sit in a wider
+    buffer whose padding columns hold NaN: a K quad that runs past K must be
+    zero-filled, not read, or the NaN would reach C."""
+    h.set_option("tile_n", tile_n)
+    h.set_option("pretranspose", pre)
+    lda = (K + 3) // 4 * 4 + 4
+    a = si.normal((M, K), 81)
+    b = si.normal((K, N), 82)
+    c0 = si.normal((M, N), 83)
+    buf = torch.full((M, lda), float("nan"), device="cuda")
+    buf[:, :K] = a.cuda()
+    A = buf[:, :K]
+    C = c0.clone().cuda()
+    h.run(A, b.cuda(), C, mode="fp32", alpha=0.75, beta=-0.5)
+    assert h.check_device() == 0
+    assert h.plan()["packed"] & 1 == 0  # read in place, not copied into the workspace
+    ref, D = oracle.gemm("fp32", a.numpy(), b.numpy(), alpha=0.75, beta=-0.5, C=c0.numpy())
+    _gate.assert_within("fp32", C.cpu().numpy(), ref, D, 0.75, -0.5, c0.numpy(), what=f"{M}x{N}x{K}")
+    ai = si.integers((M, K), 84)
+    bi = si.integers((K, N), 85)
+    buf[:, :K] = ai.cuda()
+    C = torch.full((M, N), float("nan"), device="cuda")
+    h.run(A, bi.cuda(), C, mode="fp32")
+    ref, _ = oracle.gemm("fp32", ai.numpy(), bi.numpy())
+    assert np.array_equal(C.cpu().numpy().astype(np.float64), ref), "not bit-exact"
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_many_tiles_persistent_loop(h, mode):
     # More tiles than SMs: every CTA of the persistent grid loops over several
