@@ -179,7 +179,10 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   int grid = static_cast<int>(std::min<int64_t>(tiles, INT32_MAX));
   int kernels = 1;
   // Whole tiles when they fill whole waves of the resident CTAs (or the
-  // problem is too small to share out); stream-K otherwise.
+  // problem is too small to share out, or K is under 16 k-tiles: then every
+  // tile would be split and its partial stores and fixup cost more than the
+  // idle part of the last wave -- K = 65, 384 tiles: 58 us as stream-K,
+  // 32 us as two waves of whole tiles); stream-K otherwise.
   if (h->opt_split_k > 0) {
     int64_t splits = h->opt_split_k;
     const int64_t kps = round_up(ceil_div(K, splits), kSimtTileK);
@@ -188,7 +191,7 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
     a.splits = static_cast<int>(splits);
     a.k_per_split = kps;
     grid = static_cast<int>(tiles * splits);
-  } else if (wave_eff(tiles, slots) >= 0.92 || tiles * kt < 4 * slots) {
+  } else if (wave_eff(tiles, slots) >= 0.92 || tiles * kt < 4 * slots || kt < 16) {
     a.schedule = kSimtTiles;
   } else {
     // Whole-tile waves first, stream-K over the rest: the last partial wave
