@@ -280,14 +280,15 @@ struct OperandPack {
   size_t bytes = 0;
 };
 
-OperandPack plan_pack(const void* src, int64_t ld, int64_t rows, int64_t cols, bool mn_major, int mode, int es) {
+OperandPack plan_pack(const void* src, int64_t ld, int64_t rows, int64_t cols, bool mn_major, int mode, int es,
+                      bool mn_ok = false) {
   OperandPack p;
   p.src = src;
   p.ld = ld;
   p.rows = rows;
   p.cols = cols;
   p.mn_major_after = mn_major;
-  if (mode == GEMM_MODE_TF32 && mn_major) {
+  if (mode == GEMM_MODE_TF32 && mn_major && !mn_ok) {
     p.kind = OperandPack::kTranspose;  // stored K x MN -> MN x K
     p.dst_ld = round_up(rows, 16 / es);
     p.bytes = static_cast<size_t>(cols * p.dst_ld * es);
@@ -486,9 +487,18 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   // when the TMA unit cannot read it in place (base not 16-byte aligned, or a
   // row pitch that is not a multiple of 16 bytes), and transposed into K-major
   // order when it is MN-major in TF32 mode: kind::tf32 takes K-major operands
-  // only (an MN-major TF32 operand produced zeros on this part, while BF16
-  // reads both orders).
-  OperandPack pa = plan_pack(Ak, ldak, ta_k ? K : Mk, ta_k ? Mk : K, ta_k != 0, mode, es);
+  // from shared memory only (an MN-major TF32 operand produced zeros on this
+  // part, while BF16 reads both orders).  The exception is an MN-major A with
+  // 128-column tiles and no CTA pairs: that kernel moves A into TMEM, where
+  // the MMA reads it row by row, so no transpose pass is needed (unless
+  // pretranspose = 2 asks for one).  The warps that move A slow the MMA
+  // loop by ~20% on long K, against a pass that costs 8 bytes of HBM
+  // traffic per element of A for 2N FLOPs per element: measured on the TF32
+  // dW products, TMEM took 20-25% off for N = 65-384, broke even at
+  // N = 1152 and lost 2% at N = 1536, so it is used for N < 1536.
+  const bool a_tmem = mode == GEMM_MODE_TF32 && !swap && tile_n == 128 && !pair && Nk < 1536 &&
+                      h->opt_pretranspose != 2;
+  OperandPack pa = plan_pack(Ak, ldak, ta_k ? K : Mk, ta_k ? Mk : K, ta_k != 0, mode, es, a_tmem);
   OperandPack pb = plan_pack(Bk, ldbk, tb_k ? Nk : K, tb_k ? K : Nk, tb_k == 0, mode, es);
   WsLayout L;
   L.a_off = 0;

@@ -20,6 +20,11 @@
 //               update, and the stores; then they release the accumulator
 //               so the next tile's MMAs can start.  Two accumulators let the
 //               epilogue of tile i overlap the mainloop of tile i+1.
+//   TF32 with an MN-major A (128-column tiles, one CTA): kind::tf32 reads
+//               only K-major operands from shared memory, so warps 2-5 read
+//               each stage's A tile there (one row of A per lane, down the
+//               MN-major rows) and store it into TMEM, whose lanes are the
+//               rows the MMA takes A from; warps 6-9 are the epilogue.
 //
 // Work units are tiles, or (tile, K slice) pairs, handed out round-robin to
 // a persistent grid of one CTA per SM (or one CTA pair per two SMs, see PAIR
@@ -195,13 +200,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   static_assert(!MMA2 || PAIR, "the two-CTA MMA runs on pairs");
   using Cfg = TcCfg<MODE, BN, MMA2>;
   constexpr int S = Cfg::STAGES;
-  constexpr uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN, B_MN, MMA2 ? 2 * Cfg::BM : Cfg::BM, BN);
+  // TF32 with an MN-major A: kind::tf32 reads only K-major operands from
+  // shared memory, so warps 2-5 move each stage's A tile into TMEM (row i of
+  // the tile in lane i, K along the columns), where the MMA takes A from;
+  // warps 6-9 are the epilogue.  A ring of NA buffers of BK columns sits
+  // after the two accumulators.
+  constexpr bool A_TMEM = MODE == 1 && A_MN;
+  static_assert(!A_TMEM || (BN == 128 && !PAIR && !MMA2 && !TRANS_C), "A through TMEM: 128-column tiles, one CTA");
+  constexpr int NA = 4;
+  constexpr int A_COL0 = 2 * BN;  // first TMEM column of the A buffers
+  constexpr int TMEM_COLS = A_TMEM ? 512 : Cfg::TMEM_COLS;
+  constexpr int EXTRA_BARS = A_TMEM ? 2 * NA : 0;
+  static_assert((Cfg::NUM_BARS + EXTRA_BARS) * 8 + 16 <= 256, "barrier area");
+  static_assert(!A_TMEM || A_COL0 + NA * Cfg::BK <= TMEM_COLS, "TMEM columns");
+  constexpr uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN && !A_TMEM, B_MN, MMA2 ? 2 * Cfg::BM : Cfg::BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + S * Cfg::STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS + EXTRA_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const uint32_t smem0 = smem_u32(smem);
@@ -211,6 +229,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto accf_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto acce_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+  auto afull_bar = [&](int b) { return bar0 + 8u * (Cfg::NUM_BARS + b); };        // A_TMEM: A in TMEM
+  auto aempty_bar = [&](int b) { return bar0 + 8u * (Cfg::NUM_BARS + NA + b); };  // A_TMEM: buffer read
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   static_assert(!PAIR || (!TRANS_C && BN >= 128 && (!B_MN || (BN / Cfg::CH) % 2 == 0)),
@@ -226,12 +246,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      // PAIR: both CTAs' MMAs must have read the stage; MMA2: the one pair MMA
-      mbar_init(empty_bar(s), (PAIR && !MMA2) ? 2 : 1);
+      // PAIR: both CTAs' MMAs must have read the stage; MMA2: the one pair
+      // MMA; A_TMEM: the MMAs (B) and the four warps that read A
+      mbar_init(empty_bar(s), A_TMEM ? 5 : (PAIR && !MMA2) ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
-      mbar_init(acce_bar(a), MMA2 ? 2 * kTcEpiWarps : kTcEpiWarps);  // one arrival per epilogue warp (of both CTAs)
+      // one arrival per epilogue warp (of both CTAs)
+      mbar_init(acce_bar(a), A_TMEM ? 4 : MMA2 ? 2 * kTcEpiWarps : kTcEpiWarps);
+    }
+    for (int b = 0; b < (A_TMEM ? NA : 0); ++b) {
+      mbar_init(afull_bar(b), 4);
+      mbar_init(aempty_bar(b), 1);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -249,7 +275,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
       tmem_relinquish_pair();
     } else {
-      tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
       tmem_relinquish();
     }
   }
@@ -363,6 +389,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      int ab = 0;  // A_TMEM: buffer of the next stage's A
+      uint32_t a_phase = 0;
       bool ok = true;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Unit w = decode_unit(u, p);
@@ -374,16 +402,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = false;
             break;
           }
+          if constexpr (A_TMEM) {
+            if (!bar_wait<false>(afull_bar(ab), a_phase, abort_flag, p.status, kDevTimeoutFull)) {
+              ok = false;
+              break;
+            }
+          }
           tc_fence_after();
           const uint32_t a_base = smem0 + stage * Cfg::STAGE_BYTES;
           const uint32_t b_base = a_base + Cfg::A_BYTES;
 #pragma unroll
           for (int j = 0; j < Cfg::BK / Cfg::UK; ++j) {
-            const uint64_t ad = A_MN ? smem_desc_sw128(a_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
-                                     : smem_desc_sw128(a_base + j * Cfg::UK * Cfg::ES, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(b_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
                                      : smem_desc_sw128(b_base + j * Cfg::UK * Cfg::ES, 16, 1024);
-            issue_mma<MODE, MMA2>(d_tmem, ad, bd, IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
+            if constexpr (A_TMEM) {
+              mma_tf32_tmem_a(d_tmem, tmem_base + static_cast<uint32_t>(A_COL0 + ab * Cfg::BK + j * Cfg::UK), bd,
+                              IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
+            } else {
+              const uint64_t ad = A_MN ? smem_desc_sw128(a_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
+                                       : smem_desc_sw128(a_base + j * Cfg::UK * Cfg::ES, 16, 1024);
+              issue_mma<MODE, MMA2>(d_tmem, ad, bd, IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
+            }
+          }
+          if constexpr (A_TMEM) {
+            mma_commit(aempty_bar(ab));  // the A buffer is free once these MMAs are done
+            if (++ab == NA) {
+              ab = 0;
+              a_phase ^= 1u;
+            }
           }
           if constexpr (MMA2)
             mma_commit_pair_multicast(empty_bar(stage), 0x3);  // both CTAs' halves of the stage are free
@@ -413,6 +459,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mma_commit(drain_bar);
       drain_wait(drain_bar, 0, p.status);
     }
+  } else if (A_TMEM && warp < 6) {
+    // ------------------------------------------------------------ A into TMEM
+    // Warp w moves rows 32q..32q+31 (q = w % 4, the TMEM lane quarter it may
+    // access) of each stage's A tile: lane l reads its row's BK values down
+    // the MN-major tile -- 128-byte chunk q of the stage, K row k at k * 128
+    // bytes, 16-byte unit (l / 4) ^ (k % 8), element l % 4: one conflict-free
+    // access of the warp per k -- and stores them as BK columns of lane 32q + l.
+    if constexpr (A_TMEM) {
+      const int q = warp & 3;
+      int stage = 0, ab = 0;
+      uint32_t phase = 0, a_phase = 0;
+      bool ok = true;
+      for (int u = unit0; u < p.num_units && ok; u += unit_step) {
+        const Unit w = decode_unit(u, p);
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          if (!bar_wait<false>(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull) ||
+              !bar_wait<false>(aempty_bar(ab), a_phase ^ 1u, abort_flag, p.status, kDevTimeoutEmpty)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* a_s = smem + stage * Cfg::STAGE_BYTES + q * (Cfg::BK * 128);
+          uint32_t v[Cfg::BK];
+#pragma unroll
+          for (int k = 0; k < Cfg::BK; ++k)
+            v[k] = *reinterpret_cast<const uint32_t*>(a_s + k * 128 + ((((lane >> 2) ^ (k & 7))) << 4) + (lane & 3) * 4);
+          __syncwarp();
+          tmem_st_32x32b_x32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                 static_cast<uint32_t>(A_COL0 + ab * Cfg::BK),
+                             v);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(afull_bar(ab));
+            mbar_arrive(empty_bar(stage));  // this warp's reads of the stage are done
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++ab == NA) {
+            ab = 0;
+            a_phase ^= 1u;
+          }
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int sub = warp & 3;          // TMEM lane quarter this warp may access
@@ -437,9 +531,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool vec_ok = !TRANS_C && (partial || p.c_vec);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
       constexpr int NCH = BN / CW;  // column chunks of a tile
-      // Warps of half 0 take the first ceil(NCH / 2) chunks, half 1 the rest.
-      const int cc_begin = (half == 0) ? 0 : (NCH + 1) / 2;
-      const int cc_end = (half == 0) ? (NCH + 1) / 2 : NCH;
+      // Warps of half 0 take the first ceil(NCH / 2) chunks, half 1 the rest
+      // (A_TMEM: the four epilogue warps take all of them).
+      const int cc_begin = (A_TMEM || half == 0) ? 0 : (NCH + 1) / 2;
+      const int cc_end = (!A_TMEM && half == 0) ? (NCH + 1) / 2 : NCH;
 #pragma unroll 1
       for (int cc = cc_begin; cc < cc_end; ++cc) {
         uint32_t r[CW];
@@ -551,7 +646,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if constexpr (MMA2)
       tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
     else
-      tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 

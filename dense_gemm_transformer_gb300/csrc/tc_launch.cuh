@@ -43,7 +43,9 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
 }
 
 // Which operand layouts a tile width can take.  kind::tf32 reads K-major
-// operands only (the planner transposes MN-major TF32 operands first); an
+// operands only from shared memory: the planner transposes an MN-major TF32
+// B first, and an MN-major TF32 A too unless the 128-column, one-CTA kernel
+// takes it through TMEM; an
 // MN-major B is loaded in 128-byte column chunks, so its tile width must be
 // a whole number of chunks, and an even number when a pair of CTAs loads
 // one half each.
@@ -56,6 +58,10 @@ template <int MODE, int BN, bool PAIR, bool MMA2 = false>
 cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                          const CUtensorMap& tw, const TcParams& p, int grid, cudaStream_t s) {
   if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN, false, PAIR, MMA2>(ta, tb, tc, tw, p, grid, s);
+  if constexpr (MODE == 1 && BN == 128 && !PAIR && !MMA2) {
+    // an MN-major TF32 A goes to the MMA through TMEM
+    if (a_mn && !b_mn) return tc_launch_one<1, true, false, 128>(ta, tb, tc, tw, p, grid, s);
+  }
   if constexpr (MODE == 2) {
     if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN, false, PAIR, MMA2>(ta, tb, tc, tw, p, grid, s);
     if constexpr (tc_mn_b_ok<MODE, BN, PAIR>()) {

@@ -79,7 +79,9 @@ typedef enum {
                             for pairs, 192 need a K-major B in BF16); SIMT: 128 or 256    */
   GEMM_OPT_PRETRANSPOSE = 4, /* SIMT: 0 = planner's choice (K-contiguous operands transposed,
                                 misaligned ones re-packed into the workspace first), 1 = never
-                                (operands read in place), 2 = always transpose              */
+                                (operands read in place), 2 = always transpose.  TF32: 2 also
+                                transposes an MN-major A that the 128-column kernel would
+                                otherwise move into TMEM itself (0 and 1: it does)          */
   GEMM_OPT_PAIR = 5          /* TC: two-CTA clusters (tiles of 192 or more columns, two or more
                                 rows of tiles).  0 = planner's choice (256 columns: one 256-row
                                 MMA per pair, tcgen05 cta_group::2; 192/224: pairs sharing B by

@@ -244,6 +244,27 @@ def test_fp32_k_contiguous_a_transposed_in_kernel(h, tile_n, pre, M, N, K):
     assert np.array_equal(C.cpu().numpy().astype(np.float64), ref), "not bit-exact"
 
 
+@pytest.mark.parametrize("pre", [0, 2])
+@pytest.mark.parametrize("M,N,K,splits", [(384, 1152, 4096, 0), (300, 260, 1000, 0), (129, 130, 70, 0),
+                                          (1000, 384, 2048, 3), (256, 300, 16384, 0)])
+def test_tf32_mn_major_a_through_tmem(h, pre, M, N, K, splits):
+    """TF32 with A stored K x M (MN-major) on 128-column tiles: the kernel
+    moves each stage of A into TMEM and the MMA reads it there (pre = 0), or
+    the planner transposes A into the workspace first (pre = 2).  Ragged
+    M, N and K, split-K and deep K."""
+    h.set_option("tile_n", 128)
+    h.set_option("pretranspose", pre)
+    if splits:
+        h.set_option("split_k", splits)
+    rows = _cases.sample_rows(M) if M * N * K > 2e9 else None
+    _cases.run_and_check(h, "tf32", M, N, K, True, False, alpha=0.75, beta=0.5, seed=91, dist="normal", rows=rows)
+    plan = h.plan()
+    assert plan["family"] == "tc" and plan["tile_n"] == 128 and plan["cluster"] == 1
+    if M % 4 == 0:  # A rows 16-byte aligned: read in place (N < 1536) unless asked to transpose
+        assert plan["packed"] & 1 == (0 if pre == 0 and N < 1536 else 1)
+    _cases.run_and_check(h, "tf32", M, N, min(K, 1024), True, False, seed=92, dist="int", exact=True)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_many_tiles_persistent_loop(h, mode):
     # More tiles than SMs: every CTA of the persistent grid loops over several
