@@ -88,6 +88,28 @@ typedef enum {
                                 multicast), 1 = never, 2 = multicast pairs only, 3 = as 0     */
 } gemm_option_t;
 
+/* Elementwise work fused into the GEMM's epilogue (gemm_run_epilogue), the
+ * variants a transformer layer's projections need ("bare-metal-bard", second
+ * paragraph: a GPT whose every matmul, GELU and layernorm kernel is written
+ * from scratch).  GELU is the function's definition, x * Phi(x) with the
+ * exact error function (the page names GELU without a variant). */
+typedef enum {
+  GEMM_ACT_NONE = 0,  /* C = alpha*op(A)*op(B) + beta*C + bias                          */
+  GEMM_ACT_GELU = 1,  /* C = GELU(alpha*op(A)*op(B) + beta*C + bias): a forward layer     */
+  GEMM_ACT_DGELU = 2  /* C = (alpha*op(A)*op(B) + beta*C) * GELU'(Z): the gradient through
+                         a GELU whose input Z (M x N) was kept from the forward pass      */
+} gemm_activation_t;
+
+typedef struct {
+  int32_t activation;  /* gemm_activation_t */
+  int32_t reserved;
+  const float* bias;   /* NONE / GELU: N floats added to every row of the result, or NULL;
+                          must be NULL for DGELU. Device memory, 4-byte aligned.          */
+  const float* aux;    /* DGELU: Z, M x N row-major with leading dimension ld_aux (>= N);
+                          ignored otherwise. Device memory, 4-byte aligned.              */
+  int64_t ld_aux;
+} gemm_epilogue_t;
+
 /* What the last successful gemm_run on a handle launched. */
 typedef struct {
   int32_t family;        /* gemm_family_t actually used (0 when nothing was launched) */
@@ -131,6 +153,21 @@ gemm_status_t gemm_run(gemm_handle_t h, int mode, int transA, int transB,
                        int64_t M, int64_t N, int64_t K, float alpha,
                        const void* A, int64_t lda, const void* B, int64_t ldb,
                        float beta, float* C, int64_t ldc, void* stream);
+
+/* gemm_run with the elementwise epilogue `*ep` applied to every element of
+ * the result before it is stored (same kernels and plans; the activation
+ * is applied once, after split-K or stream-K partial sums are added).  The
+ * bias and Z are read, never written; C must not overlap them.  ep == NULL
+ * is gemm_run.  With K == 0 or alpha == 0 the product is zero and the
+ * epilogue still applies to beta*C.  Errors: GEMM_ERR_INVALID_VALUE for an
+ * unknown activation, a bias with DGELU, DGELU without Z or with
+ * ld_aux < N; GEMM_ERR_MISALIGNED for a bias or Z not 4-byte aligned; the
+ * other checks are gemm_run's. */
+gemm_status_t gemm_run_epilogue(gemm_handle_t h, int mode, int transA, int transB,
+                                int64_t M, int64_t N, int64_t K, float alpha,
+                                const void* A, int64_t lda, const void* B, int64_t ldb,
+                                float beta, float* C, int64_t ldc,
+                                const gemm_epilogue_t* ep, void* stream);
 
 /* The argument checks gemm_run performs, without a handle or a device.
  * Returns GEMM_OK or the status gemm_run would return for these arguments

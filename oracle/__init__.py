@@ -63,6 +63,12 @@ def _load():
         lib.oracle_tf32_array.argtypes = [ctypes.c_int, p, p, i64]
         lib.oracle_bf16_array.restype = None
         lib.oracle_bf16_array.argtypes = [p, p, i64]
+        lib.oracle_gelu.restype = d
+        lib.oracle_gelu.argtypes = [d]
+        lib.oracle_dgelu.restype = d
+        lib.oracle_dgelu.argtypes = [d]
+        lib.oracle_epilogue.restype = ctypes.c_int
+        lib.oracle_epilogue.argtypes = [ctypes.c_int, i64, i64, p, i64, p, p, i64, p, i64]
         _lib = lib
     return _lib
 
@@ -137,4 +143,41 @@ def bf16_to_f64(bits):
     bits = np.ascontiguousarray(bits, dtype=np.uint16)
     out = np.empty(bits.shape, dtype=np.float64)
     lib.oracle_bf16_array(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+ACTIVATIONS = {"none": 0, "gelu": 1, "dgelu": 2}
+
+
+def gelu(x: float) -> float:
+    """GELU(x) = x * Phi(x), Phi the standard normal distribution function."""
+    return _load().oracle_gelu(float(x))
+
+
+def dgelu(x: float) -> float:
+    """GELU'(x) = Phi(x) + x * phi(x)."""
+    return _load().oracle_dgelu(float(x))
+
+
+def epilogue(act, Y, bias=None, Z=None):
+    """The fused epilogue of gemm_run_epilogue applied to the exact
+    pre-activation Y (float64 rows x N, e.g. from gemm()):
+    none: Y + bias; gelu: GELU(Y + bias); dgelu: Y * GELU'(Z).
+    bias: float32 vector of N (or None); Z: float32 rows x N."""
+    lib = _load()
+    Y = np.ascontiguousarray(Y, dtype=np.float64)
+    rows, N = Y.shape
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+        if bias.shape != (N,):
+            raise ValueError("bias must have N elements")
+    if Z is not None:
+        Z = np.ascontiguousarray(Z, dtype=np.float32)
+        if Z.shape != (rows, N):
+            raise ValueError("Z must be rows x N")
+    out = np.empty_like(Y)
+    rc = lib.oracle_epilogue(ACTIVATIONS[act], rows, N, _ptr(Y), max(N, 1), _ptr(bias), _ptr(Z), max(N, 1),
+                             _ptr(out), max(N, 1))
+    if rc != 0:
+        raise ValueError(f"oracle_epilogue rejected its arguments ({rc})")
     return out

@@ -140,3 +140,47 @@ int oracle_gemm(int mode, int tf32_rule, int transA, int transB,
   }
   return 0;
 }
+
+/*
+ * The fused epilogue of gemm_run_epilogue, in double, applied to the exact
+ * pre-activation Y[i][j] = alpha * sum_k opA*opB + beta * Cin (as returned by
+ * oracle_gemm) for a block of rows:
+ *
+ *   act 0:  out = Y + bias[j]
+ *   act 1:  out = GELU(Y + bias[j])
+ *   act 2:  out = Y * GELU'(Z[i][j])
+ *
+ * "bare-metal-bard" (second paragraph) trains a GPT whose GELU kernel is
+ * written by hand; it does not say which GELU.  The reading taken is the
+ * function's definition, GELU(x) = x * Phi(x) with Phi the standard normal
+ * distribution function, Phi(x) = (1 + erf(x / sqrt 2)) / 2, and its
+ * derivative GELU'(x) = Phi(x) + x * phi(x), phi(x) = exp(-x^2 / 2) / sqrt(2 pi).
+ * bias may be NULL (no bias); Z is read only for act 2.
+ */
+double oracle_gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+
+double oracle_dgelu(double x) {
+  const double Phi = 0.5 * (1.0 + erf(x / sqrt(2.0)));
+  const double phi = exp(-0.5 * x * x) / sqrt(2.0 * 3.14159265358979323846);
+  return Phi + x * phi;
+}
+
+int oracle_epilogue(int act, int64_t rows, int64_t N, const double* y, int64_t ldy, const float* bias,
+                    const float* z, int64_t ldz, double* out, int64_t ldo) {
+  if (act < 0 || act > 2 || rows < 0 || N < 0) return 1;
+  if (act == 2 && (z == 0 || bias != 0)) return 2;
+  for (int64_t i = 0; i < rows; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      const double v = y[i * ldy + j];
+      double r;
+      if (act == 2) {
+        r = v * oracle_dgelu((double)z[i * ldz + j]);
+      } else {
+        const double pre = v + (bias ? (double)bias[j] : 0.0);
+        r = (act == 1) ? oracle_gelu(pre) : pre;
+      }
+      out[i * ldo + j] = r;
+    }
+  }
+  return 0;
+}

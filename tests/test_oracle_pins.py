@@ -297,3 +297,53 @@ def test_gate_rejects_one_dropped_term():
     with pytest.raises(AssertionError):
         _gate.assert_within("bf16", flipped, ref, D)
     _gate.assert_within("fp32", ref.astype(np.float32), ref, D)
+
+
+# ------------------------------------------------------------ fused epilogue
+# Standard normal distribution function Phi at 1, 2 and -1 as tabulated
+# (Abramowitz and Stegun, table 26.1, to 10 digits).  GELU(x) = x * Phi(x).
+PHI_TABLE = {1.0: 0.8413447461, 2.0: 0.9772498681, -1.0: 0.1586552539}
+
+
+def test_gelu_matches_the_tabulated_normal_distribution():
+    """Pins GELU to x * Phi(x) with the exact Phi: the tanh approximation
+    differs by 1.5e-4 at x = 1, a sign or factor error by far more."""
+    for x, phi in PHI_TABLE.items():
+        assert abs(oracle.gelu(x) - x * phi) < 1e-9, x
+    assert oracle.gelu(0.0) == 0.0
+
+
+def test_gelu_odd_part_is_the_identity():
+    """GELU(x) - GELU(-x) = x (Phi(x) + Phi(-x) = 1), at any x."""
+    for x in (0.1, 0.5, 1.7, 3.0, 6.0):
+        assert abs(oracle.gelu(x) - oracle.gelu(-x) - x) < 1e-12 * max(1.0, x)
+
+
+def test_dgelu_is_the_derivative_of_gelu():
+    """GELU' against a central difference of GELU (brute force), and its
+    limits: 1/2 at 0, 1 far right, 0 far left."""
+    h = 1e-5
+    for x in (-3.0, -1.2, -0.3, 0.0, 0.4, 1.0, 2.5):
+        fd = (oracle.gelu(x + h) - oracle.gelu(x - h)) / (2 * h)
+        assert abs(fd - oracle.dgelu(x)) < 1e-8, x
+    assert oracle.dgelu(0.0) == 0.5
+    assert abs(oracle.dgelu(12.0) - 1.0) < 1e-12 and abs(oracle.dgelu(-12.0)) < 1e-12
+
+
+def test_epilogue_variants_elementwise():
+    """none adds the bias to every row; gelu applies GELU after the bias;
+    dgelu multiplies by GELU'(Z) and takes no bias."""
+    Y = np.array([[0.5, -1.0, 2.0], [0.0, 1.0, -2.0]])
+    bias = np.array([0.5, 0.0, -1.0], dtype=np.float32)
+    Z = np.array([[1.0, -1.0, 0.0], [2.0, 0.0, -3.0]], dtype=np.float32)
+    assert np.array_equal(oracle.epilogue("none", Y, bias), Y + bias.astype(np.float64))
+    assert np.array_equal(oracle.epilogue("none", Y), Y)
+    g = oracle.epilogue("gelu", Y, bias)
+    assert abs(g[0, 0] - 1.0 * PHI_TABLE[1.0]) < 1e-9 and abs(g[0, 1] + PHI_TABLE[-1.0]) < 1e-9
+    assert abs(g[0, 2] - PHI_TABLE[1.0]) < 1e-9 and abs(g[1, 1] - PHI_TABLE[1.0]) < 1e-9
+    d = oracle.epilogue("dgelu", Y, Z=Z)
+    for i in range(2):
+        for j in range(3):
+            assert d[i, j] == Y[i, j] * oracle.dgelu(float(Z[i, j]))
+    with pytest.raises(ValueError):
+        oracle.epilogue("dgelu", Y, bias, Z)
