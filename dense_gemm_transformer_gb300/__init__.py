@@ -34,6 +34,15 @@ class GemmError(RuntimeError):
         super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
 
 
+ACTIVATIONS = {"none": 0, "gelu": 1, "dgelu": 2}
+
+
+class Epilogue(ctypes.Structure):
+    """gemm_epilogue_t."""
+    _fields_ = [("activation", ctypes.c_int32), ("reserved", ctypes.c_int32), ("bias", ctypes.c_void_p),
+                ("aux", ctypes.c_void_p), ("ld_aux", ctypes.c_int64)]
+
+
 class Plan(ctypes.Structure):
     _fields_ = [("family", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
                 ("tile_k", ctypes.c_int32), ("split_k", ctypes.c_int32), ("stages", ctypes.c_int32),
@@ -72,10 +81,12 @@ def load(build_if_missing: bool = False):
         lib.gemm_get_plan.argtypes = [vp, ctypes.POINTER(Plan)]
         lib.gemm_check_device.argtypes = [vp, vp]
         lib.gemm_launch_null.argtypes = [vp, vp]
+        lib.gemm_run_epilogue.argtypes = [vp, i32, i32, i32, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64,
+                                          ctypes.POINTER(Epilogue), vp]
         lib.gemm_status_string.argtypes = [i32]
         lib.gemm_status_string.restype = ctypes.c_char_p
         for name in ("gemm_create", "gemm_destroy", "gemm_run", "gemm_validate", "gemm_set_option",
-                     "gemm_get_plan", "gemm_check_device", "gemm_launch_null"):
+                     "gemm_get_plan", "gemm_check_device", "gemm_launch_null", "gemm_run_epilogue"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -168,8 +179,15 @@ class Gemm:
                                 float(beta), C, int(ldc), _stream_ptr(stream))
         _check(st, "gemm_run")
 
-    def run(self, A, B, C, mode="fp32", transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
-        """C = alpha * op(A) op(B) + beta * C on torch CUDA tensors (row-major)."""
+    def run(self, A, B, C, mode="fp32", transA=False, transB=False, alpha=1.0, beta=0.0, stream=None,
+            act="none", bias=None, aux=None):
+        """C = alpha * op(A) op(B) + beta * C on torch CUDA tensors (row-major).
+
+        With act / bias / aux, the fused epilogue of gemm_run_epilogue:
+        act "none" or "gelu": C = act(alpha op(A) op(B) + beta C + bias) with
+        bias a float32 vector of N (or None); act "dgelu": C = (alpha op(A)
+        op(B) + beta C) * GELU'(aux), aux the float32 M x N pre-activation.
+        """
         import torch
         want = torch.bfloat16 if mode == "bf16" else torch.float32
         if A.dtype != want or B.dtype != want:
@@ -185,7 +203,22 @@ class Gemm:
         pc, ldc = _matrix(C, "C")
         if stream is None:
             stream = torch.cuda.current_stream(C.device)
-        self.run_ptr(mode, transA, transB, M, N, K, alpha, pa, lda, pb, ldb, beta, pc, ldc, stream)
+        if act == "none" and bias is None and aux is None:
+            self.run_ptr(mode, transA, transB, M, N, K, alpha, pa, lda, pb, ldb, beta, pc, ldc, stream)
+            return C
+        ep = Epilogue(ACTIVATIONS[act], 0, None, None, 0)
+        if bias is not None:
+            if bias.dtype != torch.float32 or bias.dim() != 1 or bias.numel() != N or bias.stride(0) != 1:
+                raise ValueError("bias must be a contiguous float32 vector of N elements")
+            ep.bias = bias.data_ptr()
+        if aux is not None:
+            if aux.dtype != torch.float32 or tuple(aux.shape) != (M, N):
+                raise ValueError("aux must be float32 M x N")
+            ep.aux, ep.ld_aux = _matrix(aux, "aux")
+        st = self._lib.gemm_run_epilogue(self._h, MODES[mode], int(transA), int(transB), int(M), int(N), int(K),
+                                         float(alpha), pa, int(lda), pb, int(ldb), float(beta), pc, int(ldc),
+                                         ctypes.byref(ep), _stream_ptr(stream))
+        _check(st, "gemm_run_epilogue")
         return C
 
 
@@ -208,9 +241,11 @@ def default_handle() -> Gemm:
     return _default[dev]
 
 
-def gemm(A, B, C, mode="fp32", transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
-    """C = alpha * op(A) op(B) + beta * C with the current device's default handle."""
-    return default_handle().run(A, B, C, mode, transA, transB, alpha, beta, stream)
+def gemm(A, B, C, mode="fp32", transA=False, transB=False, alpha=1.0, beta=0.0, stream=None, act="none",
+         bias=None, aux=None):
+    """C = alpha * op(A) op(B) + beta * C with the current device's default handle
+    (and the fused epilogue of Gemm.run when act / bias / aux are given)."""
+    return default_handle().run(A, B, C, mode, transA, transB, alpha, beta, stream, act, bias, aux)
 
 
 def run_small_m_noalloc(A, B, C, mode="bf16", transB=False, alpha=1.0, beta=0.0, stream=None):

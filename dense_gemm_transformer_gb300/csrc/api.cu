@@ -120,7 +120,7 @@ double wave_eff(int64_t tiles, int64_t slots) {
 
 gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                        const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
-                       cudaStream_t s) {
+                       const dgt::EpiParams& epi, cudaStream_t s) {
   using namespace dgt;
   const int64_t kt = ceil_div(K, kSimtTileK);
   // Tile width: the 256-column kernel (one CTA per SM, half the shared-memory
@@ -173,6 +173,7 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   a.alpha = alpha;
   a.beta = beta;
   a.tile_n = tile_n;
+  a.epi = epi;
   a.ws_ld = round_up(N, 4);
   a.splits = 1;
   a.k_per_split = K;
@@ -259,7 +260,7 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   }
   if (launch_simt(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
   if (a.schedule == kSimtSplitK) {
-    if (launch_splitk_reduce(M, N, a.splits, a.ws, a.ws_ld, C, ldc, alpha, beta, s) != cudaSuccess)
+    if (launch_splitk_reduce(M, N, a.splits, a.ws, a.ws_ld, C, ldc, alpha, beta, epi, 0, s) != cudaSuccess)
       return GEMM_ERR_CUDA;
     ++kernels;
   }
@@ -377,7 +378,7 @@ int64_t skinny_cluster_size(gemm_handle_s* h, int mode, bool a_mn, int64_t tiles
 
 gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
                      float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
-                     int64_t ldc, cudaStream_t s, bool swap) {
+                     int64_t ldc, const dgt::EpiParams& epi, cudaStream_t s, bool swap) {
   using namespace dgt;
   const int es = (mode == GEMM_MODE_BF16) ? 2 : 4;
   const int bk = tc_tile_k(mode);
@@ -552,6 +553,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.splits = static_cast<int>(splits);
   a.kb_per_split = static_cast<int>(kb_per);
   a.tma_cache = h->tma_cache;
+  a.epi = epi;  // the caller's coordinates, whichever orientation the kernel computes
   if (cluster_form) {
     a.status = h->d_status;
     a.grid = static_cast<int>(tiles * splits);
@@ -581,7 +583,8 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   if (launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
   ++kernels;
   if (splits > 1) {
-    if (launch_splitk_reduce(M - tail_row0, N, a.splits, a.ws, ws_ld, C + tail_row0 * ldc, ldc, alpha, beta, s) !=
+    if (launch_splitk_reduce(M - tail_row0, N, a.splits, a.ws, ws_ld, C + tail_row0 * ldc, ldc, alpha, beta, epi,
+                             tail_row0, s) !=
         cudaSuccess)
       return GEMM_ERR_CUDA;
     ++kernels;
@@ -597,13 +600,13 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
 // gemm_run after its argument checks.
 gemm_status_t run_checked(gemm_handle_t h, int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
                           float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
-                          int64_t ldc, cudaStream_t s) {
+                          int64_t ldc, const dgt::EpiParams& epi, cudaStream_t s) {
   if (M == 0 || N == 0) {
     set_plan(h, 0, 0, 0, 0, 0, 0, 0, 0, 0);
     return GEMM_OK;
   }
   if (K == 0 || alpha == 0.f) {
-    if (dgt::launch_scale(M, N, C, ldc, beta, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (dgt::launch_scale(M, N, C, ldc, beta, epi, s) != cudaSuccess) return GEMM_ERR_CUDA;
     set_plan(h, 0, 0, 0, 0, 1, 0, 0, 1, 0);
     return GEMM_OK;
   }
@@ -611,7 +614,7 @@ gemm_status_t run_checked(gemm_handle_t h, int mode, int transA, int transB, int
   if (mode == GEMM_MODE_FP32) {
     if (fam != GEMM_FAMILY_AUTO && fam != GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
     return run_simt(h, transA, transB, M, N, K, alpha, static_cast<const float*>(A), lda,
-                    static_cast<const float*>(B), ldb, beta, C, ldc, s);
+                    static_cast<const float*>(B), ldb, beta, C, ldc, epi, s);
   }
   // Small M: the swapped form, which streams the weights through the 128-row
   // MMA side once (activations must be stored M x K).
@@ -619,7 +622,7 @@ gemm_status_t run_checked(gemm_handle_t h, int mode, int transA, int transB, int
   if (fam == GEMM_FAMILY_SKINNY && !skinny_ok) return GEMM_ERR_NOT_SUPPORTED;
   if (fam == GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
   const bool swap = (fam == GEMM_FAMILY_SKINNY) || (fam == GEMM_FAMILY_AUTO && skinny_ok);
-  return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, s, swap);
+  return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, s, swap);
 }
 
 }  // namespace
@@ -693,7 +696,34 @@ gemm_status_t gemm_run(gemm_handle_t h, int mode, int transA, int transB, int64_
   gemm_status_t st = check_args(mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc);
   if (st != GEMM_OK) return st;
   dgt::last_main_launch().valid = false;
-  st = run_checked(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+  st = run_checked(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dgt::EpiParams{},
+                   static_cast<cudaStream_t>(stream));
+  if (st == GEMM_OK) h->null_shape = dgt::last_main_launch();
+  return st;
+}
+
+gemm_status_t gemm_run_epilogue(gemm_handle_t h, int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta,
+                                float* C, int64_t ldc, const gemm_epilogue_t* ep, void* stream) {
+  if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
+  gemm_status_t st = check_args(mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, C, ldc);
+  if (st != GEMM_OK) return st;
+  dgt::EpiParams epi;
+  if (ep != nullptr) {
+    if (ep->activation < GEMM_ACT_NONE || ep->activation > GEMM_ACT_DGELU) return GEMM_ERR_INVALID_VALUE;
+    if (ep->activation == GEMM_ACT_DGELU) {
+      if (ep->bias != nullptr || ep->aux == nullptr || ep->ld_aux < std::max<int64_t>(N, 1))
+        return GEMM_ERR_INVALID_VALUE;
+      if (!aligned(ep->aux, 4)) return GEMM_ERR_MISALIGNED;
+      epi.aux = ep->aux;
+      epi.ld_aux = ep->ld_aux;
+    }
+    if (ep->bias != nullptr && !aligned(ep->bias, 4)) return GEMM_ERR_MISALIGNED;
+    epi.act = ep->activation;
+    epi.bias = ep->bias;
+  }
+  dgt::last_main_launch().valid = false;
+  st = run_checked(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi,
                    static_cast<cudaStream_t>(stream));
   if (st == GEMM_OK) h->null_shape = dgt::last_main_launch();
   return st;

@@ -10,6 +10,7 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -31,7 +32,8 @@ int grid_for(int64_t work, int threads) {
 // aligned (ws_ld % 4 == 0), C is read/written by float4 only when CVEC.
 template <bool CVEC>
 __global__ void splitk_reduce_kernel(int64_t M, int64_t N, int splits, const float* __restrict__ ws, int64_t ws_ld,
-                                     float* __restrict__ C, int64_t ldc, float alpha, float beta) {
+                                     float* __restrict__ C, int64_t ldc, float alpha, float beta, EpiParams epi,
+                                     int64_t row0) {
   grid_dep_wait();
   grid_dep_launch();
   const int64_t groups = (N + 3) / 4;
@@ -63,6 +65,7 @@ __global__ void splitk_reduce_kernel(int64_t M, int64_t N, int splits, const flo
     }
     float v[4] = {alpha * s.x, alpha * s.y, alpha * s.z, alpha * s.w};
     float* dst = C + r * ldc + c;
+    const bool epi_on = epilogue_active(epi);
     if (CVEC && c + 3 < N) {
       float4* d4 = reinterpret_cast<float4*>(dst);
       if (beta != 0.f) {
@@ -72,14 +75,22 @@ __global__ void splitk_reduce_kernel(int64_t M, int64_t N, int splits, const flo
         v[2] = fmaf(beta, old.z, v[2]);
         v[3] = fmaf(beta, old.w, v[3]);
       }
+      if (epi_on) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = apply_epilogue(epi, v[j], row0 + r, c + j);
+      }
       *d4 = make_float4(v[0], v[1], v[2], v[3]);
     } else {
-      for (int j = 0; j < 4 && c + j < N; ++j) dst[j] = (beta != 0.f) ? fmaf(beta, dst[j], v[j]) : v[j];
+      for (int j = 0; j < 4 && c + j < N; ++j) {
+        float o = (beta != 0.f) ? fmaf(beta, dst[j], v[j]) : v[j];
+        if (epi_on) o = apply_epilogue(epi, o, row0 + r, c + j);
+        dst[j] = o;
+      }
     }
   }
 }
 
-__global__ void scale_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_t ldc, float beta) {
+__global__ void scale_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_t ldc, float beta, EpiParams epi) {
   grid_dep_wait();
   grid_dep_launch();
   const int64_t total = M * N;
@@ -87,7 +98,8 @@ __global__ void scale_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_
        g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = g / N, c = g % N;
     float* p = C + r * ldc + c;
-    *p = (beta != 0.f) ? beta * *p : 0.f;
+    const float v = (beta != 0.f) ? beta * *p : 0.f;
+    *p = apply_epilogue(epi, v, r, c);
   }
 }
 
@@ -251,22 +263,24 @@ cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t
 }
 
 cudaError_t launch_splitk_reduce(int64_t M, int64_t N, int splits, const float* ws, int64_t ws_ld, float* C,
-                                 int64_t ldc, float alpha, float beta, cudaStream_t stream) {
+                                 int64_t ldc, float alpha, float beta, const EpiParams& epi, int64_t row0,
+                                 cudaStream_t stream) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   const int threads = 256;
   const dim3 blocks(grid_for(M * ((N + 3) / 4), threads));
   const bool cvec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && (ldc % 4 == 0);
   if (cvec)
     return launch_pdl(splitk_reduce_kernel<true>, blocks, dim3(threads), 0, stream, M, N, splits, ws, ws_ld, C, ldc,
-                      alpha, beta);
+                      alpha, beta, epi, row0);
   return launch_pdl(splitk_reduce_kernel<false>, blocks, dim3(threads), 0, stream, M, N, splits, ws, ws_ld, C, ldc,
-                    alpha, beta);
+                    alpha, beta, epi, row0);
 }
 
-cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta, cudaStream_t stream) {
+cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta, const EpiParams& epi,
+                         cudaStream_t stream) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   const int threads = 256;
-  return launch_pdl(scale_kernel, dim3(grid_for(M * N, threads)), dim3(threads), 0, stream, M, N, C, ldc, beta);
+  return launch_pdl(scale_kernel, dim3(grid_for(M * N, threads)), dim3(threads), 0, stream, M, N, C, ldc, beta, epi);
 }
 
 cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,

@@ -58,6 +58,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// The elementwise epilogue of gemm_run_epilogue (activation as
+// gemm_activation_t): applied to alpha * product + beta * C at the final
+// store of each element, in the caller's (row, column) coordinates.
+enum { kActNone = 0, kActGelu = 1, kActDGelu = 2 };
+struct EpiParams {
+  int act = kActNone;
+  const float* bias = nullptr;  // N floats, or null
+  const float* aux = nullptr;   // DGELU: the M x N pre-activation
+  int64_t ld_aux = 0;
+};
+
 // The launch configuration of the main GEMM kernel most recently launched
 // from this host thread (the SIMT, tcgen05 or small-M kernel of a call, not
 // its transposes, re-packs or reductions).
@@ -103,6 +114,7 @@ struct SimtArgs {
   int64_t grid;
   float* ws;
   int64_t ws_ld;
+  EpiParams epi;
 };
 constexpr int kSimtTileM = 128, kSimtTileN = 128, kSimtTileK = 16, kSimtThreads = 256;
 int64_t simt_streamk_slot_floats(int tile_n);  // floats per stream-K partial slot
@@ -139,6 +151,7 @@ struct TcArgs {
   int grid;              // persistent CTAs
   int group_m;           // raster group height in M tiles
   TmaCache* tma_cache;   // the handle's descriptor cache (null: encode every call)
+  EpiParams epi;         // in the caller's coordinates (C^T's transposes for the swapped form)
 };
 // tile_n == 16 selects the swapped small-M form: the caller passes the
 // operands exchanged (C^T = op(B)^T op(A)^T, M and N exchanged) and the
@@ -159,11 +172,15 @@ cudaError_t launch_skinny(const TcArgs& a, cudaStream_t stream);
 cudaError_t tc_init_driver();         // resolves cuTensorMapEncodeTiled once
 
 // ---------------------------------------------------------------- helpers
-// C = alpha * sum_s ws[s] + beta * C over an M x N matrix (s ascending).
+// C = epi(alpha * sum_s ws[s] + beta * C) over an M x N matrix (s
+// ascending); row0 is the caller's row of the matrix's first row (for the
+// epilogue's Z).
 cudaError_t launch_splitk_reduce(int64_t M, int64_t N, int splits, const float* ws, int64_t ws_ld,
-                                 float* C, int64_t ldc, float alpha, float beta, cudaStream_t stream);
-// C = beta * C (beta == 0 writes zeros without reading C).
-cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta, cudaStream_t stream);
+                                 float* C, int64_t ldc, float alpha, float beta, const EpiParams& epi, int64_t row0,
+                                 cudaStream_t stream);
+// C = epi(beta * C) (beta == 0 writes epi(0) without reading C).
+cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta, const EpiParams& epi,
+                         cudaStream_t stream);
 // Copy a rows x cols matrix of elem_bytes-sized elements to dst with a new
 // leading dimension (elements).
 cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,

@@ -116,7 +116,8 @@ extern "C" gemm_status_t gemm_run_small_m_noalloc(int mode, int transB, int64_t 
   if (st != GEMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M == 0 || N == 0) return GEMM_OK;
-  if (K == 0 || alpha == 0.f) return dgt::launch_scale(M, N, C, ldc, beta, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  if (K == 0 || alpha == 0.f)
+    return dgt::launch_scale(M, N, C, ldc, beta, dgt::EpiParams{}, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 
   // Both operands must be readable in place by the TMA unit: nothing is
   // re-packed here.  kind::tf32 takes K-major operands only, so TF32 weights
@@ -169,7 +170,8 @@ extern "C" gemm_status_t gemm_run_small_m_noalloc(int mode, int transB, int64_t 
   a.grid = static_cast<int>(std::min<int64_t>(tiles * splits, d.sms));
   a.group_m = 16;
   if (dgt::launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
-  if (splits > 1 && dgt::launch_splitk_reduce(M, N, a.splits, a.ws, ws_ld, C, ldc, alpha, beta, s) != cudaSuccess)
+  if (splits > 1 &&
+      dgt::launch_splitk_reduce(M, N, a.splits, a.ws, ws_ld, C, ldc, alpha, beta, dgt::EpiParams{}, 0, s) != cudaSuccess)
     return GEMM_ERR_CUDA;
   return GEMM_OK;
 }

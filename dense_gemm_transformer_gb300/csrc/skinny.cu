@@ -35,6 +35,7 @@
 // never arrive gives up its receive wait the same way.
 #include "skinny.cuh"
 
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
             float* dst = p.C + static_cast<int64_t>(j) * p.ldc + row;
             float out = p.alpha * v[j];
             if (p.beta != 0.f) out = fmaf(p.beta, *dst, out);
-            *dst = out;
+            *dst = apply_epilogue(p.epi, out, j, row);  // caller's element (j, row)
           }
         }
       }
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
             if (row + i < p.M) {
               float out = p.alpha * sum[i];
               if (p.beta != 0.f) out = fmaf(p.beta, dst[i], out);
-              dst[i] = out;
+              dst[i] = apply_epilogue(p.epi, out, col, row + i);  // caller's element (col, row + i)
             }
           }
         }
