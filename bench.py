@@ -698,6 +698,87 @@ def merge_process_runs(runs):
     return shapes
 
 
+def bench_epilogue(args):
+    """The fused epilogue on the GPT products that carry one: the MLP-up
+    forward with bias + GELU (C = GELU(X W + b)) and the MLP-down dX with
+    GELU' (dH = (dY W^T) * GELU'(Z), Z the kept pre-activation), in FP32 and
+    TF32.  Each is timed as the plain GEMM and as the fused call (median of 5
+    samples of >= 20 ms, operands rotated over > 3x L2); "pass_ms" is what a
+    separate elementwise pass would take at the measured HBM bandwidth
+    (read and write C, and read Z for GELU'), the least the unfused form
+    adds."""
+    import dense_gemm_transformer_gb300 as dg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dg.load(build_if_missing=True)
+    h = dg.Gemm()
+    stream = torch.cuda.Stream(dev)
+    pk = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    T, D, F = si.GPT_TOKENS, 384, 1536
+    shapes = []
+    with ClockSampler(dev.index) as clk:
+        for mode in ("fp32", "tf32"):
+            for name, M, N, K, tB, act in (("mlp_up.fwd+bias+gelu", T, F, D, False, "gelu"),
+                                           ("mlp_down.dX*dgelu", T, F, D, True, "dgelu")):
+                g = torch.Generator(device="cpu")
+                g.manual_seed(si.BASE_SEED)
+                per_set = 4 * (M * K + K * N + M * N * (2 if act == "dgelu" else 1))
+                copies = max(1, min(8, -(-3 * l2 // per_set)))
+                sets = []
+                for _ in range(copies):
+                    A = torch.randn((M, K), generator=g).to(dev)
+                    B = (torch.randn((N, K) if tB else (K, N), generator=g) * 0.02).to(dev)
+                    C = torch.empty((M, N), device=dev)
+                    Z = torch.randn((M, N), generator=g).to(dev) if act == "dgelu" else None
+                    sets.append((A, B, C, Z))
+                bias = (torch.randn((N,), generator=g) * 0.02).to(dev) if act == "gelu" else None
+
+                def plain(r):
+                    A, B, C, _ = sets[r % copies]
+                    h.run(A, B, C, mode=mode, transB=tB, stream=stream)
+
+                def fused(r):
+                    A, B, C, Z = sets[r % copies]
+                    h.run(A, B, C, mode=mode, transB=tB, stream=stream, act=act, bias=bias, aux=Z)
+
+                res = {}
+                for label, fn in (("plain", plain), ("fused", fused)):
+                    with torch.cuda.stream(stream):
+                        for r in range(copies):
+                            fn(r)
+                    stream.synchronize()
+                    t_est = _timed_back_to_back(fn, max(2 * copies, 10), stream, 300)
+                    reps = int(min(MAX_REPS, max(10, math.ceil(SAMPLE_MS / max(t_est, 1e-4)))))
+                    res[label] = _stats([_timed_back_to_back(fn, reps, stream, 300) for _ in range(SAMPLES)])
+                assert h.check_device(stream) == 0
+                flops = 2 * M * N * K
+                pass_bytes = 4 * M * N * (3 if act == "dgelu" else 2)
+                pass_ms = pass_bytes / (pk["hbm_gbs"] * 1e9) * 1e3
+                byts = 4 * (M * K + K * N + M * N) + (4 * M * N if act == "dgelu" else 4 * N)
+                peak = pk["fp32_alu_tflops"] if mode == "fp32" else pk["tf32_tflops_sustained"]
+                t_roof = max(flops / (peak * 1e12), byts / (pk["hbm_gbs"] * 1e9))
+                fm = res["fused"]["median"]
+                shapes.append({"gemm": f"{mode}.{name}", "M": M, "N": N, "K": K,
+                               "ms_plain": round(res["plain"]["median"], 5), "ms_fused": round(fm, 5),
+                               "fused_overhead_ms": round(fm - res["plain"]["median"], 5),
+                               "pass_ms": round(pass_ms, 5),
+                               "unfused_floor_ms": round(res["plain"]["median"] + pass_ms, 5),
+                               "tflops_fused": round(flops / (fm * 1e-3) / 1e12, 2),
+                               "roofline_frac_fused": round(t_roof / (fm * 1e-3), 3),
+                               "plan": h.plan()})
+                del sets
+                torch.cuda.empty_cache()
+    h.close()
+    total_flops = sum(2 * x["M"] * x["N"] * x["K"] for x in shapes)
+    line = {"metric": METRIC, "value": total_flops / (sum(x["ms_fused"] for x in shapes) * 1e-3) / 1e12,
+            "unit": "TFLOP/s", "n_gpus": 1, "higher_is_better": True, "dtype": "f32+tf32", "data": "synthetic",
+            "config": {"workload": "epilogue", "l2": "operands rotated over copies > 3x L2",
+                       "samples": f"median of {SAMPLES} samples of >= {SAMPLE_MS:g} ms"},
+            "clocks": clk.summary(), "shapes": shapes, "peaks": pk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -713,7 +794,7 @@ def main():
     ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
     ap.add_argument("--pair", type=int, default=None,
                     help="sweeps: force the CTA-pair form (0 planner, 1 none, 2 multicast B, 3 one 256-row MMA per pair)")
-    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny"],
+    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny", "epilogue"],
                     help="gpt: the timed step; the others print a per-shape sweep")
     ap.add_argument("--processes", type=int, default=3,
                     help="sweeps: separate processes to run the sweep in (median and spread across them)")
@@ -723,6 +804,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         bench_reference(args, world, rank)
+    elif args.workload == "epilogue":
+        bench_epilogue(args)
     elif args.workload != "gpt":
         bench_sweep_processes(args)
     else:

@@ -73,6 +73,8 @@ gemm_status_t check_args(int mode, int transA, int transB, int64_t M, int64_t N,
 
 gemm_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA; }
 
+bool epilogue_active(const dgt::EpiParams& e) { return e.act != dgt::kActNone || e.bias != nullptr; }
+
 // Grow the workspace to at least `bytes`.  Freeing the old block waits for
 // the device, so earlier launches that still use it are finished.
 gemm_status_t ensure_ws(gemm_handle_s* h, size_t bytes) {
@@ -173,7 +175,6 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   a.alpha = alpha;
   a.beta = beta;
   a.tile_n = tile_n;
-  a.epi = epi;
   a.ws_ld = round_up(N, 4);
   a.splits = 1;
   a.k_per_split = K;
@@ -259,9 +260,14 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
     ++kernels;
   }
   if (launch_simt(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  // The epilogue: in the split-K reduction, which writes every element
+  // anyway, or else in one pass over C after the GEMM.
   if (a.schedule == kSimtSplitK) {
     if (launch_splitk_reduce(M, N, a.splits, a.ws, a.ws_ld, C, ldc, alpha, beta, epi, 0, s) != cudaSuccess)
       return GEMM_ERR_CUDA;
+    ++kernels;
+  } else if (epilogue_active(epi)) {
+    if (launch_epilogue(M, N, C, ldc, epi, s) != cudaSuccess) return GEMM_ERR_CUDA;
     ++kernels;
   }
   set_plan(h, GEMM_FAMILY_SIMT, kSimtTileM, tile_n, kSimtTileK, a.splits, tile_n == 256 ? 4 : 3, grid, kernels,
@@ -553,12 +559,15 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.splits = static_cast<int>(splits);
   a.kb_per_split = static_cast<int>(kb_per);
   a.tma_cache = h->tma_cache;
-  a.epi = epi;  // the caller's coordinates, whichever orientation the kernel computes
   if (cluster_form) {
     a.status = h->d_status;
     a.grid = static_cast<int>(tiles * splits);
     if (launch_skinny(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
     ++kernels;
+    if (epilogue_active(epi)) {
+      if (launch_epilogue(M, N, C, ldc, epi, s) != cudaSuccess) return GEMM_ERR_CUDA;
+      ++kernels;
+    }
     set_plan(h, GEMM_FAMILY_SKINNY, 128, 16, bk, a.splits, dgt::kSkinnyStages, a.grid, kernels,
              (pack_b ? 1 : 0) | (pack_a ? 2 : 0));
     h->plan.cluster = a.splits;
@@ -582,11 +591,17 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.group_m = a.pair ? 8 : 16;
   if (launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
   ++kernels;
+  // The epilogue: in the split-K reduction when it writes every element of
+  // C (plain split-K), or else in one pass over C after the GEMM.
+  const bool epi_in_reduce = splits > 1 && tail_row0 == 0;
   if (splits > 1) {
-    if (launch_splitk_reduce(M - tail_row0, N, a.splits, a.ws, ws_ld, C + tail_row0 * ldc, ldc, alpha, beta, epi,
-                             tail_row0, s) !=
-        cudaSuccess)
+    if (launch_splitk_reduce(M - tail_row0, N, a.splits, a.ws, ws_ld, C + tail_row0 * ldc, ldc, alpha, beta,
+                             epi_in_reduce ? epi : dgt::EpiParams{}, tail_row0, s) != cudaSuccess)
       return GEMM_ERR_CUDA;
+    ++kernels;
+  }
+  if (!epi_in_reduce && epilogue_active(epi)) {
+    if (launch_epilogue(M, N, C, ldc, epi, s) != cudaSuccess) return GEMM_ERR_CUDA;
     ++kernels;
   }
   set_plan(h, swap ? GEMM_FAMILY_SKINNY : GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n, a.pair == 2),

@@ -103,6 +103,36 @@ __global__ void scale_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_
   }
 }
 
+// C = epi(C): one thread per 4-column group of a row (16-byte accesses when
+// the row allows), grid-stride; the epilogue's inputs come with the same
+// coalesced pattern (a bias slice, or Z's row).  (Four groups per thread per
+// iteration, for more loads in flight, measured slower: 56 registers halve
+// the resident threads.)
+template <bool CVEC>
+__global__ void epilogue_kernel(int64_t M, int64_t N, float* __restrict__ C, int64_t ldc, EpiParams epi) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int64_t groups = (N + 3) / 4;
+  const int64_t total = M * groups;
+  for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = g / groups, c = (g % groups) * 4;
+    float* dst = C + r * ldc + c;
+    const float4 x = epilogue_fetch4(epi, r, c, N);
+    if (CVEC && c + 3 < N) {
+      float4 v = *reinterpret_cast<float4*>(dst);
+      v.x = epilogue_finish(epi, v.x, x.x);
+      v.y = epilogue_finish(epi, v.y, x.y);
+      v.z = epilogue_finish(epi, v.z, x.z);
+      v.w = epilogue_finish(epi, v.w, x.w);
+      *reinterpret_cast<float4*>(dst) = v;
+    } else {
+      const float xs[4] = {x.x, x.y, x.z, x.w};
+      for (int j = 0; j < 4 && c + j < N; ++j) dst[j] = epilogue_finish(epi, dst[j], xs[j]);
+    }
+  }
+}
+
 template <typename T>
 __global__ void pack_kernel(const T* __restrict__ src, int64_t ld_src, T* __restrict__ dst, int64_t ld_dst,
                             int64_t rows, int64_t cols) {
@@ -281,6 +311,15 @@ cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta
   if (M <= 0 || N <= 0) return cudaSuccess;
   const int threads = 256;
   return launch_pdl(scale_kernel, dim3(grid_for(M * N, threads)), dim3(threads), 0, stream, M, N, C, ldc, beta, epi);
+}
+
+cudaError_t launch_epilogue(int64_t M, int64_t N, float* C, int64_t ldc, const EpiParams& epi, cudaStream_t stream) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  const int threads = 256;
+  const dim3 blocks(grid_for(M * ((N + 3) / 4), threads));
+  const bool cvec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) && (ldc % 4 == 0);
+  if (cvec) return launch_pdl(epilogue_kernel<true>, blocks, dim3(threads), 0, stream, M, N, C, ldc, epi);
+  return launch_pdl(epilogue_kernel<false>, blocks, dim3(threads), 0, stream, M, N, C, ldc, epi);
 }
 
 cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,

@@ -114,7 +114,6 @@ struct SimtArgs {
   int64_t grid;
   float* ws;
   int64_t ws_ld;
-  EpiParams epi;
 };
 constexpr int kSimtTileM = 128, kSimtTileN = 128, kSimtTileK = 16, kSimtThreads = 256;
 int64_t simt_streamk_slot_floats(int tile_n);  // floats per stream-K partial slot
@@ -151,7 +150,6 @@ struct TcArgs {
   int grid;              // persistent CTAs
   int group_m;           // raster group height in M tiles
   TmaCache* tma_cache;   // the handle's descriptor cache (null: encode every call)
-  EpiParams epi;         // in the caller's coordinates (C^T's transposes for the swapped form)
 };
 // tile_n == 16 selects the swapped small-M form: the caller passes the
 // operands exchanged (C^T = op(B)^T op(A)^T, M and N exchanged) and the
@@ -181,6 +179,9 @@ cudaError_t launch_splitk_reduce(int64_t M, int64_t N, int splits, const float* 
 // C = epi(beta * C) (beta == 0 writes epi(0) without reading C).
 cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta, const EpiParams& epi,
                          cudaStream_t stream);
+// C = epi(C) in place over an M x N matrix: the epilogue of a call whose
+// GEMM kernels have stored alpha * product + beta * C.
+cudaError_t launch_epilogue(int64_t M, int64_t N, float* C, int64_t ldc, const EpiParams& epi, cudaStream_t stream);
 // Copy a rows x cols matrix of elem_bytes-sized elements to dst with a new
 // leading dimension (elements).
 cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,

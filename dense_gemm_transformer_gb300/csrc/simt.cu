@@ -34,7 +34,6 @@
 
 #include <type_traits>
 
-#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -453,7 +452,6 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
     float* __restrict__ out = partial ? p.ws + index * p.M * p.ws_ld : p.C;
     const int64_t ldo = partial ? p.ws_ld : p.ldc;
     const bool read_c = !partial && p.beta != 0.f;
-    const bool epi_on = !partial && epilogue_active(p.epi);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int64_t row = em0 + am + (i & 3) + (i >> 2) * 16;
@@ -476,10 +474,6 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
             v[2] = fmaf(p.beta, c.z, v[2]);
             v[3] = fmaf(p.beta, c.w, v[3]);
           }
-          if (epi_on) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = apply_epilogue(p.epi, v[j], row, col + j);
-          }
           *dst = make_float4(v[0], v[1], v[2], v[3]);
         } else {
 #pragma unroll
@@ -487,7 +481,6 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
             if (col + j < p.N) {
               float r = v[j];
               if (read_c) r = fmaf(p.beta, crow[col + j], r);
-              if (epi_on) r = apply_epilogue(p.epi, r, row, col + j);
               crow[col + j] = r;
             }
           }
@@ -563,16 +556,10 @@ __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
     }
     float* crow = p.C + row * p.ldc + n0 + c4;
     const int64_t left = p.N - (n0 + c4);
-    const float s[4] = {sum.x, sum.y, sum.z, sum.w};
-    const bool epi_on = epilogue_active(p.epi);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (left > j) {
-        float o = (p.beta != 0.f) ? fmaf(p.beta, crow[j], p.alpha * s[j]) : p.alpha * s[j];
-        if (epi_on) o = apply_epilogue(p.epi, o, row, n0 + c4 + j);
-        crow[j] = o;
-      }
-    }
+    if (left > 0) crow[0] = (p.beta != 0.f) ? fmaf(p.beta, crow[0], p.alpha * sum.x) : p.alpha * sum.x;
+    if (left > 1) crow[1] = (p.beta != 0.f) ? fmaf(p.beta, crow[1], p.alpha * sum.y) : p.alpha * sum.y;
+    if (left > 2) crow[2] = (p.beta != 0.f) ? fmaf(p.beta, crow[2], p.alpha * sum.z) : p.alpha * sum.z;
+    if (left > 3) crow[3] = (p.beta != 0.f) ? fmaf(p.beta, crow[3], p.alpha * sum.w) : p.alpha * sum.w;
   }
 }
 

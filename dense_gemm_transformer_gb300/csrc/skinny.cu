@@ -35,7 +35,6 @@
 // never arrive gives up its receive wait the same way.
 #include "skinny.cuh"
 
-#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -240,7 +239,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
             float* dst = p.C + static_cast<int64_t>(j) * p.ldc + row;
             float out = p.alpha * v[j];
             if (p.beta != 0.f) out = fmaf(p.beta, *dst, out);
-            *dst = apply_epilogue(p.epi, out, j, row);  // caller's element (j, row)
+            *dst = out;
           }
         }
       }
@@ -296,7 +295,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
             if (row + i < p.M) {
               float out = p.alpha * sum[i];
               if (p.beta != 0.f) out = fmaf(p.beta, dst[i], out);
-              dst[i] = apply_epilogue(p.epi, out, col, row + i);  // caller's element (col, row + i)
+              dst[i] = out;
             }
           }
         }

@@ -6,8 +6,6 @@
 
 #include <cstdint>
 
-#include "kernels.h"
-
 namespace dgt {
 
 // The kernel computes C^T = W^T X^T for C = X W with X of M <= 16 rows: the
@@ -24,7 +22,6 @@ struct SkParams {
   float* C;     // caller's C, element (m, n) at C[m * ldc + n]
   int64_t ldc;
   int* status;  // device status word (bounded waits)
-  EpiParams epi;  // in the caller's coordinates
 };
 
 constexpr int kSkinnyThreads = 192;  // TMA producer warp, MMA warp, four epilogue warps

@@ -46,7 +46,6 @@
 
 #include <cstdint>
 
-#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -74,7 +73,6 @@ struct TcParams {
   int c_vec;  // C rows are 16-byte aligned (ldc % 4 == 0 and C aligned)
   int c_tma;  // whole tiles leave through shared memory and TMA stores (tmC is valid)
   int w_tma;  // partial tiles likewise (tmW is valid)
-  EpiParams epi;  // applied to whole tiles, in the caller's coordinates
 };
 
 // MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands).  BHALF: a
@@ -522,7 +520,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const bool partial = w.partial;
       const bool read_c = !partial && p.beta != 0.f;
-      const bool epi_on = !partial && epilogue_active(p.epi);
       const int tm = tile_row(w);
       const int64_t row = static_cast<int64_t>(tm) * Cfg::BM + sub * 32 + lane;
       const bool row_ok = row < p.M;
@@ -558,14 +555,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float a = partial ? 1.f : p.alpha;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              float v[4];
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                v[c] = a * __uint_as_float(r[4 * q + c]);
-                // (the TMA unit clips rows past M and columns past N: nothing is read for them)
-                if (epi_on && row_ok && col0 + 4 * q + c < p.N) v[c] = apply_epilogue(p.epi, v[c], row, col0 + 4 * q + c);
-              }
-              *reinterpret_cast<float4*>(buf + lane * 128 + ((q ^ (lane & 7)) * 16)) = make_float4(v[0], v[1], v[2], v[3]);
+              float4 v;
+              v.x = a * __uint_as_float(r[4 * q + 0]);
+              v.y = a * __uint_as_float(r[4 * q + 1]);
+              v.z = a * __uint_as_float(r[4 * q + 2]);
+              v.w = a * __uint_as_float(r[4 * q + 3]);
+              *reinterpret_cast<float4*>(buf + lane * 128 + ((q ^ (lane & 7)) * 16)) = v;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -602,13 +597,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               v.z = fmaf(p.beta, c[q].z, v.z);
               v.w = fmaf(p.beta, c[q].w, v.w);
             }
-            if (epi_on) {
-              const int64_t cc4 = col0 + 4 * q;
-              v.x = apply_epilogue(p.epi, v.x, row, cc4 + 0);
-              v.y = apply_epilogue(p.epi, v.y, row, cc4 + 1);
-              v.z = apply_epilogue(p.epi, v.z, row, cc4 + 2);
-              v.w = apply_epilogue(p.epi, v.w, row, cc4 + 3);
-            }
             dst[q] = v;
           }
         } else {
@@ -625,8 +613,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (col0 + j < p.N) {
               float v = a * __uint_as_float(r[j]);
               if (read_c) v = fmaf(p.beta, c[j], v);
-              // TRANS_C: the kernel's row is the caller's column
-              if (epi_on) v = TRANS_C ? apply_epilogue(p.epi, v, col0 + j, wrow) : apply_epilogue(p.epi, v, row, col0 + j);
               *at(j) = v;
             }
           }

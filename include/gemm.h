@@ -155,8 +155,10 @@ gemm_status_t gemm_run(gemm_handle_t h, int mode, int transA, int transB,
                        float beta, float* C, int64_t ldc, void* stream);
 
 /* gemm_run with the elementwise epilogue `*ep` applied to every element of
- * the result before it is stored (same kernels and plans; the activation
- * is applied once, after split-K or stream-K partial sums are added).  The
+ * the result (same GEMM kernels and plans; the activation is applied once,
+ * after split-K or stream-K partial sums are added: inside the split-K
+ * reduction when the call has one that writes all of C, otherwise in one
+ * pass over C right after the GEMM, in the same stream).  The
  * bias and Z are read, never written; C must not overlap them.  ep == NULL
  * is gemm_run.  With K == 0 or alpha == 0 the product is zero and the
  * epilogue still applies to beta*C.  Errors: GEMM_ERR_INVALID_VALUE for an

@@ -1,9 +1,9 @@
-"""The fused epilogue (gemm_run_epilogue) against the oracle: a per-column
-bias, GELU after it, and the product with GELU'(Z) of a kept pre-activation,
-in every kernel family and through every place a result is finished -- the
-kernels' own stores (TMA-staged and direct, transposed for the small-M
-form), the stream-K fixup, the split-K and tail-slice reductions, and the
-beta-only path for K = 0."""
+"""The epilogue (gemm_run_epilogue) against the oracle: a per-column bias,
+GELU after it, and the product with GELU'(Z) of a kept pre-activation, in
+every kernel family and schedule -- applied in the split-K reduction where a
+call ends with one that writes all of C, in the pass over C after the GEMM
+otherwise (whole tiles, stream-K, tail slices, the small-M kernel), and in
+the beta-only path for K = 0."""
 import numpy as np
 import pytest
 import torch
