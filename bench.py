@@ -779,6 +779,86 @@ def bench_epilogue(args):
     print(json.dumps(line), flush=True)
 
 
+def bench_gpt_full(args):
+    """The full projection step of the GPT (six layers of QKV, attention-out,
+    MLP-up and MLP-down, each forward, dX and dW, plus the LM head: 75 GEMMs,
+    1046.6 GFLOP), timed as the host issues it and as one CUDA graph of the
+    whole step replayed.  Each layer has its own weights and activations
+    (seeded, drawn on the device); one mode for the whole step."""
+    import dense_gemm_transformer_gb300 as dg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dg.load(build_if_missing=True)
+    h = dg.Gemm()
+    stream = torch.cuda.Stream(dev)
+    mode = args.mode
+    dt = torch.bfloat16 if mode == "bf16" else torch.float32
+    T, layers = si.GPT_TOKENS, 6
+    g = torch.Generator(device=dev)
+    g.manual_seed(si.BASE_SEED + 4000)
+    calls = []
+    shapes = []
+    projs = [(name, kin, nout) for name, kin, nout in si.GPT_PROJECTIONS if name != "lm_head"]
+    head = [(name, kin, nout) for name, kin, nout in si.GPT_PROJECTIONS if name == "lm_head"]
+    for layer in range(layers + 1):
+        for name, kin, nout in (projs if layer < layers else head):
+            X = torch.randn((T, kin), generator=g, device=dev).to(dt)
+            W = (torch.randn((kin, nout), generator=g, device=dev) * 0.02).to(dt)
+            dY = torch.randn((T, nout), generator=g, device=dev).to(dt)
+            for A, B, tA, tB, M, N, K in ((X, W, False, False, T, nout, kin), (dY, W, False, True, T, kin, nout),
+                                          (X, dY, True, False, kin, nout, T)):
+                calls.append((A, B, torch.empty((M, N), device=dev), tA, tB))
+                shapes.append((M, N, K))
+    flops = sum(2 * M * N * K for M, N, K in shapes)
+
+    def step():
+        for A, B, C, tA, tB in calls:
+            h.run(A, B, C, mode=mode, transA=tA, transB=tB, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            step()
+    stream.synchronize()
+    launches = 0
+    with torch.cuda.stream(stream):
+        for A, B, C, tA, tB in calls:
+            h.run(A, B, C, mode=mode, transA=tA, transB=tB, stream=stream)
+            launches += h.plan()["kernels"]
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                step()
+            e1.record(stream)
+        stream.synchronize()
+        eager_ms = e0.elapsed_time(e1) / args.steps
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        graph.replay()
+        stream.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record(stream)
+        stream.synchronize()
+        graph_ms = e0.elapsed_time(e1) / args.steps
+    assert h.check_device(stream) == 0
+    h.close()
+    line = {"metric": METRIC, "value": flops / (graph_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": graph_ms, "higher_is_better": True,
+            "dtype": {"fp32": "f32", "tf32": "tf32", "bf16": "bf16"}[mode], "data": "synthetic (seeded, drawn on the device)",
+            "config": {"workload": f"gpt_full_step_{mode}", "layers": layers, "tokens": T, "d_model": 384,
+                       "gemms_per_step": len(calls), "gflop_per_step": round(flops / 1e9, 1),
+                       "timing": "one CUDA graph of the step, replayed; eager = as the host issues it"},
+            "eager": {"value": flops / (eager_ms * 1e-3) / 1e12, "ms_per_step": eager_ms},
+            "gpu_launches_per_step": launches, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -794,8 +874,10 @@ def main():
     ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
     ap.add_argument("--pair", type=int, default=None,
                     help="sweeps: force the CTA-pair form (0 planner, 1 none, 2 multicast B, 3 one 256-row MMA per pair)")
-    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny", "epilogue"],
+    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny", "epilogue", "gpt_full"],
                     help="gpt: the timed step; the others print a per-shape sweep")
+    ap.add_argument("--mode", default="tf32", choices=["fp32", "tf32", "bf16"],
+                    help="gpt_full: the mode of the whole step")
     ap.add_argument("--processes", type=int, default=3,
                     help="sweeps: separate processes to run the sweep in (median and spread across them)")
     args = ap.parse_args()
@@ -806,6 +888,8 @@ def main():
         bench_reference(args, world, rank)
     elif args.workload == "epilogue":
         bench_epilogue(args)
+    elif args.workload == "gpt_full":
+        bench_gpt_full(args)
     elif args.workload != "gpt":
         bench_sweep_processes(args)
     else:
