@@ -25,6 +25,15 @@
  *          (truncation toward zero) or rounding to nearest with ties away from
  *          zero.  The caller chooses.
  *   BF16 : the inputs arrive as bfloat16 bit patterns and are widened exactly.
+ *   FP8  : the inputs arrive as 8-bit E4M3 codes and are decoded exactly.  The
+ *          pages name FP8 among the tensor-core input types ("Tensor Cores:
+ *          Matrix Instructions, Swizzling and FP8, Measured" and "Low-Precision
+ *          Kernels: INT4, INT8 and FP8 Matmuls, Measured", their summaries)
+ *          without defining it; the reading taken is the E4M3 format of the
+ *          OCP 8-bit floating-point specification: 1 sign bit, 4 exponent bits
+ *          with bias 7, 3 mantissa bits, subnormals at exponent 0, no
+ *          infinities, and S.1111.111 the only NaN pattern (largest finite
+ *          magnitude 448).  Per-tensor scale factors are the caller's alpha.
  *
  * Conventions the pages leave open (BLAS readings): when K == 0 or alpha == 0
  * A and B are not read; when beta == 0 Cin is not read, so a NaN there does
@@ -45,6 +54,7 @@
 #define ORACLE_MODE_FP32 0
 #define ORACLE_MODE_TF32 1
 #define ORACLE_MODE_BF16 2
+#define ORACLE_MODE_FP8_E4M3 3
 
 #define ORACLE_TF32_TRUNCATE 0
 #define ORACLE_TF32_NEAREST_AWAY 1
@@ -87,8 +97,21 @@ double oracle_bf16_to_double(uint16_t b) {
   return (double)bits_float((uint32_t)b << 16);
 }
 
+/* An E4M3 code as a double.  Fields: s = bit 7, e = bits 6..3, m = bits 2..0.
+ *   e == 15 and m == 7 : NaN (either sign)
+ *   e == 0             : (-1)^s * (m / 8) * 2^(1 - 7)       (zero and subnormals)
+ *   otherwise          : (-1)^s * (1 + m / 8) * 2^(e - 7)
+ * Every value is a small integer times a power of two, so ldexp is exact. */
+double oracle_e4m3_to_double(uint8_t code) {
+  const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = (e == 0) ? ldexp((double)m, 1 - 7 - 3) : ldexp((double)(8 + m), e - 7 - 3);
+  return s ? -mag : mag;
+}
+
 static double operand(int mode, int tf32_rule, const void* base, int64_t idx) {
   if (mode == ORACLE_MODE_BF16) return oracle_bf16_to_double(((const uint16_t*)base)[idx]);
+  if (mode == ORACLE_MODE_FP8_E4M3) return oracle_e4m3_to_double(((const uint8_t*)base)[idx]);
   float v = ((const float*)base)[idx];
   if (mode == ORACLE_MODE_TF32)
     v = (tf32_rule == ORACLE_TF32_NEAREST_AWAY) ? oracle_tf32_nearest_away(v) : oracle_tf32_truncate(v);
@@ -106,13 +129,18 @@ void oracle_bf16_array(const uint16_t* in, double* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_double(in[i]);
 }
 
+/* Elementwise exact decoding of E4M3 codes (used by the tests). */
+void oracle_e4m3_array(const uint8_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_to_double(in[i]);
+}
+
 /* Returns 0 on success, a negative number for an argument it cannot take. */
 int oracle_gemm(int mode, int tf32_rule, int transA, int transB,
                 int64_t M, int64_t N, int64_t K, double alpha,
                 const void* A, int64_t lda, const void* B, int64_t ldb,
                 double beta, const float* Cin, int64_t ldc,
                 int64_t row0, int64_t row1, double* Cref, double* D, int64_t ldr) {
-  if (mode < ORACLE_MODE_FP32 || mode > ORACLE_MODE_BF16) return -1;
+  if (mode < ORACLE_MODE_FP32 || mode > ORACLE_MODE_FP8_E4M3) return -1;
   if (M < 0 || N < 0 || K < 0) return -2;
   if (row0 < 0 || row1 < row0 || row1 > M) return -3;
   if (ldr < N) return -4;

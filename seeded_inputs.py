@@ -84,6 +84,26 @@ def bf16_bits(t: torch.Tensor):
     return t.contiguous().view(torch.int16).numpy().view("uint16")
 
 
+FP8_E4M3_MAX = 448.0  # largest finite E4M3 magnitude
+
+
+def to_fp8_e4m3(t: torch.Tensor, amax_to: float = 0.0):
+    """Quantise fp32 to 8-bit E4M3 codes (torch's round-to-nearest-even
+    conversion on the CPU) with one scale for the whole tensor.
+
+    amax_to == 0: no scaling, the values must already lie within +-448.
+    amax_to > 0: the tensor is divided by s = max|t| / amax_to first, the way
+    per-tensor FP8 recipes map a tensor's range onto the format's.
+    Returns (codes as a uint8 numpy array, s); the product of two operands'
+    s is the alpha that restores the unscaled product."""
+    s = 1.0
+    if amax_to > 0.0:
+        amax = float(t.abs().max())
+        s = amax / amax_to if amax > 0.0 else 1.0
+    q = (t / s).to(torch.float8_e4m3fn)
+    return q.contiguous().view(torch.uint8).numpy(), s
+
+
 @dataclass(frozen=True)
 class GemmCase:
     """One GEMM of a workload: C (M x N) = alpha op(A) op(B) + beta C."""

@@ -9,7 +9,14 @@ K = 1); where the whole denominator is zero the result must be exact.
 """
 import numpy as np
 
-TOL = {"fp32": 1e-6, "tf32": 2e-3, "bf16": 8e-3}
+# FP8 (E4M3 operands): every product of two E4M3 values is exact in fp32 and
+# the tensor cores accumulate in fp32, so a full-precision accumulation would
+# stay near K / 32 * 2^-24 of D.  The gate allows the accumulator of one MMA
+# to keep as few as 14 mantissa bits (2^-14 ~ 6e-5 of D per MMA of 32 terms)
+# over K / 32 MMAs with random signs: sqrt(280) * 6e-5 ~ 1e-3 at K = 8960,
+# doubled.  Dropped or doubled K blocks are caught separately, on
+# non-negative operands, where one block of K = 8960 is 1.4e-2 of D.
+TOL = {"fp32": 1e-6, "tf32": 2e-3, "bf16": 8e-3, "fp8": 2e-3}
 
 
 def errors(C, Cref, D, alpha=1.0, beta=0.0, Cin=None):

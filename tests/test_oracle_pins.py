@@ -93,9 +93,35 @@ def test_bf16_widening_exhaustive():
     assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
 
 
+def test_e4m3_decoding_exhaustive():
+    """All 256 codes against torch's float8_e4m3fn widening (a library
+    routine the oracle does not use), plus values fixed by the format."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_to_f64(codes)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.flatnonzero(nan).tolist() == [0x7F, 0xFF]  # S.1111.111 only: no infinities
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+    fixed = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3C: 1.5,
+             0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in fixed.items():
+        assert got[c] == v, hex(c)
+    assert np.signbit(got[0x80]) and got[0x80] == 0.0
+    # positive codes 0 .. 0x7E are strictly increasing; negatives mirror them
+    assert np.all(np.diff(got[:0x7F]) > 0)
+    assert np.array_equal(got[0x80:0xFF], -got[:0x7F])
+
+
 # ---------------------------------------------------------------- helpers
 def _operands(mode, a, b):
     """numpy operands for the oracle plus their exact values as Fractions."""
+    if mode == "fp8":
+        (ca, _), (cb, _) = si.to_fp8_e4m3(torch.from_numpy(a)), si.to_fp8_e4m3(torch.from_numpy(b))
+        def widen(c):
+            return torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        return ca, cb, widen(ca), widen(cb)
     if mode == "bf16":
         ab, bb = si.to_bf16(torch.from_numpy(a)), si.to_bf16(torch.from_numpy(b))
         qa, qb = ab.to(torch.float64).numpy(), bb.to(torch.float64).numpy()
@@ -112,7 +138,7 @@ def _op(x, t):
 
 
 # ---------------------------------------------------------------- brute force
-@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16", "fp8"])
 @pytest.mark.parametrize("tA,tB", TRANS)
 @pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (0.5, 1.0), (-2.0, 0.25)])
 def test_bruteforce_exact_rational(mode, tA, tB, alpha, beta):
@@ -159,7 +185,7 @@ def test_golden_hand_computed_example():
 
 
 # ---------------------------------------------------------------- structure
-@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16", "fp8"])
 def test_identity_and_permutation(mode):
     rng = np.random.default_rng(3)
     M, N = 9, 11
@@ -183,7 +209,7 @@ def test_identity_and_permutation(mode):
     assert np.array_equal(got, qa2[:, perm])
 
 
-@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16", "fp8"])
 @pytest.mark.parametrize("tA,tB", TRANS)
 def test_small_integers_are_exact(mode, tA, tB):
     M, N, K = 40, 33, 1024
@@ -209,7 +235,7 @@ def test_rank_one_closed_form():
     assert np.array_equal(D, K * np.abs(np.outer(u, v)).astype(np.float64))
 
 
-@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16", "fp8"])
 def test_transpose_flags_match_explicit_transpose(mode):
     rng = np.random.default_rng(5)
     M, N, K = 19, 23, 29
@@ -297,6 +323,25 @@ def test_gate_rejects_one_dropped_term():
     with pytest.raises(AssertionError):
         _gate.assert_within("bf16", flipped, ref, D)
     _gate.assert_within("fp32", ref.astype(np.float32), ref, D)
+
+
+def test_fp8_gate_catches_one_missing_k_block_on_nonnegative_operands():
+    """At decode depth (K = 8960, 70 blocks of 128 bytes) a missing or doubled
+    K block moves a random-sign result by less than the FP8 gate, so the FP8
+    parity tests also run non-negative operands, where D = |Cref| and one
+    block of 128 is 1/70 of every element.  Planted in the oracle's inputs."""
+    K = 8960
+    a8, _ = si.to_fp8_e4m3(si.uniform((2, K), 43, lo=0.0, hi=1.0))
+    b8, _ = si.to_fp8_e4m3(si.uniform((24, K), 44, lo=0.0, hi=1.0))
+    ref, D = oracle.gemm("fp8", a8, b8, transB=True)
+    assert np.allclose(D, ref)
+    dropped = a8.copy()
+    dropped[:, 128 * 37:128 * 38] = 0  # planted: one K block missing
+    broken, _ = oracle.gemm("fp8", dropped, b8, transB=True)
+    assert _gate.max_err(broken, ref, D) > 5 * _gate.TOL["fp8"]
+    with pytest.raises(AssertionError):
+        _gate.assert_within("fp8", broken, ref, D)
+    _gate.assert_within("fp8", ref.astype(np.float32), ref, D)
 
 
 # ------------------------------------------------------------ fused epilogue
