@@ -43,8 +43,9 @@ METRIC = "GEMM TFLOP/s per shape & % of GB300 roofline (tensor peak or HBM BW), 
 SMS = 152
 FP32_LANES_PER_SM = 128
 SM_MAX_MHZ = 2070.0
-# Nominal dense rates (recipe): tf32 1.1 PF vs bf16 2.25 PF.
+# Nominal dense rates (recipe): tf32 1.1 PF, bf16 2.25 PF, fp8 4.5 PF.
 TF32_OVER_BF16 = 1.1 / 2.25
+FP8_OVER_BF16 = 4.5 / 2.25
 
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
@@ -81,6 +82,7 @@ def peaks():
     fp32_alu = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
     return {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": bf16_s,
             "tf32_tflops": bf16 * TF32_OVER_BF16, "tf32_tflops_sustained": bf16_s * TF32_OVER_BF16,
+            "fp8_tflops": bf16 * FP8_OVER_BF16, "fp8_tflops_sustained": bf16_s * FP8_OVER_BF16,
             "fp32_alu_tflops": fp32_alu, "source": src}
 
 
@@ -475,7 +477,21 @@ def sweep_cases(workload):
             for c in si.skinny_cases():
                 case = si.GemmCase(c.name + (".T" if tB else ""), False, tB, c.M, c.N, c.K)
                 out.append((f"bf16.{case.name}", "bf16", case, 1.0, 0.0, 0.02))
+    elif workload == "skinny_fp8":
+        # E4M3 weights stored N x K (the form the FP8 mode takes), N(0, 1)
+        # codes: a per-tensor scale would only change alpha
+        for c in si.skinny_cases():
+            case = si.GemmCase(c.name + ".T", False, True, c.M, c.N, c.K)
+            out.append((f"fp8.{case.name}", "fp8", case, 1.0, 0.0, 1.0))
     return out
+
+
+def _elem_bytes(mode):
+    return {"bf16": 2, "fp8": 1}.get(mode, 4)
+
+
+def _operand_dtype(mode):
+    return {"bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}.get(mode, torch.float32)
 
 
 SAMPLES = 5          # timed samples per shape (median and spread)
@@ -550,8 +566,8 @@ def _sweep_shapes(args, h, stream, pk, l2, dev, shapes):
             import re
             if not re.fullmatch(args.only, label):
                 continue
-        dt = torch.bfloat16 if mode == "bf16" else torch.float32
-        es = 2 if mode == "bf16" else 4
+        dt = _operand_dtype(mode)
+        es = _elem_bytes(mode)
         per_set = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N
         copies = max(1, min(32, -(-3 * l2 // per_set)))
         g = torch.Generator(device="cpu")
@@ -618,9 +634,10 @@ def _sweep_shapes(args, h, stream, pk, l2, dev, shapes):
                           for _ in range(SAMPLES)])
         stream.synchronize()
         byts = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N * (2 if beta != 0 else 1)
-        peak = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops"], "bf16": pk["bf16_tflops"]}[mode]
+        peak = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops"], "bf16": pk["bf16_tflops"],
+                "fp8": pk["fp8_tflops"]}[mode]
         peak_s = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops_sustained"],
-                  "bf16": pk["bf16_tflops_sustained"]}[mode]
+                  "bf16": pk["bf16_tflops_sustained"], "fp8": pk["fp8_tflops_sustained"]}[mode]
         t_c, t_m = c.flops / (peak * 1e12), byts / (pk["hbm_gbs"] * 1e9)
         t_cs = c.flops / (peak_s * 1e12)
         st = _stats(dev_ms)
@@ -874,7 +891,7 @@ def main():
     ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
     ap.add_argument("--pair", type=int, default=None,
                     help="sweeps: force the CTA-pair form (0 planner, 1 none, 2 multicast B, 3 one 256-row MMA per pair)")
-    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny", "epilogue", "gpt_full"],
+    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny", "skinny_fp8", "epilogue", "gpt_full"],
                     help="gpt: the timed step; the others print a per-shape sweep")
     ap.add_argument("--mode", default="tf32", choices=["fp32", "tf32", "bf16"],
                     help="gpt_full: the mode of the whole step")

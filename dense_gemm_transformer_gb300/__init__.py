@@ -10,6 +10,7 @@ without the built extension raises.
     C = torch.empty(M, N, device="cuda")
     dg.gemm(A, B, C, mode="tf32")                # C = A @ B
     dg.gemm(A, W, C, mode="bf16", transB=True)   # C = A @ W^T, W stored N x K
+    dg.gemm(X8, W8, C, mode="fp8", transB=True, alpha=sx * sw)  # E4M3 codes, M <= 16
 """
 from __future__ import annotations
 
@@ -20,7 +21,7 @@ import threading
 
 from . import _build
 
-MODES = {"fp32": 0, "tf32": 1, "bf16": 2}
+MODES = {"fp32": 0, "tf32": 1, "bf16": 2, "fp8": 3}
 FAMILIES = {"auto": 0, "simt": 1, "tc": 2, "skinny": 3}
 OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3, "pretranspose": 4, "pair": 5}
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED", 3: "GEMM_ERR_MISALIGNED",
@@ -127,6 +128,16 @@ def _matrix(t, name):
     return t.data_ptr(), ld
 
 
+def _operand_dtypes(torch, mode):
+    """Tensor types an operand may have in `mode` (fp8: E4M3 codes, as
+    torch.float8_e4m3fn or as raw uint8)."""
+    if mode == "bf16":
+        return (torch.bfloat16,)
+    if mode == "fp8":
+        return (torch.float8_e4m3fn, torch.uint8)
+    return (torch.float32,)
+
+
 class Gemm:
     """A library handle bound to the current CUDA device."""
 
@@ -189,8 +200,8 @@ class Gemm:
         op(B) + beta C) * GELU'(aux), aux the float32 M x N pre-activation.
         """
         import torch
-        want = torch.bfloat16 if mode == "bf16" else torch.float32
-        if A.dtype != want or B.dtype != want:
+        want = _operand_dtypes(torch, mode)
+        if A.dtype not in want or B.dtype not in want:
             raise TypeError(f"mode {mode} takes {want} operands")
         if C.dtype != torch.float32:
             raise TypeError("C must be float32")

@@ -40,7 +40,7 @@ struct gemm_handle_s {
   int opt_tile_n = 0;
   int opt_pretranspose = 0;
   int opt_pair = 0;
-  int sk_active[2][dgt::kSkinnyMaxCluster + 1];  // small-M kernel: resident clusters (-1: not queried)
+  int sk_active[3][dgt::kSkinnyMaxCluster + 1];  // small-M kernel per mode (TF32, BF16, FP8): resident clusters (-1: not queried)
   dgt::TmaCache* tma_cache = nullptr;             // TMA descriptors of earlier calls
   gemm_plan_t plan{};
   dgt::LaunchShape null_shape;  // main kernel of the last successful gemm_run (for gemm_launch_null)
@@ -53,10 +53,11 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+int elem_bytes(int mode) { return mode == GEMM_MODE_FP8_E4M3 ? 1 : mode == GEMM_MODE_BF16 ? 2 : 4; }
 
 gemm_status_t check_args(int mode, int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                          const void* A, int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc) {
-  if (mode < GEMM_MODE_FP32 || mode > GEMM_MODE_BF16) return GEMM_ERR_INVALID_VALUE;
+  if (mode < GEMM_MODE_FP32 || mode > GEMM_MODE_FP8_E4M3) return GEMM_ERR_INVALID_VALUE;
   if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return GEMM_ERR_INVALID_VALUE;
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) return GEMM_OK;
@@ -66,8 +67,7 @@ gemm_status_t check_args(int mode, int transA, int transB, int64_t M, int64_t N,
   if (A == nullptr || B == nullptr) return GEMM_ERR_INVALID_VALUE;
   if (lda < std::max<int64_t>(transA ? M : K, 1)) return GEMM_ERR_INVALID_VALUE;
   if (ldb < std::max<int64_t>(transB ? K : N, 1)) return GEMM_ERR_INVALID_VALUE;
-  const size_t es = (mode == GEMM_MODE_BF16) ? 2 : 4;
-  if (!aligned(A, es) || !aligned(B, es)) return GEMM_ERR_MISALIGNED;
+  if (!aligned(A, elem_bytes(mode)) || !aligned(B, elem_bytes(mode))) return GEMM_ERR_MISALIGNED;
   return GEMM_OK;
 }
 
@@ -374,7 +374,7 @@ int64_t skinny_cluster_size(gemm_handle_s* h, int mode, bool a_mn, int64_t tiles
   int64_t cs = std::min<int64_t>(2 * h->sms / tiles, dgt::kSkinnyMaxCluster);
   cs = std::max<int64_t>(1, std::min<int64_t>(cs, kb / 2));
   while (cs > 8) {
-    int& act = h->sk_active[mode == GEMM_MODE_BF16 ? 1 : 0][cs];
+    int& act = h->sk_active[mode - GEMM_MODE_TF32][cs];
     if (act < 0) act = dgt::skinny_max_active_clusters(mode, a_mn, static_cast<int>(cs));
     if (act > 0) break;
     --cs;
@@ -386,7 +386,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
                      float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
                      int64_t ldc, const dgt::EpiParams& epi, cudaStream_t s, bool swap) {
   using namespace dgt;
-  const int es = (mode == GEMM_MODE_BF16) ? 2 : 4;
+  const int es = elem_bytes(mode);
   const int bk = tc_tile_k(mode);
   const int sms = h->sms;
   // The swapped form computes C^T = op(B)^T op(A)^T: the kernel sees M' = N,
@@ -458,8 +458,10 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   const int64_t tiles = ceil_div(Mk, 128) * ceil_div(Nk, tile_n);
   // Small M with fewer than two waves of weight tiles: the cluster kernel
   // (one tile and K slice per CTA, slices reduced within the cluster).
-  // With more tiles, the persistent kernel streams them without a split.
-  const bool cluster_form = swap && tiles < 2 * sms;
+  // With more tiles, the persistent kernel streams them without a split;
+  // FP8 is built into the cluster kernel only, which then runs one CTA per
+  // tile.
+  const bool cluster_form = swap && (tiles < 2 * sms || mode == GEMM_MODE_FP8_E4M3);
   int64_t splits = 1;
   if (cluster_form) {
     splits = (h->opt_split_k > 0)
@@ -635,6 +637,10 @@ gemm_status_t run_checked(gemm_handle_t h, int mode, int transA, int transB, int
   // MMA side once (activations must be stored M x K).
   const bool skinny_ok = (transA == 0) && M <= 16;
   if (fam == GEMM_FAMILY_SKINNY && !skinny_ok) return GEMM_ERR_NOT_SUPPORTED;
+  // FP8: the small-M product with both operands K-major (the weights
+  // stored N x K); kind::f8f6f4 is used here with K-major operands only.
+  if (mode == GEMM_MODE_FP8_E4M3 && (!skinny_ok || transB != 1 || fam == GEMM_FAMILY_TC))
+    return GEMM_ERR_NOT_SUPPORTED;
   if (fam == GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
   const bool swap = (fam == GEMM_FAMILY_SKINNY) || (fam == GEMM_FAMILY_AUTO && skinny_ok);
   return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, s, swap);

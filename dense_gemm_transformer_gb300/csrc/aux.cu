@@ -327,6 +327,9 @@ cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_d
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   const int threads = 256;
   const dim3 blocks(grid_for(rows * cols, threads));
+  if (elem_bytes == 1)
+    return launch_pdl(pack_kernel<uint8_t>, blocks, dim3(threads), 0, stream, static_cast<const uint8_t*>(src),
+                      ld_src, static_cast<uint8_t*>(dst), ld_dst, rows, cols);
   if (elem_bytes == 2)
     return launch_pdl(pack_kernel<uint16_t>, blocks, dim3(threads), 0, stream, static_cast<const uint16_t*>(src),
                       ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols);

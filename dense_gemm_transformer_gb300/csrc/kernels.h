@@ -124,7 +124,7 @@ cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream);
 // an smem ring fed by a TMA producer warp, a single-thread MMA issuer with a
 // double-buffered TMEM accumulator, and four epilogue warps.
 struct TcArgs {
-  int mode;              // 1 = tf32, 2 = bf16 (gemm_mode_t)
+  int mode;              // 1 = tf32, 2 = bf16, 3 = fp8 e4m3 (gemm_mode_t; fp8: small-M kernel only)
   int a_mn_major;        // A stored with M contiguous (transA == 1)
   int b_mn_major;        // B stored with N contiguous (transB == 0)
   int tile_n;            // 128, 192, 224 or 256 (16: the swapped small-M form)

@@ -260,6 +260,18 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Same, kind::f8f6f4 with both operands 8-bit (the formats are named in the
+// instruction descriptor: E4M3 = 0); K = 32 elements (32 bytes) per MMA.
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Same, with the A operand in TMEM at `a_tmem` (row i of A in lane i, one
 // 32-bit element per column, K along the columns) and B in shared memory.
 __device__ __forceinline__ void mma_tf32_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -460,9 +472,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor for kind::f16 / kind::tf32 with an fp32 accumulator.
+// Instruction descriptor for kind::f16 / kind::tf32 / kind::f8f6f4 with an
+// fp32 accumulator.
 //   bits 4-5 D format (1 = f32); bits 7-9 / 10-12 A / B format
-//   (kind::f16: 1 = bf16; kind::tf32: 2 = tf32); bit 15 / 16 A / B MN-major;
+//   (kind::f16: 1 = bf16; kind::tf32: 2 = tf32; kind::f8f6f4: 0 = e4m3);
+//   bit 15 / 16 A / B MN-major;
 //   bits 17-22 N >> 3; bits 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, bool a_mn_major, bool b_mn_major, uint32_t m,
                                                   uint32_t n) {

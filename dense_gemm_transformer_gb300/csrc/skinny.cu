@@ -41,13 +41,14 @@
 namespace dgt {
 namespace {
 
+// MODE: 1 TF32 (fp32 operands), 2 BF16, 3 FP8 E4M3 (8-bit codes).
 template <int MODE>
 struct SkCfg {
-  static constexpr int ES = (MODE == 2) ? 2 : 4;   // operand bytes
+  static constexpr int ES = (MODE == 3) ? 1 : (MODE == 2) ? 2 : 4;  // operand bytes
   static constexpr int BM = 128;                   // weight rows per tile (UMMA M)
   static constexpr int BN = 16;                    // activation rows (UMMA N)
   static constexpr int BK = 128 / ES;              // K elements per stage (one 128-byte swizzle row)
-  static constexpr int UK = (MODE == 2) ? 16 : 8;  // K of one MMA (32 bytes)
+  static constexpr int UK = 32 / ES;                // K of one MMA (32 bytes)
   static constexpr int CH = 128 / ES;              // weight rows in one 128-byte MN-major row
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
@@ -58,7 +59,7 @@ struct SkCfg {
   static constexpr int RECV_BYTES = (BN * BM / 4 + kSkinnyMaxCluster) * 16;  // shares pushed by the peers
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + RECV_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr int PREFETCH_KB = 16;              // K blocks of weights warmed in L2 before the wait
-  static constexpr uint32_t FORMAT = (MODE == 2) ? 1u : 2u;
+  static constexpr uint32_t FORMAT = (MODE == 3) ? 0u : (MODE == 2) ? 1u : 2u;  // e4m3 / bf16 / tf32
   static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM (228 KB, 1 KB reserved per CTA)");
   static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
   static_assert(BM * BN * 4 <= STAGES * STAGE_BYTES, "the partial tile fits in the drained stages");
@@ -67,7 +68,9 @@ struct SkCfg {
 
 template <int MODE>
 __device__ __forceinline__ void sk_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  if (MODE == 2)
+  if (MODE == 3)
+    mma_f8f6f4(d, a, b, idesc, acc);
+  else if (MODE == 2)
     mma_bf16(d, a, b, idesc, acc);
   else
     mma_tf32(d, a, b, idesc, acc);
@@ -379,13 +382,15 @@ cudaError_t skinny_launch(int mode, bool a_mn, const CUtensorMap& ta, const CUte
     return cudaErrorInvalidValue;
   if (mode == 2) return a_mn ? launch_one<2, true>(ta, tb, p, grid, s) : launch_one<2, false>(ta, tb, p, grid, s);
   if (mode == 1 && !a_mn) return launch_one<1, false>(ta, tb, p, grid, s);
-  return cudaErrorInvalidValue;  // kind::tf32 takes K-major operands only
+  if (mode == 3 && !a_mn) return launch_one<3, false>(ta, tb, p, grid, s);
+  return cudaErrorInvalidValue;  // kind::tf32 and the FP8 form take K-major operands only
 }
 
 int skinny_max_active_clusters(int mode, bool a_mn, int cluster) {
   if (cluster < 1 || cluster > kSkinnyMaxCluster) return 0;
   if (mode == 2) return a_mn ? active_clusters<2, true>(cluster) : active_clusters<2, false>(cluster);
   if (mode == 1 && !a_mn) return active_clusters<1, false>(cluster);
+  if (mode == 3 && !a_mn) return active_clusters<3, false>(cluster);
   return 0;
 }
 

@@ -30,8 +30,9 @@ constexpr int kSkinnyMaxCluster = 16;
 constexpr int kSkinnyStages = 5;  // with the 8 KB receive buffer ~100 KB of shared memory: two CTAs per SM
 
 // Launch on `grid` = tiles * p.cluster CTAs, clusters of p.cluster CTAs
-// along x, with programmatic dependent launch.  a_mn: the weights are stored
-// with the caller's N contiguous (transB == 0); BF16 only.
+// along x, with programmatic dependent launch.  mode: 1 TF32, 2 BF16, 3 FP8
+// E4M3.  a_mn: the weights are stored with the caller's N contiguous
+// (transB == 0); BF16 only.
 cudaError_t skinny_launch(int mode, bool a_mn, const CUtensorMap& ta, const CUtensorMap& tb, const SkParams& p,
                           int grid, cudaStream_t s);
 // Clusters of `cluster` CTAs of the kernel that can be resident at once

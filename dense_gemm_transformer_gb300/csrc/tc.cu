@@ -25,8 +25,10 @@ cudaError_t g_encode_status = cudaSuccess;
 
 cudaError_t encode_2d(CUtensorMap* m, int mode, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
                       uint32_t box_inner, uint32_t box_outer) {
-  const int es = (mode == 2) ? 2 : 4;
-  const CUtensorMapDataType dt = (mode == 2) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int es = (mode == 3) ? 1 : (mode == 2) ? 2 : 4;
+  const CUtensorMapDataType dt = (mode == 3)   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : (mode == 2) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
   cuuint32_t box[2] = {box_inner, box_outer};
@@ -110,7 +112,7 @@ cudaError_t tc_init_driver() {
   return g_encode_status;
 }
 
-int tc_tile_k(int mode) { return mode == 2 ? 64 : 32; }
+int tc_tile_k(int mode) { return mode == 3 ? 128 : mode == 2 ? 64 : 32; }
 
 int tc_stages(int mode, int tile_n, bool mma2) {
   (void)mode;  // a stage holds 128 bytes of K per row in both modes
@@ -123,6 +125,7 @@ int tc_stages(int mode, int tile_n, bool mma2) {
 }
 
 bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major) {
+  if (mode != 1 && mode != 2) return false;
   if (tile_n != 128 && tile_n != 192 && tile_n != 224 && tile_n != 256) return false;
   if (pair && tile_n == 128) return false;
   if (!b_mn_major) return true;
@@ -132,10 +135,11 @@ bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major) {
 }
 
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
+  if (a.mode != 1 && a.mode != 2) return cudaErrorInvalidValue;  // FP8 runs in the small-M kernel only
   cudaError_t e = tc_init_driver();
   if (e != cudaSuccess) return e;
   const int bk = tc_tile_k(a.mode);
-  const int ch = (a.mode == 2) ? 64 : 32;  // elements in a 128-byte MN-major row
+  const int ch = 128 / ((a.mode == 3) ? 1 : (a.mode == 2) ? 2 : 4);  // elements in a 128-byte MN-major row
   CUtensorMap ta, tb;
   e = a.a_mn_major ? encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
                    : encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
@@ -203,7 +207,7 @@ cudaError_t launch_skinny(const TcArgs& a, cudaStream_t stream) {
   cudaError_t e = tc_init_driver();
   if (e != cudaSuccess) return e;
   const int bk = tc_tile_k(a.mode);
-  const int ch = (a.mode == 2) ? 64 : 32;
+  const int ch = 128 / ((a.mode == 3) ? 1 : (a.mode == 2) ? 2 : 4);
   CUtensorMap ta, tb;
   e = a.a_mn_major ? encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
                    : encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);

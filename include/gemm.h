@@ -7,10 +7,12 @@
  *
  *     C = alpha * op(A) * op(B) + beta * C
  *
- * computed in one of three modes: exact FP32 on the CUDA cores, TF32 on the
+ * computed in one of four modes: exact FP32 on the CUDA cores, TF32 on the
  * tensor cores (the mode the page's tensor-core kernel uses, first paragraph),
- * or BF16 inputs on the tensor cores.  Every mode accumulates in FP32 and
- * writes FP32.
+ * BF16 inputs on the tensor cores, or -- for small M only -- FP8 E4M3 inputs
+ * on the tensor cores ("Tensor Cores: Matrix Instructions, Swizzling and FP8,
+ * Measured" and "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured"
+ * name the format).  Every mode accumulates in FP32 and writes FP32.
  *
  * Layout (all matrices row-major, element (r, c) at base[r * ld + c]):
  *   op(A) is M x K.  transA == 0: A is stored M x K, lda >= max(K, 1).
@@ -24,6 +26,13 @@
  *   mantissa bits.  The TF32 tensor-core instruction reads K-major operands
  *   only, so in TF32 mode an operand stored with M (or N) contiguous (A with
  *   transA == 1, B with transB == 0) is first transposed into the workspace.
+ *   In GEMM_MODE_FP8_E4M3, A and B hold 8-bit E4M3 codes of the OCP 8-bit
+ *   floating-point format (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ *   bits, no infinities, S.1111.111 = NaN, largest magnitude 448); there is
+ *   no per-block scale, so per-tensor scale factors go into alpha.  The mode
+ *   covers the small-M product only: M <= 16, transA == 0 and transB == 1
+ *   (both operands K-major, the weights stored N x K); anything else gives
+ *   GEMM_ERR_NOT_SUPPORTED.
  *
  * Ownership: the caller owns A, B and C, which are device memory.  A handle
  * owns its device properties, a device status word and a scratch workspace
@@ -50,7 +59,9 @@ typedef struct gemm_handle_s* gemm_handle_t;
 typedef enum {
   GEMM_MODE_FP32 = 0, /* fp32 operands, FFMA on CUDA cores, exact fp32 products */
   GEMM_MODE_TF32 = 1, /* fp32 operands, tcgen05 kind::tf32, fp32 accumulate   */
-  GEMM_MODE_BF16 = 2  /* bf16 operands, tcgen05 kind::f16, fp32 accumulate    */
+  GEMM_MODE_BF16 = 2, /* bf16 operands, tcgen05 kind::f16, fp32 accumulate    */
+  GEMM_MODE_FP8_E4M3 = 3 /* e4m3 operands, tcgen05 kind::f8f6f4, fp32 accumulate;
+                            M <= 16, transA == 0, transB == 1 only             */
 } gemm_mode_t;
 
 typedef enum {
@@ -69,7 +80,7 @@ typedef enum {
   GEMM_FAMILY_AUTO = 0,
   GEMM_FAMILY_SIMT = 1,   /* register-tiled FFMA kernel (GEMM_MODE_FP32 only)           */
   GEMM_FAMILY_TC = 2,     /* persistent TMA + tcgen05 kernel, 1 CTA per tile (TF32/BF16) */
-  GEMM_FAMILY_SKINNY = 3  /* HBM-bound small-M kernels, M <= 16 (TF32/BF16)             */
+  GEMM_FAMILY_SKINNY = 3  /* HBM-bound small-M kernels, M <= 16 (TF32/BF16/FP8)         */
 } gemm_family_t;
 
 typedef enum {
@@ -145,7 +156,8 @@ gemm_status_t gemm_destroy(gemm_handle_t h);
  * Small M (M <= 16, transA == 0, TF32/BF16) with fewer than two waves of
  * 128-column weight tiles runs one kernel that splits K across the CTAs of a
  * thread-block cluster and sums the slices in distributed shared memory (no
- * workspace).  It is launched with programmatic dependent launch: its set-up
+ * workspace).  FP8 always runs that kernel (one CTA per weight tile, no K
+ * split, when there are two or more waves of tiles).  It is launched with programmatic dependent launch: its set-up
  * and an L2 prefetch of the weights may overlap the end of the previous
  * kernel in `stream`, but it reads and writes no memory before that kernel
  * has completed, so stream order is kept. */
@@ -228,8 +240,9 @@ gemm_status_t gemm_launch_null(gemm_handle_t h, void* stream);
  * Limits and errors: M > 16, or split-K partial sums that would not fit the
  * array even with a single K slice, give GEMM_ERR_TOO_LARGE; an operand the
  * TMA unit cannot read in place (base not 16-byte aligned, row pitch not a
- * multiple of 16 bytes) gives GEMM_ERR_MISALIGNED; FP32 mode or TF32 with
- * transB == 0 gives GEMM_ERR_NOT_SUPPORTED; the other checks are gemm_run's.
+ * multiple of 16 bytes) gives GEMM_ERR_MISALIGNED; FP32 or FP8 mode, or TF32
+ * with transB == 0, gives GEMM_ERR_NOT_SUPPORTED; the other checks are
+ * gemm_run's.
  * The planner's K-slice count is lowered when its partial sums would not fit.
  *
  * The first call on a device looks up the array's device address (with that

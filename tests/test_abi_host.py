@@ -48,7 +48,9 @@ def test_validate_accepts_good_arguments(lib):
 
 
 def test_validate_rejects_bad_flags_and_sizes(lib):
-    assert dg.validate(3, 0, 0, 8, 8, 8, 1.0, P, 8, P, 8, P, 8) == INVALID
+    assert dg.validate(4, 0, 0, 8, 8, 8, 1.0, P, 8, P, 8, P, 8) == INVALID
+    # FP8 (mode 3): one-byte operands, so any operand address is aligned
+    assert dg.validate(3, 0, 1, 8, 8, 8, 1.0, P + 1, 8, P + 3, 8, P, 8) == OK
     assert dg.validate(-1, 0, 0, 8, 8, 8, 1.0, P, 8, P, 8, P, 8) == INVALID
     assert v(tA=2) == INVALID and v(tB=-1) == INVALID
     assert v(M=-1) == INVALID and v(N=-5) == INVALID and v(K=-1) == INVALID

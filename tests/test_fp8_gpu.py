@@ -1,0 +1,209 @@
+"""Parity of the FP8 (E4M3) small-M product with the CPU oracle, through the C ABI.
+
+The FP8 mode runs the decode-shaped tensor-core kernel with kind::f8f6f4:
+both operands K-major (activations M x K, weights stored N x K), M <= 16.
+Inputs are quantised per tensor the way FP8 inference stores them (each
+tensor divided by max|t| / 440, rounded to E4M3 by torch on the CPU) and the
+two scales come back through alpha.  The oracle decodes the same codes
+exactly and accumulates in fp64.  Gate: 2e-3 of |alpha| * sum|a||b|
+(tests/_gate.py); non-negative operands at decode depth catch a missing or
+doubled K block, small integers must come out bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_transformer_gb300 as dg
+import oracle
+import seeded_inputs as si
+from tests import _gate
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def h():
+    dg.load(build_if_missing=True)
+    handle = dg.Gemm()
+    yield handle
+    handle.close()
+
+
+@pytest.fixture(autouse=True)
+def _reset(h):
+    h.set_option("family", "auto")
+    h.set_option("split_k", 0)
+    yield
+    h.set_option("family", "auto")
+    h.set_option("split_k", 0)
+
+
+def _draw(shape, seed, dist, std=1.0):
+    if dist == "int":
+        return si.integers(shape, seed)
+    if dist == "pos":
+        return si.uniform(shape, seed, lo=0.0, hi=1.0)
+    return si.normal(shape, seed, std=std)
+
+
+def _operands(M, N, K, seed, dist="normal"):
+    """E4M3 codes of the activations (M x K) and weights (N x K) and the
+    alpha that undoes their per-tensor scales (1 for integers)."""
+    amax = 0.0 if dist == "int" else 440.0
+    a8, sa = si.to_fp8_e4m3(_draw((M, K), seed, dist), amax)
+    w8, sw = si.to_fp8_e4m3(_draw((N, K), seed + 1, dist, std=0.02), amax)
+    return a8, w8, sa * sw
+
+
+def _device(codes, as_fp8=False):
+    t = torch.from_numpy(codes).cuda()
+    return t.view(torch.float8_e4m3fn) if as_fp8 else t
+
+
+def _run_and_check(h, M, N, K, seed, dist="normal", beta=0.0, exact=False, as_fp8=False, cols=None):
+    a8, w8, alpha = _operands(M, N, K, seed, dist)
+    cin = si.normal((M, N), seed + 2).numpy() if beta != 0.0 else None
+    C = torch.from_numpy(cin).cuda() if cin is not None else torch.full((M, N), float("nan"), device="cuda")
+    h.run(_device(a8, as_fp8), _device(w8, as_fp8), C, mode="fp8", transB=True, alpha=alpha, beta=beta)
+    assert h.check_device() == 0
+    got = C.cpu().numpy()
+    assert h.plan()["family"] == "skinny"
+    for c0, c1 in cols or [(0, N)]:
+        ref, D = oracle.gemm("fp8", a8, w8[c0:c1], transB=True, alpha=alpha, beta=beta,
+                             C=None if cin is None else np.ascontiguousarray(cin[:, c0:c1]))
+        if exact:
+            assert np.array_equal(got[:, c0:c1].astype(np.float64), ref), (M, N, K, c0)
+        else:
+            _gate.assert_within("fp8", got[:, c0:c1], ref, D, alpha=alpha, beta=beta,
+                                Cin=None if cin is None else cin[:, c0:c1],
+                                what=f"fp8 M={M} N={N} K={K} cols {c0}:{c1}")
+    return got
+
+
+# ------------------------------------------------------------ ragged shapes
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 768), (7, 300, 128), (16, 129, 2048), (3, 65, 40),
+                                   (16, 384, 96), (5, 1, 256)])
+def test_fp8_ragged(h, M, N, K):
+    _run_and_check(h, M, N, K, seed=71)
+    _run_and_check(h, M, N, K, seed=72, beta=1.0)
+
+
+def test_fp8_takes_float8_tensors_and_uint8_codes_alike(h):
+    g1 = _run_and_check(h, 4, 300, 512, seed=73)
+    g2 = _run_and_check(h, 4, 300, 512, seed=73, as_fp8=True)
+    assert np.array_equal(g1, g2)
+
+
+@pytest.mark.parametrize("K", [1000, 1512])
+def test_fp8_row_pitch_not_a_multiple_of_16_bytes(h, K):
+    """K = 1000 or 1512 bytes per row: the TMA unit cannot read the rows in
+    place, so both operands are re-packed first (and K ends inside a block)."""
+    _run_and_check(h, 9, 500, K, seed=74)
+    assert h.plan()["packed"] == 3
+
+
+def test_fp8_unaligned_base_pointer(h):
+    M, N, K = 4, 200, 256
+    a8, w8, alpha = _operands(M, N, K, 75)
+    buf = torch.zeros(M * K + 16, dtype=torch.uint8, device="cuda")
+    A = buf[1:1 + M * K].view(M, K)  # base one byte past a 16-byte boundary
+    A.copy_(torch.from_numpy(a8).cuda())
+    C = torch.full((M, N), float("nan"), device="cuda")
+    h.run(A, torch.from_numpy(w8).cuda(), C, mode="fp8", transB=True, alpha=alpha)
+    assert h.check_device() == 0
+    assert h.plan()["packed"] == 1  # A (the activations) re-packed, the weights read in place
+    ref, D = oracle.gemm("fp8", a8, w8, transB=True, alpha=alpha)
+    _gate.assert_within("fp8", C.cpu().numpy(), ref, D, alpha=alpha)
+
+
+# ------------------------------------------------------------ K slices in one cluster
+@pytest.mark.parametrize("cs", [1, 2, 3, 8, 12, 16])
+def test_fp8_cluster_k_slices(h, cs):
+    h.set_option("family", "skinny")
+    h.set_option("split_k", cs)
+    M, N, K = 5, 300, 46 * 128 + 16  # 47 K blocks, the last one ragged: every cs gives cs slices
+    _run_and_check(h, M, N, K, seed=76)
+    plan = h.plan()
+    assert plan["split_k"] == cs and plan["cluster"] == cs and plan["grid"] == 3 * cs
+    _run_and_check(h, M, N, K, seed=77, beta=1.0)
+
+
+@pytest.mark.parametrize("cs", [1, 5, 16])
+def test_fp8_integers_bit_exact(h, cs):
+    # integers in [-4, 4] are E4M3 values.  K = 256 keeps every partial sum
+    # below 2^12, exact in any accumulator the gate allows; at K = 1792 the
+    # sums of these random signs stay far below 2^14 as well
+    h.set_option("split_k", cs)
+    _run_and_check(h, 16, 260, 256, seed=78, dist="int", exact=True)
+    _run_and_check(h, 16, 260, 256 * 7, seed=79, dist="int", exact=True)
+
+
+# ------------------------------------------------------------ the decode shapes
+def _column_ranges(N, tile=128, width=4):
+    picks = sorted({0, tile - 2, N // 2 - 1, N - width})
+    return [(c, min(c + width, N)) for c in picks if 0 <= c < N]
+
+
+@pytest.mark.parametrize("M", si.SKINNY_M)
+@pytest.mark.parametrize("w", range(len(si.SKINNY_WEIGHTS)))
+def test_fp8_decode_shapes_sampled(h, M, w):
+    """The decode shapes at full size (the benchmark's launch configuration),
+    checked on sampled columns around tile edges."""
+    K, N = si.SKINNY_WEIGHTS[w]
+    _run_and_check(h, M, N, K, seed=si.seed_for(4, w, 5), cols=_column_ranges(N))
+    plan = h.plan()
+    tiles = -(-N // 128)
+    assert plan["grid"] == tiles * plan["split_k"]
+
+
+@pytest.mark.parametrize("w", range(len(si.SKINNY_WEIGHTS)))
+def test_fp8_nonnegative_operands_catch_a_missing_k_block(h, w):
+    """With non-negative operands D equals |Cref|, and one K block of 128 is
+    at least 1/70 of every element at these depths, far above the gate."""
+    K, N = si.SKINNY_WEIGHTS[w]
+    _run_and_check(h, 16, N, K, seed=si.seed_for(4, w, 7), dist="pos", cols=_column_ranges(N))
+
+
+# ------------------------------------------------------------ what the mode does not take
+def test_fp8_unsupported_forms(h):
+    A = torch.zeros((4, 64), dtype=torch.uint8, device="cuda")
+    Wnk = torch.zeros((32, 64), dtype=torch.uint8, device="cuda")
+    C = torch.zeros((4, 32), device="cuda")
+    with pytest.raises(dg.GemmError) as e:  # weights stored K x N (MN-major)
+        h.run(A, Wnk.t().contiguous(), C, mode="fp8", transB=False)
+    assert e.value.status == 2
+    with pytest.raises(dg.GemmError) as e:  # activations stored K x M
+        h.run(A.t().contiguous(), Wnk, C, mode="fp8", transA=True, transB=True)
+    assert e.value.status == 2
+    A17 = torch.zeros((17, 64), dtype=torch.uint8, device="cuda")
+    with pytest.raises(dg.GemmError) as e:  # more than 16 rows
+        h.run(A17, Wnk, torch.zeros((17, 32), device="cuda"), mode="fp8", transB=True)
+    assert e.value.status == 2
+    h.set_option("family", "tc")
+    with pytest.raises(dg.GemmError) as e:
+        h.run(A, Wnk, C, mode="fp8", transB=True)
+    assert e.value.status == 2
+    h.set_option("family", "auto")
+    with pytest.raises(dg.GemmError) as e:  # no allocation-free FP8 entry
+        dg.run_small_m_noalloc(A, Wnk, C, mode="fp8", transB=True)
+    assert e.value.status == 2
+    assert h.check_device() == 0
+
+
+def test_fp8_epilogue_bias_gelu(h):
+    """The fused epilogue runs after the FP8 product like after any other."""
+    M, N, K = 16, 8960, 1536
+    a8, w8, alpha = _operands(M, N, K, 80)
+    bias = si.normal((N,), 81).numpy()
+    C = torch.full((M, N), float("nan"), device="cuda")
+    h.run(torch.from_numpy(a8).cuda(), torch.from_numpy(w8).cuda(), C, mode="fp8", transB=True, alpha=alpha,
+          act="gelu", bias=torch.from_numpy(bias).cuda())
+    assert h.check_device() == 0
+    got = C.cpu().numpy()
+    for c0, c1 in _column_ranges(N):
+        Y, D = oracle.gemm("fp8", a8, w8[c0:c1], transB=True, alpha=alpha)
+        ref = oracle.epilogue("gelu", Y, bias[c0:c1])
+        # GELU' is at most 1.13: the product's bound carries through, plus
+        # fp32 rounding of the bias sum and of GELU itself
+        tol = 1.13 * _gate.TOL["fp8"] * abs(alpha) * D + 1e-6 * (np.abs(ref) + np.abs(bias[c0:c1]) + 1e-3)
+        assert np.all(np.abs(got[:, c0:c1] - ref) <= tol), (c0, np.max(np.abs(got[:, c0:c1] - ref) - tol))
