@@ -477,6 +477,11 @@ def sweep_cases(workload):
             for c in si.skinny_cases():
                 case = si.GemmCase(c.name + (".T" if tB else ""), False, tB, c.M, c.N, c.K)
                 out.append((f"bf16.{case.name}", "bf16", case, 1.0, 0.0, 0.02))
+    elif workload == "large_fp8":
+        # E4M3 operands, both K-major (B stored N x K), N(0, 1) codes
+        for M, N, K in ((4096, 4096, 4096),) + si.LARGE_BF16:
+            out.append((f"fp8.{M}x{N}x{K}.T", "fp8", si.GemmCase(f"{M}x{N}x{K}.T", False, True, M, N, K),
+                        1.0, 0.0, 1.0))
     elif workload == "skinny_fp8":
         # E4M3 weights stored N x K (the form the FP8 mode takes), N(0, 1)
         # codes: a per-tensor scale would only change alpha
@@ -891,7 +896,8 @@ def main():
     ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
     ap.add_argument("--pair", type=int, default=None,
                     help="sweeps: force the CTA-pair form (0 planner, 1 none, 2 multicast B, 3 one 256-row MMA per pair)")
-    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "skinny", "skinny_fp8", "epilogue", "gpt_full"],
+    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "large_fp8", "skinny", "skinny_fp8", "epilogue",
+                             "gpt_full"],
                     help="gpt: the timed step; the others print a per-shape sweep")
     ap.add_argument("--mode", default="tf32", choices=["fp32", "tf32", "bf16"],
                     help="gpt_full: the mode of the whole step")

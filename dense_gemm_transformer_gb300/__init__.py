@@ -10,7 +10,7 @@ without the built extension raises.
     C = torch.empty(M, N, device="cuda")
     dg.gemm(A, B, C, mode="tf32")                # C = A @ B
     dg.gemm(A, W, C, mode="bf16", transB=True)   # C = A @ W^T, W stored N x K
-    dg.gemm(X8, W8, C, mode="fp8", transB=True, alpha=sx * sw)  # E4M3 codes, M <= 16
+    dg.gemm(X8, W8, C, mode="fp8", transB=True, alpha=sx * sw)  # E4M3 codes, W stored N x K
 """
 from __future__ import annotations
 

@@ -319,6 +319,7 @@ cudaError_t run_pack(const OperandPack& p, void* dst, int es, cudaStream_t s) {
 // (programmatically launched) kernel.
 constexpr double kBf16Flops = 1.9e15 * 0.8;
 constexpr double kTf32Flops = 0.95e15 * 0.8;
+constexpr double kFp8Flops = 3.8e15 * 0.8;  // twice the bf16 rate (nominal ratio)
 constexpr double kHbmBytes = 6.5e12;
 constexpr double kLaunchS = 1.5e-6;
 
@@ -414,7 +415,8 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   auto pair_ok = [&](int tn) {
     return !swap && tm_tiles >= 2 && h->opt_pair != 1 && dgt::tc_tile_ok(mode, tn, true, b_mn_kernel);
   };
-  const double peak = (mode == GEMM_MODE_BF16 ? kBf16Flops : kTf32Flops) / sms;
+  const double peak =
+      (mode == GEMM_MODE_FP8_E4M3 ? kFp8Flops : mode == GEMM_MODE_BF16 ? kBf16Flops : kTf32Flops) / sms;
   // Pairs of 256-column tiles issue one MMA of 256 rows per pair (tcgen05
   // cta_group::2) unless told to share B by multicast only: each CTA then
   // stages and reads half of B, which measured 1.14x the speed on large
@@ -458,10 +460,8 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   const int64_t tiles = ceil_div(Mk, 128) * ceil_div(Nk, tile_n);
   // Small M with fewer than two waves of weight tiles: the cluster kernel
   // (one tile and K slice per CTA, slices reduced within the cluster).
-  // With more tiles, the persistent kernel streams them without a split;
-  // FP8 is built into the cluster kernel only, which then runs one CTA per
-  // tile.
-  const bool cluster_form = swap && (tiles < 2 * sms || mode == GEMM_MODE_FP8_E4M3);
+  // With more tiles, the persistent kernel streams them without a split.
+  const bool cluster_form = swap && tiles < 2 * sms;
   int64_t splits = 1;
   if (cluster_form) {
     splits = (h->opt_split_k > 0)
@@ -637,10 +637,9 @@ gemm_status_t run_checked(gemm_handle_t h, int mode, int transA, int transB, int
   // MMA side once (activations must be stored M x K).
   const bool skinny_ok = (transA == 0) && M <= 16;
   if (fam == GEMM_FAMILY_SKINNY && !skinny_ok) return GEMM_ERR_NOT_SUPPORTED;
-  // FP8: the small-M product with both operands K-major (the weights
-  // stored N x K); kind::f8f6f4 is used here with K-major operands only.
-  if (mode == GEMM_MODE_FP8_E4M3 && (!skinny_ok || transB != 1 || fam == GEMM_FAMILY_TC))
-    return GEMM_ERR_NOT_SUPPORTED;
+  // FP8: both operands K-major (A stored M x K, B stored N x K);
+  // kind::f8f6f4 is used with K-major operands only.
+  if (mode == GEMM_MODE_FP8_E4M3 && (transA != 0 || transB != 1)) return GEMM_ERR_NOT_SUPPORTED;
   if (fam == GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
   const bool swap = (fam == GEMM_FAMILY_SKINNY) || (fam == GEMM_FAMILY_AUTO && skinny_ok);
   return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, s, swap);

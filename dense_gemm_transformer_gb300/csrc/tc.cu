@@ -115,7 +115,7 @@ cudaError_t tc_init_driver() {
 int tc_tile_k(int mode) { return mode == 3 ? 128 : mode == 2 ? 64 : 32; }
 
 int tc_stages(int mode, int tile_n, bool mma2) {
-  (void)mode;  // a stage holds 128 bytes of K per row in both modes
+  (void)mode;  // a stage holds 128 bytes of K per row in every mode
   if (tile_n == 256 && mma2) return TcCfg<2, 256, true>::STAGES;
   if (tile_n == 256) return TcCfg<2, 256>::STAGES;
   if (tile_n == 224) return TcCfg<2, 224>::STAGES;
@@ -125,17 +125,17 @@ int tc_stages(int mode, int tile_n, bool mma2) {
 }
 
 bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major) {
-  if (mode != 1 && mode != 2) return false;
+  if (mode < 1 || mode > 3) return false;
   if (tile_n != 128 && tile_n != 192 && tile_n != 224 && tile_n != 256) return false;
   if (pair && tile_n == 128) return false;
   if (!b_mn_major) return true;
-  if (mode != 2) return false;  // kind::tf32: K-major operands only
+  if (mode != 2) return false;  // kind::tf32 and the FP8 build: K-major operands only
   const int ch = 64;            // bf16 columns in one 128-byte chunk
   return tile_n % ch == 0 && (!pair || (tile_n / ch) % 2 == 0);
 }
 
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
-  if (a.mode != 1 && a.mode != 2) return cudaErrorInvalidValue;  // FP8 runs in the small-M kernel only
+  if (a.mode < 1 || a.mode > 3) return cudaErrorInvalidValue;
   cudaError_t e = tc_init_driver();
   if (e != cudaSuccess) return e;
   const int bk = tc_tile_k(a.mode);
@@ -195,6 +195,11 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
     if (whole && a.beta == 0.f && p.c_vec)
       p.c_tma = (encode_out_c(a.tma_cache, &tcm, a.C, a.N, a.M, 1, a.ldc, a.M * a.ldc) == cudaSuccess) ? 1 : 0;
   }
+  if (a.mode == 3 && (a.tile_n == 192 || a.tile_n == 224))
+    return tc_launch_fp8_mid(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid,
+                             stream);
+  if (a.mode == 3)
+    return tc_launch_fp8(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid, stream);
   if (a.mode == 2 && (a.tile_n == 192 || a.tile_n == 224))
     return tc_launch_bf16_mid(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid,
                               stream);

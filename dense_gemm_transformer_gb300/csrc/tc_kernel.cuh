@@ -75,15 +75,16 @@ struct TcParams {
   int w_tma;  // partial tiles likewise (tmW is valid)
 };
 
-// MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands).  BHALF: a
+// MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands), 3 = fp8
+// e4m3 (1-byte operands, K-major only).  BHALF: a
 // stage holds one half of the B tile (the two-CTA MMA, where the other CTA
 // of the pair holds the other half).
 template <int MODE, int BN, bool BHALF = false>
 struct TcCfg {
-  static constexpr int ES = (MODE == 2) ? 2 : 4;      // operand bytes
+  static constexpr int ES = (MODE == 3) ? 1 : (MODE == 2) ? 2 : 4;  // operand bytes
   static constexpr int BM = 128;                      // rows of the tile (UMMA M)
   static constexpr int BK = 128 / ES;                 // K elements per stage: one 128-byte swizzle row
-  static constexpr int UK = (MODE == 2) ? 16 : 8;     // K of one MMA instruction (32 bytes)
+  static constexpr int UK = 32 / ES;                  // K of one MMA instruction (32 bytes)
   static constexpr int CH = 128 / ES;                 // M/N elements of one 128-byte MN-major row
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BHALF ? BN * 64 : BN * 128;
@@ -102,7 +103,7 @@ struct TcCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 5;     // full/empty per stage, acc full/empty x2, drain
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
-  static constexpr uint32_t FORMAT = (MODE == 2) ? 1u : 2u;  // bf16 / tf32 in the instruction descriptor
+  static constexpr uint32_t FORMAT = (MODE == 3) ? 0u : (MODE == 2) ? 1u : 2u;  // e4m3 / bf16 / tf32 (descriptor)
   static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
   static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -112,12 +113,16 @@ struct TcCfg {
 template <int MODE, bool MMA2>
 __device__ __forceinline__ void issue_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   if constexpr (MMA2) {
-    if (MODE == 2)
+    if (MODE == 3)
+      mma_f8f6f4_pair(d, a, b, idesc, acc);
+    else if (MODE == 2)
       mma_bf16_pair(d, a, b, idesc, acc);
     else
       mma_tf32_pair(d, a, b, idesc, acc);
   } else {
-    if (MODE == 2)
+    if (MODE == 3)
+      mma_f8f6f4(d, a, b, idesc, acc);
+    else if (MODE == 2)
       mma_bf16(d, a, b, idesc, acc);
     else
       mma_tf32(d, a, b, idesc, acc);

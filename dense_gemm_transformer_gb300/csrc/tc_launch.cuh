@@ -1,6 +1,6 @@
 // tc_launch.cuh -- host-side launch of the tcgen05 kernel for one operand mode
-// (included once by each of tc_tf32.cu and tc_bf16.cu so the two modes
-// compile in parallel).
+// (included by each of tc_tf32.cu, tc_bf16.cu, tc_bf16_mid.cu, tc_fp8.cu and
+// tc_fp8_mid.cu so that the modes compile in parallel).
 #pragma once
 
 #include "tc_kernel.cuh"
@@ -109,7 +109,8 @@ cudaError_t tc_launch_mode_mid(int tile_n, int pair, bool a_mn, bool b_mn, const
 }
 
 // Defined in tc_tf32.cu (MODE 1), tc_bf16.cu (MODE 2: 16, 128 and 256
-// columns) and tc_bf16_mid.cu (MODE 2: 192 and 224 columns).
+// columns), tc_bf16_mid.cu (MODE 2: 192 and 224 columns), tc_fp8.cu and
+// tc_fp8_mid.cu (MODE 3, K-major operands only, the same widths).
 cudaError_t tc_launch_tf32(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid,
                            cudaStream_t s);
@@ -119,5 +120,10 @@ cudaError_t tc_launch_bf16(int tile_n, int pair, bool a_mn, bool b_mn, const CUt
 cudaError_t tc_launch_bf16_mid(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
                                const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                                const TcParams& p, int grid, cudaStream_t s);
+cudaError_t tc_launch_fp8(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+                          const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid, cudaStream_t s);
+cudaError_t tc_launch_fp8_mid(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
+                              const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
+                              const TcParams& p, int grid, cudaStream_t s);
 
 }  // namespace dgt

@@ -9,10 +9,10 @@
  *
  * computed in one of four modes: exact FP32 on the CUDA cores, TF32 on the
  * tensor cores (the mode the page's tensor-core kernel uses, first paragraph),
- * BF16 inputs on the tensor cores, or -- for small M only -- FP8 E4M3 inputs
- * on the tensor cores ("Tensor Cores: Matrix Instructions, Swizzling and FP8,
- * Measured" and "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured"
- * name the format).  Every mode accumulates in FP32 and writes FP32.
+ * BF16 inputs on the tensor cores, or FP8 E4M3 inputs on the tensor cores
+ * ("Tensor Cores: Matrix Instructions, Swizzling and FP8, Measured" and
+ * "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured" name the
+ * format).  Every mode accumulates in FP32 and writes FP32.
  *
  * Layout (all matrices row-major, element (r, c) at base[r * ld + c]):
  *   op(A) is M x K.  transA == 0: A is stored M x K, lda >= max(K, 1).
@@ -29,10 +29,10 @@
  *   In GEMM_MODE_FP8_E4M3, A and B hold 8-bit E4M3 codes of the OCP 8-bit
  *   floating-point format (1 sign, 4 exponent bits with bias 7, 3 mantissa
  *   bits, no infinities, S.1111.111 = NaN, largest magnitude 448); there is
- *   no per-block scale, so per-tensor scale factors go into alpha.  The mode
- *   covers the small-M product only: M <= 16, transA == 0 and transB == 1
- *   (both operands K-major, the weights stored N x K); anything else gives
- *   GEMM_ERR_NOT_SUPPORTED.
+ *   no per-block scale, so per-tensor scale factors go into alpha.  Both
+ *   operands must be K-major: transA == 0 and transB == 1 (A stored M x K,
+ *   B stored N x K, the weights of a linear layer as usually kept); other
+ *   layouts give GEMM_ERR_NOT_SUPPORTED.
  *
  * Ownership: the caller owns A, B and C, which are device memory.  A handle
  * owns its device properties, a device status word and a scratch workspace
@@ -61,7 +61,7 @@ typedef enum {
   GEMM_MODE_TF32 = 1, /* fp32 operands, tcgen05 kind::tf32, fp32 accumulate   */
   GEMM_MODE_BF16 = 2, /* bf16 operands, tcgen05 kind::f16, fp32 accumulate    */
   GEMM_MODE_FP8_E4M3 = 3 /* e4m3 operands, tcgen05 kind::f8f6f4, fp32 accumulate;
-                            M <= 16, transA == 0, transB == 1 only             */
+                            transA == 0 and transB == 1 only                   */
 } gemm_mode_t;
 
 typedef enum {
@@ -79,7 +79,7 @@ typedef enum {
 typedef enum {
   GEMM_FAMILY_AUTO = 0,
   GEMM_FAMILY_SIMT = 1,   /* register-tiled FFMA kernel (GEMM_MODE_FP32 only)           */
-  GEMM_FAMILY_TC = 2,     /* persistent TMA + tcgen05 kernel, 1 CTA per tile (TF32/BF16) */
+  GEMM_FAMILY_TC = 2,     /* persistent TMA + tcgen05 kernel (TF32/BF16/FP8)             */
   GEMM_FAMILY_SKINNY = 3  /* HBM-bound small-M kernels, M <= 16 (TF32/BF16/FP8)         */
 } gemm_family_t;
 
@@ -153,11 +153,10 @@ gemm_status_t gemm_destroy(gemm_handle_t h);
  * (a NaN in C does not propagate).  C must not overlap A or B.  The workspace
  * may grow (cudaMalloc) on the first call that needs a larger one.
  *
- * Small M (M <= 16, transA == 0, TF32/BF16) with fewer than two waves of
+ * Small M (M <= 16, transA == 0, TF32/BF16/FP8) with fewer than two waves of
  * 128-column weight tiles runs one kernel that splits K across the CTAs of a
  * thread-block cluster and sums the slices in distributed shared memory (no
- * workspace).  FP8 always runs that kernel (one CTA per weight tile, no K
- * split, when there are two or more waves of tiles).  It is launched with programmatic dependent launch: its set-up
+ * workspace).  It is launched with programmatic dependent launch: its set-up
  * and an L2 prefetch of the weights may overlap the end of the previous
  * kernel in `stream`, but it reads and writes no memory before that kernel
  * has completed, so stream order is kept. */

@@ -1,7 +1,9 @@
-"""Parity of the FP8 (E4M3) small-M product with the CPU oracle, through the C ABI.
+"""Parity of the FP8 (E4M3) mode with the CPU oracle, through the C ABI.
 
-The FP8 mode runs the decode-shaped tensor-core kernel with kind::f8f6f4:
-both operands K-major (activations M x K, weights stored N x K), M <= 16.
+The FP8 mode runs the tensor-core kernels with kind::f8f6f4, both operands
+K-major (A stored M x K, B stored N x K): the decode-shaped kernel for
+M <= 16 and the persistent tile kernel (every tile width, CTA pairs, K
+splits) above.
 Inputs are quantised per tensor the way FP8 inference stores them (each
 tensor divided by max|t| / 440, rounded to E4M3 by torch on the CPU) and the
 two scales come back through alpha.  The oracle decodes the same codes
@@ -29,13 +31,18 @@ def h():
     handle.close()
 
 
+def _defaults(h):
+    h.set_option("family", "auto")
+    h.set_option("split_k", 0)
+    h.set_option("tile_n", 0)
+    h.set_option("pair", 0)
+
+
 @pytest.fixture(autouse=True)
 def _reset(h):
-    h.set_option("family", "auto")
-    h.set_option("split_k", 0)
+    _defaults(h)
     yield
-    h.set_option("family", "auto")
-    h.set_option("split_k", 0)
+    _defaults(h)
 
 
 def _draw(shape, seed, dist, std=1.0):
@@ -60,23 +67,27 @@ def _device(codes, as_fp8=False):
     return t.view(torch.float8_e4m3fn) if as_fp8 else t
 
 
-def _run_and_check(h, M, N, K, seed, dist="normal", beta=0.0, exact=False, as_fp8=False, cols=None):
+def _run_and_check(h, M, N, K, seed, dist="normal", beta=0.0, exact=False, as_fp8=False, cols=None, rows=None,
+                   family="skinny"):
     a8, w8, alpha = _operands(M, N, K, seed, dist)
     cin = si.normal((M, N), seed + 2).numpy() if beta != 0.0 else None
     C = torch.from_numpy(cin).cuda() if cin is not None else torch.full((M, N), float("nan"), device="cuda")
     h.run(_device(a8, as_fp8), _device(w8, as_fp8), C, mode="fp8", transB=True, alpha=alpha, beta=beta)
     assert h.check_device() == 0
     got = C.cpu().numpy()
-    assert h.plan()["family"] == "skinny"
-    for c0, c1 in cols or [(0, N)]:
-        ref, D = oracle.gemm("fp8", a8, w8[c0:c1], transB=True, alpha=alpha, beta=beta,
-                             C=None if cin is None else np.ascontiguousarray(cin[:, c0:c1]))
-        if exact:
-            assert np.array_equal(got[:, c0:c1].astype(np.float64), ref), (M, N, K, c0)
-        else:
-            _gate.assert_within("fp8", got[:, c0:c1], ref, D, alpha=alpha, beta=beta,
-                                Cin=None if cin is None else cin[:, c0:c1],
-                                what=f"fp8 M={M} N={N} K={K} cols {c0}:{c1}")
+    assert h.plan()["family"] == family
+    for r0, r1 in rows or [(0, M)]:
+        for c0, c1 in cols or [(0, N)]:
+            cpart = None if cin is None else np.ascontiguousarray(cin[:, c0:c1])
+            ref, D = oracle.gemm("fp8", a8, w8[c0:c1], transB=True, alpha=alpha, beta=beta, C=cpart,
+                                 rows=(r0, r1))
+            part = got[r0:r1, c0:c1]
+            if exact:
+                assert np.array_equal(part.astype(np.float64), ref), (M, N, K, r0, c0)
+            else:
+                _gate.assert_within("fp8", part, ref, D, alpha=alpha, beta=beta,
+                                    Cin=None if cpart is None else cpart[r0:r1],
+                                    what=f"fp8 M={M} N={N} K={K} rows {r0}:{r1} cols {c0}:{c1}")
     return got
 
 
@@ -153,7 +164,10 @@ def test_fp8_decode_shapes_sampled(h, M, w):
     _run_and_check(h, M, N, K, seed=si.seed_for(4, w, 5), cols=_column_ranges(N))
     plan = h.plan()
     tiles = -(-N // 128)
-    assert plan["grid"] == tiles * plan["split_k"]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # fewer than two waves of weight tiles: one cluster of K slices per tile;
+    # more: the persistent kernel, one CTA per SM, no split
+    assert plan["grid"] == (tiles * plan["split_k"] if tiles < 2 * sms else sms)
 
 
 @pytest.mark.parametrize("w", range(len(si.SKINNY_WEIGHTS)))
@@ -175,11 +189,11 @@ def test_fp8_unsupported_forms(h):
     with pytest.raises(dg.GemmError) as e:  # activations stored K x M
         h.run(A.t().contiguous(), Wnk, C, mode="fp8", transA=True, transB=True)
     assert e.value.status == 2
-    A17 = torch.zeros((17, 64), dtype=torch.uint8, device="cuda")
-    with pytest.raises(dg.GemmError) as e:  # more than 16 rows
-        h.run(A17, Wnk, torch.zeros((17, 32), device="cuda"), mode="fp8", transB=True)
+    A300 = torch.zeros((300, 64), dtype=torch.uint8, device="cuda")
+    with pytest.raises(dg.GemmError) as e:  # the same above 16 rows
+        h.run(A300, Wnk.t().contiguous(), torch.zeros((300, 32), device="cuda"), mode="fp8")
     assert e.value.status == 2
-    h.set_option("family", "tc")
+    h.set_option("family", "simt")
     with pytest.raises(dg.GemmError) as e:
         h.run(A, Wnk, C, mode="fp8", transB=True)
     assert e.value.status == 2
@@ -207,3 +221,63 @@ def test_fp8_epilogue_bias_gelu(h):
         # fp32 rounding of the bias sum and of GELU itself
         tol = 1.13 * _gate.TOL["fp8"] * abs(alpha) * D + 1e-6 * (np.abs(ref) + np.abs(bias[c0:c1]) + 1e-3)
         assert np.all(np.abs(got[:, c0:c1] - ref) <= tol), (c0, np.max(np.abs(got[:, c0:c1] - ref) - tol))
+
+
+# ------------------------------------------------------------ M > 16: the persistent tile kernel
+@pytest.mark.parametrize("tile_n,pair", [(128, 1), (192, 1), (192, 2), (224, 1), (224, 2), (256, 1), (256, 2),
+                                         (256, 3)])
+def test_fp8_tiles_and_pairs(h, tile_n, pair):
+    """Every tile width, one CTA per tile, pairs sharing B by multicast (2)
+    and pairs issuing one 256-row MMA (3); ragged M, N and K."""
+    h.set_option("tile_n", tile_n)
+    h.set_option("pair", pair)
+    M, N, K = 700, 650, 1008  # K: 8 blocks of 128 bytes, the last one ragged
+    _run_and_check(h, M, N, K, seed=90, family="tc", rows=_cases_rows(M))
+    plan = h.plan()
+    assert plan["tile_n"] == tile_n
+    assert plan["cluster"] == (1 if pair == 1 else 2)
+    assert plan["pair_mma"] == (1 if pair == 3 else 0)
+    _run_and_check(h, M, N, K, seed=91, beta=1.0, family="tc", rows=_cases_rows(M))
+
+
+def _cases_rows(M, tile=128, width=2):
+    picks = sorted({0, tile - 1, 2 * tile - 1, M // 2, M - (M % tile or tile) - 1, M - width})
+    return [(r, min(r + width, M)) for r in picks if 0 <= r < M]
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 300, 512), (100, 129, 2048), (300, 260, 1000), (1000, 1000, 768),
+                                   (2304, 2304, 1024)])
+def test_fp8_planner_shapes(h, M, N, K):
+    """The planner's own choices (tile width, pairs, cut final wave)."""
+    _run_and_check(h, M, N, K, seed=92, family="tc", rows=_cases_rows(M))
+    _run_and_check(h, M, N, K, seed=93, beta=1.0, family="tc", rows=_cases_rows(M))
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7])
+def test_fp8_split_k(h, splits):
+    h.set_option("split_k", splits)
+    M, N, K = 300, 260, 26 * 128 + 64  # 27 K blocks: each count gives that many slices
+    _run_and_check(h, M, N, K, seed=94, family="tc", rows=_cases_rows(M))
+    assert h.plan()["split_k"] == splits
+    _run_and_check(h, M, N, K, seed=95, beta=1.0, family="tc", rows=_cases_rows(M))
+
+
+@pytest.mark.parametrize("tile_n,pair", [(128, 1), (224, 2), (256, 3)])
+def test_fp8_tiles_integers_bit_exact(h, tile_n, pair):
+    h.set_option("tile_n", tile_n)
+    h.set_option("pair", pair)
+    _run_and_check(h, 512, 512, 1024, seed=96, dist="int", exact=True, family="tc")
+
+
+def test_fp8_nonnegative_deep_k(h):
+    """Non-negative operands at K = 8192 (64 K blocks): a missing or doubled
+    block would be 1/64 of every element."""
+    _run_and_check(h, 512, 768, 8192, seed=97, dist="pos", family="tc", rows=_cases_rows(512))
+
+
+@pytest.mark.parametrize("M,N,K", [(8192, 8192, 8192), (8192, 28672, 8192)])
+def test_fp8_large_sampled(h, M, N, K):
+    """The large shapes in FP8 (A stored M x K, B stored N x K), checked on
+    rows at tile edges and on columns around tile edges."""
+    _run_and_check(h, M, N, K, seed=98, family="tc", rows=[(0, 1), (4095, 4097), (M - 1, M)],
+                   cols=_column_ranges(N, tile=256))
