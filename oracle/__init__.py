@@ -13,7 +13,7 @@ kernel), with BLAS scaling:
 
 with the operands first reduced to the mode's precision (FP32: unchanged,
 TF32: reduced to 10 mantissa bits, BF16: bfloat16 inputs widened exactly,
-FP8: E4M3 codes decoded exactly).
+FP8: E4M3 / E5M2 codes decoded exactly, each operand in its mode's format).
 """
 from __future__ import annotations
 
@@ -23,8 +23,9 @@ import subprocess
 
 import numpy as np
 
-MODES = {"fp32": 0, "tf32": 1, "bf16": 2, "fp8": 3}
-_OPERAND_DTYPE = {"fp32": np.float32, "tf32": np.float32, "bf16": np.uint16, "fp8": np.uint8}
+MODES = {"fp32": 0, "tf32": 1, "bf16": 2, "fp8": 3, "fp8_e4m3": 3, "fp8_e5m2": 4, "fp8_e4m3_e5m2": 5,
+         "fp8_e5m2_e4m3": 6}
+_OPERAND_DTYPE = {"fp32": np.float32, "tf32": np.float32, "bf16": np.uint16}
 TF32_RULES = {"truncate": 0, "nearest_away": 1}
 # The reading taken for how the tensor cores treat raw fp32 operands in
 # kind::tf32: the 13 low mantissa bits are dropped.  A GPU test checks this
@@ -67,6 +68,8 @@ def _load():
         lib.oracle_bf16_array.argtypes = [p, p, i64]
         lib.oracle_e4m3_array.restype = None
         lib.oracle_e4m3_array.argtypes = [p, p, i64]
+        lib.oracle_e5m2_array.restype = None
+        lib.oracle_e5m2_array.argtypes = [p, p, i64]
         lib.oracle_gelu.restype = d
         lib.oracle_gelu.argtypes = [d]
         lib.oracle_dgelu.restype = d
@@ -82,7 +85,7 @@ def _ptr(a):
 
 
 def _operand(x, mode):
-    want = _OPERAND_DTYPE[mode]
+    want = _OPERAND_DTYPE.get(mode, np.uint8)  # the FP8 modes take 8-bit codes
     x = np.asarray(x)
     if x.dtype != want:
         raise TypeError(f"mode {mode} takes {want.__name__} operands, got {x.dtype}")
@@ -100,7 +103,8 @@ def gemm(mode, A, B, *, transA=False, transB=False, alpha=1.0, beta=0.0, C=None,
     """Return (Cref, D) as float64 arrays of shape (rows, N).
 
     A, B: 2-D numpy arrays, float32 for fp32/tf32, uint16 bfloat16 bit patterns
-    for bf16, uint8 E4M3 codes for fp8, stored as described for gemm_run
+    for bf16, uint8 codes for the fp8 modes ("fp8" = "fp8_e4m3", "fp8_e5m2",
+    "fp8_e4m3_e5m2": A E4M3 and B E5M2, "fp8_e5m2_e4m3"), stored as described for gemm_run
     (row-major, op() by trans flag).
     C: float32 M x N input, read only when beta != 0.
     rows: (row0, row1) to compute only part of the output.
@@ -148,6 +152,15 @@ def bf16_to_f64(bits):
     bits = np.ascontiguousarray(bits, dtype=np.uint16)
     out = np.empty(bits.shape, dtype=np.float64)
     lib.oracle_bf16_array(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def e5m2_to_f64(codes):
+    """Decode 8-bit E5M2 codes (uint8) to float64 exactly (+-Inf, NaN as in IEEE 754)."""
+    lib = _load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(codes.shape, dtype=np.float64)
+    lib.oracle_e5m2_array(_ptr(codes), _ptr(out), codes.size)
     return out
 
 

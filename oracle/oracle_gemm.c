@@ -34,6 +34,11 @@
  *          with bias 7, 3 mantissa bits, subnormals at exponent 0, no
  *          infinities, and S.1111.111 the only NaN pattern (largest finite
  *          magnitude 448).  Per-tensor scale factors are the caller's alpha.
+ *   FP8 E5M2 and the mixed pairs: E5M2 is the specification's other 8-bit
+ *          format: 1 sign bit, 5 exponent bits with bias 15, 2 mantissa bits,
+ *          subnormals at exponent 0, and exponent 31 holding the infinities
+ *          (mantissa 0) and NaNs as in IEEE 754 (largest finite magnitude
+ *          57344).  Mixed modes take A in one format and B in the other.
  *
  * Conventions the pages leave open (BLAS readings): when K == 0 or alpha == 0
  * A and B are not read; when beta == 0 Cin is not read, so a NaN there does
@@ -55,6 +60,12 @@
 #define ORACLE_MODE_TF32 1
 #define ORACLE_MODE_BF16 2
 #define ORACLE_MODE_FP8_E4M3 3
+#define ORACLE_MODE_FP8_E5M2 4
+#define ORACLE_MODE_FP8_E4M3_E5M2 5 /* A E4M3, B E5M2 */
+#define ORACLE_MODE_FP8_E5M2_E4M3 6 /* A E5M2, B E4M3 */
+
+/* What one operand holds. */
+enum { KIND_FP32, KIND_TF32, KIND_BF16, KIND_E4M3, KIND_E5M2 };
 
 #define ORACLE_TF32_TRUNCATE 0
 #define ORACLE_TF32_NEAREST_AWAY 1
@@ -109,11 +120,36 @@ double oracle_e4m3_to_double(uint8_t code) {
   return s ? -mag : mag;
 }
 
-static double operand(int mode, int tf32_rule, const void* base, int64_t idx) {
-  if (mode == ORACLE_MODE_BF16) return oracle_bf16_to_double(((const uint16_t*)base)[idx]);
-  if (mode == ORACLE_MODE_FP8_E4M3) return oracle_e4m3_to_double(((const uint8_t*)base)[idx]);
+/* An E5M2 code as a double.  Fields: s = bit 7, e = bits 6..2, m = bits 1..0.
+ *   e == 31            : +-Inf when m == 0, NaN otherwise
+ *   e == 0             : (-1)^s * (m / 4) * 2^(1 - 15)      (zero and subnormals)
+ *   otherwise          : (-1)^s * (1 + m / 4) * 2^(e - 15) */
+double oracle_e5m2_to_double(uint8_t code) {
+  const int s = code >> 7, e = (code >> 2) & 31, m = code & 3;
+  if (e == 31) return m ? NAN : (s ? -INFINITY : INFINITY);
+  const double mag = (e == 0) ? ldexp((double)m, 1 - 15 - 2) : ldexp((double)(4 + m), e - 15 - 2);
+  return s ? -mag : mag;
+}
+
+/* The kind of operand `side` (0 = A, 1 = B) in `mode`. */
+static int operand_kind(int mode, int side) {
+  switch (mode) {
+    case ORACLE_MODE_TF32: return KIND_TF32;
+    case ORACLE_MODE_BF16: return KIND_BF16;
+    case ORACLE_MODE_FP8_E4M3: return KIND_E4M3;
+    case ORACLE_MODE_FP8_E5M2: return KIND_E5M2;
+    case ORACLE_MODE_FP8_E4M3_E5M2: return side == 0 ? KIND_E4M3 : KIND_E5M2;
+    case ORACLE_MODE_FP8_E5M2_E4M3: return side == 0 ? KIND_E5M2 : KIND_E4M3;
+    default: return KIND_FP32;
+  }
+}
+
+static double operand(int kind, int tf32_rule, const void* base, int64_t idx) {
+  if (kind == KIND_BF16) return oracle_bf16_to_double(((const uint16_t*)base)[idx]);
+  if (kind == KIND_E4M3) return oracle_e4m3_to_double(((const uint8_t*)base)[idx]);
+  if (kind == KIND_E5M2) return oracle_e5m2_to_double(((const uint8_t*)base)[idx]);
   float v = ((const float*)base)[idx];
-  if (mode == ORACLE_MODE_TF32)
+  if (kind == KIND_TF32)
     v = (tf32_rule == ORACLE_TF32_NEAREST_AWAY) ? oracle_tf32_nearest_away(v) : oracle_tf32_truncate(v);
   return (double)v;
 }
@@ -129,9 +165,13 @@ void oracle_bf16_array(const uint16_t* in, double* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_double(in[i]);
 }
 
-/* Elementwise exact decoding of E4M3 codes (used by the tests). */
+/* Elementwise exact decoding of E4M3 / E5M2 codes (used by the tests). */
 void oracle_e4m3_array(const uint8_t* in, double* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_to_double(in[i]);
+}
+
+void oracle_e5m2_array(const uint8_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e5m2_to_double(in[i]);
 }
 
 /* Returns 0 on success, a negative number for an argument it cannot take. */
@@ -140,7 +180,8 @@ int oracle_gemm(int mode, int tf32_rule, int transA, int transB,
                 const void* A, int64_t lda, const void* B, int64_t ldb,
                 double beta, const float* Cin, int64_t ldc,
                 int64_t row0, int64_t row1, double* Cref, double* D, int64_t ldr) {
-  if (mode < ORACLE_MODE_FP32 || mode > ORACLE_MODE_FP8_E4M3) return -1;
+  if (mode < ORACLE_MODE_FP32 || mode > ORACLE_MODE_FP8_E5M2_E4M3) return -1;
+  const int kind_a = operand_kind(mode, 0), kind_b = operand_kind(mode, 1);
   if (M < 0 || N < 0 || K < 0) return -2;
   if (row0 < 0 || row1 < row0 || row1 > M) return -3;
   if (ldr < N) return -4;
@@ -155,7 +196,7 @@ int oracle_gemm(int mode, int tf32_rule, int transA, int transB,
         for (int64_t k = 0; k < K; ++k) {
           int64_t ia = transA ? k * lda + i : i * lda + k;
           int64_t ib = transB ? j * ldb + k : k * ldb + j;
-          double p = operand(mode, tf32_rule, A, ia) * operand(mode, tf32_rule, B, ib);
+          double p = operand(kind_a, tf32_rule, A, ia) * operand(kind_b, tf32_rule, B, ib);
           acc += p;
           mag += fabs(p);
         }

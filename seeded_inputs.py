@@ -84,7 +84,20 @@ def bf16_bits(t: torch.Tensor):
     return t.contiguous().view(torch.int16).numpy().view("uint16")
 
 
-FP8_E4M3_MAX = 448.0  # largest finite E4M3 magnitude
+FP8_E4M3_MAX = 448.0    # largest finite E4M3 magnitude
+FP8_E5M2_MAX = 57344.0  # largest finite E5M2 magnitude
+
+
+def to_fp8(t: torch.Tensor, fmt: str = "e4m3", amax_to: float = 0.0):
+    """to_fp8_e4m3, or with fmt == "e5m2" the same into E5M2 codes."""
+    if fmt == "e4m3":
+        return to_fp8_e4m3(t, amax_to)
+    s = 1.0
+    if amax_to > 0.0:
+        amax = float(t.abs().max())
+        s = amax / amax_to if amax > 0.0 else 1.0
+    q = (t / s).to(torch.float8_e5m2)
+    return q.contiguous().view(torch.uint8).numpy(), s
 
 
 def to_fp8_e4m3(t: torch.Tensor, amax_to: float = 0.0):

@@ -114,14 +114,46 @@ def test_e4m3_decoding_exhaustive():
     assert np.array_equal(got[0x80:0xFF], -got[:0x7F])
 
 
+def test_e5m2_decoding_exhaustive():
+    """All 256 codes against torch's float8_e5m2 widening, plus values the
+    format fixes (IEEE-style infinities and NaNs at exponent 31)."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e5m2_to_f64(codes)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e5m2).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.flatnonzero(nan).tolist() == [0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF]
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+    fixed = {0x00: 0.0, 0x01: 2.0 ** -16, 0x03: 3 * 2.0 ** -16, 0x04: 2.0 ** -14, 0x3C: 1.0, 0x3E: 1.5,
+             0x40: 2.0, 0x7B: 57344.0, 0x7C: np.inf, 0xBC: -1.0, 0xFC: -np.inf}
+    for c, v in fixed.items():
+        assert got[c] == v, hex(c)
+    assert np.all(np.diff(got[:0x7D]) > 0)
+    assert np.array_equal(got[0x80:0xFD], -got[:0x7D])
+    # E5M2 is E4M3's range traded for precision: every E5M2 value of
+    # magnitude in [2^-6, 448] with one mantissa bit to spare is also E4M3
+    e4 = set(oracle.e4m3_to_f64(codes[:0x7F]).tolist())
+    for v in got[:0x7C]:
+        if 2.0 ** -6 <= v <= 448.0:
+            assert v in e4, v
+
+
+FP8_MODES = ["fp8", "fp8_e5m2", "fp8_e4m3_e5m2", "fp8_e5m2_e4m3"]
+_FP8_TORCH = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+_FP8_SIDES = {"fp8": ("e4m3", "e4m3"), "fp8_e5m2": ("e5m2", "e5m2"), "fp8_e4m3_e5m2": ("e4m3", "e5m2"),
+              "fp8_e5m2_e4m3": ("e5m2", "e4m3")}
+
+
 # ---------------------------------------------------------------- helpers
 def _operands(mode, a, b):
     """numpy operands for the oracle plus their exact values as Fractions."""
-    if mode == "fp8":
-        (ca, _), (cb, _) = si.to_fp8_e4m3(torch.from_numpy(a)), si.to_fp8_e4m3(torch.from_numpy(b))
-        def widen(c):
-            return torch.from_numpy(c.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
-        return ca, cb, widen(ca), widen(cb)
+    if mode in _FP8_SIDES:
+        fa, fb = _FP8_SIDES[mode]
+        (ca, _), (cb, _) = si.to_fp8(torch.from_numpy(a), fa), si.to_fp8(torch.from_numpy(b), fb)
+        def widen(c, f):
+            return torch.from_numpy(c.copy()).view(_FP8_TORCH[f]).to(torch.float64).numpy()
+        return ca, cb, widen(ca, fa), widen(cb, fb)
     if mode == "bf16":
         ab, bb = si.to_bf16(torch.from_numpy(a)), si.to_bf16(torch.from_numpy(b))
         qa, qb = ab.to(torch.float64).numpy(), bb.to(torch.float64).numpy()
@@ -138,7 +170,7 @@ def _op(x, t):
 
 
 # ---------------------------------------------------------------- brute force
-@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16", "fp8"])
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"] + FP8_MODES)
 @pytest.mark.parametrize("tA,tB", TRANS)
 @pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (0.5, 1.0), (-2.0, 0.25)])
 def test_bruteforce_exact_rational(mode, tA, tB, alpha, beta):
@@ -185,7 +217,7 @@ def test_golden_hand_computed_example():
 
 
 # ---------------------------------------------------------------- structure
-@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16", "fp8"])
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"] + FP8_MODES)
 def test_identity_and_permutation(mode):
     rng = np.random.default_rng(3)
     M, N = 9, 11
@@ -209,7 +241,7 @@ def test_identity_and_permutation(mode):
     assert np.array_equal(got, qa2[:, perm])
 
 
-@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16", "fp8"])
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"] + FP8_MODES)
 @pytest.mark.parametrize("tA,tB", TRANS)
 def test_small_integers_are_exact(mode, tA, tB):
     M, N, K = 40, 33, 1024
@@ -235,7 +267,7 @@ def test_rank_one_closed_form():
     assert np.array_equal(D, K * np.abs(np.outer(u, v)).astype(np.float64))
 
 
-@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16", "fp8"])
+@pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"] + FP8_MODES)
 def test_transpose_flags_match_explicit_transpose(mode):
     rng = np.random.default_rng(5)
     M, N, K = 19, 23, 29
