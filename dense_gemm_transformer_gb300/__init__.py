@@ -21,7 +21,11 @@ import threading
 
 from . import _build
 
-MODES = {"fp32": 0, "tf32": 1, "bf16": 2, "fp8": 3}
+MODES = {"fp32": 0, "tf32": 1, "bf16": 2, "fp8": 3, "fp8_e4m3": 3, "fp8_e5m2": 4, "fp8_e4m3_e5m2": 5,
+         "fp8_e5m2_e4m3": 6}
+# The 8-bit format of (A, B) in each FP8 mode.
+FP8_FORMATS = {"fp8": ("e4m3", "e4m3"), "fp8_e4m3": ("e4m3", "e4m3"), "fp8_e5m2": ("e5m2", "e5m2"),
+               "fp8_e4m3_e5m2": ("e4m3", "e5m2"), "fp8_e5m2_e4m3": ("e5m2", "e4m3")}
 FAMILIES = {"auto": 0, "simt": 1, "tc": 2, "skinny": 3}
 OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3, "pretranspose": 4, "pair": 5}
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED", 3: "GEMM_ERR_MISALIGNED",
@@ -128,13 +132,14 @@ def _matrix(t, name):
     return t.data_ptr(), ld
 
 
-def _operand_dtypes(torch, mode):
-    """Tensor types an operand may have in `mode` (fp8: E4M3 codes, as
-    torch.float8_e4m3fn or as raw uint8)."""
+def _operand_dtypes(torch, mode, which):
+    """Tensor types operand `which` (0 = A, 1 = B) may have in `mode`: FP8
+    codes as torch's float8 type of the operand's format or as raw uint8."""
     if mode == "bf16":
         return (torch.bfloat16,)
-    if mode == "fp8":
-        return (torch.float8_e4m3fn, torch.uint8)
+    if mode in FP8_FORMATS:
+        fmt = FP8_FORMATS[mode][which]
+        return (torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2, torch.uint8)
     return (torch.float32,)
 
 
@@ -200,9 +205,10 @@ class Gemm:
         op(B) + beta C) * GELU'(aux), aux the float32 M x N pre-activation.
         """
         import torch
-        want = _operand_dtypes(torch, mode)
-        if A.dtype not in want or B.dtype not in want:
-            raise TypeError(f"mode {mode} takes {want} operands")
+        for which, t in enumerate((A, B)):
+            want = _operand_dtypes(torch, mode, which)
+            if t.dtype not in want:
+                raise TypeError(f"mode {mode} takes {want} for {'AB'[which]}, got {t.dtype}")
         if C.dtype != torch.float32:
             raise TypeError("C must be float32")
         M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])

@@ -53,11 +53,16 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-int elem_bytes(int mode) { return mode == GEMM_MODE_FP8_E4M3 ? 1 : mode == GEMM_MODE_BF16 ? 2 : 4; }
+bool is_fp8(int mode) { return mode >= GEMM_MODE_FP8_E4M3 && mode <= GEMM_MODE_FP8_E5M2_E4M3; }
+int elem_bytes(int mode) { return is_fp8(mode) ? 1 : mode == GEMM_MODE_BF16 ? 2 : 4; }
+// The 8-bit formats of A and B in an FP8 mode (0 = E4M3, 1 = E5M2), the
+// codes the kind::f8f6f4 instruction descriptor takes.
+uint32_t fp8_format_a(int mode) { return (mode == GEMM_MODE_FP8_E5M2 || mode == GEMM_MODE_FP8_E5M2_E4M3) ? 1u : 0u; }
+uint32_t fp8_format_b(int mode) { return (mode == GEMM_MODE_FP8_E5M2 || mode == GEMM_MODE_FP8_E4M3_E5M2) ? 1u : 0u; }
 
 gemm_status_t check_args(int mode, int transA, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                          const void* A, int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc) {
-  if (mode < GEMM_MODE_FP32 || mode > GEMM_MODE_FP8_E4M3) return GEMM_ERR_INVALID_VALUE;
+  if (mode < GEMM_MODE_FP32 || mode > GEMM_MODE_FP8_E5M2_E4M3) return GEMM_ERR_INVALID_VALUE;
   if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return GEMM_ERR_INVALID_VALUE;
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_VALUE;
   if (M == 0 || N == 0) return GEMM_OK;
@@ -385,7 +390,8 @@ int64_t skinny_cluster_size(gemm_handle_s* h, int mode, bool a_mn, int64_t tiles
 
 gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t M, int64_t N, int64_t K,
                      float alpha, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
-                     int64_t ldc, const dgt::EpiParams& epi, cudaStream_t s, bool swap) {
+                     int64_t ldc, const dgt::EpiParams& epi, cudaStream_t s, bool swap, uint32_t fmt_a = 0,
+                     uint32_t fmt_b = 0) {
   using namespace dgt;
   const int es = elem_bytes(mode);
   const int bk = tc_tile_k(mode);
@@ -544,6 +550,8 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
 
   TcArgs a{};
   a.mode = mode;
+  // the kernel's operands are the caller's exchanged in the swapped form
+  a.fmt8 = mode == GEMM_MODE_FP8_E4M3 ? fp8_format_bits(swap ? fmt_b : fmt_a, swap ? fmt_a : fmt_b) : 0u;
   a.a_mn_major = a_mn ? 1 : 0;
   a.b_mn_major = b_mn ? 1 : 0;
   a.tile_n = tile_n;
@@ -639,9 +647,14 @@ gemm_status_t run_checked(gemm_handle_t h, int mode, int transA, int transB, int
   if (fam == GEMM_FAMILY_SKINNY && !skinny_ok) return GEMM_ERR_NOT_SUPPORTED;
   // FP8: both operands K-major (A stored M x K, B stored N x K);
   // kind::f8f6f4 is used with K-major operands only.
-  if (mode == GEMM_MODE_FP8_E4M3 && (transA != 0 || transB != 1)) return GEMM_ERR_NOT_SUPPORTED;
+  if (is_fp8(mode) && (transA != 0 || transB != 1)) return GEMM_ERR_NOT_SUPPORTED;
   if (fam == GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
   const bool swap = (fam == GEMM_FAMILY_SKINNY) || (fam == GEMM_FAMILY_AUTO && skinny_ok);
+  // Every FP8 mode runs the kernels' 8-bit build (GEMM_MODE_FP8_E4M3) with
+  // its operand formats named at run time.
+  if (is_fp8(mode))
+    return run_tc(h, GEMM_MODE_FP8_E4M3, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, s, swap,
+                  fp8_format_a(mode), fp8_format_b(mode));
   return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, s, swap);
 }
 

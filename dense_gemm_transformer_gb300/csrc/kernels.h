@@ -124,7 +124,9 @@ cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream);
 // an smem ring fed by a TMA producer warp, a single-thread MMA issuer with a
 // double-buffered TMEM accumulator, and four epilogue warps.
 struct TcArgs {
-  int mode;              // 1 = tf32, 2 = bf16, 3 = fp8 e4m3 (gemm_mode_t; fp8: small-M kernel only)
+  int mode;              // 1 = tf32, 2 = bf16, 3 = 8-bit floats (formats in fmt8)
+  uint32_t fmt8;         // mode 3: the A and B formats of the kernel's operands, as instruction
+                         // descriptor bits (fp8_format_bits); 0 otherwise
   int a_mn_major;        // A stored with M contiguous (transA == 1)
   int b_mn_major;        // B stored with N contiguous (transB == 0)
   int tile_n;            // 128, 192, 224 or 256 (16: the swapped small-M form)
@@ -156,6 +158,9 @@ struct TcArgs {
 // kernel stores its tile transposed into the caller's C.
 constexpr int kTcEpiWarps = 8;                        // epilogue warps (two per TMEM lane quarter)
 constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);  // producer + MMA warps + epilogue warps
+// The A / B format fields (bits 7-9 / 10-12) of a kind::f8f6f4 instruction
+// descriptor: 0 = E4M3, 1 = E5M2.
+constexpr uint32_t fp8_format_bits(uint32_t a_fmt, uint32_t b_fmt) { return (a_fmt << 7) | (b_fmt << 10); }
 int tc_tile_k(int mode);              // k elements per stage (128 bytes)
 int tc_stages(int mode, int tile_n, bool mma2);  // pipeline depth (mma2: one 256-row MMA per CTA pair)
 // Whether the kernel is built for this tile width, pairing and B layout

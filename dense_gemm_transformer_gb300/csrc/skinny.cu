@@ -41,7 +41,8 @@
 namespace dgt {
 namespace {
 
-// MODE: 1 TF32 (fp32 operands), 2 BF16, 3 FP8 E4M3 (8-bit codes).
+// MODE: 1 TF32 (fp32 operands), 2 BF16, 3 8-bit floats (E4M3 / E5M2 codes,
+// the formats named at run time in SkParams::fmt8).
 template <int MODE>
 struct SkCfg {
   static constexpr int ES = (MODE == 3) ? 1 : (MODE == 2) ? 2 : 4;  // operand bytes
@@ -59,7 +60,7 @@ struct SkCfg {
   static constexpr int RECV_BYTES = (BN * BM / 4 + kSkinnyMaxCluster) * 16;  // shares pushed by the peers
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + RECV_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr int PREFETCH_KB = 16;              // K blocks of weights warmed in L2 before the wait
-  static constexpr uint32_t FORMAT = (MODE == 3) ? 0u : (MODE == 2) ? 1u : 2u;  // e4m3 / bf16 / tf32
+  static constexpr uint32_t FORMAT = (MODE == 3) ? 0u : (MODE == 2) ? 1u : 2u;  // 8-bit (fmt8) / bf16 / tf32
   static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM (228 KB, 1 KB reserved per CTA)");
   static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
   static_assert(BM * BN * 4 <= STAGES * STAGE_BYTES, "the partial tile fits in the drained stages");
@@ -82,7 +83,8 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
                        const SkParams p) {
   using Cfg = SkCfg<MODE>;
   constexpr int S = Cfg::STAGES;
-  constexpr uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN, false, Cfg::BM, Cfg::BN);
+  // MODE 3 names its operand formats at run time (the FORMAT fields are 0).
+  const uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN, false, Cfg::BM, Cfg::BN) | (MODE == 3 ? p.fmt8 : 0u);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

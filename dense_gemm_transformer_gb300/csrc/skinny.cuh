@@ -22,6 +22,7 @@ struct SkParams {
   float* C;     // caller's C, element (m, n) at C[m * ldc + n]
   int64_t ldc;
   int* status;  // device status word (bounded waits)
+  uint32_t fmt8;  // mode 3: operand format bits of the instruction descriptor (E4M3 / E5M2)
 };
 
 constexpr int kSkinnyThreads = 192;  // TMA producer warp, MMA warp, four epilogue warps
@@ -30,8 +31,8 @@ constexpr int kSkinnyMaxCluster = 16;
 constexpr int kSkinnyStages = 5;  // with the 8 KB receive buffer ~100 KB of shared memory: two CTAs per SM
 
 // Launch on `grid` = tiles * p.cluster CTAs, clusters of p.cluster CTAs
-// along x, with programmatic dependent launch.  mode: 1 TF32, 2 BF16, 3 FP8
-// E4M3.  a_mn: the weights are stored with the caller's N contiguous
+// along x, with programmatic dependent launch.  mode: 1 TF32, 2 BF16, 3 8-bit
+// floats (p.fmt8).  a_mn: the weights are stored with the caller's N contiguous
 // (transB == 0); BF16 only.
 cudaError_t skinny_launch(int mode, bool a_mn, const CUtensorMap& ta, const CUtensorMap& tb, const SkParams& p,
                           int grid, cudaStream_t s);

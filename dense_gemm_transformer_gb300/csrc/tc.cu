@@ -175,6 +175,7 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.ws_slice = a.ws_slice;
   p.ws_row0 = a.ws_row0;
   p.status = a.status;
+  p.fmt8 = a.mode == 3 ? a.fmt8 : 0u;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
   // Tiles leave through TMA stores when the destination allows it: not the
   // transposed small-M form, no read of C (beta == 0, or partial sums), and
@@ -231,6 +232,7 @@ cudaError_t launch_skinny(const TcArgs& a, cudaStream_t stream) {
   p.C = a.C;
   p.ldc = a.ldc;
   p.status = a.status;
+  p.fmt8 = a.mode == 3 ? a.fmt8 : 0u;
   return skinny_launch(a.mode, a.a_mn_major != 0, ta, tb, p, a.grid, stream);
 }
 

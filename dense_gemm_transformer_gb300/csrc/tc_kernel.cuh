@@ -73,10 +73,12 @@ struct TcParams {
   int c_vec;  // C rows are 16-byte aligned (ldc % 4 == 0 and C aligned)
   int c_tma;  // whole tiles leave through shared memory and TMA stores (tmC is valid)
   int w_tma;  // partial tiles likewise (tmW is valid)
+  uint32_t fmt8;  // MODE 3: operand format bits of the instruction descriptor (E4M3 / E5M2)
 };
 
-// MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands), 3 = fp8
-// e4m3 (1-byte operands, K-major only).  BHALF: a
+// MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands), 3 = 8-bit
+// floats (E4M3 or E5M2, named at run time in TcParams::fmt8; K-major only).
+// BHALF: a
 // stage holds one half of the B tile (the two-CTA MMA, where the other CTA
 // of the pair holds the other half).
 template <int MODE, int BN, bool BHALF = false>
@@ -103,7 +105,7 @@ struct TcCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 5;     // full/empty per stage, acc full/empty x2, drain
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
-  static constexpr uint32_t FORMAT = (MODE == 3) ? 0u : (MODE == 2) ? 1u : 2u;  // e4m3 / bf16 / tf32 (descriptor)
+  static constexpr uint32_t FORMAT = (MODE == 3) ? 0u : (MODE == 2) ? 1u : 2u;  // 8-bit (fmt8) / bf16 / tf32
   static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
   static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -218,7 +220,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int EXTRA_BARS = A_TMEM ? 2 * NA : 0;
   static_assert((Cfg::NUM_BARS + EXTRA_BARS) * 8 + 16 <= 256, "barrier area");
   static_assert(!A_TMEM || A_COL0 + NA * Cfg::BK <= TMEM_COLS, "TMEM columns");
-  constexpr uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN && !A_TMEM, B_MN, MMA2 ? 2 * Cfg::BM : Cfg::BM, BN);
+  // MODE 3 names its operand formats at run time (the FORMAT fields are 0).
+  const uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN && !A_TMEM, B_MN, MMA2 ? 2 * Cfg::BM : Cfg::BM, BN) |
+                         (MODE == 3 ? p.fmt8 : 0u);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

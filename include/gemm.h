@@ -26,10 +26,13 @@
  *   mantissa bits.  The TF32 tensor-core instruction reads K-major operands
  *   only, so in TF32 mode an operand stored with M (or N) contiguous (A with
  *   transA == 1, B with transB == 0) is first transposed into the workspace.
- *   In GEMM_MODE_FP8_E4M3, A and B hold 8-bit E4M3 codes of the OCP 8-bit
- *   floating-point format (1 sign, 4 exponent bits with bias 7, 3 mantissa
- *   bits, no infinities, S.1111.111 = NaN, largest magnitude 448); there is
- *   no per-block scale, so per-tensor scale factors go into alpha.  Both
+ *   In the FP8 modes, A and B hold 8-bit codes of the OCP 8-bit
+ *   floating-point formats: E4M3 (1 sign, 4 exponent bits with bias 7, 3
+ *   mantissa bits, no infinities, S.1111.111 = NaN, largest magnitude 448)
+ *   or E5M2 (5 exponent bits with bias 15, 2 mantissa bits, infinities and
+ *   NaNs as in IEEE 754, largest magnitude 57344), each operand in the
+ *   format its mode names; there is no per-block scale, so per-tensor scale
+ *   factors go into alpha.  Both
  *   operands must be K-major: transA == 0 and transB == 1 (A stored M x K,
  *   B stored N x K, the weights of a linear layer as usually kept); other
  *   layouts give GEMM_ERR_NOT_SUPPORTED.
@@ -60,8 +63,11 @@ typedef enum {
   GEMM_MODE_FP32 = 0, /* fp32 operands, FFMA on CUDA cores, exact fp32 products */
   GEMM_MODE_TF32 = 1, /* fp32 operands, tcgen05 kind::tf32, fp32 accumulate   */
   GEMM_MODE_BF16 = 2, /* bf16 operands, tcgen05 kind::f16, fp32 accumulate    */
-  GEMM_MODE_FP8_E4M3 = 3 /* e4m3 operands, tcgen05 kind::f8f6f4, fp32 accumulate;
-                            transA == 0 and transB == 1 only                   */
+  GEMM_MODE_FP8_E4M3 = 3,      /* e4m3 A and B, tcgen05 kind::f8f6f4, fp32 accumulate;
+                                  transA == 0 and transB == 1 only (every FP8 mode) */
+  GEMM_MODE_FP8_E5M2 = 4,      /* e5m2 A and B                                          */
+  GEMM_MODE_FP8_E4M3_E5M2 = 5, /* e4m3 A, e5m2 B                                        */
+  GEMM_MODE_FP8_E5M2_E4M3 = 6  /* e5m2 A, e4m3 B                                        */
 } gemm_mode_t;
 
 typedef enum {

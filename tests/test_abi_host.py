@@ -48,7 +48,9 @@ def test_validate_accepts_good_arguments(lib):
 
 
 def test_validate_rejects_bad_flags_and_sizes(lib):
-    assert dg.validate(4, 0, 0, 8, 8, 8, 1.0, P, 8, P, 8, P, 8) == INVALID
+    assert dg.validate(7, 0, 0, 8, 8, 8, 1.0, P, 8, P, 8, P, 8) == INVALID
+    for fp8_mode in (4, 5, 6):  # E5M2 and the mixed pairs
+        assert dg.validate(fp8_mode, 0, 1, 8, 8, 8, 1.0, P + 1, 8, P + 3, 8, P, 8) == OK
     # FP8 (mode 3): one-byte operands, so any operand address is aligned
     assert dg.validate(3, 0, 1, 8, 8, 8, 1.0, P + 1, 8, P + 3, 8, P, 8) == OK
     assert dg.validate(-1, 0, 0, 8, 8, 8, 1.0, P, 8, P, 8, P, 8) == INVALID

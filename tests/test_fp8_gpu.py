@@ -53,33 +53,42 @@ def _draw(shape, seed, dist, std=1.0):
     return si.normal(shape, seed, std=std)
 
 
-def _operands(M, N, K, seed, dist="normal"):
-    """E4M3 codes of the activations (M x K) and weights (N x K) and the
-    alpha that undoes their per-tensor scales (1 for integers)."""
-    amax = 0.0 if dist == "int" else 440.0
-    a8, sa = si.to_fp8_e4m3(_draw((M, K), seed, dist), amax)
-    w8, sw = si.to_fp8_e4m3(_draw((N, K), seed + 1, dist, std=0.02), amax)
+FORMATS = {"fp8": ("e4m3", "e4m3"), "fp8_e5m2": ("e5m2", "e5m2"), "fp8_e4m3_e5m2": ("e4m3", "e5m2"),
+           "fp8_e5m2_e4m3": ("e5m2", "e4m3")}
+OTHER_MODES = ["fp8_e5m2", "fp8_e4m3_e5m2", "fp8_e5m2_e4m3"]
+_AMAX = {"e4m3": 440.0, "e5m2": 0.98 * si.FP8_E5M2_MAX}
+_TORCH = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
+
+def _operands(M, N, K, seed, dist="normal", mode="fp8"):
+    """8-bit codes of the activations (M x K) and weights (N x K), each in
+    its mode's format, and the alpha that undoes their per-tensor scales
+    (1 for integers)."""
+    fa, fb = FORMATS[mode]
+    a8, sa = si.to_fp8(_draw((M, K), seed, dist), fa, 0.0 if dist == "int" else _AMAX[fa])
+    w8, sw = si.to_fp8(_draw((N, K), seed + 1, dist, std=0.02), fb, 0.0 if dist == "int" else _AMAX[fb])
     return a8, w8, sa * sw
 
 
-def _device(codes, as_fp8=False):
+def _device(codes, as_fp8=False, fmt="e4m3"):
     t = torch.from_numpy(codes).cuda()
-    return t.view(torch.float8_e4m3fn) if as_fp8 else t
+    return t.view(_TORCH[fmt]) if as_fp8 else t
 
 
 def _run_and_check(h, M, N, K, seed, dist="normal", beta=0.0, exact=False, as_fp8=False, cols=None, rows=None,
-                   family="skinny"):
-    a8, w8, alpha = _operands(M, N, K, seed, dist)
+                   family="skinny", mode="fp8"):
+    a8, w8, alpha = _operands(M, N, K, seed, dist, mode)
+    fa, fb = FORMATS[mode]
     cin = si.normal((M, N), seed + 2).numpy() if beta != 0.0 else None
     C = torch.from_numpy(cin).cuda() if cin is not None else torch.full((M, N), float("nan"), device="cuda")
-    h.run(_device(a8, as_fp8), _device(w8, as_fp8), C, mode="fp8", transB=True, alpha=alpha, beta=beta)
+    h.run(_device(a8, as_fp8, fa), _device(w8, as_fp8, fb), C, mode=mode, transB=True, alpha=alpha, beta=beta)
     assert h.check_device() == 0
     got = C.cpu().numpy()
     assert h.plan()["family"] == family
     for r0, r1 in rows or [(0, M)]:
         for c0, c1 in cols or [(0, N)]:
             cpart = None if cin is None else np.ascontiguousarray(cin[:, c0:c1])
-            ref, D = oracle.gemm("fp8", a8, w8[c0:c1], transB=True, alpha=alpha, beta=beta, C=cpart,
+            ref, D = oracle.gemm(mode, a8, w8[c0:c1], transB=True, alpha=alpha, beta=beta, C=cpart,
                                  rows=(r0, r1))
             part = got[r0:r1, c0:c1]
             if exact:
@@ -87,7 +96,7 @@ def _run_and_check(h, M, N, K, seed, dist="normal", beta=0.0, exact=False, as_fp
             else:
                 _gate.assert_within("fp8", part, ref, D, alpha=alpha, beta=beta,
                                     Cin=None if cpart is None else cpart[r0:r1],
-                                    what=f"fp8 M={M} N={N} K={K} rows {r0}:{r1} cols {c0}:{c1}")
+                                    what=f"{mode} M={M} N={N} K={K} rows {r0}:{r1} cols {c0}:{c1}")
     return got
 
 
@@ -281,3 +290,43 @@ def test_fp8_large_sampled(h, M, N, K):
     rows at tile edges and on columns around tile edges."""
     _run_and_check(h, M, N, K, seed=98, family="tc", rows=[(0, 1), (4095, 4097), (M - 1, M)],
                    cols=_column_ranges(N, tile=256))
+
+
+# ------------------------------------------------------------ E5M2 and the mixed pairs
+@pytest.mark.parametrize("mode", OTHER_MODES)
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 768), (16, 129, 2048), (3, 65, 40)])
+def test_fp8_formats_small_m(h, mode, M, N, K):
+    """The small-M kernel exchanges the operands (C^T = B^T A^T), so the
+    formats must follow them: a mixed pair catches a missed exchange."""
+    _run_and_check(h, M, N, K, seed=101, mode=mode)
+    _run_and_check(h, M, N, K, seed=102, beta=1.0, mode=mode, as_fp8=True)
+
+
+@pytest.mark.parametrize("mode", OTHER_MODES)
+@pytest.mark.parametrize("tile_n,pair", [(128, 1), (224, 2), (256, 3)])
+def test_fp8_formats_tiles(h, mode, tile_n, pair):
+    h.set_option("tile_n", tile_n)
+    h.set_option("pair", pair)
+    _run_and_check(h, 700, 650, 1008, seed=103, family="tc", rows=_cases_rows(700), mode=mode)
+
+
+@pytest.mark.parametrize("mode", OTHER_MODES)
+def test_fp8_formats_integers_bit_exact(h, mode):
+    h.set_option("split_k", 5)
+    _run_and_check(h, 16, 260, 1792, seed=104, dist="int", exact=True, mode=mode)
+    h.set_option("split_k", 0)
+    _run_and_check(h, 512, 512, 1024, seed=105, dist="int", exact=True, family="tc", mode=mode)
+
+
+@pytest.mark.parametrize("mode", OTHER_MODES)
+@pytest.mark.parametrize("w", [0, 2])
+def test_fp8_formats_decode_shapes(h, mode, w):
+    """1536 x 8960 (cluster kernel) and 1536 x 151936 (the persistent
+    kernel's swapped form), M = 16, sampled columns."""
+    K, N = si.SKINNY_WEIGHTS[w]
+    _run_and_check(h, 16, N, K, seed=si.seed_for(4, w, 9), cols=_column_ranges(N), mode=mode)
+
+
+def test_fp8_formats_large_sampled(h):
+    _run_and_check(h, 4096, 4096, 4096, seed=106, family="tc", rows=[(0, 2), (2047, 2049), (4094, 4096)],
+                   cols=_column_ranges(4096, tile=256), mode="fp8_e5m2_e4m3")
