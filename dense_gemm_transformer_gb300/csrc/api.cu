@@ -300,7 +300,7 @@ OperandPack plan_pack(const void* src, int64_t ld, int64_t rows, int64_t cols, b
   p.rows = rows;
   p.cols = cols;
   p.mn_major_after = mn_major;
-  if (mode == GEMM_MODE_TF32 && mn_major && !mn_ok) {
+  if ((mode == GEMM_MODE_TF32 || mode == GEMM_MODE_FP8_E4M3) && mn_major && !mn_ok) {
     p.kind = OperandPack::kTranspose;  // stored K x MN -> MN x K
     p.dst_ld = round_up(rows, 16 / es);
     p.bytes = static_cast<size_t>(cols * p.dst_ld * es);
@@ -501,9 +501,10 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   // Workspace: re-packed operands and split-K partials.  An operand is copied
   // when the TMA unit cannot read it in place (base not 16-byte aligned, or a
   // row pitch that is not a multiple of 16 bytes), and transposed into K-major
-  // order when it is MN-major in TF32 mode: kind::tf32 takes K-major operands
-  // from shared memory only (an MN-major TF32 operand produced zeros on this
-  // part, while BF16 reads both orders).  The exception is an MN-major A with
+  // order when it is MN-major in TF32 or FP8 mode: kind::tf32 takes K-major
+  // operands from shared memory only (an MN-major TF32 operand produced zeros
+  // on this part, while BF16 reads both orders), and the FP8 build reads
+  // K-major operands only.  The exception is an MN-major A with
   // 128-column tiles and no CTA pairs: that kernel moves A into TMEM, where
   // the MMA reads it row by row, so no transpose pass is needed (unless
   // pretranspose = 2 asks for one).  The warps that move A slow the MMA
@@ -645,9 +646,6 @@ gemm_status_t run_checked(gemm_handle_t h, int mode, int transA, int transB, int
   // MMA side once (activations must be stored M x K).
   const bool skinny_ok = (transA == 0) && M <= 16;
   if (fam == GEMM_FAMILY_SKINNY && !skinny_ok) return GEMM_ERR_NOT_SUPPORTED;
-  // FP8: both operands K-major (A stored M x K, B stored N x K);
-  // kind::f8f6f4 is used with K-major operands only.
-  if (is_fp8(mode) && (transA != 0 || transB != 1)) return GEMM_ERR_NOT_SUPPORTED;
   if (fam == GEMM_FAMILY_SIMT) return GEMM_ERR_NOT_SUPPORTED;
   const bool swap = (fam == GEMM_FAMILY_SKINNY) || (fam == GEMM_FAMILY_AUTO && skinny_ok);
   // Every FP8 mode runs the kernels' 8-bit build (GEMM_MODE_FP8_E4M3) with

@@ -285,6 +285,9 @@ cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t
   const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
   const dim3 blocks(grid_for(tiles * 256, 256));
   const dim3 block(32, 8);
+  if (elem_bytes == 1)
+    return launch_pdl(transpose_kernel<uint8_t>, blocks, block, 0, stream, static_cast<const uint8_t*>(src), ld_src,
+                      static_cast<uint8_t*>(dst), ld_dst, rows, cols);
   if (elem_bytes == 2)
     return launch_pdl(transpose_kernel<uint16_t>, blocks, block, 0, stream, static_cast<const uint16_t*>(src),
                       ld_src, static_cast<uint16_t*>(dst), ld_dst, rows, cols);

@@ -32,10 +32,10 @@
  *   or E5M2 (5 exponent bits with bias 15, 2 mantissa bits, infinities and
  *   NaNs as in IEEE 754, largest magnitude 57344), each operand in the
  *   format its mode names; there is no per-block scale, so per-tensor scale
- *   factors go into alpha.  Both
- *   operands must be K-major: transA == 0 and transB == 1 (A stored M x K,
- *   B stored N x K, the weights of a linear layer as usually kept); other
- *   layouts give GEMM_ERR_NOT_SUPPORTED.
+ *   factors go into alpha.  The FP8 kernels read K-major operands (A
+ *   stored M x K, B stored N x K, the weights of a linear layer as usually
+ *   kept) in place; an FP8 operand stored MN-major is first transposed into
+ *   the workspace, as in TF32 mode.
  *
  * Ownership: the caller owns A, B and C, which are device memory.  A handle
  * owns its device properties, a device status word and a scratch workspace
@@ -64,7 +64,7 @@ typedef enum {
   GEMM_MODE_TF32 = 1, /* fp32 operands, tcgen05 kind::tf32, fp32 accumulate   */
   GEMM_MODE_BF16 = 2, /* bf16 operands, tcgen05 kind::f16, fp32 accumulate    */
   GEMM_MODE_FP8_E4M3 = 3,      /* e4m3 A and B, tcgen05 kind::f8f6f4, fp32 accumulate;
-                                  transA == 0 and transB == 1 only (every FP8 mode) */
+                                  K-major operands read in place (every FP8 mode)   */
   GEMM_MODE_FP8_E5M2 = 4,      /* e5m2 A and B                                          */
   GEMM_MODE_FP8_E4M3_E5M2 = 5, /* e4m3 A, e5m2 B                                        */
   GEMM_MODE_FP8_E5M2_E4M3 = 6  /* e5m2 A, e4m3 B                                        */

@@ -1,9 +1,9 @@
 """Parity of the FP8 (E4M3) mode with the CPU oracle, through the C ABI.
 
-The FP8 mode runs the tensor-core kernels with kind::f8f6f4, both operands
-K-major (A stored M x K, B stored N x K): the decode-shaped kernel for
-M <= 16 and the persistent tile kernel (every tile width, CTA pairs, K
-splits) above.
+The FP8 modes run the tensor-core kernels with kind::f8f6f4 on K-major
+operands (A stored M x K, B stored N x K; an MN-major operand is transposed
+first): the decode-shaped kernel for M <= 16 and the persistent tile kernel
+(every tile width, CTA pairs, K splits) above.
 Inputs are quantised per tensor the way FP8 inference stores them (each
 tensor divided by max|t| / 440, rounded to E4M3 by torch on the CPU) and the
 two scales come back through alpha.  The oracle decodes the same codes
@@ -187,21 +187,33 @@ def test_fp8_nonnegative_operands_catch_a_missing_k_block(h, w):
     _run_and_check(h, 16, N, K, seed=si.seed_for(4, w, 7), dist="pos", cols=_column_ranges(N))
 
 
-# ------------------------------------------------------------ what the mode does not take
+# ------------------------------------------------------------ MN-major operands
+@pytest.mark.parametrize("mode", ["fp8", "fp8_e4m3_e5m2"])
+@pytest.mark.parametrize("tA,tB", [(False, False), (True, False), (True, True), (False, True)])
+@pytest.mark.parametrize("M,N,K", [(300, 260, 1024), (4, 1000, 768)])
+def test_fp8_any_layout(h, mode, tA, tB, M, N, K):
+    """An operand stored MN-major (A as K x M, B as K x N) is transposed into
+    the workspace first; the kernels then read K-major operands."""
+    a8, w8, alpha = _operands(M, N, K, 107, mode=mode)
+    A = np.ascontiguousarray(a8.T) if tA else a8      # op(A) = A^T when stored K x M
+    B = w8 if tB else np.ascontiguousarray(w8.T)      # op(B) = B^T when stored N x K
+    C = torch.full((M, N), float("nan"), device="cuda")
+    h.run(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), C, mode=mode, transA=tA, transB=tB, alpha=alpha)
+    assert h.check_device() == 0
+    plan = h.plan()
+    swapped = plan["family"] == "skinny"
+    assert swapped == (M <= 16 and not tA)
+    # packed bit 0: A, bit 1: B (re-packed or transposed)
+    assert bool(plan["packed"] & 1) == tA
+    assert bool(plan["packed"] & 2) == (not tB)
+    ref, D = oracle.gemm(mode, A, B, transA=tA, transB=tB, alpha=alpha)
+    _gate.assert_within("fp8", C.cpu().numpy(), ref, D, alpha=alpha, what=f"{mode} tA={tA} tB={tB}")
+
+
 def test_fp8_unsupported_forms(h):
     A = torch.zeros((4, 64), dtype=torch.uint8, device="cuda")
     Wnk = torch.zeros((32, 64), dtype=torch.uint8, device="cuda")
     C = torch.zeros((4, 32), device="cuda")
-    with pytest.raises(dg.GemmError) as e:  # weights stored K x N (MN-major)
-        h.run(A, Wnk.t().contiguous(), C, mode="fp8", transB=False)
-    assert e.value.status == 2
-    with pytest.raises(dg.GemmError) as e:  # activations stored K x M
-        h.run(A.t().contiguous(), Wnk, C, mode="fp8", transA=True, transB=True)
-    assert e.value.status == 2
-    A300 = torch.zeros((300, 64), dtype=torch.uint8, device="cuda")
-    with pytest.raises(dg.GemmError) as e:  # the same above 16 rows
-        h.run(A300, Wnk.t().contiguous(), torch.zeros((300, 32), device="cuda"), mode="fp8")
-    assert e.value.status == 2
     h.set_option("family", "simt")
     with pytest.raises(dg.GemmError) as e:
         h.run(A, Wnk, C, mode="fp8", transB=True)
