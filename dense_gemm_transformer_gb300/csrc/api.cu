@@ -414,7 +414,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   // bytes each: that makes a 128-column tile 3/4 as fast per column as a
   // 256-column one, as measured on square and large shapes.  Ties go to the
   // wider tile.  The B layout the kernel reads is MN-major only for BF16
-  // (TF32 operands are made K-major).
+  // (TF32 and FP8 operands are made K-major).
   const bool b_mn_kernel = (mode == GEMM_MODE_BF16) && tb_k == 0;
   const int64_t tm_tiles = ceil_div(Mk, 128);
   const int64_t kb = ceil_div(K, bk);
