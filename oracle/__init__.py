@@ -70,6 +70,12 @@ def _load():
         lib.oracle_e4m3_array.argtypes = [p, p, i64]
         lib.oracle_e5m2_array.restype = None
         lib.oracle_e5m2_array.argtypes = [p, p, i64]
+        for name in ("oracle_e2m1_array", "oracle_e8m0_array", "oracle_ue4m3_array"):
+            getattr(lib, name).restype = None
+            getattr(lib, name).argtypes = [p, p, i64]
+        lib.oracle_gemm_block_scaled.restype = ctypes.c_int
+        lib.oracle_gemm_block_scaled.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, i64, i64, i64, d,
+                                                 p, i64, p, i64, p, i64, p, i64, d, p, i64, i64, i64, p, p, i64]
         lib.oracle_gelu.restype = d
         lib.oracle_gelu.argtypes = [d]
         lib.oracle_dgelu.restype = d
@@ -171,6 +177,73 @@ def e4m3_to_f64(codes):
     out = np.empty(codes.shape, dtype=np.float64)
     lib.oracle_e4m3_array(_ptr(codes), _ptr(out), codes.size)
     return out
+
+
+def _decode(fn_name, codes):
+    lib = _load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(codes.shape, dtype=np.float64)
+    getattr(lib, fn_name)(_ptr(codes), _ptr(out), codes.size)
+    return out
+
+
+def e2m1_to_f64(codes):
+    """Decode 4-bit E2M1 codes (uint8 values 0..15, one per byte) exactly."""
+    return _decode("oracle_e2m1_array", codes)
+
+
+def e8m0_to_f64(codes):
+    """Decode E8M0 scale codes: 2^(e - 127), NaN for 0xFF."""
+    return _decode("oracle_e8m0_array", codes)
+
+
+def ue4m3_to_f64(codes):
+    """Decode UE4M3 scale codes: the E4M3 magnitude, sign bit ignored."""
+    return _decode("oracle_ue4m3_array", codes)
+
+
+ELEMENT_FORMATS = {"e4m3": 0, "e5m2": 1, "e2m1": 2}
+SCALE_FORMATS = {"e8m0": 0, "ue4m3": 1}
+# The block-scaled formats: (element format, block size, scale format).
+BLOCK_SCALED = {"mxfp8_e4m3": ("e4m3", 32, "e8m0"), "mxfp8_e5m2": ("e5m2", 32, "e8m0"),
+                "mxfp4": ("e2m1", 32, "e8m0"), "nvfp4": ("e2m1", 16, "ue4m3")}
+
+
+def gemm_block_scaled(fmt_a, fmt_b, A, SA, B, SB, *, block, scale_fmt, alpha=1.0, beta=0.0, C=None, rows=None):
+    """Return (Cref, D) of the block-scaled product, float64 (rows, N).
+
+    A: uint8 M x K codes (M x K/2 bytes for e2m1, two per byte, the even
+    element in the low nibble); SA: uint8 M x ceil(K / block) scale codes.
+    B and SB likewise for B stored N x K (K-major).  fmt_a / fmt_b: "e4m3",
+    "e5m2" or "e2m1"; scale_fmt: "e8m0" or "ue4m3".  K is A's width in
+    elements (twice its bytes for e2m1, so K is even there)."""
+    lib = _load()
+    A, SA, B, SB = (np.ascontiguousarray(x, dtype=np.uint8) for x in (A, SA, B, SB))
+    M, N = A.shape[0], B.shape[0]
+    K = A.shape[1] * (2 if fmt_a == "e2m1" else 1)
+    Kb = B.shape[1] * (2 if fmt_b == "e2m1" else 1)
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    nb = -(-K // block)
+    if SA.shape != (M, nb) or SB.shape != (N, nb):
+        raise ValueError(f"scales must be {M} x {nb} and {N} x {nb}")
+    row0, row1 = rows if rows is not None else (0, M)
+    if beta != 0.0:
+        C = np.asarray(C)
+        if C is None or C.dtype != np.float32 or C.shape != (M, N) or C.strides[1] != 4:
+            raise ValueError("beta != 0 needs C, float32 M x N with unit column stride")
+        ldc = C.strides[0] // 4
+    else:
+        C, ldc = None, max(N, 1)
+    out = np.zeros((row1 - row0, N), dtype=np.float64)
+    D = np.zeros((row1 - row0, N), dtype=np.float64)
+    rc = lib.oracle_gemm_block_scaled(ELEMENT_FORMATS[fmt_a], ELEMENT_FORMATS[fmt_b], SCALE_FORMATS[scale_fmt],
+                                      int(block), M, N, K, float(alpha), _ptr(A), max(A.shape[1], 1), _ptr(SA),
+                                      max(nb, 1), _ptr(B), max(B.shape[1], 1), _ptr(SB), max(nb, 1), float(beta),
+                                      _ptr(C), ldc, row0, row1, _ptr(out), _ptr(D), max(N, 1))
+    if rc != 0:
+        raise ValueError(f"oracle_gemm_block_scaled rejected its arguments ({rc})")
+    return out, D
 
 
 ACTIVATIONS = {"none": 0, "gelu": 1, "dgelu": 2}

@@ -253,3 +253,107 @@ int oracle_epilogue(int act, int64_t rows, int64_t N, const double* y, int64_t l
   }
   return 0;
 }
+
+/*
+ * Block-scaled products: the MX formats and NVFP4.  "Low-Precision Kernels:
+ * INT4, INT8 and FP8 Matmuls, Measured" (its summary) names FP8, MX and
+ * NVFP4 scales without defining them; the reading taken is the OCP
+ * Microscaling (MX) specification and NVIDIA's NVFP4 layout:
+ *
+ *   every run of `bs` consecutive K elements of a row of A (and of a row of
+ *   the N x K-stored B) shares one scale; an element's value is its scale
+ *   times its own decoded value, so
+ *
+ *   Cref[i][j] = alpha * sum_k (SA[i][k / bs] * a[i][k]) * (SB[j][k / bs] * b[j][k])
+ *                + beta * Cin[i][j]
+ *   D[i][j]    =         sum_k |SA[i][k / bs] * a[i][k]| * |SB[j][k / bs] * b[j][k]|
+ *
+ *   MXFP8: elements E4M3 or E5M2, bs = 32, scales E8M0.
+ *   MXFP4: elements E2M1, bs = 32, scales E8M0.
+ *   NVFP4: elements E2M1, bs = 16, scales UE4M3 (and a per-tensor factor,
+ *          which is the caller's alpha).
+ *
+ * Element formats: 0 = E4M3, 1 = E5M2, 2 = E2M1.  E2M1 elements are packed
+ * two to a byte, element 2t in the low four bits of byte t.
+ * Scale formats: 0 = E8M0, 1 = UE4M3.
+ * Both operands are K-major: A is M x K (row pitch lda bytes), B is N x K
+ * (ldb bytes); SA is M x ceil(K / bs) bytes (pitch ldsa), SB N x ceil(K / bs)
+ * (ldsb).  The last block of a row may be partial.
+ */
+
+/* E2M1: s = bit 3, e = bits 2..1 (bias 1), m = bit 0; no infinities or NaNs.
+ *   e == 0 : (-1)^s * (m / 2) * 2^(1 - 1)
+ *   else   : (-1)^s * (1 + m / 2) * 2^(e - 1)
+ * giving the magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double oracle_e2m1_to_double(uint8_t code) {
+  const int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  const double mag = (e == 0) ? ldexp((double)m, -1) : ldexp((double)(2 + m), e - 2);
+  return s ? -mag : mag;
+}
+
+/* E8M0: an exponent alone, 2^(e - 127); 0xFF is NaN. */
+double oracle_e8m0_to_double(uint8_t code) {
+  if (code == 0xFF) return NAN;
+  return ldexp(1.0, (int)code - 127);
+}
+
+/* UE4M3: the E4M3 magnitude of the code with its sign bit ignored. */
+double oracle_ue4m3_to_double(uint8_t code) { return oracle_e4m3_to_double((uint8_t)(code & 0x7F)); }
+
+static double block_element(int fmt, const uint8_t* row, int64_t k) {
+  if (fmt == 2) {
+    const uint8_t byte = row[k >> 1];
+    return oracle_e2m1_to_double((uint8_t)((k & 1) ? (byte >> 4) : (byte & 15)));
+  }
+  return fmt == 1 ? oracle_e5m2_to_double(row[k]) : oracle_e4m3_to_double(row[k]);
+}
+
+static double block_scale(int scale_fmt, uint8_t code) {
+  return scale_fmt == 1 ? oracle_ue4m3_to_double(code) : oracle_e8m0_to_double(code);
+}
+
+void oracle_e2m1_array(const uint8_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_to_double(in[i]);
+}
+
+void oracle_e8m0_array(const uint8_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e8m0_to_double(in[i]);
+}
+
+void oracle_ue4m3_array(const uint8_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_ue4m3_to_double(in[i]);
+}
+
+/* Returns 0 on success, a negative number for an argument it cannot take. */
+int oracle_gemm_block_scaled(int fmt_a, int fmt_b, int scale_fmt, int64_t bs, int64_t M, int64_t N, int64_t K,
+                             double alpha, const uint8_t* A, int64_t lda, const uint8_t* SA, int64_t ldsa,
+                             const uint8_t* B, int64_t ldb, const uint8_t* SB, int64_t ldsb, double beta,
+                             const float* Cin, int64_t ldc, int64_t row0, int64_t row1, double* Cref, double* D,
+                             int64_t ldr) {
+  if (fmt_a < 0 || fmt_a > 2 || fmt_b < 0 || fmt_b > 2 || scale_fmt < 0 || scale_fmt > 1) return -1;
+  if (M < 0 || N < 0 || K < 0 || bs < 1) return -2;
+  if (row0 < 0 || row1 < row0 || row1 > M) return -3;
+  if (ldr < N) return -4;
+  const int read_ab = (K > 0 && alpha != 0.0);
+  const int read_c = (beta != 0.0);
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = row0; i < row1; ++i) {
+    for (int64_t j = 0; j < N; ++j) {
+      double acc = 0.0, mag = 0.0;
+      if (read_ab) {
+        for (int64_t k = 0; k < K; ++k) {
+          const double a = block_scale(scale_fmt, SA[i * ldsa + k / bs]) * block_element(fmt_a, A + i * lda, k);
+          const double b = block_scale(scale_fmt, SB[j * ldsb + k / bs]) * block_element(fmt_b, B + j * ldb, k);
+          acc += a * b;
+          mag += fabs(a * b);
+        }
+      }
+      double c = alpha * acc;
+      if (read_c) c += beta * (double)Cin[i * ldc + j];
+      Cref[(i - row0) * ldr + j] = c;
+      if (D) D[(i - row0) * ldr + j] = mag;
+    }
+  }
+  return 0;
+}

@@ -376,6 +376,154 @@ def test_fp8_gate_catches_one_missing_k_block_on_nonnegative_operands():
     _gate.assert_within("fp8", ref.astype(np.float32), ref, D)
 
 
+# ------------------------------------------------------------ block-scaled (MX / NVFP4)
+# The E2M1 magnitudes as the OCP Microscaling specification tabulates them.
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_values():
+    got = oracle.e2m1_to_f64(np.arange(16, dtype=np.uint8))
+    assert got[:8].tolist() == E2M1_VALUES
+    assert np.array_equal(got[8:], -got[:8]) and np.signbit(got[8])
+
+
+def test_e8m0_scales():
+    got = oracle.e8m0_to_f64(np.arange(256, dtype=np.uint8))
+    assert got[127] == 1.0 and got[128] == 2.0 and got[126] == 0.5
+    assert got[0] == 2.0 ** -127 and got[254] == 2.0 ** 127
+    assert np.isnan(got[255]) and not np.isnan(got[:255]).any()
+    assert np.all(got[1:255] / got[:254] == 2.0)
+
+
+def test_ue4m3_scales_are_e4m3_magnitudes():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.ue4m3_to_f64(codes)
+    want = np.abs(torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy())
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def _fp8_values(codes, fmt):
+    """Exact values of element codes, decoded without the oracle: torch's
+    float8 widening, or the E2M1 table (two codes per byte, low nibble first)."""
+    if fmt == "e2m1":
+        lo, hi = codes & 15, codes >> 4
+        nib = np.stack([lo, hi], axis=-1).reshape(codes.shape[0], -1)
+        mag = np.array(E2M1_VALUES)[nib & 7]
+        return np.where(nib & 8, -mag, mag)
+    dt = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    return torch.from_numpy(codes.copy()).view(dt).to(torch.float64).numpy()
+
+
+def _scale_values(codes, scale_fmt):
+    if scale_fmt == "e8m0":
+        return np.vectorize(lambda c: Fraction(2) ** (int(c) - 127))(codes)
+    return np.abs(torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy())
+
+
+def _random_codes(rng, rows, K, fmt):
+    if fmt == "e2m1":
+        return rng.integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
+    codes = rng.integers(0, 256, size=(rows, K), dtype=np.uint8)
+    nan = np.isnan(_fp8_values(codes, fmt)) | np.isinf(_fp8_values(codes, fmt))
+    codes[nan] = 0x38 if fmt == "e4m3" else 0x3C  # 1.0 in place of the non-finite codes
+    return codes
+
+
+@pytest.mark.parametrize("fmt_a,fmt_b,block,scale_fmt", [
+    ("e4m3", "e4m3", 32, "e8m0"), ("e5m2", "e4m3", 32, "e8m0"), ("e4m3", "e5m2", 32, "e8m0"),
+    ("e2m1", "e2m1", 32, "e8m0"), ("e2m1", "e2m1", 16, "ue4m3")])
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (-0.75, 0.5)])
+def test_block_scaled_exact_rational(fmt_a, fmt_b, block, scale_fmt, alpha, beta):
+    """Every output against a Fraction evaluation of the definition, with
+    elements and scales decoded without the oracle; K ends in a partial
+    block, and every block has its own scale."""
+    rng = np.random.default_rng(hash((fmt_a, fmt_b, block, alpha)) % 2 ** 32)
+    M, N, K = 3, 4, 2 * block + 6
+    nb = -(-K // block)
+    A, B = _random_codes(rng, M, K, fmt_a), _random_codes(rng, N, K, fmt_b)
+    if scale_fmt == "e8m0":
+        SA, SB = (rng.integers(118, 137, size=(r, nb), dtype=np.uint8) for r in (M, N))
+    else:
+        SA, SB = (rng.integers(0x20, 0x58, size=(r, nb), dtype=np.uint8) for r in (M, N))
+    c = rng.standard_normal((M, N)).astype(np.float32)
+    got, D = oracle.gemm_block_scaled(fmt_a, fmt_b, A, SA, B, SB, block=block, scale_fmt=scale_fmt,
+                                      alpha=alpha, beta=beta, C=c)
+    va, vb = _fp8_values(A, fmt_a), _fp8_values(B, fmt_b)
+    sa, sb = _scale_values(SA, scale_fmt), _scale_values(SB, scale_fmt)
+    for i in range(M):
+        for j in range(N):
+            terms = [Fraction(sa[i, k // block]) * Fraction(float(va[i, k])) *
+                     Fraction(sb[j, k // block]) * Fraction(float(vb[j, k])) for k in range(K)]
+            exact = Fraction(alpha) * sum(terms) + Fraction(beta) * Fraction(float(c[i, j]))
+            d = sum(abs(t) for t in terms)
+            bound = 2 * (K + 2) * 2.0 ** -53 * (abs(alpha) * float(d) + abs(beta * float(c[i, j])))
+            assert abs(Fraction(float(got[i, j])) - exact) <= Fraction(bound), (i, j)
+            assert abs(Fraction(float(D[i, j])) - d) <= Fraction(2 * K * 2.0 ** -53 * float(d))
+
+
+@pytest.mark.parametrize("mode,fa,fb", [("fp8", "e4m3", "e4m3"), ("fp8_e5m2", "e5m2", "e5m2"),
+                                        ("fp8_e4m3_e5m2", "e4m3", "e5m2")])
+def test_block_scaled_unit_scales_is_the_plain_product(mode, fa, fb):
+    """Scales of 1 (E8M0 code 127) reduce MXFP8 to the per-tensor FP8
+    product, which has its own pins."""
+    rng = np.random.default_rng(7)
+    M, N, K = 9, 11, 100
+    A, B = _random_codes(rng, M, K, fa), _random_codes(rng, N, K, fb)
+    ones_a = np.full((M, 4), 127, dtype=np.uint8)
+    ones_b = np.full((N, 4), 127, dtype=np.uint8)
+    got, D = oracle.gemm_block_scaled(fa, fb, A, ones_a, B, ones_b, block=32, scale_fmt="e8m0", alpha=0.5)
+    ref, Dref = oracle.gemm(mode, A, B, transB=True, alpha=0.5)
+    assert np.array_equal(got, ref) and np.array_equal(D, Dref)
+
+
+def test_block_scale_applies_to_its_own_block_only():
+    """A scale of 8 on block 1 of one row of A multiplies that block's
+    share of the row's products and nothing else (a wrong block index, or
+    a scale taken from the wrong row, fails)."""
+    rng = np.random.default_rng(8)
+    M, N, K, bs = 4, 5, 90, 32  # blocks 0..31, 32..63, 64..89
+    A, B = _random_codes(rng, M, K, "e4m3"), _random_codes(rng, N, K, "e4m3")
+    SA = np.full((M, 3), 127, dtype=np.uint8)
+    SB = np.full((N, 3), 127, dtype=np.uint8)
+    SA[2, 1] = 130  # 2^3
+    got, D = oracle.gemm_block_scaled("e4m3", "e4m3", A, SA, B, SB, block=bs, scale_fmt="e8m0")
+    inside = np.zeros_like(A)
+    inside[:, 32:64] = A[:, 32:64]
+    outside = A.copy()
+    outside[:, 32:64] = 0
+    p_in, _ = oracle.gemm("fp8", inside, B, transB=True)
+    p_out, _ = oracle.gemm("fp8", outside, B, transB=True)
+    want = p_in + p_out
+    want[2] = 8.0 * p_in[2] + p_out[2]
+    assert np.allclose(got, want, rtol=0, atol=1e-12 * D.max())
+    # NVFP4-sized blocks: the same scale codes now cover 16 elements each
+    SA16 = np.full((M, 6), 0x38, dtype=np.uint8)  # UE4M3 1.0
+    SB16 = np.full((N, 6), 0x38, dtype=np.uint8)
+    SA16[1, 5] = 0x40  # 2.0 on elements 80..89 of row 1
+    A4 = _random_codes(rng, M, K, "e2m1")
+    B4 = _random_codes(rng, N, K, "e2m1")
+    got4, D4 = oracle.gemm_block_scaled("e2m1", "e2m1", A4, SA16, B4, SB16, block=16, scale_fmt="ue4m3")
+    va, vb = _fp8_values(A4, "e2m1"), _fp8_values(B4, "e2m1")
+    want4 = va @ vb.T
+    want4[1] += (va[1, 80:] @ vb[:, 80:].T)  # doubled: the scale of 2 adds one more copy
+    assert np.allclose(got4, want4, rtol=0, atol=1e-12 * max(D4.max(), 1.0))
+
+
+def test_e2m1_packing_low_nibble_first():
+    """Byte t holds elements 2t (low four bits) and 2t + 1 (high four bits)."""
+    K = 8
+    B = np.full((1, K // 2), 0x22, dtype=np.uint8)  # every element 1.0
+    SB = np.full((1, 1), 127, dtype=np.uint8)
+    SA = np.full((1, 1), 127, dtype=np.uint8)
+    for k in range(K):
+        A = np.zeros((1, K // 2), dtype=np.uint8)
+        A[0, k // 2] = (7 << 4) if k % 2 else 5  # 6.0 high, or 3.0 low
+        got, _ = oracle.gemm_block_scaled("e2m1", "e2m1", A, SA, B, SB, block=32, scale_fmt="e8m0")
+        assert got[0, 0] == (6.0 if k % 2 else 3.0)
+
+
 # ------------------------------------------------------------ fused epilogue
 # Standard normal distribution function Phi at 1, 2 and -1 as tabulated
 # (Abramowitz and Stegun, table 26.1, to 10 digits).  GELU(x) = x * Phi(x).
