@@ -75,3 +75,20 @@ def test_sweep_processes_merge_takes_the_median_process():
     assert out[1]["ms"] == 2.0 and out[1]["roofline_frac"] == 0.25
     with pytest.raises(ValueError):
         bench.merge_process_runs([[mk("a", 1.0)], [mk("b", 1.0)]])
+
+
+def test_fp8_sweeps_time_the_k_major_form_against_the_fp8_peak():
+    """The FP8 sweeps time B stored N x K (the form the kernels read in
+    place, no transpose pass), one byte per operand element, against twice
+    the measured bf16 tensor rate (the nominal FP8 / BF16 ratio)."""
+    import bench
+    for workload in ("large_fp8", "skinny_fp8"):
+        cases = bench.sweep_cases(workload)
+        assert cases and all(mode == "fp8" and c.transB and not c.transA for _, mode, c, *_ in cases)
+    assert {(c.M, c.N, c.K) for _, _, c, *_ in bench.sweep_cases("large_fp8")} == \
+        {(4096, 4096, 4096), (8192, 8192, 8192), (8192, 28672, 8192)}
+    assert len(bench.sweep_cases("skinny_fp8")) == 9
+    pk = bench.peaks()
+    assert pk["fp8_tflops"] == 2 * pk["bf16_tflops"]
+    assert pk["fp8_tflops_sustained"] == 2 * pk["bf16_tflops_sustained"]
+    assert bench._elem_bytes("fp8") == 1
