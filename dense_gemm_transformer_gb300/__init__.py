@@ -199,6 +199,12 @@ class Gemm:
             act="none", bias=None, aux=None):
         """C = alpha * op(A) op(B) + beta * C on torch CUDA tensors (row-major).
 
+        mode: "fp32", "tf32", "bf16", or an FP8 mode ("fp8" = "fp8_e4m3",
+        "fp8_e5m2", "fp8_e4m3_e5m2", "fp8_e5m2_e4m3": the formats of A and B),
+        whose operands are torch.float8_e4m3fn / torch.float8_e5m2 tensors or
+        raw uint8 codes; FP8 is fastest with A stored M x K and B stored N x K
+        (transB=True), which the kernels read in place.
+
         With act / bias / aux, the fused epilogue of gemm_run_epilogue:
         act "none" or "gelu": C = act(alpha op(A) op(B) + beta C + bias) with
         bias a float32 vector of N (or None); act "dgelu": C = (alpha op(A)
