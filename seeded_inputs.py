@@ -117,6 +117,71 @@ def to_fp8_e4m3(t: torch.Tensor, amax_to: float = 0.0):
     return q.contiguous().view(torch.uint8).numpy(), s
 
 
+# Largest magnitudes of the block-scaled element formats and the exponent of
+# each one's largest power of two (448 = 1.75 * 2^8, 57344 = 1.75 * 2^15,
+# 6 = 1.5 * 2^2).
+_ELEM_MAX = {"e4m3": (448.0, 8), "e5m2": (57344.0, 15), "e2m1": (6.0, 2)}
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _e2m1_codes(x):
+    """Round to the nearest E2M1 value (ties to the even code), saturating
+    at +-6; returns 4-bit codes as uint8."""
+    import numpy as np
+    mags = np.array(E2M1_MAGNITUDES)
+    a = np.minimum(np.abs(x), 6.0)
+    d = np.abs(a[..., None] - mags)
+    best = d.min(axis=-1, keepdims=True)
+    tie = (d == best)
+    # among equally near values take the even code (mantissa bit 0)
+    even = tie & ((np.arange(8) % 2) == 0)
+    idx = np.where(even.any(axis=-1), even.argmax(axis=-1), tie.argmax(axis=-1)).astype(np.uint8)
+    return np.where(np.signbit(x) & (idx > 0), idx | 8, idx).astype(np.uint8)
+
+
+def to_block_scaled(t: torch.Tensor, elem: str = "e4m3", block: int = 32, scale: str = "e8m0"):
+    """Quantise a rows x K fp32 tensor to a block-scaled format: every run of
+    `block` elements of a row gets one scale, chosen from the run's largest
+    magnitude, and the elements are rounded to `elem` after division by it.
+
+    E8M0 scales (MX): 2^(floor(log2 amax) - e), e the exponent of the
+    element format's largest power of two, so the run's largest element lands
+    in the format's top binade.  UE4M3 scales (NVFP4): amax / 6 rounded to
+    E4M3.  An all-zero run takes the scale 1.  Returns (element codes as
+    uint8 -- two E2M1 codes per byte, the even element in the low nibble --,
+    scale codes as uint8 rows x ceil(K / block))."""
+    import numpy as np
+    x = t.to(torch.float64).numpy()
+    rows, K = x.shape
+    nb = -(-K // block)
+    pad = np.zeros((rows, nb * block))
+    pad[:, :K] = x
+    amax = np.abs(pad.reshape(rows, nb, block)).max(axis=-1)
+    emax_val, emax_exp = _ELEM_MAX[elem]
+    if scale == "e8m0":
+        e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - emax_exp, 0.0)
+        e = np.clip(e, -127, 127)
+        scodes = (e + 127).astype(np.uint8)
+        sval = np.ldexp(1.0, e.astype(np.int64))
+    else:
+        want = torch.from_numpy(np.where(amax > 0, amax / 6.0, 1.0)).to(torch.float8_e4m3fn)
+        scodes = want.view(torch.uint8).numpy().copy()
+        sval = want.to(torch.float64).numpy()
+        sval = np.where(sval > 0, sval, 1.0)
+        scodes = np.where(want.to(torch.float64).numpy() > 0, scodes, np.uint8(0x38))
+    y = pad / np.repeat(sval, block, axis=1)
+    y = np.clip(y, -emax_val, emax_val)[:, :K]
+    if elem == "e2m1":
+        if K % 2:
+            raise ValueError("E2M1 rows need an even K (two codes per byte)")
+        c = _e2m1_codes(y)
+        codes = (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    else:
+        dt = torch.float8_e4m3fn if elem == "e4m3" else torch.float8_e5m2
+        codes = torch.from_numpy(y).to(dt).view(torch.uint8).numpy().copy()
+    return codes, scodes.astype(np.uint8)
+
+
 @dataclass(frozen=True)
 class GemmCase:
     """One GEMM of a workload: C (M x N) = alpha op(A) op(B) + beta C."""
