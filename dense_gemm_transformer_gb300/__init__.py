@@ -27,7 +27,8 @@ MODES = {"fp32": 0, "tf32": 1, "bf16": 2, "fp8": 3, "fp8_e4m3": 3, "fp8_e5m2": 4
 FP8_FORMATS = {"fp8": ("e4m3", "e4m3"), "fp8_e4m3": ("e4m3", "e4m3"), "fp8_e5m2": ("e5m2", "e5m2"),
                "fp8_e4m3_e5m2": ("e4m3", "e5m2"), "fp8_e5m2_e4m3": ("e5m2", "e4m3")}
 FAMILIES = {"auto": 0, "simt": 1, "tc": 2, "skinny": 3}
-OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3, "pretranspose": 4, "pair": 5}
+OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3, "pretranspose": 4, "pair": 5, "wait_limit_us": 6,
+           "fault_skip_stage": 7}
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED", 3: "GEMM_ERR_MISALIGNED",
           4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_ALLOC", 6: "GEMM_ERR_DEVICE_TIMEOUT", 7: "GEMM_ERR_TOO_LARGE"}
 HEADER = os.path.join(_build.ROOT, "include", "gemm.h")

@@ -40,6 +40,8 @@ struct gemm_handle_s {
   int opt_tile_n = 0;
   int opt_pretranspose = 0;
   int opt_pair = 0;
+  int64_t opt_wait_us = 0;   // bounded-wait limit of the tcgen05 kernel (0: the default)
+  int opt_fault_skip = 0;    // test hook (GEMM_OPT_FAULT_SKIP_STAGE)
   int sk_active[3][dgt::kSkinnyMaxCluster + 1];  // small-M kernel per mode (TF32, BF16, FP8): resident clusters (-1: not queried)
   dgt::TmaCache* tma_cache = nullptr;             // TMA descriptors of earlier calls
   gemm_plan_t plan{};
@@ -407,9 +409,9 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
 
   // Tile width (128, 192, 224 or 256 columns) and schedule: the least
   // estimated time over waves of work units, a unit being one tile per CTA
-  // or, where two CTAs share each B tile, two vertically adjacent tiles per
-  // CTA pair; the last rows of units may be cut into K slices to fill the
-  // final wave (plan_tail).  A tile's time is taken as proportional to the
+  // or, where a CTA pair issues one 256-row MMA, two vertically adjacent
+  // tiles per pair; the last rows of units may be cut into K slices to fill
+  // the final wave (plan_tail).  A tile's time is taken as proportional to the
   // shared-memory bytes of one stage, A (128 rows) + B (tile_n rows) of 128
   // bytes each: that makes a 128-column tile 3/4 as fast per column as a
   // 256-column one, as measured on square and large shapes.  Ties go to the
@@ -419,26 +421,26 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   const int64_t tm_tiles = ceil_div(Mk, 128);
   const int64_t kb = ceil_div(K, bk);
   auto pair_ok = [&](int tn) {
-    return !swap && tm_tiles >= 2 && h->opt_pair != 1 && dgt::tc_tile_ok(mode, tn, true, b_mn_kernel);
+    return !swap && tm_tiles >= 2 && h->opt_pair != 1 && h->opt_fault_skip == 0 &&
+           dgt::tc_tile_ok(mode, tn, true, b_mn_kernel);
   };
   const double peak =
       (mode == GEMM_MODE_FP8_E4M3 ? kFp8Flops : mode == GEMM_MODE_BF16 ? kBf16Flops : kTf32Flops) / sms;
-  // Pairs of 256-column tiles issue one MMA of 256 rows per pair (tcgen05
-  // cta_group::2) unless told to share B by multicast only: each CTA then
-  // stages and reads half of B, which measured 1.14x the speed on large
-  // shapes (BF16 8192^3: 1687 -> 1929 TFLOP/s).  TF32 stages twice the bytes
-  // per FLOP, and with 24 or more K blocks the halved B measured worth more:
-  // on the N = 384 GPT products (K = 1152-1536) the 256-column pairs, padding
-  // N to 512, ran 8-10% faster than 192-column pairs (MLP-down forward 46.9
-  // -> 42.4 us), which a factor of 1.3 reproduces; with short K the tile's
-  // fixed cost dominates and 1.14 still ranks the widths as measured.
-  auto mma2_for = [&](int tn) { return tn == 256 && pair_ok(tn) && (h->opt_pair == 0 || h->opt_pair == 3); };
-  const double mma2_gain = (mode == GEMM_MODE_TF32 && kb >= 24) ? 1.3 : 1.14;
+  // A CTA pair issues one MMA of 256 rows (tcgen05 cta_group::2): each CTA
+  // then stages and reads half of B, which measured 1.14x the speed on large
+  // shapes (BF16 8192^3: 1687 -> 1929 TFLOP/s at 256 columns).  TF32 stages
+  // twice the bytes per FLOP, and with 24 or more K blocks the halved B
+  // measured worth more: on the N = 384 GPT products (K = 1152-1536) the
+  // 256-column pairs, padding N to 512, ran 8-10% faster than 192-column
+  // tiles (MLP-down forward 46.9 -> 42.4 us), which a factor of 1.3
+  // reproduces; with short K the tile's fixed cost dominates and 1.14 still
+  // ranks the widths as measured.
+  const double pair_gain = (mode == GEMM_MODE_TF32 && kb >= 24) ? 1.3 : 1.14;
   auto plan_for = [&](int tn) {
     const bool pr = pair_ok(tn);
     const int64_t rows = pr ? ceil_div(tm_tiles, 2) : tm_tiles;
     const double unit_s = 2.0 * 128.0 * 256.0 * static_cast<double>(K) / peak *
-                          (128.0 * 128.0 + 128.0 * tn) / (128.0 * 384.0) / (mma2_for(tn) ? mma2_gain : 1.0);
+                          (128.0 * 128.0 + 128.0 * tn) / (128.0 * 384.0) / (pr ? pair_gain : 1.0);
     const double c_row_bytes = 4.0 * static_cast<double>(Nk) * (pr ? 256.0 : 128.0);
     const bool may_cut = !swap && h->opt_split_k == 0 && !(2 * tm_tiles * ceil_div(Nk, tn) <= sms && kb >= 8);
     if (!may_cut) {
@@ -593,10 +595,12 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.dp_units = static_cast<int>(tail.rows > 0 ? (unit_rows - tail.rows) * unit_cols : 0);
   a.tail_tm0 = static_cast<int>(tail.rows > 0 ? unit_rows - tail.rows : 0);
   a.status = h->d_status;
-  // Two-CTA clusters sharing each B tile (TMA multicast) for tiles of 192
-  // columns or more with at least two rows of tiles: each CTA then pulls
-  // half of B per stage from L2 (256 columns: 32 KB instead of 48 KB).
-  a.pair = !pair ? 0 : mma2_for(tile_n) ? 2 : 1;
+  a.wait_ns = static_cast<uint64_t>(h->opt_wait_us) * 1000u;
+  a.fault_skip = h->opt_fault_skip;
+  // CTA pairs issuing one 256-row MMA for tiles of 192 columns or more
+  // with at least two rows of tiles: each CTA then stages half of B per
+  // stage (256 columns: 32 KB instead of 48 KB).
+  a.pair = pair ? 1 : 0;
   const int64_t units = a.dp_units + (unit_rows - a.tail_tm0) * unit_cols * splits;
   a.grid = static_cast<int>(pair ? 2 * std::min<int64_t>(units, sms / 2) : std::min<int64_t>(units, sms));
   a.group_m = a.pair ? 8 : 16;
@@ -615,10 +619,10 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
     if (launch_epilogue(M, N, C, ldc, epi, s) != cudaSuccess) return GEMM_ERR_CUDA;
     ++kernels;
   }
-  set_plan(h, swap ? GEMM_FAMILY_SKINNY : GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n, a.pair == 2),
+  set_plan(h, swap ? GEMM_FAMILY_SKINNY : GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n, a.pair != 0),
            a.grid, kernels, (swap ? ((pack_b ? 1 : 0) | (pack_a ? 2 : 0)) : ((pack_a ? 1 : 0) | (pack_b ? 2 : 0))));
   h->plan.cluster = a.pair ? 2 : 1;
-  h->plan.pair_mma = a.pair == 2 ? 1 : 0;
+  h->plan.pair_mma = a.pair;
   h->plan.schedule = tail.rows > 0 ? 3 : (a.splits > 1 ? 1 : 0);
   return GEMM_OK;
 }
@@ -786,8 +790,16 @@ gemm_status_t gemm_set_option(gemm_handle_t h, int option, int64_t value) {
       h->opt_pretranspose = static_cast<int>(value);
       return GEMM_OK;
     case GEMM_OPT_PAIR:
-      if (value < 0 || value > 3) return GEMM_ERR_INVALID_VALUE;
+      if (value < 0 || value > 1) return GEMM_ERR_INVALID_VALUE;
       h->opt_pair = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_WAIT_LIMIT_US:
+      if (value < 0 || value > 60000000) return GEMM_ERR_INVALID_VALUE;
+      h->opt_wait_us = value;
+      return GEMM_OK;
+    case GEMM_OPT_FAULT_SKIP_STAGE:
+      if (value < 0 || value > (int64_t(1) << 30)) return GEMM_ERR_INVALID_VALUE;
+      h->opt_fault_skip = static_cast<int>(value);
       return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_VALUE;

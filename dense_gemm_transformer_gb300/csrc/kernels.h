@@ -130,8 +130,8 @@ struct TcArgs {
   int a_mn_major;        // A stored with M contiguous (transA == 1)
   int b_mn_major;        // B stored with N contiguous (transB == 0)
   int tile_n;            // 128, 192, 224 or 256 (16: the swapped small-M form)
-  int pair;              // tile_n >= 192: two-CTA clusters; 1: sharing each B tile by TMA multicast,
-                         // 2 (tile_n 256): one MMA of 256 rows per pair (tcgen05 cta_group::2)
+  int pair;              // tile_n >= 192: two-CTA clusters issuing one MMA of 256 rows per pair
+                         // (tcgen05 cta_group::2), each CTA staging half of every B tile
   int64_t M, N, K;
   const void* A;         // base of the (possibly re-packed) operand
   int64_t lda;           // elements
@@ -152,6 +152,9 @@ struct TcArgs {
   int grid;              // persistent CTAs
   int group_m;           // raster group height in M tiles
   TmaCache* tma_cache;   // the handle's descriptor cache (null: encode every call)
+  uint64_t wait_ns;      // limit of every bounded wait (0: the default, kWaitLimitNs)
+  int fault_skip;        // test hook: n > 0 makes CTA 0's producer issue no copies for its n-th stage
+                         // (one CTA per tile only); 0: none
 };
 // tile_n == 16 selects the swapped small-M form: the caller passes the
 // operands exchanged (C^T = op(B)^T op(A)^T, M and N exchanged) and the
@@ -162,7 +165,7 @@ constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);  // producer + MMA warps + ep
 // descriptor: 0 = E4M3, 1 = E5M2.
 constexpr uint32_t fp8_format_bits(uint32_t a_fmt, uint32_t b_fmt) { return (a_fmt << 7) | (b_fmt << 10); }
 int tc_tile_k(int mode);              // k elements per stage (128 bytes)
-int tc_stages(int mode, int tile_n, bool mma2);  // pipeline depth (mma2: one 256-row MMA per CTA pair)
+int tc_stages(int mode, int tile_n, bool pair);  // pipeline depth (pair: one 256-row MMA per CTA pair)
 // Whether the kernel is built for this tile width, pairing and B layout
 // (tile_n 128, 192, 224 or 256; pairs from 192 columns).
 bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major);

@@ -18,7 +18,8 @@ enum DeviceStatus : int {
   kDevTimeoutDrain = 5      // abort path waited too long for in-flight copies
 };
 
-// A wait that has not finished after this long is treated as a hang.
+// A wait that has not finished after this long is treated as a hang (the
+// default; the tcgen05 kernel takes its limit from its launch parameters).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -65,18 +66,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase of `bar` with the given parity has completed.  Gives
-// up after kWaitLimitNs, or as soon as another thread of the CTA has set
+// up after `limit` ns, or as soon as another thread of the CTA has set
 // *abort: on a timeout it records `code` in the device status word, sets
 // *abort for the rest of the CTA and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int* status, int code) {
+                                          int* status, int code, uint64_t limit = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit) {
         *abort = 1;
         if (status) atomicExch(status, code);
         return false;
@@ -85,11 +86,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Bounded wait used only on the abort path: it ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+// Bounded wait for work already in flight (copies, MMAs) before a CTA
+// exits: it ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status,
+                                           uint64_t limit = kWaitLimitNs) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit) {
       atomicExch(status, kDevTimeoutDrain);
       return;
     }
@@ -108,18 +111,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-// The same load delivered to every CTA of the cluster in `mask`, at the same
-// shared-memory offset, each CTA's barrier at `bar`'s offset receiving the
-// bytes that land in its own shared memory.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
-                                                      int32_t c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
       : "memory");
 }
 
@@ -291,15 +282,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-// Same, arriving on the barrier at `bar`'s offset in every CTA of the cluster
-// in `mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(mask)
-               : "memory");
-}
-
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives the
 // 32 columns of TMEM lane (lane base + i).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -442,14 +424,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // mbar_wait for barriers that CTAs of the cluster other than this one
 // arrive on (acquire at cluster scope); same bound and abort protocol.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
-                                                  int code) {
+                                                  int code, uint64_t limit = kWaitLimitNs) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((i & 255u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit) {
         *abort = 1;
         if (status) atomicExch(status, code);
         return false;

@@ -114,9 +114,11 @@ cudaError_t tc_init_driver() {
 
 int tc_tile_k(int mode) { return mode == 3 ? 128 : mode == 2 ? 64 : 32; }
 
-int tc_stages(int mode, int tile_n, bool mma2) {
+int tc_stages(int mode, int tile_n, bool pair) {
   (void)mode;  // a stage holds 128 bytes of K per row in every mode
-  if (tile_n == 256 && mma2) return TcCfg<2, 256, true>::STAGES;
+  if (tile_n == 256 && pair) return TcCfg<2, 256, true>::STAGES;
+  if (tile_n == 224 && pair) return TcCfg<2, 224, true>::STAGES;
+  if (tile_n == 192 && pair) return TcCfg<2, 192, true>::STAGES;
   if (tile_n == 256) return TcCfg<2, 256>::STAGES;
   if (tile_n == 224) return TcCfg<2, 224>::STAGES;
   if (tile_n == 192) return TcCfg<2, 192>::STAGES;
@@ -144,10 +146,9 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   e = a.a_mn_major ? encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
                    : encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
   if (e != cudaSuccess) return e;
-  // A pair of CTAs loads one half of each B tile apiece (K-major: half the
-  // rows): pair 1 shares the halves by multicast, pair 2 (256 columns)
-  // issues one MMA of 256 rows over both CTAs.
-  const int pair = (a.tile_n >= 192) ? a.pair : 0;
+  // Each CTA of a pair loads one half of each B tile (K-major: half the
+  // rows), and the pair issues one MMA of 256 rows over both CTAs.
+  const bool pair = a.tile_n >= 192 && a.pair;
   e = a.b_mn_major ? encode_2d_c(a.tma_cache, &tb, a.mode, a.B, a.N, a.K, a.ldb, ch, bk)
                    : encode_2d_c(a.tma_cache, &tb, a.mode, a.B, a.K, a.N, a.ldb, bk, pair ? a.tile_n / 2 : a.tile_n);
   if (e != cudaSuccess) return e;
@@ -176,6 +177,8 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.ws_row0 = a.ws_row0;
   p.status = a.status;
   p.fmt8 = a.mode == 3 ? a.fmt8 : 0u;
+  p.wait_ns = a.wait_ns > 0 ? a.wait_ns : kWaitLimitNs;
+  p.fault_skip = (a.fault_skip > 0 && !pair) ? a.fault_skip - 1 : -1;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
   // Tiles leave through TMA stores when the destination allows it: not the
   // transposed small-M form, no read of C (beta == 0, or partial sums), and

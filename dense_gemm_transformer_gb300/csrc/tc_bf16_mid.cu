@@ -4,7 +4,7 @@
 #include "tc_launch.cuh"
 
 namespace dgt {
-cudaError_t tc_launch_bf16_mid(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
+cudaError_t tc_launch_bf16_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
                                const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                                const TcParams& p, int grid, cudaStream_t s) {
   return tc_launch_mode_mid<2>(tile_n, pair, a_mn, b_mn, ta, tb, tc, tw, p, grid, s);

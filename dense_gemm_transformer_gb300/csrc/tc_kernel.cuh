@@ -28,7 +28,7 @@
 //
 // Work units are tiles, or (tile, K slice) pairs, handed out round-robin to
 // a persistent grid of one CTA per SM (or one CTA pair per two SMs, see PAIR
-// and MMA2 below), in a grouped raster order (group_m tiles of M walk all
+// below), in a grouped raster order (group_m tiles of M walk all
 // tiles of N) so that CTAs running at the same time share A and B tiles in
 // L2.  Whole tiles come first; the last rows of tiles may be cut into K
 // slices to fill the final wave (or every tile, for plain split-K), and each
@@ -74,6 +74,9 @@ struct TcParams {
   int c_tma;  // whole tiles leave through shared memory and TMA stores (tmC is valid)
   int w_tma;  // partial tiles likewise (tmW is valid)
   uint32_t fmt8;  // MODE 3: operand format bits of the instruction descriptor (E4M3 / E5M2)
+  uint64_t wait_ns;  // limit of every bounded wait
+  int fault_skip;    // test hook: CTA 0's producer issues no copies for its fault_skip-th stage
+                     // (0-based; -1: none), so the MMA's wait for that stage runs out
 };
 
 // MODE: 1 = tf32 (4-byte operands), 2 = bf16 (2-byte operands), 3 = 8-bit
@@ -112,9 +115,9 @@ struct TcCfg {
   static_assert(BN < 32 || BN % 32 == 0, "the epilogue moves 32-column chunks");
 };
 
-template <int MODE, bool MMA2>
+template <int MODE, bool PAIR>
 __device__ __forceinline__ void issue_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  if constexpr (MMA2) {
+  if constexpr (PAIR) {
     if (MODE == 3)
       mma_f8f6f4_pair(d, a, b, idesc, acc);
     else if (MODE == 2)
@@ -131,14 +134,15 @@ __device__ __forceinline__ void issue_mma(uint32_t d, uint64_t a, uint64_t b, ui
   }
 }
 
-// Bounded wait on a barrier of this CTA; MMA2 kernels wait with cluster
+// Bounded wait on a barrier of this CTA; PAIR kernels wait with cluster
 // scope (the other CTA of the pair or its MMAs arrive on it).
 template <bool CLUSTER>
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status, int code) {
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status, int code,
+                                         uint64_t limit) {
   if constexpr (CLUSTER)
-    return mbar_wait_cluster(bar, parity, abort, status, code);
+    return mbar_wait_cluster(bar, parity, abort, status, code, limit);
   else
-    return mbar_wait(bar, parity, abort, status, code);
+    return mbar_wait(bar, parity, abort, status, code, limit);
 }
 
 struct Unit {
@@ -186,26 +190,22 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
 // swapped by the host (a small-M product whose weights fill the 128-row MMA
 // side), so element (r, c) of its tile is stored at C[c * ldc + r].
 // PAIR: the grid is made of two-CTA clusters that work on vertically
-// adjacent tiles (same columns) in lockstep; each CTA loads its own A tile
-// and one half of the shared B tile, which TMA multicast writes into both
-// CTAs' shared memory, so each stage costs each CTA 16 KB of L2 traffic for
-// B instead of 32 KB.  A stage may be refilled only when both CTAs' MMAs have
-// read it: each MMA warp commits to the "empty" barrier of both CTAs.
-// MMA2 (with PAIR): instead, the pair issues one MMA of 256 rows
+// adjacent tiles (same columns), and the pair issues one MMA of 256 rows
 // (tcgen05 cta_group::2): each CTA loads its own 128 rows of A and its own
-// half of B into its own shared memory, and counts the bytes on the even
-// CTA's "full" barrier; one thread of the even CTA issues the MMAs, which
-// read A and B from both CTAs and write each CTA's 128 rows of the
-// accumulator into that CTA's TMEM, and commits to both CTAs' barriers;
-// both CTAs' epilogue warps release an accumulator on the even CTA's
-// barrier.  Each CTA then stages 32 KB per 256-column stage instead of 48.
-template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C, bool PAIR, bool MMA2 = false>
+// half of B (BN / 2 rows) into its own shared memory, and counts the bytes
+// on the even CTA's "full" barrier; one thread of the even CTA issues the
+// MMAs, which read A and B from both CTAs and write each CTA's 128 rows of
+// the accumulator into that CTA's TMEM, and commits to both CTAs'
+// barriers; both CTAs' epilogue warps release an accumulator on the even
+// CTA's barrier.  Each CTA then stages 32 KB per 256-column stage instead of
+// 48.  Every copy a CTA issues lands in its own shared memory: no operand
+// tile is multicast.
+template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                    const TcParams p) {
-  static_assert(!MMA2 || PAIR, "the two-CTA MMA runs on pairs");
-  using Cfg = TcCfg<MODE, BN, MMA2>;
+  using Cfg = TcCfg<MODE, BN, PAIR>;
   constexpr int S = Cfg::STAGES;
   // TF32 with an MN-major A: kind::tf32 reads only K-major operands from
   // shared memory, so warps 2-5 move each stage's A tile into TMEM (row i of
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // warps 6-9 are the epilogue.  A ring of NA buffers of BK columns sits
   // after the two accumulators.
   constexpr bool A_TMEM = MODE == 1 && A_MN;
-  static_assert(!A_TMEM || (BN == 128 && !PAIR && !MMA2 && !TRANS_C), "A through TMEM: 128-column tiles, one CTA");
+  static_assert(!A_TMEM || (BN == 128 && !PAIR && !TRANS_C), "A through TMEM: 128-column tiles, one CTA");
   constexpr int NA = 4;
   constexpr int A_COL0 = 2 * BN;  // first TMEM column of the A buffers
   constexpr int TMEM_COLS = A_TMEM ? 512 : Cfg::TMEM_COLS;
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   static_assert((Cfg::NUM_BARS + EXTRA_BARS) * 8 + 16 <= 256, "barrier area");
   static_assert(!A_TMEM || A_COL0 + NA * Cfg::BK <= TMEM_COLS, "TMEM columns");
   // MODE 3 names its operand formats at run time (the FORMAT fields are 0).
-  const uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN && !A_TMEM, B_MN, MMA2 ? 2 * Cfg::BM : Cfg::BM, BN) |
+  const uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN && !A_TMEM, B_MN, PAIR ? 2 * Cfg::BM : Cfg::BM, BN) |
                          (MODE == 3 ? p.fmt8 : 0u);
 
   extern __shared__ uint8_t smem_raw[];
@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // Work units: one per CTA, or one per two-CTA cluster (the pair's rank
   // picks its row of tiles).  The cluster of a pair is blockIdx.x / 2.
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  const bool leader = rank == 0u;  // MMA2: the CTA that issues the pair's MMAs
+  const bool leader = rank == 0u;  // PAIR: the CTA that issues the pair's MMAs
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int unit_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   auto tile_row = [&](const Unit& w) { return PAIR ? 2 * w.tm + static_cast<int>(rank) : w.tm; };
@@ -255,14 +255,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      // PAIR: both CTAs' MMAs must have read the stage; MMA2: the one pair
-      // MMA; A_TMEM: the MMAs (B) and the four warps that read A
-      mbar_init(empty_bar(s), A_TMEM ? 5 : (PAIR && !MMA2) ? 2 : 1);
+      // the stage is free once its MMAs (PAIR: the one pair MMA) have read
+      // it; A_TMEM: the MMAs (B) and the four warps that read A
+      mbar_init(empty_bar(s), A_TMEM ? 5 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
       // one arrival per epilogue warp (of both CTAs)
-      mbar_init(acce_bar(a), A_TMEM ? 4 : MMA2 ? 2 * kTcEpiWarps : kTcEpiWarps);
+      mbar_init(acce_bar(a), A_TMEM ? 4 : PAIR ? 2 * kTcEpiWarps : kTcEpiWarps);
     }
     for (int b = 0; b < (A_TMEM ? NA : 0); ++b) {
       mbar_init(afull_bar(b), 4);
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (p.w_tma) tma_prefetch_desc(&tmW);
   }
   if (warp == 1) {
-    if constexpr (MMA2) {
+    if constexpr (PAIR) {
       tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
       tmem_relinquish_pair();
     } else {
@@ -290,8 +290,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // PAIR: the peer's barriers must be initialised before any multicast copy
-  // or commit can signal them.
+  // PAIR: the peer's barriers must be initialised before its copies or the
+  // pair's MMA commits can signal them.
   if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -305,20 +305,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued = 0;
+      uint32_t issued = 0;  // stages taken so far (their positions in the ring's sequence)
       bool ok = true;
+      // The test hook's position (CTA 0 only): its stage is taken but gets
+      // no copies, so its "full" barrier never completes.
+      const uint32_t skip = (blockIdx.x == 0 && p.fault_skip >= 0) ? static_cast<uint32_t>(p.fault_skip) : ~0u;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Unit w = decode_unit(u, p);
         const int tm = tile_row(w);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!bar_wait<MMA2>(empty_bar(stage), phase ^ 1u, abort_flag, p.status, kDevTimeoutEmpty)) {
+          if (!bar_wait<PAIR>(empty_bar(stage), phase ^ 1u, abort_flag, p.status, kDevTimeoutEmpty, p.wait_ns)) {
             ok = false;
             break;
+          }
+          if (issued == skip) {
+            ++issued;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
           }
           const uint32_t a_dst = smem0 + stage * Cfg::STAGE_BYTES;
           const uint32_t b_dst = a_dst + Cfg::A_BYTES;
           const int k0 = kb * Cfg::BK;
-          if constexpr (MMA2) {
+          if constexpr (PAIR) {
             // Both CTAs' copies are counted on the even CTA's barrier, which
             // expects the bytes of the two (a copy of the odd CTA may land
             // before that expectation: the barrier's phase cannot complete
@@ -341,39 +352,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else {
               tma_load_2d_pair(b_dst, &tmB, fb, k0, w.tn * BN + static_cast<int>(rank) * (BN / 2));
             }
-            ++issued;
-            if (++stage == S) {
-              stage = 0;
-              phase ^= 1u;
-            }
-            continue;
-          }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-          if (A_MN) {
-#pragma unroll
-            for (int c = 0; c < Cfg::BM / Cfg::CH; ++c)
-              tma_load_2d(a_dst + c * Cfg::BK * 128, &tmA, fb, tm * Cfg::BM + c * Cfg::CH, k0);
           } else {
-            tma_load_2d(a_dst, &tmA, fb, k0, tm * Cfg::BM);
-          }
-          if constexpr (PAIR) {
-            // This CTA's half of B, written into both CTAs of the pair.
-            constexpr uint16_t kBoth = 0x3;
-            if (B_MN) {
-              constexpr int NC = BN / Cfg::CH;
+            const uint32_t fb = full_bar(stage);
+            mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+            if (A_MN) {
 #pragma unroll
-              for (int c = static_cast<int>(rank) * NC / 2; c < (static_cast<int>(rank) + 1) * NC / 2; ++c)
-                tma_load_2d_multicast(b_dst + c * Cfg::BK * 128, &tmB, fb, w.tn * BN + c * Cfg::CH, k0, kBoth);
+              for (int c = 0; c < Cfg::BM / Cfg::CH; ++c)
+                tma_load_2d(a_dst + c * Cfg::BK * 128, &tmA, fb, tm * Cfg::BM + c * Cfg::CH, k0);
             } else {
-              tma_load_2d_multicast(b_dst + rank * (BN / 2) * 128, &tmB, fb, k0, w.tn * BN + rank * (BN / 2), kBoth);
+              tma_load_2d(a_dst, &tmA, fb, k0, tm * Cfg::BM);
             }
-          } else if (B_MN) {
+            if (B_MN) {
 #pragma unroll
-            for (int c = 0; c < BN / Cfg::CH; ++c)
-              tma_load_2d(b_dst + c * Cfg::BK * 128, &tmB, fb, w.tn * BN + c * Cfg::CH, k0);
-          } else {
-            tma_load_2d(b_dst, &tmB, fb, k0, w.tn * BN);
+              for (int c = 0; c < BN / Cfg::CH; ++c)
+                tma_load_2d(b_dst + c * Cfg::BK * 128, &tmB, fb, w.tn * BN + c * Cfg::CH, k0);
+            } else {
+              tma_load_2d(b_dst, &tmB, fb, k0, w.tn * BN);
+            }
           }
           ++issued;
           if (++stage == S) {
@@ -382,18 +377,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      if (!ok && (!MMA2 || leader)) {
-        // Wait for every copy still in flight before the CTA can exit (an
-        // MMA2 odd CTA's copies complete on the even CTA's barriers, whose
-        // drain covers them; the pair leaves together).
+      if (!PAIR || leader) {
+        // Every copy still in flight lands before the CTA can exit.  Normally
+        // the MMAs have waited for all of them already and this returns at
+        // once; but when the MMA warp gave up a wait, the copies issued after
+        // the stage it waited for are waited for here, whether or not this
+        // loop ran to its end.  (An odd CTA's copies complete on the even
+        // CTA's barriers, whose drain covers them; the pair leaves together.)
         const uint32_t n = issued < static_cast<uint32_t>(S) ? issued : static_cast<uint32_t>(S);
-        for (uint32_t i = issued - n; i < issued; ++i) drain_wait(full_bar(i % S), (i / S) & 1u, p.status);
+        for (uint32_t i = issued - n; i < issued; ++i)
+          if (i != skip) drain_wait(full_bar(i % S), (i / S) & 1u, p.status, p.wait_ns);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // MMA2: only the even CTA of the pair issues (its MMAs cover both CTAs).
-    if (lane == 0 && (!MMA2 || leader)) {
+    // PAIR: only the even CTA of the pair issues (its MMAs cover both CTAs).
+    if (lane == 0 && (!PAIR || leader)) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -403,16 +402,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Unit w = decode_unit(u, p);
-        if (!bar_wait<MMA2>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty)) break;
+        if (!bar_wait<PAIR>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!bar_wait<MMA2>(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull)) {
+          if (!bar_wait<PAIR>(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull, p.wait_ns)) {
             ok = false;
             break;
           }
           if constexpr (A_TMEM) {
-            if (!bar_wait<false>(afull_bar(ab), a_phase, abort_flag, p.status, kDevTimeoutFull)) {
+            if (!bar_wait<false>(afull_bar(ab), a_phase, abort_flag, p.status, kDevTimeoutFull, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -430,7 +429,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else {
               const uint64_t ad = A_MN ? smem_desc_sw128(a_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
                                        : smem_desc_sw128(a_base + j * Cfg::UK * Cfg::ES, 16, 1024);
-              issue_mma<MODE, MMA2>(d_tmem, ad, bd, IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
+              issue_mma<MODE, PAIR>(d_tmem, ad, bd, IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
             }
           }
           if constexpr (A_TMEM) {
@@ -440,10 +439,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               a_phase ^= 1u;
             }
           }
-          if constexpr (MMA2)
+          if constexpr (PAIR)
             mma_commit_pair_multicast(empty_bar(stage), 0x3);  // both CTAs' halves of the stage are free
-          else if constexpr (PAIR)
-            mma_commit_multicast(empty_bar(stage), 0x3);  // both CTAs' copies of the stage are free
           else
             mma_commit(empty_bar(stage));
           if (++stage == S) {
@@ -452,7 +449,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (!ok) break;
-        if constexpr (MMA2)
+        if constexpr (PAIR)
           mma_commit_pair_multicast(accf_bar(acc), 0x3);  // each CTA's 128 rows are ready in its TMEM
         else
           mma_commit(accf_bar(acc));
@@ -462,11 +459,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       // Every MMA this thread issued has finished once drain_bar flips.
-      if constexpr (MMA2)
+      if constexpr (PAIR)
         mma_commit_pair(drain_bar);
       else
         mma_commit(drain_bar);
-      drain_wait(drain_bar, 0, p.status);
+      drain_wait(drain_bar, 0, p.status, p.wait_ns);
     }
   } else if (A_TMEM && warp < 6) {
     // ------------------------------------------------------------ A into TMEM
@@ -483,8 +480,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Unit w = decode_unit(u, p);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!bar_wait<false>(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull) ||
-              !bar_wait<false>(aempty_bar(ab), a_phase ^ 1u, abort_flag, p.status, kDevTimeoutEmpty)) {
+          if (!bar_wait<false>(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull, p.wait_ns) ||
+              !bar_wait<false>(aempty_bar(ab), a_phase ^ 1u, abort_flag, p.status, kDevTimeoutEmpty, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -525,7 +522,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int CW = Cfg::CW;
     for (int u = unit0; u < p.num_units; u += unit_step) {
       const Unit w = decode_unit(u, p);
-      if (!bar_wait<MMA2>(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull)) break;
+      if (!bar_wait<PAIR>(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns)) break;
       tc_fence_after();
       const bool partial = w.partial;
       const bool read_c = !partial && p.beta != 0.f;
@@ -630,7 +627,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if constexpr (MMA2)
+        if constexpr (PAIR)
           mbar_arrive_cluster(dsmem_map(acce_bar(acc), 0));  // the even CTA's MMAs reuse the accumulator
         else
           mbar_arrive(acce_bar(acc));
@@ -652,7 +649,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    if constexpr (MMA2)
+    if constexpr (PAIR)
       tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
     else
       tmem_dealloc(tmem_base, TMEM_COLS);

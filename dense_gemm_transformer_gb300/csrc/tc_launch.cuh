@@ -7,11 +7,11 @@
 
 namespace dgt {
 
-template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C = false, bool PAIR = false, bool MMA2 = false>
+template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C = false, bool PAIR = false>
 cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                           const TcParams& p, int grid, cudaStream_t s) {
-  using Cfg = TcCfg<MODE, BN, MMA2>;
-  auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN, TRANS_C, PAIR, MMA2>;
+  using Cfg = TcCfg<MODE, BN, PAIR>;
+  auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN, TRANS_C, PAIR>;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [&] {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
@@ -45,28 +45,27 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
 // Which operand layouts a tile width can take.  kind::tf32 reads K-major
 // operands only from shared memory: the planner transposes an MN-major TF32
 // B first, and an MN-major TF32 A too unless the 128-column, one-CTA kernel
-// takes it through TMEM; an
-// MN-major B is loaded in 128-byte column chunks, so its tile width must be
-// a whole number of chunks, and an even number when a pair of CTAs loads
-// one half each.
+// takes it through TMEM; an MN-major B is loaded in 128-byte column chunks,
+// so its tile width must be a whole number of chunks, and an even number
+// when each CTA of a pair loads one half.
 template <int MODE, int BN, bool PAIR>
 constexpr bool tc_mn_b_ok() {
   return MODE == 2 && BN % TcCfg<MODE, BN>::CH == 0 && (!PAIR || (BN / TcCfg<MODE, BN>::CH) % 2 == 0);
 }
 
-template <int MODE, int BN, bool PAIR, bool MMA2 = false>
+template <int MODE, int BN, bool PAIR>
 cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                          const CUtensorMap& tw, const TcParams& p, int grid, cudaStream_t s) {
-  if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN, false, PAIR, MMA2>(ta, tb, tc, tw, p, grid, s);
-  if constexpr (MODE == 1 && BN == 128 && !PAIR && !MMA2) {
+  if (!a_mn && !b_mn) return tc_launch_one<MODE, false, false, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
+  if constexpr (MODE == 1 && BN == 128 && !PAIR) {
     // an MN-major TF32 A goes to the MMA through TMEM
     if (a_mn && !b_mn) return tc_launch_one<1, true, false, 128>(ta, tb, tc, tw, p, grid, s);
   }
   if constexpr (MODE == 2) {
-    if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN, false, PAIR, MMA2>(ta, tb, tc, tw, p, grid, s);
+    if (a_mn && !b_mn) return tc_launch_one<MODE, true, false, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
     if constexpr (tc_mn_b_ok<MODE, BN, PAIR>()) {
-      if (!a_mn) return tc_launch_one<MODE, false, true, BN, false, PAIR, MMA2>(ta, tb, tc, tw, p, grid, s);
-      return tc_launch_one<MODE, true, true, BN, false, PAIR, MMA2>(ta, tb, tc, tw, p, grid, s);
+      if (!a_mn) return tc_launch_one<MODE, false, true, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
+      return tc_launch_one<MODE, true, true, BN, false, PAIR>(ta, tb, tc, tw, p, grid, s);
     }
   }
   return cudaErrorInvalidValue;
@@ -74,15 +73,12 @@ cudaError_t tc_launch_bn(bool a_mn, bool b_mn, const CUtensorMap& ta, const CUte
 
 // The 128- and 256-column tiles and the swapped small-M form (tile_n 16:
 // the weights are the 128-row operand, K-major or MN-major, the activations
-// a K-major 16-row operand, and C is written transposed).  `pair`: 0 one
-// CTA per tile, 1 pairs sharing B by multicast, 2 pairs issuing one MMA of
-// 256 rows (256 columns only).
+// a K-major 16-row operand, and C is written transposed).  `pair`: CTA
+// pairs issuing one MMA of 256 rows (tcgen05 cta_group::2; 256 columns).
 template <int MODE>
-cudaError_t tc_launch_mode(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t tc_launch_mode(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid,
                            cudaStream_t s) {
-  if (tile_n == 256 && pair == 2) return tc_launch_bn<MODE, 256, true, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
-  if (pair == 2) return cudaErrorInvalidValue;
   if (tile_n == 256 && pair) return tc_launch_bn<MODE, 256, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
   if (tile_n == 256) return tc_launch_bn<MODE, 256, false>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
   if (tile_n == 128 && !pair) return tc_launch_bn<MODE, 128, false>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
@@ -95,12 +91,12 @@ cudaError_t tc_launch_mode(int tile_n, int pair, bool a_mn, bool b_mn, const CUt
 
 // The 192- and 224-column tiles, which let the planner fill whole waves
 // where 256 would leave the last one mostly idle (4096 columns: 19 tiles of
-// 224 instead of 16 of 256).
+// 224 instead of 16 of 256), alone or as CTA pairs issuing one MMA of 256
+// rows (each CTA stages 96 or 112 rows of a K-major B).
 template <int MODE>
-cudaError_t tc_launch_mode_mid(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
+cudaError_t tc_launch_mode_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
                                const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                                const TcParams& p, int grid, cudaStream_t s) {
-  if (pair == 2) return cudaErrorInvalidValue;
   if (tile_n == 192 && pair) return tc_launch_bn<MODE, 192, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
   if (tile_n == 192) return tc_launch_bn<MODE, 192, false>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
   if (tile_n == 224 && pair) return tc_launch_bn<MODE, 224, true>(a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
@@ -111,18 +107,18 @@ cudaError_t tc_launch_mode_mid(int tile_n, int pair, bool a_mn, bool b_mn, const
 // Defined in tc_tf32.cu (MODE 1), tc_bf16.cu (MODE 2: 16, 128 and 256
 // columns), tc_bf16_mid.cu (MODE 2: 192 and 224 columns), tc_fp8.cu and
 // tc_fp8_mid.cu (MODE 3, K-major operands only, the same widths).
-cudaError_t tc_launch_tf32(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t tc_launch_tf32(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid,
                            cudaStream_t s);
-cudaError_t tc_launch_bf16(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t tc_launch_bf16(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                            const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid,
                            cudaStream_t s);
-cudaError_t tc_launch_bf16_mid(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
+cudaError_t tc_launch_bf16_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
                                const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                                const TcParams& p, int grid, cudaStream_t s);
-cudaError_t tc_launch_fp8(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
+cudaError_t tc_launch_fp8(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta, const CUtensorMap& tb,
                           const CUtensorMap& tc, const CUtensorMap& tw, const TcParams& p, int grid, cudaStream_t s);
-cudaError_t tc_launch_fp8_mid(int tile_n, int pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
+cudaError_t tc_launch_fp8_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
                               const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                               const TcParams& p, int grid, cudaStream_t s);
 

@@ -245,19 +245,20 @@ def test_fp8_epilogue_bias_gelu(h):
 
 
 # ------------------------------------------------------------ M > 16: the persistent tile kernel
-@pytest.mark.parametrize("tile_n,pair", [(128, 1), (192, 1), (192, 2), (224, 1), (224, 2), (256, 1), (256, 2),
-                                         (256, 3)])
+@pytest.mark.parametrize("tile_n,pair", [(128, 1), (128, 0), (192, 1), (192, 0), (224, 1), (224, 0), (256, 1),
+                                         (256, 0)])
 def test_fp8_tiles_and_pairs(h, tile_n, pair):
-    """Every tile width, one CTA per tile, pairs sharing B by multicast (2)
-    and pairs issuing one 256-row MMA (3); ragged M, N and K."""
+    """Every tile width, one CTA per tile (pair option 1) and CTA pairs
+    issuing one 256-row MMA (option 0, from 192 columns); ragged M, N and K."""
     h.set_option("tile_n", tile_n)
     h.set_option("pair", pair)
     M, N, K = 700, 650, 1008  # K: 8 blocks of 128 bytes, the last one ragged
     _run_and_check(h, M, N, K, seed=90, family="tc", rows=_cases_rows(M))
     plan = h.plan()
+    paired = pair == 0 and tile_n >= 192
     assert plan["tile_n"] == tile_n
-    assert plan["cluster"] == (1 if pair == 1 else 2)
-    assert plan["pair_mma"] == (1 if pair == 3 else 0)
+    assert plan["cluster"] == (2 if paired else 1)
+    assert plan["pair_mma"] == (1 if paired else 0)
     _run_and_check(h, M, N, K, seed=91, beta=1.0, family="tc", rows=_cases_rows(M))
 
 
@@ -283,7 +284,7 @@ def test_fp8_split_k(h, splits):
     _run_and_check(h, M, N, K, seed=95, beta=1.0, family="tc", rows=_cases_rows(M))
 
 
-@pytest.mark.parametrize("tile_n,pair", [(128, 1), (224, 2), (256, 3)])
+@pytest.mark.parametrize("tile_n,pair", [(128, 1), (192, 0), (224, 0), (256, 0)])
 def test_fp8_tiles_integers_bit_exact(h, tile_n, pair):
     h.set_option("tile_n", tile_n)
     h.set_option("pair", pair)
@@ -315,7 +316,7 @@ def test_fp8_formats_small_m(h, mode, M, N, K):
 
 
 @pytest.mark.parametrize("mode", OTHER_MODES)
-@pytest.mark.parametrize("tile_n,pair", [(128, 1), (224, 2), (256, 3)])
+@pytest.mark.parametrize("tile_n,pair", [(128, 1), (224, 0), (256, 0)])
 def test_fp8_formats_tiles(h, mode, tile_n, pair):
     h.set_option("tile_n", tile_n)
     h.set_option("pair", pair)

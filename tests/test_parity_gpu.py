@@ -101,39 +101,36 @@ def test_tc_tile_widths(h, mode, tile_n, tA, tB):
 
 
 @pytest.mark.parametrize("mode", ["tf32", "bf16"])
-@pytest.mark.parametrize("pair", [0, 1, 2])
+@pytest.mark.parametrize("pair", [0, 1])
 @pytest.mark.parametrize("tA,tB", TRANS)
 @pytest.mark.parametrize("M,N,K", [(640, 600, 200), (300, 260, 1000), (1100, 300, 64)])
 @pytest.mark.parametrize("tile_n", [192, 224, 256])
 def test_tc_paired_ctas(h, mode, pair, tA, tB, M, N, K, tile_n):
     """Tiles of 192-256 columns with and without two-CTA clusters: pairs
-    sharing B tiles by TMA multicast (each CTA loads one half; option 2, and
-    the planner's choice below 256 columns), and pairs issuing one MMA of 256
-    rows over both CTAs' shared memory and TMEM (tcgen05 cta_group::2; the
-    planner's choice at 256 columns).  Odd tile-row counts
-    leave the second CTA of the last pair with no rows of C.  An
-    N-contiguous BF16 B pairs only when its tile is an even number of
-    128-byte chunks (256), and takes no 224-column tile."""
+    issue one MMA of 256 rows over both CTAs' shared memory and TMEM
+    (tcgen05 cta_group::2; option 0, the planner's choice), each CTA
+    staging its own 128 rows of A and one half of the B tile (96, 112 or 128
+    rows).  Odd tile-row counts leave the second CTA of the last pair with no
+    rows of C.  An N-contiguous BF16 B pairs only when its tile is an even
+    number of 128-byte chunks (256), and takes no 224-column tile."""
     b_mn = mode == "bf16" and not tB
     if b_mn and tile_n == 224:
         pytest.skip("224-column tiles need a K-major B in BF16 (covered by test_tc_tile_widths)")
     h.set_option("tile_n", tile_n)
     h.set_option("pair", pair)
     _cases.run_and_check(h, mode, M, N, K, tA, tB, alpha=0.5, beta=-1.0, seed=77, dist="normal")
-    paired = pair != 1 and not (b_mn and tile_n == 192)
-    mma2 = paired and tile_n == 256 and pair in (0, 3)
+    paired = pair == 0 and not (b_mn and tile_n == 192)
     plan = h.plan()
     assert plan["cluster"] == (2 if paired else 1) and plan["tile_n"] == tile_n
-    assert plan["pair_mma"] == (1 if mma2 else 0)
+    assert plan["pair_mma"] == (1 if paired else 0)
     _cases.run_and_check(h, mode, M, N, min(K, 1024), tA, tB, seed=78, dist="int", exact=True)
     h.set_option("split_k", 3)
     _cases.run_and_check(h, mode, M, N, K, tA, tB, seed=79, dist="normal")
 
 
 @pytest.mark.parametrize("mode,M,N,K,tile_n,pair", [("bf16", 4096, 4096, 4096, 256, 0),
-                                                      ("bf16", 4096, 4096, 4096, 256, 3),
                                                       ("tf32", 2304, 2304, 1024, 0, 0),
-                                                      ("tf32", 2304, 2304, 1024, 256, 3),
+                                                      ("tf32", 2304, 2304, 1024, 256, 0),
                                                       ("tf32", 2200, 2100, 1000, 0, 0)])
 @pytest.mark.parametrize("tB", [False, True])
 def test_tc_tail_rows_cut_into_k_slices(h, mode, M, N, K, tile_n, pair, tB):
