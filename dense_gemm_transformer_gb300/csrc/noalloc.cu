@@ -8,11 +8,14 @@
 // must not call into the allocator).  gemm_run cannot serve them: its handle
 // allocates a status word at creation and a workspace on first use.
 //
-// This entry point runs the same swapped tcgen05 kernel that gemm_run picks
-// for M <= 16, with every piece of scratch it needs -- the device status word
+// This entry point runs the persistent tcgen05 kernel in its swapped
+// small-M form (C^T = B^T A^T) and, when K is split, the separate slice-sum
+// kernel, with every piece of scratch they need -- the device status word
 // and the split-K partial sums -- in one fixed array compiled into the
-// library.  Nothing is allocated: no cudaMalloc, no cudaFree, no allocating
-// library call.
+// library.  (gemm_run serves the same shapes with a different kernel, the
+// cluster kernel that sums its K slices in distributed shared memory; the
+// two agree within the mode's tolerance, not bit for bit.)  Nothing is
+// allocated: no cudaMalloc, no cudaFree, no allocating library call.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -78,8 +81,8 @@ gemm_status_t scratch_for_current_device(DeviceScratch* out) {
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t x, int64_t m) { return ceil_div(x, m) * m; }
 
-// The slice count gemm_run's planner uses for this form: the count whose
-// (tile, slice) units fill whole waves of one CTA per SM best.
+// The K-slice count: the one whose (tile, slice) units fill whole waves of
+// one CTA per SM best (at most 32 slices of at least two K blocks each).
 int64_t planned_splits(int64_t tiles, int64_t kb, int sms) {
   int64_t best = 1;
   double best_eff = 0.0;
@@ -135,10 +138,9 @@ extern "C" gemm_status_t gemm_run_small_m_noalloc(int mode, int transB, int64_t 
   const int64_t slice_bytes = M * ws_ld * static_cast<int64_t>(sizeof(float));
   int64_t splits = (tiles >= 2 * d.sms) ? 1 : planned_splits(tiles, kb, d.sms);
   const int64_t room = static_cast<int64_t>(kScratchBytes - kStatusBytes);
-  while (splits > 1 && splits * slice_bytes > room) --splits;
+  while (splits > 1 && splits * slice_bytes > room) --splits;  // one slice needs no partial sums
   const int64_t kb_per = ceil_div(kb, splits);
-  splits = ceil_div(kb, kb_per);
-  if (splits > 1 && splits * slice_bytes > room) return GEMM_ERR_TOO_LARGE;
+  splits = ceil_div(kb, kb_per);  // never more slices than chosen above
 
   // The status word must start at zero on every call; partial sums are fully
   // overwritten before they are read, so they need no clearing.
@@ -173,5 +175,21 @@ extern "C" gemm_status_t gemm_run_small_m_noalloc(int mode, int transB, int64_t 
   if (splits > 1 &&
       dgt::launch_splitk_reduce(M, N, a.splits, a.ws, ws_ld, C, ldc, alpha, beta, dgt::EpiParams{}, 0, s) != cudaSuccess)
     return GEMM_ERR_CUDA;
+  return GEMM_OK;
+}
+
+extern "C" gemm_status_t gemm_noalloc_check_device(void* stream) {
+  // Like gemm_check_device, for the fixed array's status word: nothing is
+  // allocated (the word is copied into a local variable and cleared in place).
+  DeviceScratch d;
+  gemm_status_t st = scratch_for_current_device(&d);
+  if (st != GEMM_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GEMM_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, d.base, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (v != 0) {
+    if (cudaMemset(d.base, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+    return GEMM_ERR_DEVICE_TIMEOUT;
+  }
   return GEMM_OK;
 }

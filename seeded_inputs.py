@@ -147,7 +147,7 @@ def to_block_scaled(t: torch.Tensor, elem: str = "e4m3", block: int = 32, scale:
     E8M0 scales (MX): 2^(floor(log2 amax) - e), e the exponent of the
     element format's largest power of two, so the run's largest element lands
     in the format's top binade.  UE4M3 scales (NVFP4): amax / 6 rounded to
-    E4M3.  An all-zero run takes the scale 1.  Returns (element codes as
+    E4M3, kept within [2^-9, 448].  An all-zero run takes the scale 1.  Returns (element codes as
     uint8 -- two E2M1 codes per byte, the even element in the low nibble --,
     scale codes as uint8 rows x ceil(K / block))."""
     import numpy as np
@@ -164,11 +164,14 @@ def to_block_scaled(t: torch.Tensor, elem: str = "e4m3", block: int = 32, scale:
         scodes = (e + 127).astype(np.uint8)
         sval = np.ldexp(1.0, e.astype(np.int64))
     else:
-        want = torch.from_numpy(np.where(amax > 0, amax / 6.0, 1.0)).to(torch.float8_e4m3fn)
+        # amax / 6 kept inside the positive E4M3 range, [2^-9, 448], before
+        # the cast (which does not saturate): a run beyond 6 * 448 takes the
+        # largest scale and its elements clip to +-6; a run so small that
+        # amax / 6 is below the smallest subnormal takes the smallest scale.
+        want = np.where(amax > 0, np.clip(amax / 6.0, 2.0 ** -9, 448.0), 1.0)
+        want = torch.from_numpy(want).to(torch.float8_e4m3fn)
         scodes = want.view(torch.uint8).numpy().copy()
         sval = want.to(torch.float64).numpy()
-        sval = np.where(sval > 0, sval, 1.0)
-        scodes = np.where(want.to(torch.float64).numpy() > 0, scodes, np.uint8(0x38))
     y = pad / np.repeat(sval, block, axis=1)
     y = np.clip(y, -emax_val, emax_val)[:, :K]
     if elem == "e2m1":

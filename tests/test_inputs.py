@@ -76,3 +76,21 @@ def test_e2m1_rounding_ties_to_even():
     want = [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 6.0, -1.0, -4.0]
     got = oracle.e2m1_to_f64(si._e2m1_codes(x))
     assert got.tolist() == want
+
+
+def test_nvfp4_scale_stays_in_range_for_huge_and_tiny_runs():
+    """A run whose amax / 6 is above E4M3's largest value takes the largest
+    scale (448) and clips to +-6 x 448; one below the smallest subnormal
+    takes the smallest scale (2^-9): neither gets a NaN or zero scale."""
+    x = np.zeros((2, 32))
+    x[0, :16] = np.linspace(-6000.0, 6000.0, 16)  # amax / 6 = 1000 > 448
+    x[0, 16:] = np.linspace(-1e-5, 1e-5, 16)      # amax / 6 ~ 1.7e-6 < 2^-9 ~ 1.95e-3
+    x[1, :16] = 1.0
+    codes, scodes = si.to_block_scaled(torch.from_numpy(x), "e2m1", 16, "ue4m3")
+    svals = oracle.ue4m3_to_f64(scodes)
+    assert svals[0, 0] == 448.0 and svals[0, 1] == 2.0 ** -9
+    assert np.all(np.isfinite(svals)) and np.all(svals > 0)
+    got, _ = _decode(codes, scodes, "e2m1", 16, "ue4m3")
+    assert got[0, 0] == -6.0 * 448.0 and got[0, 15] == 6.0 * 448.0  # clipped at the top of the range
+    assert np.all(np.abs(got[0, 16:] - x[0, 16:]) <= 2.0 ** -9 * 0.5)  # below one step of the smallest scale
+    assert svals[1, 0] == 0.171875  # an in-range run keeps amax / 6 rounded to E4M3
