@@ -7,12 +7,14 @@
  *
  *     C = alpha * op(A) * op(B) + beta * C
  *
- * computed in one of four modes: exact FP32 on the CUDA cores, TF32 on the
- * tensor cores (the mode the page's tensor-core kernel uses, first paragraph),
- * BF16 inputs on the tensor cores, or FP8 E4M3 inputs on the tensor cores
- * ("Tensor Cores: Matrix Instructions, Swizzling and FP8, Measured" and
- * "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls, Measured" name the
- * format).  Every mode accumulates in FP32 and writes FP32.
+ * computed in one of seven modes (gemm_mode_t): exact FP32 on the CUDA
+ * cores, TF32 on the tensor cores (the mode the page's tensor-core kernel
+ * uses, first paragraph), BF16 inputs on the tensor cores, or 8-bit float
+ * inputs on the tensor cores in four modes -- E4M3 x E4M3, E5M2 x E5M2 and
+ * the two mixed pairs ("Tensor Cores: Matrix Instructions, Swizzling and
+ * FP8, Measured" and "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls,
+ * Measured" name the formats).  Every mode accumulates in FP32 and writes
+ * FP32.
  *
  * Layout (all matrices row-major, element (r, c) at base[r * ld + c]):
  *   op(A) is M x K.  transA == 0: A is stored M x K, lda >= max(K, 1).
@@ -78,7 +80,7 @@ typedef enum {
   GEMM_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed                                */
   GEMM_ERR_ALLOC = 5,         /* device memory for the handle's workspace could not be allocated    */
   GEMM_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up a bounded wait and set the device status word     */
-  GEMM_ERR_TOO_LARGE = 7       /* the problem exceeds gemm_run_small_m_noalloc's limits (M, scratch)  */
+  GEMM_ERR_TOO_LARGE = 7       /* the problem exceeds gemm_run_small_m_noalloc's limit (M > 16)      */
 } gemm_status_t;
 
 /* Kernel families the planner chooses among (gemm_set_option/GEMM_OPT_FAMILY). */
@@ -99,10 +101,25 @@ typedef enum {
                                 (operands read in place), 2 = always transpose.  TF32: 2 also
                                 transposes an MN-major A that the 128-column kernel would
                                 otherwise move into TMEM itself (0 and 1: it does)          */
-  GEMM_OPT_PAIR = 5          /* TC: two-CTA clusters (tiles of 192 or more columns, two or more
-                                rows of tiles).  0 = planner's choice (256 columns: one 256-row
-                                MMA per pair, tcgen05 cta_group::2; 192/224: pairs sharing B by
-                                multicast), 1 = never, 2 = multicast pairs only, 3 = as 0     */
+  GEMM_OPT_PAIR = 5,         /* TC: CTA pairs issuing one 256-row MMA (tcgen05 cta_group::2;
+                                tiles of 192 or more columns, two or more rows of tiles; each
+                                CTA stages half of every B tile).  0 = wherever the tile width
+                                and B layout allow, 1 = never                                 */
+  GEMM_OPT_WAIT_LIMIT_US = 6, /* TC: how long (microseconds) a wait of the persistent tcgen05
+                                 kernel on one of its pipeline barriers may last before the
+                                 kernel gives up, records GEMM_ERR_DEVICE_TIMEOUT in the device
+                                 status word and returns.  0 = the default, 2 seconds; at most
+                                 60 s.  A limit shorter than the call's own stages take makes
+                                 correct calls time out.                                       */
+  GEMM_OPT_FAULT_SKIP_STAGE = 7 /* TC, a test hook for the bounded-wait path: n > 0 makes the
+                                   first CTA's TMA producer of the persistent tcgen05 kernel
+                                   issue no copies for the n-th pipeline stage it takes, so
+                                   that the MMA's wait for that stage runs out (after the
+                                   GEMM_OPT_WAIT_LIMIT_US limit); the kernel then drains its
+                                   copies and MMAs in flight, frees its TMEM and returns, C is
+                                   undefined, and gemm_check_device reports
+                                   GEMM_ERR_DEVICE_TIMEOUT.  Forces one CTA per tile (no pairs).
+                                   0 = off (the default).  Nothing faults or hangs.             */
 } gemm_option_t;
 
 /* Elementwise work fused into the GEMM's epilogue (gemm_run_epilogue), the
@@ -138,7 +155,7 @@ typedef struct {
   int32_t packed;        /* bit 0: A re-packed (or transposed), bit 1: B, into the workspace */
   int32_t schedule;      /* 0 one unit per tile, 1 split-K slices, 2 stream-K (SIMT),
                             3 whole tiles then K slices for the last rows of tiles (TC) */
-  int32_t cluster;       /* TC: CTAs per cluster (2 = pairs sharing each B tile) */
+  int32_t cluster;       /* TC: CTAs per cluster (2 = CTA pairs); small M: K slices per cluster */
   int32_t pair_mma;      /* TC: 1 when each CTA pair issues one 256-row MMA (tcgen05 cta_group::2) */
   int32_t reserved[4];
 } gemm_plan_t;
@@ -221,6 +238,18 @@ gemm_status_t gemm_check_device(gemm_handle_t h, void* stream);
  * GEMM_ERR_CUDA when the launch fails. */
 gemm_status_t gemm_launch_null(gemm_handle_t h, void* stream);
 
+/* A calibration kernel, not a GEMM (the source pages have no counterpart):
+ * the FP32 fused multiply-add rate of this part, against which the FP32
+ * mode is measured.  Launches, on `stream`, `grid` CTAs of 256 threads that
+ * each run 16 independent FMA chains of `iters` steps in registers --
+ * packed == 0: scalar fma.rn.f32; packed == 1: eight fma.rn.f32x2 pairs --
+ * and store one float per thread to `out` (grid * 256 floats of device
+ * memory, 4-byte aligned, owned by the caller).  FLOPs per launch =
+ * grid * 256 * iters * 32; timed with events it gives the FP32 roof.
+ * GEMM_ERR_INVALID_VALUE for grid outside [1, 2^20], iters < 1, a null
+ * `out` or packed not 0/1; GEMM_ERR_CUDA when the launch fails. */
+gemm_status_t gemm_launch_fma_peak(int packed, int64_t grid, int64_t iters, float* out, void* stream);
+
 /* Bytes of the fixed device array that gemm_run_small_m_noalloc uses as its
  * only scratch memory (one array per device, held until the process exits). */
 #define GEMM_NOALLOC_SCRATCH_BYTES (8u << 20)
@@ -234,21 +263,24 @@ gemm_status_t gemm_launch_null(gemm_handle_t h, void* stream);
  * gemm_run cannot serve such callers because its handle allocates a status
  * word when created and a workspace when first used.
  *
- * Same arithmetic and kernels as gemm_run picks for these shapes: A is stored
- * M x K (transA is always 0), B is K x N (transB == 0) or N x K (transB == 1),
- * mode is GEMM_MODE_BF16 or GEMM_MODE_TF32 (TF32 needs transB == 1), C is
- * M x N fp32.  The caller passes inputs and outputs; the only scratch is a
+ * The same product as gemm_run, within the mode's tolerance, but not the same
+ * kernels: this call runs the persistent tcgen05 kernel in its swapped form
+ * plus a separate kernel that sums the split-K partials, where gemm_run uses
+ * the cluster kernel that sums its K slices in distributed shared memory.
+ * A is stored M x K (transA is always 0), B is K x N (transB == 0) or N x K
+ * (transB == 1), mode is GEMM_MODE_BF16 or GEMM_MODE_TF32 (TF32 needs
+ * transB == 1), C is M x N fp32.  The caller passes inputs and outputs; the only scratch is a
  * fixed device array of GEMM_NOALLOC_SCRATCH_BYTES inside the library (the
  * device status word and the split-K partial sums).  The call makes no
  * cudaMalloc, no cudaFree and no allocating library call.
  *
- * Limits and errors: M > 16, or split-K partial sums that would not fit the
- * array even with a single K slice, give GEMM_ERR_TOO_LARGE; an operand the
+ * Limits and errors: M > 16 gives GEMM_ERR_TOO_LARGE (the K-slice count is
+ * lowered until the partial sums fit the array; one slice needs none); an
+ * operand the
  * TMA unit cannot read in place (base not 16-byte aligned, row pitch not a
  * multiple of 16 bytes) gives GEMM_ERR_MISALIGNED; FP32 or FP8 mode, or TF32
  * with transB == 0, gives GEMM_ERR_NOT_SUPPORTED; the other checks are
  * gemm_run's.
- * The planner's K-slice count is lowered when its partial sums would not fit.
  *
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture.  Every
@@ -256,10 +288,22 @@ gemm_status_t gemm_launch_null(gemm_handle_t h, void* stream);
  * call clears the status word itself, and calls whose kernels overlap on the
  * GPU (different streams, no ordering between them) race on the array and
  * give undefined results.  A device-side wait that times out is recorded in
- * the array's status word but not reported by this call. */
+ * the array's status word; this call returns before its kernels run and
+ * cannot report it: gemm_noalloc_check_device does, and must be called
+ * before the next call on the device clears the word. */
 gemm_status_t gemm_run_small_m_noalloc(int mode, int transB, int64_t M, int64_t N, int64_t K, float alpha,
                                        const void* A, int64_t lda, const void* B, int64_t ldb,
                                        float beta, float* C, int64_t ldc, void* stream);
+
+/* The check of gemm_check_device for gemm_run_small_m_noalloc, which has no
+ * handle (no counterpart on the source pages either): synchronize `stream`,
+ * then read and clear the status word in the library's fixed scratch array
+ * of the current device.  Returns GEMM_ERR_DEVICE_TIMEOUT if a kernel of an
+ * earlier gemm_run_small_m_noalloc call gave up a bounded wait (that call's
+ * C is then undefined), GEMM_ERR_CUDA if the stream reports an error,
+ * GEMM_OK otherwise.  Allocates nothing.  The next gemm_run_small_m_noalloc
+ * call on the device clears the word, so check before it. */
+gemm_status_t gemm_noalloc_check_device(void* stream);
 
 /* A static string naming a status code. */
 const char* gemm_status_string(gemm_status_t s);

@@ -36,11 +36,13 @@ def _reset(h):
 
 def _check(mode, got, Y, D, act, bias, Z, alpha, beta, cin, what):
     ref = oracle.epilogue(act, Y, bias, Z)
-    scale = np.abs(alpha) * D + (np.abs(beta * cin.astype(np.float64)) if cin is not None else 0.0)
-    # the product's error (the mode's gate), scaled by at most |GELU'| <= 1.13,
-    # plus the fp32 roundings of the bias add and of erff / expf
+    beta_c = np.abs(beta * cin.astype(np.float64)) if cin is not None else 0.0
+    # the product's error (the mode's gate on |alpha| D, plus the one fp32
+    # rounding of the beta * C term), scaled by at most |GELU'| <= 1.13, plus
+    # the fp32 roundings of the bias add and of the activation itself
     extra = np.abs(Y) + (np.abs(bias.astype(np.float64))[None, :] if bias is not None else 0.0)
-    bound = GELU_SLOPE * _gate.TOL[mode] * scale + 4e-6 * (np.abs(ref) + extra) + 1e-30
+    bound = (GELU_SLOPE * (_gate.TOL[mode] * np.abs(alpha) * D + _gate.U32 * beta_c) + 4e-6 * (np.abs(ref) + extra)
+             + 1e-30)
     err = np.abs(got.astype(np.float64) - ref)
     assert np.all(err <= bound), (what, float(np.max(err / bound)))
 

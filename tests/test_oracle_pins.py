@@ -357,6 +357,34 @@ def test_gate_rejects_one_dropped_term():
     _gate.assert_within("fp32", ref.astype(np.float32), ref, D)
 
 
+def test_gate_charges_beta_c_one_rounding_only():
+    """With beta != 0 the gate stays the stated |C - Cref| / (|alpha| D): the
+    beta * C term may add only the one fp32 rounding of the stored result.
+    Where D = 0 the result must be beta * C rounded once; where |beta C| is
+    large against D, an error of a few units of it fails, although the
+    beta-augmented err' would hide it."""
+    M, N, K = 8, 8, 4
+    a = si.uniform((M, K), 45).numpy()
+    b = si.uniform((K, N), 46).numpy()
+    a[3, :] = 0.0  # a zero row: D = 0 there
+    c = (si.normal((M, N), 47).numpy() * 1000.0).astype(np.float32)
+    alpha, beta = 0.5, 0.75
+    ref, D = oracle.gemm("fp32", a, b, alpha=alpha, beta=beta, C=c)
+    assert np.all(D[3] == 0)
+    once = ref.astype(np.float32)  # every element rounded once
+    _gate.assert_within("fp32", once, ref, D, alpha, beta, c)
+    off = once.astype(np.float64).copy()
+    off[3, 2] = np.nextafter(np.nextafter(once[3, 2], np.float32(np.inf)), np.float32(np.inf))  # planted: 2 ulps
+    with pytest.raises(AssertionError):
+        _gate.assert_within("fp32", off, ref, D, alpha, beta, c)
+    off = once.astype(np.float64).copy()
+    off[1, 1] += 8 * _gate.U32 * abs(beta * c[1, 1])  # planted: 8 roundings of beta*c
+    assert 8 * _gate.U32 * abs(beta * c[1, 1]) > _gate.TOL["fp32"] * alpha * D[1, 1]
+    assert _gate.errors_augmented(off, ref, D, alpha, beta, c)[1, 1] < _gate.TOL["fp32"]
+    with pytest.raises(AssertionError):
+        _gate.assert_within("fp32", off, ref, D, alpha, beta, c)
+
+
 def test_fp8_gate_catches_one_missing_k_block_on_nonnegative_operands():
     """At decode depth (K = 8960, 70 blocks of 128 bytes) a missing or doubled
     K block moves a random-sign result by less than the FP8 gate, so the FP8
