@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -54,8 +55,7 @@ FP8_OVER_BF16 = 4.5 / 2.25
 # "traffic" is reported as null.
 PROFILED_TRAFFIC = {
     "fp32": {"source": "dense_gemm_transformer_gb300/csrc/simt.cu", "sha256": "f4505c70457f11f6",
-             "bytes_per_launch": 89.17e6,
-             "capture": "profiles/simt_gemm_kernel_dram_per_launch.md"},
+             "bytes_per_launch": 89.17e6},
 }
 
 
@@ -84,6 +84,49 @@ def peaks():
             "tf32_tflops": bf16 * TF32_OVER_BF16, "tf32_tflops_sustained": bf16_s * TF32_OVER_BF16,
             "fp8_tflops": bf16 * FP8_OVER_BF16, "fp8_tflops_sustained": bf16_s * FP8_OVER_BF16,
             "fp32_alu_tflops": fp32_alu, "source": src}
+
+
+def measure_fp32_peak(dev, sample_ms=20.0, samples=3):
+    """The FP32 FMA roof of this GPU, measured: gemm_launch_fma_peak (16
+    independent FMA chains per thread, 4 CTAs of 256 threads per SM) timed
+    with CUDA events, in its scalar and packed (fma.rn.f32x2) forms, each the
+    median of `samples` launches of >= sample_ms; the roof is the faster
+    form.  No clock or other setting of the GPU is touched."""
+    import ctypes
+
+    import dense_gemm_transformer_gb300 as dg
+    fn = dg.load().gemm_launch_fma_peak
+    fn.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    grid = 4 * sms
+    out = torch.empty(grid * 256, device=dev)
+    stream = torch.cuda.Stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(packed, iters):
+        e0.record(stream)
+        st = fn(packed, grid, iters, out.data_ptr(), stream.cuda_stream)
+        e1.record(stream)
+        stream.synchronize()
+        if st != 0:
+            raise RuntimeError(f"gemm_launch_fma_peak: status {st}")
+        return e0.elapsed_time(e1)
+
+    res = {}
+    with ClockSampler(dev.index) as clk:
+        for packed, name in ((0, "scalar"), (1, "packed")):
+            timed(packed, 1000)
+            ms = timed(packed, 20000)
+            iters = int(20000 * sample_ms / max(ms, 1e-3)) + 1
+            runs = sorted(timed(packed, iters) for _ in range(samples))
+            med = runs[len(runs) // 2]
+            res[name] = grid * 256 * iters * 32 / (med * 1e-3) / 1e12
+    res["tflops"] = max(res["scalar"], res["packed"])
+    res["clocks"] = clk.summary()
+    res["how"] = (f"gemm_launch_fma_peak: {grid} CTAs x 256 threads x 16 FMA chains, median of {samples} "
+                  f"launches of >= {sample_ms:g} ms, scalar fma.rn.f32 and packed fma.rn.f32x2; the faster form")
+    return res
 
 
 class Call:
@@ -138,8 +181,7 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv") if os.path.isdir(
-            os.path.join(ROOT, "gpurun_out")) else f"/tmp/clocks_{os.getpid()}.csv"
+        self.path = os.path.join(tempfile.gettempdir(), f"dgt_clocks_{os.getpid()}_{id(self)}.csv")
 
     def __enter__(self):
         try:
@@ -271,7 +313,8 @@ def bench_reference(args, world, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights)",
             "config": {"workload": "gpt_projections_fp32_tf32", "tokens": si.GPT_TOKENS, "d_model": 384,
-                       "gemms_per_step": 30},
+                       "gemms_per_step": 30, "parallelism": f"replicas{world}",
+                       "l2": "host memory (the oracle runs on the CPU cores)"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -295,6 +338,11 @@ def bench_ours(args, world, rank, local):
             raise SystemExit(f"--only {args.only!r} matches no GEMM of the step")
     step_flops = sum(c.case.flops for c in calls)
     pk = peaks()
+    fp32_peak = None
+    if not args.no_fp32_peak:
+        fp32_peak = measure_fp32_peak(dev)
+        pk["fp32_alu_tflops_derived"] = pk["fp32_alu_tflops"]
+        pk["fp32_alu_tflops"] = fp32_peak["tflops"]
 
     def step():
         for c in calls:
@@ -359,7 +407,8 @@ def bench_ours(args, world, rank, local):
     if dom == "fp32":
         roof = {"bound": "alu", "kernel": "simt_gemm_kernel (FP32 FFMA)", "achieved": achieved,
                 "peak": pk["fp32_alu_tflops"], "unit": "TFLOP/s",
-                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz"}
+                "peak_source": ("measured on this GPU in this run: " + fp32_peak["how"]) if fp32_peak else
+                               "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz"}
     else:
         roof = {"bound": "tensor", "kernel": "tc_gemm_kernel (tcgen05 kind::tf32)", "achieved": achieved,
                 "peak": pk["tf32_tflops_sustained"], "unit": "TFLOP/s",
@@ -438,6 +487,10 @@ def bench_ours(args, world, rank, local):
         e2e = {"value": world * step_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
 
+    configs = None
+    if rank == 0 and not args.no_configs:
+        configs = bench_configs(args, h, dev, pk)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f, s, rows = oracle_sample(cpu_meta(), args.cpu_macs)
@@ -455,7 +508,8 @@ def bench_ours(args, world, rank, local):
                            "l2": "inputs larger than L2: a step touches %.2f GB; no tensor is re-read "
                                  "before >4x L2 of other traffic" % (sum(c.bytes() for c in calls) / 1e9)},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * args.steps,
-                "clocks": clk.summary(), "shapes": shapes, "peaks": pk}
+                "clocks": clk.summary(), "shapes": shapes, "peaks": pk, "fp32_peak": fp32_peak,
+                "configs": configs}
         print(json.dumps(line), flush=True)
     h.close()
 
@@ -489,6 +543,60 @@ def sweep_cases(workload):
             case = si.GemmCase(c.name + ".T", False, True, c.M, c.N, c.K)
             out.append((f"fp8.{case.name}", "fp8", case, 1.0, 0.0, 1.0))
     return out
+
+
+GATE = 0.70  # the configurations' roofline targets: tensor peak (large squares, 8192-class), HBM (decode)
+
+
+def config_cases():
+    """(config, gate, label, mode, case, alpha, beta, weight_std) of every
+    configuration other than the GPT step, for the default benchmark line:
+    0: FP32 256^3; 2: the square sweep, every mode, both alpha/beta pairs;
+    3: the large BF16 shapes; 4: the decode shapes, weights K x N and N x K.
+    The gates: the tensor peak for TF32/BF16 squares of 4096 and the large
+    BF16 shapes, HBM bandwidth for the decode shapes (graph timing)."""
+    out = [(0, None, "fp32.square256", "fp32", si.square_case(256), 1.0, 0.0, 1.0)]
+    for label, mode, c, alpha, beta, wstd in sweep_cases("square"):
+        gate = "tensor" if mode != "fp32" and c.M >= 4096 else None
+        out.append((2, gate, label, mode, c, alpha, beta, wstd))
+    for label, mode, c, alpha, beta, wstd in sweep_cases("large"):
+        out.append((3, "tensor", label, mode, c, alpha, beta, wstd))
+    for label, mode, c, alpha, beta, wstd in sweep_cases("skinny"):
+        out.append((4, "hbm", label, mode, c, alpha, beta, wstd))
+    return out
+
+
+def bench_configs(args, h, dev, pk, samples=3, sample_ms=10.0):
+    """Every other configuration's shapes, timed in this process as the
+    per-shape sweeps time them (operands rotated over > 3x L2, R launches
+    per sample for >= sample_ms, back to back, as one CUDA graph, and the
+    identity null), with fewer, shorter samples so that the default run
+    stays within minutes; gated shapes say whether they meet 0.70."""
+    stream = torch.cuda.Stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    meta = config_cases()
+    shapes = []
+    h.set_option("tile_n", 0)
+    with ClockSampler(dev.index) as clk:
+        _sweep_shapes(args, h, stream, pk, l2, dev, shapes, cases=[m[2:] for m in meta], samples=samples,
+                      sample_ms=sample_ms)
+    by_label = {m[2]: m for m in meta}
+    met = total = 0
+    for x in shapes:
+        cfg, gate = by_label[x["gemm"]][0], by_label[x["gemm"]][1]
+        x["config"] = cfg
+        x["gate"] = None if gate is None else f"{gate} >= {GATE}"
+        if gate is not None:
+            x["gate_met"] = bool(x["roofline_frac"] >= GATE and x["bound"] in (("hbm",) if gate == "hbm"
+                                                                               else ("tensor",)))
+            met += x["gate_met"]
+            total += 1
+    return {"shapes": shapes, "gates_met": met, "gates": total, "clocks": clk.summary(),
+            "timing": f"one process, median of {samples} samples of >= {sample_ms:g} ms per shape; decode shapes "
+                      "gated on the CUDA-graph timing; operands rotated over > 3x L2",
+            "roofline": "roofline_frac against the burst peaks (tensor: MEASURED_PEAKS bf16 x the nominal "
+                        "tf32/bf16 ratio for TF32), HBM: MEASURED_PEAKS copy bandwidth; FP32 against the "
+                        "measured FMA roof"}
 
 
 def _elem_bytes(mode):
@@ -565,8 +673,8 @@ def bench_sweep(args):
     return shapes, clk.summary()
 
 
-def _sweep_shapes(args, h, stream, pk, l2, dev, shapes):
-    for label, mode, c, alpha, beta, wstd in sweep_cases(args.workload):
+def _sweep_shapes(args, h, stream, pk, l2, dev, shapes, cases=None, samples=SAMPLES, sample_ms=SAMPLE_MS):
+    for label, mode, c, alpha, beta, wstd in (cases if cases is not None else sweep_cases(args.workload)):
         if args.only:
             import re
             if not re.fullmatch(args.only, label):
@@ -598,9 +706,9 @@ def _sweep_shapes(args, h, stream, pk, l2, dev, shapes):
         chunk = max(copies, QUEUE_CALLS // max(plan["kernels"], 1))
         # R: enough launches that one sample covers SAMPLE_MS of device time.
         t_est = _timed_back_to_back(call, max(2 * copies, 10), stream, chunk)
-        reps = int(min(MAX_REPS, max(10, math.ceil(SAMPLE_MS / max(t_est, 1e-4)))))
+        reps = int(min(MAX_REPS, max(10, math.ceil(sample_ms / max(t_est, 1e-4)))))
         reps = max(reps, copies)
-        dev_ms = [_timed_back_to_back(call, reps, stream, chunk) for _ in range(SAMPLES)]
+        dev_ms = [_timed_back_to_back(call, reps, stream, chunk) for _ in range(samples)]
         # As the host issues them.
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -620,7 +728,7 @@ def _sweep_shapes(args, h, stream, pk, l2, dev, shapes):
             graph.replay()
             stream.synchronize()
             gm = []
-            for _ in range(SAMPLES):
+            for _ in range(samples):
                 with torch.cuda.stream(stream):
                     e0.record(stream)
                     graph.replay()
@@ -636,7 +744,7 @@ def _sweep_shapes(args, h, stream, pk, l2, dev, shapes):
         # The identity null of this configuration.
         call(0)
         null_ms = _stats([_timed_back_to_back(lambda r: h.launch_null(stream), reps, stream, QUEUE_CALLS)
-                          for _ in range(SAMPLES)])
+                          for _ in range(samples)])
         stream.synchronize()
         byts = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N * (2 if beta != 0 else 1)
         peak = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops"], "bf16": pk["bf16_tflops"],
@@ -655,7 +763,7 @@ def _sweep_shapes(args, h, stream, pk, l2, dev, shapes):
                        "graph_error": graph_err,
                        "ms_stream": round(stream_ms, 5),
                        "null_ms": {k: round(v, 5) for k, v in null_ms.items()},
-                       "samples": SAMPLES, "reps": reps,
+                       "samples": samples, "reps": reps,
                        "tflops": round(c.flops / (t * 1e-3) / 1e12, 2),
                        "gbs": round(byts / (t * 1e-3) / 1e9, 1), "bound": "hbm" if t_m > t_c else
                        ("alu" if mode == "fp32" else "tensor"), "roofline_frac": round(max(t_c, t_m) / (t * 1e-3), 3),
@@ -889,13 +997,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-shape timing of the other configurations in the default line")
+    ap.add_argument("--no-fp32-peak", action="store_true",
+                    help="take the derived FP32 roof instead of measuring it with the FMA kernel")
     ap.add_argument("--cpu-macs", type=float, default=4.5e10,
                     help="oracle multiply-adds in the CPU baseline (about 10 s on 16 host cores)")
     ap.add_argument("--ref-macs", type=float, default=3e8, help="oracle multiply-adds per reference step")
     ap.add_argument("--tile-n", type=int, default=0, help="sweeps: force the tensor-core tile width (128/256)")
     ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
     ap.add_argument("--pair", type=int, default=None,
-                    help="sweeps: force the CTA-pair form (0 planner, 1 none, 2 multicast B, 3 one 256-row MMA per pair)")
+                    help="sweeps: CTA pairs issuing one 256-row MMA (0 wherever allowed, 1 never)")
     ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "large_fp8", "skinny", "skinny_fp8", "epilogue",
                              "gpt_full"],
                     help="gpt: the timed step; the others print a per-shape sweep")

@@ -30,6 +30,8 @@ def test_reference_arm_prints_one_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"] == "gpt_projections_fp32_tf32"
+    # the same config keys as the main line
+    assert {"tokens", "d_model", "gemms_per_step", "parallelism", "l2"} <= set(d["config"])
 
 
 def test_reference_arm_under_torchrun_two_ranks():
@@ -92,3 +94,20 @@ def test_fp8_sweeps_time_the_k_major_form_against_the_fp8_peak():
     assert pk["fp8_tflops"] == 2 * pk["bf16_tflops"]
     assert pk["fp8_tflops_sustained"] == 2 * pk["bf16_tflops_sustained"]
     assert bench._elem_bytes("fp8") == 1
+
+
+def test_default_line_times_every_other_config():
+    """The default line carries configs 0, 2, 3 and 4 beside the GPT step,
+    with the gates where the configurations set them: the tensor peak for
+    TF32/BF16 squares of 4096 (both alpha/beta pairs) and both large BF16
+    shapes, HBM for all 18 decode shapes."""
+    import bench
+    cases = bench.config_cases()
+    assert {c[0] for c in cases} == {0, 2, 3, 4}
+    labels = [c[2] for c in cases]
+    assert len(set(labels)) == len(labels)
+    assert sum(1 for c in cases if c[0] == 2) == 18 and sum(1 for c in cases if c[0] == 4) == 18
+    tensor = sorted(c[2] for c in cases if c[1] == "tensor")
+    assert len(tensor) == 6 and all("4096" in t or "8192" in t for t in tensor)
+    assert all(c[1] == "hbm" for c in cases if c[0] == 4)
+    assert all(c[1] is None for c in cases if c[3] == "fp32")
