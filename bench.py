@@ -536,6 +536,13 @@ def sweep_cases(workload):
         for M, N, K in ((4096, 4096, 4096),) + si.LARGE_BF16:
             out.append((f"fp8.{M}x{N}x{K}.T", "fp8", si.GemmCase(f"{M}x{N}x{K}.T", False, True, M, N, K),
                         1.0, 0.0, 1.0))
+    elif workload in ("skinny_nvfp4", "skinny_mxfp8"):
+        # block-scaled weights stored N x K (the form the kernels read): random
+        # finite codes and scales (a quantiser would only change their values)
+        mode = "nvfp4" if workload == "skinny_nvfp4" else "mxfp8_e4m3"
+        for c in si.skinny_cases():
+            case = si.GemmCase(c.name + ".T", False, True, c.M, c.N, c.K)
+            out.append((f"{mode}.{case.name}", mode, case, 1.0, 0.0, 1.0))
     elif workload == "skinny_fp8":
         # E4M3 weights stored N x K (the form the FP8 mode takes), N(0, 1)
         # codes: a per-tensor scale would only change alpha
@@ -600,7 +607,35 @@ def bench_configs(args, h, dev, pk, samples=3, sample_ms=10.0):
 
 
 def _elem_bytes(mode):
-    return {"bf16": 2, "fp8": 1}.get(mode, 4)
+    return {"bf16": 2, "fp8": 1, "mxfp8_e4m3": 1, "nvfp4": 0.5}.get(mode, 4)
+
+
+def _scale_bytes(mode, rows, K):
+    """Bytes of the block scales of a rows x K block-scaled operand."""
+    if mode not in ("nvfp4", "mxfp8_e4m3"):
+        return 0
+    bs = 16 if mode == "nvfp4" else 32
+    return rows * -(-K // bs)
+
+
+def _block_scaled_set(mode, c, dev, g):
+    """Codes and tiled scales of a block-scaled case (A M x K, B N x K)."""
+    import dense_gemm_transformer_gb300 as dg
+    per = 2 if mode == "nvfp4" else 1
+    bs = 16 if mode == "nvfp4" else 32
+    nb = -(-c.K // bs)
+
+    def codes(rows):
+        if mode == "nvfp4":
+            return torch.randint(0, 256, (rows, c.K // per), generator=g, dtype=torch.uint8).to(dev)
+        mag = torch.randint(0x20, 0x50, (rows, c.K), generator=g, dtype=torch.uint8)
+        return (mag | (torch.randint(0, 2, (rows, c.K), generator=g, dtype=torch.uint8) << 7)).to(dev)
+
+    def scales(rows):
+        lo, hi = (120, 131) if mode != "nvfp4" else (0x28, 0x48)
+        return dg.tile_block_scales(torch.randint(lo, hi, (rows, nb), generator=g, dtype=torch.uint8).to(dev))
+
+    return codes(c.M), scales(c.M), codes(c.N), scales(c.N)
 
 
 def _operand_dtype(mode):
@@ -663,6 +698,8 @@ def bench_sweep(args):
         h.set_option("tile_n", args.tile_n)
     if args.pair is not None:
         h.set_option("pair", args.pair)
+    if args.split_k:
+        h.set_option("split_k", args.split_k)
     stream = torch.cuda.Stream(dev)
     pk = peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -679,24 +716,35 @@ def _sweep_shapes(args, h, stream, pk, l2, dev, shapes, cases=None, samples=SAMP
             import re
             if not re.fullmatch(args.only, label):
                 continue
-        dt = _operand_dtype(mode)
         es = _elem_bytes(mode)
-        per_set = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N
+        sf_bytes = _scale_bytes(mode, c.M, c.K) + _scale_bytes(mode, c.N, c.K)
+        per_set = int(es * (c.M * c.K + c.K * c.N)) + sf_bytes + 4 * c.M * c.N
         copies = max(1, min(32, -(-3 * l2 // per_set)))
         g = torch.Generator(device="cpu")
         g.manual_seed(si.BASE_SEED)
-        A0 = torch.randn(c.a_shape, generator=g).to(dt).to(dev)
-        B0 = (torch.randn(c.b_shape, generator=g) * wstd).to(dt).to(dev)
         sets = []
-        for i in range(copies):
-            A = A0 if i == 0 else A0.clone()
-            B = B0 if i == 0 else B0.clone()
-            C = torch.randn((c.M, c.N), generator=g).to(dev)
-            sets.append((A, B, C))
+        if sf_bytes:
+            A0, SA0, B0, SB0 = _block_scaled_set(mode, c, dev, g)
+            for i in range(copies):
+                cl = (lambda t: t) if i == 0 else (lambda t: t.clone())
+                sets.append((cl(A0), cl(SA0), cl(B0), cl(SB0), torch.randn((c.M, c.N), generator=g).to(dev)))
 
-        def call(r):
-            A, B, C = sets[r % copies]
-            h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta, stream=stream)
+            def call(r):
+                A, SA, B, SB, C = sets[r % copies]
+                h.run_block_scaled(A, SA, B, SB, C, mode=mode, alpha=alpha, beta=beta, stream=stream)
+        else:
+            dt = _operand_dtype(mode)
+            A0 = torch.randn(c.a_shape, generator=g).to(dt).to(dev)
+            B0 = (torch.randn(c.b_shape, generator=g) * wstd).to(dt).to(dev)
+            for i in range(copies):
+                A = A0 if i == 0 else A0.clone()
+                B = B0 if i == 0 else B0.clone()
+                C = torch.randn((c.M, c.N), generator=g).to(dev)
+                sets.append((A, B, C))
+
+            def call(r):
+                A, B, C = sets[r % copies]
+                h.run(A, B, C, mode=mode, transA=c.transA, transB=c.transB, alpha=alpha, beta=beta, stream=stream)
 
         with torch.cuda.stream(stream):
             for r in range(copies):
@@ -746,11 +794,13 @@ def _sweep_shapes(args, h, stream, pk, l2, dev, shapes, cases=None, samples=SAMP
         null_ms = _stats([_timed_back_to_back(lambda r: h.launch_null(stream), reps, stream, QUEUE_CALLS)
                           for _ in range(samples)])
         stream.synchronize()
-        byts = es * (c.M * c.K + c.K * c.N) + 4 * c.M * c.N * (2 if beta != 0 else 1)
+        byts = int(es * (c.M * c.K + c.K * c.N)) + sf_bytes + 4 * c.M * c.N * (2 if beta != 0 else 1)
+        # block-scaled: the dense rate of the element type (FP4: twice FP8's, nominal)
         peak = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops"], "bf16": pk["bf16_tflops"],
-                "fp8": pk["fp8_tflops"]}[mode]
+                "fp8": pk["fp8_tflops"], "mxfp8_e4m3": pk["fp8_tflops"], "nvfp4": 2 * pk["fp8_tflops"]}[mode]
         peak_s = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops_sustained"],
-                  "bf16": pk["bf16_tflops_sustained"], "fp8": pk["fp8_tflops_sustained"]}[mode]
+                  "bf16": pk["bf16_tflops_sustained"], "fp8": pk["fp8_tflops_sustained"],
+                  "mxfp8_e4m3": pk["fp8_tflops_sustained"], "nvfp4": 2 * pk["fp8_tflops_sustained"]}[mode]
         t_c, t_m = c.flops / (peak * 1e12), byts / (pk["hbm_gbs"] * 1e9)
         t_cs = c.flops / (peak_s * 1e12)
         st = _stats(dev_ms)
@@ -804,6 +854,8 @@ def bench_sweep_processes(args):
             cmd += ["--tile-n", str(args.tile_n)]
         if args.pair is not None:
             cmd += ["--pair", str(args.pair)]
+        if args.split_k:
+            cmd += ["--split-k", str(args.split_k)]
         out = subprocess.run(cmd, capture_output=True, text=True, check=True).stdout
         line = json.loads(out.strip().splitlines()[-1])
         runs.append(line["shapes"])
@@ -1008,8 +1060,9 @@ def main():
     ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
     ap.add_argument("--pair", type=int, default=None,
                     help="sweeps: CTA pairs issuing one 256-row MMA (0 wherever allowed, 1 never)")
-    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "large_fp8", "skinny", "skinny_fp8", "epilogue",
-                             "gpt_full"],
+    ap.add_argument("--split-k", type=int, default=0, help="sweeps: force this many K slices (0: planner)")
+    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "large_fp8", "skinny", "skinny_fp8",
+                                                          "skinny_nvfp4", "skinny_mxfp8", "epilogue", "gpt_full"],
                     help="gpt: the timed step; the others print a per-shape sweep")
     ap.add_argument("--mode", default="tf32", choices=["fp32", "tf32", "bf16"],
                     help="gpt_full: the mode of the whole step")

@@ -26,6 +26,10 @@ MODES = {"fp32": 0, "tf32": 1, "bf16": 2, "fp8": 3, "fp8_e4m3": 3, "fp8_e5m2": 4
 # The 8-bit format of (A, B) in each FP8 mode.
 FP8_FORMATS = {"fp8": ("e4m3", "e4m3"), "fp8_e4m3": ("e4m3", "e4m3"), "fp8_e5m2": ("e5m2", "e5m2"),
                "fp8_e4m3_e5m2": ("e4m3", "e5m2"), "fp8_e5m2_e4m3": ("e5m2", "e4m3")}
+# Block-scaled modes (gemm_run_block_scaled): element format, K elements per
+# scale, scale format.
+BLOCK_SCALED_MODES = {"mxfp8_e4m3": (7, "e4m3", 32, "e8m0"), "mxfp8_e5m2": (8, "e5m2", 32, "e8m0"),
+                      "nvfp4": (9, "e2m1", 16, "ue4m3")}
 FAMILIES = {"auto": 0, "simt": 1, "tc": 2, "skinny": 3}
 OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3, "pretranspose": 4, "pair": 5, "wait_limit_us": 6,
            "fault_skip_stage": 7}
@@ -54,7 +58,7 @@ class Plan(ctypes.Structure):
                 ("tile_k", ctypes.c_int32), ("split_k", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("kernels", ctypes.c_int32), ("packed", ctypes.c_int32),
                 ("schedule", ctypes.c_int32), ("cluster", ctypes.c_int32), ("pair_mma", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 4)]
+                ("epilogue_fused", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 _lib = None
@@ -102,7 +106,7 @@ def header_functions() -> list[str]:
     """Names of the functions include/gemm.h declares."""
     with open(HEADER) as f:
         text = f.read()
-    return sorted(set(re.findall(r"^\s*(?:gemm_status_t|const char\*)\s+(gemm_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:gemm_status_t|const char\*|int64_t)\s+(gemm_\w+)\s*\(", text, re.M)))
 
 
 def status_string(status: int) -> str:
@@ -178,7 +182,7 @@ class Gemm:
                 "tile_k": p.tile_k, "split_k": p.split_k, "stages": p.stages, "grid": p.grid,
                 "kernels": p.kernels, "packed": p.packed,
                 "schedule": {0: "tiles", 1: "split_k", 2: "stream_k", 3: "tail_split"}.get(p.schedule, "tiles"),
-                "cluster": p.cluster, "pair_mma": p.pair_mma}
+                "cluster": p.cluster, "pair_mma": p.pair_mma, "epilogue_fused": p.epilogue_fused}
 
     def check_device(self, stream=None) -> int:
         """Synchronize the stream and return the device status (0 = ok)."""
@@ -195,6 +199,36 @@ class Gemm:
                                 int(transB), int(M), int(N), int(K), float(alpha), A, int(lda), B, int(ldb),
                                 float(beta), C, int(ldc), _stream_ptr(stream))
         _check(st, "gemm_run")
+
+    def run_block_scaled(self, A, SA, B, SB, C, mode="nvfp4", alpha=1.0, beta=0.0, stream=None):
+        """C = alpha * (A . SA) (B . SB)^T + beta * C through gemm_run_block_scaled.
+
+        A: M x K codes (uint8; NVFP4: M x K/2 bytes, two E2M1 codes a byte),
+        B: N x K codes (N x K/2 for NVFP4), both K contiguous; SA, SB: their
+        scales in the tiled layout (tile_block_scales); C: M x N float32."""
+        import torch
+        code, _, _, _ = BLOCK_SCALED_MODES[mode]
+        for t, name in ((A, "A"), (B, "B"), (SA, "SA"), (SB, "SB")):
+            if t.dtype != torch.uint8 or not t.is_cuda:
+                raise TypeError(f"{name} must be a uint8 CUDA tensor")
+        per = 2 if mode == "nvfp4" else 1
+        M, K = A.shape[0], A.shape[1] * per
+        N = B.shape[0]
+        if B.shape[1] * per != K or tuple(C.shape) != (M, N) or C.dtype != torch.float32:
+            raise ValueError("shapes do not agree")
+        pa, lda = _matrix(A, "A")
+        pb, ldb = _matrix(B, "B")
+        pc, ldc = _matrix(C, "C")
+        if stream is None:
+            stream = torch.cuda.current_stream(C.device)
+        fn = self._lib.gemm_run_block_scaled
+        i64, vp, f32, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+        fn.argtypes = [vp, i32, i64, i64, i64, f32, vp, i64, vp, vp, i64, vp, f32, vp, i64, vp]
+        fn.restype = i32
+        st = fn(self._h, code, M, N, K, float(alpha), pa, lda * per, SA.data_ptr(), pb, ldb * per, SB.data_ptr(),
+                float(beta), pc, ldc, _stream_ptr(stream))
+        _check(st, "gemm_run_block_scaled")
+        return C
 
     def run(self, A, B, C, mode="fp32", transA=False, transB=False, alpha=1.0, beta=0.0, stream=None,
             act="none", bias=None, aux=None):
@@ -244,6 +278,27 @@ class Gemm:
                                          ctypes.byref(ep), _stream_ptr(stream))
         _check(st, "gemm_run_epilogue")
         return C
+
+
+def tile_block_scales(S, stream=None):
+    """The tiled layout of block scales that gemm_run_block_scaled reads:
+    S is a rows x blocks uint8 tensor on the device (row-major); returns a
+    new uint8 device tensor written by gemm_block_scales_tile."""
+    import torch
+    lib = load()
+    fn_bytes, fn = lib.gemm_block_scales_tiled_bytes, lib.gemm_block_scales_tile
+    fn_bytes.argtypes, fn_bytes.restype = [ctypes.c_int64, ctypes.c_int64], ctypes.c_int64
+    fn.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    if S.dtype != torch.uint8 or S.dim() != 2 or not S.is_cuda:
+        raise ValueError("scales must be a 2-D uint8 CUDA tensor")
+    rows, blocks = S.shape
+    T = torch.empty((max(int(fn_bytes(rows, blocks)), 16),), dtype=torch.uint8, device=S.device)
+    ps, lds = _matrix(S, "S")
+    if stream is None:
+        stream = torch.cuda.current_stream(S.device)
+    _check(fn(rows, blocks, ps, lds, T.data_ptr(), _stream_ptr(stream)), "gemm_block_scales_tile")
+    return T
 
 
 def _stream_ptr(stream):

@@ -42,7 +42,7 @@ struct gemm_handle_s {
   int opt_pair = 0;
   int64_t opt_wait_us = 0;   // bounded-wait limit of the tcgen05 kernel (0: the default)
   int opt_fault_skip = 0;    // test hook (GEMM_OPT_FAULT_SKIP_STAGE)
-  int sk_active[3][dgt::kSkinnyMaxCluster + 1];  // small-M kernel per mode (TF32, BF16, FP8): resident clusters (-1: not queried)
+  int sk_active[5][dgt::kSkinnyMaxCluster + 1];  // small-M kernel per mode (TF32, BF16, FP8, MXFP8, NVFP4): resident clusters (-1: not queried)
   dgt::TmaCache* tma_cache = nullptr;             // TMA descriptors of earlier calls
   gemm_plan_t plan{};
   dgt::LaunchShape null_shape;  // main kernel of the last successful gemm_run (for gemm_launch_null)
@@ -436,32 +436,74 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   // reproduces; with short K the tile's fixed cost dominates and 1.14 still
   // ranks the widths as measured.
   const double pair_gain = (mode == GEMM_MODE_TF32 && kb >= 24) ? 1.3 : 1.14;
-  auto plan_for = [&](int tn) {
-    const bool pr = pair_ok(tn);
+  // Estimated time of tiles of tn columns, as CTA pairs (pr) or one CTA per
+  // tile.  Shapes with fewer tiles than half the SMs and 8 or more K blocks
+  // are split along K so that the (tile, slice) units fill one wave (then
+  // the slices' partial sums pass through the workspace); others may cut
+  // their last rows of units into K slices (plan_tail).
+  auto split_units = [&](int tn, bool pr) {
+    const int64_t units = (pr ? ceil_div(tm_tiles, 2) : tm_tiles) * ceil_div(Nk, tn);
+    return std::max<int64_t>(1, std::min<int64_t>((pr ? sms / 2 : sms) / units, kb / 4));
+  };
+  auto plan_for = [&](int tn, bool pr) {
     const int64_t rows = pr ? ceil_div(tm_tiles, 2) : tm_tiles;
+    const int64_t cols = ceil_div(Nk, tn);
+    const int64_t slots = pr ? sms / 2 : sms;
     const double unit_s = 2.0 * 128.0 * 256.0 * static_cast<double>(K) / peak *
                           (128.0 * 128.0 + 128.0 * tn) / (128.0 * 384.0) / (pr ? pair_gain : 1.0);
     const double c_row_bytes = 4.0 * static_cast<double>(Nk) * (pr ? 256.0 : 128.0);
-    const bool may_cut = !swap && h->opt_split_k == 0 && !(2 * tm_tiles * ceil_div(Nk, tn) <= sms && kb >= 8);
-    if (!may_cut) {
+    const bool split = !swap && h->opt_split_k == 0 && 2 * tm_tiles * cols <= sms && kb >= 8;
+    if (split) {
+      int64_t sl = split_units(tn, pr);
+      const int64_t per = ceil_div(kb, sl);
+      sl = ceil_div(kb, per);
+      TailPlan t;
+      t.seconds = static_cast<double>(ceil_div(rows * cols * sl, slots)) * unit_s * static_cast<double>(per) /
+                      static_cast<double>(kb) +
+                  4.0 * static_cast<double>(Mk) * static_cast<double>(Nk) * static_cast<double>(sl + 1 + (beta != 0.f)) /
+                      kHbmBytes +
+                  kLaunchS;
+      return t;
+    }
+    if (swap || h->opt_split_k > 0) {
       TailPlan none;
-      none.seconds = static_cast<double>(ceil_div(rows * ceil_div(Nk, tn), pr ? sms / 2 : sms)) * unit_s;
+      none.seconds = static_cast<double>(ceil_div(rows * cols, slots)) * unit_s;
       return none;
     }
-    return plan_tail(rows, ceil_div(Nk, tn), kb, pr ? sms / 2 : sms, unit_s, c_row_bytes, beta != 0.f);
+    return plan_tail(rows, cols, kb, slots, unit_s, c_row_bytes, beta != 0.f);
   };
   int tile_n = 16;
+  bool pair = false;
   if (!swap && h->opt_tile_n != 0) {
+    // a forced width pairs wherever it can (unless pairs are turned off)
     if (!dgt::tc_tile_ok(mode, h->opt_tile_n, false, b_mn_kernel)) return GEMM_ERR_NOT_SUPPORTED;
     tile_n = h->opt_tile_n;
+    pair = pair_ok(tile_n);
   } else if (!swap) {
     double best = 0.0;
+    // A TF32 A stored with M contiguous reaches the 128-column one-CTA
+    // kernel through TMEM; every other width or a pair must transpose it
+    // first: 8 bytes of HBM traffic per element of A, charged to them here
+    // (without it the dW products, whose A is the whole activation matrix,
+    // took wider pairs and ran 1.2-2x slower).
+    const bool tmem_a_possible =
+        mode == GEMM_MODE_TF32 && ta_k != 0 && Nk < 1536 && h->opt_pretranspose != 2;
+    const double a_transpose_s = 8.0 * static_cast<double>(Mk) * static_cast<double>(K) / kHbmBytes + kLaunchS;
+    // Every width, as pairs where they can run and as single CTAs: pairs
+    // halve each CTA's B traffic, but at a small odd number of tile rows
+    // (M = 384: a pair row is half idle) single CTAs win (the K-split dW
+    // products: 88-90 us as single CTAs against 101-108 us as pairs).
     for (int tn : {256, 224, 192, 128}) {
       if (!dgt::tc_tile_ok(mode, tn, false, b_mn_kernel)) continue;
-      const double cost = plan_for(tn).seconds;
-      if (tile_n == 16 || cost < best * 0.999) {
-        best = cost;
-        tile_n = tn;
+      for (const bool pr : {true, false}) {
+        if (pr && !pair_ok(tn)) continue;
+        const bool a_via_tmem = tn == 128 && !pr;
+        const double cost = plan_for(tn, pr).seconds + (tmem_a_possible && !a_via_tmem ? a_transpose_s : 0.0);
+        if (tile_n == 16 || cost < best * 0.999) {
+          best = cost;
+          tile_n = tn;
+          pair = pr;
+        }
       }
     }
   }
@@ -480,19 +522,17 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   } else if (swap) {
     splits = 1;  // two or more waves of weight tiles: a K split would only add traffic
   } else if (2 * tiles <= sms && kb >= 8) {
-    splits = std::min<int64_t>(sms / tiles, kb / 4);
-    splits = std::max<int64_t>(splits, 1);
+    splits = split_units(tile_n, pair);
   }
   int64_t kb_per = ceil_div(kb, splits);
   splits = ceil_div(kb, kb_per);
   // More than a wave of units that does not end on a whole wave: the last
   // rows of units may be cut into K slices so that the final wave is full.
-  const bool pair = pair_ok(tile_n);
   const int64_t unit_rows = pair ? ceil_div(tm_tiles, 2) : tm_tiles;
   const int64_t unit_cols = ceil_div(Nk, tile_n);
   TailPlan tail;
   if (!swap && splits == 1 && h->opt_split_k == 0) {
-    tail = plan_for(tile_n);
+    tail = plan_for(tile_n, pair);
     if (tail.rows > 0) {
       splits = tail.slices;
       kb_per = tail.kb_per;
@@ -581,9 +621,10 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
       if (launch_epilogue(M, N, C, ldc, epi, s) != cudaSuccess) return GEMM_ERR_CUDA;
       ++kernels;
     }
-    set_plan(h, GEMM_FAMILY_SKINNY, 128, 16, bk, a.splits, dgt::kSkinnyStages, a.grid, kernels,
+    set_plan(h, GEMM_FAMILY_SKINNY, 128, 16, bk, a.splits, dgt::skinny_stages(mode), a.grid, kernels,
              (pack_b ? 1 : 0) | (pack_a ? 2 : 0));
     h->plan.cluster = a.splits;
+    h->plan.schedule = a.splits > 1 ? 1 : 0;
     return GEMM_OK;
   }
   // Partial sums are kept in the caller's M x N orientation, from C row
@@ -595,6 +636,13 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.dp_units = static_cast<int>(tail.rows > 0 ? (unit_rows - tail.rows) * unit_cols : 0);
   a.tail_tm0 = static_cast<int>(tail.rows > 0 ? unit_rows - tail.rows : 0);
   a.status = h->d_status;
+  // The elementwise epilogue inside the GEMM kernel's epilogue warps, where
+  // it is built for the operand layouts (K-major A): whole tiles get it at
+  // their store, and a split's partial sums get it in the slice reduce.
+  const bool fuse = epilogue_active(epi) && (mode == GEMM_MODE_TF32 || mode == GEMM_MODE_BF16) &&
+                    dgt::tc_epi_ok(mode, a_mn, b_mn);
+  a.fuse_epi = fuse;
+  a.epi = epi;
   a.wait_ns = static_cast<uint64_t>(h->opt_wait_us) * 1000u;
   a.fault_skip = h->opt_fault_skip;
   // CTA pairs issuing one 256-row MMA for tiles of 192 columns or more
@@ -606,16 +654,17 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   a.group_m = a.pair ? 8 : 16;
   if (launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
   ++kernels;
-  // The epilogue: in the split-K reduction when it writes every element of
-  // C (plain split-K), or else in one pass over C after the GEMM.
-  const bool epi_in_reduce = splits > 1 && tail_row0 == 0;
+  // The epilogue: fused into the GEMM kernel (and the reduction of any cut
+  // rows), in the split-K reduction when it writes every element of C
+  // (plain split-K), or else in one pass over C after the GEMM.
+  const bool epi_in_reduce = splits > 1 && (tail_row0 == 0 || fuse);
   if (splits > 1) {
     if (launch_splitk_reduce(M - tail_row0, N, a.splits, a.ws, ws_ld, C + tail_row0 * ldc, ldc, alpha, beta,
                              epi_in_reduce ? epi : dgt::EpiParams{}, tail_row0, s) != cudaSuccess)
       return GEMM_ERR_CUDA;
     ++kernels;
   }
-  if (!epi_in_reduce && epilogue_active(epi)) {
+  if (!fuse && !epi_in_reduce && epilogue_active(epi)) {
     if (launch_epilogue(M, N, C, ldc, epi, s) != cudaSuccess) return GEMM_ERR_CUDA;
     ++kernels;
   }
@@ -624,6 +673,60 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
   h->plan.cluster = a.pair ? 2 : 1;
   h->plan.pair_mma = a.pair;
   h->plan.schedule = tail.rows > 0 ? 3 : (a.splits > 1 ? 1 : 0);
+  h->plan.epilogue_fused = fuse ? 1 : 0;
+  return GEMM_OK;
+}
+
+// The block-scaled product (gemm_run_block_scaled) after its argument
+// checks: the small-M cluster kernel in its block-scaled build (kernel mode
+// 4 for MXFP8, 5 for NVFP4), swapped like every small-M call -- the weights
+// B (N x K) are the 128-row MMA operand and their scales the kernel's
+// A scales, the activations A (M x K, M <= 16) the 16-row operand.  Codes
+// and scales are read in place; K and the leading dimensions travel in
+// bytes.
+gemm_status_t run_block_scaled(gemm_handle_s* h, int mode, int64_t M, int64_t N, int64_t K, float alpha,
+                               const void* A, int64_t lda, const void* SA, const void* B, int64_t ldb,
+                               const void* SB, float beta, float* C, int64_t ldc, cudaStream_t s) {
+  using namespace dgt;
+  const bool nvfp4 = mode == GEMM_MODE_NVFP4;
+  const int kmode = nvfp4 ? 5 : 4;
+  const int64_t kbytes = nvfp4 ? K / 2 : K;
+  const int64_t lda_b = nvfp4 ? lda / 2 : lda, ldb_b = nvfp4 ? ldb / 2 : ldb;
+  const int64_t bs = nvfp4 ? 16 : 32;  // K elements per scale
+  const int64_t tiles = ceil_div(N, 128);
+  const int64_t kb = ceil_div(kbytes, 128);
+  int64_t splits = (h->opt_split_k > 0) ? std::min<int64_t>({static_cast<int64_t>(h->opt_split_k), kSkinnyMaxCluster, kb})
+                                        : skinny_cluster_size(h, kmode, false, tiles, kb);
+  const int64_t kb_per = ceil_div(kb, splits);
+  splits = ceil_div(kb, kb_per);
+  TcArgs a{};
+  a.mode = kmode;
+  a.fmt8 = mode == GEMM_MODE_MXFP8_E5M2 ? fp8_format_bits(1, 1) : 0u;
+  a.tile_n = 16;
+  a.M = N;
+  a.N = M;
+  a.K = kbytes;
+  a.A = B;
+  a.lda = ldb_b;
+  a.B = A;
+  a.ldb = lda_b;
+  a.C = C;
+  a.ldc = ldc;
+  a.alpha = alpha;
+  a.beta = beta;
+  a.splits = static_cast<int>(splits);
+  a.kb_per_split = static_cast<int>(kb_per);
+  a.tma_cache = h->tma_cache;
+  a.status = h->d_status;
+  a.grid = static_cast<int>(tiles * splits);
+  a.sfa = static_cast<const uint8_t*>(SB);
+  a.sfb = static_cast<const uint8_t*>(SA);
+  a.sf_groups = block_scale_groups(ceil_div(K, bs));
+  if (launch_skinny(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  set_plan(h, GEMM_FAMILY_SKINNY, 128, 16, static_cast<int>(nvfp4 ? 256 : 128), a.splits, skinny_stages(kmode), a.grid,
+           1, 0);
+  h->plan.cluster = a.splits;
+  h->plan.schedule = a.splits > 1 ? 1 : 0;
   return GEMM_OK;
 }
 
@@ -810,6 +913,56 @@ gemm_status_t gemm_get_plan(gemm_handle_t h, gemm_plan_t* out) {
   if (h == nullptr || out == nullptr) return GEMM_ERR_INVALID_VALUE;
   *out = h->plan;
   return GEMM_OK;
+}
+
+gemm_status_t gemm_run_block_scaled(gemm_handle_t h, int mode, int64_t M, int64_t N, int64_t K, float alpha,
+                                    const void* A, int64_t lda, const void* SA, const void* B, int64_t ldb,
+                                    const void* SB, float beta, float* C, int64_t ldc, void* stream) {
+  if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
+  if (mode != GEMM_MODE_MXFP8_E4M3 && mode != GEMM_MODE_MXFP8_E5M2 && mode != GEMM_MODE_NVFP4)
+    return GEMM_ERR_INVALID_VALUE;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr || ldc < std::max<int64_t>(N, 1)) return GEMM_ERR_INVALID_VALUE;
+  if (!aligned(C, 4)) return GEMM_ERR_MISALIGNED;
+  const bool nvfp4 = mode == GEMM_MODE_NVFP4;
+  if (K > 0 && alpha != 0.f) {
+    if (A == nullptr || B == nullptr || SA == nullptr || SB == nullptr) return GEMM_ERR_INVALID_VALUE;
+    if (lda < K || ldb < K) return GEMM_ERR_INVALID_VALUE;
+    if (nvfp4 && (K % 2 != 0 || lda % 2 != 0 || ldb % 2 != 0)) return GEMM_ERR_INVALID_VALUE;
+    if (M > 16) return GEMM_ERR_NOT_SUPPORTED;
+    // the TMA unit and the bulk copies read everything in place
+    const int64_t lda_b = nvfp4 ? lda / 2 : lda, ldb_b = nvfp4 ? ldb / 2 : ldb;
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(SA, 16) || !aligned(SB, 16) || lda_b % 16 != 0 ||
+        ldb_b % 16 != 0)
+      return GEMM_ERR_MISALIGNED;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dgt::last_main_launch().valid = false;
+  gemm_status_t st;
+  if (K == 0 || alpha == 0.f) {
+    st = dgt::launch_scale(M, N, C, ldc, beta, dgt::EpiParams{}, s) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    if (st == GEMM_OK) set_plan(h, 0, 0, 0, 0, 1, 0, 0, 1, 0);
+  } else {
+    st = run_block_scaled(h, mode, M, N, K, alpha, A, lda, SA, B, ldb, SB, beta, C, ldc, s);
+  }
+  if (st == GEMM_OK) h->null_shape = dgt::last_main_launch();
+  return st;
+}
+
+int64_t gemm_block_scales_tiled_bytes(int64_t rows, int64_t blocks) {
+  if (rows < 0 || blocks < 0 || rows > kMaxDim || blocks > kMaxDim) return -1;
+  return ceil_div(rows, 128) * dgt::block_scale_groups(blocks) * 512;
+}
+
+gemm_status_t gemm_block_scales_tile(int64_t rows, int64_t blocks, const void* S, int64_t lds, void* T,
+                                     void* stream) {
+  if (rows < 0 || blocks < 0 || rows > kMaxDim || blocks > kMaxDim) return GEMM_ERR_INVALID_VALUE;
+  if (rows == 0 || blocks == 0) return GEMM_OK;
+  if (S == nullptr || T == nullptr || lds < blocks) return GEMM_ERR_INVALID_VALUE;
+  if (!aligned(T, 16)) return GEMM_ERR_MISALIGNED;
+  return cuda_status(dgt::launch_block_scales_tile(static_cast<const uint8_t*>(S), rows, blocks, lds,
+                                                   static_cast<uint8_t*>(T), static_cast<cudaStream_t>(stream)));
 }
 
 gemm_status_t gemm_check_device(gemm_handle_t h, void* stream) {

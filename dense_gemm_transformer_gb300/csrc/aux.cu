@@ -233,6 +233,33 @@ __global__ void null_kernel() {
   grid_dep_launch();
 }
 
+// One thread per (atom, row within a quarter): the atom's 16 bytes for rows
+// m0, m0 + 32, m0 + 64 and m0 + 96 of its tile, four blocks each.
+__global__ void block_scales_tile_kernel(const uint8_t* __restrict__ S, int64_t rows, int64_t blocks, int64_t lds,
+                                         uint8_t* __restrict__ T, int64_t groups, int64_t items) {
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < items;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t atom = i / 32, m0 = i % 32;
+    const int64_t rt = atom / groups, g = atom % groups;
+    uint32_t w[4];
+#pragma unroll
+    for (int m1 = 0; m1 < 4; ++m1) {
+      const int64_t r = rt * 128 + m1 * 32 + m0;
+      uint32_t v = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t b = g * 4 + j;
+        const uint32_t x = (r < rows && b < blocks) ? S[r * lds + b] : 0u;
+        v |= x << (8 * j);
+      }
+      w[m1] = v;
+    }
+    *reinterpret_cast<uint4*>(T + atom * 512 + m0 * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 }  // namespace
 
 LaunchShape& last_main_launch() {
@@ -340,4 +367,15 @@ cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_d
                     static_cast<float*>(dst), ld_dst, rows, cols);
 }
 
+}  // namespace dgt
+
+namespace dgt {
+cudaError_t launch_block_scales_tile(const uint8_t* S, int64_t rows, int64_t blocks, int64_t lds, uint8_t* T,
+                                     cudaStream_t stream) {
+  const int64_t groups = block_scale_groups(blocks);
+  const int64_t items = (rows + 127) / 128 * groups * 32;
+  if (items == 0) return cudaSuccess;
+  return launch_pdl(block_scales_tile_kernel, dim3(grid_for(items, 256)), dim3(256), 0, stream, S, rows, blocks, lds, T,
+                    groups, items);
+}
 }  // namespace dgt

@@ -10,24 +10,70 @@
 // "bare-metal-bard" (second paragraph) trains a GPT with hand-written
 // matmul, layernorm and GELU kernels; the page does not say which GELU.  The
 // reading taken here is the function's definition, GELU(x) = x * Phi(x) with
-// Phi(x) = (1 + erf(x / sqrt 2)) / 2, and GELU'(x) = Phi(x) + x * phi(x),
-// phi(x) = exp(-x^2 / 2) / sqrt(2 pi); erff and expf are CUDA's.
+// Phi the standard normal distribution function, and GELU'(x) = Phi(x) +
+// x * phi(x), phi(x) = exp(-x^2 / 2) / sqrt(2 pi).
+//
+// Phi comes from the complementary error function, Phi(x) = erfc(-x / sqrt 2)
+// / 2, evaluated by the rational approximation of Abramowitz and Stegun,
+// Handbook of Mathematical Functions, formula 7.1.26 (C. Hastings' fit):
+// for z >= 0, erfc(z) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) e^(-z^2) +
+// eps, t = 1 / (1 + p z), |eps| <= 1.5e-7.  Taking z = |x| / sqrt 2 and
+// Phi(x) = 1 - erfc(z) / 2 for x >= 0, erfc(z) / 2 for x < 0 avoids the
+// cancellation of 1 + erf(x) in the negative tail, and e^(-z^2) =
+// e^(-x^2 / 2) is phi's exponential too, so GELU' costs no second one.
+// The reciprocal and the power of two are the hardware's approximate
+// instructions (rcp.approx, ex2.approx: a few units of 2^-23 relative), so
+// |Phi - Phi_exact| stays near 1e-7.
 #pragma once
 
 #include "kernels.h"
 
 namespace dgt {
 
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float exp2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Phi(x) and e^(-x^2 / 2) together (7.1.26 above).  The constants are
+// folded: t = 1 / (1 + (p / sqrt 2) |x|), the coefficients carry the 1/2 of
+// erfc / 2, and the exponent's scale log2(e) / 2 is one multiply.
+__device__ __forceinline__ void normal_cdf_exp(float x, float& Phi, float& e) {
+  constexpr float kPs = 0.23164188f;  // 0.3275911 / sqrt(2)
+  constexpr float kH1 = 0.127414796f, kH2 = -0.142248368f, kH3 = 0.7107068705f, kH4 = -0.7265760135f,
+                  kH5 = 0.5307027145f;  // a1 .. a5 of 7.1.26, halved
+  constexpr float kNegHalfLog2e = -0.72134752044448170f;  // -log2(e) / 2
+  const float t = rcp_approx(fmaf(kPs, fabsf(x), 1.f));
+  const float half_poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, kH5, kH4), kH3), kH2), kH1);
+  e = exp2_approx((x * x) * kNegHalfLog2e);  // e^(-x^2 / 2) = e^(-z^2), z = |x| / sqrt 2
+  const float half_erfc = half_poly * e;
+  Phi = x >= 0.f ? 1.f - half_erfc : half_erfc;
+}
+
+__device__ __forceinline__ void normal_cdf_pdf(float x, float& Phi, float& phi) {
+  constexpr float kInvSqrt2Pi = 0.39894228040143268f;
+  float e;
+  normal_cdf_exp(x, Phi, e);
+  phi = kInvSqrt2Pi * e;
+}
+
 __device__ __forceinline__ float gelu_f(float x) {
-  constexpr float kInvSqrt2 = 0.70710678118654752f;
-  return 0.5f * x * (1.f + erff(x * kInvSqrt2));
+  float Phi, e;
+  normal_cdf_exp(x, Phi, e);
+  return x * Phi;
 }
 
 __device__ __forceinline__ float dgelu_f(float x) {
-  constexpr float kInvSqrt2 = 0.70710678118654752f;
-  constexpr float kInvSqrt2Pi = 0.39894228040143268f;
-  const float Phi = 0.5f * (1.f + erff(x * kInvSqrt2));
-  return fmaf(x, kInvSqrt2Pi * expf(-0.5f * x * x), Phi);
+  float Phi, phi;
+  normal_cdf_pdf(x, Phi, phi);
+  return fmaf(x, phi, Phi);
 }
 
 // The epilogue's input for element (row, col) of the caller's C: Z there
@@ -57,6 +103,16 @@ __device__ __forceinline__ float epilogue_finish(const EpiParams& e, float v, fl
   if (e.act == kActDGelu) return v * dgelu_f(x);
   v += x;
   return e.act == kActGelu ? gelu_f(v) : v;
+}
+
+// epilogue_finish with the activation fixed at compile time (ACT: kActNone,
+// kActGelu, kActDGelu), for loops that dispatch on it once.
+template <int ACT>
+__device__ __forceinline__ float epilogue_finish_t(float v, float x) {
+  if constexpr (ACT == kActDGelu) return v * dgelu_f(x);
+  v += x;
+  if constexpr (ACT == kActGelu) return gelu_f(v);
+  return v;
 }
 
 // Both steps for one element.

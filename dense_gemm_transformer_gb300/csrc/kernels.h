@@ -152,9 +152,14 @@ struct TcArgs {
   int grid;              // persistent CTAs
   int group_m;           // raster group height in M tiles
   TmaCache* tma_cache;   // the handle's descriptor cache (null: encode every call)
+  EpiParams epi;         // with fuse_epi: the elementwise epilogue, applied to whole tiles in the kernel
+  bool fuse_epi;         // run the kernel built with the fused epilogue (tc_epi_ok)
   uint64_t wait_ns;      // limit of every bounded wait (0: the default, kWaitLimitNs)
   int fault_skip;        // test hook: n > 0 makes CTA 0's producer issue no copies for its n-th stage
                          // (one CTA per tile only); 0: none
+  const uint8_t* sfa;    // block-scaled small-M modes (4, 5): the kernel's A (weights) scales, tiled
+  const uint8_t* sfb;    // ... and its B (activations) scales, tiled
+  int64_t sf_groups;     // 512-byte scale atoms per 128-row tile
 };
 // tile_n == 16 selects the swapped small-M form: the caller passes the
 // operands exchanged (C^T = op(B)^T op(A)^T, M and N exchanged) and the
@@ -165,6 +170,10 @@ constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);  // producer + MMA warps + ep
 // descriptor: 0 = E4M3, 1 = E5M2.
 constexpr uint32_t fp8_format_bits(uint32_t a_fmt, uint32_t b_fmt) { return (a_fmt << 7) | (b_fmt << 10); }
 int tc_tile_k(int mode);              // k elements per stage (128 bytes)
+// Whether the kernel is built with the fused epilogue for these operand
+// layouts (as the kernel reads them, after any transpose): TF32 or BF16
+// with a K-major A, and a K-major B in TF32; tiles of 128-256 columns.
+bool tc_epi_ok(int mode, bool a_mn_major, bool b_mn_major);
 int tc_stages(int mode, int tile_n, bool pair);  // pipeline depth (pair: one 256-row MMA per CTA pair)
 // Whether the kernel is built for this tile width, pairing and B layout
 // (tile_n 128, 192, 224 or 256; pairs from 192 columns).
@@ -190,6 +199,15 @@ cudaError_t launch_scale(int64_t M, int64_t N, float* C, int64_t ldc, float beta
 // C = epi(C) in place over an M x N matrix: the epilogue of a call whose
 // GEMM kernels have stored alpha * product + beta * C.
 cudaError_t launch_epilogue(int64_t M, int64_t N, float* C, int64_t ldc, const EpiParams& epi, cudaStream_t stream);
+// Block scale factors (one byte per (row, block), row-major with leading
+// dimension lds bytes) into the tiled layout the block-scaled kernels read:
+// for each 128-row tile, groups of 4 blocks as 512-byte atoms, row r of the
+// tile and block j of the group at byte 16 * (r % 32) + 4 * (r / 32) + j;
+// groups_per_tile = 4 * ceil(blocks / 16); bytes past the matrix are zero.
+cudaError_t launch_block_scales_tile(const uint8_t* S, int64_t rows, int64_t blocks, int64_t lds, uint8_t* T,
+                                     cudaStream_t stream);
+inline int64_t block_scale_groups(int64_t blocks) { return 4 * ((blocks + 15) / 16); }
+
 // Copy a rows x cols matrix of elem_bytes-sized elements to dst with a new
 // leading dimension (elements).
 cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,

@@ -440,7 +440,75 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------------------------------ block-scaled MMA
+// D(tmem) (+)= (A * scale_A) (B * scale_B): kind::mxf8f6f4 with one E8M0
+// scale per 32 K elements (scale_vec::1X; 8-bit elements, K = 32 per MMA),
+// and kind::mxf4nvf4 with one UE4M3 scale per 16 K elements (scale_vec::4X;
+// E2M1 elements packed two per byte, K = 64 per MMA).  The scale factors
+// sit in TMEM: row m of A reads its scale at lane m, column
+// (sfa + m / 32); column n of B at lane n % 32, column (sfb + n / 32).
+// With 1X the instruction descriptor's scale-factor ID picks the byte of
+// that 32-bit cell; with 4X its four bytes are the MMA's four K blocks.
+__device__ __forceinline__ void mma_mxf8f6f4_bs(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf4nvf4_bs(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy a 32-row x 16-byte matrix from shared memory (described by `sdesc`)
+// into TMEM columns taddr .. taddr + 3 of all four 32-lane quarters (row r
+// to lane r of each quarter).  Ordered before later tcgen05.mma of this
+// thread; completion is tracked by tcgen05.commit like an MMA's.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Instruction descriptor of the block-scaled kinds (D is fp32 implicitly):
+//   bits 4-5 B scale-factor ID; 7-9 / 10-12 A / B format (kind::mxf8f6f4:
+//   E4M3 = 0, E5M2 = 1; kind::mxf4nvf4: E2M1 = 1); 17-22 N >> 3; 23 scale
+//   format (1 = E8M0, 0 = UE4M3); 24-28 M >> 4; 29-30 A scale-factor ID.
+__host__ __device__ constexpr uint32_t make_idesc_bs(uint32_t a_fmt, uint32_t b_fmt, bool e8m0, uint32_t m, uint32_t n,
+                                                     uint32_t sfid_a, uint32_t sfid_b) {
+  return (sfid_b << 4) | (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | ((e8m0 ? 1u : 0u) << 23) |
+         ((m >> 4) << 24) | (sfid_a << 29);
+}
+
+// Untiled bulk copy global -> this CTA's shared memory (16-byte aligned
+// addresses, a multiple of 16 bytes), counted as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ descriptors
+// Shared-memory descriptor without swizzle for a K-major matrix whose 8-row
+// groups of 16-byte rows (128 contiguous bytes each) are `sbo` bytes apart:
+// a 32 x 16-byte matrix stored row after row has sbo = 128.
+__device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  return d;
+}
+
 // Shared-memory matrix descriptor for tcgen05 with the 128-byte swizzle.
 //   bits  0-13  start address >> 4
 //   bits 16-29  leading-dimension byte offset >> 4

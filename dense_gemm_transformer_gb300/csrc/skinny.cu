@@ -43,24 +43,39 @@ namespace {
 
 // MODE: 1 TF32 (fp32 operands), 2 BF16, 3 8-bit floats (E4M3 / E5M2 codes,
 // the formats named at run time in SkParams::fmt8).
+// MODE 4 / 5: block-scaled 8-bit (MXFP8: E4M3 / E5M2 with an E8M0 scale per
+// 32 K) and 4-bit (NVFP4: E2M1 packed two per byte with a UE4M3 scale per 16
+// K) codes; their TMA maps and K coordinates are in bytes.  Each stage then
+// also carries both operands' scale factors for its 128 bytes of K, as
+// 512-byte atoms (128 rows x 4 scale blocks) in the layout tcgen05.cp
+// replicates into the TMEM cells the block-scaled MMA reads.
 template <int MODE>
 struct SkCfg {
-  static constexpr int ES = (MODE == 3) ? 1 : (MODE == 2) ? 2 : 4;  // operand bytes
+  static constexpr bool BS = MODE >= 4;  // block-scaled
+  static constexpr int ES = (MODE >= 3) ? 1 : (MODE == 2) ? 2 : 4;  // operand bytes (coordinate units)
   static constexpr int BM = 128;                   // weight rows per tile (UMMA M)
   static constexpr int BN = 16;                    // activation rows (UMMA N)
-  static constexpr int BK = 128 / ES;              // K elements per stage (one 128-byte swizzle row)
-  static constexpr int UK = 32 / ES;                // K of one MMA (32 bytes)
+  static constexpr int BK = 128 / ES;              // K units per stage (one 128-byte swizzle row)
+  static constexpr int UK = 32 / ES;                // K units of one MMA (32 bytes)
   static constexpr int CH = 128 / ES;              // weight rows in one 128-byte MN-major row
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BN * 128;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = kSkinnyStages;
-  static constexpr int TMEM_COLS = 32;                // one 16-column accumulator (allocation >= 32)
+  static constexpr int SF_ATOMS = (MODE == 5) ? 4 : (MODE == 4) ? 1 : 0;  // scale atoms per operand per stage
+  static constexpr int SF_BYTES = SF_ATOMS * 512;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;
+  static constexpr int STAGES = skinny_stages(MODE);
+  // TMEM: the 16-column accumulator, then (block-scaled) one ring slot of
+  // scale columns per stage: 4 columns per atom, A's atoms then B's.
+  static constexpr int SF_COL0 = 32;
+  static constexpr int SF_COLS = 2 * SF_ATOMS * 4;
+  static constexpr int TMEM_NEED = BS ? SF_COL0 + STAGES * SF_COLS : 16;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128 : 256;
   static constexpr int NUM_BARS = 2 * STAGES + 3;     // full/empty per stage, accumulator full, drain, receive
   static constexpr int RECV_BYTES = (BN * BM / 4 + kSkinnyMaxCluster) * 16;  // shares pushed by the peers
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + RECV_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static constexpr int PREFETCH_KB = 16;              // K blocks of weights warmed in L2 before the wait
   static constexpr uint32_t FORMAT = (MODE == 3) ? 0u : (MODE == 2) ? 1u : 2u;  // 8-bit (fmt8) / bf16 / tf32
+  static_assert(!BS || TMEM_NEED <= 256, "block-scaled: two CTAs per SM");
   static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM (228 KB, 1 KB reserved per CTA)");
   static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
   static_assert(BM * BN * 4 <= STAGES * STAGE_BYTES, "the partial tile fits in the drained stages");
@@ -69,6 +84,7 @@ struct SkCfg {
 
 template <int MODE>
 __device__ __forceinline__ void sk_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  static_assert(MODE <= 3, "block-scaled kinds take scale factors (sk_mma_bs)");
   if (MODE == 3)
     mma_f8f6f4(d, a, b, idesc, acc);
   else if (MODE == 2)
@@ -83,8 +99,10 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
                        const SkParams p) {
   using Cfg = SkCfg<MODE>;
   constexpr int S = Cfg::STAGES;
-  // MODE 3 names its operand formats at run time (the FORMAT fields are 0).
+  // MODE 3 names its operand formats at run time (the FORMAT fields are 0);
+  // the block-scaled modes build theirs per MMA.
   const uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN, false, Cfg::BM, Cfg::BN) | (MODE == 3 ? p.fmt8 : 0u);
+  static_assert(!Cfg::BS || !A_MN, "block-scaled operands are K-major");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -173,6 +191,14 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
           tma_load_2d(a_dst, &tmA, fb, k0, row0);
         }
         tma_load_2d(a_dst + Cfg::A_BYTES, &tmB, fb, k0, 0);
+        if constexpr (Cfg::BS) {
+          // both operands' scale atoms for this stage's 128 bytes of K
+          const uint32_t sf_dst = a_dst + Cfg::A_BYTES + Cfg::B_BYTES;
+          bulk_copy_g2s(sf_dst, p.sfa + (static_cast<int64_t>(tile) * p.sf_groups + kb * Cfg::SF_ATOMS) * 512,
+                        Cfg::SF_BYTES, fb);
+          bulk_copy_g2s(sf_dst + Cfg::SF_BYTES, p.sfb + static_cast<int64_t>(kb) * Cfg::SF_ATOMS * 512, Cfg::SF_BYTES,
+                        fb);
+        }
         ++issued;
         if (++stage == S) {
           stage = 0;
@@ -198,12 +224,39 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
         tc_fence_after();
         const uint32_t a_base = smem0 + stage * Cfg::STAGE_BYTES;
         const uint32_t b_base = a_base + Cfg::A_BYTES;
+        if constexpr (Cfg::BS) {
+          // This stage's scale atoms into its TMEM ring slot (the slot's
+          // previous MMAs are complete: this stage's copies could only be
+          // issued after they released it), then four block-scaled MMAs of
+          // 32 bytes of K each: MXFP8 picks its byte of the 32-bit scale
+          // cells by scale-factor ID j; NVFP4 takes atom j's four bytes.
+          const uint32_t sf_col = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + stage * Cfg::SF_COLS);
+          const uint32_t sf_smem = b_base + Cfg::B_BYTES;
 #pragma unroll
-        for (int j = 0; j < Cfg::BK / Cfg::UK; ++j) {
-          const uint64_t ad = A_MN ? smem_desc_sw128(a_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
-                                   : smem_desc_sw128(a_base + j * Cfg::UK * Cfg::ES, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(b_base + j * Cfg::UK * Cfg::ES, 16, 1024);
-          sk_mma<MODE>(tmem_base, ad, bd, IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
+          for (int a = 0; a < 2 * Cfg::SF_ATOMS; ++a)
+            tmem_cp_32x128b_x4(sf_col + 4 * a, smem_desc_noswizzle(sf_smem + 512 * a, 128));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t ad = smem_desc_sw128(a_base + j * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b_base + j * 32, 16, 1024);
+            const uint32_t acc = (kb > kb0 || j > 0) ? 1u : 0u;
+            if constexpr (MODE == 4)
+              mma_mxf8f6f4_bs(tmem_base, ad, bd,
+                              make_idesc_bs(0, 0, true, Cfg::BM, Cfg::BN, static_cast<uint32_t>(j),
+                                            static_cast<uint32_t>(j)) | p.fmt8,
+                              sf_col, sf_col + 4, acc);
+            else
+              mma_mxf4nvf4_bs(tmem_base, ad, bd, make_idesc_bs(1, 1, false, Cfg::BM, Cfg::BN, 0, 0),
+                              sf_col + 4 * j, sf_col + 4 * (Cfg::SF_ATOMS + j), acc);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < Cfg::BK / Cfg::UK; ++j) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(a_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
+                                     : smem_desc_sw128(a_base + j * Cfg::UK * Cfg::ES, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b_base + j * Cfg::UK * Cfg::ES, 16, 1024);
+            sk_mma<MODE>(tmem_base, ad, bd, IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
+          }
         }
         mma_commit(empty_bar(stage));
         if (++stage == S) {
@@ -385,7 +438,9 @@ cudaError_t skinny_launch(int mode, bool a_mn, const CUtensorMap& ta, const CUte
   if (mode == 2) return a_mn ? launch_one<2, true>(ta, tb, p, grid, s) : launch_one<2, false>(ta, tb, p, grid, s);
   if (mode == 1 && !a_mn) return launch_one<1, false>(ta, tb, p, grid, s);
   if (mode == 3 && !a_mn) return launch_one<3, false>(ta, tb, p, grid, s);
-  return cudaErrorInvalidValue;  // kind::tf32 and the FP8 form take K-major operands only
+  if (mode == 4 && !a_mn) return launch_one<4, false>(ta, tb, p, grid, s);
+  if (mode == 5 && !a_mn) return launch_one<5, false>(ta, tb, p, grid, s);
+  return cudaErrorInvalidValue;  // kind::tf32 and the 8- and 4-bit forms take K-major operands only
 }
 
 int skinny_max_active_clusters(int mode, bool a_mn, int cluster) {
@@ -393,6 +448,8 @@ int skinny_max_active_clusters(int mode, bool a_mn, int cluster) {
   if (mode == 2) return a_mn ? active_clusters<2, true>(cluster) : active_clusters<2, false>(cluster);
   if (mode == 1 && !a_mn) return active_clusters<1, false>(cluster);
   if (mode == 3 && !a_mn) return active_clusters<3, false>(cluster);
+  if (mode == 4 && !a_mn) return active_clusters<4, false>(cluster);
+  if (mode == 5 && !a_mn) return active_clusters<5, false>(cluster);
   return 0;
 }
 

@@ -25,8 +25,8 @@ cudaError_t g_encode_status = cudaSuccess;
 
 cudaError_t encode_2d(CUtensorMap* m, int mode, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
                       uint32_t box_inner, uint32_t box_outer) {
-  const int es = (mode == 3) ? 1 : (mode == 2) ? 2 : 4;
-  const CUtensorMapDataType dt = (mode == 3)   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+  const int es = (mode >= 3) ? 1 : (mode == 2) ? 2 : 4;
+  const CUtensorMapDataType dt = (mode >= 3)   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : (mode == 2) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
@@ -112,7 +112,12 @@ cudaError_t tc_init_driver() {
   return g_encode_status;
 }
 
-int tc_tile_k(int mode) { return mode == 3 ? 128 : mode == 2 ? 64 : 32; }
+int tc_tile_k(int mode) { return mode >= 3 ? 128 : mode == 2 ? 64 : 32; }
+
+bool tc_epi_ok(int mode, bool a_mn_major, bool b_mn_major) {
+  if (a_mn_major) return false;
+  return mode == 2 || (mode == 1 && !b_mn_major);
+}
 
 int tc_stages(int mode, int tile_n, bool pair) {
   (void)mode;  // a stage holds 128 bytes of K per row in every mode
@@ -178,6 +183,7 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.status = a.status;
   p.fmt8 = a.mode == 3 ? a.fmt8 : 0u;
   p.wait_ns = a.wait_ns > 0 ? a.wait_ns : kWaitLimitNs;
+  p.epi = a.fuse_epi ? a.epi : EpiParams{};
   p.fault_skip = (a.fault_skip > 0 && !pair) ? a.fault_skip - 1 : -1;
   p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && a.ldc % 4 == 0) ? 1 : 0;
   // Tiles leave through TMA stores when the destination allows it: not the
@@ -199,6 +205,14 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
     if (whole && a.beta == 0.f && p.c_vec)
       p.c_tma = (encode_out_c(a.tma_cache, &tcm, a.C, a.N, a.M, 1, a.ldc, a.M * a.ldc) == cudaSuccess) ? 1 : 0;
   }
+  if (a.fuse_epi) {
+    if (a.tile_n < 128 || !tc_epi_ok(a.mode, a.a_mn_major != 0, a.b_mn_major != 0)) return cudaErrorNotSupported;
+    if (a.mode == 1)
+      return tc_launch_tf32_epi(a.tile_n, pair, false, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid, stream);
+    if (a.tile_n == 192 || a.tile_n == 224)
+      return tc_launch_bf16_epi_mid(a.tile_n, pair, false, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid, stream);
+    return tc_launch_bf16_epi(a.tile_n, pair, false, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid, stream);
+  }
   if (a.mode == 3 && (a.tile_n == 192 || a.tile_n == 224))
     return tc_launch_fp8_mid(a.tile_n, pair, a.a_mn_major != 0, a.b_mn_major != 0, ta, tb, tcm, twm, p, a.grid,
                              stream);
@@ -216,7 +230,7 @@ cudaError_t launch_skinny(const TcArgs& a, cudaStream_t stream) {
   cudaError_t e = tc_init_driver();
   if (e != cudaSuccess) return e;
   const int bk = tc_tile_k(a.mode);
-  const int ch = 128 / ((a.mode == 3) ? 1 : (a.mode == 2) ? 2 : 4);
+  const int ch = 128 / ((a.mode >= 3) ? 1 : (a.mode == 2) ? 2 : 4);
   CUtensorMap ta, tb;
   e = a.a_mn_major ? encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
                    : encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
@@ -235,7 +249,10 @@ cudaError_t launch_skinny(const TcArgs& a, cudaStream_t stream) {
   p.C = a.C;
   p.ldc = a.ldc;
   p.status = a.status;
-  p.fmt8 = a.mode == 3 ? a.fmt8 : 0u;
+  p.fmt8 = (a.mode == 3 || a.mode == 4) ? a.fmt8 : 0u;
+  p.sfa = a.sfa;
+  p.sfb = a.sfb;
+  p.sf_groups = a.sf_groups;
   return skinny_launch(a.mode, a.a_mn_major != 0, ta, tb, p, a.grid, stream);
 }
 

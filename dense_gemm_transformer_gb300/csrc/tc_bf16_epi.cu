@@ -1,0 +1,11 @@
+// tc_bf16_epi.cu -- the tcgen05 kernel for BF16 operands with the fused
+// epilogue (bias, GELU, GELU'), 128- and 256-column tiles, K-major A.
+#include "tc_launch.cuh"
+
+namespace dgt {
+cudaError_t tc_launch_bf16_epi(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
+                               const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
+                               const TcParams& p, int grid, cudaStream_t s) {
+  return tc_launch_mode<2, true>(tile_n, pair, a_mn, b_mn, ta, tb, tc, tw, p, grid, s);
+}
+}  // namespace dgt

@@ -45,7 +45,9 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -74,6 +76,7 @@ struct TcParams {
   int c_tma;  // whole tiles leave through shared memory and TMA stores (tmC is valid)
   int w_tma;  // partial tiles likewise (tmW is valid)
   uint32_t fmt8;  // MODE 3: operand format bits of the instruction descriptor (E4M3 / E5M2)
+  EpiParams epi;     // EPI kernels: bias / GELU / GELU' applied at every final store of a whole tile
   uint64_t wait_ns;  // limit of every bounded wait
   int fault_skip;    // test hook: CTA 0's producer issues no copies for its fault_skip-th stage
                      // (0-based; -1: none), so the MMA's wait for that stage runs out
@@ -150,6 +153,50 @@ struct Unit {
   bool partial;
 };
 
+// EPI: the epilogue's inputs for columns col0 .. col0 + 4 * NQ - 1 of one
+// row of C (the bias, or Z's row), all requested before any is used so
+// that they cost one memory latency; `fetch` is false for a row past M,
+// whose values are never stored.
+template <int NQ>
+__device__ __forceinline__ void epi_fetch(const EpiParams& e, int64_t row, int64_t col0, int64_t n, bool fetch,
+                                          float4 (&x)[NQ]) {
+#pragma unroll
+  for (int q = 0; q < NQ; ++q)
+    x[q] = fetch ? epilogue_fetch4(e, row, col0 + 4 * q, n) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// The elementwise epilogue of four consecutive elements, after alpha /
+// beta, with the activation fixed at compile time (ACT < 0: none at all).
+template <int ACT>
+__device__ __forceinline__ float4 epi_finish4(float4 v, const float4& x) {
+  if constexpr (ACT >= 0) {
+    v.x = epilogue_finish_t<ACT>(v.x, x.x);
+    v.y = epilogue_finish_t<ACT>(v.y, x.y);
+    v.z = epilogue_finish_t<ACT>(v.z, x.z);
+    v.w = epilogue_finish_t<ACT>(v.w, x.w);
+  }
+  return v;
+}
+
+// Calls body(std::integral_constant<int, ACT>) with the epilogue's
+// activation as a compile-time value (-1 when there is none to apply), so
+// that loops over a chunk carry no per-element test of it.
+template <bool EPI, typename F>
+__device__ __forceinline__ void with_activation(bool on, int act, F&& body) {
+  if constexpr (EPI) {
+    if (on) {
+      if (act == kActGelu)
+        body(std::integral_constant<int, kActGelu>{});
+      else if (act == kActDGelu)
+        body(std::integral_constant<int, kActDGelu>{});
+      else
+        body(std::integral_constant<int, kActNone>{});
+      return;
+    }
+  }
+  body(std::integral_constant<int, -1>{});
+}
+
 // Tile t of a region of `rows` unit rows starting at row0, in the grouped
 // raster order: group_m rows walk all columns, so units that run at the
 // same time share A and B tiles in L2.
@@ -200,11 +247,16 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
 // CTA's barrier.  Each CTA then stages 32 KB per 256-column stage instead of
 // 48.  Every copy a CTA issues lands in its own shared memory: no operand
 // tile is multicast.
-template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C, bool PAIR>
+// EPI: whole tiles get the elementwise epilogue of p.epi (bias, GELU, GELU'
+// of a kept pre-activation) in the epilogue warps, between the TMEM load
+// and the store; partial tiles of a K split stay raw for the slice reduce,
+// which applies it.
+template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C, bool PAIR, bool EPI = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                    const TcParams p) {
+  static_assert(!EPI || !TRANS_C, "the swapped small-M form applies no epilogue itself");
   using Cfg = TcCfg<MODE, BN, PAIR>;
   constexpr int S = Cfg::STAGES;
   // TF32 with an MN-major A: kind::tf32 reads only K-major operands from
@@ -543,11 +595,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int cc_end = (!A_TMEM && half == 0) ? (NCH + 1) / 2 : NCH;
 #pragma unroll 1
       for (int cc = cc_begin; cc < cc_end; ++cc) {
-        uint32_t r[CW];
-        __syncwarp();
-        tmem_ld_32x32b<CW>(t_row + cc * CW, r);
-        tmem_wait_ld();
         const int64_t col0 = static_cast<int64_t>(w.tn) * BN + cc * CW;
+        // EPI: the bias or Z values of this chunk's first quarter, requested
+        // before the TMEM load so that both latencies overlap; each further
+        // quarter is requested as a group when the previous one is done
+        // (fetching more at once spilled registers).
+        constexpr int NQH = (CW / 4 + 3) / 4;
+        const bool epi_on = EPI && !partial;
+        const bool epi_fetch_ok = row_ok && col0 < p.N;
+        float4 xe[NQH];
+        if constexpr (EPI) {
+          if (epi_on) epi_fetch<NQH>(p.epi, row, col0, p.N, epi_fetch_ok, xe);
+        }
         if constexpr (Cfg::STAGING_BYTES > 0 && CW == 32) {
           if (partial ? p.w_tma : p.c_tma) {
             // Through shared memory: this warp's 32 rows x 32 columns go to
@@ -559,15 +618,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) bulk_wait_group_read<0>();  // the buffer's previous store has read it
             __syncwarp();
             const float a = partial ? 1.f : p.alpha;
+            // EPI kernels read the chunk from TMEM in two halves of 16
+            // columns (fewer live registers beside the epilogue's inputs).
+            constexpr int SW = EPI ? 16 : CW;
+            with_activation<EPI>(epi_on, p.epi.act, [&](auto act_c) {
+              constexpr int ACT = decltype(act_c)::value;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float4 v;
-              v.x = a * __uint_as_float(r[4 * q + 0]);
-              v.y = a * __uint_as_float(r[4 * q + 1]);
-              v.z = a * __uint_as_float(r[4 * q + 2]);
-              v.w = a * __uint_as_float(r[4 * q + 3]);
-              *reinterpret_cast<float4*>(buf + lane * 128 + ((q ^ (lane & 7)) * 16)) = v;
-            }
+              for (int hh = 0; hh < CW / SW; ++hh) {
+                uint32_t r[SW];
+                __syncwarp();
+                tmem_ld_32x32b<SW>(t_row + cc * CW + hh * SW, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int qq = 0; qq < SW / 4; ++qq) {
+                  const int q = hh * (SW / 4) + qq;
+                  if constexpr (ACT >= 0) {
+                    if (q > 0 && q % NQH == 0) epi_fetch<NQH>(p.epi, row, col0 + 4 * q, p.N, epi_fetch_ok, xe);
+                  }
+                  float4 v;
+                  v.x = a * __uint_as_float(r[4 * qq + 0]);
+                  v.y = a * __uint_as_float(r[4 * qq + 1]);
+                  v.z = a * __uint_as_float(r[4 * qq + 2]);
+                  v.w = a * __uint_as_float(r[4 * qq + 3]);
+                  v = epi_finish4<ACT>(v, xe[q % NQH]);
+                  *reinterpret_cast<float4*>(buf + lane * 128 + ((q ^ (lane & 7)) * 16)) = v;
+                }
+              }
+            });
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -578,33 +655,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             continue;
           }
         }
+        // the whole chunk from TMEM, by every lane (a warp-collective load)
+        uint32_t r[CW];
+        __syncwarp();
+        tmem_ld_32x32b<CW>(t_row + cc * CW, r);
+        tmem_wait_ld();
         if (!row_ok || col0 >= p.N) {
           // nothing of this chunk is inside C for this thread
         } else if (vec_ok && col0 + CW <= p.N) {
           float4* dst = reinterpret_cast<float4*>(out + col0);
           // All of the chunk's loads of C are issued before any store, so
-          // their latencies overlap.
-          float4 c[CW / 4];
-          if (read_c) {
+          // their latencies overlap (EPI kernels: one quad at a time, to
+          // leave registers for the epilogue's inputs).
+          constexpr int NC = EPI ? 1 : CW / 4;
+          float4 c[NC];
+          if (read_c && !EPI) {
 #pragma unroll
-            for (int q = 0; q < CW / 4; ++q) c[q] = dst[q];
+            for (int q = 0; q < NC; ++q) c[q] = dst[q];
           }
           const float a = partial ? 1.f : p.alpha;
+          with_activation<EPI>(epi_on, p.epi.act, [&](auto act_c) {
+            constexpr int ACT = decltype(act_c)::value;
 #pragma unroll
-          for (int q = 0; q < CW / 4; ++q) {
-            float4 v;
-            v.x = a * __uint_as_float(r[4 * q + 0]);
-            v.y = a * __uint_as_float(r[4 * q + 1]);
-            v.z = a * __uint_as_float(r[4 * q + 2]);
-            v.w = a * __uint_as_float(r[4 * q + 3]);
-            if (read_c) {
-              v.x = fmaf(p.beta, c[q].x, v.x);
-              v.y = fmaf(p.beta, c[q].y, v.y);
-              v.z = fmaf(p.beta, c[q].z, v.z);
-              v.w = fmaf(p.beta, c[q].w, v.w);
+            for (int q = 0; q < CW / 4; ++q) {
+              if constexpr (ACT >= 0) {
+                if (q > 0 && q % NQH == 0) epi_fetch<NQH>(p.epi, row, col0 + 4 * q, p.N, epi_fetch_ok, xe);
+              }
+              float4 v;
+              v.x = a * __uint_as_float(r[4 * q + 0]);
+              v.y = a * __uint_as_float(r[4 * q + 1]);
+              v.z = a * __uint_as_float(r[4 * q + 2]);
+              v.w = a * __uint_as_float(r[4 * q + 3]);
+              if (read_c) {
+                const float4 cq = EPI ? dst[q] : c[q % NC];
+                v.x = fmaf(p.beta, cq.x, v.x);
+                v.y = fmaf(p.beta, cq.y, v.y);
+                v.z = fmaf(p.beta, cq.z, v.z);
+                v.w = fmaf(p.beta, cq.w, v.w);
+              }
+              v = epi_finish4<ACT>(v, xe[q % NQH]);
+              dst[q] = v;
             }
-            dst[q] = v;
-          }
+          });
         } else {
           // TRANS_C: lanes hold consecutive rows, so each access of the warp is contiguous.
           auto at = [&](int j) { return TRANS_C ? out + (col0 + j) * ld + wrow : out + col0 + j; };
@@ -619,6 +711,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (col0 + j < p.N) {
               float v = a * __uint_as_float(r[j]);
               if (read_c) v = fmaf(p.beta, c[j], v);
+              if constexpr (EPI) {
+                if (!partial) v = apply_epilogue(p.epi, v, row, col0 + j);
+              }
               *at(j) = v;
             }
           }

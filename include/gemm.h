@@ -69,7 +69,13 @@ typedef enum {
                                   K-major operands read in place (every FP8 mode)   */
   GEMM_MODE_FP8_E5M2 = 4,      /* e5m2 A and B                                          */
   GEMM_MODE_FP8_E4M3_E5M2 = 5, /* e4m3 A, e5m2 B                                        */
-  GEMM_MODE_FP8_E5M2_E4M3 = 6  /* e5m2 A, e4m3 B                                        */
+  GEMM_MODE_FP8_E5M2_E4M3 = 6, /* e5m2 A, e4m3 B                                        */
+  /* Block-scaled modes, gemm_run_block_scaled only (gemm_run refuses them): */
+  GEMM_MODE_MXFP8_E4M3 = 7,    /* e4m3 A and B, one E8M0 scale per 32 K elements,
+                                  tcgen05 kind::mxf8f6f4 block_scale                   */
+  GEMM_MODE_MXFP8_E5M2 = 8,    /* e5m2 A and B, E8M0 scales per 32 K                   */
+  GEMM_MODE_NVFP4 = 9          /* e2m1 A and B packed two per byte, one UE4M3 scale per
+                                  16 K elements, tcgen05 kind::mxf4nvf4 block_scale    */
 } gemm_mode_t;
 
 typedef enum {
@@ -157,7 +163,8 @@ typedef struct {
                             3 whole tiles then K slices for the last rows of tiles (TC) */
   int32_t cluster;       /* TC: CTAs per cluster (2 = CTA pairs); small M: K slices per cluster */
   int32_t pair_mma;      /* TC: 1 when each CTA pair issues one 256-row MMA (tcgen05 cta_group::2) */
-  int32_t reserved[4];
+  int32_t epilogue_fused; /* gemm_run_epilogue: 1 when the GEMM kernel itself applied the epilogue */
+  int32_t reserved[3];
 } gemm_plan_t;
 
 /* Create a handle on the current device.  Reads the device properties and
@@ -189,10 +196,15 @@ gemm_status_t gemm_run(gemm_handle_t h, int mode, int transA, int transB,
                        float beta, float* C, int64_t ldc, void* stream);
 
 /* gemm_run with the elementwise epilogue `*ep` applied to every element of
- * the result (same GEMM kernels and plans; the activation is applied once,
- * after split-K or stream-K partial sums are added: inside the split-K
- * reduction when the call has one that writes all of C, otherwise in one
- * pass over C right after the GEMM, in the same stream).  The
+ * the result, once, after split-K or stream-K partial sums are added.  In
+ * TF32 and BF16 mode with A read K-major (transA == 0, or an A the plan
+ * transposes) the tensor-core kernel applies it itself between its
+ * accumulator load and its store (and the slice reduction for rows whose K
+ * is split); otherwise it is applied inside the split-K reduction when the
+ * call has one that writes all of C, or in one pass over C right after the
+ * GEMM, in the same stream.  GELU is computed as x * Phi(x) with Phi from
+ * the Abramowitz-Stegun 7.1.26 approximation of erfc (|error| <= 1.5e-7).
+ * The
  * bias and Z are read, never written; C must not overlap them.  ep == NULL
  * is gemm_run.  With K == 0 or alpha == 0 the product is zero and the
  * epilogue still applies to beta*C.  Errors: GEMM_ERR_INVALID_VALUE for an
@@ -304,6 +316,50 @@ gemm_status_t gemm_run_small_m_noalloc(int mode, int transB, int64_t M, int64_t 
  * GEMM_OK otherwise.  Allocates nothing.  The next gemm_run_small_m_noalloc
  * call on the device clears the word, so check before it. */
 gemm_status_t gemm_noalloc_check_device(void* stream);
+
+/* Block-scaled low-precision product: C = alpha * (A . SA) * (B . SB)^T +
+ * beta * C, where every run of `bs` consecutive K elements of a row shares
+ * one scale.  The "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls,
+ * Measured" summary (vidyal.ai) names the MX and NVFP4 formats; their
+ * definitions are the OCP Microscaling specification's and NVIDIA's NVFP4:
+ *   GEMM_MODE_MXFP8_E4M3 / _E5M2: 8-bit E4M3 / E5M2 codes, bs = 32, E8M0
+ *     scales (2^(e - 127); 0xFF is NaN);
+ *   GEMM_MODE_NVFP4: E2M1 codes packed two per byte (the even element of a
+ *     pair in the low nibble), bs = 16, UE4M3 scales (the E4M3 magnitude;
+ *     the sign bit is ignored).  A per-tensor factor goes into alpha.
+ * A is stored M x K and B N x K (K contiguous in both, the weights of a
+ * linear layer as usually kept), lda / ldb in elements (NVFP4: K, lda and
+ * ldb even; a row is lda / 2 bytes); C is M x N fp32, ldc >= N.  SA and SB
+ * are the scales of A (M x ceil(K / bs)) and B (N x ceil(K / bs)) in the
+ * tiled layout gemm_block_scales_tile writes.  A partial last block is
+ * allowed.  Served for the decode shape, M <= 16, by the small-M kernel (K
+ * split across a thread-block cluster; the scale atoms of every pipeline
+ * stage are copied into tensor memory with tcgen05.cp).
+ * Errors: GEMM_ERR_INVALID_VALUE for another mode, negative sizes, a null
+ * pointer, lda or ldb < K, an odd K / lda / ldb in NVFP4; GEMM_ERR_NOT_SUPPORTED
+ * for M > 16; GEMM_ERR_MISALIGNED when A, B, SA or SB is not 16-byte aligned
+ * or a row of A or B is not a multiple of 16 bytes.  M == 0 or N == 0 is a
+ * no-op; K == 0 or alpha == 0 gives C = beta * C.  Asynchronous on `stream`. */
+gemm_status_t gemm_run_block_scaled(gemm_handle_t h, int mode, int64_t M, int64_t N, int64_t K, float alpha,
+                                    const void* A, int64_t lda, const void* SA, const void* B, int64_t ldb,
+                                    const void* SB, float beta, float* C, int64_t ldc, void* stream);
+
+/* Bytes of the tiled scale layout for a rows x blocks scale matrix:
+ * ceil(rows / 128) * 4 * ceil(blocks / 16) * 512; -1 for negative sizes.
+ * Host only (no device needed). */
+int64_t gemm_block_scales_tiled_bytes(int64_t rows, int64_t blocks);
+
+/* Rewrite block scales S (rows x blocks bytes, row-major, leading dimension
+ * lds >= blocks) into T (gemm_block_scales_tiled_bytes bytes, 16-byte
+ * aligned, device memory) in the layout the tensor cores read them in: for
+ * each tile of 128 rows, groups of four blocks as 512-byte atoms, row r of
+ * the tile and block j of the group at byte 16 * (r % 32) + 4 * (r / 32) +
+ * j, atoms ordered by group, tiles one after another, 4 * ceil(blocks / 16)
+ * atoms per tile; every byte past the matrix is 0.  No counterpart on the
+ * source pages (a layout of this library's kernels).  Asynchronous on
+ * `stream`. */
+gemm_status_t gemm_block_scales_tile(int64_t rows, int64_t blocks, const void* S, int64_t lds, void* T,
+                                     void* stream);
 
 /* A static string naming a status code. */
 const char* gemm_status_string(gemm_status_t s);

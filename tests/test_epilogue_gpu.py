@@ -1,9 +1,13 @@
 """The epilogue (gemm_run_epilogue) against the oracle: a per-column bias,
 GELU after it, and the product with GELU'(Z) of a kept pre-activation, in
-every kernel family and schedule -- applied in the split-K reduction where a
-call ends with one that writes all of C, in the pass over C after the GEMM
-otherwise (whole tiles, stream-K, tail slices, the small-M kernel), and in
-the beta-only path for K = 0."""
+every kernel family and schedule -- fused into the tensor-core kernel's
+epilogue warps where A is read K-major (whole tiles, TMA-staged and direct
+stores, pairs, tail slices with their reduction), applied in the split-K
+reduction where a call ends with one that writes all of C, in the pass over
+C after the GEMM otherwise (SIMT tiles and stream-K, A through TMEM, the
+small-M kernels), and in the beta-only path for K = 0.  GELU itself (an
+Abramowitz-Stegun erfc) is swept densely against the oracle and against
+CUDA's erf."""
 import numpy as np
 import pytest
 import torch
@@ -48,25 +52,28 @@ def _check(mode, got, Y, D, act, bias, Z, alpha, beta, cin, what):
 
 
 CASES = [
-    # mode, M, N, K, transA, transB, options  (what each exercises)
-    ("fp32", 300, 260, 200, False, False, {}),                     # SIMT whole tiles
-    ("fp32", 1000, 700, 3000, False, True, {}),                    # SIMT stream-K + fixup
-    ("fp32", 200, 272, 1000, True, False, {"split_k": 3}),         # SIMT split-K + reduce
-    ("tf32", 512, 512, 256, False, False, {}),                     # TC tiles, TMA-staged stores
-    ("tf32", 384, 1152, 4096, True, False, {"tile_n": 128}),       # TC split-K, A through TMEM
-    ("bf16", 2048, 2048, 256, False, False, {}),                   # TC pairs, one 256-row MMA
-    ("bf16", 2304, 1000, 1024, False, True, {}),                   # ragged N
-    ("bf16", 4096, 4096, 1024, False, True, {}),                   # tail slices + reduce
-    ("bf16", 4, 1536, 8960, False, True, {}),                      # small M: cluster reduction
-    ("bf16", 16, 8960, 1536, False, False, {}),                    # small M: clusters of 4
-    ("tf32", 8, 1536, 896, False, True, {"split_k": 1}),           # small M: no split
+    # mode, M, N, K, transA, transB, options, fused in the GEMM kernel  (what each exercises)
+    ("fp32", 300, 260, 200, False, False, {}, False),                  # SIMT whole tiles
+    ("fp32", 1000, 700, 3000, False, True, {}, False),                 # SIMT stream-K + fixup
+    ("fp32", 200, 272, 1000, True, False, {"split_k": 3}, False),      # SIMT split-K + reduce
+    ("tf32", 512, 512, 256, False, False, {}, True),                   # TC tiles, TMA-staged stores
+    ("tf32", 384, 1152, 4096, True, False, {"tile_n": 128}, False),    # TC split-K, A through TMEM
+    ("tf32", 384, 1152, 4096, True, False, {"tile_n": 256}, True),     # TC split-K, A transposed first
+    ("tf32", 700, 650, 300, False, True, {"tile_n": 192}, True),       # TC 192-column pairs
+    ("bf16", 2048, 2048, 256, False, False, {}, True),                 # TC pairs, one 256-row MMA
+    ("bf16", 2304, 1000, 1024, False, True, {}, True),                 # ragged N
+    ("bf16", 4096, 4096, 1024, False, True, {}, True),                 # tail slices + reduce
+    ("bf16", 600, 520, 96, True, False, {}, False),                    # MN-major A read in place
+    ("bf16", 4, 1536, 8960, False, True, {}, False),                   # small M: cluster reduction
+    ("bf16", 16, 8960, 1536, False, False, {}, False),                 # small M: clusters of 4
+    ("tf32", 8, 1536, 896, False, True, {"split_k": 1}, False),        # small M: no split
 ]
 
 
-@pytest.mark.parametrize("mode,M,N,K,tA,tB,opts", CASES)
+@pytest.mark.parametrize("mode,M,N,K,tA,tB,opts,fused", CASES)
 @pytest.mark.parametrize("act,use_bias,beta", [("none", True, 0.0), ("gelu", True, 0.0), ("gelu", False, 0.5),
                                                ("dgelu", False, 0.0), ("dgelu", False, 1.0)])
-def test_epilogue_matches_oracle(h, mode, M, N, K, tA, tB, opts, act, use_bias, beta):
+def test_epilogue_matches_oracle(h, mode, M, N, K, tA, tB, opts, fused, act, use_bias, beta):
     for k, v in opts.items():
         h.set_option(k, v)
     ops, c0 = _cases.make(mode, M, N, K, tA, tB, seed=101, dist="normal", with_c=True)
@@ -78,6 +85,7 @@ def test_epilogue_matches_oracle(h, mode, M, N, K, tA, tB, opts, act, use_bias, 
           bias=torch.from_numpy(bias).cuda() if bias is not None else None,
           aux=torch.from_numpy(Z).cuda() if Z is not None else None)
     assert h.check_device() == 0
+    assert h.plan()["epilogue_fused"] == (1 if fused else 0), h.plan()
     got = C.cpu().numpy()
     cin = c0.numpy() if beta != 0.0 else None
     rows = _cases.sample_rows(M) if M * N * K > 2e9 else [(0, M)]
@@ -123,3 +131,50 @@ def test_epilogue_argument_checks(h):
         h.run(A, A, C, act="dgelu")
     h.run(A, A, C, act="gelu")  # no bias is fine
     assert h.check_device() == 0
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("act", ["gelu", "dgelu"])
+def test_gelu_dense_sweep_against_oracle_and_cuda_erf(h, mode, act):
+    """GELU and GELU' on 8192 x 64 exact inputs spanning [-8, 8] (a K = 1
+    product a_i * b_j of values the mode holds exactly, so the GEMM adds no
+    error), fused into the tensor-core kernel: against the oracle's fp64
+    definition within the approximation's bound (|Phi error| <= 1.5e-7 plus
+    fp32 rounding), and against CUDA's erf through torch's exact GELU within
+    the same bound."""
+    M, N = 8192, 64
+    # a grid rounded to bf16 values (exact in both modes), b with 7 significant bits
+    a = np.empty((M, 1), dtype=np.float32)  # fresh arrays: unit stride along the length-1 axis too
+    a[:, 0] = si.to_bf16(torch.from_numpy((-8.0 + np.arange(M) / 512.0).astype(np.float32))).float().numpy()
+    b = np.empty((1, N), dtype=np.float32)
+    b[0, :] = 1.0 + np.arange(N) / 64.0
+    A = torch.from_numpy(a)
+    B = torch.from_numpy(b)
+    if mode == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+        a_host, b_host = si.bf16_bits(A), si.bf16_bits(B)
+    else:
+        a_host, b_host = a, b
+    Y, D = oracle.gemm(mode, a_host, b_host)
+    assert np.array_equal(Y, np.float64(a) * np.float64(b))  # the inputs are exact in the mode
+    C = torch.full((M, N), float("nan"), device="cuda")
+    if act == "gelu":
+        h.run(A.cuda(), B.cuda(), C, mode=mode, act="gelu")
+        ref = oracle.epilogue("gelu", Y)
+        cuda_ref = torch.nn.functional.gelu(torch.from_numpy(Y.astype(np.float32)).cuda(), approximate="none")
+        scale = np.abs(Y)
+    else:
+        Z = torch.from_numpy(Y.astype(np.float32)).cuda()
+        ones_a = torch.ones((M, 1), dtype=A.dtype)
+        ones_b = torch.ones((1, N), dtype=B.dtype)
+        h.run(ones_a.cuda(), ones_b.cuda(), C, mode=mode, act="dgelu", aux=Z)
+        ref = oracle.epilogue("dgelu", np.ones((M, N)), None, Y.astype(np.float32))
+        x = Z.double()
+        cuda_ref = (0.5 * (1.0 + torch.erf(x / np.sqrt(2.0))) + x * torch.exp(-0.5 * x * x) / np.sqrt(2 * np.pi))
+        scale = 1.0 + np.abs(Y)
+    assert h.check_device() == 0
+    assert h.plan()["epilogue_fused"] == 1
+    got = C.cpu().numpy().astype(np.float64)
+    bound = 4e-7 * scale + 1e-6 * np.abs(ref) + 1e-30
+    assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) / bound))
+    assert np.all(np.abs(got - cuda_ref.cpu().numpy()) <= bound + 1e-6 * np.abs(ref) + 2e-7 * scale)

@@ -33,13 +33,14 @@ def test_wait_runs_out_then_next_call_is_correct(h, mode, transA, skip):
     ops, _ = _cases.make(mode, M, N, K, transA, False, seed=311, dist="normal")
     h.set_option("family", "tc")
     h.set_option("tile_n", 128)
+    h.set_option("split_k", 1)  # CTA 0 takes one whole tile: 16 (BF16) or 32 (TF32) stages
     h.set_option("wait_limit_us", 1000)
     h.set_option("fault_skip_stage", skip)
     C = torch.zeros((M, N), device="cuda")
     h.run(ops.A, ops.B, C, mode=mode, transA=transA)
     assert h.check_device() == DEVICE_TIMEOUT
     plan = h.plan()
-    assert plan["family"] == "tc" and plan["cluster"] == 1 and plan["tile_n"] == 128, plan
+    assert plan["family"] == "tc" and plan["cluster"] == 1 and plan["tile_n"] == 128 and plan["split_k"] == 1, plan
     # the status word was cleared by the check; the GPU answers and the next
     # call on the same handle (hook off, default limit) is right again
     assert h.check_device() == 0
