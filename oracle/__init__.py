@@ -80,6 +80,8 @@ def _load():
         lib.oracle_gelu.argtypes = [d]
         lib.oracle_dgelu.restype = d
         lib.oracle_dgelu.argtypes = [d]
+        lib.oracle_attention.restype = ctypes.c_int
+        lib.oracle_attention.argtypes = [i64, i64, i64, ctypes.c_int, d, p, p, p, i64, i64, p, p]
         lib.oracle_epilogue.restype = ctypes.c_int
         lib.oracle_epilogue.argtypes = [ctypes.c_int, i64, i64, p, i64, p, p, i64, p, i64]
         _lib = lib
@@ -257,6 +259,31 @@ def gelu(x: float) -> float:
 def dgelu(x: float) -> float:
     """GELU'(x) = Phi(x) + x * phi(x)."""
     return _load().oracle_dgelu(float(x))
+
+
+def attention(Q, K, V, *, causal=True, scale=None, problems=None):
+    """Scaled dot-product attention, forward: (O, W) as float64 arrays of
+    shape [p1 - p0, T, Dh] for problems p0 .. p1-1 (all by default).
+
+    Q, K, V: uint16 bfloat16 bit patterns of shape [problems, T, Dh].
+    O[i] = sum_j softmax_j(scale * q_i . k_j) v_j over the keys query i sees
+    (j <= i when causal); W[i] = sum_j softmax_j |v_j|, the error scale.
+    scale defaults to 1 / sqrt(Dh)."""
+    lib = _load()
+    Q, K, V = (np.ascontiguousarray(x, dtype=np.uint16) for x in (Q, K, V))
+    if Q.ndim != 3 or K.shape != Q.shape or V.shape != Q.shape:
+        raise ValueError("Q, K and V must share one [problems, T, Dh] shape")
+    P, T, Dh = Q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(Dh)
+    p0, p1 = problems if problems is not None else (0, P)
+    O = np.zeros((p1 - p0, T, Dh), dtype=np.float64)
+    W = np.zeros((p1 - p0, T, Dh), dtype=np.float64)
+    rc = lib.oracle_attention(P, T, Dh, int(bool(causal)), float(scale), _ptr(Q), _ptr(K), _ptr(V), p0, p1,
+                              _ptr(O), _ptr(W))
+    if rc != 0:
+        raise ValueError(f"oracle_attention rejected its arguments ({rc})")
+    return O, W
 
 
 def epilogue(act, Y, bias=None, Z=None):

@@ -357,3 +357,63 @@ int oracle_gemm_block_scaled(int fmt_a, int fmt_b, int scale_fmt, int64_t bs, in
   }
   return 0;
 }
+
+/*
+ * Scaled dot-product attention, forward: the other GEMM-shaped operation of
+ * the GPT step.  "bare-metal-bard" (third paragraph) reports a fused
+ * attention kernel -- the score matrix never leaves the chip -- for the
+ * model's causal self-attention; the operation it computes is the plain
+ * definition, for every problem p (a batch element and head) and query row i:
+ *
+ *     s_j    = scale * sum_d q[i][d] * k[j][d]     for every key j that i sees
+ *              (j <= i when causal, every j < T otherwise)
+ *     p_j    = exp(s_j - max_j s_j),   l = sum_j p_j
+ *     O[i][d] = (sum_j p_j * v[j][d]) / l
+ *     W[i][d] = (sum_j p_j * |v[j][d]|) / l       (the error scale)
+ *
+ * Q, K and V are bfloat16 bit patterns of shape [problems][T][Dh], widened
+ * exactly; sums run over d, then j, ascending, in IEEE double.  Problems
+ * p0 .. p1-1 are produced, problem p's row i at O[((p - p0) * T + i) * Dh].
+ */
+int oracle_attention(int64_t problems, int64_t T, int64_t Dh, int causal, double scale, const uint16_t* Q,
+                     const uint16_t* K, const uint16_t* V, int64_t p0, int64_t p1, double* O, double* W) {
+  if (problems < 0 || T < 0 || Dh < 1 || p0 < 0 || p1 < p0 || p1 > problems) return 1;
+  if (T > 0 && (Q == NULL || K == NULL || V == NULL || O == NULL || W == NULL)) return 2;
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+  for (int64_t p = p0; p < p1; ++p) {
+    for (int64_t i = 0; i < T; ++i) {
+      const uint16_t* q = Q + (p * T + i) * Dh;
+      const int64_t keys = causal ? i + 1 : T;
+      double smax = -INFINITY;
+      for (int64_t j = 0; j < keys; ++j) {
+        const uint16_t* k = K + (p * T + j) * Dh;
+        double dot = 0.0;
+        for (int64_t d = 0; d < Dh; ++d) dot += oracle_bf16_to_double(q[d]) * oracle_bf16_to_double(k[d]);
+        const double s = scale * dot;
+        if (s > smax) smax = s;
+      }
+      double l = 0.0;
+      double* o = O + ((p - p0) * T + i) * Dh;
+      double* w = W + ((p - p0) * T + i) * Dh;
+      for (int64_t d = 0; d < Dh; ++d) o[d] = w[d] = 0.0;
+      for (int64_t j = 0; j < keys; ++j) {
+        const uint16_t* k = K + (p * T + j) * Dh;
+        const uint16_t* v = V + (p * T + j) * Dh;
+        double dot = 0.0;
+        for (int64_t d = 0; d < Dh; ++d) dot += oracle_bf16_to_double(q[d]) * oracle_bf16_to_double(k[d]);
+        const double pj = exp(scale * dot - smax);
+        l += pj;
+        for (int64_t d = 0; d < Dh; ++d) {
+          const double vd = oracle_bf16_to_double(v[d]);
+          o[d] += pj * vd;
+          w[d] += pj * fabs(vd);
+        }
+      }
+      for (int64_t d = 0; d < Dh; ++d) {
+        o[d] /= l;
+        w[d] /= l;
+      }
+    }
+  }
+  return 0;
+}

@@ -600,3 +600,93 @@ def test_epilogue_variants_elementwise():
             assert d[i, j] == Y[i, j] * oracle.dgelu(float(Z[i, j]))
     with pytest.raises(ValueError):
         oracle.epilogue("dgelu", Y, bias, Z)
+
+
+# ------------------------------------------------------------ attention (the fused-attention row)
+def _bf(x):
+    """bfloat16 bit patterns of float values (exact when they are bf16 values)."""
+    return si.bf16_bits(si.to_bf16(torch.from_numpy(np.asarray(x, dtype=np.float32))))
+
+
+def test_attention_zero_queries_average_the_visible_values():
+    """q = 0 gives equal scores, so every query averages the values it sees:
+    rows 0..i when causal, all rows otherwise."""
+    rng = np.random.default_rng(71)
+    P, T, D = 3, 9, 4
+    q = np.zeros((P, T, D))
+    k = rng.integers(-4, 5, size=(P, T, D)).astype(np.float32)
+    v = rng.integers(-4, 5, size=(P, T, D)).astype(np.float64)
+    O, W = oracle.attention(_bf(q), _bf(k), _bf(v), causal=True)
+    for i in range(T):
+        assert np.allclose(O[:, i], v[:, :i + 1].mean(axis=1), rtol=0, atol=1e-15)
+        assert np.allclose(W[:, i], np.abs(v[:, :i + 1]).mean(axis=1), rtol=0, atol=1e-15)
+    O, _ = oracle.attention(_bf(q), _bf(k), _bf(v), causal=False)
+    assert np.allclose(O, np.repeat(v.mean(axis=1, keepdims=True), T, axis=1), rtol=0, atol=1e-15)
+
+
+def test_attention_two_keys_closed_form():
+    """T = 2, Dh = 1, scale 1: row 0 sees only key 0; row 1 weighs the keys
+    e^1 : e^0, so O = (2e - 1) / (e + 1) and W = (2e + 1) / (e + 1)."""
+    q = np.array([[[1.0], [1.0]]])
+    k = np.array([[[1.0], [0.0]]])
+    v = np.array([[[2.0], [-1.0]]])
+    O, W = oracle.attention(_bf(q), _bf(k), _bf(v), causal=True, scale=1.0)
+    e = math.e
+    assert O[0, 0, 0] == 2.0 and W[0, 0, 0] == 2.0
+    assert abs(O[0, 1, 0] - (2 * e - 1) / (e + 1)) < 1e-15
+    assert abs(W[0, 1, 0] - (2 * e + 1) / (e + 1)) < 1e-15
+    O, _ = oracle.attention(_bf(q), _bf(k), _bf(v), causal=False, scale=1.0)
+    assert abs(O[0, 0, 0] - (2 * e - 1) / (e + 1)) < 1e-15  # non-causal row 0 sees both keys
+
+
+def test_attention_constant_values_and_a_dominant_key():
+    """Weights sum to one (constant values come back unchanged), and a key
+    whose score exceeds the others by 64 takes all the weight for the rows
+    that see it."""
+    rng = np.random.default_rng(72)
+    P, T, D = 2, 12, 2
+    q = rng.normal(size=(P, T, D)).astype(np.float32)
+    k = rng.normal(size=(P, T, D)).astype(np.float32)
+    O, W = oracle.attention(_bf(q), _bf(k), _bf(np.full((P, T, D), 3.0)), causal=True)
+    assert np.allclose(O, 3.0, rtol=0, atol=1e-14) and np.allclose(W, 3.0, rtol=0, atol=1e-14)
+    q = np.zeros((P, T, D))
+    q[..., 0] = 8.0
+    k = np.zeros((P, T, D))
+    k[:, 5, 0] = 8.0
+    v = rng.integers(-4, 5, size=(P, T, D)).astype(np.float64)
+    O, _ = oracle.attention(_bf(q), _bf(k), _bf(v), causal=True, scale=1.0)
+    for i in range(T):
+        want = v[:, 5] if i >= 5 else v[:, :i + 1].mean(axis=1)
+        assert np.allclose(O[:, i], want, rtol=0, atol=1e-20 + (1e-25 if i >= 5 else 1e-15)), i
+
+
+def test_attention_causal_rows_ignore_later_keys_and_values():
+    rng = np.random.default_rng(73)
+    P, T, D = 2, 16, 8
+    q, k, v = (rng.normal(size=(P, T, D)).astype(np.float32) for _ in range(3))
+    O1, _ = oracle.attention(_bf(q), _bf(k), _bf(v), causal=True)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, 10:] = rng.normal(size=(P, T - 10, D))
+    v2[:, 10:] = rng.normal(size=(P, T - 10, D))
+    O2, _ = oracle.attention(_bf(q), _bf(k2), _bf(v2), causal=True)
+    assert np.array_equal(O1[:, :10], O2[:, :10])
+    assert not np.allclose(O1[:, 10:], O2[:, 10:])
+    O3, _ = oracle.attention(_bf(q), _bf(k2), _bf(v2), causal=False)
+    assert not np.allclose(O3[:, :10], O2[:, :10])  # without the mask the early rows see the later keys
+
+
+def test_attention_score_shift_invariance_and_error_scale_bounds():
+    """Adding the same amount to every score of a row changes nothing (an
+    extra dimension with q = 1 and the same k for every key); and the error
+    scale W satisfies |O| <= W <= max |v|."""
+    rng = np.random.default_rng(74)
+    P, T, D = 2, 20, 6
+    q, k, v = (rng.integers(-3, 4, size=(P, T, D)).astype(np.float32) for _ in range(3))
+    O1, W1 = oracle.attention(_bf(q), _bf(k), _bf(v), causal=True, scale=0.25)
+    q2 = np.concatenate([q, np.ones((P, T, 1))], axis=2)
+    k2 = np.concatenate([k, np.full((P, T, 1), 5.0)], axis=2)
+    v2 = np.concatenate([v, np.zeros((P, T, 1))], axis=2)
+    O2, _ = oracle.attention(_bf(q2), _bf(k2), _bf(v2), causal=True, scale=0.25)
+    assert np.allclose(O2[..., :D], O1, rtol=0, atol=1e-13)
+    assert np.all(np.abs(O1) <= W1 * (1 + 1e-15))
+    assert np.all(W1 <= float(np.abs(v).max()) * (1 + 1e-14))
