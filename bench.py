@@ -490,6 +490,11 @@ def bench_ours(args, world, rank, local):
     configs = None
     if rank == 0 and not args.no_configs:
         configs = bench_configs(args, h, dev, pk)
+        # the whole 6-layer projection step (75 GEMMs) in each mode, eager
+        # and as one CUDA graph
+        with ClockSampler(dev.index) as fclk:
+            configs["full_step"] = [time_full_step(h, dev, m, 5, 3) for m in ("tf32", "bf16", "fp32")]
+        configs["full_step_clocks"] = fclk.summary()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -961,19 +966,13 @@ def bench_epilogue(args):
     print(json.dumps(line), flush=True)
 
 
-def bench_gpt_full(args):
+def time_full_step(h, dev, mode, steps, warmup):
     """The full projection step of the GPT (six layers of QKV, attention-out,
     MLP-up and MLP-down, each forward, dX and dW, plus the LM head: 75 GEMMs,
-    1046.6 GFLOP), timed as the host issues it and as one CUDA graph of the
+    1046 GFLOP), timed as the host issues it and as one CUDA graph of the
     whole step replayed.  Each layer has its own weights and activations
     (seeded, drawn on the device); one mode for the whole step."""
-    import dense_gemm_transformer_gb300 as dg
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    dg.load(build_if_missing=True)
-    h = dg.Gemm()
     stream = torch.cuda.Stream(dev)
-    mode = args.mode
     dt = torch.bfloat16 if mode == "bf16" else torch.float32
     T, layers = si.GPT_TOKENS, 6
     g = torch.Generator(device=dev)
@@ -998,7 +997,7 @@ def bench_gpt_full(args):
             h.run(A, B, C, mode=mode, transA=tA, transB=tB, stream=stream)
 
     with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 1)):
+        for _ in range(max(warmup, 1)):
             step()
     stream.synchronize()
     launches = 0
@@ -1008,36 +1007,52 @@ def bench_gpt_full(args):
             launches += h.plan()["kernels"]
     stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev.index) as clk:
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(args.steps):
-                step()
-            e1.record(stream)
-        stream.synchronize()
-        eager_ms = e0.elapsed_time(e1) / args.steps
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
             step()
-        graph.replay()
-        stream.synchronize()
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(args.steps):
-                graph.replay()
-            e1.record(stream)
-        stream.synchronize()
-        graph_ms = e0.elapsed_time(e1) / args.steps
+        e1.record(stream)
+    stream.synchronize()
+    eager_ms = e0.elapsed_time(e1) / steps
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    graph.replay()
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    graph_ms = e0.elapsed_time(e1) / steps
     assert h.check_device(stream) == 0
+    del graph, calls
+    torch.cuda.empty_cache()
+    return {"mode": mode, "gemms": len(shapes), "gflop": round(flops / 1e9, 1), "eager_ms": eager_ms,
+            "graph_ms": graph_ms, "eager_tflops": flops / (eager_ms * 1e-3) / 1e12,
+            "graph_tflops": flops / (graph_ms * 1e-3) / 1e12, "launches_per_step": launches}
+
+
+def bench_gpt_full(args):
+    """The full projection step in one mode (--mode), eager and as one graph."""
+    import dense_gemm_transformer_gb300 as dg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dg.load(build_if_missing=True)
+    h = dg.Gemm()
+    mode = args.mode
+    with ClockSampler(dev.index) as clk:
+        r = time_full_step(h, dev, mode, args.steps, args.warmup)
     h.close()
-    line = {"metric": METRIC, "value": flops / (graph_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": graph_ms, "higher_is_better": True,
+    line = {"metric": METRIC, "value": r["graph_tflops"], "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["graph_ms"], "higher_is_better": True,
             "dtype": {"fp32": "f32", "tf32": "tf32", "bf16": "bf16"}[mode], "data": "synthetic (seeded, drawn on the device)",
-            "config": {"workload": f"gpt_full_step_{mode}", "layers": layers, "tokens": T, "d_model": 384,
-                       "gemms_per_step": len(calls), "gflop_per_step": round(flops / 1e9, 1),
+            "config": {"workload": f"gpt_full_step_{mode}", "layers": 6, "tokens": si.GPT_TOKENS, "d_model": 384,
+                       "gemms_per_step": r["gemms"], "gflop_per_step": r["gflop"],
                        "timing": "one CUDA graph of the step, replayed; eager = as the host issues it"},
-            "eager": {"value": flops / (eager_ms * 1e-3) / 1e12, "ms_per_step": eager_ms},
-            "gpu_launches_per_step": launches, "clocks": clk.summary()}
+            "eager": {"value": r["eager_tflops"], "ms_per_step": r["eager_ms"]},
+            "gpu_launches_per_step": r["launches_per_step"], "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
 

@@ -695,8 +695,15 @@ gemm_status_t run_block_scaled(gemm_handle_s* h, int mode, int64_t M, int64_t N,
   const int64_t bs = nvfp4 ? 16 : 32;  // K elements per scale
   const int64_t tiles = ceil_div(N, 128);
   const int64_t kb = ceil_div(kbytes, 128);
-  int64_t splits = (h->opt_split_k > 0) ? std::min<int64_t>({static_cast<int64_t>(h->opt_split_k), kSkinnyMaxCluster, kb})
-                                        : skinny_cluster_size(h, kmode, false, tiles, kb);
+  // Two or more waves of weight tiles (the vocabulary projection): the
+  // persistent kernel, each CTA streaming tile after tile without a split
+  // (a CTA per tile would pay its set-up for a handful of stages); fewer
+  // tiles: the cluster kernel with K split across the cluster.
+  const bool persistent = tiles >= 2 * h->sms && h->opt_split_k == 0;
+  int64_t splits = persistent ? 1
+                   : (h->opt_split_k > 0)
+                       ? std::min<int64_t>({static_cast<int64_t>(h->opt_split_k), kSkinnyMaxCluster, kb})
+                       : skinny_cluster_size(h, kmode, false, tiles, kb);
   const int64_t kb_per = ceil_div(kb, splits);
   splits = ceil_div(kb, kb_per);
   TcArgs a{};
@@ -722,10 +729,17 @@ gemm_status_t run_block_scaled(gemm_handle_s* h, int mode, int64_t M, int64_t N,
   a.sfa = static_cast<const uint8_t*>(SB);
   a.sfb = static_cast<const uint8_t*>(SA);
   a.sf_groups = block_scale_groups(ceil_div(K, bs));
-  if (launch_skinny(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
-  set_plan(h, GEMM_FAMILY_SKINNY, 128, 16, static_cast<int>(nvfp4 ? 256 : 128), a.splits, skinny_stages(kmode), a.grid,
-           1, 0);
-  h->plan.cluster = a.splits;
+  if (persistent) {
+    a.grid = static_cast<int>(std::min<int64_t>(tiles, h->sms));
+    a.group_m = 16;
+    a.wait_ns = static_cast<uint64_t>(h->opt_wait_us) * 1000u;
+    if (launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  } else {
+    if (launch_skinny(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  }
+  set_plan(h, GEMM_FAMILY_SKINNY, 128, 16, static_cast<int>(nvfp4 ? 256 : 128), a.splits,
+           persistent ? tc_stages(kmode, 16, false) : skinny_stages(kmode), a.grid, 1, 0);
+  h->plan.cluster = persistent ? 1 : a.splits;
   h->plan.schedule = a.splits > 1 ? 1 : 0;
   return GEMM_OK;
 }

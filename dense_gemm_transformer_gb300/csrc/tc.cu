@@ -120,7 +120,10 @@ bool tc_epi_ok(int mode, bool a_mn_major, bool b_mn_major) {
 }
 
 int tc_stages(int mode, int tile_n, bool pair) {
-  (void)mode;  // a stage holds 128 bytes of K per row in every mode
+  // a stage holds 128 bytes of K per row in every mode; the block-scaled
+  // modes add their scale atoms to it
+  if (mode == 4) return TcCfg<4, 16>::STAGES;
+  if (mode == 5) return TcCfg<5, 16>::STAGES;
   if (tile_n == 256 && pair) return TcCfg<2, 256, true>::STAGES;
   if (tile_n == 224 && pair) return TcCfg<2, 224, true>::STAGES;
   if (tile_n == 192 && pair) return TcCfg<2, 192, true>::STAGES;
@@ -142,11 +145,12 @@ bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major) {
 }
 
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
-  if (a.mode < 1 || a.mode > 3) return cudaErrorInvalidValue;
+  if (a.mode < 1 || a.mode > 5) return cudaErrorInvalidValue;
+  if (a.mode >= 4 && (a.tile_n != 16 || a.a_mn_major || a.b_mn_major)) return cudaErrorInvalidValue;
   cudaError_t e = tc_init_driver();
   if (e != cudaSuccess) return e;
   const int bk = tc_tile_k(a.mode);
-  const int ch = 128 / ((a.mode == 3) ? 1 : (a.mode == 2) ? 2 : 4);  // elements in a 128-byte MN-major row
+  const int ch = 128 / ((a.mode >= 3) ? 1 : (a.mode == 2) ? 2 : 4);  // elements in a 128-byte MN-major row
   CUtensorMap ta, tb;
   e = a.a_mn_major ? encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.M, a.K, a.lda, ch, bk)
                    : encode_2d_c(a.tma_cache, &ta, a.mode, a.A, a.K, a.M, a.lda, bk, 128);
@@ -181,7 +185,10 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.ws_slice = a.ws_slice;
   p.ws_row0 = a.ws_row0;
   p.status = a.status;
-  p.fmt8 = a.mode == 3 ? a.fmt8 : 0u;
+  p.fmt8 = (a.mode == 3 || a.mode == 4) ? a.fmt8 : 0u;
+  p.sfa = a.sfa;
+  p.sfb = a.sfb;
+  p.sf_groups = a.sf_groups;
   p.wait_ns = a.wait_ns > 0 ? a.wait_ns : kWaitLimitNs;
   p.epi = a.fuse_epi ? a.epi : EpiParams{};
   p.fault_skip = (a.fault_skip > 0 && !pair) ? a.fault_skip - 1 : -1;
@@ -205,6 +212,7 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
     if (whole && a.beta == 0.f && p.c_vec)
       p.c_tma = (encode_out_c(a.tma_cache, &tcm, a.C, a.N, a.M, 1, a.ldc, a.M * a.ldc) == cudaSuccess) ? 1 : 0;
   }
+  if (a.mode >= 4) return tc_launch_bs(a.mode, ta, tb, tcm, twm, p, a.grid, stream);
   if (a.fuse_epi) {
     if (a.tile_n < 128 || !tc_epi_ok(a.mode, a.a_mn_major != 0, a.b_mn_major != 0)) return cudaErrorNotSupported;
     if (a.mode == 1)

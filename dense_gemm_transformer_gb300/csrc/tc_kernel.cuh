@@ -77,6 +77,9 @@ struct TcParams {
   int w_tma;  // partial tiles likewise (tmW is valid)
   uint32_t fmt8;  // MODE 3: operand format bits of the instruction descriptor (E4M3 / E5M2)
   EpiParams epi;     // EPI kernels: bias / GELU / GELU' applied at every final store of a whole tile
+  const uint8_t* sfa;  // BS: scales of the kernel's A (the weights), tiled 512-byte atoms
+  const uint8_t* sfb;  // BS: scales of the kernel's B (the activations)
+  int64_t sf_groups;   // BS: atoms per 128-row tile
   uint64_t wait_ns;  // limit of every bounded wait
   int fault_skip;    // test hook: CTA 0's producer issues no copies for its fault_skip-th stage
                      // (0-based; -1: none), so the MMA's wait for that stage runs out
@@ -89,14 +92,19 @@ struct TcParams {
 // of the pair holds the other half).
 template <int MODE, int BN, bool BHALF = false>
 struct TcCfg {
-  static constexpr int ES = (MODE == 3) ? 1 : (MODE == 2) ? 2 : 4;  // operand bytes
+  static constexpr bool BS = MODE >= 4;  // block-scaled: 4 MXFP8, 5 NVFP4 (the swapped small-M form only)
+  static constexpr int ES = (MODE >= 3) ? 1 : (MODE == 2) ? 2 : 4;  // operand bytes (coordinate units)
   static constexpr int BM = 128;                      // rows of the tile (UMMA M)
-  static constexpr int BK = 128 / ES;                 // K elements per stage: one 128-byte swizzle row
-  static constexpr int UK = 32 / ES;                  // K of one MMA instruction (32 bytes)
+  static constexpr int BK = 128 / ES;                 // K units per stage: one 128-byte swizzle row
+  static constexpr int UK = 32 / ES;                  // K units of one MMA instruction (32 bytes)
   static constexpr int CH = 128 / ES;                 // M/N elements of one 128-byte MN-major row
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_BYTES = BHALF ? BN * 64 : BN * 128;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // BS: both operands' scale atoms for the stage's 128 bytes of K (512
+  // bytes per 128 rows and 4 scale blocks: 1 atom for MXFP8, 4 for NVFP4)
+  static constexpr int SF_ATOMS = (MODE == 5) ? 4 : (MODE == 4) ? 1 : 0;
+  static constexpr int SF_BYTES = SF_ATOMS * 512;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;
   // Epilogue staging for TMA stores: one buffer of 32 rows x 128 bytes per
   // epilogue warp (the swapped small-M form stores directly and has none).
   static constexpr int STAGING_BYTES = (BN >= 128) ? kTcEpiWarps * 32 * 128 : 0;
@@ -104,14 +112,21 @@ struct TcCfg {
   // a stage holds half of B)
   static constexpr int STAGES = BHALF ? (232448 - STAGING_BYTES - 1280) / STAGE_BYTES
                                       : (BN >= 192) ? 4 : (BN == 128) ? 6 : 200 * 1024 / STAGE_BYTES;
-  // Two accumulators; an allocation is a power of two of at least 32 columns.
-  static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
-                                   : (2 * BN <= 256) ? 256 : 512;
+  // Two accumulators, then (BS) one ring slot of scale columns per stage
+  // (4 columns per atom, A's atoms then B's); an allocation is a power of
+  // two of at least 32 columns.
+  static constexpr int SF_COL0 = 2 * BN;
+  static constexpr int SF_COLS = 2 * SF_ATOMS * 4;
+  static constexpr int TMEM_NEED = SF_COL0 + (BS ? STAGES * SF_COLS : 0);
+  static constexpr int TMEM_COLS = (TMEM_NEED <= 32) ? 32 : (TMEM_NEED <= 64) ? 64 : (TMEM_NEED <= 128) ? 128
+                                   : (TMEM_NEED <= 256) ? 256 : 512;
+  static_assert(TMEM_NEED <= 512, "TMEM columns");
+  static_assert(!BS || (BN == 16 && !BHALF), "block-scaled: the swapped small-M form");
   static constexpr int CW = BN < 32 ? BN : 32;                    // accumulator columns per TMEM load
   static constexpr int NUM_BARS = 2 * STAGES + 5;     // full/empty per stage, acc full/empty x2, drain
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
-  static constexpr uint32_t FORMAT = (MODE == 3) ? 0u : (MODE == 2) ? 1u : 2u;  // 8-bit (fmt8) / bf16 / tf32
+  static constexpr uint32_t FORMAT = (MODE >= 3) ? 0u : (MODE == 2) ? 1u : 2u;  // 8-bit (fmt8) / bf16 / tf32
   static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
   static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -421,6 +436,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else {
               tma_load_2d(b_dst, &tmB, fb, k0, w.tn * BN);
             }
+            if constexpr (Cfg::BS) {
+              // both operands' scale atoms for this stage (B: the activations,
+              // one row tile)
+              const uint32_t sf_dst = b_dst + Cfg::B_BYTES;
+              bulk_copy_g2s(sf_dst, p.sfa + (static_cast<int64_t>(tm) * p.sf_groups + kb * Cfg::SF_ATOMS) * 512,
+                            Cfg::SF_BYTES, fb);
+              bulk_copy_g2s(sf_dst + Cfg::SF_BYTES, p.sfb + static_cast<int64_t>(kb) * Cfg::SF_ATOMS * 512,
+                            Cfg::SF_BYTES, fb);
+            }
           }
           ++issued;
           if (++stage == S) {
@@ -471,17 +495,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_fence_after();
           const uint32_t a_base = smem0 + stage * Cfg::STAGE_BYTES;
           const uint32_t b_base = a_base + Cfg::A_BYTES;
+          if constexpr (Cfg::BS) {
+            // The stage's scale atoms into its TMEM ring slot (free: this
+            // stage's copies were issued only after the slot's previous MMAs
+            // released the stage), then four block-scaled MMAs of 32 bytes
+            // of K: MXFP8 picks its byte of the scale cells by ID j, NVFP4
+            // reads atom j's four bytes.
+            const uint32_t sf_col = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + stage * Cfg::SF_COLS);
+            const uint32_t sf_smem = b_base + Cfg::B_BYTES;
 #pragma unroll
-          for (int j = 0; j < Cfg::BK / Cfg::UK; ++j) {
-            const uint64_t bd = B_MN ? smem_desc_sw128(b_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
-                                     : smem_desc_sw128(b_base + j * Cfg::UK * Cfg::ES, 16, 1024);
-            if constexpr (A_TMEM) {
-              mma_tf32_tmem_a(d_tmem, tmem_base + static_cast<uint32_t>(A_COL0 + ab * Cfg::BK + j * Cfg::UK), bd,
-                              IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
-            } else {
-              const uint64_t ad = A_MN ? smem_desc_sw128(a_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
-                                       : smem_desc_sw128(a_base + j * Cfg::UK * Cfg::ES, 16, 1024);
-              issue_mma<MODE, PAIR>(d_tmem, ad, bd, IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
+            for (int a = 0; a < 2 * Cfg::SF_ATOMS; ++a)
+              tmem_cp_32x128b_x4(sf_col + 4 * a, smem_desc_noswizzle(sf_smem + 512 * a, 128));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t ad = smem_desc_sw128(a_base + j * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(b_base + j * 32, 16, 1024);
+              const uint32_t acc_in = (kb > w.kb0 || j > 0) ? 1u : 0u;
+              if constexpr (MODE == 4)
+                mma_mxf8f6f4_bs(d_tmem, ad, bd,
+                                make_idesc_bs(0, 0, true, Cfg::BM, BN, static_cast<uint32_t>(j),
+                                              static_cast<uint32_t>(j)) | p.fmt8,
+                                sf_col, sf_col + 4, acc_in);
+              else
+                mma_mxf4nvf4_bs(d_tmem, ad, bd, make_idesc_bs(1, 1, false, Cfg::BM, BN, 0, 0), sf_col + 4 * j,
+                                sf_col + 4 * (Cfg::SF_ATOMS + j), acc_in);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < Cfg::BK / Cfg::UK; ++j) {
+              const uint64_t bd = B_MN ? smem_desc_sw128(b_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
+                                       : smem_desc_sw128(b_base + j * Cfg::UK * Cfg::ES, 16, 1024);
+              if constexpr (A_TMEM) {
+                mma_tf32_tmem_a(d_tmem, tmem_base + static_cast<uint32_t>(A_COL0 + ab * Cfg::BK + j * Cfg::UK), bd,
+                                IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
+              } else {
+                const uint64_t ad = A_MN ? smem_desc_sw128(a_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
+                                         : smem_desc_sw128(a_base + j * Cfg::UK * Cfg::ES, 16, 1024);
+                issue_mma<MODE, PAIR>(d_tmem, ad, bd, IDESC, (kb > w.kb0 || j > 0) ? 1u : 0u);
+              }
             }
           }
           if constexpr (A_TMEM) {

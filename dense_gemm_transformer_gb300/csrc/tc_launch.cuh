@@ -134,6 +134,11 @@ cudaError_t tc_launch_fp8(int tile_n, bool pair, bool a_mn, bool b_mn, const CUt
 cudaError_t tc_launch_fp8_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
                               const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                               const TcParams& p, int grid, cudaStream_t s);
+// The swapped small-M form for block-scaled operands (mode 4 MXFP8, 5
+// NVFP4): tc_bs.cu.
+cudaError_t tc_launch_bs(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                         const CUtensorMap& tw, const TcParams& p, int grid, cudaStream_t s);
+
 // The same kernels with the fused epilogue (EPI), K-major A: tc_tf32_epi.cu
 // (TF32, every width), tc_bf16_epi.cu (BF16, 128 and 256 columns) and
 // tc_bf16_epi_mid.cu (BF16, 192 and 224 columns).

@@ -125,6 +125,33 @@ def test_block_scaled_integers_bit_exact(h, mode, M, N, K, splits):
         assert h.plan()["split_k"] == -(-kb // per), h.plan()
 
 
+@pytest.mark.parametrize("mode", list(MODES))
+def test_block_scaled_persistent_form(h, mode):
+    """Two or more waves of 128-row weight tiles go to the persistent kernel
+    (each CTA streams tile after tile, no K split): ragged N, a partial last
+    stage; normal inputs within the gate and integers bit-exact."""
+    elem, bs, sf = MODES[mode]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, N, K = 5, 128 * (2 * sms + 9) - 37, 1056
+    ac, sa = si.to_block_scaled(si.normal((M, K), 617), elem, bs, sf)
+    bc, sb = si.to_block_scaled(si.normal((N, K), 618, std=0.02), elem, bs, sf)
+    got = _run(h, mode, ac, sa, bc, sb, M, N)
+    plan = h.plan()
+    assert plan["family"] == "skinny" and plan["cluster"] == 1 and plan["split_k"] == 1 and plan["grid"] == sms, plan
+    ref, D = _oracle(mode, ac, sa, bc, sb)
+    _gate.assert_within("fp8", got, ref, D, what=f"{mode} persistent {M}x{N}x{K}")
+    rng = np.random.default_rng(619)
+    nb = -(-K // bs)
+    ac, bc = _integer_codes(mode, (M, K), rng), _integer_codes(mode, (N, K), rng)
+    sa, sb = _pow2_scales(mode, M, nb, rng), _pow2_scales(mode, N, nb, rng)
+    c0 = si.normal((M, N), 620)
+    got = _run(h, mode, ac, sa, bc, sb, M, N, alpha=2.0, beta=1.0, c0=c0)
+    ref, _ = _oracle(mode, ac, sa, bc, sb, alpha=2.0, beta=1.0, c0=c0)
+    # integers and power-of-two scales: exact products and sums; adding
+    # beta * C rounds the result once
+    assert np.all(np.abs(got.astype(np.float64) - ref) <= 2.0 ** -24 * np.abs(ref)), mode
+
+
 def _random_codes(mode, shape, rng):
     """Random finite codes of moderate magnitude (no scaling needed)."""
     elem = MODES[mode][0]
