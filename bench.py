@@ -966,6 +966,76 @@ def bench_epilogue(args):
     print(json.dumps(line), flush=True)
 
 
+def attention_flops_bytes(P, T, D, causal):
+    """Algorithmic work of one attention forward: 4 D flops per (query, visible
+    key) pair (the score dot product and the P V product); bytes: Q, K and V
+    read once (bf16) and O written once (fp32)."""
+    pairs = T * (T + 1) // 2 if causal else T * T
+    return 4 * D * pairs * P, P * T * D * (3 * 2 + 4)
+
+
+def bench_attention(args):
+    """The fused attention forward (gemm_attention_forward) on the GPT's
+    attention (64 sequences x 6 heads of 64, context 256) and on the same
+    16384 tokens at contexts 1024 and 2048, causal.  Median of 5 samples of
+    >= 20 ms of calls back to back, inputs rotated over copies > 3x L2; the
+    roofline is the larger of the tensor time (bf16 burst peak) and the HBM
+    time of the algorithmic bytes."""
+    import dense_gemm_transformer_gb300 as dg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dg.load(build_if_missing=True)
+    h = dg.Gemm()
+    stream = torch.cuda.Stream(dev)
+    pk = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    D = si.ATTN_HEAD_DIM
+    shapes = []
+    with ClockSampler(dev.index) as clk:
+        for idx, (name, P, T) in enumerate(si.ATTN_WORKLOADS):
+            flops, byts = attention_flops_bytes(P, T, D, True)
+            copies = max(1, min(8, -(-3 * l2 // byts)))
+            Q, K, V = (t.to(dev) for t in si.attention_qkv(P, T, shape=idx))
+            sets = [(Q, K, V, torch.empty(Q.shape, dtype=torch.float32, device=dev))]
+            for _ in range(copies - 1):
+                sets.append((Q.clone(), K.clone(), V.clone(), torch.empty(Q.shape, dtype=torch.float32, device=dev)))
+
+            def call(r):
+                q, k, v, o = sets[r % copies]
+                h.attention(q, k, v, o, causal=True, stream=stream)
+
+            with torch.cuda.stream(stream):
+                for r in range(copies):
+                    call(r)
+            stream.synchronize()
+            t_est = _timed_back_to_back(call, max(2 * copies, 10), stream, 300)
+            reps = int(min(MAX_REPS, max(10, math.ceil(SAMPLE_MS / max(t_est, 1e-4)))))
+            st = _stats([_timed_back_to_back(call, reps, stream, 300) for _ in range(SAMPLES)])
+            assert h.check_device(stream) == 0
+            ms = st["median"]
+            t_tensor = flops / (pk["bf16_tflops"] * 1e12)
+            t_hbm = byts / (pk["hbm_gbs"] * 1e9)
+            shapes.append({"attention": name, "problems": P, "T": T, "Dh": D, "causal": True,
+                           "ms": round(ms, 5), "ms_min": round(st["min"], 5), "ms_max": round(st["max"], 5),
+                           "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+                           "gbs": round(byts / (ms * 1e-3) / 1e9, 1),
+                           "bound": "tensor" if t_tensor >= t_hbm else "hbm",
+                           "roofline_frac": round(max(t_tensor, t_hbm) / (ms * 1e-3), 3),
+                           "scores_bytes_not_written": 4 * P * T * T, "plan": h.plan()})
+            del sets, Q, K, V
+            torch.cuda.empty_cache()
+    h.close()
+    total_flops = sum(attention_flops_bytes(x["problems"], x["T"], D, True)[0] for x in shapes)
+    line = {"metric": "fused attention forward TFLOP/s and fraction of the roofline, 1 GPU",
+            "value": total_flops / (sum(x["ms"] for x in shapes) * 1e-3) / 1e12,
+            "unit": "TFLOP/s", "n_gpus": 1, "higher_is_better": True, "dtype": "bf16 in, fp32 accumulate and out",
+            "data": "synthetic",
+            "config": {"workload": "attention", "l2": "inputs rotated over copies > 3x L2",
+                       "samples": f"median of {SAMPLES} samples of >= {SAMPLE_MS:g} ms"},
+            "clocks": clk.summary(), "shapes": shapes, "peaks": pk}
+    print(json.dumps(line), flush=True)
+
+
 def time_full_step(h, dev, mode, steps, warmup):
     """The full projection step of the GPT (six layers of QKV, attention-out,
     MLP-up and MLP-down, each forward, dX and dW, plus the LM head: 75 GEMMs,
@@ -1077,7 +1147,8 @@ def main():
                     help="sweeps: CTA pairs issuing one 256-row MMA (0 wherever allowed, 1 never)")
     ap.add_argument("--split-k", type=int, default=0, help="sweeps: force this many K slices (0: planner)")
     ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "large_fp8", "skinny", "skinny_fp8",
-                                                          "skinny_nvfp4", "skinny_mxfp8", "epilogue", "gpt_full"],
+                                                          "skinny_nvfp4", "skinny_mxfp8", "epilogue", "gpt_full",
+                                                          "attention"],
                     help="gpt: the timed step; the others print a per-shape sweep")
     ap.add_argument("--mode", default="tf32", choices=["fp32", "tf32", "bf16"],
                     help="gpt_full: the mode of the whole step")
@@ -1091,6 +1162,8 @@ def main():
         bench_reference(args, world, rank)
     elif args.workload == "epilogue":
         bench_epilogue(args)
+    elif args.workload == "attention":
+        bench_attention(args)
     elif args.workload == "gpt_full":
         bench_gpt_full(args)
     elif args.workload != "gpt":

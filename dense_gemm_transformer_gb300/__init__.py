@@ -15,6 +15,7 @@ without the built extension raises.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import re
 import threading
@@ -177,7 +178,7 @@ class Gemm:
     def plan(self) -> dict:
         p = Plan()
         _check(self._lib.gemm_get_plan(self._h, ctypes.byref(p)), "gemm_get_plan")
-        fam = {v: k for k, v in FAMILIES.items()}.get(p.family, "none")
+        fam = {**{v: k for k, v in FAMILIES.items()}, 4: "attention"}.get(p.family, "none")
         return {"family": fam if p.kernels else "none", "tile_m": p.tile_m, "tile_n": p.tile_n,
                 "tile_k": p.tile_k, "split_k": p.split_k, "stages": p.stages, "grid": p.grid,
                 "kernels": p.kernels, "packed": p.packed,
@@ -229,6 +230,42 @@ class Gemm:
                 float(beta), pc, ldc, _stream_ptr(stream))
         _check(st, "gemm_run_block_scaled")
         return C
+
+    def attention_ptr(self, problems, T, Dh, causal, scale, Q, K, V, O, stream=None):
+        """gemm_attention_forward on raw device pointers."""
+        fn = self._lib.gemm_attention_forward
+        i64, vp, f32, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+        fn.argtypes = [vp, i64, i64, i64, i32, f32, vp, vp, vp, vp, vp]
+        fn.restype = i32
+        st = fn(self._h, int(problems), int(T), int(Dh), int(causal), float(scale), Q, K, V, O, _stream_ptr(stream))
+        _check(st, "gemm_attention_forward")
+
+    def attention(self, Q, K, V, O=None, causal=True, scale=None, stream=None):
+        """O = softmax(scale Q K^T [causal mask]) V through gemm_attention_forward.
+
+        Q, K, V: contiguous bfloat16 CUDA tensors of one shape [..., T, 64]
+        (the leading dimensions, e.g. batch and head, are the independent
+        problems); O: float32 of the same shape (allocated when None).
+        scale defaults to 1 / sqrt(64)."""
+        import torch
+        if Q.dim() < 2 or K.shape != Q.shape or V.shape != Q.shape:
+            raise ValueError("Q, K and V must share one [..., T, Dh] shape")
+        for t, name in ((Q, "Q"), (K, "K"), (V, "V")):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise TypeError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+        T, Dh = Q.shape[-2], Q.shape[-1]
+        problems = Q.numel() // max(T * Dh, 1)
+        if O is None:
+            O = torch.empty(Q.shape, dtype=torch.float32, device=Q.device)
+        elif O.shape != Q.shape or O.dtype != torch.float32 or not O.is_contiguous():
+            raise ValueError("O must be a contiguous float32 tensor of Q's shape")
+        if scale is None:
+            scale = 1.0 / math.sqrt(Dh)
+        if stream is None:
+            stream = torch.cuda.current_stream(Q.device)
+        self.attention_ptr(problems, T, Dh, causal, scale, Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                           stream)
+        return O
 
     def run(self, A, B, C, mode="fp32", transA=False, transB=False, alpha=1.0, beta=0.0, stream=None,
             act="none", bias=None, aux=None):
@@ -325,6 +362,11 @@ def gemm(A, B, C, mode="fp32", transA=False, transB=False, alpha=1.0, beta=0.0, 
     """C = alpha * op(A) op(B) + beta * C with the current device's default handle
     (and the fused epilogue of Gemm.run when act / bias / aux are given)."""
     return default_handle().run(A, B, C, mode, transA, transB, alpha, beta, stream, act, bias, aux)
+
+
+def attention(Q, K, V, O=None, causal=True, scale=None, stream=None):
+    """Fused attention forward with the current device's default handle (Gemm.attention)."""
+    return default_handle().attention(Q, K, V, O, causal=causal, scale=scale, stream=stream)
 
 
 def run_small_m_noalloc(A, B, C, mode="bf16", transB=False, alpha=1.0, beta=0.0, stream=None):

@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -962,6 +963,37 @@ gemm_status_t gemm_run_block_scaled(gemm_handle_t h, int mode, int64_t M, int64_
   }
   if (st == GEMM_OK) h->null_shape = dgt::last_main_launch();
   return st;
+}
+
+gemm_status_t gemm_attention_forward(gemm_handle_t h, int64_t problems, int64_t T, int64_t Dh, int causal,
+                                     float scale, const void* Q, const void* K, const void* V, float* O,
+                                     void* stream) {
+  if (h == nullptr) return GEMM_ERR_INVALID_VALUE;
+  if (problems < 0 || T < 0 || Dh < 1 || (causal != 0 && causal != 1) || !std::isfinite(scale))
+    return GEMM_ERR_INVALID_VALUE;
+  if (Dh != 64) return GEMM_ERR_NOT_SUPPORTED;
+  if (problems == 0 || T == 0) return GEMM_OK;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return GEMM_ERR_INVALID_VALUE;
+  // one CTA per (problem, 128 queries) in a 1-D grid; TMA extents below 2^31
+  if (T > kMaxDim || problems > kMaxDim || problems * ceil_div(T, 128) > INT32_MAX) return GEMM_ERR_INVALID_VALUE;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return GEMM_ERR_MISALIGNED;
+  dgt::AttnArgs a{};
+  a.problems = problems;
+  a.T = T;
+  a.causal = causal;
+  a.scale = scale;
+  a.Q = Q;
+  a.K = K;
+  a.V = V;
+  a.O = O;
+  a.status = h->d_status;
+  a.wait_ns = static_cast<uint64_t>(h->opt_wait_us) * 1000u;
+  dgt::last_main_launch().valid = false;
+  if (dgt::launch_attention(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return GEMM_ERR_CUDA;
+  const int64_t grid = problems * ceil_div(T, 128);
+  set_plan(h, GEMM_FAMILY_ATTENTION, 128, 128, 64, 1, 1, static_cast<int>(grid), 1, 0);
+  h->null_shape = dgt::last_main_launch();
+  return GEMM_OK;
 }
 
 int64_t gemm_block_scales_tiled_bytes(int64_t rows, int64_t blocks) {

@@ -1,11 +1,12 @@
 // epilogue.cuh -- the elementwise work of gemm_run_epilogue: a per-column
 // bias, GELU, or the product with GELU' of a kept pre-activation (the
-// backward pass through a GELU).  It runs where a call already touches every
-// element of C after the GEMM kernels (the split-K reduction, the beta-only
-// update), or else in one pass over C: computed inside the GEMM kernels'
-// epilogues it measured slower than that pass on the GPT products (K = 384:
-// the erf evaluations stall the tile pipeline more than the pass costs in
-// HBM traffic), and it took registers from kernels that sit at their limit.
+// backward pass through a GELU).  It is applied once per element, at the
+// final store: in the tcgen05 kernel's epilogue warps when that kernel
+// writes C itself (TF32 and BF16 with a K-major A, whole tiles or the tail
+// slices with their reduction), in the split-K reduction when a call ends
+// with one, in the beta-only update for K = 0, and otherwise in one pass over
+// C after the GEMM kernels (the SIMT family, A moved through TMEM, the
+// small-M kernels).
 //
 // "bare-metal-bard" (second paragraph) trains a GPT with hand-written
 // matmul, layernorm and GELU kernels; the page does not say which GELU.  The

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 namespace dgt {
 
@@ -185,6 +186,24 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream);
 // * splits.
 cudaError_t launch_skinny(const TcArgs& a, cudaStream_t stream);
 cudaError_t tc_init_driver();         // resolves cuTensorMapEncodeTiled once
+// The resolved cuTensorMapEncodeTiled (null until tc_init_driver succeeded).
+PFN_cuTensorMapEncodeTiled_v12000 tc_encoder();
+
+// ---------------------------------------------------------------- attention
+// Fused scaled dot-product attention forward over `problems` independent
+// (batch element, head) problems: Q, K, V bf16 [problems][T][64] (rows of 64
+// contiguous elements, 16-byte aligned), O fp32 of the same shape.  One CTA
+// per (problem, 128 queries); scores stay in tensor memory.
+struct AttnArgs {
+  int64_t problems, T;
+  int causal;
+  float scale;
+  const void *Q, *K, *V;
+  float* O;
+  int* status;       // device status word (bounded waits)
+  uint64_t wait_ns;  // 0: kWaitLimitNs
+};
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- helpers
 // C = epi(alpha * sum_s ws[s] + beta * C) over an M x N matrix (s

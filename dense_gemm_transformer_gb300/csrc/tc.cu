@@ -112,6 +112,8 @@ cudaError_t tc_init_driver() {
   return g_encode_status;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tc_encoder() { return g_encode; }
+
 int tc_tile_k(int mode) { return mode >= 3 ? 128 : mode == 2 ? 64 : 32; }
 
 bool tc_epi_ok(int mode, bool a_mn_major, bool b_mn_major) {

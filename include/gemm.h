@@ -94,7 +94,8 @@ typedef enum {
   GEMM_FAMILY_AUTO = 0,
   GEMM_FAMILY_SIMT = 1,   /* register-tiled FFMA kernel (GEMM_MODE_FP32 only)           */
   GEMM_FAMILY_TC = 2,     /* persistent TMA + tcgen05 kernel (TF32/BF16/FP8)             */
-  GEMM_FAMILY_SKINNY = 3  /* HBM-bound small-M kernels, M <= 16 (TF32/BF16/FP8)         */
+  GEMM_FAMILY_SKINNY = 3, /* HBM-bound small-M kernels, M <= 16 (TF32/BF16/FP8)         */
+  GEMM_FAMILY_ATTENTION = 4 /* the fused attention kernel (gemm_attention_forward)        */
 } gemm_family_t;
 
 typedef enum {
@@ -359,6 +360,32 @@ int64_t gemm_block_scales_tiled_bytes(int64_t rows, int64_t blocks);
  * source pages (a layout of this library's kernels).  Asynchronous on
  * `stream`. */
 gemm_status_t gemm_block_scales_tile(int64_t rows, int64_t blocks, const void* S, int64_t lds, void* T,
+                                     void* stream);
+
+/* Scaled dot-product attention, forward, fused: for each of `problems`
+ * independent problems (a batch element and a head) and each query row i,
+ *     O[i] = sum_j softmax_j(scale * q_i . k_j) v_j
+ * over the keys j that row i sees (j <= i when causal = 1, every j < T when
+ * causal = 0).  "bare-metal-bard" (third paragraph) reports such a fused,
+ * FlashAttention-style kernel for its GPT's causal self-attention: the score
+ * matrix is never written out; a running maximum and sum are carried from
+ * one block of keys to the next, so memory grows linearly with T.  Here the
+ * scores of 128 queries x 128 keys live in tensor memory (tcgen05), the
+ * probabilities are rounded to bf16 for the P V product, and the row sums
+ * are kept in fp32.
+ * Q, K, V: bfloat16, [problems][T][Dh] contiguous (row i of problem p at
+ * element (p * T + i) * Dh); O: float32 of the same shape.  All device
+ * memory owned by the caller, 16-byte aligned.  Dh must be 64 (the GPT's
+ * head size); scale is usually 1 / sqrt(Dh).
+ * Errors: GEMM_ERR_INVALID_VALUE for a null handle or pointer, negative
+ * sizes, causal not 0/1, a non-finite scale or more than 2^31 - 1 query
+ * tiles; GEMM_ERR_NOT_SUPPORTED for Dh != 64; GEMM_ERR_MISALIGNED for a
+ * pointer not 16-byte aligned.  problems == 0 or T == 0 is a no-op.
+ * Asynchronous on `stream`; the handle's device status word records a
+ * bounded wait that gave up (gemm_check_device).  gemm_get_plan reports
+ * family GEMM_FAMILY_ATTENTION and the grid. */
+gemm_status_t gemm_attention_forward(gemm_handle_t h, int64_t problems, int64_t T, int64_t Dh, int causal,
+                                     float scale, const void* Q, const void* K, const void* V, float* O,
                                      void* stream);
 
 /* A static string naming a status code. */

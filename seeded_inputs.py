@@ -23,6 +23,12 @@ Workloads (every one stands in for data that is not available here):
   decode shapes (1, 4 or 16 token rows against 1536 x 8960, 8960 x 1536 and
   1536 x 151936 weights: the hidden, MLP and vocabulary widths of the decode
   step on vidyal.ai's "One Token, Kernel by Kernel").
+* attention: the GPT's causal self-attention, which "bare-metal-bard"
+  (third paragraph) runs as one fused kernel -- 64 sequences x 6 heads of 64
+  at context 256 -- and the same 16384 tokens per step at the longer
+  contexts the page trains at (16 x 1024 and 8 x 2048 tokens, 6 heads); Q,
+  K and V are N(0, 1) rounded to bf16, so that with the usual 1 / sqrt(64)
+  scale the scores are N(0, 1).
 """
 from __future__ import annotations
 
@@ -45,6 +51,15 @@ SQUARE_SWEEP = (1024, 2048, 4096)
 LARGE_BF16 = ((8192, 8192, 8192), (8192, 28672, 8192))
 SKINNY_M = (1, 4, 16)
 SKINNY_WEIGHTS = ((1536, 8960), (8960, 1536), (1536, 151936))  # K x N
+
+
+ATTN_HEAD_DIM = 64
+# (name, problems = sequences x heads, context T)
+ATTN_WORKLOADS = (
+    ("gpt_ctx256", 64 * 6, 256),
+    ("ctx1024", 16 * 6, 1024),
+    ("ctx2048", 8 * 6, 2048),
+)
 
 
 def seed_for(config: int, shape: int, tensor_id: int) -> int:
@@ -238,3 +253,13 @@ def skinny_cases():
         for k, n in SKINNY_WEIGHTS:
             out.append(GemmCase(f"skinny_m{m}_{k}x{n}", False, False, m, n, k))
     return out
+
+
+def attention_qkv(problems: int, T: int, shape: int = 0, config: int = 1, std_q: float = 1.0):
+    """Q, K, V: bf16 CPU tensors of [problems, T, 64], N(0, 1) (Q: N(0, std_q^2),
+    a larger std_q makes the softmax peaked)."""
+    D = ATTN_HEAD_DIM
+    Q = to_bf16(normal((problems, T, D), seed_for(config, shape, 0), std=std_q))
+    K = to_bf16(normal((problems, T, D), seed_for(config, shape, 1)))
+    V = to_bf16(normal((problems, T, D), seed_for(config, shape, 2)))
+    return Q, K, V
