@@ -988,10 +988,10 @@ gemm_status_t gemm_attention_forward(gemm_handle_t h, int64_t problems, int64_t 
   a.O = O;
   a.status = h->d_status;
   a.wait_ns = static_cast<uint64_t>(h->opt_wait_us) * 1000u;
+  a.sms = h->sms;
   dgt::last_main_launch().valid = false;
   if (dgt::launch_attention(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return GEMM_ERR_CUDA;
-  const int64_t grid = problems * ceil_div(T, 128);
-  set_plan(h, GEMM_FAMILY_ATTENTION, 128, 128, 64, 1, 1, static_cast<int>(grid), 1, 0);
+  set_plan(h, GEMM_FAMILY_ATTENTION, 128, 128, 64, 1, 2, dgt::attention_grid(problems, T, h->sms), 1, 0);
   h->null_shape = dgt::last_main_launch();
   return GEMM_OK;
 }

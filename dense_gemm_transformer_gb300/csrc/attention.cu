@@ -8,20 +8,34 @@
 //     O[i] = sum_j softmax_j(scale * q_i . k_j) v_j     (j <= i when causal)
 //
 // with bf16 Q, K, V ([problems][T][64], rows of 64 contiguous elements) and
-// an fp32 O of the same shape.  One CTA per (problem, tile of 128 queries):
+// an fp32 O of the same shape.  The work items are (problem, tile of 128
+// queries), the tiles with the most key blocks first; a persistent grid of
+// two CTAs per SM takes them in turn, so that the copies for the next blocks
+// and the next item run while the current one computes.  Per CTA:
 //
-//   warp 0      TMA producer: the Q tile once, then per block of 128 keys the
-//               K block and the V block (128-byte swizzled rows of 64 bf16);
-//   warp 1      allocates TMEM (S: 128 fp32 columns, O: 64), then one lane
-//               issues S = Q K^T (M 128, N 128, K 64) and O += P V (M 128,
-//               N 64, K 128: P from shared memory, V read MN-major);
-//   warps 2-5   the softmax: warp w owns TMEM lane quarter w % 4, one query
-//               row per thread.  Per key block: read S from TMEM (scale,
-//               causal mask), update the running maximum m and sum l, rescale
-//               O in TMEM by 2^(m_old - m_new) when m grew (after the previous
-//               P V has completed), and write P = 2^(s - m) as bf16 into the
-//               K-major, 128-byte-swizzled layout the P V MMA reads.  At the
-//               end O / l is read from TMEM and stored.
+//   warp 0      TMA producer: per item the Q tile (two buffers), then per
+//               block of 64 keys the K and V blocks (rings of four), all as
+//               128-byte swizzled rows of 64 bf16;
+//   warp 1      allocates TMEM (two S buffers of 64 fp32 columns, O: 64,
+//               two P buffers of 32), then one lane issues S = Q K^T (M 128,
+//               N 64, K 64) and O += P V (M 128, N 64, K 64: P read from
+//               TMEM, V from shared memory MN-major).  S runs two blocks
+//               ahead of P V, so the softmax finds the next S ready and
+//               rarely waits for a P V to finish;
+//   warps 2-9   the softmax, two warps per TMEM lane quarter (warp w owns
+//               rows 32 (w % 4) .. of the tile, one per thread, and half
+//               (w - 2) / 4 of every key block).  Per key block: read its
+//               half of the row of S from TMEM (and release S), take the
+//               maximum (scale, causal mask) and combine it with the other
+//               half's, write P = 2^(scale s - m) as bf16 pairs into TMEM,
+//               and add the fp32 weights to its share of the row sum l.
+//               The running maximum m is raised only when a block's maximum
+//               exceeds it by more than kSlack (then O in TMEM and l are
+//               rescaled by 2^(m_old - m_new)); otherwise the weights stay
+//               below 2^kSlack, which bf16 and fp32 hold without loss of
+//               relative precision, and O / l is unchanged.  At the end of
+//               an item each warp reads its half of O, the two shares of l
+//               are added, and O / l is stored.
 //
 // Exponentials are base 2 with log2(e) folded into the scale.  The row sum
 // l adds the fp32 weights; the P V product uses them rounded to bf16.
@@ -40,22 +54,44 @@
 namespace dgt {
 namespace {
 
-constexpr int kAttnThreads = 192;  // producer, MMA, four softmax warps
+constexpr int kAttnThreads = 320;  // producer, MMA, eight softmax warps
 constexpr int kAttnD = 64;         // head dimension (one 128-byte bf16 row)
-constexpr int kAttnBQ = 128;       // queries per CTA (UMMA M)
-constexpr int kAttnBK = 128;       // keys per block (UMMA N of S, K of P V)
-constexpr int kTileBytes = kAttnBQ * 128;             // 128 rows x 128 bytes
-constexpr int kSmemBytes = 5 * kTileBytes + 1024 + 256;  // Q, K, V, P (two tiles), align, barriers
-constexpr int kTmemCols = 256;                         // S [0, 128), O [128, 192)
+constexpr int kAttnBQ = 128;       // queries per item (UMMA M)
+constexpr int kAttnBK = 64;        // keys per block (UMMA N of S, K of P V)
+constexpr int kQBytes = kAttnBQ * 128;   // 128 rows x 128 bytes
+constexpr int kKVBytes = kAttnBK * 128;  // 64 rows x 128 bytes
+constexpr int kQBufs = 2;                // Q buffers
+constexpr int kKVStages = 4;             // K and V ring stages
+constexpr int kNumBars = 2 * kQBufs + 4 * kKVStages + 14;
+constexpr int kXchgBytes = 2 * 2 * kAttnBQ * 4;  // two rounds x two halves x one float per row
+constexpr int kSmemBytes = kQBufs * kQBytes + 2 * kKVStages * kKVBytes + kXchgBytes + 1024 + 8 * kNumBars + 16;
+constexpr int kCtasPerSm = 2;
+constexpr int kTmemCols = 256;  // S0 [0, 64), S1 [64, 128), O [128, 192), P0 [192, 224), P1 [224, 256)
+constexpr int kSCol = 0;         // S of block n: kSCol + 64 (n % 2)
 constexpr int kOCol = 128;
+constexpr int kPCol = 192;       // P of block n: kPCol + 32 (n % 2)
+constexpr float kSlack = 8.f;   // log2 of the largest weight a stale maximum allows
 
 struct AttnParams {
-  int problems, T, q_tiles, causal;
+  int problems, T, q_tiles, k_blocks, causal, items;
   float scale_log2;  // scale * log2(e)
   float* O;
   int* status;
   uint64_t wait_ns;
 };
+
+struct Item {
+  int problem, qt, blocks;
+};
+
+__device__ __forceinline__ Item decode_item(const AttnParams& p, int w) {
+  Item it;
+  it.problem = w % p.problems;
+  it.qt = p.q_tiles - 1 - w / p.problems;
+  const int seen = (it.qt + 1) * (kAttnBQ / kAttnBK);  // blocks up to the tile's last query
+  it.blocks = (p.causal && seen < p.k_blocks) ? seen : p.k_blocks;
+  return it;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -67,7 +103,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // (so that the warp-collective TMEM accesses after it stay converged).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status, int code,
                                           uint64_t limit) {
-  const bool ok = mbar_wait(bar, parity, abort, status, code, limit);
+  const bool ok = mbar_wait_sleep(bar, parity, abort, status, code, limit);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -75,10 +111,6 @@ __device__ __forceinline__ float exp2_fast(float x) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // 3-D tiled load (one box of the [problems][T][64] tensor) completing on `bar`.
@@ -91,36 +123,62 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1)
+// Bounded drain of the last of `n` phases of `bar` (nothing when n == 0).
+__device__ __forceinline__ void drain_last(uint32_t bar, uint32_t n, int* status, uint64_t limit) {
+  if (n > 0) drain_wait(bar, (n - 1) & 1u, status, limit);
+}
+
+__global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
     attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t q_s = smem_u32(smem), k_s = q_s + kTileBytes, v_s = k_s + kTileBytes, p_s = v_s + kTileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 5 * kTileBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  const uint32_t q_s = smem_u32(smem), k_s = q_s + kQBufs * kQBytes, v_s = k_s + kKVStages * kKVBytes;
+  float* xchg = reinterpret_cast<float*>(smem + kQBufs * kQBytes + 2 * kKVStages * kKVBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBufs * kQBytes + 2 * kKVStages * kKVBytes + kXchgBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t q_full = bar0, k_full = bar0 + 8, k_empty = bar0 + 16, v_full = bar0 + 24, v_empty = bar0 + 32,
-                 s_full = bar0 + 40, s_free = bar0 + 48, p_full = bar0 + 56, o_full = bar0 + 64, drain = bar0 + 72;
+  auto q_full = [&](uint32_t b) { return bar0 + 8 * b; };
+  auto q_empty = [&](uint32_t b) { return bar0 + 8 * (kQBufs + b); };
+  const uint32_t kv0 = bar0 + 8 * (2 * kQBufs);
+  auto k_full = [&](uint32_t s) { return kv0 + 8 * s; };
+  auto k_empty = [&](uint32_t s) { return kv0 + 8 * (kKVStages + s); };
+  auto v_full = [&](uint32_t s) { return kv0 + 8 * (2 * kKVStages + s); };
+  auto v_empty = [&](uint32_t s) { return kv0 + 8 * (3 * kKVStages + s); };
+  // per S / P buffer x (block n uses x = n % 2, phase n / 2): S written,
+  // S read, P written, P V done; then the item's O read out, and the drain
+  const uint32_t sp0 = kv0 + 8 * (4 * kKVStages);
+  auto s_full = [&](uint32_t x) { return sp0 + 8 * x; };
+  auto s_free = [&](uint32_t x) { return sp0 + 8 * (2 + x); };
+  auto p_full = [&](uint32_t x) { return sp0 + 8 * (4 + x); };
+  auto pv_done = [&](uint32_t x) { return sp0 + 8 * (6 + x); };
+  const uint32_t o_empty = sp0 + 64, drain = sp0 + 72;
+  // the two softmax warps of lane quarter q exchange row values through
+  // xchg, each round on x_bar(q) (one arrival per warp)
+  auto x_bar = [&](uint32_t q) { return sp0 + 80 + 8 * q; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // the grid runs the last query tiles of every problem first: under the
-  // causal mask they have the most key blocks (longest work first)
-  const int problem = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.problems));
-  const int qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x / static_cast<unsigned>(p.problems));
-  const int key_blocks = p.causal ? qt + 1 : (p.T + kAttnBK - 1) / kAttnBK;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(k_full, 1);
-    mbar_init(k_empty, 1);
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 4);
-    mbar_init(p_full, 4);
-    mbar_init(o_full, 1);
+    for (int b = 0; b < kQBufs; ++b) {
+      mbar_init(q_full(b), 1);
+      mbar_init(q_empty(b), 1);
+    }
+    for (int s = 0; s < kKVStages; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(s_full(x), 1);
+      mbar_init(s_free(x), 8);
+      mbar_init(p_full(x), 8);
+      mbar_init(pv_done(x), 1);
+    }
+    mbar_init(o_empty, 8);
+    for (int q = 0; q < 4; ++q) mbar_init(x_bar(q), 2);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -145,69 +203,143 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t k_issued = 0, v_issued = 0;
+      uint32_t nq = 0, nk = 0, nv = 0;  // copies issued
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_3d(q_s, &tmQ, q_full, 0, qt * kAttnBQ, problem);
-      for (int j = 0; j < key_blocks && ok; ++j) {
-        const uint32_t ph = static_cast<uint32_t>(j) & 1u;
-        // K block j once S_{j-1} has read K_{j-1}; V block j once P_{j-1} V_{j-1} has read V_{j-1}
-        if (!mbar_wait(k_empty, ph ^ 1u, abort_flag, p.status, kDevTimeoutEmpty, p.wait_ns)) {
-          ok = false;
+      for (int w = blockIdx.x; w < p.items && ok; w += gridDim.x) {
+        const Item it = decode_item(p, w);
+        const uint32_t qb = nq % kQBufs;
+        if (!mbar_wait(q_empty(qb), ((nq / kQBufs) & 1u) ^ 1u, abort_flag, p.status, kDevTimeoutEmpty,
+                             p.wait_ns))
           break;
+        mbar_arrive_expect_tx(q_full(qb), kQBytes);
+        tma_load_3d(q_s + qb * kQBytes, &tmQ, q_full(qb), 0, it.qt * kAttnBQ, it.problem);
+        ++nq;
+        for (int j = 0; j < it.blocks; ++j) {
+          const uint32_t st = nk % kKVStages, ph = ((nk / kKVStages) & 1u) ^ 1u;
+          if (!mbar_wait(k_empty(st), ph, abort_flag, p.status, kDevTimeoutEmpty, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(k_full(st), kKVBytes);
+          tma_load_3d(k_s + st * kKVBytes, &tmK, k_full(st), 0, j * kAttnBK, it.problem);
+          ++nk;
+          if (!mbar_wait(v_empty(st), ph, abort_flag, p.status, kDevTimeoutEmpty, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(v_full(st), kKVBytes);
+          tma_load_3d(v_s + st * kKVBytes, &tmV, v_full(st), 0, j * kAttnBK, it.problem);
+          ++nv;
         }
-        mbar_arrive_expect_tx(k_full, kTileBytes);
-        tma_load_3d(k_s, &tmK, k_full, 0, j * kAttnBK, problem);
-        ++k_issued;
-        if (!mbar_wait(v_empty, ph ^ 1u, abort_flag, p.status, kDevTimeoutEmpty, p.wait_ns)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(v_full, kTileBytes);
-        tma_load_3d(v_s, &tmV, v_full, 0, j * kAttnBK, problem);
-        ++v_issued;
       }
-      // every copy lands before the CTA exits (the consumers normally waited
-      // for all of them already)
-      drain_wait(q_full, 0, p.status, p.wait_ns);
-      if (k_issued > 0) drain_wait(k_full, (k_issued - 1) & 1u, p.status, p.wait_ns);
-      if (v_issued > 0) drain_wait(v_full, (v_issued - 1) & 1u, p.status, p.wait_ns);
+      // every copy lands before the CTA exits: the last phase of each buffer
+      for (uint32_t b = 0; b < kQBufs; ++b) drain_last(q_full(b), (nq + kQBufs - 1 - b) / kQBufs, p.status, p.wait_ns);
+      for (uint32_t s = 0; s < kKVStages; ++s) {
+        drain_last(k_full(s), (nk + kKVStages - 1 - s) / kKVStages, p.status, p.wait_ns);
+        drain_last(v_full(s), (nv + kKVStages - 1 - s) / kKVStages, p.status, p.wait_ns);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One lane walks the CTA's key blocks twice, two blocks apart: P V of
+    // block n, then S of block n + 2 (possibly the next item's) into the S
+    // buffer the softmax read for block n.  Each chain of four MMAs is
+    // issued back to back from descriptors built once per block (the K
+    // steps only add constant offsets): a single issuing thread that
+    // rebuilds 64-bit descriptors between MMAs cannot keep the tensor pipe
+    // fed at these sizes.
     if (lane == 0) {
       const uint32_t idesc_s = make_idesc(1, false, false, kAttnBQ, kAttnBK);  // bf16, both K-major
       const uint32_t idesc_o = make_idesc(1, false, true, kAttnBQ, kAttnD);    // V read MN-major
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status, kDevTimeoutFull, p.wait_ns);
-      for (int j = 0; j < key_blocks && ok; ++j) {
-        const uint32_t ph = static_cast<uint32_t>(j) & 1u;
-        // S_j = Q K_j^T, once K_j is in and the softmax has read S_{j-1}
-        if (!mbar_wait(k_full, ph, abort_flag, p.status, kDevTimeoutFull, p.wait_ns) ||
-            (j > 0 && !mbar_wait(s_free, ph ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty, p.wait_ns))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      // S cursor: item ws, block js; ns blocks and nis items begun so far
+      int ws = blockIdx.x, js = 0;
+      Item its = decode_item(p, ws < p.items ? ws : 0);
+      uint32_t ns = 0, nis = 0;
+      // P V cursor
+      int wp = blockIdx.x, jp = 0;
+      Item itp = its;
+      uint32_t np = 0, nip = 0;
+      bool ok = true;
+      // Q of a new item, K of the block, and its S buffer read (block n - 2)
+      auto wait_s = [&]() -> bool {
+        const uint32_t qb = nis % kQBufs, st = ns % kKVStages, x = ns & 1u;
+        return (js != 0 || mbar_wait(q_full(qb), (nis / kQBufs) & 1u, abort_flag, p.status, kDevTimeoutFull,
+                                     p.wait_ns)) &&
+               mbar_wait(k_full(st), (ns / kKVStages) & 1u, abort_flag, p.status, kDevTimeoutFull, p.wait_ns) &&
+               mbar_wait(s_free(x), ((ns >> 1) & 1u) ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty, p.wait_ns);
+      };
+      // the previous item's O read out, P of the block written (and O
+      // rescaled), V of the block in
+      auto wait_pv = [&]() -> bool {
+        const uint32_t st = np % kKVStages, x = np & 1u;
+        return (jp != 0 || mbar_wait(o_empty, (nip & 1u) ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty,
+                                     p.wait_ns)) &&
+               mbar_wait(p_full(x), (np >> 1) & 1u, abort_flag, p.status, kDevTimeoutFull, p.wait_ns) &&
+               mbar_wait(v_full(st), (np / kKVStages) & 1u, abort_flag, p.status, kDevTimeoutFull, p.wait_ns);
+      };
+      // the four MMAs of S (block ns) and of P V (block np); a K step of
+      // 16 elements advances a K-major descriptor by 32 bytes (2 in its
+      // address field) and V's MN-major one by 16 rows (2048 bytes, 128)
+      auto mma_s = [&]() {
+        const uint64_t ad = smem_desc_sw128(q_s + (nis % kQBufs) * kQBytes, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(k_s + (ns % kKVStages) * kKVBytes, 16, 1024);
+        const uint32_t d = tmem + kSCol + 64 * (ns & 1u);
+        mma_bf16(d, ad, bd, idesc_s, 0u);
 #pragma unroll
-        for (int k = 0; k < kAttnD / 16; ++k)
-          mma_bf16(tmem, smem_desc_sw128(q_s + 32 * k, 16, 1024), smem_desc_sw128(k_s + 32 * k, 16, 1024), idesc_s,
-                   k > 0 ? 1u : 0u);
-        mma_commit(k_empty);
-        mma_commit(s_full);
-        // O += P_j V_j, once the softmax has written P_j (and rescaled O)
-        if (!mbar_wait(p_full, ph, abort_flag, p.status, kDevTimeoutFull, p.wait_ns) ||
-            !mbar_wait(v_full, ph, abort_flag, p.status, kDevTimeoutFull, p.wait_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        for (int k = 1; k < kAttnD / 16; ++k) mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc_s, 1u);
+      };
+      auto mma_pv = [&]() {
+        const uint64_t vd = smem_desc_sw128(v_s + (np % kKVStages) * kKVBytes, kKVBytes, 1024);
+        const uint32_t a = tmem + kPCol + 32 * (np & 1u), d = tmem + kOCol;
+        mma_bf16_tmem_a(d, a, vd, idesc_o, jp > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < kAttnBK / 16; ++k)
-          mma_bf16(tmem + kOCol,
-                   smem_desc_sw128(p_s + (k >> 2) * kTileBytes + 32 * (k & 3), 16, 1024),
-                   smem_desc_sw128(v_s + 16 * 128 * k, kTileBytes, 1024), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(v_empty);
-        mma_commit(o_full);
+        for (int k = 1; k < kAttnBK / 16; ++k) mma_bf16_tmem_a(d, a + 8 * k, vd + 128 * k, idesc_o, 1u);
+      };
+      // commits once the block's MMAs are issued, then the cursors move on
+      auto done_s = [&]() {
+        const uint32_t qb = nis % kQBufs;
+        mma_commit(k_empty(ns % kKVStages));
+        mma_commit(s_full(ns & 1u));
+        ++ns;
+        if (++js == its.blocks) {
+          mma_commit(q_empty(qb));  // the item's last S has read its Q
+          js = 0;
+          ++nis;
+          ws += gridDim.x;
+          if (ws < p.items) its = decode_item(p, ws);
+        }
+      };
+      auto done_pv = [&]() {
+        mma_commit(v_empty(np % kKVStages));
+        mma_commit(pv_done(np & 1u));
+        ++np;
+        if (++jp == itp.blocks) {
+          jp = 0;
+          ++nip;
+          wp += gridDim.x;
+          if (wp < p.items) itp = decode_item(p, wp);
+        }
+      };
+      // S of the first two blocks alone
+      for (int i = 0; i < 2 && ok && ws < p.items; ++i) {
+        ok = wait_s();
+        if (!ok) break;
+        tc_fence_after();
+        mma_s();
+        done_s();
+      }
+      // then P V of block n and S of block n + 2
+      while (ok && wp < p.items) {
+        if (!wait_pv()) break;
+        tc_fence_after();
+        mma_pv();
+        done_pv();
+        if (ws < p.items) {
+          if (!wait_s()) break;
+          tc_fence_after();
+          mma_s();
+          done_s();
+        }
       }
       // every MMA this thread issued has completed once drain flips
       mma_commit(drain);
@@ -215,116 +347,163 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int quarter = warp & 3;
+    // Warp w (2..9) owns TMEM lane quarter w % 4 (rows 32 (w % 4) ..) and
+    // half h = (w - 2) / 4 of every key block (keys 32 h .. 32 h + 31), of
+    // P (words 16 h ..) and of O (columns 32 h ..).  The two warps of a
+    // quarter combine their row maxima every block and their row sums at
+    // the end of an item.
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // this thread's query row in the tile
-    const int q_row = qt * kAttnBQ + r;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    float m = -__int_as_float(0x7f800000), l = 0.f;
+    const uint32_t xb = x_bar(static_cast<uint32_t>(quarter));
+    const float c = p.scale_log2;
+    const float kNegInf = -__int_as_float(0x7f800000);
+    constexpr int kHalf = kAttnBK / 2;
+    uint32_t nb = 0, nx = 0;  // blocks, exchange rounds
     bool ok = true;
-    for (int j = 0; j < key_blocks; ++j) {
-      const uint32_t ph = static_cast<uint32_t>(j) & 1u;
-      if (!warp_wait(s_full, ph, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // keys this row sees in block j: [0, limit)
-      const int key0 = j * kAttnBK;
-      int limit = p.T - key0;
-      if (p.causal && q_row - key0 + 1 < limit) limit = q_row - key0 + 1;
-      limit = limit < 0 ? 0 : (limit > kAttnBK ? kAttnBK : limit);
-      // pass 1: the row maximum of this block (scaled, log2 units)
-      float bmax = -__int_as_float(0x7f800000);
-#pragma unroll 1
-      for (int c = 0; c < kAttnBK; c += 32) {
-        uint32_t s[32];
-        __syncwarp();
-        tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(c), s);
-        tmem_wait_ld();
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (c + t < limit) bmax = fmaxf(bmax, __uint_as_float(s[t]) * p.scale_log2);
-      }
-      const float m_new = fmaxf(m, bmax);
-      const float alpha = exp2_fast(m - m_new);  // 0 on the first block (m = -inf)
-      // P_{j-1} V_{j-1} must be done before O is rescaled and P is rewritten
-      if (j > 0 && !warp_wait(o_full, ph ^ 1u, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // pass 2: P = 2^(s - m_new) as bf16 into the P tile (K-major, 128-byte
-      // swizzle: keys 64 h .. 64 h + 63 in tile h, row r at r * 128, 16-byte
-      // chunk u at (u ^ (r % 8)) * 16), and the row sum
-      float bsum = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < kAttnBK; c += 32) {
-        uint32_t s[32];
-        __syncwarp();
-        tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(c), s);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          const float p0 = (c + t < limit) ? exp2_fast(__uint_as_float(s[t]) * p.scale_log2 - m_new) : 0.f;
-          const float p1 = (c + t + 1 < limit) ? exp2_fast(__uint_as_float(s[t + 1]) * p.scale_log2 - m_new) : 0.f;
-          bsum += p0 + p1;
-          pk[t / 2] = pack_bf16x2(p0, p1);
-        }
-        const uint32_t tile = p_s + static_cast<uint32_t>((c >> 6) * kTileBytes + r * 128);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = ((c & 63) >> 3) + u;  // 16-byte chunk of the 128-byte row
-          st_shared_v4(tile + static_cast<uint32_t>(((chunk ^ (r & 7)) << 4)), pk[4 * u], pk[4 * u + 1],
-                       pk[4 * u + 2], pk[4 * u + 3]);
-        }
-      }
-      // S may be overwritten now
-      tc_fence_before();
+    // one exchange round: publish v, return the partner's value (false when
+    // a wait gave up)
+    auto exchange = [&](float v, float& other) -> bool {
+      float* slot = xchg + (nx & 1u) * (2 * kAttnBQ);
+      slot[half * kAttnBQ + r] = v;
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
-      l = l * alpha + bsum;
-      m = m_new;
-      // O *= alpha (O holds the previous blocks' P V; skip when no row of
-      // this warp grew its maximum)
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (lane == 0) mbar_arrive(xb);
+      const bool got = warp_wait(xb, nx & 1u, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns);
+      if (got) other = slot[(half ^ 1) * kAttnBQ + r];
+      ++nx;
+      return got;
+    };
+    for (int w = blockIdx.x; w < p.items && ok; w += gridDim.x) {
+      const Item it = decode_item(p, w);
+      const int q_row = it.qt * kAttnBQ + r;
+      float m = kNegInf, l = 0.f;  // l: this half's share of the row sum
+      for (int j = 0; j < it.blocks; ++j, ++nb) {
+        const uint32_t x = nb & 1u, xph = (nb >> 1) & 1u;
+        if (!warp_wait(s_full(x), xph, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // this half of the row of S; then release S for the block after next
+        uint32_t s[kHalf];
+        tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kSCol + 64 * x + kHalf * half), s);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free(x));
+        // keys of this half the row sees: [0, limit)
+        const int key0 = j * kAttnBK + kHalf * half;
+        int limit = p.T - key0;
+        if (p.causal && q_row - key0 + 1 < limit) limit = q_row - key0 + 1;
+        limit = limit < 0 ? 0 : (limit > kHalf ? kHalf : limit);
+        const bool whole = __all_sync(0xffffffffu, limit == kHalf);
+        // the half's maximum of c s (log2 units): the largest s for c >= 0,
+        // the smallest for c < 0 (masked keys never win), in eight chains
+        float e8[8];
+        if (whole) {
 #pragma unroll
-        for (int c = 0; c < kAttnD; c += 32) {
+          for (int q = 0; q < 8; ++q) e8[q] = __uint_as_float(s[q]);
+          if (c >= 0.f) {
+#pragma unroll
+            for (int t = 8; t < kHalf; ++t) e8[t & 7] = fmaxf(e8[t & 7], __uint_as_float(s[t]));
+          } else {
+#pragma unroll
+            for (int t = 8; t < kHalf; ++t) e8[t & 7] = fminf(e8[t & 7], __uint_as_float(s[t]));
+          }
+        } else {
+          const float none = c >= 0.f ? kNegInf : -kNegInf;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) e8[q] = none;
+#pragma unroll
+          for (int t = 0; t < kHalf; ++t) {
+            const float v = t < limit ? __uint_as_float(s[t]) : none;
+            e8[t & 7] = c >= 0.f ? fmaxf(e8[t & 7], v) : fminf(e8[t & 7], v);
+          }
+        }
+#pragma unroll
+        for (int q = 4; q > 0; q >>= 1)
+#pragma unroll
+          for (int i = 0; i < q; ++i) e8[i] = c >= 0.f ? fmaxf(e8[i], e8[i + q]) : fminf(e8[i], e8[i + q]);
+        const float hmax = limit > 0 ? e8[0] * c : kNegInf;
+        float omax = kNegInf;
+        if (!exchange(hmax, omax)) {
+          ok = false;
+          break;
+        }
+        const float bmax = fmaxf(hmax, omax);
+        // raise the running maximum only past the slack (always on the
+        // first block, where m = -inf); both warps of the quarter see the
+        // same bmax and m for every row, so they decide alike
+        const bool raise = __any_sync(0xffffffffu, bmax > m + kSlack);
+        const float m_new = raise ? fmaxf(m, bmax) : m;
+        const float alpha = raise ? exp2_fast(m - m_new) : 1.f;  // 0 when m = -inf
+        // P = 2^(c s - m_new) as bf16 pairs (key 2u in the low half of word
+        // u) and this half's sum of the fp32 weights (four partial sums)
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[kHalf / 2];
+#pragma unroll
+        for (int u = 0; u < kHalf / 2; ++u) {
+          float p0 = exp2_fast(fmaf(__uint_as_float(s[2 * u]), c, -m_new));
+          float p1 = exp2_fast(fmaf(__uint_as_float(s[2 * u + 1]), c, -m_new));
+          if (!whole) {
+            p0 = 2 * u < limit ? p0 : 0.f;
+            p1 = 2 * u + 1 < limit ? p1 : 0.f;
+          }
+          ps[u & 3] += p0 + p1;
+          pk[u] = pack_bf16x2(p0, p1);
+        }
+        const float bsum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        // P buffer x is free once P V of block n - 2 is done; O may be
+        // rescaled once P V of block n - 1 is done
+        if (!warp_wait(pv_done(x), xph ^ 1u, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns) ||
+            (raise && j > 0 &&
+             !warp_wait(pv_done(x ^ 1u), ((nb - 1) >> 1) & 1u, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st_32x32b_x16(tmem + lane_addr + static_cast<uint32_t>(kPCol + 32 * x + (kHalf / 2) * half), pk);
+        l = l * alpha + bsum;
+        m = m_new;
+        // this half of O *= alpha when the maximum was raised after the
+        // first block
+        if (raise && j > 0) {
           uint32_t o[32];
-          tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + c), o);
+          tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + 32 * half), o);
           tmem_wait_ld();
 #pragma unroll
           for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-          tmem_st_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + c), o);
+          tmem_st_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + 32 * half), o);
         }
+        // P and O visible to the next MMAs
         tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(x));
       }
-      // P (generic-proxy stores) and O visible to the next MMAs
-      fence_proxy_async_smem();
+      if (!ok) break;
+      // the item's last P V, then this half of O / l to global memory; O's
+      // columns are free for the next item once read
+      if (!warp_wait(pv_done((nb - 1) & 1u), ((nb - 1) >> 1) & 1u, abort_flag, p.status, kDevTimeoutAccFull,
+                     p.wait_ns))
+        break;
+      tc_fence_after();
+      uint32_t o[32];
+      tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + 32 * half), o);
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    // the last P V, then O / l to global memory
-    if (ok && key_blocks > 0 &&
-        warp_wait(o_full, static_cast<uint32_t>(key_blocks - 1) & 1u, abort_flag, p.status, kDevTimeoutAccFull,
-                  p.wait_ns)) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      float* out = p.O + (static_cast<int64_t>(problem) * p.T + q_row) * kAttnD;
+      if (lane == 0) mbar_arrive(o_empty);
+      float l_other = 0.f;
+      if (!exchange(l, l_other)) break;
+      if (q_row < p.T) {
+        const float inv_l = 1.f / (half == 0 ? l + l_other : l_other + l);
+        float* out = p.O + (static_cast<int64_t>(it.problem) * p.T + q_row) * kAttnD + 32 * half;
 #pragma unroll
-      for (int c = 0; c < kAttnD; c += 32) {
-        uint32_t o[32];
-        __syncwarp();
-        tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + c), o);
-        tmem_wait_ld();
-        if (q_row < p.T) {
-#pragma unroll
-          for (int t = 0; t < 32; t += 4)
-            *reinterpret_cast<float4*>(out + c + t) =
-                make_float4(__uint_as_float(o[t]) * inv_l, __uint_as_float(o[t + 1]) * inv_l,
-                            __uint_as_float(o[t + 2]) * inv_l, __uint_as_float(o[t + 3]) * inv_l);
-        }
+        for (int t = 0; t < 32; t += 4)
+          *reinterpret_cast<float4*>(out + t) =
+              make_float4(__uint_as_float(o[t]) * inv_l, __uint_as_float(o[t + 1]) * inv_l,
+                          __uint_as_float(o[t + 2]) * inv_l, __uint_as_float(o[t + 3]) * inv_l);
       }
     }
   }
@@ -338,14 +517,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 }
 
-// [problems][T][64] bf16 as a 3-D tensor map, boxes of 64 x 128 x 1,
+// [problems][T][64] bf16 as a 3-D tensor map, boxes of 64 x `rows` x 1,
 // 128-byte swizzle; rows past T read as zeros.
 CUresult encode_qkv(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m, const void* ptr, int64_t problems,
-                    int64_t T) {
+                    int64_t T, uint32_t rows) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kAttnD), static_cast<cuuint64_t>(T),
                         static_cast<cuuint64_t>(problems)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(kAttnD) * 2, static_cast<cuuint64_t>(T) * kAttnD * 2};
-  cuuint32_t box[3] = {kAttnD, kAttnBQ, 1};
+  cuuint32_t box[3] = {kAttnD, rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -354,15 +533,21 @@ CUresult encode_qkv(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap* m, co
 
 }  // namespace
 
+int attention_grid(int64_t problems, int64_t T, int sms) {
+  const int64_t items = problems * ((T + kAttnBQ - 1) / kAttnBQ);
+  const int64_t slots = static_cast<int64_t>(kCtasPerSm) * (sms > 0 ? sms : 1);
+  return static_cast<int>(items < slots ? items : slots);
+}
+
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   cudaError_t e = tc_init_driver();
   if (e != cudaSuccess) return e;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tc_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
   CUtensorMap tq, tk, tv;
-  if (encode_qkv(encode, &tq, a.Q, a.problems, a.T) != CUDA_SUCCESS ||
-      encode_qkv(encode, &tk, a.K, a.problems, a.T) != CUDA_SUCCESS ||
-      encode_qkv(encode, &tv, a.V, a.problems, a.T) != CUDA_SUCCESS)
+  if (encode_qkv(encode, &tq, a.Q, a.problems, a.T, kAttnBQ) != CUDA_SUCCESS ||
+      encode_qkv(encode, &tk, a.K, a.problems, a.T, kAttnBK) != CUDA_SUCCESS ||
+      encode_qkv(encode, &tv, a.V, a.problems, a.T, kAttnBK) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   static std::atomic<uint64_t> attr_done{0};
   e = once_per_device(attr_done, [] {
@@ -373,12 +558,14 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream) {
   p.problems = static_cast<int>(a.problems);
   p.T = static_cast<int>(a.T);
   p.q_tiles = static_cast<int>((a.T + kAttnBQ - 1) / kAttnBQ);
+  p.k_blocks = static_cast<int>((a.T + kAttnBK - 1) / kAttnBK);
   p.causal = a.causal ? 1 : 0;
+  p.items = static_cast<int>(a.problems * p.q_tiles);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.O = a.O;
   p.status = a.status;
   p.wait_ns = a.wait_ns > 0 ? a.wait_ns : kWaitLimitNs;
-  const int64_t grid = a.problems * p.q_tiles;
+  const int grid = attention_grid(a.problems, a.T, a.sms);
   last_main_launch() = LaunchShape{dim3(static_cast<unsigned>(grid)), dim3(kAttnThreads), kSmemBytes, 1, true};
   return launch_pdl(attention_fwd_kernel, dim3(static_cast<unsigned>(grid)), dim3(kAttnThreads), kSmemBytes, stream,
                     tq, tk, tv, p);

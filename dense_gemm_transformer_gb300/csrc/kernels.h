@@ -192,8 +192,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_encoder();
 // ---------------------------------------------------------------- attention
 // Fused scaled dot-product attention forward over `problems` independent
 // (batch element, head) problems: Q, K, V bf16 [problems][T][64] (rows of 64
-// contiguous elements, 16-byte aligned), O fp32 of the same shape.  One CTA
-// per (problem, 128 queries); scores stay in tensor memory.
+// contiguous elements, 16-byte aligned), O fp32 of the same shape.  A
+// persistent grid of two CTAs per SM takes the (problem, 128 queries) items
+// in turn; scores stay in tensor memory.
 struct AttnArgs {
   int64_t problems, T;
   int causal;
@@ -202,8 +203,10 @@ struct AttnArgs {
   float* O;
   int* status;       // device status word (bounded waits)
   uint64_t wait_ns;  // 0: kWaitLimitNs
+  int sms;           // the device's SMs (the persistent grid: two CTAs per SM)
 };
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t stream);
+int attention_grid(int64_t problems, int64_t T, int sms);  // CTAs launch_attention starts
 
 // ---------------------------------------------------------------- helpers
 // C = epi(alpha * sum_s ws[s] + beta * C) over an M x N matrix (s

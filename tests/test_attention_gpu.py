@@ -100,6 +100,21 @@ def test_attention_gpt_size_sampled(h):
     _check(got, Q, K, V, True, problems=(P - 16, P), what=name)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_many_items_per_cta(h, causal):
+    """Far more (problem, query tile) items than CTAs, so that every CTA of
+    the persistent grid runs several in turn (Q buffers and the output
+    accumulator handed from one item to the next); ragged T; sampled."""
+    P, T = 700, 200
+    Q, K, V = si.attention_qkv(P, T, shape=7, std_q=2.0)
+    got = _run(h, Q, K, V, causal, guard=1024)
+    assert h.plan()["grid"] < P * 2
+    assert np.all(np.isfinite(got))
+    _check(got, Q, K, V, causal, problems=(0, 12), what="first")
+    _check(got, Q, K, V, causal, problems=(343, 351), what="middle")
+    _check(got, Q, K, V, causal, problems=(P - 12, P), what="last")
+
+
 @pytest.mark.parametrize("idx", [1, 2])
 def test_attention_long_context_sampled(h, idx):
     """Context 1024 and 2048 at full size; the first and last problems against the oracle."""
