@@ -22,20 +22,17 @@
 //               TMEM, V from shared memory MN-major).  S runs two blocks
 //               ahead of P V, so the softmax finds the next S ready and
 //               rarely waits for a P V to finish;
-//   warps 2-9   the softmax, two warps per TMEM lane quarter (warp w owns
-//               rows 32 (w % 4) .. of the tile, one per thread, and half
-//               (w - 2) / 4 of every key block).  Per key block: read its
-//               half of the row of S from TMEM (and release S), take the
-//               maximum (scale, causal mask) and combine it with the other
-//               half's, write P = 2^(scale s - m) as bf16 pairs into TMEM,
-//               and add the fp32 weights to its share of the row sum l.
-//               The running maximum m is raised only when a block's maximum
+//   warps 2-5   the softmax: warp w owns TMEM lane quarter w % 4, one query
+//               row per thread.  Per key block: read the row of S from TMEM
+//               into registers (and release S), take its maximum (scale,
+//               causal mask), write P = 2^(scale s - m) as bf16 pairs into
+//               TMEM, and add the fp32 weights to the row sum l.  The
+//               running maximum m is raised only when a block's maximum
 //               exceeds it by more than kSlack (then O in TMEM and l are
 //               rescaled by 2^(m_old - m_new)); otherwise the weights stay
 //               below 2^kSlack, which bf16 and fp32 hold without loss of
 //               relative precision, and O / l is unchanged.  At the end of
-//               an item each warp reads its half of O, the two shares of l
-//               are added, and O / l is stored.
+//               an item O / l is read from TMEM and stored.
 //
 // Exponentials are base 2 with log2(e) folded into the scale.  The row sum
 // l adds the fp32 weights; the P V product uses them rounded to bf16.
@@ -54,7 +51,7 @@
 namespace dgt {
 namespace {
 
-constexpr int kAttnThreads = 320;  // producer, MMA, eight softmax warps
+constexpr int kAttnThreads = 192;  // producer, MMA, four softmax warps
 constexpr int kAttnD = 64;         // head dimension (one 128-byte bf16 row)
 constexpr int kAttnBQ = 128;       // queries per item (UMMA M)
 constexpr int kAttnBK = 64;        // keys per block (UMMA N of S, K of P V)
@@ -62,9 +59,8 @@ constexpr int kQBytes = kAttnBQ * 128;   // 128 rows x 128 bytes
 constexpr int kKVBytes = kAttnBK * 128;  // 64 rows x 128 bytes
 constexpr int kQBufs = 2;                // Q buffers
 constexpr int kKVStages = 4;             // K and V ring stages
-constexpr int kNumBars = 2 * kQBufs + 4 * kKVStages + 14;
-constexpr int kXchgBytes = 2 * 2 * kAttnBQ * 4;  // two rounds x two halves x one float per row
-constexpr int kSmemBytes = kQBufs * kQBytes + 2 * kKVStages * kKVBytes + kXchgBytes + 1024 + 8 * kNumBars + 16;
+constexpr int kNumBars = 2 * kQBufs + 4 * kKVStages + 10;
+constexpr int kSmemBytes = kQBufs * kQBytes + 2 * kKVStages * kKVBytes + 1024 + 8 * kNumBars + 16;
 constexpr int kCtasPerSm = 2;
 constexpr int kTmemCols = 256;  // S0 [0, 64), S1 [64, 128), O [128, 192), P0 [192, 224), P1 [224, 256)
 constexpr int kSCol = 0;         // S of block n: kSCol + 64 (n % 2)
@@ -134,8 +130,7 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t q_s = smem_u32(smem), k_s = q_s + kQBufs * kQBytes, v_s = k_s + kKVStages * kKVBytes;
-  float* xchg = reinterpret_cast<float*>(smem + kQBufs * kQBytes + 2 * kKVStages * kKVBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBufs * kQBytes + 2 * kKVStages * kKVBytes + kXchgBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQBufs * kQBytes + 2 * kKVStages * kKVBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -154,9 +149,6 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
   auto p_full = [&](uint32_t x) { return sp0 + 8 * (4 + x); };
   auto pv_done = [&](uint32_t x) { return sp0 + 8 * (6 + x); };
   const uint32_t o_empty = sp0 + 64, drain = sp0 + 72;
-  // the two softmax warps of lane quarter q exchange row values through
-  // xchg, each round on x_bar(q) (one arrival per warp)
-  auto x_bar = [&](uint32_t q) { return sp0 + 80 + 8 * q; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -173,12 +165,11 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(s_full(x), 1);
-      mbar_init(s_free(x), 8);
-      mbar_init(p_full(x), 8);
+      mbar_init(s_free(x), 4);
+      mbar_init(p_full(x), 4);
       mbar_init(pv_done(x), 1);
     }
-    mbar_init(o_empty, 8);
-    for (int q = 0; q < 4; ++q) mbar_init(x_bar(q), 2);
+    mbar_init(o_empty, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -347,36 +338,19 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Warp w (2..9) owns TMEM lane quarter w % 4 (rows 32 (w % 4) ..) and
-    // half h = (w - 2) / 4 of every key block (keys 32 h .. 32 h + 31), of
-    // P (words 16 h ..) and of O (columns 32 h ..).  The two warps of a
-    // quarter combine their row maxima every block and their row sums at
-    // the end of an item.
-    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    // Warp w (2..5) owns TMEM lane quarter w % 4: rows 32 (w % 4) .. of the
+    // tile, one per thread.
+    const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // this thread's query row in the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t xb = x_bar(static_cast<uint32_t>(quarter));
     const float c = p.scale_log2;
     const float kNegInf = -__int_as_float(0x7f800000);
-    constexpr int kHalf = kAttnBK / 2;
-    uint32_t nb = 0, nx = 0;  // blocks, exchange rounds
+    uint32_t nb = 0;
     bool ok = true;
-    // one exchange round: publish v, return the partner's value (false when
-    // a wait gave up)
-    auto exchange = [&](float v, float& other) -> bool {
-      float* slot = xchg + (nx & 1u) * (2 * kAttnBQ);
-      slot[half * kAttnBQ + r] = v;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(xb);
-      const bool got = warp_wait(xb, nx & 1u, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns);
-      if (got) other = slot[(half ^ 1) * kAttnBQ + r];
-      ++nx;
-      return got;
-    };
     for (int w = blockIdx.x; w < p.items && ok; w += gridDim.x) {
       const Item it = decode_item(p, w);
       const int q_row = it.qt * kAttnBQ + r;
-      float m = kNegInf, l = 0.f;  // l: this half's share of the row sum
+      float m = kNegInf, l = 0.f;
       for (int j = 0; j < it.blocks; ++j, ++nb) {
         const uint32_t x = nb & 1u, xph = (nb >> 1) & 1u;
         if (!warp_wait(s_full(x), xph, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns)) {
@@ -384,20 +358,29 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
           break;
         }
         tc_fence_after();
-        // this half of the row of S; then release S for the block after next
-        uint32_t s[kHalf];
-        tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kSCol + 64 * x + kHalf * half), s);
-        tmem_wait_ld();
+        // the row of S: two loads, one wait; then release S for block n + 2
+        uint32_t s[kAttnBK];
+        {
+          uint32_t lo[32], hi[32];
+          tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kSCol + 64 * x), lo);
+          tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kSCol + 64 * x + 32), hi);
+          tmem_wait_ld();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            s[t] = lo[t];
+            s[32 + t] = hi[t];
+          }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free(x));
-        // keys of this half the row sees: [0, limit)
-        const int key0 = j * kAttnBK + kHalf * half;
+        // keys this row sees in block j: [0, limit)
+        const int key0 = j * kAttnBK;
         int limit = p.T - key0;
         if (p.causal && q_row - key0 + 1 < limit) limit = q_row - key0 + 1;
-        limit = limit < 0 ? 0 : (limit > kHalf ? kHalf : limit);
-        const bool whole = __all_sync(0xffffffffu, limit == kHalf);
-        // the half's maximum of c s (log2 units): the largest s for c >= 0,
+        limit = limit < 0 ? 0 : (limit > kAttnBK ? kAttnBK : limit);
+        const bool whole = __all_sync(0xffffffffu, limit == kAttnBK);
+        // the block's maximum of c s (log2 units): the largest s for c >= 0,
         // the smallest for c < 0 (masked keys never win), in eight chains
         float e8[8];
         if (whole) {
@@ -405,17 +388,17 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
           for (int q = 0; q < 8; ++q) e8[q] = __uint_as_float(s[q]);
           if (c >= 0.f) {
 #pragma unroll
-            for (int t = 8; t < kHalf; ++t) e8[t & 7] = fmaxf(e8[t & 7], __uint_as_float(s[t]));
+            for (int t = 8; t < kAttnBK; ++t) e8[t & 7] = fmaxf(e8[t & 7], __uint_as_float(s[t]));
           } else {
 #pragma unroll
-            for (int t = 8; t < kHalf; ++t) e8[t & 7] = fminf(e8[t & 7], __uint_as_float(s[t]));
+            for (int t = 8; t < kAttnBK; ++t) e8[t & 7] = fminf(e8[t & 7], __uint_as_float(s[t]));
           }
         } else {
           const float none = c >= 0.f ? kNegInf : -kNegInf;
 #pragma unroll
           for (int q = 0; q < 8; ++q) e8[q] = none;
 #pragma unroll
-          for (int t = 0; t < kHalf; ++t) {
+          for (int t = 0; t < kAttnBK; ++t) {
             const float v = t < limit ? __uint_as_float(s[t]) : none;
             e8[t & 7] = c >= 0.f ? fmaxf(e8[t & 7], v) : fminf(e8[t & 7], v);
           }
@@ -424,25 +407,19 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
         for (int q = 4; q > 0; q >>= 1)
 #pragma unroll
           for (int i = 0; i < q; ++i) e8[i] = c >= 0.f ? fmaxf(e8[i], e8[i + q]) : fminf(e8[i], e8[i + q]);
-        const float hmax = limit > 0 ? e8[0] * c : kNegInf;
-        float omax = kNegInf;
-        if (!exchange(hmax, omax)) {
-          ok = false;
-          break;
-        }
-        const float bmax = fmaxf(hmax, omax);
+        const float bmax = limit > 0 ? e8[0] * c : kNegInf;
         // raise the running maximum only past the slack (always on the
-        // first block, where m = -inf); both warps of the quarter see the
-        // same bmax and m for every row, so they decide alike
+        // first block, where m = -inf); the warp decides together, since
+        // the rescale of O is warp-collective
         const bool raise = __any_sync(0xffffffffu, bmax > m + kSlack);
         const float m_new = raise ? fmaxf(m, bmax) : m;
         const float alpha = raise ? exp2_fast(m - m_new) : 1.f;  // 0 when m = -inf
         // P = 2^(c s - m_new) as bf16 pairs (key 2u in the low half of word
-        // u) and this half's sum of the fp32 weights (four partial sums)
+        // u) and the row sum of the fp32 weights (four partial sums)
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[kHalf / 2];
+        uint32_t pk[kAttnBK / 2];
 #pragma unroll
-        for (int u = 0; u < kHalf / 2; ++u) {
+        for (int u = 0; u < kAttnBK / 2; ++u) {
           float p0 = exp2_fast(fmaf(__uint_as_float(s[2 * u]), c, -m_new));
           float p1 = exp2_fast(fmaf(__uint_as_float(s[2 * u + 1]), c, -m_new));
           if (!whole) {
@@ -462,18 +439,20 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
           break;
         }
         tc_fence_after();
-        tmem_st_32x32b_x16(tmem + lane_addr + static_cast<uint32_t>(kPCol + 32 * x + (kHalf / 2) * half), pk);
+        tmem_st_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kPCol + 32 * x), pk);
         l = l * alpha + bsum;
         m = m_new;
-        // this half of O *= alpha when the maximum was raised after the
-        // first block
+        // O *= alpha when the maximum was raised after the first block
         if (raise && j > 0) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + 32 * half), o);
-          tmem_wait_ld();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-          tmem_st_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + 32 * half), o);
+          for (int h = 0; h < kAttnD; h += 32) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + h), o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+            tmem_st_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + h), o);
+          }
         }
         // P and O visible to the next MMAs
         tmem_wait_st();
@@ -482,28 +461,29 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
         if (lane == 0) mbar_arrive(p_full(x));
       }
       if (!ok) break;
-      // the item's last P V, then this half of O / l to global memory; O's
-      // columns are free for the next item once read
+      // the item's last P V, then O / l to global memory; O's columns are
+      // free for the next item once read
       if (!warp_wait(pv_done((nb - 1) & 1u), ((nb - 1) >> 1) & 1u, abort_flag, p.status, kDevTimeoutAccFull,
                      p.wait_ns))
         break;
       tc_fence_after();
-      uint32_t o[32];
-      tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + 32 * half), o);
+      uint32_t o[2][32];
+      tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol), o[0]);
+      tmem_ld_32x32b_x32(tmem + lane_addr + static_cast<uint32_t>(kOCol + 32), o[1]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_empty);
-      float l_other = 0.f;
-      if (!exchange(l, l_other)) break;
       if (q_row < p.T) {
-        const float inv_l = 1.f / (half == 0 ? l + l_other : l_other + l);
-        float* out = p.O + (static_cast<int64_t>(it.problem) * p.T + q_row) * kAttnD + 32 * half;
+        const float inv_l = 1.f / l;
+        float* out = p.O + (static_cast<int64_t>(it.problem) * p.T + q_row) * kAttnD;
 #pragma unroll
-        for (int t = 0; t < 32; t += 4)
-          *reinterpret_cast<float4*>(out + t) =
-              make_float4(__uint_as_float(o[t]) * inv_l, __uint_as_float(o[t + 1]) * inv_l,
-                          __uint_as_float(o[t + 2]) * inv_l, __uint_as_float(o[t + 3]) * inv_l);
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int t = 0; t < 32; t += 4)
+            *reinterpret_cast<float4*>(out + 32 * h + t) =
+                make_float4(__uint_as_float(o[h][t]) * inv_l, __uint_as_float(o[h][t + 1]) * inv_l,
+                            __uint_as_float(o[h][t + 2]) * inv_l, __uint_as_float(o[h][t + 3]) * inv_l);
       }
     }
   }
