@@ -495,6 +495,11 @@ def bench_ours(args, world, rank, local):
         with ClockSampler(dev.index) as fclk:
             configs["full_step"] = [time_full_step(h, dev, m, 5, 3) for m in ("tf32", "bf16", "fp32")]
         configs["full_step_clocks"] = fclk.summary()
+        # the fused attention forward (the GPT's attention and two longer
+        # contexts), a shorter sample than --workload attention takes
+        with ClockSampler(dev.index) as aclk:
+            configs["attention"] = attention_shapes(h, dev, stream, pk, samples=3, sample_ms=10.0)
+        configs["attention_clocks"] = aclk.summary()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -974,13 +979,54 @@ def attention_flops_bytes(P, T, D, causal):
     return 4 * D * pairs * P, P * T * D * (3 * 2 + 4)
 
 
-def bench_attention(args):
+def attention_shapes(h, dev, stream, pk, samples=SAMPLES, sample_ms=SAMPLE_MS):
     """The fused attention forward (gemm_attention_forward) on the GPT's
     attention (64 sequences x 6 heads of 64, context 256) and on the same
-    16384 tokens at contexts 1024 and 2048, causal.  Median of 5 samples of
-    >= 20 ms of calls back to back, inputs rotated over copies > 3x L2; the
-    roofline is the larger of the tensor time (bf16 burst peak) and the HBM
-    time of the algorithmic bytes."""
+    16384 tokens at contexts 1024 and 2048, causal: median of `samples`
+    samples of >= sample_ms of calls back to back, inputs rotated over copies
+    > 3x L2; the roofline is the larger of the tensor time (bf16 burst peak)
+    and the HBM time of the algorithmic bytes."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    D = si.ATTN_HEAD_DIM
+    shapes = []
+    for idx, (name, P, T) in enumerate(si.ATTN_WORKLOADS):
+        flops, byts = attention_flops_bytes(P, T, D, True)
+        copies = max(1, min(8, -(-3 * l2 // byts)))
+        Q, K, V = (t.to(dev) for t in si.attention_qkv(P, T, shape=idx))
+        sets = [(Q, K, V, torch.empty(Q.shape, dtype=torch.float32, device=dev))]
+        for _ in range(copies - 1):
+            sets.append((Q.clone(), K.clone(), V.clone(), torch.empty(Q.shape, dtype=torch.float32, device=dev)))
+
+        def call(r):
+            q, k, v, o = sets[r % copies]
+            h.attention(q, k, v, o, causal=True, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for r in range(copies):
+                call(r)
+        stream.synchronize()
+        t_est = _timed_back_to_back(call, max(2 * copies, 10), stream, 300)
+        reps = int(min(MAX_REPS, max(10, math.ceil(sample_ms / max(t_est, 1e-4)))))
+        st = _stats([_timed_back_to_back(call, reps, stream, 300) for _ in range(samples)])
+        assert h.check_device(stream) == 0
+        ms = st["median"]
+        t_tensor = flops / (pk["bf16_tflops"] * 1e12)
+        t_hbm = byts / (pk["hbm_gbs"] * 1e9)
+        shapes.append({"attention": name, "problems": P, "T": T, "Dh": D, "causal": True,
+                       "ms": round(ms, 5), "ms_min": round(st["min"], 5), "ms_max": round(st["max"], 5),
+                       "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+                       "gbs": round(byts / (ms * 1e-3) / 1e9, 1),
+                       "bound": "tensor" if t_tensor >= t_hbm else "hbm",
+                       "roofline_frac": round(max(t_tensor, t_hbm) / (ms * 1e-3), 3),
+                       "scores_bytes_not_written": 4 * P * T * T, "plan": h.plan()})
+        del sets, Q, K, V
+        torch.cuda.empty_cache()
+    return shapes
+
+
+def bench_attention(args):
+    """The fused attention forward on its three workloads (attention_shapes),
+    median of 5 samples of >= 20 ms each."""
     import dense_gemm_transformer_gb300 as dg
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -988,42 +1034,9 @@ def bench_attention(args):
     h = dg.Gemm()
     stream = torch.cuda.Stream(dev)
     pk = peaks()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     D = si.ATTN_HEAD_DIM
-    shapes = []
     with ClockSampler(dev.index) as clk:
-        for idx, (name, P, T) in enumerate(si.ATTN_WORKLOADS):
-            flops, byts = attention_flops_bytes(P, T, D, True)
-            copies = max(1, min(8, -(-3 * l2 // byts)))
-            Q, K, V = (t.to(dev) for t in si.attention_qkv(P, T, shape=idx))
-            sets = [(Q, K, V, torch.empty(Q.shape, dtype=torch.float32, device=dev))]
-            for _ in range(copies - 1):
-                sets.append((Q.clone(), K.clone(), V.clone(), torch.empty(Q.shape, dtype=torch.float32, device=dev)))
-
-            def call(r):
-                q, k, v, o = sets[r % copies]
-                h.attention(q, k, v, o, causal=True, stream=stream)
-
-            with torch.cuda.stream(stream):
-                for r in range(copies):
-                    call(r)
-            stream.synchronize()
-            t_est = _timed_back_to_back(call, max(2 * copies, 10), stream, 300)
-            reps = int(min(MAX_REPS, max(10, math.ceil(SAMPLE_MS / max(t_est, 1e-4)))))
-            st = _stats([_timed_back_to_back(call, reps, stream, 300) for _ in range(SAMPLES)])
-            assert h.check_device(stream) == 0
-            ms = st["median"]
-            t_tensor = flops / (pk["bf16_tflops"] * 1e12)
-            t_hbm = byts / (pk["hbm_gbs"] * 1e9)
-            shapes.append({"attention": name, "problems": P, "T": T, "Dh": D, "causal": True,
-                           "ms": round(ms, 5), "ms_min": round(st["min"], 5), "ms_max": round(st["max"], 5),
-                           "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
-                           "gbs": round(byts / (ms * 1e-3) / 1e9, 1),
-                           "bound": "tensor" if t_tensor >= t_hbm else "hbm",
-                           "roofline_frac": round(max(t_tensor, t_hbm) / (ms * 1e-3), 3),
-                           "scores_bytes_not_written": 4 * P * T * T, "plan": h.plan()})
-            del sets, Q, K, V
-            torch.cuda.empty_cache()
+        shapes = attention_shapes(h, dev, stream, pk)
     h.close()
     total_flops = sum(attention_flops_bytes(x["problems"], x["T"], D, True)[0] for x in shapes)
     line = {"metric": "fused attention forward TFLOP/s and fraction of the roofline, 1 GPU",

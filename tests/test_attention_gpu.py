@@ -126,6 +126,24 @@ def test_attention_long_context_sampled(h, idx):
     _check(got, Q, K, V, True, problems=(P - 1, P), what=name)
 
 
+@pytest.mark.parametrize("offset", [4, 8])
+def test_attention_output_only_16_byte_aligned(h, offset):
+    """O at 16 (not 32) bytes past an allocation: the kernel stores 16 bytes
+    at a time there; the floats around O stay untouched."""
+    P, T = 3, 300
+    Q, K, V = si.attention_qkv(P, T, shape=11)
+    dev = torch.device("cuda", 0)
+    n = Q.numel()
+    buf = torch.full((n + 2 * offset + 64,), 12345.0, dtype=torch.float32, device=dev)
+    O = buf[offset:offset + n].view(Q.shape)
+    assert O.data_ptr() % 32 == 16 if offset == 4 else O.data_ptr() % 32 == 0
+    h.attention(Q.to(dev), K.to(dev), V.to(dev), O, causal=True)
+    torch.cuda.synchronize()
+    out = buf.cpu()
+    assert torch.all(out[:offset] == 12345.0) and torch.all(out[offset + n:] == 12345.0)
+    _check(O.cpu().numpy().astype(np.float64), Q, K, V, True, what=f"offset {offset}")
+
+
 def test_attention_row_sums_of_constant_values(h):
     """V constant c: every output is c whatever the weights (the weights sum to one)."""
     Q, K, _ = si.attention_qkv(2, 333, shape=5, std_q=3.0)
