@@ -26,6 +26,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -979,17 +980,20 @@ def attention_flops_bytes(P, T, D, causal):
     return 4 * D * pairs * P, P * T * D * (3 * 2 + 4)
 
 
-def attention_shapes(h, dev, stream, pk, samples=SAMPLES, sample_ms=SAMPLE_MS):
+def attention_shapes(h, dev, stream, pk, samples=SAMPLES, sample_ms=SAMPLE_MS, only=None):
     """The fused attention forward (gemm_attention_forward) on the GPT's
     attention (64 sequences x 6 heads of 64, context 256) and on the same
     16384 tokens at contexts 1024 and 2048, causal: median of `samples`
     samples of >= sample_ms of calls back to back, inputs rotated over copies
     > 3x L2; the roofline is the larger of the tensor time (bf16 burst peak)
-    and the HBM time of the algorithmic bytes."""
+    and the HBM time of the algorithmic bytes.  only: a regex on the
+    workload names (gpt_ctx256, ctx1024, ctx2048), or None for all."""
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     D = si.ATTN_HEAD_DIM
     shapes = []
     for idx, (name, P, T) in enumerate(si.ATTN_WORKLOADS):
+        if only and not re.search(only, name):
+            continue
         flops, byts = attention_flops_bytes(P, T, D, True)
         copies = max(1, min(8, -(-3 * l2 // byts)))
         Q, K, V = (t.to(dev) for t in si.attention_qkv(P, T, shape=idx))
@@ -1036,7 +1040,7 @@ def bench_attention(args):
     pk = peaks()
     D = si.ATTN_HEAD_DIM
     with ClockSampler(dev.index) as clk:
-        shapes = attention_shapes(h, dev, stream, pk)
+        shapes = attention_shapes(h, dev, stream, pk, only=args.only)
     h.close()
     total_flops = sum(attention_flops_bytes(x["problems"], x["T"], D, True)[0] for x in shapes)
     line = {"metric": "fused attention forward TFLOP/s and fraction of the roofline, 1 GPU",
@@ -1155,7 +1159,8 @@ def main():
                     help="oracle multiply-adds in the CPU baseline (about 10 s on 16 host cores)")
     ap.add_argument("--ref-macs", type=float, default=3e8, help="oracle multiply-adds per reference step")
     ap.add_argument("--tile-n", type=int, default=0, help="sweeps: force the tensor-core tile width (128/256)")
-    ap.add_argument("--only", default=None, help="regex: time only the matching GEMMs of the step (profiling)")
+    ap.add_argument("--only", default=None,
+                    help="regex: time only the matching GEMMs of the step, or attention workloads (profiling)")
     ap.add_argument("--pair", type=int, default=None,
                     help="sweeps: CTA pairs issuing one 256-row MMA (0 wherever allowed, 1 never)")
     ap.add_argument("--split-k", type=int, default=0, help="sweeps: force this many K slices (0: planner)")
