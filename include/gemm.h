@@ -7,14 +7,17 @@
  *
  *     C = alpha * op(A) * op(B) + beta * C
  *
- * computed in one of seven modes (gemm_mode_t): exact FP32 on the CUDA
- * cores, TF32 on the tensor cores (the mode the page's tensor-core kernel
- * uses, first paragraph), BF16 inputs on the tensor cores, or 8-bit float
- * inputs on the tensor cores in four modes -- E4M3 x E4M3, E5M2 x E5M2 and
- * the two mixed pairs ("Tensor Cores: Matrix Instructions, Swizzling and
- * FP8, Measured" and "Low-Precision Kernels: INT4, INT8 and FP8 Matmuls,
- * Measured" name the formats).  Every mode accumulates in FP32 and writes
- * FP32.
+ * computed by gemm_run in one of seven modes (gemm_mode_t): exact FP32 on
+ * the CUDA cores, TF32 on the tensor cores (the mode the page's tensor-core
+ * kernel uses, first paragraph), BF16 inputs on the tensor cores, or 8-bit
+ * float inputs on the tensor cores in four modes -- E4M3 x E4M3, E5M2 x E5M2
+ * and the two mixed pairs ("Tensor Cores: Matrix Instructions, Swizzling
+ * and FP8, Measured" and "Low-Precision Kernels: INT4, INT8 and FP8
+ * Matmuls, Measured" name the formats).  Three more modes, the block-scaled
+ * MXFP8 (E4M3, E5M2) and NVFP4, run through gemm_run_block_scaled.  Every
+ * mode accumulates in FP32 and writes FP32.  gemm_run_epilogue adds a bias,
+ * GELU or GELU' to the product, and gemm_attention_forward is the fused
+ * attention forward of the same GPT (third paragraph).
  *
  * Layout (all matrices row-major, element (r, c) at base[r * ld + c]):
  *   op(A) is M x K.  transA == 0: A is stored M x K, lda >= max(K, 1).
