@@ -216,14 +216,21 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // Stage 0's descriptors; a stage's are these plus its byte offset in
+      // the address field (bits 0-13, address >> 4: every shared address
+      // here is below 256 KB, so the field cannot carry).  Rebuilding the
+      // 64-bit descriptors between these small MMAs is what would pace the
+      // single issuing thread.
+      const uint64_t a_desc0 = smem_desc_sw128(smem0, A_MN ? Cfg::BK * 128 : 16, 1024);
+      const uint64_t b_desc0 = smem_desc_sw128(smem0 + Cfg::A_BYTES, 16, 1024);
+      [[maybe_unused]] const uint64_t sf_desc0 = smem_desc_noswizzle(smem0 + Cfg::A_BYTES + Cfg::B_BYTES, 128);
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem0 + stage * Cfg::STAGE_BYTES;
-        const uint32_t b_base = a_base + Cfg::A_BYTES;
+        const uint64_t soff = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
         if constexpr (Cfg::BS) {
           // This stage's scale atoms into its TMEM ring slot (the slot's
           // previous MMAs are complete: this stage's copies could only be
@@ -231,14 +238,12 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
           // 32 bytes of K each: MXFP8 picks its byte of the 32-bit scale
           // cells by scale-factor ID j; NVFP4 takes atom j's four bytes.
           const uint32_t sf_col = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + stage * Cfg::SF_COLS);
-          const uint32_t sf_smem = b_base + Cfg::B_BYTES;
 #pragma unroll
-          for (int a = 0; a < 2 * Cfg::SF_ATOMS; ++a)
-            tmem_cp_32x128b_x4(sf_col + 4 * a, smem_desc_noswizzle(sf_smem + 512 * a, 128));
+          for (int a = 0; a < 2 * Cfg::SF_ATOMS; ++a) tmem_cp_32x128b_x4(sf_col + 4 * a, sf_desc0 + soff + 32 * a);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint64_t ad = smem_desc_sw128(a_base + j * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(b_base + j * 32, 16, 1024);
+            const uint64_t ad = a_desc0 + soff + 2 * j;
+            const uint64_t bd = b_desc0 + soff + 2 * j;
             const uint32_t acc = (kb > kb0 || j > 0) ? 1u : 0u;
             if constexpr (MODE == 4)
               mma_mxf8f6f4_bs(tmem_base, ad, bd,
@@ -252,9 +257,8 @@ __global__ void __launch_bounds__(kSkinnyThreads, 2)
         } else {
 #pragma unroll
           for (int j = 0; j < Cfg::BK / Cfg::UK; ++j) {
-            const uint64_t ad = A_MN ? smem_desc_sw128(a_base + j * Cfg::UK * 128, Cfg::BK * 128, 1024)
-                                     : smem_desc_sw128(a_base + j * Cfg::UK * Cfg::ES, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(b_base + j * Cfg::UK * Cfg::ES, 16, 1024);
+            const uint64_t ad = a_desc0 + soff + ((A_MN ? j * Cfg::UK * 128 : j * Cfg::UK * Cfg::ES) >> 4);
+            const uint64_t bd = b_desc0 + soff + ((j * Cfg::UK * Cfg::ES) >> 4);
             sk_mma<MODE>(tmem_base, ad, bd, IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
           }
         }

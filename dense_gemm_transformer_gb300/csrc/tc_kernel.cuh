@@ -476,6 +476,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int ab = 0;  // A_TMEM: buffer of the next stage's A
       uint32_t a_phase = 0;
       bool ok = true;
+      // block-scaled builds: stage 0's operand and scale-atom descriptors
+      [[maybe_unused]] const uint64_t a_desc0 = smem_desc_sw128(smem0, 16, 1024);
+      [[maybe_unused]] const uint64_t b_desc0 = smem_desc_sw128(smem0 + Cfg::A_BYTES, 16, 1024);
+      [[maybe_unused]] const uint64_t sf_desc0 = smem_desc_noswizzle(smem0 + Cfg::A_BYTES + Cfg::B_BYTES, 128);
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Unit w = decode_unit(u, p);
         if (!bar_wait<PAIR>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty, p.wait_ns)) break;
@@ -501,15 +505,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // released the stage), then four block-scaled MMAs of 32 bytes
             // of K: MXFP8 picks its byte of the scale cells by ID j, NVFP4
             // reads atom j's four bytes.
+            // The descriptors are stage 0's plus the stage's byte offset in
+            // their address field (bits 0-13, address >> 4; every shared
+            // address here is below 256 KB, so the field cannot carry): a
+            // single issuing thread rebuilding 64-bit descriptors between
+            // these small instructions is what would pace them.
             const uint32_t sf_col = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + stage * Cfg::SF_COLS);
-            const uint32_t sf_smem = b_base + Cfg::B_BYTES;
+            const uint64_t soff = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
 #pragma unroll
-            for (int a = 0; a < 2 * Cfg::SF_ATOMS; ++a)
-              tmem_cp_32x128b_x4(sf_col + 4 * a, smem_desc_noswizzle(sf_smem + 512 * a, 128));
+            for (int a = 0; a < 2 * Cfg::SF_ATOMS; ++a) tmem_cp_32x128b_x4(sf_col + 4 * a, sf_desc0 + soff + 32 * a);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const uint64_t ad = smem_desc_sw128(a_base + j * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(b_base + j * 32, 16, 1024);
+              const uint64_t ad = a_desc0 + soff + 2 * j;
+              const uint64_t bd = b_desc0 + soff + 2 * j;
               const uint32_t acc_in = (kb > w.kb0 || j > 0) ? 1u : 0u;
               if constexpr (MODE == 4)
                 mma_mxf8f6f4_bs(d_tmem, ad, bd,
