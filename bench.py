@@ -914,6 +914,8 @@ def bench_epilogue(args):
         for mode in ("fp32", "tf32"):
             for name, M, N, K, tB, act in (("mlp_up.fwd+bias+gelu", T, F, D, False, "gelu"),
                                            ("mlp_down.dX*dgelu", T, F, D, True, "dgelu")):
+                if args.only and not re.fullmatch(args.only, f"{mode}.{name}"):
+                    continue
                 g = torch.Generator(device="cpu")
                 g.manual_seed(si.BASE_SEED)
                 per_set = 4 * (M * K + K * N + M * N * (2 if act == "dgelu" else 1))
@@ -963,6 +965,8 @@ def bench_epilogue(args):
                 del sets
                 torch.cuda.empty_cache()
     h.close()
+    if not shapes:
+        raise SystemExit(f"--only {args.only!r} matches no epilogue product")
     total_flops = sum(2 * x["M"] * x["N"] * x["K"] for x in shapes)
     line = {"metric": METRIC, "value": total_flops / (sum(x["ms_fused"] for x in shapes) * 1e-3) / 1e12,
             "unit": "TFLOP/s", "n_gpus": 1, "higher_is_better": True, "dtype": "f32+tf32", "data": "synthetic",
@@ -1160,7 +1164,8 @@ def main():
     ap.add_argument("--ref-macs", type=float, default=3e8, help="oracle multiply-adds per reference step")
     ap.add_argument("--tile-n", type=int, default=0, help="sweeps: force the tensor-core tile width (128/256)")
     ap.add_argument("--only", default=None,
-                    help="regex: time only the matching GEMMs of the step, or attention workloads (profiling)")
+                    help="regex: time only the matching GEMMs of the step, sweep shapes, epilogue products or "
+                         "attention workloads (profiling)")
     ap.add_argument("--pair", type=int, default=None,
                     help="sweeps: CTA pairs issuing one 256-row MMA (0 wherever allowed, 1 never)")
     ap.add_argument("--split-k", type=int, default=0, help="sweeps: force this many K slices (0: planner)")
