@@ -191,6 +191,16 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   p.sfa = a.sfa;
   p.sfb = a.sfb;
   p.sf_groups = a.sf_groups;
+  // Block-scaled: the activations' scale atoms (SF_ATOMS per stage, the
+  // same for every weight tile) are copied into TMEM once per CTA when they
+  // fit its reserved columns, instead of with every stage.
+  {
+    const int per_kb = a.mode == 5 ? TcCfg<5, 16>::SF_ATOMS : a.mode == 4 ? TcCfg<4, 16>::SF_ATOMS : 0;
+    const int64_t res = static_cast<int64_t>(p.num_kb) * per_kb;
+    p.sfb_res = (per_kb > 0 && a.sfb != nullptr && res <= TcCfg<5, 16>::RES_ATOMS && res <= a.sf_groups)
+                    ? static_cast<int>(res)
+                    : 0;
+  }
   p.wait_ns = a.wait_ns > 0 ? a.wait_ns : kWaitLimitNs;
   p.epi = a.fuse_epi ? a.epi : EpiParams{};
   p.fault_skip = (a.fault_skip > 0 && !pair) ? a.fault_skip - 1 : -1;

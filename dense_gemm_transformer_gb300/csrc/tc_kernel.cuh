@@ -80,6 +80,8 @@ struct TcParams {
   const uint8_t* sfa;  // BS: scales of the kernel's A (the weights), tiled 512-byte atoms
   const uint8_t* sfb;  // BS: scales of the kernel's B (the activations)
   int64_t sf_groups;   // BS: atoms per 128-row tile
+  int sfb_res;         // BS: the activations' scale atoms held in TMEM for the whole call (their count,
+                       // copied once per CTA), or 0: copied with every stage
   uint64_t wait_ns;  // limit of every bounded wait
   int fault_skip;    // test hook: CTA 0's producer issues no copies for its fault_skip-th stage
                      // (0-based; -1: none), so the MMA's wait for that stage runs out
@@ -117,14 +119,21 @@ struct TcCfg {
   // two of at least 32 columns.
   static constexpr int SF_COL0 = 2 * BN;
   static constexpr int SF_COLS = 2 * SF_ATOMS * 4;
-  static constexpr int TMEM_NEED = SF_COL0 + (BS ? STAGES * SF_COLS : 0);
+  // BS: up to RES_ATOMS of the activations' scale atoms (the same for every
+  // weight tile) kept in TMEM for the whole call, after the ring, and
+  // staged through RES_BYTES of shared memory after the barriers.
+  static constexpr int RES_ATOMS = BS ? 32 : 0;
+  static constexpr int RES_BYTES = RES_ATOMS * 512;
+  static constexpr int RES_COL0 = SF_COL0 + (BS ? STAGES * SF_COLS : 0);
+  static constexpr int TMEM_NEED = RES_COL0 + 4 * RES_ATOMS;
   static constexpr int TMEM_COLS = (TMEM_NEED <= 32) ? 32 : (TMEM_NEED <= 64) ? 64 : (TMEM_NEED <= 128) ? 128
                                    : (TMEM_NEED <= 256) ? 256 : 512;
   static_assert(TMEM_NEED <= 512, "TMEM columns");
   static_assert(!BS || (BN == 16 && !BHALF), "block-scaled: the swapped small-M form");
   static constexpr int CW = BN < 32 ? BN : 32;                    // accumulator columns per TMEM load
-  static constexpr int NUM_BARS = 2 * STAGES + 5;     // full/empty per stage, acc full/empty x2, drain
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int NUM_BARS = 2 * STAGES + 6;     // full/empty per stage, acc full/empty x2, drain, resident scales
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/ + RES_BYTES;
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
   static constexpr uint32_t FORMAT = (MODE >= 3) ? 0u : (MODE == 2) ? 1u : 2u;  // 8-bit (fmt8) / bf16 / tf32
   static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
@@ -305,6 +314,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto accf_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto acce_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+  // BS: the activations' scale atoms for the whole call land here (one
+  // bulk copy, completing on res_bar) before they are copied into TMEM
+  const uint32_t res_bar = bar0 + 8u * (2 * S + 5);
+  [[maybe_unused]] const uint32_t res_smem = bar0 + 256u;
   auto afull_bar = [&](int b) { return bar0 + 8u * (Cfg::NUM_BARS + b); };        // A_TMEM: A in TMEM
   auto aempty_bar = [&](int b) { return bar0 + 8u * (Cfg::NUM_BARS + NA + b); };  // A_TMEM: buffer read
 
@@ -336,6 +349,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(aempty_bar(b), 1);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(res_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -373,6 +387,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;  // stages taken so far (their positions in the ring's sequence)
+      if constexpr (Cfg::BS) {
+        if (p.sfb_res > 0) {
+          mbar_arrive_expect_tx(res_bar, static_cast<uint32_t>(p.sfb_res) * 512u);
+          bulk_copy_g2s(res_smem, p.sfb, static_cast<uint32_t>(p.sfb_res) * 512u, res_bar);
+        }
+      }
       bool ok = true;
       // The test hook's position (CTA 0 only): its stage is taken but gets
       // no copies, so its "full" barrier never completes.
@@ -421,7 +441,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           } else {
             const uint32_t fb = full_bar(stage);
-            mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
+            mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES - ((Cfg::BS && p.sfb_res > 0) ? Cfg::SF_BYTES : 0));
             if (A_MN) {
 #pragma unroll
               for (int c = 0; c < Cfg::BM / Cfg::CH; ++c)
@@ -442,8 +462,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const uint32_t sf_dst = b_dst + Cfg::B_BYTES;
               bulk_copy_g2s(sf_dst, p.sfa + (static_cast<int64_t>(tm) * p.sf_groups + kb * Cfg::SF_ATOMS) * 512,
                             Cfg::SF_BYTES, fb);
-              bulk_copy_g2s(sf_dst + Cfg::SF_BYTES, p.sfb + static_cast<int64_t>(kb) * Cfg::SF_ATOMS * 512,
-                            Cfg::SF_BYTES, fb);
+              if (p.sfb_res == 0)
+                bulk_copy_g2s(sf_dst + Cfg::SF_BYTES, p.sfb + static_cast<int64_t>(kb) * Cfg::SF_ATOMS * 512,
+                              Cfg::SF_BYTES, fb);
             }
           }
           ++issued;
@@ -460,6 +481,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the stage it waited for are waited for here, whether or not this
         // loop ran to its end.  (An odd CTA's copies complete on the even
         // CTA's barriers, whose drain covers them; the pair leaves together.)
+        if constexpr (Cfg::BS) {
+          if (p.sfb_res > 0) drain_wait(res_bar, 0, p.status, p.wait_ns);
+        }
         const uint32_t n = issued < static_cast<uint32_t>(S) ? issued : static_cast<uint32_t>(S);
         for (uint32_t i = issued - n; i < issued; ++i)
           if (i != skip) drain_wait(full_bar(i % S), (i / S) & 1u, p.status, p.wait_ns);
@@ -480,6 +504,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       [[maybe_unused]] const uint64_t a_desc0 = smem_desc_sw128(smem0, 16, 1024);
       [[maybe_unused]] const uint64_t b_desc0 = smem_desc_sw128(smem0 + Cfg::A_BYTES, 16, 1024);
       [[maybe_unused]] const uint64_t sf_desc0 = smem_desc_noswizzle(smem0 + Cfg::A_BYTES + Cfg::B_BYTES, 128);
+      [[maybe_unused]] const uint32_t res_col = tmem_base + static_cast<uint32_t>(Cfg::RES_COL0);
+      if constexpr (Cfg::BS) {
+        // The activations' scale atoms for the whole call into TMEM once:
+        // atom a (stage a / SF_ATOMS, block group a % SF_ATOMS) at columns
+        // res_col + 4 a.  The MMAs issued after these copies by this thread
+        // see them (tcgen05 operations of one thread run in issue order).
+        if (p.sfb_res > 0) {
+          if (!bar_wait<false>(res_bar, 0, abort_flag, p.status, kDevTimeoutFull, p.wait_ns)) {
+            ok = false;
+          } else {
+            tc_fence_after();
+            const uint64_t rd0 = smem_desc_noswizzle(res_smem, 128);
+            for (int a = 0; a < p.sfb_res; ++a) tmem_cp_32x128b_x4(res_col + 4 * a, rd0 + 32 * a);
+          }
+        }
+      }
       for (int u = unit0; u < p.num_units && ok; u += unit_step) {
         const Unit w = decode_unit(u, p);
         if (!bar_wait<PAIR>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty, p.wait_ns)) break;
@@ -512,8 +552,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // these small instructions is what would pace them.
             const uint32_t sf_col = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + stage * Cfg::SF_COLS);
             const uint64_t soff = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
+            const bool res = p.sfb_res > 0;
+            // B's atoms of this stage: in the resident area, or copied with it
+            const uint32_t sfb_col = res ? res_col + static_cast<uint32_t>(4 * Cfg::SF_ATOMS * kb)
+                                         : sf_col + static_cast<uint32_t>(4 * Cfg::SF_ATOMS);
 #pragma unroll
-            for (int a = 0; a < 2 * Cfg::SF_ATOMS; ++a) tmem_cp_32x128b_x4(sf_col + 4 * a, sf_desc0 + soff + 32 * a);
+            for (int a = 0; a < Cfg::SF_ATOMS; ++a) tmem_cp_32x128b_x4(sf_col + 4 * a, sf_desc0 + soff + 32 * a);
+            if (!res) {
+#pragma unroll
+              for (int a = Cfg::SF_ATOMS; a < 2 * Cfg::SF_ATOMS; ++a)
+                tmem_cp_32x128b_x4(sf_col + 4 * a, sf_desc0 + soff + 32 * a);
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint64_t ad = a_desc0 + soff + 2 * j;
@@ -523,10 +572,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mma_mxf8f6f4_bs(d_tmem, ad, bd,
                                 make_idesc_bs(0, 0, true, Cfg::BM, BN, static_cast<uint32_t>(j),
                                               static_cast<uint32_t>(j)) | p.fmt8,
-                                sf_col, sf_col + 4, acc_in);
+                                sf_col, sfb_col, acc_in);
               else
                 mma_mxf4nvf4_bs(d_tmem, ad, bd, make_idesc_bs(1, 1, false, Cfg::BM, BN, 0, 0), sf_col + 4 * j,
-                                sf_col + 4 * (Cfg::SF_ATOMS + j), acc_in);
+                                sfb_col + 4 * j, acc_in);
             }
           } else {
 #pragma unroll

@@ -126,13 +126,17 @@ def test_block_scaled_integers_bit_exact(h, mode, M, N, K, splits):
 
 
 @pytest.mark.parametrize("mode", list(MODES))
-def test_block_scaled_persistent_form(h, mode):
+@pytest.mark.parametrize("deep", [False, True])
+def test_block_scaled_persistent_form(h, mode, deep):
     """Two or more waves of 128-row weight tiles go to the persistent kernel
     (each CTA streams tile after tile, no K split): ragged N, a partial last
-    stage; normal inputs within the gate and integers bit-exact."""
+    stage; normal inputs within the gate and integers bit-exact.  K = 1056
+    keeps the activations' scale atoms in TMEM for the whole call; the deep
+    K (more than 32 atoms) copies them with every stage."""
     elem, bs, sf = MODES[mode]
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    M, N, K = 5, 128 * (2 * sms + 9) - 37, 1056
+    K = (2400 if elem == "e2m1" else 4200) if deep else 1056
+    M, N = 5, 128 * (2 * sms + 9) - 37
     ac, sa = si.to_block_scaled(si.normal((M, K), 617), elem, bs, sf)
     bc, sb = si.to_block_scaled(si.normal((N, K), 618, std=0.02), elem, bs, sf)
     got = _run(h, mode, ac, sa, bc, sb, M, N)
