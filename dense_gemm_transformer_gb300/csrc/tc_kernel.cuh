@@ -25,6 +25,12 @@
 //               each stage's A tile there (one row of A per lane, down the
 //               MN-major rows) and store it into TMEM, whose lanes are the
 //               rows the MMA takes A from; warps 6-9 are the epilogue.
+//   Block-scaled builds (MXFP8 / NVFP4, the swapped small-M form): warp 10
+//               copies each stage's scale atoms into the stage's TMEM slot
+//               with tcgen05.cp once its data has arrived, and the MMA lane
+//               waits for that; the activations' atoms, the same for every
+//               weight tile, are copied once per CTA when they fit.  A lane
+//               issuing both the copies and the MMAs paced the stages.
 //
 // Work units are tiles, or (tile, K slice) pairs, handed out round-robin to
 // a persistent grid of one CTA per SM (or one CTA pair per two SMs, see PAIR
@@ -131,12 +137,18 @@ struct TcCfg {
   static_assert(TMEM_NEED <= 512, "TMEM columns");
   static_assert(!BS || (BN == 16 && !BHALF), "block-scaled: the swapped small-M form");
   static constexpr int CW = BN < 32 ? BN : 32;                    // accumulator columns per TMEM load
-  static constexpr int NUM_BARS = 2 * STAGES + 6;     // full/empty per stage, acc full/empty x2, drain, resident scales
+  // full/empty per stage, acc full/empty x2, drain, resident scales; BS
+  // also: per stage "scale atoms copied", and the copier's drain
+  static constexpr int NUM_BARS = 2 * STAGES + 6 + (BS ? STAGES + 1 : 0);
+  static constexpr int BAR_BYTES = BS ? 512 : 256;  // barriers, the TMEM address and the abort flag
+  // BS builds add a warp that copies every stage's scale atoms into TMEM,
+  // so that the MMA thread issues only the MMAs
+  static constexpr int THREADS = kTcThreads + (BS ? 32 : 0);
   static constexpr int SMEM_BYTES =
-      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/ + RES_BYTES;
+      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + BAR_BYTES + RES_BYTES;
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
   static constexpr uint32_t FORMAT = (MODE >= 3) ? 0u : (MODE == 2) ? 1u : 2u;  // 8-bit (fmt8) / bf16 / tf32
-  static_assert(NUM_BARS * 8 + 16 <= 256, "barrier area");
+  static_assert(NUM_BARS * 8 + 16 <= BAR_BYTES, "barrier area");
   static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle atoms aligned");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   static_assert(BN < 32 || BN % 32 == 0, "the epilogue moves 32-column chunks");
@@ -276,7 +288,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
 // and the store; partial tiles of a K split stay raw for the slice reduce,
 // which applies it.
 template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C, bool PAIR, bool EPI = false>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                    const TcParams p) {
@@ -294,7 +306,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int A_COL0 = 2 * BN;  // first TMEM column of the A buffers
   constexpr int TMEM_COLS = A_TMEM ? 512 : Cfg::TMEM_COLS;
   constexpr int EXTRA_BARS = A_TMEM ? 2 * NA : 0;
-  static_assert((Cfg::NUM_BARS + EXTRA_BARS) * 8 + 16 <= 256, "barrier area");
+  static_assert((Cfg::NUM_BARS + EXTRA_BARS) * 8 + 16 <= Cfg::BAR_BYTES, "barrier area");
   static_assert(!A_TMEM || A_COL0 + NA * Cfg::BK <= TMEM_COLS, "TMEM columns");
   // MODE 3 names its operand formats at run time (the FORMAT fields are 0).
   const uint32_t IDESC = make_idesc(Cfg::FORMAT, A_MN && !A_TMEM, B_MN, PAIR ? 2 * Cfg::BM : Cfg::BM, BN) |
@@ -317,7 +329,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // BS: the activations' scale atoms for the whole call land here (one
   // bulk copy, completing on res_bar) before they are copied into TMEM
   const uint32_t res_bar = bar0 + 8u * (2 * S + 5);
-  [[maybe_unused]] const uint32_t res_smem = bar0 + 256u;
+  [[maybe_unused]] const uint32_t res_smem = bar0 + static_cast<uint32_t>(Cfg::BAR_BYTES);
+  // BS: stage s's scale atoms are in TMEM (the copier warp commits it)
+  auto cpd_bar = [&](int st) { return bar0 + 8u * (2 * S + 6 + st); };
+  [[maybe_unused]] const uint32_t cdrain_bar = bar0 + 8u * (3 * S + 6);
   auto afull_bar = [&](int b) { return bar0 + 8u * (Cfg::NUM_BARS + b); };        // A_TMEM: A in TMEM
   auto aempty_bar = [&](int b) { return bar0 + 8u * (Cfg::NUM_BARS + NA + b); };  // A_TMEM: buffer read
 
@@ -350,6 +365,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(drain_bar, 1);
     mbar_init(res_bar, 1);
+    if constexpr (Cfg::BS) {
+      for (int st = 0; st < S; ++st) mbar_init(cpd_bar(st), 1);
+      mbar_init(cdrain_bar, 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -526,7 +545,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!bar_wait<PAIR>(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull, p.wait_ns)) {
+          // The stage's data; BS: also its scale atoms, which the copier
+          // warp puts into TMEM after the data arrived (so the second wait
+          // is the one that lasts)
+          if (!bar_wait<PAIR>(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull, p.wait_ns) ||
+              (Cfg::BS && !bar_wait<false>(cpd_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull, p.wait_ns))) {
             ok = false;
             break;
           }
@@ -540,11 +563,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t a_base = smem0 + stage * Cfg::STAGE_BYTES;
           const uint32_t b_base = a_base + Cfg::A_BYTES;
           if constexpr (Cfg::BS) {
-            // The stage's scale atoms into its TMEM ring slot (free: this
-            // stage's copies were issued only after the slot's previous MMAs
-            // released the stage), then four block-scaled MMAs of 32 bytes
-            // of K: MXFP8 picks its byte of the scale cells by ID j, NVFP4
-            // reads atom j's four bytes.
+            // Four block-scaled MMAs of 32 bytes of K, the stage's scale
+            // atoms already in its TMEM ring slot (the copier warp's): MXFP8
+            // picks its byte of the scale cells by ID j, NVFP4 reads atom
+            // j's four bytes.
             // The descriptors are stage 0's plus the stage's byte offset in
             // their address field (bits 0-13, address >> 4; every shared
             // address here is below 256 KB, so the field cannot carry): a
@@ -553,16 +575,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t sf_col = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + stage * Cfg::SF_COLS);
             const uint64_t soff = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
             const bool res = p.sfb_res > 0;
-            // B's atoms of this stage: in the resident area, or copied with it
+            // B's atoms of this stage: in the resident area, or in the slot
             const uint32_t sfb_col = res ? res_col + static_cast<uint32_t>(4 * Cfg::SF_ATOMS * kb)
                                          : sf_col + static_cast<uint32_t>(4 * Cfg::SF_ATOMS);
-#pragma unroll
-            for (int a = 0; a < Cfg::SF_ATOMS; ++a) tmem_cp_32x128b_x4(sf_col + 4 * a, sf_desc0 + soff + 32 * a);
-            if (!res) {
-#pragma unroll
-              for (int a = Cfg::SF_ATOMS; a < 2 * Cfg::SF_ATOMS; ++a)
-                tmem_cp_32x128b_x4(sf_col + 4 * a, sf_desc0 + soff + 32 * a);
-            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint64_t ad = a_desc0 + soff + 2 * j;
@@ -624,6 +639,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       else
         mma_commit(drain_bar);
       drain_wait(drain_bar, 0, p.status, p.wait_ns);
+    }
+  } else if (Cfg::BS && warp == 2 + kTcEpiWarps) {
+    // ------------------------------------------------------------ scale copier
+    // BS builds: one lane walks the stages in the MMA thread's order and
+    // copies each stage's scale atoms (the weights'; the activations' too
+    // unless they are resident) into the stage's TMEM ring slot once its
+    // data has arrived, then commits cpd_bar(stage).  The slot is free: the
+    // stage was refilled only after the MMAs that read it released it.
+    if constexpr (Cfg::BS) {
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        const uint64_t sf_desc0 = smem_desc_noswizzle(smem0 + Cfg::A_BYTES + Cfg::B_BYTES, 128);
+        const int atoms = p.sfb_res > 0 ? Cfg::SF_ATOMS : 2 * Cfg::SF_ATOMS;
+        for (int u = unit0; u < p.num_units && ok; u += unit_step) {
+          const Unit w = decode_unit(u, p);
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!bar_wait<false>(full_bar(stage), phase, abort_flag, p.status, kDevTimeoutFull, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sf_col = tmem_base + static_cast<uint32_t>(Cfg::SF_COL0 + stage * Cfg::SF_COLS);
+            const uint64_t soff = static_cast<uint64_t>((stage * Cfg::STAGE_BYTES) >> 4);
+            for (int a = 0; a < atoms; ++a) tmem_cp_32x128b_x4(sf_col + 4 * a, sf_desc0 + soff + 32 * a);
+            mma_commit(cpd_bar(stage));
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        // every copy this thread issued has finished once cdrain_bar flips
+        mma_commit(cdrain_bar);
+        drain_wait(cdrain_bar, 0, p.status, p.wait_ns);
+      }
     }
   } else if (A_TMEM && warp < 6) {
     // ------------------------------------------------------------ A into TMEM

@@ -17,13 +17,13 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   });
   if (e != cudaSuccess) return e;
-  last_main_launch() = LaunchShape{dim3(static_cast<unsigned>(grid)), dim3(kTcThreads),
+  last_main_launch() = LaunchShape{dim3(static_cast<unsigned>(grid)), dim3(Cfg::THREADS),
                                    static_cast<size_t>(Cfg::SMEM_BYTES), PAIR ? 2 : 1, true};
   if constexpr (PAIR) {
     // Two-CTA clusters along x: CTAs 2c and 2c+1 form pair c.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(Cfg::THREADS);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -37,7 +37,7 @@ cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CU
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tw, p);
   } else {
-    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kTcThreads), Cfg::SMEM_BYTES, s, ta, tb, tc, tw,
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, s, ta, tb, tc, tw,
                       p);
   }
 }
