@@ -17,11 +17,12 @@
 //               block of 64 keys the K and V blocks (rings of four), all as
 //               128-byte swizzled rows of 64 bf16;
 //   warp 1      allocates TMEM (two S buffers of 64 fp32 columns, O: 64,
-//               two P buffers of 32), then one lane issues S = Q K^T (M 128,
-//               N 64, K 64) and O += P V (M 128, N 64, K 64: P read from
-//               TMEM, V from shared memory MN-major).  S runs two blocks
-//               ahead of P V, so the softmax finds the next S ready and
-//               rarely waits for a P V to finish;
+//               two P buffers of 32); one lane issues S = Q K^T (M 128, N
+//               64, K 64) into the S buffers, up to two blocks ahead;
+//   warp 6      one lane issues O += P V (M 128, N 64, K 64: P read from
+//               TMEM, V from shared memory MN-major) once the softmax has
+//               written P; the two chains are independent, and one lane
+//               issuing both spent most of every block issuing;
 //   warps 2-5   the softmax: warp w owns TMEM lane quarter w % 4, one query
 //               row per thread.  Per key block: read the row of S from TMEM
 //               into registers (and release S), take its maximum (scale,
@@ -51,7 +52,7 @@
 namespace dgt {
 namespace {
 
-constexpr int kAttnThreads = 192;  // producer, MMA, four softmax warps
+constexpr int kAttnThreads = 224;  // producer, S issuer, four softmax warps, P V issuer
 constexpr int kAttnD = 64;         // head dimension (one 128-byte bf16 row)
 constexpr int kAttnBQ = 128;       // queries per item (UMMA M)
 constexpr int kAttnBK = 64;        // keys per block (UMMA N of S, K of P V)
@@ -59,7 +60,7 @@ constexpr int kQBytes = kAttnBQ * 128;   // 128 rows x 128 bytes
 constexpr int kKVBytes = kAttnBK * 128;  // 64 rows x 128 bytes
 constexpr int kQBufs = 2;                // Q buffers
 constexpr int kKVStages = 4;             // K and V ring stages
-constexpr int kNumBars = 2 * kQBufs + 4 * kKVStages + 10;
+constexpr int kNumBars = 2 * kQBufs + 4 * kKVStages + 11;
 constexpr int kSmemBytes = kQBufs * kQBytes + 2 * kKVStages * kKVBytes + 1024 + 8 * kNumBars + 16;
 constexpr int kCtasPerSm = 2;
 constexpr int kTmemCols = 256;  // S0 [0, 64), S1 [64, 128), O [128, 192), P0 [192, 224), P1 [224, 256)
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
   auto s_free = [&](uint32_t x) { return sp0 + 8 * (2 + x); };
   auto p_full = [&](uint32_t x) { return sp0 + 8 * (4 + x); };
   auto pv_done = [&](uint32_t x) { return sp0 + 8 * (6 + x); };
-  const uint32_t o_empty = sp0 + 64, drain = sp0 + 72;
+  const uint32_t o_empty = sp0 + 64, drain = sp0 + 72, drain2 = sp0 + 80;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -182,6 +183,7 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
     }
     mbar_init(o_empty, 4);
     mbar_init(drain, 1);
+    mbar_init(drain2, 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -241,111 +243,70 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
         drain_last(v_full(s), (nv + kKVStages - 1 - s) / kKVStages, p.status, p.wait_ns);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // One lane walks the CTA's key blocks twice, two blocks apart: P V of
-    // block n, then S of block n + 2 (possibly the next item's) into the S
-    // buffer the softmax read for block n.  Each chain of four MMAs is
-    // issued back to back from descriptors built once per block (the K
-    // steps only add constant offsets): a single issuing thread that
-    // rebuilds 64-bit descriptors between MMAs cannot keep the tensor pipe
-    // fed at these sizes.
+  } else if (warp == 1 || warp == 6) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two lanes issue the two independent chains: warp 1's S = Q K^T of
+    // every block into its S buffer (two blocks ahead at most, as the
+    // buffers allow), warp 6's O += P V once the softmax has written P.  A
+    // single lane issuing both spent most of each block issuing.  Each chain
+    // of four MMAs goes out back to back from descriptors built once (a K
+    // step of 16 elements advances a K-major descriptor by 32 bytes, 2 in
+    // its address field, and V's MN-major one by 16 rows, 2048 bytes, 128).
     if (lane == 0) {
-      const uint32_t idesc_s = make_idesc(1, false, false, kAttnBQ, kAttnBK);  // bf16, both K-major
-      const uint32_t idesc_o = make_idesc(1, false, true, kAttnBQ, kAttnD);    // V read MN-major
-      // S cursor: item ws, block js; ns blocks and nis items begun so far
-      int ws = blockIdx.x, js = 0;
-      Item its = decode_item(p, ws < p.items ? ws : 0);
-      uint32_t ns = 0, nis = 0;
-      // P V cursor
-      int wp = blockIdx.x, jp = 0;
-      Item itp = its;
-      uint32_t np = 0, nip = 0;
+      const bool s_lane = warp == 1;
+      const uint32_t idesc = s_lane ? make_idesc(1, false, false, kAttnBQ, kAttnBK)  // bf16, both K-major
+                                    : make_idesc(1, false, true, kAttnBQ, kAttnD);   // V read MN-major
+      const uint32_t my_drain = s_lane ? drain : drain2;
+      uint32_t n = 0, ni = 0;  // blocks and items begun so far
       bool ok = true;
-      // Q of a new item, K of the block, and its S buffer read (block n - 2)
-      auto wait_s = [&]() -> bool {
-        const uint32_t qb = nis % kQBufs, st = ns % kKVStages, x = ns & 1u;
-        return (js != 0 || mbar_wait(q_full(qb), (nis / kQBufs) & 1u, abort_flag, p.status, kDevTimeoutFull,
-                                     p.wait_ns)) &&
-               mbar_wait(k_full(st), (ns / kKVStages) & 1u, abort_flag, p.status, kDevTimeoutFull, p.wait_ns) &&
-               mbar_wait(s_free(x), ((ns >> 1) & 1u) ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty, p.wait_ns);
-      };
-      // the previous item's O read out, P of the block written (and O
-      // rescaled), V of the block in
-      auto wait_pv = [&]() -> bool {
-        const uint32_t st = np % kKVStages, x = np & 1u;
-        return (jp != 0 || mbar_wait(o_empty, (nip & 1u) ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty,
-                                     p.wait_ns)) &&
-               mbar_wait(p_full(x), (np >> 1) & 1u, abort_flag, p.status, kDevTimeoutFull, p.wait_ns) &&
-               mbar_wait(v_full(st), (np / kKVStages) & 1u, abort_flag, p.status, kDevTimeoutFull, p.wait_ns);
-      };
-      // the four MMAs of S (block ns) and of P V (block np); a K step of
-      // 16 elements advances a K-major descriptor by 32 bytes (2 in its
-      // address field) and V's MN-major one by 16 rows (2048 bytes, 128)
-      auto mma_s = [&]() {
-        const uint64_t ad = smem_desc_sw128(q_s + (nis % kQBufs) * kQBytes, 16, 1024);
-        const uint64_t bd = smem_desc_sw128(k_s + (ns % kKVStages) * kKVBytes, 16, 1024);
-        const uint32_t d = tmem + kSCol + 64 * (ns & 1u);
-        mma_bf16(d, ad, bd, idesc_s, 0u);
+      for (int w = blockIdx.x; w < p.items && ok; w += gridDim.x, ++ni) {
+        const Item it = decode_item(p, w);
+        const uint32_t qb = ni % kQBufs;
+        for (int j = 0; j < it.blocks; ++j, ++n) {
+          const uint32_t st = n % kKVStages, kph = (n / kKVStages) & 1u, x = n & 1u, xph = (n >> 1) & 1u;
+          if (s_lane) {
+            // Q of a new item, K of the block, and its S buffer read (block n - 2)
+            if ((j == 0 && !mbar_wait(q_full(qb), (ni / kQBufs) & 1u, abort_flag, p.status, kDevTimeoutFull,
+                                      p.wait_ns)) ||
+                !mbar_wait(k_full(st), kph, abort_flag, p.status, kDevTimeoutFull, p.wait_ns) ||
+                !mbar_wait(s_free(x), xph ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad = smem_desc_sw128(q_s + qb * kQBytes, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(k_s + st * kKVBytes, 16, 1024);
+            const uint32_t d = tmem + kSCol + 64 * x;
+            mma_bf16(d, ad, bd, idesc, 0u);
 #pragma unroll
-        for (int k = 1; k < kAttnD / 16; ++k) mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc_s, 1u);
-      };
-      auto mma_pv = [&]() {
-        const uint64_t vd = smem_desc_sw128(v_s + (np % kKVStages) * kKVBytes, kKVBytes, 1024);
-        const uint32_t a = tmem + kPCol + 32 * (np & 1u), d = tmem + kOCol;
-        mma_bf16_tmem_a(d, a, vd, idesc_o, jp > 0 ? 1u : 0u);
+            for (int k = 1; k < kAttnD / 16; ++k) mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, 1u);
+            mma_commit(k_empty(st));
+            mma_commit(s_full(x));
+            if (j == it.blocks - 1) mma_commit(q_empty(qb));  // the item's last S has read its Q
+          } else {
+            // the previous item's O read out, P of the block written (and O
+            // rescaled), V of the block in
+            if ((j == 0 && !mbar_wait(o_empty, (ni & 1u) ^ 1u, abort_flag, p.status, kDevTimeoutAccEmpty,
+                                      p.wait_ns)) ||
+                !mbar_wait(p_full(x), xph, abort_flag, p.status, kDevTimeoutFull, p.wait_ns) ||
+                !mbar_wait(v_full(st), kph, abort_flag, p.status, kDevTimeoutFull, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t vd = smem_desc_sw128(v_s + st * kKVBytes, kKVBytes, 1024);
+            const uint32_t a = tmem + kPCol + 32 * x, d = tmem + kOCol;
+            mma_bf16_tmem_a(d, a, vd, idesc, j > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 1; k < kAttnBK / 16; ++k) mma_bf16_tmem_a(d, a + 8 * k, vd + 128 * k, idesc_o, 1u);
-      };
-      // commits once the block's MMAs are issued, then the cursors move on
-      auto done_s = [&]() {
-        const uint32_t qb = nis % kQBufs;
-        mma_commit(k_empty(ns % kKVStages));
-        mma_commit(s_full(ns & 1u));
-        ++ns;
-        if (++js == its.blocks) {
-          mma_commit(q_empty(qb));  // the item's last S has read its Q
-          js = 0;
-          ++nis;
-          ws += gridDim.x;
-          if (ws < p.items) its = decode_item(p, ws);
-        }
-      };
-      auto done_pv = [&]() {
-        mma_commit(v_empty(np % kKVStages));
-        mma_commit(pv_done(np & 1u));
-        ++np;
-        if (++jp == itp.blocks) {
-          jp = 0;
-          ++nip;
-          wp += gridDim.x;
-          if (wp < p.items) itp = decode_item(p, wp);
-        }
-      };
-      // S of the first two blocks alone
-      for (int i = 0; i < 2 && ok && ws < p.items; ++i) {
-        ok = wait_s();
-        if (!ok) break;
-        tc_fence_after();
-        mma_s();
-        done_s();
-      }
-      // then P V of block n and S of block n + 2
-      while (ok && wp < p.items) {
-        if (!wait_pv()) break;
-        tc_fence_after();
-        mma_pv();
-        done_pv();
-        if (ws < p.items) {
-          if (!wait_s()) break;
-          tc_fence_after();
-          mma_s();
-          done_s();
+            for (int k = 1; k < kAttnBK / 16; ++k) mma_bf16_tmem_a(d, a + 8 * k, vd + 128 * k, idesc, 1u);
+            mma_commit(v_empty(st));
+            mma_commit(pv_done(x));
+          }
         }
       }
-      // every MMA this thread issued has completed once drain flips
-      mma_commit(drain);
-      drain_wait(drain, 0, p.status, p.wait_ns);
+      // every MMA this lane issued has completed once its drain barrier flips
+      mma_commit(my_drain);
+      drain_wait(my_drain, 0, p.status, p.wait_ns);
     }
   } else {
     // ------------------------------------------------------------ softmax
