@@ -115,6 +115,38 @@ __device__ __forceinline__ void st_global_v8(float* dst, const uint32_t* v, floa
                : "memory");
 }
 
+// Three-input max / min, and packed pairs of fp32 (two independent
+// round-to-nearest operations per instruction, the same results as two
+// scalar ones): fewer instructions per score in the softmax.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 __device__ __forceinline__ float exp2_fast(float x) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -360,10 +392,12 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
           for (int q = 0; q < 8; ++q) e8[q] = __uint_as_float(s[q]);
           if (c >= 0.f) {
 #pragma unroll
-            for (int t = 8; t < kAttnBK; ++t) e8[t & 7] = fmaxf(e8[t & 7], __uint_as_float(s[t]));
+            for (int t = 8; t < kAttnBK; t += 2)
+              e8[(t >> 1) & 7] = max3f(e8[(t >> 1) & 7], __uint_as_float(s[t]), __uint_as_float(s[t + 1]));
           } else {
 #pragma unroll
-            for (int t = 8; t < kAttnBK; ++t) e8[t & 7] = fminf(e8[t & 7], __uint_as_float(s[t]));
+            for (int t = 8; t < kAttnBK; t += 2)
+              e8[(t >> 1) & 7] = min3f(e8[(t >> 1) & 7], __uint_as_float(s[t]), __uint_as_float(s[t + 1]));
           }
         } else {
           const float none = c >= 0.f ? kNegInf : -kNegInf;
@@ -388,20 +422,27 @@ __global__ void __launch_bounds__(kAttnThreads, kCtasPerSm)
         const float alpha = raise ? exp2_fast(m - m_new) : 1.f;  // 0 when m = -inf
         // P = 2^(c s - m_new) as bf16 pairs (key 2u in the low half of word
         // u) and the row sum of the fp32 weights (four partial sums)
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        // (the exponent c s - m_new and the sums as packed pairs)
+        const uint64_t cc = f2_pack(c, c), mm = f2_pack(-m_new, -m_new);
+        uint64_t ps2[2] = {0ull, 0ull};  // +0.0f pairs
         uint32_t pk[kAttnBK / 2];
 #pragma unroll
         for (int u = 0; u < kAttnBK / 2; ++u) {
-          float p0 = exp2_fast(fmaf(__uint_as_float(s[2 * u]), c, -m_new));
-          float p1 = exp2_fast(fmaf(__uint_as_float(s[2 * u + 1]), c, -m_new));
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * u]), __uint_as_float(s[2 * u + 1])), cc, mm), x0, x1);
+          float p0 = exp2_fast(x0);
+          float p1 = exp2_fast(x1);
           if (!whole) {
             p0 = 2 * u < limit ? p0 : 0.f;
             p1 = 2 * u + 1 < limit ? p1 : 0.f;
           }
-          ps[u & 3] += p0 + p1;
+          ps2[u & 1] = f2_add(ps2[u & 1], f2_pack(p0, p1));
           pk[u] = pack_bf16x2(p0, p1);
         }
-        const float bsum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        float sa, sb, sc, sd;
+        f2_unpack(ps2[0], sa, sb);
+        f2_unpack(ps2[1], sc, sd);
+        const float bsum = (sa + sb) + (sc + sd);
         // P buffer x is free once P V of block n - 2 is done; O may be
         // rescaled once P V of block n - 1 is done
         if (!warp_wait(pv_done(x), xph ^ 1u, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns) ||
