@@ -28,6 +28,7 @@
 #pragma once
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace dgt {
 
@@ -75,6 +76,72 @@ __device__ __forceinline__ float dgelu_f(float x) {
   float Phi, phi;
   normal_cdf_pdf(x, Phi, phi);
   return fmaf(x, phi, Phi);
+}
+
+// The same functions on a pair of elements (a packed fp32 pair of ptx.cuh):
+// the multiplies and adds of the pair are packed instructions, the
+// reciprocal and the power of two stay per element.  normal_cdf_exp_x2 and
+// dgelu_x2 take the steps of the scalar forms above in the same order, so
+// each element comes out exactly as the scalar function gives it.
+__device__ __forceinline__ uint64_t f2_splat(float c) { return f2_pack(c, c); }
+
+__device__ __forceinline__ void normal_cdf_exp_x2(uint64_t x, uint64_t& Phi, uint64_t& e) {
+  constexpr float kPs = 0.23164188f;
+  constexpr float kH1 = 0.127414796f, kH2 = -0.142248368f, kH3 = 0.7107068705f, kH4 = -0.7265760135f,
+                  kH5 = 0.5307027145f;
+  constexpr float kNegHalfLog2e = -0.72134752044448170f;
+  float x0, x1;
+  f2_unpack(x, x0, x1);
+  // (scalar: the absolute value folds into the multiply-add's operand)
+  const uint64_t t = f2_pack(rcp_approx(fmaf(kPs, fabsf(x0), 1.f)), rcp_approx(fmaf(kPs, fabsf(x1), 1.f)));
+  uint64_t q = f2_fma(t, f2_splat(kH5), f2_splat(kH4));
+  q = f2_fma(t, q, f2_splat(kH3));
+  q = f2_fma(t, q, f2_splat(kH2));
+  q = f2_fma(t, q, f2_splat(kH1));
+  const uint64_t half_poly = f2_mul(t, q);
+  float a0, a1;
+  f2_unpack(f2_mul(f2_mul(x, x), f2_splat(kNegHalfLog2e)), a0, a1);
+  e = f2_pack(exp2_approx(a0), exp2_approx(a1));
+  const uint64_t half_erfc = f2_mul(half_poly, e);
+  float h0, h1, o0, o1;
+  f2_unpack(half_erfc, h0, h1);
+  f2_unpack(f2_fma(half_erfc, f2_splat(-1.f), f2_splat(1.f)), o0, o1);  // 1 - half_erfc, one rounding
+  Phi = f2_pack(x0 >= 0.f ? o0 : h0, x1 >= 0.f ? o1 : h1);
+}
+
+// GELU of a pair, in the form GELU(x) = max(x, 0) - |x| erfc(|x| / sqrt 2) / 2
+// (for x >= 0 it is x - x (1 - Phi(x)), for x < 0 it is x Phi(x)): the
+// erfc term comes out of 7.1.26 with its coefficients negated, and one
+// multiply-add with max(x, 0) finishes the element, so that no per-element
+// sign test is needed; an element rounds once at the end, and in the
+// negative tail the result keeps its relative accuracy.
+__device__ __forceinline__ uint64_t gelu_x2(uint64_t x) {
+  constexpr float kPs = 0.23164188f;
+  constexpr float kH1 = 0.127414796f, kH2 = -0.142248368f, kH3 = 0.7107068705f, kH4 = -0.7265760135f,
+                  kH5 = 0.5307027145f;
+  constexpr float kNegHalfLog2e = -0.72134752044448170f;
+  float x0, x1;
+  f2_unpack(x, x0, x1);
+  const uint64_t ax = f2_pack(fabsf(x0), fabsf(x1));
+  float d0, d1;
+  f2_unpack(f2_fma(f2_splat(kPs), ax, f2_splat(1.f)), d0, d1);
+  const uint64_t t = f2_pack(rcp_approx(d0), rcp_approx(d1));
+  uint64_t q = f2_fma(t, f2_splat(-kH5), f2_splat(-kH4));
+  q = f2_fma(t, q, f2_splat(-kH3));
+  q = f2_fma(t, q, f2_splat(-kH2));
+  q = f2_fma(t, q, f2_splat(-kH1));
+  const uint64_t neg_half_poly = f2_mul(t, q);
+  float a0, a1;
+  f2_unpack(f2_mul(f2_mul(x, x), f2_splat(kNegHalfLog2e)), a0, a1);
+  const uint64_t e = f2_pack(exp2_approx(a0), exp2_approx(a1));
+  return f2_fma(ax, f2_mul(neg_half_poly, e), f2_pack(fmaxf(x0, 0.f), fmaxf(x1, 0.f)));
+}
+
+__device__ __forceinline__ uint64_t dgelu_x2(uint64_t x) {
+  constexpr float kInvSqrt2Pi = 0.39894228040143268f;
+  uint64_t Phi, e;
+  normal_cdf_exp_x2(x, Phi, e);
+  return f2_fma(x, f2_mul(f2_splat(kInvSqrt2Pi), e), Phi);
 }
 
 // The epilogue's input for element (row, col) of the caller's C: Z there

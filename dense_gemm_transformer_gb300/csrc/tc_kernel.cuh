@@ -118,7 +118,10 @@ struct TcCfg {
   static constexpr int STAGING_BYTES = (BN >= 128) ? kTcEpiWarps * 32 * 128 : 0;
   // ~192-200 KB of operand stages (as many as fit beside the staging when
   // a stage holds half of B)
-  static constexpr int STAGES = BHALF ? (232448 - STAGING_BYTES - 1280) / STAGE_BYTES
+  // EPI kernels: one 128-byte slot per epilogue warp for the bias values
+  // of the 32 columns it is storing (read back as broadcasts).
+  static constexpr int EPI_BYTES = BS ? 0 : kTcEpiWarps * 128;
+  static constexpr int STAGES = BHALF ? (232448 - STAGING_BYTES - 1280 - EPI_BYTES) / STAGE_BYTES
                                       : (BN >= 192) ? 4 : (BN == 128) ? 6 : 200 * 1024 / STAGE_BYTES;
   // Two accumulators, then (BS) one ring slot of scale columns per stage
   // (4 columns per atom, A's atoms then B's); an allocation is a power of
@@ -145,7 +148,7 @@ struct TcCfg {
   // so that the MMA thread issues only the MMAs
   static constexpr int THREADS = kTcThreads + (BS ? 32 : 0);
   static constexpr int SMEM_BYTES =
-      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + BAR_BYTES + RES_BYTES;
+      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + BAR_BYTES + RES_BYTES + EPI_BYTES;
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
   static constexpr uint32_t FORMAT = (MODE >= 3) ? 0u : (MODE == 2) ? 1u : 2u;  // 8-bit (fmt8) / bf16 / tf32
   static_assert(NUM_BARS * 8 + 16 <= BAR_BYTES, "barrier area");
@@ -203,14 +206,53 @@ __device__ __forceinline__ void epi_fetch(const EpiParams& e, int64_t row, int64
 
 // The elementwise epilogue of four consecutive elements, after alpha /
 // beta, with the activation fixed at compile time (ACT < 0: none at all).
+// Two packed pairs per quad, each element the same as epilogue_finish_t's.
 template <int ACT>
 __device__ __forceinline__ float4 epi_finish4(float4 v, const float4& x) {
   if constexpr (ACT >= 0) {
-    v.x = epilogue_finish_t<ACT>(v.x, x.x);
-    v.y = epilogue_finish_t<ACT>(v.y, x.y);
-    v.z = epilogue_finish_t<ACT>(v.z, x.z);
-    v.w = epilogue_finish_t<ACT>(v.w, x.w);
+    uint64_t lo = f2_pack(v.x, v.y), hi = f2_pack(v.z, v.w);
+    const uint64_t xl = f2_pack(x.x, x.y), xh = f2_pack(x.z, x.w);
+    if constexpr (ACT == kActDGelu) {
+      lo = f2_mul(lo, dgelu_x2(xl));
+      hi = f2_mul(hi, dgelu_x2(xh));
+    } else {
+      lo = f2_add(lo, xl);
+      hi = f2_add(hi, xh);
+      if constexpr (ACT == kActGelu) {
+        lo = gelu_x2(lo);
+        hi = gelu_x2(hi);
+      }
+    }
+    f2_unpack(lo, v.x, v.y);
+    f2_unpack(hi, v.z, v.w);
   }
+  return v;
+}
+
+// alpha times four accumulator words plus x (the bias), then GELU or
+// nothing (ACT: kActGelu, kActNone): two packed multiply-adds, each element
+// rounded once before the activation.
+template <int ACT>
+__device__ __forceinline__ float4 scaled_bias_act4(float a, const uint32_t* r, const float4& x) {
+  const uint64_t a2 = f2_pack(a, a);
+  uint64_t lo = f2_fma(a2, f2_pack(__uint_as_float(r[0]), __uint_as_float(r[1])), f2_pack(x.x, x.y));
+  uint64_t hi = f2_fma(a2, f2_pack(__uint_as_float(r[2]), __uint_as_float(r[3])), f2_pack(x.z, x.w));
+  if constexpr (ACT == kActGelu) {
+    lo = gelu_x2(lo);
+    hi = gelu_x2(hi);
+  }
+  float4 v;
+  f2_unpack(lo, v.x, v.y);
+  f2_unpack(hi, v.z, v.w);
+  return v;
+}
+
+// alpha times four accumulator words, as two packed products.
+__device__ __forceinline__ float4 scaled4(float a, const uint32_t* r) {
+  const uint64_t a2 = f2_pack(a, a);
+  float4 v;
+  f2_unpack(f2_mul(a2, f2_pack(__uint_as_float(r[0]), __uint_as_float(r[1]))), v.x, v.y);
+  f2_unpack(f2_mul(a2, f2_pack(__uint_as_float(r[2]), __uint_as_float(r[3]))), v.z, v.w);
   return v;
 }
 
@@ -318,6 +360,8 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS + EXTRA_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  [[maybe_unused]] float* bias_slots =
+      reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + Cfg::BAR_BYTES + Cfg::RES_BYTES);
 
   const uint32_t smem0 = smem_u32(smem);
   const uint32_t bar0 = smem_u32(bars);
@@ -732,6 +776,25 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     constexpr int CW = Cfg::CW;
+    constexpr int NCH = BN / CW;  // column chunks of a tile
+    // Warps of half 0 take the first ceil(NCH / 2) chunks, half 1 the rest
+    // (A_TMEM: the four epilogue warps take all of them).
+    const int cc_begin = (A_TMEM || half == 0) ? 0 : (NCH + 1) / 2;
+    const int cc_end = (!A_TMEM && half == 0) ? (NCH + 1) / 2 : NCH;
+    // EPI with a bias (or no input at all): lane l holds the bias of column
+    // l of the warp's next chunk, loaded one chunk ahead; at the chunk's
+    // start the warp puts its 32 values into its shared-memory slot, and
+    // every lane reads them back four at a time as broadcasts.
+    [[maybe_unused]] const bool bias_slot = EPI && p.epi.act != kActDGelu;
+    [[maybe_unused]] float* const bslot = bias_slots + (warp - 2) * 32;
+    [[maybe_unused]] auto bias_of = [&](int64_t col) {
+      return (p.epi.bias != nullptr && col < p.N) ? ld_nc_f32_here(p.epi.bias + col) : 0.f;
+    };
+    [[maybe_unused]] float bias_next = 0.f;
+    if constexpr (EPI) {
+      if (bias_slot && unit0 < p.num_units)
+        bias_next = bias_of(static_cast<int64_t>(decode_unit(unit0, p).tn) * BN + cc_begin * CW + lane);
+    }
     for (int u = unit0; u < p.num_units; u += unit_step) {
       const Unit w = decode_unit(u, p);
       if (!bar_wait<PAIR>(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns)) break;
@@ -748,24 +811,32 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
       float* out = TRANS_C ? base : base + (row_ok ? wrow : 0) * ld;
       const bool vec_ok = !TRANS_C && (partial || p.c_vec);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      constexpr int NCH = BN / CW;  // column chunks of a tile
-      // Warps of half 0 take the first ceil(NCH / 2) chunks, half 1 the rest
-      // (A_TMEM: the four epilogue warps take all of them).
-      const int cc_begin = (A_TMEM || half == 0) ? 0 : (NCH + 1) / 2;
-      const int cc_end = (!A_TMEM && half == 0) ? (NCH + 1) / 2 : NCH;
 #pragma unroll 1
       for (int cc = cc_begin; cc < cc_end; ++cc) {
         const int64_t col0 = static_cast<int64_t>(w.tn) * BN + cc * CW;
-        // EPI: the bias or Z values of this chunk's first quarter, requested
-        // before the TMEM load so that both latencies overlap; each further
-        // quarter is requested as a group when the previous one is done
-        // (fetching more at once spilled registers).
+        // EPI with GELU': Z's values for this row in the chunk's first
+        // quarter, requested before the TMEM load so that both latencies
+        // overlap; each further quarter is requested as a group when the
+        // previous one is done (fetching more at once spilled registers).
         constexpr int NQH = (CW / 4 + 3) / 4;
         const bool epi_on = EPI && !partial;
         const bool epi_fetch_ok = row_ok && col0 < p.N;
         float4 xe[NQH];
         if constexpr (EPI) {
-          if (epi_on) epi_fetch<NQH>(p.epi, row, col0, p.N, epi_fetch_ok, xe);
+          if (epi_on && !bias_slot) epi_fetch<NQH>(p.epi, row, col0, p.N, epi_fetch_ok, xe);
+          if (bias_slot) {
+            __syncwarp();  // every lane has read the slot's previous values
+            bslot[lane] = bias_next;
+            __syncwarp();
+            // the next chunk of this warp: the next one of this tile, or the
+            // first of its next unit's tile
+            int64_t ncol = -1;
+            if (cc + 1 < cc_end)
+              ncol = col0 + CW + lane;
+            else if (u + unit_step < p.num_units)
+              ncol = static_cast<int64_t>(decode_unit(u + unit_step, p).tn) * BN + cc_begin * CW + lane;
+            bias_next = ncol >= 0 ? bias_of(ncol) : 0.f;
+          }
         }
         if constexpr (Cfg::STAGING_BYTES > 0 && CW == 32) {
           if (partial ? p.w_tma : p.c_tma) {
@@ -792,15 +863,15 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
 #pragma unroll
                 for (int qq = 0; qq < SW / 4; ++qq) {
                   const int q = hh * (SW / 4) + qq;
-                  if constexpr (ACT >= 0) {
-                    if (q > 0 && q % NQH == 0) epi_fetch<NQH>(p.epi, row, col0 + 4 * q, p.N, epi_fetch_ok, xe);
-                  }
                   float4 v;
-                  v.x = a * __uint_as_float(r[4 * qq + 0]);
-                  v.y = a * __uint_as_float(r[4 * qq + 1]);
-                  v.z = a * __uint_as_float(r[4 * qq + 2]);
-                  v.w = a * __uint_as_float(r[4 * qq + 3]);
-                  v = epi_finish4<ACT>(v, xe[q % NQH]);
+                  if constexpr (ACT == kActDGelu) {
+                    if (q > 0 && q % NQH == 0) epi_fetch<NQH>(p.epi, row, col0 + 4 * q, p.N, epi_fetch_ok, xe);
+                    v = epi_finish4<ACT>(scaled4(a, r + 4 * qq), xe[q % NQH]);
+                  } else if constexpr (ACT >= 0) {
+                    v = scaled_bias_act4<ACT>(a, r + 4 * qq, reinterpret_cast<const float4*>(bslot)[q]);
+                  } else {
+                    v = scaled4(a, r + 4 * qq);
+                  }
                   *reinterpret_cast<float4*>(buf + lane * 128 + ((q ^ (lane & 7)) * 16)) = v;
                 }
               }
@@ -838,14 +909,14 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
             constexpr int ACT = decltype(act_c)::value;
 #pragma unroll
             for (int q = 0; q < CW / 4; ++q) {
-              if constexpr (ACT >= 0) {
+              float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+              if constexpr (ACT == kActDGelu) {
                 if (q > 0 && q % NQH == 0) epi_fetch<NQH>(p.epi, row, col0 + 4 * q, p.N, epi_fetch_ok, xe);
+                x = xe[q % NQH];
+              } else if constexpr (ACT >= 0) {
+                x = reinterpret_cast<const float4*>(bslot)[q];
               }
-              float4 v;
-              v.x = a * __uint_as_float(r[4 * q + 0]);
-              v.y = a * __uint_as_float(r[4 * q + 1]);
-              v.z = a * __uint_as_float(r[4 * q + 2]);
-              v.w = a * __uint_as_float(r[4 * q + 3]);
+              float4 v = scaled4(a, r + 4 * q);
               if (read_c) {
                 const float4 cq = EPI ? dst[q] : c[q % NC];
                 v.x = fmaf(p.beta, cq.x, v.x);
@@ -853,7 +924,7 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
                 v.z = fmaf(p.beta, cq.z, v.z);
                 v.w = fmaf(p.beta, cq.w, v.w);
               }
-              v = epi_finish4<ACT>(v, xe[q % NQH]);
+              v = epi_finish4<ACT>(v, x);
               dst[q] = v;
             }
           });
