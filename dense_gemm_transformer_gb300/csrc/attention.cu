@@ -133,16 +133,6 @@ __device__ __forceinline__ float exp2_fast(float x) {
   return r;
 }
 
-// 3-D tiled load (one box of the [problems][T][64] tensor) completing on `bar`.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0, int32_t c1,
-                                            int32_t c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 // Bounded drain of the last of `n` phases of `bar` (nothing when n == 0).
 __device__ __forceinline__ void drain_last(uint32_t bar, uint32_t n, int* status, uint64_t limit) {
   if (n > 0) drain_wait(bar, (n - 1) & 1u, status, limit);

@@ -15,7 +15,8 @@ enum DeviceStatus : int {
   kDevTimeoutEmpty = 2,     // producer waited too long for a free stage
   kDevTimeoutAccFull = 3,   // epilogue waited too long for an accumulator
   kDevTimeoutAccEmpty = 4,  // MMA warp waited too long for a drained accumulator
-  kDevTimeoutDrain = 5      // abort path waited too long for in-flight copies
+  kDevTimeoutDrain = 5,     // abort path waited too long for in-flight copies
+  kDevTimeoutEpiInput = 6   // epilogue waited too long for a block of its input (Z)
 };
 
 // A wait that has not finished after this long is treated as a hang (the
@@ -147,6 +148,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 3-D tiled load of one box (c0 innermost), completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0, int32_t c1,
+                                            int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -205,6 +216,13 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(c0), "r"(c1)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
                : "memory");
 }
 

@@ -224,6 +224,16 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
     if (whole && a.beta == 0.f && p.c_vec)
       p.c_tma = (encode_out_c(a.tma_cache, &tcm, a.C, a.N, a.M, 1, a.ldc, a.M * a.ldc) == cudaSuccess) ? 1 : 0;
   }
+  // GELU' with C leaving through TMA stores and no partial tiles: Z's
+  // blocks come in by TMA too, in the same boxes, through the workspace's
+  // map slot (unused then), when Z's rows are 16-byte aligned.
+  p.z_tma = 0;
+  if (a.fuse_epi && a.epi.act == kActDGelu && p.c_tma && !p.w_tma && a.splits == 1 && a.epi.aux != nullptr &&
+      (reinterpret_cast<uintptr_t>(a.epi.aux) & 15u) == 0 && a.epi.ld_aux % 4 == 0)
+    p.z_tma = (encode_out_c(a.tma_cache, &twm, const_cast<float*>(a.epi.aux), a.N, a.M, 1, a.epi.ld_aux,
+                            a.M * a.epi.ld_aux) == cudaSuccess)
+                  ? 1
+                  : 0;
   if (a.mode >= 4) return tc_launch_bs(a.mode, ta, tb, tcm, twm, p, a.grid, stream);
   if (a.fuse_epi) {
     if (a.tile_n < 128 || !tc_epi_ok(a.mode, a.a_mn_major != 0, a.b_mn_major != 0)) return cudaErrorNotSupported;

@@ -81,6 +81,7 @@ struct TcParams {
   int c_vec;  // C rows are 16-byte aligned (ldc % 4 == 0 and C aligned)
   int c_tma;  // whole tiles leave through shared memory and TMA stores (tmC is valid)
   int w_tma;  // partial tiles likewise (tmW is valid)
+  int z_tma;  // EPI with GELU' and no partial tiles: tmW maps Z, whose 32 x 32 blocks the epilogue loads by TMA
   uint32_t fmt8;  // MODE 3: operand format bits of the instruction descriptor (E4M3 / E5M2)
   EpiParams epi;     // EPI kernels: bias / GELU / GELU' applied at every final store of a whole tile
   const uint8_t* sfa;  // BS: scales of the kernel's A (the weights), tiled 512-byte atoms
@@ -121,7 +122,8 @@ struct TcCfg {
   // EPI kernels: one 128-byte slot per epilogue warp for the bias values
   // of the 32 columns it is storing (read back as broadcasts).
   static constexpr int EPI_BYTES = BS ? 0 : kTcEpiWarps * 128;
-  static constexpr int STAGES = BHALF ? (232448 - STAGING_BYTES - 1280 - EPI_BYTES) / STAGE_BYTES
+  static constexpr int BAR_BYTES = BS ? 512 : 256;  // barriers, the TMEM address and the abort flag
+  static constexpr int STAGES = BHALF ? (232448 - STAGING_BYTES - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES
                                       : (BN >= 192) ? 4 : (BN == 128) ? 6 : 200 * 1024 / STAGE_BYTES;
   // Two accumulators, then (BS) one ring slot of scale columns per stage
   // (4 columns per atom, A's atoms then B's); an allocation is a power of
@@ -143,7 +145,6 @@ struct TcCfg {
   // full/empty per stage, acc full/empty x2, drain, resident scales; BS
   // also: per stage "scale atoms copied", and the copier's drain
   static constexpr int NUM_BARS = 2 * STAGES + 6 + (BS ? STAGES + 1 : 0);
-  static constexpr int BAR_BYTES = BS ? 512 : 256;  // barriers, the TMEM address and the abort flag
   // BS builds add a warp that copies every stage's scale atoms into TMEM,
   // so that the MMA thread issues only the MMAs
   static constexpr int THREADS = kTcThreads + (BS ? 32 : 0);
@@ -422,6 +423,7 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
     tma_prefetch_desc(&tmB);
     if (p.c_tma) tma_prefetch_desc(&tmC);
     if (p.w_tma) tma_prefetch_desc(&tmW);
+    if (p.z_tma) tma_prefetch_desc(&tmW);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -771,201 +773,284 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int sub = warp & 3;          // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;  // which half of the tile's column chunks it stores
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    constexpr int CW = Cfg::CW;
-    constexpr int NCH = BN / CW;  // column chunks of a tile
-    // Warps of half 0 take the first ceil(NCH / 2) chunks, half 1 the rest
-    // (A_TMEM: the four epilogue warps take all of them).
-    const int cc_begin = (A_TMEM || half == 0) ? 0 : (NCH + 1) / 2;
-    const int cc_end = (!A_TMEM && half == 0) ? (NCH + 1) / 2 : NCH;
-    // EPI with a bias (or no input at all): lane l holds the bias of column
-    // l of the warp's next chunk, loaded one chunk ahead; at the chunk's
-    // start the warp puts its 32 values into its shared-memory slot, and
-    // every lane reads them back four at a time as broadcasts.
-    [[maybe_unused]] const bool bias_slot = EPI && p.epi.act != kActDGelu;
-    [[maybe_unused]] float* const bslot = bias_slots + (warp - 2) * 32;
-    [[maybe_unused]] auto bias_of = [&](int64_t col) {
-      return (p.epi.bias != nullptr && col < p.N) ? ld_nc_f32_here(p.epi.bias + col) : 0.f;
-    };
-    [[maybe_unused]] float bias_next = 0.f;
-    if constexpr (EPI) {
-      if (bias_slot && unit0 < p.num_units)
-        bias_next = bias_of(static_cast<int64_t>(decode_unit(unit0, p).tn) * BN + cc_begin * CW + lane);
-    }
-    for (int u = unit0; u < p.num_units; u += unit_step) {
-      const Unit w = decode_unit(u, p);
-      if (!bar_wait<PAIR>(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns)) break;
-      tc_fence_after();
-      const bool partial = w.partial;
-      const bool read_c = !partial && p.beta != 0.f;
-      const int tm = tile_row(w);
-      const int64_t row = static_cast<int64_t>(tm) * Cfg::BM + sub * 32 + lane;
-      const bool row_ok = row < p.M;
-      const int64_t row_base = partial ? p.ws_row0 : 0;  // C row of row 0 of the destination
-      const int64_t wrow = row - row_base;
-      float* base = partial ? p.ws + static_cast<int64_t>(w.split) * p.ws_slice : p.C;
-      const int64_t ld = partial ? p.ws_ld : p.ldc;
-      float* out = TRANS_C ? base : base + (row_ok ? wrow : 0) * ld;
-      const bool vec_ok = !TRANS_C && (partial || p.c_vec);
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-      for (int cc = cc_begin; cc < cc_end; ++cc) {
-        const int64_t col0 = static_cast<int64_t>(w.tn) * BN + cc * CW;
-        // EPI with GELU': Z's values for this row in the chunk's first
-        // quarter, requested before the TMEM load so that both latencies
-        // overlap; each further quarter is requested as a group when the
-        // previous one is done (fetching more at once spilled registers).
-        constexpr int NQH = (CW / 4 + 3) / 4;
-        const bool epi_on = EPI && !partial;
-        const bool epi_fetch_ok = row_ok && col0 < p.N;
-        float4 xe[NQH];
-        if constexpr (EPI) {
-          if (epi_on && !bias_slot) epi_fetch<NQH>(p.epi, row, col0, p.N, epi_fetch_ok, xe);
-          if (bias_slot) {
-            __syncwarp();  // every lane has read the slot's previous values
-            bslot[lane] = bias_next;
-            __syncwarp();
-            // the next chunk of this warp: the next one of this tile, or the
-            // first of its next unit's tile
-            int64_t ncol = -1;
-            if (cc + 1 < cc_end)
-              ncol = col0 + CW + lane;
-            else if (u + unit_step < p.num_units)
-              ncol = static_cast<int64_t>(decode_unit(u + unit_step, p).tn) * BN + cc_begin * CW + lane;
-            bias_next = ncol >= 0 ? bias_of(ncol) : 0.f;
+    // The epilogue's loop is built twice: with ZT (GELU' whose Z comes in
+    // by TMA, chosen when the call allows it) and without, so that the
+    // other epilogues carry none of its code.
+    auto epilogue_role = [&](auto zt_c) {
+      constexpr bool ZT = decltype(zt_c)::value;
+      const int sub = warp & 3;          // TMEM lane quarter this warp may access
+      const int half = (warp - 2) >> 2;  // which half of the tile's column chunks it stores
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      constexpr int CW = Cfg::CW;
+      constexpr int NCH = BN / CW;  // column chunks of a tile
+      // Warps of half 0 take the first ceil(NCH / 2) chunks, half 1 the rest
+      // (A_TMEM: the four epilogue warps take all of them).
+      const int cc_begin = (A_TMEM || half == 0) ? 0 : (NCH + 1) / 2;
+      const int cc_end = (!A_TMEM && half == 0) ? (NCH + 1) / 2 : NCH;
+      // EPI with a bias (or no input at all): lane l holds the bias of column
+      // l of the warp's next chunk, loaded one chunk ahead; at the chunk's
+      // start the warp puts its 32 values into its shared-memory slot, and
+      // every lane reads them back four at a time as broadcasts.
+      [[maybe_unused]] const bool bias_slot = EPI && p.epi.act != kActDGelu;
+      [[maybe_unused]] float* const bslot = bias_slots + (warp - 2) * 32;
+      [[maybe_unused]] auto bias_of = [&](int64_t col) {
+        return (p.epi.bias != nullptr && col < p.N) ? ld_nc_f32_here(p.epi.bias + col) : 0.f;
+      };
+      [[maybe_unused]] float bias_next = 0.f;
+      // EPI with GELU' and Z readable by TMA: each chunk's 32 x 32 block of Z
+      // is loaded into the warp's staging buffer, in the layout the chunk's
+      // result takes there, and the result overwrites it in place; the block
+      // of the warp's next chunk is pulled into L2 one chunk ahead.  The
+      // warp's bias slot (unused with GELU') holds the loads' barrier (its
+      // first 8 bytes), the barrier's phase (bit 0 of the next word) and
+      // whether a load was left unobserved (bit 1), so that the GELU kernels
+      // carry no extra registers through their loops.
+      [[maybe_unused]] const uint32_t z_bar = smem_u32(bslot);
+      [[maybe_unused]] volatile uint32_t* const z_word = reinterpret_cast<volatile uint32_t*>(bslot) + 2;
+      if constexpr (EPI) {
+        if (ZT && lane == 0) {
+          mbar_init(z_bar, 1);
+          fence_barrier_init();
+          fence_proxy_async_smem();
+          *z_word = 0u;
+          if (unit0 < p.num_units) {
+            const Unit w0 = decode_unit(unit0, p);
+            tma_prefetch_l2_3d(&tmW, w0.tn * BN + cc_begin * CW, tile_row(w0) * Cfg::BM + sub * 32, 0);
           }
         }
-        if constexpr (Cfg::STAGING_BYTES > 0 && CW == 32) {
-          if (partial ? p.w_tma : p.c_tma) {
-            // Through shared memory: this warp's 32 rows x 32 columns go to
-            // one of its two 4 KB buffers in the 128-byte-swizzled layout the
-            // TMA unit reads (16-byte chunk j of row t sits at chunk j ^ (t % 8)),
-            // then one lane stores the box; the unit clips rows past M and
-            // columns past N.
-            uint8_t* buf = staging + (warp - 2) * 4096;
-            if (lane == 0) bulk_wait_group_read<0>();  // the buffer's previous store has read it
-            __syncwarp();
+        __syncwarp();
+      }
+      if constexpr (EPI) {
+        if (bias_slot && unit0 < p.num_units)
+          bias_next = bias_of(static_cast<int64_t>(decode_unit(unit0, p).tn) * BN + cc_begin * CW + lane);
+      }
+      for (int u = unit0; u < p.num_units; u += unit_step) {
+        const Unit w = decode_unit(u, p);
+        if (!bar_wait<PAIR>(accf_bar(acc), acc_phase, abort_flag, p.status, kDevTimeoutAccFull, p.wait_ns)) break;
+        tc_fence_after();
+        const bool partial = w.partial;
+        const bool read_c = !partial && p.beta != 0.f;
+        const int tm = tile_row(w);
+        const int64_t row = static_cast<int64_t>(tm) * Cfg::BM + sub * 32 + lane;
+        const bool row_ok = row < p.M;
+        const int64_t row_base = partial ? p.ws_row0 : 0;  // C row of row 0 of the destination
+        const int64_t wrow = row - row_base;
+        float* base = partial ? p.ws + static_cast<int64_t>(w.split) * p.ws_slice : p.C;
+        const int64_t ld = partial ? p.ws_ld : p.ldc;
+        float* out = TRANS_C ? base : base + (row_ok ? wrow : 0) * ld;
+        const bool vec_ok = !TRANS_C && (partial || p.c_vec);
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + static_cast<uint32_t>(acc * BN);
+  #pragma unroll 1
+        for (int cc = cc_begin; cc < cc_end; ++cc) {
+          const int64_t col0 = static_cast<int64_t>(w.tn) * BN + cc * CW;
+          // EPI with GELU': Z's values for this row in the chunk's first
+          // quarter, requested before the TMEM load so that both latencies
+          // overlap; each further quarter is requested as a group when the
+          // previous one is done (fetching more at once spilled registers).
+          constexpr int NQH = (CW / 4 + 3) / 4;
+          const bool epi_on = EPI && !partial;
+          const bool epi_fetch_ok = row_ok && col0 < p.N;
+          float4 xe[NQH];
+          if constexpr (EPI) {
+            if (epi_on && !bias_slot && !ZT) epi_fetch<NQH>(p.epi, row, col0, p.N, epi_fetch_ok, xe);
+            if (bias_slot) {
+              __syncwarp();  // every lane has read the slot's previous values
+              bslot[lane] = bias_next;
+              __syncwarp();
+              // the next chunk of this warp: the next one of this tile, or the
+              // first of its next unit's tile
+              int64_t ncol = -1;
+              if (cc + 1 < cc_end)
+                ncol = col0 + CW + lane;
+              else if (u + unit_step < p.num_units)
+                ncol = static_cast<int64_t>(decode_unit(u + unit_step, p).tn) * BN + cc_begin * CW + lane;
+              bias_next = ncol >= 0 ? bias_of(ncol) : 0.f;
+            } else if (ZT && lane == 0) {
+              // the same next chunk's block of Z into L2
+              if (cc + 1 < cc_end) {
+                if (col0 + CW < p.N)
+                  tma_prefetch_l2_3d(&tmW, static_cast<int32_t>(col0 + CW), tm * Cfg::BM + sub * 32, 0);
+              } else if (u + unit_step < p.num_units) {
+                const Unit nw = decode_unit(u + unit_step, p);
+                tma_prefetch_l2_3d(&tmW, nw.tn * BN + cc_begin * CW, tile_row(nw) * Cfg::BM + sub * 32, 0);
+              }
+            }
+          }
+          if constexpr (Cfg::STAGING_BYTES > 0 && CW == 32) {
+            if (partial ? p.w_tma : p.c_tma) {
+              // Through shared memory: this warp's 32 rows x 32 columns go to
+              // one of its two 4 KB buffers in the 128-byte-swizzled layout the
+              // TMA unit reads (16-byte chunk j of row t sits at chunk j ^ (t % 8)),
+              // then one lane stores the box; the unit clips rows past M and
+              // columns past N.
+              uint8_t* buf = staging + (warp - 2) * 4096;
+              if (lane == 0) bulk_wait_group_read<0>();  // the buffer's previous store has read it
+              __syncwarp();
+              [[maybe_unused]] const bool zt = epi_on && ZT;
+              [[maybe_unused]] bool z_fail = false;
+              const float a = partial ? 1.f : p.alpha;
+              // EPI kernels read the chunk from TMEM in two halves of 16
+              // columns (fewer live registers beside the epilogue's inputs).
+              constexpr int SW = EPI ? 16 : CW;
+              with_activation<EPI>(epi_on, p.epi.act, [&](auto act_c) {
+                constexpr int ACT = decltype(act_c)::value;
+                if constexpr (ACT == kActDGelu) {
+                  if (zt && lane == 0) {
+                    mbar_arrive_expect_tx(z_bar, 4096u);
+                    tma_load_3d(smem_u32(buf), &tmW, z_bar, static_cast<int32_t>(col0),
+                                static_cast<int32_t>(tm * Cfg::BM + sub * 32), 0);
+                  }
+                }
+  #pragma unroll
+                for (int hh = 0; hh < CW / SW; ++hh) {
+                  uint32_t r[SW];
+                  __syncwarp();
+                  tmem_ld_32x32b<SW>(t_row + cc * CW + hh * SW, r);
+                  tmem_wait_ld();
+                  if constexpr (ACT == kActDGelu) {
+                    if (zt && hh == 0) {
+                      // the warp decides together, so that a wait that gave up
+                      // takes every lane out of the loop at the same point
+                      const uint32_t par = *z_word & 1u;
+                      const bool ok =
+                          mbar_wait(z_bar, par, abort_flag, p.status, kDevTimeoutEpiInput, p.wait_ns);
+                      z_fail = !__all_sync(0xffffffffu, ok);
+                      if (lane == 0) *z_word = z_fail ? (par | 2u) : (par ^ 1u);
+                    }
+                  }
+  #pragma unroll
+                  for (int qq = 0; qq < SW / 4; ++qq) {
+                    const int q = hh * (SW / 4) + qq;
+                    float4* const slot = reinterpret_cast<float4*>(buf + lane * 128 + ((q ^ (lane & 7)) * 16));
+                    float4 v;
+                    if constexpr (ACT == kActDGelu) {
+                      if (zt) {
+                        v = epi_finish4<ACT>(scaled4(a, r + 4 * qq), *slot);
+                      } else {
+                        if (q > 0 && q % NQH == 0) epi_fetch<NQH>(p.epi, row, col0 + 4 * q, p.N, epi_fetch_ok, xe);
+                        v = epi_finish4<ACT>(scaled4(a, r + 4 * qq), xe[q % NQH]);
+                      }
+                    } else if constexpr (ACT >= 0) {
+                      v = scaled_bias_act4<ACT>(a, r + 4 * qq, reinterpret_cast<const float4*>(bslot)[q]);
+                    } else {
+                      v = scaled4(a, r + 4 * qq);
+                    }
+                    *slot = v;
+                  }
+                }
+              });
+              if constexpr (EPI) {
+                if (z_fail) break;  // the run is being abandoned (status set); Z's load is drained below
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(partial ? &tmW : &tmC, smem_u32(buf), static_cast<int32_t>(col0),
+                             static_cast<int32_t>(tm * Cfg::BM + sub * 32 - row_base), partial ? w.split : 0);
+                bulk_commit_group();
+              }
+              continue;
+            }
+          }
+          // the whole chunk from TMEM, by every lane (a warp-collective load)
+          uint32_t r[CW];
+          __syncwarp();
+          tmem_ld_32x32b<CW>(t_row + cc * CW, r);
+          tmem_wait_ld();
+          if (!row_ok || col0 >= p.N) {
+            // nothing of this chunk is inside C for this thread
+          } else if (vec_ok && col0 + CW <= p.N) {
+            float4* dst = reinterpret_cast<float4*>(out + col0);
+            // All of the chunk's loads of C are issued before any store, so
+            // their latencies overlap (EPI kernels: one quad at a time, to
+            // leave registers for the epilogue's inputs).
+            constexpr int NC = EPI ? 1 : CW / 4;
+            float4 c[NC];
+            if (read_c && !EPI) {
+  #pragma unroll
+              for (int q = 0; q < NC; ++q) c[q] = dst[q];
+            }
             const float a = partial ? 1.f : p.alpha;
-            // EPI kernels read the chunk from TMEM in two halves of 16
-            // columns (fewer live registers beside the epilogue's inputs).
-            constexpr int SW = EPI ? 16 : CW;
             with_activation<EPI>(epi_on, p.epi.act, [&](auto act_c) {
               constexpr int ACT = decltype(act_c)::value;
-#pragma unroll
-              for (int hh = 0; hh < CW / SW; ++hh) {
-                uint32_t r[SW];
-                __syncwarp();
-                tmem_ld_32x32b<SW>(t_row + cc * CW + hh * SW, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int qq = 0; qq < SW / 4; ++qq) {
-                  const int q = hh * (SW / 4) + qq;
-                  float4 v;
-                  if constexpr (ACT == kActDGelu) {
-                    if (q > 0 && q % NQH == 0) epi_fetch<NQH>(p.epi, row, col0 + 4 * q, p.N, epi_fetch_ok, xe);
-                    v = epi_finish4<ACT>(scaled4(a, r + 4 * qq), xe[q % NQH]);
-                  } else if constexpr (ACT >= 0) {
-                    v = scaled_bias_act4<ACT>(a, r + 4 * qq, reinterpret_cast<const float4*>(bslot)[q]);
-                  } else {
-                    v = scaled4(a, r + 4 * qq);
-                  }
-                  *reinterpret_cast<float4*>(buf + lane * 128 + ((q ^ (lane & 7)) * 16)) = v;
+  #pragma unroll
+              for (int q = 0; q < CW / 4; ++q) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if constexpr (ACT == kActDGelu) {
+                  if (q > 0 && q % NQH == 0) epi_fetch<NQH>(p.epi, row, col0 + 4 * q, p.N, epi_fetch_ok, xe);
+                  x = xe[q % NQH];
+                } else if constexpr (ACT >= 0) {
+                  x = reinterpret_cast<const float4*>(bslot)[q];
                 }
+                float4 v = scaled4(a, r + 4 * q);
+                if (read_c) {
+                  const float4 cq = EPI ? dst[q] : c[q % NC];
+                  v.x = fmaf(p.beta, cq.x, v.x);
+                  v.y = fmaf(p.beta, cq.y, v.y);
+                  v.z = fmaf(p.beta, cq.z, v.z);
+                  v.w = fmaf(p.beta, cq.w, v.w);
+                }
+                v = epi_finish4<ACT>(v, x);
+                dst[q] = v;
               }
             });
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_3d(partial ? &tmW : &tmC, smem_u32(buf), static_cast<int32_t>(col0),
-                           static_cast<int32_t>(tm * Cfg::BM + sub * 32 - row_base), partial ? w.split : 0);
-              bulk_commit_group();
+          } else {
+            // TRANS_C: lanes hold consecutive rows, so each access of the warp is contiguous.
+            auto at = [&](int j) { return TRANS_C ? out + (col0 + j) * ld + wrow : out + col0 + j; };
+            float c[CW];
+            if (read_c) {
+  #pragma unroll
+              for (int j = 0; j < CW; ++j) c[j] = (col0 + j < p.N) ? *at(j) : 0.f;
             }
-            continue;
+            const float a = partial ? 1.f : p.alpha;
+  #pragma unroll
+            for (int j = 0; j < CW; ++j) {
+              if (col0 + j < p.N) {
+                float v = a * __uint_as_float(r[j]);
+                if (read_c) v = fmaf(p.beta, c[j], v);
+                if constexpr (EPI) {
+                  if (!partial) v = apply_epilogue(p.epi, v, row, col0 + j);
+                }
+                *at(j) = v;
+              }
+            }
           }
         }
-        // the whole chunk from TMEM, by every lane (a warp-collective load)
-        uint32_t r[CW];
+        tc_fence_before();
         __syncwarp();
-        tmem_ld_32x32b<CW>(t_row + cc * CW, r);
-        tmem_wait_ld();
-        if (!row_ok || col0 >= p.N) {
-          // nothing of this chunk is inside C for this thread
-        } else if (vec_ok && col0 + CW <= p.N) {
-          float4* dst = reinterpret_cast<float4*>(out + col0);
-          // All of the chunk's loads of C are issued before any store, so
-          // their latencies overlap (EPI kernels: one quad at a time, to
-          // leave registers for the epilogue's inputs).
-          constexpr int NC = EPI ? 1 : CW / 4;
-          float4 c[NC];
-          if (read_c && !EPI) {
-#pragma unroll
-            for (int q = 0; q < NC; ++q) c[q] = dst[q];
-          }
-          const float a = partial ? 1.f : p.alpha;
-          with_activation<EPI>(epi_on, p.epi.act, [&](auto act_c) {
-            constexpr int ACT = decltype(act_c)::value;
-#pragma unroll
-            for (int q = 0; q < CW / 4; ++q) {
-              float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-              if constexpr (ACT == kActDGelu) {
-                if (q > 0 && q % NQH == 0) epi_fetch<NQH>(p.epi, row, col0 + 4 * q, p.N, epi_fetch_ok, xe);
-                x = xe[q % NQH];
-              } else if constexpr (ACT >= 0) {
-                x = reinterpret_cast<const float4*>(bslot)[q];
-              }
-              float4 v = scaled4(a, r + 4 * q);
-              if (read_c) {
-                const float4 cq = EPI ? dst[q] : c[q % NC];
-                v.x = fmaf(p.beta, cq.x, v.x);
-                v.y = fmaf(p.beta, cq.y, v.y);
-                v.z = fmaf(p.beta, cq.z, v.z);
-                v.w = fmaf(p.beta, cq.w, v.w);
-              }
-              v = epi_finish4<ACT>(v, x);
-              dst[q] = v;
-            }
-          });
-        } else {
-          // TRANS_C: lanes hold consecutive rows, so each access of the warp is contiguous.
-          auto at = [&](int j) { return TRANS_C ? out + (col0 + j) * ld + wrow : out + col0 + j; };
-          float c[CW];
-          if (read_c) {
-#pragma unroll
-            for (int j = 0; j < CW; ++j) c[j] = (col0 + j < p.N) ? *at(j) : 0.f;
-          }
-          const float a = partial ? 1.f : p.alpha;
-#pragma unroll
-          for (int j = 0; j < CW; ++j) {
-            if (col0 + j < p.N) {
-              float v = a * __uint_as_float(r[j]);
-              if (read_c) v = fmaf(p.beta, c[j], v);
-              if constexpr (EPI) {
-                if (!partial) v = apply_epilogue(p.epi, v, row, col0 + j);
-              }
-              *at(j) = v;
-            }
-          }
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster(dsmem_map(acce_bar(acc), 0));  // the even CTA's MMAs reuse the accumulator
+          else
+            mbar_arrive(acce_bar(acc));
+        }
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
         }
       }
-      tc_fence_before();
+      // A load of Z still in flight (a wait that gave up) lands before the
+      // CTA exits, and so does every TMA store of this warp.
+      if constexpr (EPI) {
+        __syncwarp();
+        if (ZT) {
+          const uint32_t zs = *z_word;
+          if (zs & 2u) drain_wait(z_bar, zs & 1u, p.status, p.wait_ns);
+        }
+      }
+      if (lane == 0) bulk_wait_group<0>();
       __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR)
-          mbar_arrive_cluster(dsmem_map(acce_bar(acc), 0));  // the even CTA's MMAs reuse the accumulator
-        else
-          mbar_arrive(acce_bar(acc));
+    };
+    if constexpr (EPI) {
+      if (p.epi.act == kActDGelu && p.z_tma != 0) {
+        epilogue_role(std::true_type{});
+      } else {
+        epilogue_role(std::false_type{});
       }
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
+    } else {
+      epilogue_role(std::false_type{});
     }
-    // Every TMA store of this warp has completed before the CTA exits.
-    if (lane == 0) bulk_wait_group<0>();
-    __syncwarp();
   }
 
   tc_fence_before();

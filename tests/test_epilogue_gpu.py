@@ -96,6 +96,31 @@ def test_epilogue_matches_oracle(h, mode, M, N, K, tA, tB, opts, fused, act, use
                cin[r0:r1] if cin is not None else None, f"{mode} {M}x{N}x{K} rows {r0}:{r1}")
 
 
+@pytest.mark.parametrize("mode,opts", [("tf32", {"tile_n": 192}), ("bf16", {})])
+@pytest.mark.parametrize("pad,offset", [(0, 0), (4, 0), (3, 0), (4, 1)])
+def test_dgelu_z_layouts(h, mode, opts, pad, offset):
+    """GELU' with Z a view into a wider buffer: rows padded by 4 (Z still
+    read in 32 x 32 blocks by the epilogue's TMA loads, through a map whose
+    row pitch is not N), by 3 (rows no longer 16-byte aligned: per-row loads
+    instead) and shifted by one element (a misaligned start: per-row loads),
+    on ragged M and N."""
+    for k, v in opts.items():
+        h.set_option(k, v)
+    M, N, K = 700, 650, 300
+    ops, _ = _cases.make(mode, M, N, K, False, True, seed=111, dist="normal")
+    Zw = si.normal((M, N + pad + offset), 112).numpy()
+    Z = Zw[:, offset:offset + N]
+    Zd = torch.from_numpy(Zw).cuda()[:, offset:offset + N]
+    assert Zd.stride(0) == N + pad + offset
+    C = torch.full((M, N), float("nan"), device="cuda")
+    h.run(ops.A, ops.B, C, mode=mode, transB=True, act="dgelu", aux=Zd)
+    assert h.check_device() == 0
+    assert h.plan()["epilogue_fused"] == 1
+    Y, D = oracle.gemm(mode, ops.a_host, ops.b_host, transB=True)
+    _check(mode, C.cpu().numpy(), Y, D, "dgelu", None, np.ascontiguousarray(Z), 1.0, 0.0, None,
+           f"{mode} pad {pad} offset {offset}")
+
+
 @pytest.mark.parametrize("mode", ["fp32", "tf32", "bf16"])
 def test_bias_is_exact_on_integers(h, mode):
     """Integer operands and an integer bias: product and bias add are exact."""
