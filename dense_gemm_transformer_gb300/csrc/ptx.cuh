@@ -87,39 +87,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// try_wait with a suspend-time hint: the thread may sleep (up to hint_ns)
-// until the phase completes instead of spinning, leaving the issue slots to
-// the other warps of its SM sub-partition.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-// mbar_wait with sleeping tries (the time limit, abort flag and status word
-// as there; both are checked after every try).
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
-                                                int code, uint64_t limit = kWaitLimitNs) {
-  constexpr uint32_t kHintNs = 20000;
-  if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
-  const uint64_t t0 = globaltimer();
-  for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > limit) {
-      *abort = 1;
-      if (status) atomicExch(status, code);
-      return false;
-    }
-  }
-}
-
 // Bounded wait for work already in flight (copies, MMAs) before a CTA
 // exits: it ignores the abort flag.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status,
