@@ -36,6 +36,8 @@ struct gemm_handle_s {
   int* d_status = nullptr;
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  void* ws_t = nullptr;  // the transposed result of a weight-gradient-shaped TF32 product (run_checked)
+  size_t ws_t_bytes = 0;
   int opt_family = GEMM_FAMILY_AUTO;
   int opt_split_k = 0;
   int opt_tile_n = 0;
@@ -100,6 +102,25 @@ gemm_status_t ensure_ws(gemm_handle_s* h, size_t bytes) {
     return GEMM_ERR_ALLOC;
   }
   h->ws_bytes = want;
+  return GEMM_OK;
+}
+
+// The same for the handle's second buffer.
+gemm_status_t ensure_ws_t(gemm_handle_s* h, size_t bytes) {
+  if (bytes <= h->ws_t_bytes) return GEMM_OK;
+  if (h->ws_t) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+    cudaFree(h->ws_t);
+    h->ws_t = nullptr;
+    h->ws_t_bytes = 0;
+  }
+  size_t want = std::max<size_t>(bytes, size_t(1) << 20);
+  if (cudaMalloc(&h->ws_t, want) != cudaSuccess) {
+    cudaGetLastError();
+    h->ws_t = nullptr;
+    return GEMM_ERR_ALLOC;
+  }
+  h->ws_t_bytes = want;
   return GEMM_OK;
 }
 
@@ -775,6 +796,32 @@ gemm_status_t run_checked(gemm_handle_t h, int mode, int transA, int transB, int
   if (is_fp8(mode))
     return run_tc(h, GEMM_MODE_FP8_E4M3, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, s, swap,
                   fp8_format_a(mode), fp8_format_b(mode));
+  // Weight-gradient-shaped TF32 products, C = A^T B with A stored K x M and
+  // B stored K x N and N well above M (a dW = X^T dY): kind::tf32 reads only
+  // K-major operands, so one operand is moved through TMEM (the kernel's A,
+  // 128-column tiles) and the other is transposed into the workspace first.
+  // Computed as it stands, that transposes the wide B; computed as
+  // C^T = B^T A into a second buffer, B becomes the kernel's A (through
+  // TMEM) and only the narrow A is transposed, and a final transpose of the
+  // M x N result (much smaller than B when K is long) puts C in place.
+  if (mode == GEMM_MODE_TF32 && fam == GEMM_FAMILY_AUTO && !swap && transA == 1 && transB == 0 &&
+      epi.act == dgt::kActNone && epi.bias == nullptr && beta == 0.f && N >= 2 * M && K >= 4096 &&
+      h->opt_tile_n == 0 && h->opt_pair == 0 && h->opt_split_k == 0 && h->opt_pretranspose == 0 &&
+      h->opt_fault_skip == 0) {
+    const int64_t ldt = round_up(M, 4);
+    gemm_status_t st = ensure_ws_t(h, static_cast<size_t>(N * ldt) * sizeof(float));
+    if (st != GEMM_OK) return st;
+    float* ct = static_cast<float*>(h->ws_t);
+    h->opt_tile_n = 128;  // the kernel that takes its A through TMEM
+    h->opt_pair = 1;
+    st = run_tc(h, mode, 1, 0, N, M, K, alpha, B, ldb, A, lda, 0.f, ct, ldt, epi, s, false);
+    h->opt_tile_n = 0;
+    h->opt_pair = 0;
+    if (st != GEMM_OK) return st;
+    if (dgt::launch_transpose(ct, ldt, C, ldc, N, M, 4, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    h->plan.kernels += 1;
+    return GEMM_OK;
+  }
   return run_tc(h, mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, epi, s, swap);
 }
 
@@ -830,6 +877,7 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
   cudaSetDevice(h->device);
   gemm_status_t st = cuda_status(cudaDeviceSynchronize());
   if (h->ws) cudaFree(h->ws);
+  if (h->ws_t) cudaFree(h->ws_t);
   if (h->d_status) cudaFree(h->d_status);
   delete h->tma_cache;
   cudaSetDevice(prev);

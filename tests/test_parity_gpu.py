@@ -262,6 +262,20 @@ def test_tf32_mn_major_a_through_tmem(h, pre, M, N, K, splits):
     _cases.run_and_check(h, "tf32", M, N, min(K, 1024), True, False, seed=92, dist="int", exact=True)
 
 
+@pytest.mark.parametrize("M,N,K", [(384, 1152, 4096), (200, 610, 4100), (129, 1000, 8192)])
+def test_tf32_weight_gradient_form(h, M, N, K):
+    """TF32 C = A^T B with A stored K x M, B stored K x N, N >= 2 M and
+    K >= 4096 (a weight gradient): computed as C^T = B^T A into the
+    handle's second buffer (B through TMEM, only A transposed) and
+    transposed into place.  Ragged M, N and K; alpha scales the product;
+    integer inputs bit-exact."""
+    rows = _cases.sample_rows(M) if M * N * K > 2e9 else None
+    _cases.run_and_check(h, "tf32", M, N, K, True, False, alpha=0.75, seed=95, dist="normal", rows=rows)
+    plan = h.plan()
+    assert plan["family"] == "tc" and plan["tile_n"] == 128 and plan["pair_mma"] == 0, plan
+    _cases.run_and_check(h, "tf32", M, N, K, True, False, seed=96, dist="int", exact=True)
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_many_tiles_persistent_loop(h, mode):
     # More tiles than SMs: every CTA of the persistent grid loops over several
