@@ -436,14 +436,15 @@ def bench_ours(args, world, rank, local):
             bufs[1] = (dev_inputs2, [c for c in bufs[1][1] if re.fullmatch(args.only, c.name)])
         pinned_out = [torch.empty(c.C.shape, dtype=c.C.dtype, pin_memory=True) for c in calls]
         d2h = sum(t.numel() * t.element_size() for t in pinned_out)
-        # Two copy streams per direction, so that transfers can use more
+        # Several copy streams per direction, so that transfers can use more
         # than one copy engine at a time.
-        ups = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-        downs = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+        nq = max(1, args.copy_streams)
+        ups = [torch.cuda.Stream(dev) for _ in range(nq)]
+        downs = [torch.cuda.Stream(dev) for _ in range(nq)]
         done = [torch.cuda.Event() for _ in calls]
-        up_done = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(2)]
+        up_done = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(nq)]
         comp_done = [torch.cuda.Event(), torch.cuda.Event()]
-        down_done = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(2)]
+        down_done = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(nq)]
 
         def e2e_step(s):
             b = s % 2
@@ -451,16 +452,16 @@ def bench_ours(args, world, rank, local):
             for i, up in enumerate(ups):
                 up.wait_event(comp_done[b])  # the GEMMs that last read these inputs are done
                 with torch.cuda.stream(up):
-                    for src, dst in list(zip(pinned_in, ins))[i::2]:
+                    for src, dst in list(zip(pinned_in, ins))[i::nq]:
                         dst.copy_(src, non_blocking=True)
                 up_done[i][b].record(up)
                 stream.wait_event(up_done[i][b])
-            for i in range(2):
+            for i in range(nq):
                 stream.wait_event(down_done[i][b])  # these outputs have been downloaded
             for j, (c, dst, ev) in enumerate(zip(cls, pinned_out, done)):
                 run_call(h, c, stream)
                 ev.record(stream)
-                down = downs[j % 2]
+                down = downs[j % nq]
                 down.wait_event(ev)
                 with torch.cuda.stream(down):
                     dst.copy_(c.C, non_blocking=True)
@@ -1154,6 +1155,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--copy-streams", type=int, default=2, help="copy streams per direction in the end-to-end step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-shape timing of the other configurations in the default line")
