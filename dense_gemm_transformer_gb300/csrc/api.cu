@@ -690,7 +690,7 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
     if (launch_epilogue(M, N, C, ldc, epi, s) != cudaSuccess) return GEMM_ERR_CUDA;
     ++kernels;
   }
-  set_plan(h, swap ? GEMM_FAMILY_SKINNY : GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n, a.pair != 0),
+  set_plan(h, swap ? GEMM_FAMILY_SKINNY : GEMM_FAMILY_TC, 128, tile_n, bk, a.splits, tc_stages(mode, tile_n, a.pair != 0, fuse),
            a.grid, kernels, (swap ? ((pack_b ? 1 : 0) | (pack_a ? 2 : 0)) : ((pack_a ? 1 : 0) | (pack_b ? 2 : 0))));
   h->plan.cluster = a.pair ? 2 : 1;
   h->plan.pair_mma = a.pair;

@@ -166,7 +166,7 @@ struct TcArgs {
 // operands exchanged (C^T = op(B)^T op(A)^T, M and N exchanged) and the
 // kernel stores its tile transposed into the caller's C.
 constexpr int kTcEpiWarps = 8;                        // epilogue warps (two per TMEM lane quarter)
-constexpr int kTcThreads = 32 * (2 + kTcEpiWarps);  // producer + MMA warps + epilogue warps
+constexpr int kTcEpiWarpsEpi = 12;                    // the same in the builds with the fused epilogue
 // The A / B format fields (bits 7-9 / 10-12) of a kind::f8f6f4 instruction
 // descriptor: 0 = E4M3, 1 = E5M2.
 constexpr uint32_t fp8_format_bits(uint32_t a_fmt, uint32_t b_fmt) { return (a_fmt << 7) | (b_fmt << 10); }
@@ -175,7 +175,7 @@ int tc_tile_k(int mode);              // k elements per stage (128 bytes)
 // layouts (as the kernel reads them, after any transpose): TF32 or BF16
 // with a K-major A, and a K-major B in TF32; tiles of 128-256 columns.
 bool tc_epi_ok(int mode, bool a_mn_major, bool b_mn_major);
-int tc_stages(int mode, int tile_n, bool pair);  // pipeline depth (pair: one 256-row MMA per CTA pair)
+int tc_stages(int mode, int tile_n, bool pair, bool epi = false);  // pipeline depth (pair: one 256-row MMA per CTA pair; epi: the fused-epilogue build)
 // Whether the kernel is built for this tile width, pairing and B layout
 // (tile_n 128, 192, 224 or 256; pairs from 192 columns).
 bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major);

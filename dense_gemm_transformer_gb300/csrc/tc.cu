@@ -121,19 +121,27 @@ bool tc_epi_ok(int mode, bool a_mn_major, bool b_mn_major) {
   return mode == 2 || (mode == 1 && !b_mn_major);
 }
 
-int tc_stages(int mode, int tile_n, bool pair) {
+namespace {
+template <int EW>
+int tc_stages_for(int tile_n, bool pair) {
+  if (tile_n == 256 && pair) return TcCfg<2, 256, true, EW>::STAGES;
+  if (tile_n == 224 && pair) return TcCfg<2, 224, true, EW>::STAGES;
+  if (tile_n == 192 && pair) return TcCfg<2, 192, true, EW>::STAGES;
+  if (tile_n == 256) return TcCfg<2, 256, false, EW>::STAGES;
+  if (tile_n == 224) return TcCfg<2, 224, false, EW>::STAGES;
+  if (tile_n == 192) return TcCfg<2, 192, false, EW>::STAGES;
+  if (tile_n == 128) return TcCfg<2, 128, false, EW>::STAGES;
+  return TcCfg<2, 16, false, EW>::STAGES;
+}
+}  // namespace
+
+int tc_stages(int mode, int tile_n, bool pair, bool epi) {
   // a stage holds 128 bytes of K per row in every mode; the block-scaled
-  // modes add their scale atoms to it
+  // modes add their scale atoms to it; the builds with the fused epilogue
+  // stage the stores of more epilogue warps
   if (mode == 4) return TcCfg<4, 16>::STAGES;
   if (mode == 5) return TcCfg<5, 16>::STAGES;
-  if (tile_n == 256 && pair) return TcCfg<2, 256, true>::STAGES;
-  if (tile_n == 224 && pair) return TcCfg<2, 224, true>::STAGES;
-  if (tile_n == 192 && pair) return TcCfg<2, 192, true>::STAGES;
-  if (tile_n == 256) return TcCfg<2, 256>::STAGES;
-  if (tile_n == 224) return TcCfg<2, 224>::STAGES;
-  if (tile_n == 192) return TcCfg<2, 192>::STAGES;
-  if (tile_n == 128) return TcCfg<2, 128>::STAGES;
-  return TcCfg<2, 16>::STAGES;
+  return epi ? tc_stages_for<kTcEpiWarpsEpi>(tile_n, pair) : tc_stages_for<kTcEpiWarps>(tile_n, pair);
 }
 
 bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major) {

@@ -19,7 +19,11 @@
 //               and w+4 split the tile's columns), the fused alpha/beta
 //               update, and the stores; then they release the accumulator
 //               so the next tile's MMAs can start.  Two accumulators let the
-//               epilogue of tile i overlap the mainloop of tile i+1.
+//               epilogue of tile i overlap the mainloop of tile i+1.  The
+//               builds with the fused epilogue (EPI) have twelve epilogue
+//               warps, 2-13, three per lane quarter, each group of four
+//               taking a third of the tile's columns (128 registers a
+//               thread, one stage fewer where their staging needs room).
 //   TF32 with an MN-major A (128-column tiles, one CTA): kind::tf32 reads
 //               only K-major operands from shared memory, so warps 2-5 read
 //               each stage's A tile there (one row of A per lane, down the
@@ -99,8 +103,9 @@ struct TcParams {
 // BHALF: a
 // stage holds one half of the B tile (the two-CTA MMA, where the other CTA
 // of the pair holds the other half).
-template <int MODE, int BN, bool BHALF = false>
+template <int MODE, int BN, bool BHALF = false, int EW_ = kTcEpiWarps>
 struct TcCfg {
+  static constexpr int EW = EW_;  // epilogue warps (a multiple of 4: one group per TMEM lane quarter)
   static constexpr bool BS = MODE >= 4;  // block-scaled: 4 MXFP8, 5 NVFP4 (the swapped small-M form only)
   static constexpr int ES = (MODE >= 3) ? 1 : (MODE == 2) ? 2 : 4;  // operand bytes (coordinate units)
   static constexpr int BM = 128;                      // rows of the tile (UMMA M)
@@ -116,15 +121,22 @@ struct TcCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;
   // Epilogue staging for TMA stores: one buffer of 32 rows x 128 bytes per
   // epilogue warp (the swapped small-M form stores directly and has none).
-  static constexpr int STAGING_BYTES = (BN >= 128) ? kTcEpiWarps * 32 * 128 : 0;
-  // ~192-200 KB of operand stages (as many as fit beside the staging when
-  // a stage holds half of B)
+  static constexpr int STAGING_BYTES = (BN >= 128) ? EW * 32 * 128 : 0;
   // EPI kernels: one 128-byte slot per epilogue warp for the bias values
   // of the 32 columns it is storing (read back as broadcasts).
-  static constexpr int EPI_BYTES = BS ? 0 : kTcEpiWarps * 128;
+  static constexpr int EPI_BYTES = BS ? 0 : EW * 128;
   static constexpr int BAR_BYTES = BS ? 512 : 256;  // barriers, the TMEM address and the abort flag
-  static constexpr int STAGES = BHALF ? (232448 - STAGING_BYTES - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES
-                                      : (BN >= 192) ? 4 : (BN == 128) ? 6 : 200 * 1024 / STAGE_BYTES;
+  // BS: up to RES_ATOMS of the activations' scale atoms held in TMEM for
+  // the whole call (below), staged through RES_BYTES of shared memory
+  static constexpr int RES_ATOMS = BS ? 32 : 0;
+  static constexpr int RES_BYTES = RES_ATOMS * 512;
+  // as many as fit beside the staging when a stage holds half of B, else
+  // the planned count, fewer when the staging of twelve epilogue warps
+  // leaves less room
+  static constexpr int STAGES_FIT =
+      (232448 - STAGING_BYTES - 1024 - BAR_BYTES - RES_BYTES - EPI_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES_PLAN = (BN >= 192) ? 4 : (BN == 128) ? 6 : 200 * 1024 / STAGE_BYTES;
+  static constexpr int STAGES = BHALF ? STAGES_FIT : (STAGES_PLAN < STAGES_FIT ? STAGES_PLAN : STAGES_FIT);
   // Two accumulators, then (BS) one ring slot of scale columns per stage
   // (4 columns per atom, A's atoms then B's); an allocation is a power of
   // two of at least 32 columns.
@@ -133,8 +145,6 @@ struct TcCfg {
   // BS: up to RES_ATOMS of the activations' scale atoms (the same for every
   // weight tile) kept in TMEM for the whole call, after the ring, and
   // staged through RES_BYTES of shared memory after the barriers.
-  static constexpr int RES_ATOMS = BS ? 32 : 0;
-  static constexpr int RES_BYTES = RES_ATOMS * 512;
   static constexpr int RES_COL0 = SF_COL0 + (BS ? STAGES * SF_COLS : 0);
   static constexpr int TMEM_NEED = RES_COL0 + 4 * RES_ATOMS;
   static constexpr int TMEM_COLS = (TMEM_NEED <= 32) ? 32 : (TMEM_NEED <= 64) ? 64 : (TMEM_NEED <= 128) ? 128
@@ -147,7 +157,7 @@ struct TcCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 6 + (BS ? STAGES + 1 : 0);
   // BS builds add a warp that copies every stage's scale atoms into TMEM,
   // so that the MMA thread issues only the MMAs
-  static constexpr int THREADS = kTcThreads + (BS ? 32 : 0);
+  static constexpr int THREADS = 32 * (2 + EW) + (BS ? 32 : 0);
   static constexpr int SMEM_BYTES =
       STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + BAR_BYTES + RES_BYTES + EPI_BYTES;
   static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
@@ -331,12 +341,12 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
 // and the store; partial tiles of a K split stay raw for the slice reduce,
 // which applies it.
 template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C, bool PAIR, bool EPI = false>
-__global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
+__global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR, EPI ? kTcEpiWarpsEpi : kTcEpiWarps>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
                    const TcParams p) {
   static_assert(!EPI || !TRANS_C, "the swapped small-M form applies no epilogue itself");
-  using Cfg = TcCfg<MODE, BN, PAIR>;
+  using Cfg = TcCfg<MODE, BN, PAIR, EPI ? kTcEpiWarpsEpi : kTcEpiWarps>;
   constexpr int S = Cfg::STAGES;
   // TF32 with an MN-major A: kind::tf32 reads only K-major operands from
   // shared memory, so warps 2-5 move each stage's A tile into TMEM (row i of
@@ -402,7 +412,7 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
       // one arrival per epilogue warp (of both CTAs)
-      mbar_init(acce_bar(a), A_TMEM ? 4 : PAIR ? 2 * kTcEpiWarps : kTcEpiWarps);
+      mbar_init(acce_bar(a), A_TMEM ? 4 : PAIR ? 2 * Cfg::EW : Cfg::EW);
     }
     for (int b = 0; b < (A_TMEM ? NA : 0); ++b) {
       mbar_init(afull_bar(b), 4);
@@ -686,7 +696,7 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
         mma_commit(drain_bar);
       drain_wait(drain_bar, 0, p.status, p.wait_ns);
     }
-  } else if (Cfg::BS && warp == 2 + kTcEpiWarps) {
+  } else if (Cfg::BS && warp == 2 + Cfg::EW) {
     // ------------------------------------------------------------ scale copier
     // BS builds: one lane walks the stages in the MMA thread's order and
     // copies each stage's scale atoms (the weights'; the activations' too
@@ -779,15 +789,18 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR>::THREADS, 1)
     auto epilogue_role = [&](auto zt_c) {
       constexpr bool ZT = decltype(zt_c)::value;
       const int sub = warp & 3;          // TMEM lane quarter this warp may access
-      const int half = (warp - 2) >> 2;  // which half of the tile's column chunks it stores
+      const int group = (warp - 2) >> 2;  // which group of the tile's column chunks it stores
       int acc = 0;
       uint32_t acc_phase = 0;
       constexpr int CW = Cfg::CW;
       constexpr int NCH = BN / CW;  // column chunks of a tile
-      // Warps of half 0 take the first ceil(NCH / 2) chunks, half 1 the rest
-      // (A_TMEM: the four epilogue warps take all of them).
-      const int cc_begin = (A_TMEM || half == 0) ? 0 : (NCH + 1) / 2;
-      const int cc_end = (!A_TMEM && half == 0) ? (NCH + 1) / 2 : NCH;
+      // The EW / 4 groups of warps take consecutive runs of chunks, the
+      // first NCH % groups runs one chunk longer (A_TMEM: the four epilogue
+      // warps take all of them).
+      constexpr int NG = A_TMEM ? 1 : Cfg::EW / 4;
+      const int g = A_TMEM ? 0 : group;
+      const int cc_begin = g * (NCH / NG) + (g < NCH % NG ? g : NCH % NG);
+      const int cc_end = cc_begin + NCH / NG + (g < NCH % NG ? 1 : 0);
       // EPI with a bias (or no input at all): lane l holds the bias of column
       // l of the warp's next chunk, loaded one chunk ahead; at the chunk's
       // start the warp puts its 32 values into its shared-memory slot, and

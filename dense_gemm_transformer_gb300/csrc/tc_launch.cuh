@@ -10,7 +10,7 @@ namespace dgt {
 template <int MODE, bool A_MN, bool B_MN, int BN, bool TRANS_C = false, bool PAIR = false, bool EPI = false>
 cudaError_t tc_launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                           const TcParams& p, int grid, cudaStream_t s) {
-  using Cfg = TcCfg<MODE, BN, PAIR>;
+  using Cfg = TcCfg<MODE, BN, PAIR, EPI ? kTcEpiWarpsEpi : kTcEpiWarps>;
   auto kern = tc_gemm_kernel<MODE, A_MN, B_MN, BN, TRANS_C, PAIR, EPI>;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [&] {
