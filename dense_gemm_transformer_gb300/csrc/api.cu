@@ -700,12 +700,14 @@ gemm_status_t run_tc(gemm_handle_s* h, int mode, int transA, int transB, int64_t
 }
 
 // The block-scaled product (gemm_run_block_scaled) after its argument
-// checks: the small-M cluster kernel in its block-scaled build (kernel mode
-// 4 for MXFP8, 5 for NVFP4), swapped like every small-M call -- the weights
-// B (N x K) are the 128-row MMA operand and their scales the kernel's
-// A scales, the activations A (M x K, M <= 16) the 16-row operand.  Codes
-// and scales are read in place; K and the leading dimensions travel in
-// bytes.
+// checks, in the kernels' block-scaled builds (kernel mode 4 for MXFP8, 5
+// for NVFP4).  M <= 16: the small-M kernels, swapped like every small-M
+// call -- the weights B (N x K) are the 128-row MMA operand and their
+// scales the kernel's A scales, the activations A (M x K) the 16-row
+// operand.  M > 16: the persistent kernel on 128 x 128 tiles of one CTA,
+// A and B as they are, every stage bringing both operands' scale atoms.
+// Codes and scales are read in place; K and the leading dimensions travel
+// in bytes.
 gemm_status_t run_block_scaled(gemm_handle_s* h, int mode, int64_t M, int64_t N, int64_t K, float alpha,
                                const void* A, int64_t lda, const void* SA, const void* B, int64_t ldb,
                                const void* SB, float beta, float* C, int64_t ldc, cudaStream_t s) {
@@ -715,6 +717,38 @@ gemm_status_t run_block_scaled(gemm_handle_s* h, int mode, int64_t M, int64_t N,
   const int64_t kbytes = nvfp4 ? K / 2 : K;
   const int64_t lda_b = nvfp4 ? lda / 2 : lda, ldb_b = nvfp4 ? ldb / 2 : ldb;
   const int64_t bs = nvfp4 ? 16 : 32;  // K elements per scale
+  if (M > 16) {
+    const int64_t tiles = ceil_div(M, 128) * ceil_div(N, 128);
+    TcArgs a{};
+    a.mode = kmode;
+    a.fmt8 = mode == GEMM_MODE_MXFP8_E5M2 ? fp8_format_bits(1, 1) : 0u;
+    a.tile_n = 128;
+    a.M = M;
+    a.N = N;
+    a.K = kbytes;
+    a.A = A;
+    a.lda = lda_b;
+    a.B = B;
+    a.ldb = ldb_b;
+    a.C = C;
+    a.ldc = ldc;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.splits = 1;
+    a.kb_per_split = static_cast<int>(ceil_div(kbytes, 128));
+    a.tma_cache = h->tma_cache;
+    a.status = h->d_status;
+    a.grid = static_cast<int>(std::min<int64_t>(tiles, h->sms));
+    a.group_m = 16;
+    a.wait_ns = static_cast<uint64_t>(h->opt_wait_us) * 1000u;
+    a.sfa = static_cast<const uint8_t*>(SA);
+    a.sfb = static_cast<const uint8_t*>(SB);
+    a.sf_groups = block_scale_groups(ceil_div(K, bs));
+    if (launch_tc(a, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    set_plan(h, GEMM_FAMILY_TC, 128, 128, static_cast<int>(nvfp4 ? 256 : 128), 1, tc_stages(kmode, 128, false),
+             a.grid, 1, 0);
+    return GEMM_OK;
+  }
   const int64_t tiles = ceil_div(N, 128);
   const int64_t kb = ceil_div(kbytes, 128);
   // Two or more waves of weight tiles (the vocabulary projection): the
@@ -993,7 +1027,6 @@ gemm_status_t gemm_run_block_scaled(gemm_handle_t h, int mode, int64_t M, int64_
     if (A == nullptr || B == nullptr || SA == nullptr || SB == nullptr) return GEMM_ERR_INVALID_VALUE;
     if (lda < K || ldb < K) return GEMM_ERR_INVALID_VALUE;
     if (nvfp4 && (K % 2 != 0 || lda % 2 != 0 || ldb % 2 != 0)) return GEMM_ERR_INVALID_VALUE;
-    if (M > 16) return GEMM_ERR_NOT_SUPPORTED;
     // the TMA unit and the bulk copies read everything in place
     const int64_t lda_b = nvfp4 ? lda / 2 : lda, ldb_b = nvfp4 ? ldb / 2 : ldb;
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(SA, 16) || !aligned(SB, 16) || lda_b % 16 != 0 ||

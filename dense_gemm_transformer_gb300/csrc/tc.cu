@@ -139,8 +139,8 @@ int tc_stages(int mode, int tile_n, bool pair, bool epi) {
   // a stage holds 128 bytes of K per row in every mode; the block-scaled
   // modes add their scale atoms to it; the builds with the fused epilogue
   // stage the stores of more epilogue warps
-  if (mode == 4) return TcCfg<4, 16>::STAGES;
-  if (mode == 5) return TcCfg<5, 16>::STAGES;
+  if (mode == 4) return tile_n == 128 ? TcCfg<4, 128>::STAGES : TcCfg<4, 16>::STAGES;
+  if (mode == 5) return tile_n == 128 ? TcCfg<5, 128>::STAGES : TcCfg<5, 16>::STAGES;
   return epi ? tc_stages_for<kTcEpiWarpsEpi>(tile_n, pair) : tc_stages_for<kTcEpiWarps>(tile_n, pair);
 }
 
@@ -156,7 +156,8 @@ bool tc_tile_ok(int mode, int tile_n, bool pair, bool b_mn_major) {
 
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   if (a.mode < 1 || a.mode > 5) return cudaErrorInvalidValue;
-  if (a.mode >= 4 && (a.tile_n != 16 || a.a_mn_major || a.b_mn_major)) return cudaErrorInvalidValue;
+  if (a.mode >= 4 && ((a.tile_n != 16 && a.tile_n != 128) || a.pair || a.a_mn_major || a.b_mn_major))
+    return cudaErrorInvalidValue;
   cudaError_t e = tc_init_driver();
   if (e != cudaSuccess) return e;
   const int bk = tc_tile_k(a.mode);
@@ -205,7 +206,8 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
   {
     const int per_kb = a.mode == 5 ? TcCfg<5, 16>::SF_ATOMS : a.mode == 4 ? TcCfg<4, 16>::SF_ATOMS : 0;
     const int64_t res = static_cast<int64_t>(p.num_kb) * per_kb;
-    p.sfb_res = (per_kb > 0 && a.sfb != nullptr && res <= TcCfg<5, 16>::RES_ATOMS && res <= a.sf_groups)
+    p.sfb_res = (a.tile_n == 16 && per_kb > 0 && a.sfb != nullptr && res <= TcCfg<5, 16>::RES_ATOMS &&
+                 res <= a.sf_groups)
                     ? static_cast<int>(res)
                     : 0;
   }
@@ -242,7 +244,7 @@ cudaError_t launch_tc(const TcArgs& a, cudaStream_t stream) {
                             a.M * a.epi.ld_aux) == cudaSuccess)
                   ? 1
                   : 0;
-  if (a.mode >= 4) return tc_launch_bs(a.mode, ta, tb, tcm, twm, p, a.grid, stream);
+  if (a.mode >= 4) return tc_launch_bs(a.mode, a.tile_n, ta, tb, tcm, twm, p, a.grid, stream);
   if (a.fuse_epi) {
     if (a.tile_n < 128 || !tc_epi_ok(a.mode, a.a_mn_major != 0, a.b_mn_major != 0)) return cudaErrorNotSupported;
     if (a.mode == 1)

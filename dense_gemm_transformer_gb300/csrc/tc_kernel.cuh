@@ -106,7 +106,7 @@ struct TcParams {
 template <int MODE, int BN, bool BHALF = false, int EW_ = kTcEpiWarps>
 struct TcCfg {
   static constexpr int EW = EW_;  // epilogue warps (a multiple of 4: one group per TMEM lane quarter)
-  static constexpr bool BS = MODE >= 4;  // block-scaled: 4 MXFP8, 5 NVFP4 (the swapped small-M form only)
+  static constexpr bool BS = MODE >= 4;  // block-scaled: 4 MXFP8, 5 NVFP4 (swapped small-M form, or 128-column tiles)
   static constexpr int ES = (MODE >= 3) ? 1 : (MODE == 2) ? 2 : 4;  // operand bytes (coordinate units)
   static constexpr int BM = 128;                      // rows of the tile (UMMA M)
   static constexpr int BK = 128 / ES;                 // K units per stage: one 128-byte swizzle row
@@ -150,7 +150,8 @@ struct TcCfg {
   static constexpr int TMEM_COLS = (TMEM_NEED <= 32) ? 32 : (TMEM_NEED <= 64) ? 64 : (TMEM_NEED <= 128) ? 128
                                    : (TMEM_NEED <= 256) ? 256 : 512;
   static_assert(TMEM_NEED <= 512, "TMEM columns");
-  static_assert(!BS || (BN == 16 && !BHALF), "block-scaled: the swapped small-M form");
+  static_assert(!BS || ((BN == 16 || BN == 128) && !BHALF),
+                "block-scaled: the swapped small-M form, or 128-column tiles of one CTA");
   static constexpr int CW = BN < 32 ? BN : 32;                    // accumulator columns per TMEM load
   // full/empty per stage, acc full/empty x2, drain, resident scales; BS
   // also: per stage "scale atoms copied", and the copier's drain
@@ -532,13 +533,15 @@ __global__ void __launch_bounds__(TcCfg<MODE, BN, PAIR, EPI ? kTcEpiWarpsEpi : k
               tma_load_2d(b_dst, &tmB, fb, k0, w.tn * BN);
             }
             if constexpr (Cfg::BS) {
-              // both operands' scale atoms for this stage (B: the activations,
-              // one row tile)
+              // both operands' scale atoms for this stage (the swapped form's
+              // B: the activations, one row tile; 128-column tiles: B's tile
+              // w.tn of 128 rows)
               const uint32_t sf_dst = b_dst + Cfg::B_BYTES;
               bulk_copy_g2s(sf_dst, p.sfa + (static_cast<int64_t>(tm) * p.sf_groups + kb * Cfg::SF_ATOMS) * 512,
                             Cfg::SF_BYTES, fb);
               if (p.sfb_res == 0)
-                bulk_copy_g2s(sf_dst + Cfg::SF_BYTES, p.sfb + static_cast<int64_t>(kb) * Cfg::SF_ATOMS * 512,
+                bulk_copy_g2s(sf_dst + Cfg::SF_BYTES,
+                              p.sfb + (static_cast<int64_t>(TRANS_C ? 0 : w.tn) * p.sf_groups + kb * Cfg::SF_ATOMS) * 512,
                               Cfg::SF_BYTES, fb);
             }
           }

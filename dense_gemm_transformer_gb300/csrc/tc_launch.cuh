@@ -134,9 +134,9 @@ cudaError_t tc_launch_fp8(int tile_n, bool pair, bool a_mn, bool b_mn, const CUt
 cudaError_t tc_launch_fp8_mid(int tile_n, bool pair, bool a_mn, bool b_mn, const CUtensorMap& ta,
                               const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& tw,
                               const TcParams& p, int grid, cudaStream_t s);
-// The swapped small-M form for block-scaled operands (mode 4 MXFP8, 5
-// NVFP4): tc_bs.cu.
-cudaError_t tc_launch_bs(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+// Block-scaled operands (mode 4 MXFP8, 5 NVFP4), the swapped small-M form
+// (tile_n 16) or 128 x 128 tiles: tc_bs.cu.
+cudaError_t tc_launch_bs(int mode, int tile_n, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                          const CUtensorMap& tw, const TcParams& p, int grid, cudaStream_t s);
 
 // The same kernels with the fused epilogue (EPI), K-major A: tc_tf32_epi.cu

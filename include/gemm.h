@@ -336,12 +336,14 @@ gemm_status_t gemm_noalloc_check_device(void* stream);
  * ldb even; a row is lda / 2 bytes); C is M x N fp32, ldc >= N.  SA and SB
  * are the scales of A (M x ceil(K / bs)) and B (N x ceil(K / bs)) in the
  * tiled layout gemm_block_scales_tile writes.  A partial last block is
- * allowed.  Served for the decode shape, M <= 16, by the small-M kernel (K
- * split across a thread-block cluster; the scale atoms of every pipeline
- * stage are copied into tensor memory with tcgen05.cp).
+ * allowed.  Served for the decode shape, M <= 16, by the small-M kernels (K
+ * split across a thread-block cluster, or the persistent swapped form for
+ * wide weights), and for M > 16 by the persistent kernel on 128 x 128
+ * tiles; the scale atoms of every pipeline stage are copied into tensor
+ * memory with tcgen05.cp.
  * Errors: GEMM_ERR_INVALID_VALUE for another mode, negative sizes, a null
- * pointer, lda or ldb < K, an odd K / lda / ldb in NVFP4; GEMM_ERR_NOT_SUPPORTED
- * for M > 16; GEMM_ERR_MISALIGNED when A, B, SA or SB is not 16-byte aligned
+ * pointer, lda or ldb < K, an odd K / lda / ldb in NVFP4;
+ * GEMM_ERR_MISALIGNED when A, B, SA or SB is not 16-byte aligned
  * or a row of A or B is not a multiple of 16 bytes.  M == 0 or N == 0 is a
  * no-op; K == 0 or alpha == 0 gives C = beta * C.  Asynchronous on `stream`. */
 gemm_status_t gemm_run_block_scaled(gemm_handle_t h, int mode, int64_t M, int64_t N, int64_t K, float alpha,

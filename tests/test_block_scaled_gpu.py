@@ -1,7 +1,7 @@
 """Block-scaled products (gemm_run_block_scaled) against the oracle's
 block-scaled definition: MXFP8 (E4M3 / E5M2 elements, one E8M0 scale per 32
-K) and NVFP4 (E2M1 elements two per byte, one UE4M3 scale per 16 K), for the
-decode shape M <= 16.
+K) and NVFP4 (E2M1 elements two per byte, one UE4M3 scale per 16 K): the
+decode shape M <= 16 (the small-M kernels) and M > 16 (128 x 128 tiles).
 
 Products of the decoded elements and scales are exact in fp32 and the tensor
 cores accumulate in fp32, so the FP8 gate (2e-3 of |alpha| D) applies.
@@ -210,15 +210,40 @@ def test_scale_tiling_layout(h):
     assert np.array_equal(T, want)
 
 
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("M,N,K", [(200, 300, 1056), (256, 256, 4096), (1000, 130, 520), (17, 129, 96)])
+def test_block_scaled_large_m(h, mode, M, N, K):
+    """M > 16: the persistent kernel on 128 x 128 tiles, both operands'
+    scale atoms brought with every stage.  Ragged M and N, a partial last
+    stage (K = 1056, 520, 96) and a partial last block (K = 520 in MXFP8:
+    16.25 blocks of 32), alpha / beta, then integers with power-of-two
+    scales bit-exact."""
+    elem, bs, sf = MODES[mode]
+    ac, sa = si.to_block_scaled(si.normal((M, K), 621), elem, bs, sf)
+    bc, sb = si.to_block_scaled(si.normal((N, K), 622, std=0.02), elem, bs, sf)
+    got = _run(h, mode, ac, sa, bc, sb, M, N)
+    ref, D = _oracle(mode, ac, sa, bc, sb)
+    _gate.assert_within("fp8", got, ref, D, what=f"{mode} {M}x{N}x{K}")
+    plan = h.plan()
+    assert plan["family"] == "tc" and plan["tile_n"] == 128, plan
+    c0 = si.normal((M, N), 623)
+    got = _run(h, mode, ac, sa, bc, sb, M, N, alpha=0.75, beta=-0.5, c0=c0)
+    ref, D = _oracle(mode, ac, sa, bc, sb, alpha=0.75, beta=-0.5, c0=c0)
+    _gate.assert_within("fp8", got, ref, D, 0.75, -0.5, c0.numpy(), what=f"{mode} {M}x{N}x{K} alpha/beta")
+    rng = np.random.default_rng(624 + M + K)
+    nb = -(-K // bs)
+    ac, bc = _integer_codes(mode, (M, K), rng), _integer_codes(mode, (N, K), rng)
+    sa, sb = _pow2_scales(mode, M, nb, rng), _pow2_scales(mode, N, nb, rng)
+    got = _run(h, mode, ac, sa, bc, sb, M, N)
+    ref, _ = _oracle(mode, ac, sa, bc, sb)
+    assert np.array_equal(got.astype(np.float64), ref), f"{mode} {M}x{N}x{K} integers"
+
+
 def test_block_scaled_argument_checks(h):
     C = torch.full((4, 256), 5.0, device="cuda")
     A = torch.zeros((4, 64), dtype=torch.uint8, device="cuda")
     B = torch.zeros((256, 64), dtype=torch.uint8, device="cuda")
     S = dg.tile_block_scales(torch.zeros((256, 4), dtype=torch.uint8, device="cuda"))
-    with pytest.raises(dg.GemmError) as e:  # M > 16
-        h.run_block_scaled(torch.zeros((17, 64), dtype=torch.uint8, device="cuda"), S, B, S,
-                           torch.zeros((17, 256), device="cuda"), mode="mxfp8_e4m3")
-    assert e.value.status == 2
     with pytest.raises(dg.GemmError) as e:  # scales not 16-byte aligned
         h.run_block_scaled(A, S[1:], B, S, C, mode="mxfp8_e4m3")
     assert e.value.status == 3
