@@ -126,9 +126,10 @@ struct TcCfg {
   // of the 32 columns it is storing (read back as broadcasts).
   static constexpr int EPI_BYTES = BS ? 0 : EW * 128;
   static constexpr int BAR_BYTES = BS ? 512 : 256;  // barriers, the TMEM address and the abort flag
-  // BS: up to RES_ATOMS of the activations' scale atoms held in TMEM for
-  // the whole call (below), staged through RES_BYTES of shared memory
-  static constexpr int RES_ATOMS = BS ? 32 : 0;
+  // BS, swapped small-M form: up to RES_ATOMS of the activations' scale
+  // atoms held in TMEM for the whole call (below), staged through RES_BYTES
+  // of shared memory (the 128-column tiles' B scales change with the tile)
+  static constexpr int RES_ATOMS = (BS && BN == 16) ? 32 : 0;
   static constexpr int RES_BYTES = RES_ATOMS * 512;
   // as many as fit beside the staging when a stage holds half of B, else
   // the planned count, fewer when the staging of twelve epilogue warps
