@@ -548,6 +548,13 @@ def sweep_cases(workload):
         for M, N, K in ((4096, 4096, 4096),) + si.LARGE_BF16:
             out.append((f"fp8.{M}x{N}x{K}.T", "fp8", si.GemmCase(f"{M}x{N}x{K}.T", False, True, M, N, K),
                         1.0, 0.0, 1.0))
+    elif workload == "large_bs":
+        # block-scaled operands with M > 16, both stored K-major (B N x K):
+        # random finite codes and scales, as for the decode shapes below
+        for mode in ("mxfp8_e4m3", "nvfp4"):
+            for M, N, K in ((4096, 4096, 4096),) + si.LARGE_BF16:
+                out.append((f"{mode}.{M}x{N}x{K}.T", mode, si.GemmCase(f"{M}x{N}x{K}.T", False, True, M, N, K),
+                            1.0, 0.0, 1.0))
     elif workload in ("skinny_nvfp4", "skinny_mxfp8"):
         # block-scaled weights stored N x K (the form the kernels read): random
         # finite codes and scales (a quantiser would only change their values)
@@ -1171,7 +1178,8 @@ def main():
     ap.add_argument("--pair", type=int, default=None,
                     help="sweeps: CTA pairs issuing one 256-row MMA (0 wherever allowed, 1 never)")
     ap.add_argument("--split-k", type=int, default=0, help="sweeps: force this many K slices (0: planner)")
-    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "large_fp8", "skinny", "skinny_fp8",
+    ap.add_argument("--workload", default="gpt", choices=["gpt", "square", "large", "large_fp8", "large_bs", "skinny",
+                                                          "skinny_fp8",
                                                           "skinny_nvfp4", "skinny_mxfp8", "epilogue", "gpt_full",
                                                           "attention"],
                     help="gpt: the timed step; the others print a per-shape sweep")
