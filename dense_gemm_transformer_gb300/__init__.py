@@ -33,7 +33,7 @@ BLOCK_SCALED_MODES = {"mxfp8_e4m3": (7, "e4m3", 32, "e8m0"), "mxfp8_e5m2": (8, "
                       "nvfp4": (9, "e2m1", 16, "ue4m3")}
 FAMILIES = {"auto": 0, "simt": 1, "tc": 2, "skinny": 3}
 OPTIONS = {"family": 1, "split_k": 2, "tile_n": 3, "pretranspose": 4, "pair": 5, "wait_limit_us": 6,
-           "fault_skip_stage": 7}
+           "fault_skip_stage": 7, "sk_fixup": 8}
 STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_VALUE", 2: "GEMM_ERR_NOT_SUPPORTED", 3: "GEMM_ERR_MISALIGNED",
           4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_ALLOC", 6: "GEMM_ERR_DEVICE_TIMEOUT", 7: "GEMM_ERR_TOO_LARGE"}
 HEADER = os.path.join(_build.ROOT, "include", "gemm.h")
@@ -59,7 +59,8 @@ class Plan(ctypes.Structure):
                 ("tile_k", ctypes.c_int32), ("split_k", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("kernels", ctypes.c_int32), ("packed", ctypes.c_int32),
                 ("schedule", ctypes.c_int32), ("cluster", ctypes.c_int32), ("pair_mma", ctypes.c_int32),
-                ("epilogue_fused", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("epilogue_fused", ctypes.c_int32), ("sk_fixup", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 _lib = None
@@ -183,7 +184,8 @@ class Gemm:
                 "tile_k": p.tile_k, "split_k": p.split_k, "stages": p.stages, "grid": p.grid,
                 "kernels": p.kernels, "packed": p.packed,
                 "schedule": {0: "tiles", 1: "split_k", 2: "stream_k", 3: "tail_split"}.get(p.schedule, "tiles"),
-                "cluster": p.cluster, "pair_mma": p.pair_mma, "epilogue_fused": p.epilogue_fused}
+                "cluster": p.cluster, "pair_mma": p.pair_mma, "epilogue_fused": p.epilogue_fused,
+                "sk_fixup": {1: "kernel", 2: "inline"}.get(p.sk_fixup, "none")}
 
     def check_device(self, stream=None) -> int:
         """Synchronize the stream and return the device status (0 = ok)."""

@@ -33,7 +33,7 @@
 struct gemm_handle_s {
   int device = 0;
   int sms = 0;
-  int* d_status = nullptr;
+  int* d_status = nullptr;   // the status word, then (from word kSkCntOffset) the SIMT stream-K arrival counters
   void* ws = nullptr;
   size_t ws_bytes = 0;
   void* ws_t = nullptr;  // the transposed result of a weight-gradient-shaped TF32 product (run_checked)
@@ -45,6 +45,7 @@ struct gemm_handle_s {
   int opt_pair = 0;
   int64_t opt_wait_us = 0;   // bounded-wait limit of the tcgen05 kernel (0: the default)
   int opt_fault_skip = 0;    // test hook (GEMM_OPT_FAULT_SKIP_STAGE)
+  int opt_sk_fixup = 0;      // GEMM_OPT_SK_FIXUP
   int sk_active[5][dgt::kSkinnyMaxCluster + 1];  // small-M kernel per mode (TF32, BF16, FP8, MXFP8, NVFP4): resident clusters (-1: not queried)
   dgt::TmaCache* tma_cache = nullptr;             // TMA descriptors of earlier calls
   gemm_plan_t plan{};
@@ -54,6 +55,7 @@ struct gemm_handle_s {
 namespace {
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+constexpr int kSkCntOffset = 64;  // words: the counters start 256 bytes after the status word
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -237,6 +239,16 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
     // at least 8 k-tiles per CTA when stream-K is all there is
     a.grid = a.dp_tiles > 0 ? g : std::max<int64_t>(1, std::min<int64_t>(g, a.iters / 8));
     grid = static_cast<int>(a.grid);
+    // A tile cut into about two parts (runs of at least half its k-tiles) is
+    // summed by the last CTA to finish a part of it, from L2, without a
+    // fixup launch: measured on the GPT products, 10 us less per call on the
+    // 256-column tiles of the K = 384 products (about two parts a tile), but
+    // 5-7 us more where 128-column tiles have about five parts (one CTA then
+    // reads more partials than the fixup kernel's 16 CTAs per tile), so
+    // those, and deep-K tiles with dozens of parts, keep the fixup kernel.
+    const bool few_parts = h->opt_sk_fixup == 2 || (h->opt_sk_fixup == 0 && kt <= 2 * (a.iters / a.grid));
+    a.sk_inline = (few_parts && tiles - a.dp_tiles <= kSimtInlineMaxTiles) ? 1 : 0;
+    a.sk_cnt = h->d_status + kSkCntOffset;
   }
   // Workspace: [split-K slices or stream-K slots][A transposed][B transposed].
   size_t part_bytes = 0;
@@ -256,7 +268,7 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   }
   char* ws = static_cast<char*>(h->ws);
   if (part_bytes > 0) a.ws = reinterpret_cast<float*>(ws);
-  if (a.schedule == kSimtStreamK) ++kernels;  // the fixup
+  if (a.schedule == kSimtStreamK && !a.sk_inline) ++kernels;  // the fixup
   if (a.schedule != kSimtStreamK && ceil_div(M, kSimtTileM) > 65535) return GEMM_ERR_NOT_SUPPORTED;
   if (tr_a) {
     float* at = reinterpret_cast<float*>(ws + a_off);
@@ -302,6 +314,7 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
   set_plan(h, GEMM_FAMILY_SIMT, kSimtTileM, tile_n, kSimtTileK, a.splits, tile_n == 256 ? 4 : 3, grid, kernels,
            ((tr_a || pk_a) ? 1 : 0) | ((tr_b || pk_b) ? 2 : 0));
   h->plan.schedule = a.schedule;
+  h->plan.sk_fixup = a.schedule != kSimtStreamK ? 0 : a.sk_inline ? 2 : 1;
   return GEMM_OK;
 }
 
@@ -884,12 +897,13 @@ gemm_status_t gemm_create(gemm_handle_t* out) {
   h->sms = sms;
   for (auto& per_mode : h->sk_active)
     for (int& n : per_mode) n = -1;
-  if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess) {
+  const size_t status_bytes = (kSkCntOffset + dgt::kSimtInlineMaxTiles) * sizeof(int);
+  if (cudaMalloc(&h->d_status, status_bytes) != cudaSuccess) {
     cudaGetLastError();
     delete h;
     return GEMM_ERR_ALLOC;
   }
-  if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
+  if (cudaMemset(h->d_status, 0, status_bytes) != cudaSuccess) {
     cudaFree(h->d_status);
     delete h;
     return GEMM_ERR_CUDA;
@@ -1000,6 +1014,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, int option, int64_t value) {
     case GEMM_OPT_FAULT_SKIP_STAGE:
       if (value < 0 || value > (int64_t(1) << 30)) return GEMM_ERR_INVALID_VALUE;
       h->opt_fault_skip = static_cast<int>(value);
+      return GEMM_OK;
+    case GEMM_OPT_SK_FIXUP:
+      if (value < 0 || value > 2) return GEMM_ERR_INVALID_VALUE;
+      h->opt_sk_fixup = static_cast<int>(value);
       return GEMM_OK;
     default:
       return GEMM_ERR_INVALID_VALUE;

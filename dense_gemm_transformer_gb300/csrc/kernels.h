@@ -115,8 +115,14 @@ struct SimtArgs {
   int64_t grid;
   float* ws;
   int64_t ws_ld;
+  // stream-K: 1 when the last CTA to store a partial of a tile sums the
+  // tile's partials itself (no fixup kernel); sk_cnt then holds one arrival
+  // counter per tile from dp_tiles on, zero between calls.
+  int sk_inline;
+  int* sk_cnt;
 };
 constexpr int kSimtTileM = 128, kSimtTileN = 128, kSimtTileK = 16, kSimtThreads = 256;
+constexpr int kSimtInlineMaxTiles = 1024;  // arrival counters a handle keeps
 int64_t simt_streamk_slot_floats(int tile_n);  // floats per stream-K partial slot
 cudaError_t launch_simt(const SimtArgs& a, cudaStream_t stream);
 

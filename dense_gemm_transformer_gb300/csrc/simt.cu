@@ -232,6 +232,14 @@ __host__ __device__ __forceinline__ int64_t sk_begin(int64_t c, int64_t iters, i
   return c * iters / grid;
 }
 
+// The stream-K CTA whose run holds iteration x.
+__device__ __forceinline__ int64_t sk_owner(int64_t x, int64_t iters, int64_t grid) {
+  int64_t c = x * grid / iters;
+  while (c + 1 < grid && sk_begin(c + 1, iters, grid) <= x) ++c;
+  while (c > 0 && sk_begin(c, iters, grid) > x) --c;
+  return c;
+}
+
 template <int TBN, bool TA, bool TB, bool VEC, bool CVEC>
 __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel(SimtArgs p) {
   using Cfg = SimtCfg<TBN>;
@@ -264,6 +272,8 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
     Segment sg;
     int64_t it, it_end, dp;
     int valid;
+    int last, nparts;        // inline stream-K fixup: this CTA sums the tile; its parts
+    int64_t part0, owner0;   // slot of the first part, and the CTA that stored it
   };
   __shared__ SegState sh;
   if (tid == 0) {
@@ -431,7 +441,7 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
     __syncthreads();  // the ring is idle before the next segment refills it
 
     // Epilogue.  Rows am + {0..3}, am + 16 + {0..3}; cols bn + 32q + {0..3}.
-    const int dest = sh.sg.dest;
+    int dest = sh.sg.dest;
     const int64_t index = sh.sg.index;
     const int64_t em0 = (sh.sg.tile / tiles_n) * BM;  // re-read: the mainloop kept no copy
     const int64_t en0 = (sh.sg.tile % tiles_n) * TBN;
@@ -446,7 +456,57 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
           *reinterpret_cast<float4*>(rowp + 32 * q) =
               make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
       }
-      continue;
+      if (!p.sk_inline) continue;
+      // Inline fixup: the partial is published (fence, then one arrival on
+      // the tile's counter); the CTA whose arrival completes the count sums
+      // every part of the tile, in ascending k order as the fixup kernel
+      // does, and stores the tile through the normal epilogue.  It also
+      // resets the counter for the next call.
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        const int64_t t = sh.sg.tile - p.dp_tiles;
+        const int64_t f = t * kt, l = f + kt - 1;
+        const int64_t cf = sk_owner(f, p.iters, p.grid), cl = sk_owner(l, p.iters, p.grid);
+        const int n = static_cast<int>(cl - cf + 1);
+        const int prev = atomicAdd(p.sk_cnt + t, 1);
+        sh.last = prev == n - 1;
+        if (sh.last) atomicExch(p.sk_cnt + t, 0);
+        sh.nparts = n;
+        sh.owner0 = cf;
+        sh.part0 = 2 * cf + (sk_begin(cf, p.iters, p.grid) >= f ? 0 : 1);
+      }
+      __syncthreads();
+      if (!sh.last) continue;
+      __threadfence();
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+      // Four rows at a time, one part at a time: at most 4 x QN float4 loads
+      // in flight, so the sum needs no more registers than the mainloop.
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+#pragma unroll 1
+        for (int j = 0; j < sh.nparts; ++j) {
+          // parts after the first start their CTA's run: slot 2c
+          const int64_t sl = j == 0 ? sh.part0 : 2 * (sh.owner0 + j);
+          const float* __restrict__ src = p.ws + sl * (BM * TBN) + (am + 16 * g) * TBN + bn;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+#pragma unroll
+            for (int q = 0; q < QN; ++q) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(src + r * TBN + 32 * q));
+              float* a = acc[4 * g + r] + 4 * q;
+              a[0] += v.x;
+              a[1] += v.y;
+              a[2] += v.z;
+              a[3] += v.w;
+            }
+          }
+        }
+      }
+      dest = kToC;
     }
     const bool partial = dest == kToSlice;
     float* __restrict__ out = partial ? p.ws + index * p.M * p.ws_ld : p.C;
@@ -509,13 +569,7 @@ __global__ void __launch_bounds__(NT) simt_streamk_fixup_kernel(SimtArgs p) {
   if (threadIdx.x == 0) {
     const int64_t kt = (p.K + BK - 1) / BK;
     const int64_t f = (tile - p.dp_tiles) * kt, l = f + kt - 1;
-    auto owner = [&](int64_t x) {
-      int64_t c = x * p.grid / p.iters;
-      while (c + 1 < p.grid && sk_begin(c + 1, p.iters, p.grid) <= x) ++c;
-      while (c > 0 && sk_begin(c, p.iters, p.grid) > x) --c;
-      return c;
-    };
-    const int64_t cf = owner(f), cl = owner(l);
+    const int64_t cf = sk_owner(f, p.iters, p.grid), cl = sk_owner(l, p.iters, p.grid);
     int n = 0;
     if (cf != cl) {
       for (int64_t c = cf; c <= cl && n < kMaxParts; ++c)
@@ -606,7 +660,7 @@ cudaError_t launch_tbn(const SimtArgs& a, cudaStream_t stream) {
     e = launch_vec<TBN, true, false>(a, grid, stream, vec, cvec);
   else
     e = launch_vec<TBN, true, true>(a, grid, stream, vec, cvec);
-  if (e != cudaSuccess || a.schedule != kSimtStreamK) return e;
+  if (e != cudaSuccess || a.schedule != kSimtStreamK || a.sk_inline) return e;
   const int64_t tiles = ((a.M + BM - 1) / BM) * ((a.N + TBN - 1) / TBN);
   return launch_pdl(simt_streamk_fixup_kernel<TBN>, dim3(static_cast<unsigned>((tiles - a.dp_tiles) * kFixupChunks)),
                     dim3(NT), 0, stream, a);

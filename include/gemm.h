@@ -121,7 +121,7 @@ typedef enum {
                                  status word and returns.  0 = the default, 2 seconds; at most
                                  60 s.  A limit shorter than the call's own stages take makes
                                  correct calls time out.                                       */
-  GEMM_OPT_FAULT_SKIP_STAGE = 7 /* TC, a test hook for the bounded-wait path: n > 0 makes the
+  GEMM_OPT_FAULT_SKIP_STAGE = 7, /* TC, a test hook for the bounded-wait path: n > 0 makes the
                                    first CTA's TMA producer of the persistent tcgen05 kernel
                                    issue no copies for the n-th pipeline stage it takes, so
                                    that the MMA's wait for that stage runs out (after the
@@ -130,6 +130,12 @@ typedef enum {
                                    undefined, and gemm_check_device reports
                                    GEMM_ERR_DEVICE_TIMEOUT.  Forces one CTA per tile (no pairs).
                                    0 = off (the default).  Nothing faults or hangs.             */
+  GEMM_OPT_SK_FIXUP = 8       /* SIMT stream-K: how the partial tiles are summed.  0 = planner's
+                                 choice (by the last CTA to finish a part of each tile when
+                                 every tile is cut into a few long parts, else by a separate
+                                 fixup kernel), 1 = always the fixup kernel, 2 = by the last CTA
+                                 wherever the tiles cut into parts number at most 1024.  The
+                                 sums are the same either way (ascending k order).            */
 } gemm_option_t;
 
 /* Elementwise work fused into the GEMM's epilogue (gemm_run_epilogue), the
@@ -168,7 +174,9 @@ typedef struct {
   int32_t cluster;       /* TC: CTAs per cluster (2 = CTA pairs); small M: K slices per cluster */
   int32_t pair_mma;      /* TC: 1 when each CTA pair issues one 256-row MMA (tcgen05 cta_group::2) */
   int32_t epilogue_fused; /* gemm_run_epilogue: 1 when the GEMM kernel itself applied the epilogue */
-  int32_t reserved[3];
+  int32_t sk_fixup;      /* SIMT stream-K: 1 partial tiles summed by a separate fixup kernel,
+                            2 by the last CTA to finish a part of each tile (0 otherwise) */
+  int32_t reserved[2];
 } gemm_plan_t;
 
 /* Create a handle on the current device.  Reads the device properties and

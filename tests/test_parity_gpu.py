@@ -36,6 +36,7 @@ def _reset(h):
     h.set_option("tile_n", 0)
     h.set_option("pretranspose", 0)
     h.set_option("pair", 0)
+    h.set_option("sk_fixup", 0)
     yield
 
 
@@ -176,6 +177,39 @@ def test_fp32_stream_k(h, tA, tB, M, N, K):
     _cases.run_and_check(h, "fp32", M, N, K, tA, tB, alpha=0.5, beta=0.75, seed=61, dist="normal", rows=rows)
     assert h.plan()["schedule"] == "stream_k"
     _cases.run_and_check(h, "fp32", M, N, min(K, 1024), tA, tB, seed=62, dist="int", exact=True)
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("M,N,K,tA,tB,auto", [(5000, 1000, 520, True, False, "inline"),
+                                              (4000, 384, 384, False, False, "kernel"),
+                                              (1000, 700, 3000, False, True, "kernel"),
+                                              (130, 390, 20000, True, True, "kernel")])
+def test_fp32_stream_k_fixup_forms(h, tile_n, M, N, K, tA, tB, auto):
+    """Stream-K partial tiles summed by the fixup kernel or by the last CTA
+    to finish a part of each tile: both sum the parts in ascending k order,
+    so the results are bit-identical, and the per-tile arrival counters the
+    second form uses are back at zero after every call (it runs twice)."""
+    ops, c0 = _cases.make("fp32", M, N, K, tA, tB, seed=63, dist="normal", with_c=True)
+    out = {}
+    for fix in (0, 1, 2, 2):
+        h.set_option("tile_n", tile_n)
+        h.set_option("sk_fixup", fix)
+        C = c0.clone().cuda()
+        h.run(ops.A, ops.B, C, mode="fp32", transA=tA, transB=tB, alpha=0.5, beta=0.75)
+        assert h.check_device() == 0
+        plan = h.plan()
+        if plan["schedule"] != "stream_k":
+            pytest.skip(f"tile_n {tile_n}: the planner chose {plan['schedule']}")
+        want = {0: None, 1: "kernel", 2: "inline"}[fix]
+        assert plan["sk_fixup"] == (want or plan["sk_fixup"]), plan
+        if fix == 0 and tile_n == 128:
+            assert plan["sk_fixup"] == auto, plan
+        out.setdefault(fix, []).append(C.cpu().numpy())
+    h.set_option("sk_fixup", 0)
+    assert np.array_equal(out[1][0], out[2][0]) and np.array_equal(out[2][0], out[2][1])
+    assert np.array_equal(out[0][0], out[1][0])
+    rows = _cases.sample_rows(M)
+    _cases.run_and_check(h, "fp32", M, N, K, tA, tB, alpha=0.5, beta=0.75, seed=63, dist="normal", rows=rows)
 
 
 @pytest.mark.parametrize("tile_n", [128, 256])
