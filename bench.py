@@ -48,6 +48,7 @@ SM_MAX_MHZ = 2070.0
 # Nominal dense rates (recipe): tf32 1.1 PF, bf16 2.25 PF, fp8 4.5 PF.
 TF32_OVER_BF16 = 1.1 / 2.25
 FP8_OVER_BF16 = 4.5 / 2.25
+FP4_OVER_FP8 = 3.0     # nominal dense FP4 / FP8 tensor rate of this GPU (13.5 / 4.5 PFLOP/s)
 
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
@@ -814,12 +815,14 @@ def _sweep_shapes(args, h, stream, pk, l2, dev, shapes, cases=None, samples=SAMP
                           for _ in range(samples)])
         stream.synchronize()
         byts = int(es * (c.M * c.K + c.K * c.N)) + sf_bytes + 4 * c.M * c.N * (2 if beta != 0 else 1)
-        # block-scaled: the dense rate of the element type (FP4: twice FP8's, nominal)
+        # block-scaled: the dense rate of the element type (FP4: FP8's x the nominal ratio)
         peak = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops"], "bf16": pk["bf16_tflops"],
-                "fp8": pk["fp8_tflops"], "mxfp8_e4m3": pk["fp8_tflops"], "nvfp4": 2 * pk["fp8_tflops"]}[mode]
+                "fp8": pk["fp8_tflops"], "mxfp8_e4m3": pk["fp8_tflops"],
+                "nvfp4": FP4_OVER_FP8 * pk["fp8_tflops"]}[mode]
         peak_s = {"fp32": pk["fp32_alu_tflops"], "tf32": pk["tf32_tflops_sustained"],
                   "bf16": pk["bf16_tflops_sustained"], "fp8": pk["fp8_tflops_sustained"],
-                  "mxfp8_e4m3": pk["fp8_tflops_sustained"], "nvfp4": 2 * pk["fp8_tflops_sustained"]}[mode]
+                  "mxfp8_e4m3": pk["fp8_tflops_sustained"],
+                  "nvfp4": FP4_OVER_FP8 * pk["fp8_tflops_sustained"]}[mode]
         t_c, t_m = c.flops / (peak * 1e12), byts / (pk["hbm_gbs"] * 1e9)
         t_cs = c.flops / (peak_s * 1e12)
         st = _stats(dev_ms)
