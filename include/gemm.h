@@ -43,9 +43,11 @@
  *   the workspace, as in TF32 mode.
  *
  * Ownership: the caller owns A, B and C, which are device memory.  A handle
- * owns its device properties, a device status word and a scratch workspace
- * (split-K partial sums, re-packed and transposed operands) that grows on
- * demand and is freed by gemm_destroy.  A handle is bound to the device that was current at
+ * owns its device properties, a device status word (with, beside it, the
+ * per-tile arrival counters of the FP32 kernel's stream-K schedule, zero
+ * between calls) and a scratch workspace (split-K partial sums, re-packed
+ * and transposed operands) that grows on demand and is freed by
+ * gemm_destroy.  A handle is bound to the device that was current at
  * gemm_create and must not be used from two streams at the same time.
  *
  * Errors: every call returns a status and never throws.  Arguments are checked
