@@ -57,7 +57,7 @@ FP4_OVER_FP8 = 3.0     # nominal dense FP4 / FP8 tensor rate of this GPU (13.5 /
 # "traffic" is reported as null.
 PROFILED_TRAFFIC = {
     "fp32": {"source": "dense_gemm_transformer_gb300/csrc/simt.cu", "sha256": "0ed7a1a79cc80738",
-             "bytes_per_launch": 92.30e6},
+             "bytes_per_launch": 92.53e6},
 }
 
 

@@ -156,14 +156,15 @@ gemm_status_t run_simt(gemm_handle_s* h, int transA, int transB, int64_t M, int6
                        const dgt::EpiParams& epi, cudaStream_t s) {
   using namespace dgt;
   const int64_t kt = ceil_div(K, kSimtTileK);
-  // Tile width: the 256-column kernel (one CTA per SM, half the shared-memory
-  // reads per FFMA) measured 5-10% faster when N needs no padding and M is
-  // large, and slower on deep-K products with few output rows (more stream-K
-  // partial traffic) or when N pads up; so 256 columns only for N % 256 == 0
-  // and M >= 1024, 128 otherwise.
+  // Tile width: 128 columns, two CTAs per SM.  The 256-column kernel (one
+  // CTA per SM, fewer shared-memory reads per FFMA) measured 2-3% slower on
+  // every shape where it needs no padding -- M = 4096-16384, N = 1536,
+  // K = 384-1536, and the 2048^3 / 4096^3 squares (1024^3 a tie): with packed
+  // FMAs and the next step's fragments preloaded in both, the second
+  // resident CTA hiding each tile's fill and stores is worth more.  It stays
+  // available through the tile-width option.
   if (h->opt_tile_n != 0 && h->opt_tile_n != 128 && h->opt_tile_n != 256) return GEMM_ERR_NOT_SUPPORTED;
-  int tile_n = h->opt_tile_n;
-  if (tile_n == 0) tile_n = (N % 256 == 0 && M >= 1024) ? 256 : 128;
+  const int tile_n = h->opt_tile_n != 0 ? h->opt_tile_n : 128;
   const int64_t tiles = ceil_div(M, kSimtTileM) * ceil_div(N, tile_n);
   const int64_t slots = (tile_n == 256 ? 1 : 2) * static_cast<int64_t>(h->sms);  // resident CTAs
   // An operand stored with K contiguous must be transposed on its way to
