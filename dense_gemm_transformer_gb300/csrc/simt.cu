@@ -5,8 +5,10 @@
 // tiling, float4 loads, warp-level blocking and double buffering.  This is
 // that end point, re-sized for a 152-SM part with 64K registers per SM:
 //   * a 128 x TBN block tile (TBN = 128: two CTAs per SM, 8 x 8 outputs per
-//     thread; TBN = 256: one CTA per SM, 8 x 16 outputs per thread, which
-//     halves the shared-memory reads per FFMA), BK = 16, 256 threads;
+//     thread, the planner's choice; TBN = 256: one CTA per SM, 8 x 16
+//     outputs per thread, which halves the shared-memory reads per FFMA but
+//     leaves no second CTA to cover each tile's fill and stores), BK = 16,
+//     256 threads;
 //   * warps tile the block 4 (M) x 2 (N), lanes tile a warp 4 x 8, and every
 //     thread's register tile is split into 4 x 4 quadrants so each of its
 //     shared-memory reads is one float4 that the lanes sharing a row or column
@@ -26,8 +28,9 @@
 //     resident CTAs, and otherwise as whole-tile waves followed by stream-K
 //     for the rest: the remaining (tile, k-tile) iterations are cut into one
 //     equal contiguous run per resident CTA, runs that cover part of a tile
-//     store a raw partial tile, and a fixup kernel sums each such tile's
-//     partials in ascending k order (deterministic);
+//     store a raw partial tile, and each such tile's partials are summed in
+//     ascending k order (deterministic) by the last CTA to store one when a
+//     tile has about two parts, else by a fixup kernel;
 //   * products are single-rounded FFMA in fp32, the accumulation order along
 //     K is ascending, and the alpha/beta epilogue is fused into the stores.
 #include <cuda_runtime.h>
