@@ -449,15 +449,17 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
     const int64_t em0 = (sh.sg.tile / tiles_n) * BM;  // re-read: the mainloop kept no copy
     const int64_t en0 = (sh.sg.tile % tiles_n) * TBN;
     if (dest == kToSlot) {
-      // A stream-K partial: the raw 128 x TBN tile, rows of TBN floats.
+      // A stream-K partial: the raw 128 x TBN tile, rows of TBN floats
+      // (quadrants wholly past column N are neither stored nor read back).
       float* __restrict__ slot = p.ws + index * (BM * TBN);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float* rowp = slot + (am + (i & 3) + (i >> 2) * 16) * TBN + bn;
 #pragma unroll
         for (int q = 0; q < QN; ++q)
-          *reinterpret_cast<float4*>(rowp + 32 * q) =
-              make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
+          if (en0 + bn + 32 * q < p.N)
+            *reinterpret_cast<float4*>(rowp + 32 * q) =
+                make_float4(acc[i][4 * q], acc[i][4 * q + 1], acc[i][4 * q + 2], acc[i][4 * q + 3]);
       }
       if (!p.sk_inline) continue;
       // Inline fixup: the partial is published (fence, then one arrival on
@@ -499,6 +501,7 @@ __global__ void __launch_bounds__(NT, SimtCfg<TBN>::MIN_BLOCKS) simt_gemm_kernel
           for (int r = 0; r < 4; ++r) {
 #pragma unroll
             for (int q = 0; q < QN; ++q) {
+              if (en0 + bn + 32 * q >= p.N) continue;
               const float4 v = __ldcg(reinterpret_cast<const float4*>(src + r * TBN + 32 * q));
               float* a = acc[4 * g + r] + 4 * q;
               a[0] += v.x;
