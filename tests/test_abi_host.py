@@ -112,3 +112,60 @@ def test_every_kernel_is_free_of_spills(lib):
     for name, regs in per_kernel:
         limit = 128 if "simt_gemm_kernelILi128" in name else 255
         assert int(regs) <= limit, (name, regs)
+
+
+def _header_enum(prefix):
+    """NAME -> value of the enumerators of include/gemm.h that start with prefix."""
+    import os
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gemm.h")
+    text = re.sub(r"/\*.*?\*/", " ", open(path).read(), flags=re.S)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(" + prefix + r"\w*)\s*=\s*(\d+)", text)}
+
+
+def test_binding_constants_match_the_header():
+    """The ctypes binding's option, mode, family, activation and status
+    codes are the header's enumerators, so no call passes a stale code."""
+    opts = _header_enum("GEMM_OPT_")
+    assert sorted(dg.OPTIONS.values()) == sorted(opts.values())
+    for name, code in dg.OPTIONS.items():
+        assert opts["GEMM_OPT_" + name.upper()] == code, name
+    modes = _header_enum("GEMM_MODE_")
+    for name, code in dg.MODES.items():
+        key = "GEMM_MODE_" + ("FP8_E4M3" if name == "fp8" else name.upper())
+        assert modes[key] == code, name
+    for name, (code, _, _, _) in dg.BLOCK_SCALED_MODES.items():
+        assert modes["GEMM_MODE_" + name.upper()] == code, name
+    assert set(modes.values()) == set(dg.MODES.values()) | {v[0] for v in dg.BLOCK_SCALED_MODES.values()}
+    fams = _header_enum("GEMM_FAMILY_")
+    for name, code in dg.FAMILIES.items():
+        assert fams["GEMM_FAMILY_" + name.upper()] == code, name
+    acts = _header_enum("GEMM_ACT_")
+    for name, code in dg.ACTIVATIONS.items():
+        assert acts["GEMM_ACT_" + name.upper()] == code, name
+    status = {**_header_enum("GEMM_OK"), **_header_enum("GEMM_ERR_")}
+    assert {v: k for k, v in status.items()} == dg.STATUS
+
+
+def test_plan_struct_matches_the_header():
+    """gemm_plan_t field by field: every int32 member of the header's struct,
+    in order, is a field of the ctypes Plan at the same offset."""
+    import os
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gemm.h")
+    text = re.sub(r"/\*.*?\*/", " ", open(path).read(), flags=re.S)
+    body = re.search(r"typedef struct \{([^}]*)\} gemm_plan_t;", text).group(1)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        assert decl.startswith("int32_t "), decl
+        for name in decl[len("int32_t "):].split(","):
+            name = name.strip()
+            m = re.fullmatch(r"(\w+)\[(\d+)\]", name)
+            fields.append((m.group(1), int(m.group(2))) if m else (name, 1))
+    offset = 0
+    for name, count in fields:
+        f = getattr(dg.Plan, name)
+        assert f.offset == offset and f.size == 4 * count, name
+        offset += 4 * count
+    assert ctypes.sizeof(dg.Plan) == offset
