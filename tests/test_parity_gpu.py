@@ -206,6 +206,9 @@ def test_fp32_stream_k_fixup_forms(h, tile_n, M, N, K, tA, tB, auto):
             assert plan["sk_fixup"] == auto, plan
         out.setdefault(fix, []).append(C.cpu().numpy())
     h.set_option("sk_fixup", 0)
+    with pytest.raises(dg.GemmError) as e:
+        h.set_option("sk_fixup", 3)
+    assert e.value.status == 1  # GEMM_ERR_INVALID_VALUE
     assert np.array_equal(out[1][0], out[2][0]) and np.array_equal(out[2][0], out[2][1])
     assert np.array_equal(out[0][0], out[1][0])
     rows = _cases.sample_rows(M)
